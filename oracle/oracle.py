@@ -1,0 +1,199 @@
+"""Python face of the CPU oracle (test infrastructure only).
+
+Only tests/, the smoke check and the benchmark's cpu_baseline / reference legs
+may import this module.  It wraps ufp4_oracle.c through ctypes and works on
+numpy arrays; it never touches the CUDA library or its Python binding.
+
+Sources: the three pages on arXiv:2606.20381 ("Rethinking Shrinkage Bias in
+LLM FP4 Pretraining"), cited as in ufp4_oracle.c ([ZC] zhichai.net post,
+[AN] autonainews.com article, [HP] hotpaper.ai card).
+
+Layouts produced here are the plain ones: one code per element (rows x k,
+unpacked), row-major scales (rows x k/16), packed codes with element 2j in the
+low nibble of byte j.  Column-wise quantization is literally "transpose, then
+quantize row-wise".
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+E2M1, E1M2 = 0, 1
+RTNE, SR = 0, 1
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build_oracle()
+        L = ctypes.CDLL(path)
+        u32p = ctypes.POINTER(ctypes.c_uint32)
+        L.ref_philox4x32_10.argtypes = [u32p, u32p, u32p]
+        L.ref_rht_signs.argtypes = [ctypes.c_uint64, ctypes.POINTER(ctypes.c_int32)]
+        L.ref_hadamard16.argtypes = [ctypes.c_int32, ctypes.c_int32]
+        L.ref_hadamard16.restype = ctypes.c_int32
+        L.ref_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.ref_e4m3_decode.restype = ctypes.c_double
+        L.ref_e4m3_encode.argtypes = [ctypes.c_float]
+        L.ref_e4m3_encode.restype = ctypes.c_uint8
+        L.ref_grid_value.argtypes = [ctypes.c_int, ctypes.c_int]
+        L.ref_grid_value.restype = ctypes.c_double
+        L.ref_grid_qmax.argtypes = [ctypes.c_int]
+        L.ref_grid_qmax.restype = ctypes.c_double
+        L.ref_round_rtne.argtypes = [ctypes.c_int, ctypes.c_float]
+        L.ref_round_rtne.restype = ctypes.c_int
+        L.ref_round_sr.argtypes = [ctypes.c_int, ctypes.c_float, ctypes.c_uint32]
+        L.ref_round_sr.restype = ctypes.c_int
+        L.ref_sr_word.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64]
+        L.ref_sr_word.restype = ctypes.c_uint32
+        vp = ctypes.c_void_p
+        L.ref_quantize.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_uint64,
+                                   ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64,
+                                   ctypes.c_uint64, vp, vp, vp, vp, vp]
+        L.ref_quantize.restype = ctypes.c_int
+        L.ref_dequantize.argtypes = [vp, vp, ctypes.c_float, ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_uint64, vp]
+        L.ref_gemm_f64.argtypes = [vp, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp]
+        L.ref_gemm_entries.argtypes = [vp, vp, ctypes.c_int64, vp, vp, ctypes.c_int64, vp]
+        L.ref_stats.argtypes = [vp, vp, vp, ctypes.c_float, ctypes.c_int64, ctypes.c_int64,
+                                ctypes.c_int, vp]
+        _lib = L
+    return _lib
+
+
+def _p(a):
+    return ctypes.c_void_p(a.ctypes.data) if a is not None else None
+
+
+# --------------------------------------------------------------- primitives
+def philox4x32_10(ctr, key):
+    """Philox4x32-10 (Salmon et al., SC'11) of a 4-word counter and 2-word key."""
+    c = (ctypes.c_uint32 * 4)(*[int(v) & 0xFFFFFFFF for v in ctr])
+    k = (ctypes.c_uint32 * 2)(*[int(v) & 0xFFFFFFFF for v in key])
+    o = (ctypes.c_uint32 * 4)()
+    lib().ref_philox4x32_10(c, k, o)
+    return [int(v) for v in o]
+
+
+def rht_signs(seed):
+    d = (ctypes.c_int32 * 16)()
+    lib().ref_rht_signs(ctypes.c_uint64(seed), d)
+    return np.array(list(d), dtype=np.int32)
+
+
+def hadamard16():
+    return np.array([[lib().ref_hadamard16(i, j) for j in range(16)] for i in range(16)],
+                    dtype=np.int64)
+
+
+def e4m3_decode(c):
+    return lib().ref_e4m3_decode(int(c))
+
+
+def e4m3_encode(v):
+    return int(lib().ref_e4m3_encode(float(v)))
+
+
+def grid_value(grid, m):
+    return lib().ref_grid_value(grid, int(m))
+
+
+def grid_qmax(grid):
+    return lib().ref_grid_qmax(grid)
+
+
+def round_rtne(grid, a):
+    return lib().ref_round_rtne(grid, float(a))
+
+
+def round_sr(grid, a, r):
+    return lib().ref_round_sr(grid, float(a), int(r) & 0xFFFFFFFF)
+
+
+def sr_word(sr_seed, sr_counter, i):
+    return int(lib().ref_sr_word(sr_seed, sr_counter, i))
+
+
+# ------------------------------------------------------------------ tensors
+def quantize(x, grid, rht=False, rht_seed=0, round_mode=RTNE, sr_seed=0, sr_counter=0,
+             colwise=False, amax_in=None, elem_base=0):
+    """Quantize a 2-D fp32 array with 16-blocks along its last dim (row-wise),
+    or along its first dim (colwise: the result is the quantization of x.T).
+
+    Returns dict(codes=u8[rows_out, k] (one code per element), scales=u8
+    [rows_out, k//16] (row-major E4M3), tensor_scale=float (S_dec),
+    y=f32[rows_out, k] (the tensor actually quantized: rotated when rht)).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    if colwise:
+        x = x.T
+    x = np.ascontiguousarray(x)
+    rows, k = x.shape
+    codes = np.zeros((rows, k), dtype=np.uint8)
+    scales = np.zeros((rows, max(k // 16, 0)), dtype=np.uint8)
+    ts = np.zeros(1, dtype=np.float32)
+    y = np.zeros((rows, k), dtype=np.float32)
+    am = None if amax_in is None else np.array([amax_in], dtype=np.float32)
+    rc = lib().ref_quantize(_p(x), rows, k, k, grid, int(bool(rht)), ctypes.c_uint64(rht_seed),
+                            round_mode, ctypes.c_uint64(sr_seed), ctypes.c_uint64(sr_counter),
+                            ctypes.c_uint64(elem_base), _p(am), _p(codes), _p(scales), _p(ts),
+                            _p(y))
+    if rc != 0:
+        raise ValueError("ref_quantize failed (%d): k must be a multiple of 16" % rc)
+    return dict(codes=codes, scales=scales, tensor_scale=float(ts[0]), y=y)
+
+
+def pack_codes(codes):
+    """Two codes per byte: element 2j in bits 3..0, element 2j+1 in bits 7..4."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 0::2] & 0xF) | ((c[..., 1::2] & 0xF) << 4)
+
+
+def dequantize(codes, scales, tensor_scale, grid, inverse_rht=False, rht_seed=0):
+    """fp64 value of every element: v(m) * e_b * S_dec (then the inverse RHT)."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    rows, k = codes.shape
+    out = np.zeros((rows, k), dtype=np.float64)
+    lib().ref_dequantize(_p(codes), _p(scales), ctypes.c_float(tensor_scale), rows, k, grid,
+                         int(bool(inverse_rht)), ctypes.c_uint64(rht_seed), _p(out))
+    return out
+
+
+def gemm_f64(a, b):
+    """C = a @ b.T in fp64 with a plain triple loop (a: M x K, b: N x K)."""
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    b = np.ascontiguousarray(b, dtype=np.float64)
+    M, K = a.shape
+    N = b.shape[0]
+    c = np.zeros((M, N), dtype=np.float64)
+    lib().ref_gemm_f64(_p(a), _p(b), M, N, K, _p(c))
+    return c
+
+
+def gemm_entries(a, b, mi, ni):
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    b = np.ascontiguousarray(b, dtype=np.float64)
+    mi = np.ascontiguousarray(mi, dtype=np.int64)
+    ni = np.ascontiguousarray(ni, dtype=np.int64)
+    out = np.zeros(len(mi), dtype=np.float64)
+    lib().ref_gemm_entries(_p(a), _p(b), a.shape[1], _p(mi), _p(ni), len(mi), _p(out))
+    return out
+
+
+def stats(y, codes, scales, tensor_scale, grid):
+    """alpha, SQNR and mean rounding bias of one quantization (see ufp4_oracle.c)."""
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    rows, k = codes.shape
+    out = np.zeros(7, dtype=np.float64)
+    lib().ref_stats(_p(y), _p(codes), _p(scales), ctypes.c_float(tensor_scale), rows, k,
+                    grid, _p(out))
+    keys = ["alpha", "sqnr_db", "mean_bias", "sum_aq", "sum_aa", "sum_err2", "bias_count"]
+    return dict(zip(keys, [float(v) for v in out]))

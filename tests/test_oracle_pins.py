@@ -1,0 +1,428 @@
+"""Pins of the CPU oracle to facts outside itself (CPU only).
+
+Each test ties one oracle function to something the oracle cannot have
+produced: published known-answer vectors, the pages' worked example, closed
+forms, invariants, or an independent library routine (numpy / scipy / torch)
+computing the same quantity by a different route.  A plausible mistake in the
+oracle -- a dropped term, a wrong sign, a transposed operand, a wrong tie rule
+or rounding order -- fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+from fp4_quantized_numerics_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ----------------------------------------------------------------- Philox
+def test_philox_known_answer_vectors(oracle):
+    rows = _read_rows("philox4x32_10_kat.txt")
+    assert len(rows) == 3
+    for r in rows:
+        v = [int(t, 16) for t in r]
+        assert oracle.philox4x32_10(v[0:4], v[4:6]) == v[6:10]
+
+
+def test_sr_word_counter_layout(oracle):
+    # element i draws word i%4 of Philox(key=seed, ctr=(i//4, counter)).
+    seed, ctr = 0x0123456789ABCDEF, 0xFEDCBA9876543210
+    for i in [0, 1, 2, 3, 4, 7, 2**33 + 5]:
+        q = i >> 2
+        words = oracle.philox4x32_10([q & 0xFFFFFFFF, q >> 32, ctr & 0xFFFFFFFF, ctr >> 32],
+                                     [seed & 0xFFFFFFFF, seed >> 32])
+        assert oracle.sr_word(seed, ctr, i) == words[i & 3]
+
+
+# ------------------------------------------------------------ Hadamard/RHT
+def test_hadamard_is_sylvester_and_orthogonal(oracle):
+    import scipy.linalg
+    H = oracle.hadamard16()
+    assert np.array_equal(H, scipy.linalg.hadamard(16))
+    assert np.array_equal(H @ H.T, 16 * np.eye(16, dtype=np.int64))
+
+
+def test_rht_signs_are_pm1_and_seeded(oracle):
+    d2 = oracle.rht_signs(2)
+    assert set(np.unique(d2)) <= {-1, 1}
+    assert np.array_equal(d2, oracle.rht_signs(2))
+    assert not np.array_equal(d2, oracle.rht_signs(3))
+
+
+def _rotate_numpy(x, d):
+    import scipy.linalg
+    H = scipy.linalg.hadamard(16).astype(np.float64)
+    xb = x.astype(np.float64).reshape(-1, 16)
+    return ((0.25 * (xb * d[None, :]) @ H.T).astype(np.float32)).reshape(x.shape)
+
+
+def test_rht_forward_matches_matrix_product(oracle):
+    x = inputs.normal(5, (8, 64))
+    q = oracle.quantize(x, oracle.E1M2, rht=True, rht_seed=2)
+    ref = _rotate_numpy(x, oracle.rht_signs(2).astype(np.float64))
+    np.testing.assert_array_equal(q["y"], ref)
+
+
+def test_rht_spike_closed_form_and_norm(oracle):
+    d = oracle.rht_signs(2)
+    for j in [0, 5, 15]:
+        x = np.zeros((1, 16), np.float32)
+        x[0, j] = 3.0
+        y = oracle.quantize(x, oracle.E2M1, rht=True, rht_seed=2)["y"][0]
+        H = oracle.hadamard16()
+        np.testing.assert_array_equal(y, 0.75 * d[j] * H[:, j])
+    x = inputs.normal(7, (16, 128))
+    y = oracle.quantize(x, oracle.E2M1, rht=True, rht_seed=9)["y"]
+    assert abs(np.linalg.norm(y.astype(np.float64)) / np.linalg.norm(x.astype(np.float64)) - 1) < 1e-6
+
+
+def test_rht_preserves_inner_products_along_k(oracle):
+    a = inputs.normal(11, (4, 64))
+    b = inputs.normal(12, (3, 64))
+    ya = oracle.quantize(a, oracle.E1M2, rht=True, rht_seed=2)["y"].astype(np.float64)
+    yb = oracle.quantize(b, oracle.E1M2, rht=True, rht_seed=2)["y"].astype(np.float64)
+    ref = a.astype(np.float64) @ b.astype(np.float64).T
+    np.testing.assert_allclose(ya @ yb.T, ref, rtol=0, atol=1e-5 * np.abs(ref).max())
+
+
+def test_inverse_rht_in_dequantize(oracle):
+    x = inputs.normal(13, (4, 32))
+    q = oracle.quantize(x, oracle.E1M2, rht=True, rht_seed=2)
+    plain = oracle.dequantize(q["codes"], q["scales"], q["tensor_scale"], oracle.E1M2)
+    back = oracle.dequantize(q["codes"], q["scales"], q["tensor_scale"], oracle.E1M2,
+                             inverse_rht=True, rht_seed=2)
+    import scipy.linalg
+    H = scipy.linalg.hadamard(16).astype(np.float64)
+    d = oracle.rht_signs(2).astype(np.float64)
+    ref = ((0.25 * plain.reshape(-1, 16) @ H.T) * d[None, :]).reshape(plain.shape)
+    np.testing.assert_allclose(back, ref, rtol=1e-14, atol=1e-14)
+    # and the round trip is close to the original (quantization error only)
+    assert np.linalg.norm(back - x) / np.linalg.norm(x) < 0.2
+
+
+# -------------------------------------------------------------------- E4M3
+def test_e4m3_decode_all_codes_vs_torch(oracle):
+    import torch
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    for c in range(256):
+        v = oracle.e4m3_decode(c)
+        if np.isnan(ref[c]):
+            assert math.isnan(v), c
+        else:
+            assert v == float(ref[c]), c
+    assert oracle.e4m3_decode(0x7E) == 448.0
+    assert oracle.e4m3_decode(0x01) == 2.0 ** -9
+
+
+def _e4m3_probe_values(oracle):
+    vals = [0.0, 2.0 ** -10, 1.5 * 2.0 ** -10, 2.0 ** -9, 448.0, 300.0, 1e-12]
+    codes = [oracle.e4m3_decode(c) for c in range(0x7F)]
+    for lo, hi in zip(codes[:-1], codes[1:]):
+        mid = np.float32((lo + hi) / 2)
+        vals += [float(mid), float(np.nextafter(mid, np.float32(0))),
+                 float(np.nextafter(mid, np.float32(1e9))), lo]
+    g = np.random.default_rng(1)
+    vals += list(np.exp(g.uniform(np.log(1e-4), np.log(448), 2000)).astype(np.float32))
+    return np.array(vals, dtype=np.float32)
+
+
+def test_e4m3_encode_rne_vs_torch(oracle):
+    import torch
+    v = _e4m3_probe_values(oracle)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    for x, r in zip(v, ref):
+        assert oracle.e4m3_encode(x) == int(r), float(x)
+        assert oracle.e4m3_encode(-x) == (int(r) | 0x80) if x != 0 else True
+
+
+def test_e4m3_encode_saturates(oracle):
+    for x in [448.0, 449.0, 464.0, 480.0, 1e6, float("inf")]:
+        assert oracle.e4m3_encode(x) == 0x7E
+    assert oracle.e4m3_encode(float("nan")) == 0x7F
+
+
+# ------------------------------------------------------------- grid rounding
+def _e2m1_rne_by_exponent(a):
+    """IEEE round-to-nearest-even into E2M1 (1 mantissa bit, exponent bias 1,
+    subnormal step 0.5), computed from the binade instead of a value table."""
+    a = np.asarray(a, dtype=np.float64)
+    e = np.floor(np.log2(np.maximum(a, 1e-300)))
+    step = np.where(a < 1.0, 0.5, 2.0 ** (e - 1))
+    return np.minimum(np.rint(a / step) * step, 6.0)
+
+
+def _grid_probe(qmax, extra):
+    g = np.random.default_rng(3)
+    a = list(g.uniform(0, qmax, 20000).astype(np.float32)) + extra
+    out = []
+    for v in a:
+        v = np.float32(v)
+        out += [v, np.nextafter(v, np.float32(0)), np.nextafter(v, np.float32(10))]
+    return np.minimum(np.array(out, dtype=np.float32), np.float32(qmax))
+
+
+def test_e2m1_rtne_vs_binade_rounding(oracle):
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.0, 6.0]
+    for a in _grid_probe(6.0, mids):
+        m = oracle.round_rtne(oracle.E2M1, a)
+        assert oracle.grid_value(oracle.E2M1, m) == _e2m1_rne_by_exponent(a), float(a)
+    # ties go to the even code: 0.25->0, 0.75->1.0, 1.25->1.0, 1.75->2, 2.5->2, 3.5->4, 5->4
+    want = {0.25: 0, 0.75: 2, 1.25: 2, 1.75: 4, 2.5: 4, 3.5: 6, 5.0: 6}
+    for a, m in want.items():
+        assert oracle.round_rtne(oracle.E2M1, a) == m
+
+
+def test_e1m2_rtne_vs_rint(oracle):
+    for a in _grid_probe(3.5, [0.25 * i for i in range(15)]):
+        m = oracle.round_rtne(oracle.E1M2, a)
+        assert m == int(min(np.rint(2.0 * float(a)), 7.0)), float(a)
+
+
+def test_grids_have_all_codes(oracle):
+    e2 = [oracle.grid_value(oracle.E2M1, m) for m in range(8)]
+    e1 = [oracle.grid_value(oracle.E1M2, m) for m in range(8)]
+    assert e2 == [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    assert e1 == [0.5 * m for m in range(8)]
+    assert np.allclose(np.diff(e1), 0.5)          # uniform
+    assert len(set(np.diff(e2))) == 3             # non-uniform
+
+
+# ------------------------------------------------------ worked example: bias
+def test_shrinkage_bias_worked_example(oracle):
+    row = [r for r in _read_rows("shrinkage_worked_example.txt") if r[0] == "e2m1_q2"][0]
+    lo, hi, want = float(row[2]), float(row[3]), float(row[4])
+    n = 200000
+    a = (lo + (np.arange(n) + 0.5) * (hi - lo) / n).astype(np.float32)
+    err = np.mean([oracle.grid_value(oracle.E2M1, oracle.round_rtne(oracle.E2M1, v)) - v
+                   for v in a[::20]])
+    assert abs(err - want) < 1e-3
+
+
+def test_e2m1_bin_asymmetry_general_formula(oracle):
+    # every interior E2M1 point: mean error over its rounding interval is (left - right)/2
+    g = [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    for i in range(1, 7):
+        left, right = (g[i] - g[i - 1]) / 2, (g[i + 1] - g[i]) / 2
+        a = np.linspace(g[i] - left, g[i] + right, 4001)[1:-1].astype(np.float32)
+        err = np.mean([oracle.grid_value(oracle.E2M1, oracle.round_rtne(oracle.E2M1, v)) - v
+                       for v in a])
+        assert abs(err - (left - right) / 2) < 2e-3, g[i]
+
+
+def test_e1m2_interior_bins_unbiased(oracle):
+    for q0 in [0.5, 1.0, 1.5, 2.0, 2.5, 3.0]:
+        a = np.linspace(q0 - 0.25, q0 + 0.25, 4001)[1:-1].astype(np.float32)
+        err = np.mean([oracle.grid_value(oracle.E1M2, oracle.round_rtne(oracle.E1M2, v)) - v
+                       for v in a])
+        assert abs(err) < 1e-6, q0
+
+
+def test_attenuation_closed_form():
+    row = [r for r in _read_rows("shrinkage_worked_example.txt") if r[0] == "attenuation"][0]
+    loss, layers, left = float(row[1]), int(row[2]), float(row[3])
+    assert round((1 - loss) ** layers, 2) == left
+    assert abs(math.exp(-loss * layers) - (1 - loss) ** layers) < 0.01
+
+
+# ---------------------------------------------------- stochastic rounding
+@pytest.mark.parametrize("grid", [0, 1])
+def test_sr_is_unbiased_within_5_sigma(oracle, grid):
+    qmax = oracle.grid_qmax(grid)
+    g = np.random.default_rng(4)
+    N = 4096
+    for a in g.uniform(0, qmax, 24).astype(np.float32):
+        m0 = oracle.round_sr(grid, a, 0xFFFFFFFF)  # never rounds up: the floor
+        lo = oracle.grid_value(grid, m0)
+        hi = oracle.grid_value(grid, min(m0 + 1, 7))
+        vals = [oracle.grid_value(grid, oracle.round_sr(grid, a, oracle.sr_word(3, 0, i)))
+                for i in range(N)]
+        p = (float(a) - lo) / (hi - lo) if hi > lo else 0.0
+        sigma = (hi - lo) * math.sqrt(max(p * (1 - p), 1e-12) / N)
+        assert abs(np.mean(vals) - float(a)) <= 5 * sigma + 1e-12, float(a)
+        assert set(vals) <= {lo, hi}
+
+
+def test_sr_exact_points_and_edges(oracle):
+    for grid in (0, 1):
+        for m in range(8):
+            v = oracle.grid_value(grid, m)
+            for r in (0, 0x7FFFFFFF, 0xFFFFFFFF):
+                assert oracle.round_sr(grid, v, r) == m
+    # r = 0 gives u = 0 < p for any p > 0: always rounds up off-grid
+    assert oracle.round_sr(1, 0.1, 0) == 1
+    assert oracle.round_sr(1, 0.1, 0xFFFFFFFF) == 0
+
+
+# -------------------------------------------------- quantization end to end
+@pytest.mark.parametrize("grid", [0, 1])
+def test_quantize_scale_path_exact_case(oracle, grid):
+    qmax = oracle.grid_qmax(grid)
+    x = np.full((1, 16), qmax / 8, np.float32)  # A_t = qmax/8: every step exact
+    q = oracle.quantize(x, grid)
+    assert q["scales"][0, 0] == 0x7E                      # E4M3 448
+    assert np.all(q["codes"] == 7)
+    assert q["tensor_scale"] == np.float32(qmax / 8) / np.float32(448 * qmax)
+
+
+def test_quantize_zero_and_single_spike(oracle):
+    z = oracle.quantize(np.zeros((4, 32), np.float32), 0)
+    assert not z["codes"].any() and not z["scales"].any() and z["tensor_scale"] == 1.0
+    x = np.zeros((2, 32), np.float32)
+    x[1, 17] = -0.3
+    for grid in (0, 1):
+        q = oracle.quantize(x, grid)
+        assert q["codes"][1, 17] == 0x8 | 7
+        others = np.delete(q["codes"].ravel(), 1 * 32 + 17)
+        assert np.all((others & 7) == 0)
+
+
+@pytest.mark.parametrize("grid", [0, 1])
+def test_quantize_sign_and_power_of_two_invariance(oracle, grid):
+    x = inputs.normal(21, (16, 64))
+    q = oracle.quantize(x, grid)
+    qn = oracle.quantize(-x, grid)
+    np.testing.assert_array_equal(qn["codes"], q["codes"] ^ 0x8)
+    q2 = oracle.quantize(x * np.float32(8), grid)
+    np.testing.assert_array_equal(q2["codes"], q["codes"])
+    np.testing.assert_array_equal(q2["scales"], q["scales"])
+    assert q2["tensor_scale"] == q["tensor_scale"] * 8
+
+
+@pytest.mark.parametrize("grid", [0, 1])
+def test_quantize_picks_nearest_representable(oracle, grid):
+    """Brute force: with the block scale fixed, every code is (to within the
+    rounding of k = S_enc/e_b) the nearest of the 16 representable values."""
+    x = inputs.normal(22, (8, 64))
+    q = oracle.quantize(x, grid)
+    deq = oracle.dequantize(q["codes"], q["scales"], q["tensor_scale"], grid)
+    qmax = oracle.grid_qmax(grid)
+    for r in range(8):
+        for b in range(4):
+            e = oracle.e4m3_decode(q["scales"][r, b])
+            unit = e * q["tensor_scale"]
+            cand = np.array([s * oracle.grid_value(grid, m) * unit
+                             for s in (1, -1) for m in range(8)])
+            for j in range(16):
+                y = float(x[r, 16 * b + j])
+                best = np.min(np.abs(cand - y))
+                got = abs(deq[r, 16 * b + j] - y)
+                assert got <= best + 1e-6 * qmax * unit, (r, b, j)
+
+
+def test_colwise_is_rowwise_of_transpose(oracle):
+    x = inputs.normal(23, (64, 48))
+    c = oracle.quantize(x, 1, colwise=True)
+    r = oracle.quantize(np.ascontiguousarray(x.T), 1)
+    for key in ("codes", "scales"):
+        np.testing.assert_array_equal(c[key], r[key])
+    assert c["codes"].shape == (48, 64)
+
+
+def test_pack_codes_nibble_order(oracle):
+    c = np.array([[1, 2, 3, 4, 0xF, 0x8]], np.uint8)
+    assert list(oracle.pack_codes(c)[0]) == [0x21, 0x43, 0x8F]
+
+
+def test_sr_quantize_reproducible_and_counter_sensitive(oracle):
+    x = inputs.normal(24, (16, 64), std=1e-3)
+    a = oracle.quantize(x, 1, round_mode=oracle.SR, sr_seed=3, sr_counter=0)
+    b = oracle.quantize(x, 1, round_mode=oracle.SR, sr_seed=3, sr_counter=0)
+    c = oracle.quantize(x, 1, round_mode=oracle.SR, sr_seed=3, sr_counter=1)
+    np.testing.assert_array_equal(a["codes"], b["codes"])
+    assert (a["codes"] != c["codes"]).any()
+    np.testing.assert_array_equal(a["scales"], c["scales"])
+
+
+# ------------------------------------------------------------------- GEMM
+def test_gemm_f64_vs_numpy(oracle):
+    d = inputs.smoke(0)
+    qa = oracle.quantize(d["a"][:64, :128], 0)
+    qb = oracle.quantize(d["b"][:48, :128], 1)
+    A = oracle.dequantize(qa["codes"], qa["scales"], qa["tensor_scale"], 0)
+    B = oracle.dequantize(qb["codes"], qb["scales"], qb["tensor_scale"], 1)
+    C = oracle.gemm_f64(A, B)
+    np.testing.assert_allclose(C, A @ B.T, rtol=1e-12, atol=1e-12)
+    mi, ni = np.array([0, 63, 5]), np.array([47, 0, 9])
+    np.testing.assert_allclose(oracle.gemm_entries(A, B, mi, ni), C[mi, ni], rtol=1e-13)
+
+
+def test_gemm_identity_and_one_hot(oracle):
+    I = np.eye(32)
+    B = np.arange(32 * 32, dtype=np.float64).reshape(32, 32)
+    np.testing.assert_array_equal(oracle.gemm_f64(I, B), B.T)
+    e = np.zeros((1, 32))
+    e[0, 7] = 1
+    np.testing.assert_array_equal(oracle.gemm_f64(e, B)[0], B[:, 7])
+
+
+def test_dequantize_values_are_exact_products(oracle):
+    # value = v(m) e_b S_dec exactly, checked with fractions on a few entries
+    from fractions import Fraction
+    x = inputs.normal(25, (2, 32))
+    for grid in (0, 1):
+        q = oracle.quantize(x, grid)
+        deq = oracle.dequantize(q["codes"], q["scales"], q["tensor_scale"], grid)
+        for (r, j) in [(0, 0), (1, 31), (0, 17)]:
+            c = q["codes"][r, j]
+            v = Fraction(oracle.grid_value(grid, c & 7)) * (-1 if c & 8 else 1)
+            want = v * Fraction(oracle.e4m3_decode(q["scales"][r, j // 16])) * \
+                Fraction(float(np.float32(q["tensor_scale"])))
+            assert Fraction(deq[r, j]) == want
+
+
+# ------------------------------------------------------------- statistics
+def test_alpha_shrinkage_on_gaussian(oracle):
+    x = inputs.smoke(0)["x"]
+    s = {}
+    for grid in (0, 1):
+        q = oracle.quantize(x, grid)
+        s[grid] = oracle.stats(q["y"], q["codes"], q["scales"], q["tensor_scale"], grid)
+    assert s[0]["alpha"] < 0.999           # E2M1 shrinks
+    assert abs(s[1]["alpha"] - 1.0) < 2e-3  # E1M2 does not
+    assert s[0]["mean_bias"] < 0
+    assert abs(s[1]["mean_bias"]) < abs(s[0]["mean_bias"])
+
+
+def test_stats_match_numpy(oracle):
+    x = inputs.normal(26, (32, 64))
+    q = oracle.quantize(x, 0)
+    st = oracle.stats(q["y"], q["codes"], q["scales"], q["tensor_scale"], 0)
+    deq = oracle.dequantize(q["codes"], q["scales"], q["tensor_scale"], 0)
+    a = q["y"].astype(np.float64)
+    assert math.isclose(st["alpha"], float(np.vdot(deq, a) / np.vdot(a, a)), rel_tol=1e-12)
+    assert math.isclose(st["sqnr_db"],
+                        10 * math.log10(np.vdot(a, a) / np.sum((a - deq) ** 2)), rel_tol=1e-12)
+
+
+def test_compounding_chain_small(oracle):
+    """prod eta ~ exp(-sum delta) on a short chain of quantized GEMMs."""
+    n, steps = 64, 12
+    g = np.random.default_rng(8)
+    X = inputs.to_bf16_f32(g.standard_normal((n, n), dtype=np.float32))
+    etas = []
+    for _ in range(steps):
+        W = inputs.to_bf16_f32(g.standard_normal((n, n), dtype=np.float32) / np.float32(8))
+        qx, qw = oracle.quantize(X, 0), oracle.quantize(W, 0)
+        A = oracle.dequantize(qx["codes"], qx["scales"], qx["tensor_scale"], 0)
+        B = oracle.dequantize(qw["codes"], qw["scales"], qw["tensor_scale"], 0)
+        Yq = oracle.gemm_f64(A, B)
+        Yr = X.astype(np.float64) @ W.astype(np.float64).T
+        etas.append(float(np.vdot(Yq, Yr) / np.vdot(Yr, Yr)))
+        X = Yq.astype(np.float32)
+    deltas = 1 - np.array(etas)
+    assert np.all(deltas > 0)                       # E2M1 attenuates every step
+    lhs = math.log(np.prod(etas))
+    assert abs(lhs + deltas.sum()) <= np.sum(deltas ** 2) + 1e-12
