@@ -1,0 +1,183 @@
+// api.cu -- the libufp4 C ABI: host-side validation and launch.
+//
+// Every entry point checks its arguments on the host and returns
+// UFP4_ERR_INVALID before anything is enqueued; the library never allocates
+// device memory and never synchronises except in ufp4_check / ufp4_stats,
+// which return host values.
+#include "../../include/ufp4.h"
+#include "common.cuh"
+#include "internal.h"
+
+#include <cmath>
+#include <vector>
+
+using namespace ufp4;
+
+namespace {
+
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline ufp4_status from_cuda(cudaError_t e) {
+    return e == cudaSuccess ? UFP4_OK : (e == cudaErrorNotSupported ? UFP4_ERR_UNSUPPORTED : UFP4_ERR_CUDA);
+}
+
+bool valid_qtensor(const ufp4_qtensor *q) {
+    if (!q || q->reserved != 0) return false;
+    if (q->rows < 0 || q->k < 0 || q->k % UFP4_BLOCK != 0) return false;
+    if (q->grid != UFP4_E2M1 && q->grid != UFP4_E1M2) return false;
+    if (q->rows == 0 || q->k == 0) return true;
+    if (!q->codes || !q->scales || !q->tensor_scale) return false;
+    return aligned(q->codes, 16) && aligned(q->scales, 16) && aligned(q->tensor_scale, 4);
+}
+
+// Shared validation of ufp4_quantize / ufp4_stats arguments.  Fills `ql`.
+ufp4_status check_quant_args(const void *x, int32_t dtype, int64_t rows, int64_t cols, int64_t ld,
+                             const ufp4_qparams *p, const ufp4_qtensor *out, QuantLaunch *ql) {
+    if (!p || !out) return UFP4_ERR_INVALID;
+    if (dtype != UFP4_BF16 && dtype != UFP4_FP32) return UFP4_ERR_INVALID;
+    if (p->block != UFP4_BLOCK) return UFP4_ERR_UNSUPPORTED;
+    if (p->grid != UFP4_E2M1 && p->grid != UFP4_E1M2) return UFP4_ERR_INVALID;
+    if (p->round != UFP4_RTNE && p->round != UFP4_SR) return UFP4_ERR_INVALID;
+    if ((p->rht != 0 && p->rht != 1) || (p->colwise != 0 && p->colwise != 1) || p->reserved != 0)
+        return UFP4_ERR_INVALID;
+    if (rows < 0 || cols < 0 || ld < cols) return UFP4_ERR_INVALID;
+    const int64_t out_rows = p->colwise ? cols : rows;
+    const int64_t k = p->colwise ? rows : cols;
+    if (!valid_qtensor(out) || out->grid != p->grid || out->rows != out_rows || out->k != k)
+        return UFP4_ERR_INVALID;
+    if (k % UFP4_BLOCK != 0) return UFP4_ERR_INVALID;
+    if (p->colwise && cols % 4 != 0) return UFP4_ERR_INVALID;
+    const size_t esz = dtype == UFP4_BF16 ? 2 : 4;
+    if (rows > 0 && cols > 0) {
+        if (!x || !aligned(x, 16) || (ld * (int64_t)esz) % 16 != 0) return UFP4_ERR_INVALID;
+    }
+    if (p->amax_in && !aligned(p->amax_in, 4)) return UFP4_ERR_INVALID;
+    QuantLaunch q{};
+    q.x = x; q.dtype = dtype; q.rows = rows; q.cols = cols; q.ld = ld;
+    q.grid = p->grid; q.rht = p->rht; q.round = p->round; q.colwise = p->colwise;
+    q.rht_seed = p->rht_seed; q.sr_seed = p->sr_seed; q.sr_counter = p->sr_counter;
+    q.amax_in = p->amax_in;
+    q.codes = out->codes; q.scales = out->scales; q.tensor_scale = out->tensor_scale;
+    q.out_rows = out_rows; q.k = k; q.elem_base = 0;
+    *ql = q;
+    return UFP4_OK;
+}
+
+bool valid_workspace(const void *ws, size_t bytes) {
+    return ws && aligned(ws, 16) && bytes >= kWorkspaceBytes;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t ufp4_kpad(int64_t k) { return k <= 0 ? 0 : kpad_of(k); }
+
+int64_t ufp4_codes_bytes(int64_t rows, int64_t k) {
+    if (rows <= 0 || k <= 0) return 0;
+    return rows * (kpad_of(k) / 2);
+}
+
+int64_t ufp4_scales_bytes(int64_t rows, int64_t k) {
+    if (rows <= 0 || k <= 0) return 0;
+    return rpad_of(rows) * (kpad_of(k) / 16);
+}
+
+size_t ufp4_workspace_bytes(void) { return kWorkspaceBytes; }
+
+const char *ufp4_status_string(ufp4_status s) {
+    switch (s) {
+        case UFP4_OK: return "ok";
+        case UFP4_ERR_INVALID: return "invalid argument";
+        case UFP4_ERR_UNSUPPORTED: return "unsupported by this build";
+        case UFP4_ERR_NONFINITE: return "non-finite input";
+        case UFP4_ERR_CUDA: return "CUDA runtime error";
+        case UFP4_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+ufp4_status ufp4_quantize(const void *x, int32_t dtype, int64_t rows, int64_t cols, int64_t ld,
+                          const ufp4_qparams *p, const ufp4_qtensor *out, void *workspace,
+                          size_t workspace_bytes, ufp4_stream_t stream) {
+    QuantLaunch q;
+    ufp4_status st = check_quant_args(x, dtype, rows, cols, ld, p, out, &q);
+    if (st != UFP4_OK) return st;
+    if (!p->amax_in && !valid_workspace(workspace, workspace_bytes)) return UFP4_ERR_INVALID;
+    if (workspace && !aligned(workspace, 16)) return UFP4_ERR_INVALID;
+    if (rows == 0 || cols == 0) return UFP4_OK;
+    return from_cuda(launch_quantize(q, workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ufp4_status ufp4_check(const void *workspace, ufp4_stream_t stream) {
+    if (workspace && !aligned(workspace, 16)) return UFP4_ERR_INVALID;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t timeout = 0;
+    if (read_timeout_flag(&timeout, s) != cudaSuccess) return UFP4_ERR_CUDA;
+    if (timeout) return UFP4_ERR_TIMEOUT;
+    if (!workspace) return UFP4_OK;
+    uint32_t flag = 0;
+    cudaError_t e = cudaMemcpyAsync(&flag, static_cast<const char *>(workspace) + kWsStatus,
+                                    sizeof flag, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return UFP4_ERR_CUDA;
+    return flag ? UFP4_ERR_NONFINITE : UFP4_OK;
+}
+
+ufp4_status ufp4_dequantize(const ufp4_qtensor *q, int32_t inverse_rht, uint64_t rht_seed,
+                            float *out, int64_t ld_out, ufp4_stream_t stream) {
+    if (!valid_qtensor(q) || (inverse_rht != 0 && inverse_rht != 1)) return UFP4_ERR_INVALID;
+    if (q->rows == 0 || q->k == 0) return UFP4_OK;
+    if (!out || !aligned(out, 16) || ld_out < q->k || ld_out % 4 != 0) return UFP4_ERR_INVALID;
+    return from_cuda(launch_dequantize(q->codes, q->scales, q->tensor_scale, q->rows, q->k,
+                                       q->grid, inverse_rht, rht_seed, out, ld_out,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ufp4_status ufp4_gemm(const ufp4_qtensor *a, const ufp4_qtensor *b, float *c, int64_t ldc,
+                      ufp4_stream_t stream) {
+    if (!valid_qtensor(a) || !valid_qtensor(b)) return UFP4_ERR_INVALID;
+    if (a->k != b->k) return UFP4_ERR_INVALID;
+    if (a->grid != b->grid) return UFP4_ERR_UNSUPPORTED;
+    const int64_t M = a->rows, N = b->rows, K = a->k;
+    if (M == 0 || N == 0) return UFP4_OK;
+    if (!c || !aligned(c, 16) || ldc < N || ldc % 4 != 0) return UFP4_ERR_INVALID;
+    if (M > (int64_t)INT32_MAX || N > (int64_t)INT32_MAX || K > (int64_t)INT32_MAX)
+        return UFP4_ERR_INVALID;
+    return from_cuda(launch_gemm(a->codes, a->scales, a->tensor_scale, b->codes, b->scales,
+                                 b->tensor_scale, M, N, K, a->grid, c, ldc,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ufp4_status ufp4_stats(const void *x, int32_t dtype, int64_t rows, int64_t cols, int64_t ld,
+                       const ufp4_qparams *p, const ufp4_qtensor *qt, void *workspace,
+                       size_t workspace_bytes, ufp4_stats_t *host_out, ufp4_stream_t stream) {
+    if (!host_out) return UFP4_ERR_INVALID;
+    QuantLaunch q;
+    ufp4_status st = check_quant_args(x, dtype, rows, cols, ld, p, qt, &q);
+    if (st != UFP4_OK) return st;
+    if (!valid_workspace(workspace, workspace_bytes)) return UFP4_ERR_INVALID;
+    double s[5] = {0, 0, 0, 0, 0};
+    if (rows > 0 && cols > 0) {
+        cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+        int n = 0;
+        cudaError_t e = launch_stats(q, workspace, &n, cs);
+        if (e != cudaSuccess) return from_cuda(e);
+        std::vector<double> part((size_t)n * 8);
+        e = cudaMemcpyAsync(part.data(), static_cast<char *>(workspace) + kWsStats,
+                            part.size() * sizeof(double), cudaMemcpyDeviceToHost, cs);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+        if (e != cudaSuccess) return UFP4_ERR_CUDA;
+        for (int i = 0; i < n; ++i)
+            for (int j = 0; j < 5; ++j) s[j] += part[(size_t)i * 8 + j];
+    }
+    ufp4_stats_t r{};
+    r.sum_aq = s[0]; r.sum_aa = s[1]; r.sum_err2 = s[2]; r.bias_count = s[4];
+    r.alpha = s[1] > 0 ? s[0] / s[1] : 1.0;
+    r.sqnr_db = s[2] > 0 ? 10.0 * std::log10(s[1] / s[2]) : INFINITY;
+    r.mean_bias = s[4] > 0 ? s[3] / s[4] : 0.0;
+    *host_out = r;
+    return UFP4_OK;
+}
+
+}  // extern "C"

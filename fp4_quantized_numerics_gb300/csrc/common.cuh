@@ -1,0 +1,171 @@
+// common.cuh -- device helpers shared by the libufp4 kernels (sm_103a).
+//
+// Method sources: the pages on arXiv:2606.20381 ("Rethinking Shrinkage Bias
+// in LLM FP4 Pretraining"), cited as [ZC] zhichai.net post, [AN]
+// autonainews.com article, [HP] hotpaper.ai card.  Formats and layouts that
+// the pages leave open follow the contract stated in include/ufp4.h.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace ufp4 {
+
+constexpr int kE2M1 = 0;
+constexpr int kE1M2 = 1;
+constexpr int kRTNE = 0;
+constexpr int kSR = 1;
+constexpr float kFltMax = 3.402823466e38f;
+
+__host__ __device__ __forceinline__ float grid_qmax(int grid) { return grid == kE2M1 ? 6.0f : 3.5f; }
+
+__host__ __device__ __forceinline__ int64_t kpad_of(int64_t k) { return (k + 63) / 64 * 64; }
+__host__ __device__ __forceinline__ int64_t rpad_of(int64_t r) { return (r + 127) / 128 * 128; }
+
+// Byte offset of block scale (row r, 16-block b) in the tensor-core scale
+// layout: 512-byte atoms of 128 rows x 4 blocks, atoms ordered (row tile,
+// block group); inside an atom row r sits at (r%32)*16 + ((r%128)/32)*4.
+__host__ __device__ __forceinline__ int64_t scale_offset(int64_t r, int64_t b, int64_t nkt) {
+    return (((r >> 7) * nkt + (b >> 2)) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2) + (b & 3);
+}
+
+// ---------------------------------------------------------------- Philox
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of the 4x32
+// S-box with multipliers 0xD2511F53 / 0xCD9E8D57 and key increments
+// 0x9E3779B9 / 0xBB67AE85.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+        k.x += 0x9E3779B9u;
+        k.y += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// RHT sign pattern d as a 16-bit mask (bit j set <=> d_j = -1): bits 0..15
+// of word 0 of Philox4x32-10(key = seed, counter = 0).
+__device__ __forceinline__ uint32_t rht_sign_mask(uint64_t seed) {
+    const uint4 w = philox4x32_10(make_uint4(0u, 0u, 0u, 0u),
+                                  make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+    return w.x & 0xFFFFu;
+}
+
+// ------------------------------------------------------------- E4M3 codec
+// fp32 -> E4M3, round to nearest even, saturating to +-448 (hardware cvt).
+__device__ __forceinline__ uint32_t e4m3_from_f32(float v) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+    return r & 0xFFu;
+}
+
+// E4M3 -> fp32 (exact; via the hardware f16 path).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+    uint32_t h2;
+    const uint16_t in = (uint16_t)(c & 0xFFu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+    return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+
+// --------------------------------------------------------------- bf16 bits
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// NaN-propagating max of magnitudes.
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+// ------------------------------------------------------------- grid codes
+// E2M1 round-to-nearest-even of a pair, satfinite; first argument goes to
+// the LOW nibble of the returned byte.
+__device__ __forceinline__ uint32_t e2m1x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+        "cvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// E1M2 round-to-nearest-even of q (grid units): m = rint(min(2|q|, 7)); 2|q|
+// is exact (or +inf, which clamps to 7).  Adding 2^23 rounds a value in
+// [0, 8) to an integer with ties to even, leaving it in the low mantissa bits.
+__device__ __forceinline__ uint32_t e1m2_rn(float q) {
+    const float a2 = fminf(fabsf(q) * 2.0f, 7.0f);
+    const uint32_t m = __float_as_uint(__fadd_rn(a2, 8388608.0f)) & 7u;
+    return m | ((__float_as_uint(q) >> 28) & 8u);
+}
+
+// Stochastic rounding of q (in grid units) with 32 random bits r: floor to
+// the grid point below |q| (clamped to qmax), then up with probability
+// p = (a - lo) / (hi - lo) against u = (r >> 8) * 2^-24.  Returns the code.
+template <int GRID>
+__device__ __forceinline__ uint32_t sr_code(float q, uint32_t r) {
+    const uint32_t sgn = (__float_as_uint(q) >> 28) & 8u;
+    const float u = __fmul_rn(__uint2float_rn(r >> 8), 5.9604644775390625e-8f);
+    if (GRID == kE1M2) {
+        const float a2 = fminf(fabsf(q) * 2.0f, 7.0f);   // 2a, exact
+        const float fl = floorf(a2);
+        const float p = __fsub_rn(a2, fl);               // exact
+        uint32_t m = (uint32_t)fl + (u < p ? 1u : 0u);
+        return sgn | m;
+    } else {
+        const float a = fminf(fabsf(q), 6.0f);
+        if (a >= 6.0f) return sgn | 7u;
+        const float step = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
+        const float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
+        const float lo = __fmul_rn(floorf(__fmul_rn(a, inv)), step);  // exact
+        const float p = __fmul_rn(__fsub_rn(a, lo), inv);             // exact
+        // index of lo: 0,.5,1,1.5 -> 0..3 ; 2 -> 4 ; 3 -> 5 ; 4 -> 6
+        uint32_t m = lo < 2.0f ? (uint32_t)(lo * 2.0f) : (lo < 4.0f ? (uint32_t)lo + 2u : 6u);
+        m += (u < p ? 1u : 0u);
+        return sgn | m;
+    }
+}
+
+// Grid value of a magnitude index.
+// E2M1: 0, .5, 1, 1.5, 2, 3, 4, 6;  E1M2: m / 2.
+__device__ __forceinline__ float grid_value(int grid, uint32_t m) {
+    m &= 7u;
+    if (grid == kE1M2 || m < 4u) return 0.5f * (float)m;
+    return m == 7u ? 6.0f : (float)(m - 2u);
+}
+
+// ---------------------------------------------------------- in-register FWHT
+// Unnormalised 8-point Walsh-Hadamard butterflies (Sylvester order):
+// v_i <- sum_j (-1)^popcount(i&j) v_j.
+__device__ __forceinline__ void fwht8(float v[8]) {
+#pragma unroll
+    for (int s = 1; s < 8; s <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if ((i & s) == 0) {
+                const float a = v[i], b = v[i + s];
+                v[i] = a + b;
+                v[i + s] = a - b;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void fwht16(float v[16]) {
+#pragma unroll
+    for (int s = 1; s < 16; s <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if ((i & s) == 0) {
+                const float a = v[i], b = v[i + s];
+                v[i] = a + b;
+                v[i + s] = a - b;
+            }
+        }
+    }
+}
+
+}  // namespace ufp4

@@ -1,0 +1,365 @@
+// gemm.cu -- block-scaled FP4 GEMM C = A B^T on the sm_100-family tcgen05
+// tensor cores (hand-written PTX: TMA, mbarriers, TMEM, tcgen05.mma).
+//
+// The three training GEMMs of the recipe (fwd_y, bwd_dx, bwd_dw) consume the
+// quantized operands ([ZC] zhichai.net post "Shrinkage Bias: The Hidden
+// Geometric Trap in FP4 Training ... and the UFP4 Fix", Key points, "The fix
+// -- UFP4"; [HP] hotpaper.ai card, technical approach).  Both operands are
+// K-major packed 4-bit codes with one E4M3 scale per 16 K-elements and one
+// FP32 tensor scale:  C[m][n] = S_A S_B sum_k (v_A e_A)(v_B e_B).
+//
+// E2M1: the codes ARE the tensor cores' E2M1 elements and the block scales
+//   are UE4M3 scale_vec::4X factors, so each 64-wide K step is one
+//   tcgen05.mma.kind::mxf4nvf4.block_scale.
+// E1M2: not a tensor-core format.  Each magnitude m/2 splits exactly as
+//   a + b/2 with a = m >> 1 in {0,1,2,3} and b = m & 1, both representable in
+//   E2M1 (a -> 0,1,2,3; b/2 -> 0 or 0.5), with the sign copied to both parts
+//   and the block scale shared.  Warps expand each staged tile into a "hi"
+//   and a "lo" E2M1 plane in shared memory and four MMAs (hi*hi, hi*lo,
+//   lo*hi, lo*lo) accumulate into the same TMEM accumulator -- exact, since
+//   every product and partial sum of the dequantized values is what the
+//   single E1M2 product would give.
+//
+// CTA: 192 threads.  Warp 0 = TMA producer, warp 1 = TMEM owner + single-
+// thread MMA issuer, warps 2-5 = epilogue (and, for E1M2, the expanders).
+// Tile 128 x 128, K step per stage 256 (128 bytes per row, one 128-byte
+// swizzle atom), multi-stage mbarrier ring, accumulator in TMEM.
+// Every wait is bounded: on timeout the kernel raises g_ufp4_timeout, drains
+// its own copies, frees TMEM and returns.
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+namespace ufp4 {
+
+__device__ uint32_t g_ufp4_timeout;
+
+namespace {
+
+constexpr int BM = 128, BN = 128;
+constexpr int BK_BYTES = 128;                 // 256 FP4 elements per stage
+constexpr uint32_t TILE_BYTES = 128 * 128;    // 16 KB per operand tile
+constexpr uint32_t SF_BYTES = 4 * 512;        // 4 scale atoms per operand per stage
+constexpr int kGemmThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCol = 0;               // accumulator: columns [0, 128)
+constexpr uint32_t kSfCol = 128;              // scales: 32 columns per stage
+constexpr long long kWaitBudget = 4000000000LL;
+
+template <int GRID>
+struct Cfg {
+    static constexpr int kStages = GRID == kE2M1 ? 5 : 3;
+    // stage layout: A | B | (A_lo | B_lo for E1M2) | SFA | SFB
+    static constexpr uint32_t kAOff = 0;
+    static constexpr uint32_t kBOff = TILE_BYTES;
+    static constexpr uint32_t kALoOff = 2 * TILE_BYTES;
+    static constexpr uint32_t kBLoOff = 3 * TILE_BYTES;
+    static constexpr uint32_t kSfaOff = (GRID == kE2M1 ? 2 : 4) * TILE_BYTES;
+    static constexpr uint32_t kSfbOff = kSfaOff + SF_BYTES;
+    static constexpr uint32_t kStageBytes = kSfbOff + SF_BYTES;  // multiple of 1024
+    static constexpr uint32_t kBarOff = kStages * kStageBytes;
+    static constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;  // + barriers + alignment slack
+};
+
+struct GemmParams {
+    const uint8_t *sfa, *sfb;
+    const float *ts_a, *ts_b;
+    float *c;
+    int64_t ldc;
+    int M, N;
+    int nkt;      // kpad / 64: scale atoms per 128-row tile
+    int num_kb;   // ceil(nkt / 4): pipeline stages of K
+};
+
+__device__ __forceinline__ void raise_timeout() { atomicOr(&g_ufp4_timeout, 1u); }
+
+// E1M2 nibbles -> (hi, lo) E2M1 nibbles, 8 at a time (see file header).
+__device__ __forceinline__ void split_e1m2(uint32_t w, uint32_t &hi, uint32_t &lo) {
+    const uint32_t s = w & 0x88888888u;
+    const uint32_t m2 = (w >> 2) & 0x11111111u;
+    const uint32_t m1 = (w >> 1) & 0x11111111u;
+    const uint32_t m0 = w & 0x11111111u;
+    hi = s | (m2 << 2) | ((m1 & ~m2) << 1) | (m1 & m2);
+    lo = s | m0;
+}
+
+template <int GRID>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+           GemmParams p) {
+    using C = Cfg<GRID>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+    // bars[0..S): full (TMA landed), [S..2S): empty (MMA done with stage),
+    // [2S..3S): expanded (E1M2 planes ready), [3S]: accumulator ready
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * S + 1);
+    const uint32_t smem_base = ptx::smem_u32(smem);
+    const uint32_t bar_base = ptx::smem_u32(bars);
+    auto full = [&](int s) { return bar_base + 8u * s; };
+    auto empty = [&](int s) { return bar_base + 8u * (S + s); };
+    auto expd = [&](int s) { return bar_base + 8u * (2 * S + s); };
+    const uint32_t acc_bar = bar_base + 8u * (3 * S);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(full(s), 1);
+            ptx::mbar_init(empty(s), 1);
+            ptx::mbar_init(expd(s), 4);   // one arrival per expander warp
+        }
+        ptx::mbar_init(acc_bar, 1);
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tma_a);
+        ptx::prefetch_tmap(&tma_b);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                const int s = kb % S, round = kb / S;
+                if (round > 0 && !ptx::mbar_wait_bounded(empty(s), (round - 1) & 1, kWaitBudget)) {
+                    raise_timeout();
+                    break;
+                }
+                const int atoms = min(4, p.nkt - 4 * kb);
+                const uint32_t st = smem_base + s * C::kStageBytes;
+                ptx::mbar_arrive_expect_tx(full(s), 2 * TILE_BYTES + 2u * atoms * 512u);
+                ptx::tma_load_2d(st + C::kAOff, &tma_a, kb * BK_BYTES, m0, full(s));
+                ptx::tma_load_2d(st + C::kBOff, &tma_b, kb * BK_BYTES, n0, full(s));
+                ptx::bulk_load(st + C::kSfaOff, p.sfa + ((size_t)(m0 / 128) * p.nkt + 4 * kb) * 512,
+                               atoms * 512u, full(s));
+                ptx::bulk_load(st + C::kSfbOff, p.sfb + ((size_t)(n0 / 128) * p.nkt + 4 * kb) * 512,
+                               atoms * 512u, full(s));
+                issued = kb + 1;
+            }
+            // Drain: every copy this thread issued has landed before exit.
+            for (int kb = max(0, issued - S); kb < issued; ++kb) {
+                if (!ptx::mbar_wait_bounded(full(kb % S), (kb / S) & 1, kWaitBudget)) {
+                    raise_timeout();
+                    break;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            // instruction descriptor, kind::mxf4nvf4: A/B E2M1 (1), K-major,
+            // N >> 3 at [17,23), UE4M3 scales (bit 23 = 0), M >> 4 at [24,29).
+            const uint32_t idesc = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                                   ((uint32_t)(BM >> 4) << 24);
+            bool ok = true;
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                const int s = kb % S, round = kb / S;
+                const uint32_t wait_bar = GRID == kE2M1 ? full(s) : expd(s);
+                if (!ptx::mbar_wait_bounded(wait_bar, round & 1, kWaitBudget)) {
+                    raise_timeout();
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const int atoms = min(4, p.nkt - 4 * kb);
+                const uint32_t st = smem_base + s * C::kStageBytes;
+                const uint32_t sf_t = tmem + kSfCol + 32u * s;
+                for (int j = 0; j < atoms; ++j) {
+                    ptx::tc_cp_32x128b_warpx4(sf_t + 4u * j, ptx::sdesc(st + C::kSfaOff + 512u * j, 0, 128, 0));
+                    ptx::tc_cp_32x128b_warpx4(sf_t + 16u + 4u * j, ptx::sdesc(st + C::kSfbOff + 512u * j, 0, 128, 0));
+                }
+                for (int j = 0; j < atoms; ++j) {
+                    const uint32_t sfa = sf_t + 4u * j, sfb = sf_t + 16u + 4u * j;
+                    const uint32_t first = (kb == 0 && j == 0) ? 0u : 1u;
+                    if (GRID == kE2M1) {
+                        ptx::tc_mma_nvf4(tmem + kAccCol, ptx::sdesc(st + C::kAOff + 32u * j, 16, 1024, 2),
+                                         ptx::sdesc(st + C::kBOff + 32u * j, 16, 1024, 2), idesc, sfa, sfb,
+                                         first);
+                    } else {
+                        const uint32_t ah = st + C::kAOff + 32u * j, al = st + C::kALoOff + 32u * j;
+                        const uint32_t bh = st + C::kBOff + 32u * j, bl = st + C::kBLoOff + 32u * j;
+                        ptx::tc_mma_nvf4(tmem + kAccCol, ptx::sdesc(ah, 16, 1024, 2), ptx::sdesc(bh, 16, 1024, 2),
+                                         idesc, sfa, sfb, first);
+                        ptx::tc_mma_nvf4(tmem + kAccCol, ptx::sdesc(ah, 16, 1024, 2), ptx::sdesc(bl, 16, 1024, 2),
+                                         idesc, sfa, sfb, 1u);
+                        ptx::tc_mma_nvf4(tmem + kAccCol, ptx::sdesc(al, 16, 1024, 2), ptx::sdesc(bh, 16, 1024, 2),
+                                         idesc, sfa, sfb, 1u);
+                        ptx::tc_mma_nvf4(tmem + kAccCol, ptx::sdesc(al, 16, 1024, 2), ptx::sdesc(bl, 16, 1024, 2),
+                                         idesc, sfa, sfb, 1u);
+                    }
+                }
+                ptx::tc_commit(empty(s));
+            }
+            (void)ok;
+            ptx::tc_commit(acc_bar);   // fires once every MMA above has completed
+            // TMEM is freed below only after every MMA has finished with it.
+            if (!ptx::mbar_wait_bounded(acc_bar, 0, kWaitBudget)) raise_timeout();
+        }
+    } else {
+        // ------------------------------------- expanders (E1M2) + epilogue
+        const int et = threadIdx.x - 64;   // 0..127
+        bool ok = true;
+        if (GRID == kE1M2) {
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                const int s = kb % S, round = kb / S;
+                if (!ptx::mbar_wait_bounded(full(s), round & 1, kWaitBudget)) {
+                    raise_timeout();
+                    ok = false;
+                    break;
+                }
+                uint8_t *st = smem + s * C::kStageBytes;
+#pragma unroll 4
+                for (int i = et; i < (int)(TILE_BYTES / 16); i += 128) {
+                    uint4 *pa = reinterpret_cast<uint4 *>(st + C::kAOff) + i;
+                    uint4 *pb = reinterpret_cast<uint4 *>(st + C::kBOff) + i;
+                    uint4 a = *pa, b = *pb, ah, alo, bh, blo;
+                    split_e1m2(a.x, ah.x, alo.x); split_e1m2(a.y, ah.y, alo.y);
+                    split_e1m2(a.z, ah.z, alo.z); split_e1m2(a.w, ah.w, alo.w);
+                    split_e1m2(b.x, bh.x, blo.x); split_e1m2(b.y, bh.y, blo.y);
+                    split_e1m2(b.z, bh.z, blo.z); split_e1m2(b.w, bh.w, blo.w);
+                    *pa = ah;
+                    *pb = bh;
+                    reinterpret_cast<uint4 *>(st + C::kALoOff)[i] = alo;
+                    reinterpret_cast<uint4 *>(st + C::kBLoOff)[i] = blo;
+                }
+                // generic-proxy writes -> visible to the tensor cores (async proxy)
+                ptx::fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(expd(s));
+            }
+        }
+        const int q = warp & 3;                 // TMEM lane quadrant of this warp
+        const int row = m0 + 32 * q + lane;
+        if (ok && !ptx::mbar_wait_bounded(acc_bar, 0, kWaitBudget)) {
+            raise_timeout();
+            ok = false;
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        ptx::tc_fence_after();
+        if (ok) {
+            const float alpha = __fmul_rn(*p.ts_a, *p.ts_b);
+            float *crow = p.c + (int64_t)row * p.ldc;
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                uint32_t r[32];
+                ptx::tc_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + kAccCol + 32u * ch, r);
+                ptx::tc_wait_ld();
+                const int col0 = n0 + 32 * ch;
+                if (row < p.M) {
+                    if (col0 + 32 <= p.N) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            float4 v = make_float4(__uint_as_float(r[i]) * alpha, __uint_as_float(r[i + 1]) * alpha,
+                                                   __uint_as_float(r[i + 2]) * alpha, __uint_as_float(r[i + 3]) * alpha);
+                            *reinterpret_cast<float4 *>(crow + col0 + i) = v;
+                        }
+                    } else {
+                        for (int i = 0; i < 32; ++i)
+                            if (col0 + i < p.N) crow[col0 + i] = __uint_as_float(r[i]) * alpha;
+                    }
+                }
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+bool make_code_map(CUtensorMap *m, const uint8_t *codes, int64_t rows, int64_t kpad) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)(kpad / 2), (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(kpad / 2)};
+    cuuint32_t box[2] = {(cuuint32_t)BK_BYTES, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int GRID>
+cudaError_t run_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams &p, cudaStream_t s) {
+    using C = Cfg<GRID>;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(k_gemm<GRID>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    dim3 grid((p.N + BN - 1) / BN, (p.M + BM - 1) / BM);
+    k_gemm<GRID><<<grid, kGemmThreads, C::kSmemBytes, s>>>(ma, mb, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_ts,
+                        const uint8_t *b_codes, const uint8_t *b_scales, const float *b_ts, int64_t M,
+                        int64_t N, int64_t K, int grid, float *c, int64_t ldc, cudaStream_t s) {
+    if (K == 0) return cudaMemset2DAsync(c, ldc * sizeof(float), 0, N * sizeof(float), M, s);
+    const int64_t kpad = kpad_of(K);
+    CUtensorMap ma, mb;
+    if (!make_code_map(&ma, a_codes, M, kpad) || !make_code_map(&mb, b_codes, N, kpad))
+        return cudaErrorInvalidValue;
+    GemmParams p{};
+    p.sfa = a_scales; p.sfb = b_scales; p.ts_a = a_ts; p.ts_b = b_ts;
+    p.c = c; p.ldc = ldc; p.M = (int)M; p.N = (int)N;
+    p.nkt = (int)(kpad / 64);
+    p.num_kb = (p.nkt + 3) / 4;
+    if (grid == kE2M1) return run_gemm<kE2M1>(ma, mb, p, s);
+    return run_gemm<kE1M2>(ma, mb, p, s);
+}
+
+cudaError_t read_timeout_flag(uint32_t *flag, cudaStream_t s) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(flag, g_ufp4_timeout, sizeof(uint32_t), 0,
+                                              cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && *flag) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_ufp4_timeout, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    return e;
+}
+
+}  // namespace ufp4

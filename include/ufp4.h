@@ -1,0 +1,225 @@
+/*
+ * ufp4.h -- C ABI of libufp4, the GB300 (sm_103a) hot path of the UFP4 FP4
+ * training recipe: fused Random Hadamard Transform + block-scaled 4-bit
+ * quantization of GEMM operands, and block-scaled FP4 GEMMs on the tcgen05
+ * tensor cores.
+ *
+ * Method sources (three web pages on arXiv:2606.20381, "Rethinking Shrinkage
+ * Bias in LLM FP4 Pretraining: Geometric Origin, Systemic Impact, and UFP4
+ * Recipe"):
+ *   [ZC] zhichai.net post "Shrinkage Bias: The Hidden Geometric Trap in FP4
+ *        Training ... and the UFP4 Fix" (Key points: "The cause", "Compounding
+ *        decay", "The RHT paradox", "The fix -- UFP4");
+ *   [AN] autonainews.com article "UFP4 Eliminates Shrinkage Bias in FP4 LLM
+ *        Pretraining, Ant Group Research Finds" ("The UFP4 Recipe");
+ *   [HP] hotpaper.ai card of the paper (abstract, technical approach).
+ * The pages define the grids, the rounding modes and where RHT and SR apply;
+ * they fix no block size, scale format, RNG, layout or interface.  The choices
+ * made here (16-element blocks, E4M3 block scale, FP32 tensor scale, Philox
+ * stochastic rounding, layouts below) are this library's contract.
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers unless marked "host".  The
+ *     caller allocates and owns every buffer; the library never allocates,
+ *     never frees, and keeps no state between calls.
+ *   - Work is enqueued on `stream` and returns without synchronising, except
+ *     where a call is documented to synchronise (it returns host values).
+ *   - Argument errors are found on the host before anything is launched and
+ *     return UFP4_ERR_INVALID (or UFP4_ERR_UNSUPPORTED for a valid request
+ *     this build does not implement); a failed launch returns UFP4_ERR_CUDA.
+ *     Faults inside an already-launched kernel surface through the CUDA
+ *     runtime on a later synchronisation, as for any CUDA library.
+ *   - Zero-sized tensors are a no-op returning UFP4_OK.
+ */
+#ifndef UFP4_H_
+#define UFP4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define UFP4_API __attribute__((visibility("default")))
+#else
+#define UFP4_API
+#endif
+
+typedef struct CUstream_st *ufp4_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    UFP4_OK = 0,
+    UFP4_ERR_INVALID = 1,      /* bad pointer, size, alignment or enum */
+    UFP4_ERR_UNSUPPORTED = 2,  /* valid request not implemented by this build */
+    UFP4_ERR_NONFINITE = 3,    /* NaN/Inf input seen (reported by ufp4_check) */
+    UFP4_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+    UFP4_ERR_TIMEOUT = 5       /* a bounded device-side wait gave up */
+} ufp4_status;
+
+/* 4-bit grids.  A code is (sign << 3) | m with magnitude index m = 0..7.
+ *   UFP4_E2M1: magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6} -- the non-uniform
+ *              Blackwell FP4 format ([ZC] "The cause").
+ *   UFP4_E1M2: magnitudes {0, .5, 1, ..., 3.5} = m/2 -- the uniform grid of
+ *              UFP4 ([ZC] "The fix -- UFP4"; [AN] "The UFP4 Recipe"). */
+typedef enum { UFP4_E2M1 = 0, UFP4_E1M2 = 1 } ufp4_grid;
+
+/* Rounding onto the grid: round-to-nearest-even, or stochastic rounding
+ * (the pages apply SR to dY only: [HP] key contributions; [ZC] "The fix"). */
+typedef enum { UFP4_RTNE = 0, UFP4_SR = 1 } ufp4_round;
+
+/* Element type of the tensor to quantize. */
+typedef enum { UFP4_BF16 = 0, UFP4_FP32 = 1 } ufp4_dtype;
+
+#define UFP4_BLOCK 16
+
+/* Quantization parameters.
+ *   grid, round  : see above.
+ *   block        : must be 16.
+ *   rht          : 1 = rotate every 16-block along K by y = (1/4) H16 diag(d) x
+ *                  before quantizing ([ZC] "The RHT paradox"; UFP4 applies it
+ *                  on all three GEMMs).  H16 is the Sylvester Hadamard matrix,
+ *                  H[i][j] = (-1)^popcount(i & j); d_j = -1 iff bit j of word 0
+ *                  of Philox4x32-10(key = rht_seed, counter = 0) is set.  Both
+ *                  operands of a GEMM must use the same rht_seed.
+ *   sr_seed, sr_counter : SR draws, for logical element i of the output
+ *                  (i = row * k + col of the quantized orientation), word i%4
+ *                  of Philox4x32-10(key = sr_seed, ctr = (i/4, sr_counter)),
+ *                  and rounds up iff (word >> 8) * 2^-24 < p, p the position of
+ *                  the value between its two neighbouring grid points.
+ *   colwise      : 0 = 16-blocks run along the contiguous (last) dim and the
+ *                  result is the quantization of X (rows x cols); 1 = blocks
+ *                  run down the columns and the result is the quantization of
+ *                  X^T (cols x rows), as the bwd_dx / bwd_dw GEMMs need.
+ *   amax_in      : optional device pointer to the tensor amax A_t of the
+ *                  (rotated) input; NULL = computed by the call.
+ * Tensor scale: S_enc = fl32(448 qmax / A_t) (clamped to FLT_MAX), stored
+ * S_dec = fl32(A_t / (448 qmax)); A_t = 0 gives S_enc = S_dec = 1.
+ * Block scale:  e_b = E4M3_rne_satfinite(fl32(fl32(amax_b / qmax) * S_enc)).
+ * Element:      q = fl32(y * fl32(S_enc / e_b)), a = min(|q|, qmax),
+ *               code = signbit(q) << 3 | round(a); e_b = 0 gives code 0.   */
+typedef struct {
+    int32_t grid;
+    int32_t block;
+    int32_t rht;
+    int32_t round;
+    uint64_t rht_seed;
+    uint64_t sr_seed;
+    uint64_t sr_counter;
+    int32_t colwise;
+    int32_t reserved;          /* must be 0 */
+    const float *amax_in;
+} ufp4_qparams;
+
+/* A quantized tensor of logical shape rows x k (16-blocks along k).
+ *   kpad   = ufp4_kpad(k) = k rounded up to a multiple of 64.
+ *   codes  : uint8 [rows][kpad/2]; byte j of a row holds element 2j in bits
+ *            3..0 and element 2j+1 in bits 7..4 (the packed K-major FP4
+ *            operand layout of the tensor cores).  Elements k..kpad-1 are 0.
+ *   scales : E4M3 bytes in the tensor cores' block-scale layout: atoms of
+ *            128 rows x 4 blocks (512 bytes); scale (r, b) of row r and
+ *            16-block b lives at byte
+ *              ((r / 128) * (kpad / 64) + b / 4) * 512
+ *              + (r % 32) * 16 + ((r % 128) / 32) * 4 + (b % 4).
+ *            Size ufp4_scales_bytes(rows, k); entries of rows >= rows or
+ *            blocks >= k/16 are written as 0.
+ *   tensor_scale : 1 fp32, S_dec.
+ *   Values: x ~= v(m) * e_b * S_dec (then the inverse RHT when rht was on).
+ *   Alignment: codes and scales 16-byte aligned, tensor_scale 4-byte.  */
+typedef struct {
+    uint8_t *codes;
+    uint8_t *scales;
+    float *tensor_scale;
+    int64_t rows;
+    int64_t k;
+    int32_t grid;
+    int32_t reserved;          /* must be 0 */
+} ufp4_qtensor;
+
+/* Host-side size helpers (no GPU needed). */
+UFP4_API int64_t ufp4_kpad(int64_t k);
+UFP4_API int64_t ufp4_codes_bytes(int64_t rows, int64_t k);
+UFP4_API int64_t ufp4_scales_bytes(int64_t rows, int64_t k);
+/* Bytes of the scratch buffer that ufp4_quantize and ufp4_stats take. */
+UFP4_API size_t ufp4_workspace_bytes(void);
+
+/* Fused (RHT +) block quantization of one BF16 or FP32 matrix.
+ *   x        : device, rows x cols elements of `dtype`, row stride ld
+ *              elements; 16-byte aligned, ld * sizeof(elem) a multiple of 16.
+ *   rows, cols: the matrix as stored.  Row-wise: cols % 16 == 0 and the
+ *              result has shape rows x cols.  Column-wise: rows % 16 == 0,
+ *              cols % 4 == 0 and the result has shape cols x rows.
+ *   p        : host pointer to the parameters above.
+ *   out      : host pointer; caller fills codes/scales/tensor_scale with
+ *              device buffers and rows/k/grid with the result's shape.
+ *   workspace: device scratch of workspace_bytes >= ufp4_workspace_bytes(),
+ *              16-byte aligned; used when p->amax_in is NULL to hold per-CTA
+ *              partial maxima and a status word (see ufp4_check).
+ * ([ZC] "The fix -- UFP4"; [AN] "The UFP4 Recipe".)                        */
+UFP4_API ufp4_status ufp4_quantize(const void *x, int32_t dtype, int64_t rows, int64_t cols, int64_t ld,
+                          const ufp4_qparams *p, const ufp4_qtensor *out,
+                          void *workspace, size_t workspace_bytes, ufp4_stream_t stream);
+
+/* Reports device-side problems (synchronises `stream`):
+ *   UFP4_ERR_TIMEOUT   -- a bounded wait inside a GEMM kernel gave up since
+ *                         the last check (the flag is then cleared); that
+ *                         GEMM's output is unspecified;
+ *   UFP4_ERR_NONFINITE -- the last ufp4_quantize that used `workspace` saw a
+ *                         NaN/Inf input (computed-amax path) or a non-finite
+ *                         amax_in; its outputs are unspecified.
+ * `workspace` may be NULL to check only the timeout flag. */
+UFP4_API ufp4_status ufp4_check(const void *workspace, ufp4_stream_t stream);
+
+/* out[r][c] = v(m) * e_b * S_dec as fp32, computed as fl32(fl32(v e_b) S_dec);
+ * with inverse_rht = 1, each 16-block is then rotated back with the signs of
+ * rht_seed: x = diag(d) (1/4) H16 y.  out: device fp32, q->rows x q->k, row
+ * stride ld_out >= q->k elements, 16-byte aligned, ld_out % 4 == 0. */
+UFP4_API ufp4_status ufp4_dequantize(const ufp4_qtensor *q, int32_t inverse_rht, uint64_t rht_seed,
+                            float *out, int64_t ld_out, ufp4_stream_t stream);
+
+/* C = A B^T with FP32 accumulation: A is M x K, B is N x K (both quantized
+ * along K, same grid), C is M x N fp32 row-major with row stride ldc.
+ *   C[m][n] = S_A S_B sum_k (v_A e_A)(v_B e_B)
+ * This is fwd_y (Y = X W^T: A = X rows, B = W rows), bwd_dx (dX = dY W:
+ * A = dY rows, B = W columns) or bwd_dw (dW = dY^T X: A = dY columns,
+ * B = X columns) ([ZC] "The fix -- UFP4"; [HP] technical approach).
+ * E2M1 runs natively on tcgen05 block-scaled FP4 MMAs; E1M2 codes are split
+ * exactly into two E2M1 planes per operand in shared memory.
+ * Requirements: a->k == b->k, a->grid == b->grid; c 16-byte aligned,
+ * ldc >= N and ldc % 4 == 0.  K = 0 writes zeros. */
+UFP4_API ufp4_status ufp4_gemm(const ufp4_qtensor *a, const ufp4_qtensor *b, float *c, int64_t ldc,
+                      ufp4_stream_t stream);
+
+/* Quality of one quantization, in fp64 on the host ([ZC] "The cause",
+ * "Compounding decay", "The RHT paradox").  A is the tensor that was
+ * quantized (x, rotated when p->rht; transposed when p->colwise):
+ *   alpha = <deq, A> / <A, A>       (shrinkage factor; < 1 pulls to zero)
+ *   sqnr_db = 10 log10(<A, A> / ||A - deq||^2)
+ *   mean_bias = mean over elements with a != 0 of (v(m) - a), grid units,
+ *               a = min(|A| / (e_b S_dec), qmax); blocks with e_b = 0 skipped.
+ * x, dtype, rows, cols, ld, p: exactly as given to ufp4_quantize for q.
+ * Synchronises `stream`; host_out is a host pointer. */
+typedef struct {
+    double alpha;
+    double sqnr_db;
+    double mean_bias;
+    double sum_aq;
+    double sum_aa;
+    double sum_err2;
+    double bias_count;
+} ufp4_stats_t;
+
+UFP4_API ufp4_status ufp4_stats(const void *x, int32_t dtype, int64_t rows, int64_t cols, int64_t ld,
+                       const ufp4_qparams *p, const ufp4_qtensor *q,
+                       void *workspace, size_t workspace_bytes,
+                       ufp4_stats_t *host_out, ufp4_stream_t stream);
+
+/* Static description of a status code. */
+UFP4_API const char *ufp4_status_string(ufp4_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UFP4_H_ */

@@ -1,0 +1,146 @@
+"""CPU-only checks of the libufp4 C ABI: the library loads, exports every
+symbol include/ufp4.h declares, its size helpers agree with the documented
+layouts, and invalid arguments are rejected on the host before any launch.
+No call here reaches the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.layouts import kpad, rpad
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from fp4_quantized_numerics_gb300 import build, ufp4
+    build.build()
+    return ufp4.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "ufp4.h")).read()
+    return sorted(set(re.findall(r"UFP4_API[^;(]*?\b(ufp4_\w+)\s*\(", src)))
+
+
+def test_header_declares_expected_calls():
+    names = _declared()
+    for n in ["ufp4_quantize", "ufp4_dequantize", "ufp4_gemm", "ufp4_stats", "ufp4_check",
+              "ufp4_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    from fp4_quantized_numerics_gb300 import ufp4
+    for n in _declared():
+        assert hasattr(L, n), n
+    assert set(_declared()) == set(ufp4.EXPORTED)
+
+
+def test_size_helpers(L):
+    for k in [16, 48, 64, 1024, 1040]:
+        assert L.ufp4_kpad(k) == kpad(k)
+        for r in [1, 127, 128, 300]:
+            assert L.ufp4_codes_bytes(r, k) == r * kpad(k) // 2
+            assert L.ufp4_scales_bytes(r, k) == rpad(r) * kpad(k) // 16
+    assert L.ufp4_codes_bytes(0, 16) == 0
+    assert L.ufp4_workspace_bytes() >= 16 * 1024
+
+
+def test_status_strings(L):
+    from fp4_quantized_numerics_gb300 import ufp4
+    for s in range(6):
+        assert len(ufp4.ufp4_status_string(s)) > 0
+    assert ufp4.ufp4_status_string(99) == "unknown status"
+
+
+def _q(**kw):
+    from fp4_quantized_numerics_gb300 import ufp4
+    base = dict(grid=0, rht=False, rht_seed=0, round=0, sr_seed=0, sr_counter=0, colwise=False)
+    base.update(kw)
+    return ufp4.qparams(**base)
+
+
+def _qt(rows, k, grid=0, ptr=0x1000):
+    from fp4_quantized_numerics_gb300 import ufp4
+    return ufp4.QTensorC(ptr, ptr, ptr, rows, k, grid, 0)
+
+
+def test_quantize_rejects_bad_arguments_on_host(L):
+    from fp4_quantized_numerics_gb300 import ufp4
+    ws, x = 0x10000, 0x20000
+    wsb = L.ufp4_workspace_bytes()
+    INV = ufp4.UFP4_ERR_INVALID
+
+    def call(p, out, rows=32, cols=64, ld=64, dtype=0, xp=x, w=ws, wb=wsb):
+        return L.ufp4_quantize(xp, dtype, rows, cols, ld, ctypes.byref(p) if p is not None else None,
+                               ctypes.byref(out) if out is not None else None, w, wb, None)
+
+    assert call(None, _qt(32, 64)) == INV                              # no params
+    assert call(_q(), None) == INV                                     # no output
+    assert call(_q(grid=7), _qt(32, 64, 7)) == INV                     # bad grid
+    assert call(_q(round=3), _qt(32, 64)) == INV                       # bad rounding
+    assert call(_q(), _qt(32, 64), dtype=5) == INV                     # bad dtype
+    assert call(_q(), _qt(32, 48)) == INV                              # shape mismatch
+    assert call(_q(), _qt(32, 64, grid=1)) == INV                      # grid mismatch
+    assert call(_q(), _qt(32, 40), cols=40, ld=40) == INV              # k % 16
+    assert call(_q(), _qt(32, 64), ld=32) == INV                       # ld < cols
+    assert call(_q(), _qt(32, 64), xp=x + 2) == INV                    # misaligned x
+    assert call(_q(), _qt(32, 64), ld=68) == INV                       # row stride not 16 B
+    assert call(_q(), _qt(32, 64), w=0) == INV                         # no workspace
+    assert call(_q(), _qt(32, 64), wb=16) == INV                       # workspace too small
+    assert call(_q(), _qt(32, 64, ptr=0x1001)) == INV                  # misaligned codes
+    assert call(_q(colwise=True), _qt(64, 30), rows=30) == INV         # colwise rows % 16
+    assert call(_q(colwise=True), _qt(62, 32), rows=32, cols=62, ld=64) == INV  # colwise cols % 4
+    p = _q()
+    p.block = 32
+    assert call(p, _qt(32, 64)) == ufp4.UFP4_ERR_UNSUPPORTED
+    p = _q()
+    p.reserved = 1
+    assert call(p, _qt(32, 64)) == INV
+
+
+def test_zero_sized_quantize_is_a_noop(L):
+    from fp4_quantized_numerics_gb300 import ufp4
+    p = _q()
+    out = ufp4.QTensorC(0, 0, 0, 0, 64, 0, 0)
+    assert L.ufp4_quantize(None, 0, 0, 64, 64, ctypes.byref(p), ctypes.byref(out), 0x10000,
+                           L.ufp4_workspace_bytes(), None) == ufp4.UFP4_OK
+
+
+def test_gemm_and_dequant_reject_bad_arguments_on_host(L):
+    from fp4_quantized_numerics_gb300 import ufp4
+    INV = ufp4.UFP4_ERR_INVALID
+    a, b = _qt(128, 256), _qt(64, 128)
+    assert L.ufp4_gemm(ctypes.byref(a), ctypes.byref(b), 0x4000, 64, None) == INV   # K mismatch
+    b = _qt(64, 256, grid=1)
+    assert L.ufp4_gemm(ctypes.byref(a), ctypes.byref(b), 0x4000, 64, None) == ufp4.UFP4_ERR_UNSUPPORTED
+    b = _qt(64, 256)
+    assert L.ufp4_gemm(ctypes.byref(a), ctypes.byref(b), 0x4000, 32, None) == INV   # ldc < N
+    assert L.ufp4_gemm(ctypes.byref(a), ctypes.byref(b), 0x4004, 64, None) == INV   # c alignment
+    assert L.ufp4_gemm(ctypes.byref(a), ctypes.byref(b), 0, 64, None) == INV        # no C
+    q = _qt(16, 32)
+    assert L.ufp4_dequantize(ctypes.byref(q), 2, 0, 0x4000, 32, None) == INV
+    assert L.ufp4_dequantize(ctypes.byref(q), 0, 0, 0x4000, 30, None) == INV
+    z = _qt(0, 32)
+    assert L.ufp4_dequantize(ctypes.byref(z), 0, 0, 0, 0, None) == ufp4.UFP4_OK
+
+
+def test_stats_rejects_bad_arguments_on_host(L):
+    from fp4_quantized_numerics_gb300 import ufp4
+    p = _q()
+    q = _qt(32, 64)
+    out = ufp4.StatsC()
+    assert L.ufp4_stats(0x20000, 0, 32, 64, 64, ctypes.byref(p), ctypes.byref(q), 0x10000,
+                        L.ufp4_workspace_bytes(), None, None) == ufp4.UFP4_ERR_INVALID
+    assert L.ufp4_stats(0x20000, 0, 32, 64, 64, ctypes.byref(p), ctypes.byref(q), 0, 0,
+                        ctypes.byref(out), None) == ufp4.UFP4_ERR_INVALID
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    from fp4_quantized_numerics_gb300 import ufp4
+    with pytest.raises(TypeError):
+        ufp4.ufp4_quantize(torch.zeros(16, 16, dtype=torch.bfloat16), 0)
