@@ -1,0 +1,473 @@
+"""Benchmark of the UFP4 hot path on GB300.
+
+One step = one UFP4 training step of the dense-1.5B-shaped linear layer
+(X 8192 x 2048, W 5632 x 2048, dY 8192 x 5632, BF16, seeded synthetic data):
+six fused RHT + E1M2 quantizations (X, W, dY, each row-wise and
+column-wise; stochastic rounding on dY only) followed by the three training
+GEMMs fwd_y = X W^T, bwd_dx = dY W and bwd_dw = dY^T X.
+
+Reported (one JSON line from rank 0):
+  value         fused RHT+quantize throughput, GB/s of algorithmic traffic
+                (2 B read + 0.5625 B written per element) over the
+                quantization launches of the step (tensor-amax pass included
+                in the time, not in the bytes);
+  gemm          GEMM TFLOP/s (2 M N K logical flops) and fractions of the
+                FP8 / FP4 dense peaks;
+  roofline      for the dominant kernel by time (the E1M2 GEMM);
+  e2e           the same metric through the public API with the inputs
+                copied from pinned host memory each step and the three GEMM
+                outputs read back;
+  cpu_baseline  the CPU oracle on a bounded sample of the same step.
+L2 is flushed (a 256 MiB write) before every timed step, outside the events.
+
+--impl reference runs the CPU oracle (the reference arm of this tier) on a
+bounded sample of the same workload and prints the same line shape.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = dict(name="dense1p5b_linear_train_step", tokens=8192, hidden=2048, ffn=5632)
+METRIC = ("fused RHT+quantize GB/s (% HBM peak); FP4 GEMM TFLOPS (% tensor peak)")
+Q_BYTES_PER_ELEM = 2.0 + 0.5 + 1.0 / 16.0
+FALLBACK = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        def pick(*keys):
+            for k in keys:
+                if k in d and isinstance(d[k], (int, float)):
+                    return float(d[k])
+            return None
+        hbm = pick("hbm_gbs", "hbm_GBps", "copy_gbs")
+        bf = pick("bf16_tflops", "bf16_tflops_burst")
+        bfs = pick("bf16_tflops_sustained")
+        if hbm and bf:
+            return dict(hbm_gbs=hbm, bf16_tflops=bf, bf16_tflops_sustained=bfs or bf,
+                        source="measured")
+    return dict(FALLBACK, source="fallback")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [t.strip() for t in l.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- the step
+class Step:
+    """Buffers and launches of one UFP4 training step (E1M2 + RHT on all
+    GEMM operands, SR on dY), all through the libufp4 binding."""
+
+    def __init__(self, U, x, w, dy, grid):
+        import torch
+        self.U, self.torch = U, torch
+        self.x, self.w, self.dy = x, w, dy
+        self.grid = grid
+        T, H = x.shape
+        F = w.shape[0]
+        dev = x.device
+        Q = U.QTensor.empty
+        self.qx_r, self.qw_r, self.qdy_r = Q(T, H, grid, dev), Q(F, H, grid, dev), Q(T, F, grid, dev)
+        self.qw_c, self.qdy_c, self.qx_c = Q(H, F, grid, dev), Q(F, T, grid, dev), Q(H, T, grid, dev)
+        self.y = torch.empty(T, F, dtype=torch.float32, device=dev)
+        self.dx = torch.empty(T, H, dtype=torch.float32, device=dev)
+        self.dw = torch.empty(F, H, dtype=torch.float32, device=dev)
+        self.ws = U.workspace(dev)
+        self.counter = 0
+        self.q_elems = 2 * (x.numel() + w.numel() + dy.numel())
+        self.flops_each = [2 * T * F * H, 2 * T * H * F, 2 * F * H * T]
+
+    def quantize_all(self):
+        U, g = self.U, self.grid
+        kw = dict(rht=True, rht_seed=2, ws=self.ws)
+        sr = dict(round=U.UFP4_SR, sr_seed=3, sr_counter=self.counter)
+        U.ufp4_quantize(self.x, g, out=self.qx_r, **kw)
+        U.ufp4_quantize(self.w, g, out=self.qw_r, **kw)
+        U.ufp4_quantize(self.dy, g, out=self.qdy_r, **kw, **sr)
+        U.ufp4_quantize(self.w, g, colwise=True, out=self.qw_c, **kw)
+        U.ufp4_quantize(self.dy, g, colwise=True, out=self.qdy_c, **kw, **sr)
+        U.ufp4_quantize(self.x, g, colwise=True, out=self.qx_c, **kw)
+        self.counter += 1
+
+    def gemms(self, events=None):
+        U = self.U
+        pairs = [(self.qx_r, self.qw_r, self.y), (self.qdy_r, self.qw_c, self.dx),
+                 (self.qdy_c, self.qx_c, self.dw)]
+        for i, (a, b, c) in enumerate(pairs):
+            U.ufp4_gemm(a, b, out=c)
+            if events is not None:
+                events[i + 1].record()
+
+    launches_per_step = 6 * 2 + 3
+
+
+def run_gpu(args):
+    import torch
+    from fp4_quantized_numerics_gb300 import build, inputs, ufp4 as U
+
+    ws_n, rank, local = dist_env()
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    build.build()
+    U.lib()
+    dev = torch.device("cuda", local)
+    pk = peaks()
+
+    d = inputs.device_dense(seed=rank, tokens=WORKLOAD["tokens"], hidden=WORKLOAD["hidden"],
+                            ffn=WORKLOAD["ffn"], device=dev)
+    step = Step(U, d["x"], d["w"], d["dy"], U.UFP4_E1M2)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        step.quantize_all()
+        step.gemms()
+    torch.cuda.synchronize()
+
+    # per-step events: [start, after quantize, after gemm0, gemm1, gemm2]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if ws_n > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            e = evs[i]
+            e[0].record()
+            step.quantize_all()
+            e[1].record()
+            step.gemms(events=[None, e[2], e[3], e[4]])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if ws_n > 1:
+        torch.distributed.barrier()
+    q_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    g_ms = [[e[1 + j].elapsed_time(e[2 + j]) for j in range(3)] for e in evs]
+    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
+    tq, tg, tstep = sum(q_ms), sum(sum(g) for g in g_ms), sum(step_ms)
+
+    def allmax(v):
+        if ws_n == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    tq, tg, tstep = allmax(tq), allmax(tg), allmax(tstep)
+    q_bytes = step.q_elems * Q_BYTES_PER_ELEM
+    q_gbs = ws_n * args.steps * q_bytes / (tq * 1e-3) / 1e9
+    flops = sum(step.flops_each)
+    gemm_tflops = ws_n * args.steps * flops / (tg * 1e-3) / 1e12
+    per_gpu_tflops = gemm_tflops / ws_n
+    fp8_peak = pk["bf16_tflops"] * 2.0    # nominal dense ratio fp8:bf16 = 4.5 : 2.25
+    fp4_peak = pk["bf16_tflops"] * 6.0    # nominal dense ratio fp4:bf16 = 13.5 : 2.25
+    gemm_each = [sum(g[j] for g in g_ms) / args.steps for j in range(3)]
+
+    # ---------------------------------------------------- e2e through the API
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, U, step, d, dev, q_bytes)
+        e2e["value"] = allmax(e2e["time_s"])
+        e2e["value"] = ws_n * e2e["steps"] * q_bytes / e2e["value"] / 1e9
+        del e2e["time_s"]
+
+    extra = {}
+    if not args.quick:
+        extra = side_measurements(U, torch, dev, pk, flush)
+
+    if rank == 0:
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": round(q_gbs, 2), "unit": "GB/s",
+            "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tstep / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp32 quantize / e2m1-plane MMA, f32 accumulate",
+            "data": "synthetic (seeded N(0,1)/N(0,0.02)/N(0,1e-3) BF16; 1 outlier column x50)",
+            "config": {"workload": WORKLOAD["name"], "X": [WORKLOAD["tokens"], WORKLOAD["hidden"]],
+                       "W": [WORKLOAD["ffn"], WORKLOAD["hidden"]],
+                       "dY": [WORKLOAD["tokens"], WORKLOAD["ffn"]],
+                       "recipe": "UFP4: E1M2, RHT16 on all GEMM operands, SR on dY",
+                       "l2": "flushed (256 MiB write) before every timed step",
+                       "parallelism": "replicas" if ws_n > 1 else "single"},
+            "quantize": {"gbs": round(q_gbs, 1), "frac_hbm": round(q_gbs / ws_n / pk["hbm_gbs"], 4),
+                         "ms_per_step": round(tq / args.steps, 4),
+                         "elements_per_step": step.q_elems, "launches_per_step": 12},
+            "gemm": {"tflops": round(gemm_tflops, 1), "ms_per_step": round(tg / args.steps, 4),
+                     "ms_each": [round(v, 4) for v in gemm_each],
+                     "frac_fp8_peak": round(per_gpu_tflops / fp8_peak, 4),
+                     "frac_fp4_peak": round(per_gpu_tflops / fp4_peak, 4)},
+            "roofline": {"bound": "tensor", "kernel": "k_gemm<E1M2>",
+                         "achieved": round(per_gpu_tflops, 1), "peak": round(fp8_peak, 1),
+                         "unit": "TFLOP/s", "frac": round(per_gpu_tflops / fp8_peak, 4),
+                         "traffic": traffic_for("k_gemm_e1m2_dense1p5b"),
+                         "peak_kind": "dense FP8 = %s bf16 x 2 (%s)" % ("measured" if pk["source"] == "measured" else "fallback", pk["source"])},
+            "gpu_launches": Step.launches_per_step * args.steps,
+            "clocks": clocks,
+            "peaks": pk,
+        }
+        if e2e is not None:
+            line["e2e"] = e2e
+        line.update(extra)
+        if not args.no_cpu_baseline and ws_n >= 1:
+            line["cpu_baseline"] = cpu_baseline(args)
+        print(json.dumps(line), flush=True)
+    if ws_n > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(args, U, step, d, dev, q_bytes):
+    """The public API end to end: pinned host inputs -> device, full step,
+    results back to pinned host memory, all inside the timed region."""
+    import torch
+    hx = d["x"].cpu().pin_memory()
+    hw = d["w"].cpu().pin_memory()
+    hdy = d["dy"].cpu().pin_memory()
+    outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (step.y, step.dx, step.dw)]
+    n = max(3, min(args.steps, 20))
+    for i in range(2 + n):
+        if i == 2:
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+        step.x.copy_(hx, non_blocking=True)
+        step.w.copy_(hw, non_blocking=True)
+        step.dy.copy_(hdy, non_blocking=True)
+        step.quantize_all()
+        step.gemms()
+        for h, t in zip(outs, (step.y, step.dx, step.dw)):
+            h.copy_(t, non_blocking=True)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hw, hdy))
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    return {"time_s": dt, "steps": n, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(dt / n * 1e3, 3)}
+
+
+def side_measurements(U, torch, dev, pk, flush):
+    """Secondary numbers: RHT on/off overhead of the E1M2 quantizer, the
+    outlier-heavy 4096 x 4096 quantization, and the E2M1 GEMM."""
+    from fp4_quantized_numerics_gb300 import inputs
+
+    def timeit(fn, n=30):
+        fn(); fn(); fn()
+        torch.cuda.synchronize()
+        tot = 0.0
+        for _ in range(n):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(); fn(); b.record()
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b)
+        return tot / n
+
+    out = {}
+    x = inputs.device_normal((8192, 2048), 1.0, 11, dev)
+    q = U.QTensor.empty(8192, 2048, U.UFP4_E1M2, dev)
+    amax = torch.ones(1, device=dev)
+    ws = U.workspace(dev)
+    el = x.numel()
+    r = {}
+    for rht in (False, True):
+        for name, am in (("with_amax_pass", None), ("amax_given", amax)):
+            ms = timeit(lambda: U.ufp4_quantize(x, U.UFP4_E1M2, rht=rht, out=q, ws=ws, amax_in=am))
+            r["rht_%s_%s" % ("on" if rht else "off", name)] = round(el * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
+    r["rht_overhead_amax_given"] = round(r["rht_off_amax_given"] / r["rht_on_amax_given"] - 1, 4)
+    r["frac_hbm_rht_on_amax_given"] = round(r["rht_on_amax_given"] / pk["hbm_gbs"], 4)
+    out["quantize_x_8192x2048_gbs"] = r
+
+    xo = inputs.device_normal((4096, 4096), 1.0, 12, dev)
+    qo = U.QTensor.empty(4096, 4096, U.UFP4_E2M1, dev)
+    qo1 = U.QTensor.empty(4096, 4096, U.UFP4_E1M2, dev)
+    o = {}
+    for g, qq in ((U.UFP4_E2M1, qo), (U.UFP4_E1M2, qo1)):
+        ms = timeit(lambda: U.ufp4_quantize(xo, g, rht=True, out=qq, ws=ws))
+        o["e2m1" if g == 0 else "e1m2"] = round(xo.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
+    out["quantize_outlier_4096x4096_rht_gbs"] = o
+
+    # E2M1 GEMM at the fwd_y shape
+    a = U.ufp4_quantize(inputs.device_normal((8192, 2048), 1.0, 13, dev), U.UFP4_E2M1)
+    b = U.ufp4_quantize(inputs.device_normal((5632, 2048), 0.02, 14, dev), U.UFP4_E2M1)
+    c = torch.empty(8192, 5632, dtype=torch.float32, device=dev)
+    ms = timeit(lambda: U.ufp4_gemm(a, b, out=c))
+    tf = 2 * 8192 * 5632 * 2048 / (ms * 1e-3) / 1e12
+    out["gemm_e2m1_fwd_y"] = {"tflops": round(tf, 1), "frac_fp4_peak": round(tf / (pk["bf16_tflops"] * 6), 4),
+                              "output_bytes_bound_tflops": round(2 * 2048 / 4 * pk["hbm_gbs"] / 1e3, 1)}
+    return out
+
+
+def traffic_for(key):
+    """dram bytes per launch from a committed ncu summary, if its kernel
+    source hash still matches the current source (else null)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(key)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "fp4_quantized_numerics_gb300", "csrc", ent.get("source", ""))
+    if not os.path.exists(src):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return ent.get("bytes_per_launch") if h == ent.get("sha256_16") else None
+
+
+# ------------------------------------------------------------ CPU oracle
+def cpu_sample(rows_x=2048, rows_dy=2048, gemm_rows=32):
+    """The oracle on a bounded sample of the step: RHT + E1M2 row-wise
+    quantization of the first rows of X and of dY (SR), and gemm_rows rows of
+    fwd_y in fp64.  Returns (quantize GB/s, GEMM GFLOP/s, seconds, desc)."""
+    from fp4_quantized_numerics_gb300 import inputs
+    from oracle import oracle
+    g = np.random.default_rng(0)
+    x = inputs.to_bf16_f32(g.standard_normal((rows_x, WORKLOAD["hidden"]), dtype=np.float32))
+    dy = inputs.to_bf16_f32(g.standard_normal((rows_dy, WORKLOAD["ffn"]), dtype=np.float32) * np.float32(1e-3))
+    w = inputs.to_bf16_f32(g.standard_normal((WORKLOAD["ffn"], WORKLOAD["hidden"]), dtype=np.float32) * np.float32(0.02))
+    t0 = time.perf_counter()
+    rx = oracle.quantize(x, oracle.E1M2, rht=True, rht_seed=2)
+    oracle.quantize(dy, oracle.E1M2, rht=True, rht_seed=2, round_mode=oracle.SR, sr_seed=3)
+    tq = time.perf_counter() - t0
+    rw = oracle.quantize(w, oracle.E1M2, rht=True, rht_seed=2)
+    A = oracle.dequantize(rx["codes"][:gemm_rows], rx["scales"][:gemm_rows], rx["tensor_scale"], oracle.E1M2)
+    B = oracle.dequantize(rw["codes"], rw["scales"], rw["tensor_scale"], oracle.E1M2)
+    t1 = time.perf_counter()
+    oracle.gemm_f64(A, B)
+    tg = time.perf_counter() - t1
+    el = x.size + dy.size
+    flops = 2.0 * gemm_rows * w.shape[0] * w.shape[1]
+    desc = ("RHT+E1M2 row-wise quantization of %d x %d of X and %d x %d of dY (SR), "
+            "plus %d rows of fwd_y in fp64" % (rows_x, WORKLOAD["hidden"], rows_dy, WORKLOAD["ffn"], gemm_rows))
+    return el * Q_BYTES_PER_ELEM / tq / 1e9, flops / tg / 1e9, tq + tg, desc
+
+
+def cpu_baseline(args):
+    gbs, gflops, secs, desc = cpu_sample()
+    return {"value": round(gbs, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": desc, "gemm_gflops": round(gflops, 3), "seconds": round(secs, 2),
+            "host": host_desc()}
+
+
+def host_desc():
+    try:
+        import platform
+        return "%s, %d logical cores" % (platform.machine(), os.cpu_count() or 0)
+    except Exception:
+        return None
+
+
+def run_reference(args):
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return
+    t_all = 0.0
+    vals = []
+    for i in range(args.warmup + args.steps):
+        gbs, gflops, secs, desc = cpu_sample(rows_x=256, rows_dy=256, gemm_rows=4)
+        if i >= args.warmup:
+            t_all += secs
+            vals.append(gbs)
+    value = statistics.mean(vals) if vals else 0.0
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s",
+            "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t_all / max(args.steps, 1) * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32 (CPU oracle)",
+            "data": "synthetic", "config": {"workload": WORKLOAD["name"]},
+            "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true", help="skip the secondary measurements")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -216,8 +216,9 @@ def ufp4_gemm(a, b, out=None, stream=None):
     """C = A B^T (fp32), A: M x K and B: N x K quantized along K."""
     _cuda(a.codes, "a.codes")
     _cuda(b.codes, "b.codes")
-    if out is None:
-        out = torch.empty(a.rows, b.rows, dtype=torch.float32, device=a.codes.device)
+    if out is None:   # row stride rounded up to 4 floats (16 bytes), as the ABI requires
+        ld = (b.rows + 3) // 4 * 4
+        out = torch.empty(a.rows, ld, dtype=torch.float32, device=a.codes.device)[:, : b.rows]
     ac, bc = a.c(), b.c()
     st = lib().ufp4_gemm(ctypes.byref(ac), ctypes.byref(bc), out.data_ptr(), out.stride(0),
                          _stream(stream))

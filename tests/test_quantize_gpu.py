@@ -29,6 +29,12 @@ def U():
 def _gpu_quant(U, x, grid, rht, rnd, colwise, dtype=torch.bfloat16, sr_seed=1, sr_counter=0,
                amax_in=None):
     xt = torch.from_numpy(np.ascontiguousarray(x)).to(dtype).cuda()
+    esz = 2 if dtype == torch.bfloat16 else 4
+    if (xt.shape[1] * esz) % 16:   # the ABI wants 16-byte row strides: pad ld
+        ld = (xt.shape[1] * esz + 15) // 16 * 16 // esz
+        wide = torch.zeros(xt.shape[0], ld, dtype=dtype, device="cuda")
+        wide[:, : xt.shape[1]] = xt
+        xt = wide[:, : xt.shape[1]]
     am = None if amax_in is None else torch.tensor([amax_in], dtype=torch.float32, device="cuda")
     q = U.ufp4_quantize(xt, grid, rht=rht, rht_seed=2, round=rnd, sr_seed=sr_seed,
                         sr_counter=sr_counter, colwise=colwise, amax_in=am)
