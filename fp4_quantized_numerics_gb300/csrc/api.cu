@@ -8,7 +8,9 @@
 #include "common.cuh"
 #include "internal.h"
 
+#include <algorithm>
 #include <cmath>
+#include <mutex>
 #include <vector>
 
 using namespace ufp4;
@@ -181,3 +183,60 @@ ufp4_status ufp4_stats(const void *x, int32_t dtype, int64_t rows, int64_t cols,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// ufp4_quantize_noalloc: ufp4_quantize for callers that cannot allocate
+// device memory.  Some host programs may not call cudaMalloc at the point
+// where they quantize -- a custom allocator owns all device memory, a memory
+// pool is frozen after start-up, or the code runs where an allocation could
+// synchronise the device.  This variant needs no caller workspace: its
+// scratch (the amax pass's per-CTA partial maxima and the status word) lives
+// in the file-scope array below, which every GPU that loads libufp4 holds
+// until the process exits.
+//
+// Layout of the array: the same as the first kNoAllocBytes of a regular
+// workspace -- status word at 0, up to kMaxPartials float partial maxima at
+// kWsPartials.  Nothing in it has to start at zero: the amax pass writes every
+// slot that the quantization pass reads, and the quantization pass writes
+// the status word.  The array keeps the last call's contents, and all calls
+// on a device share it, so calls whose work overlaps on the GPU (different
+// streams, or different host threads without ordering) race on it.
+namespace {
+constexpr size_t kNoAllocBytes = kWsPartials + size_t(kMaxPartials) * sizeof(float);  // 16,640 B
+static __device__ __align__(256) unsigned char g_ufp4_noalloc_scratch[kNoAllocBytes];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[64] = {nullptr};
+
+// Device address of the scratch array for the current device, looked up once
+// per device (host code only holds a stand-in for the array's name).
+ufp4_status noalloc_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return UFP4_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_ufp4_noalloc_scratch) != cudaSuccess || !p) return UFP4_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return UFP4_OK;
+}
+}  // namespace
+
+extern "C" ufp4_status ufp4_quantize_noalloc(const void *x, int32_t dtype, int64_t rows, int64_t cols,
+                                             int64_t ld, const ufp4_qparams *p,
+                                             const ufp4_qtensor *out, ufp4_stream_t stream) {
+    QuantLaunch q;
+    ufp4_status st = check_quant_args(x, dtype, rows, cols, ld, p, out, &q);
+    if (st != UFP4_OK) return st;
+    if (rows == 0 || cols == 0) return UFP4_OK;
+    // The amax pass never launches more than min(8 x SMs, kMaxPartials) CTAs;
+    // refuse a call whose partial maxima would not fit the array.
+    const int64_t slots = std::min<int64_t>((int64_t)num_sms() * 8, kMaxPartials);
+    if (kWsPartials + (size_t)slots * sizeof(float) > kNoAllocBytes) return UFP4_ERR_INVALID;
+    void *scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != UFP4_OK) return st;
+    return from_cuda(launch_quantize(q, scratch, reinterpret_cast<cudaStream_t>(stream)));
+}

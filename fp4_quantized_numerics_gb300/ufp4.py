@@ -28,7 +28,7 @@ UFP4_OK, UFP4_ERR_INVALID, UFP4_ERR_UNSUPPORTED, UFP4_ERR_NONFINITE, UFP4_ERR_CU
 
 EXPORTED = ["ufp4_kpad", "ufp4_codes_bytes", "ufp4_scales_bytes", "ufp4_workspace_bytes",
             "ufp4_quantize", "ufp4_check", "ufp4_dequantize", "ufp4_gemm", "ufp4_stats",
-            "ufp4_status_string"]
+            "ufp4_status_string", "ufp4_quantize_noalloc"]
 
 
 class QParamsC(ctypes.Structure):

@@ -161,6 +161,27 @@ UFP4_API ufp4_status ufp4_quantize(const void *x, int32_t dtype, int64_t rows, i
                           const ufp4_qparams *p, const ufp4_qtensor *out,
                           void *workspace, size_t workspace_bytes, ufp4_stream_t stream);
 
+/* ufp4_quantize without a caller workspace, for callers that cannot
+ * allocate device memory when they quantize (a frozen memory pool, a custom
+ * allocator that owns all device memory, code that must not risk an
+ * allocation's implicit synchronisation).  The paper has no counterpart:
+ * this is a deployment convenience of this library.
+ * Arguments and results are exactly those of ufp4_quantize, minus the
+ * workspace.  Its scratch -- the amax pass's partial maxima and a status
+ * word, 16,640 bytes -- is a fixed array inside the library that every GPU
+ * using libufp4 holds until the process exits; it fits every tensor that
+ * ufp4_quantize accepts (the amax pass launches at most 4096 CTAs), and a
+ * call that would need more is refused with UFP4_ERR_INVALID.  The first call
+ * on each device looks up the array's device address, so make that first call
+ * before capturing any stream into a CUDA graph.  All calls on a device share
+ * the array and it keeps the last call's contents: calls that overlap on the
+ * GPU (other streams, unordered host threads) race and give wrong results.
+ * Allocates nothing.  The non-finite status of this variant is not
+ * reported (use ufp4_quantize with a workspace and ufp4_check for that). */
+UFP4_API ufp4_status ufp4_quantize_noalloc(const void *x, int32_t dtype, int64_t rows, int64_t cols,
+                                           int64_t ld, const ufp4_qparams *p, const ufp4_qtensor *out,
+                                           ufp4_stream_t stream);
+
 /* Reports device-side problems (synchronises `stream`):
  *   UFP4_ERR_TIMEOUT   -- a bounded wait inside a GEMM kernel gave up since
  *                         the last check (the flag is then cleared); that
