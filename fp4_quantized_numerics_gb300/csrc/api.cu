@@ -114,9 +114,10 @@ ufp4_status ufp4_quantize(const void *x, int32_t dtype, int64_t rows, int64_t co
 ufp4_status ufp4_check(const void *workspace, ufp4_stream_t stream) {
     if (workspace && !aligned(workspace, 16)) return UFP4_ERR_INVALID;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    uint32_t timeout = 0;
+    uint32_t timeout = 0, qtimeout = 0;
     if (read_timeout_flag(&timeout, s) != cudaSuccess) return UFP4_ERR_CUDA;
-    if (timeout) return UFP4_ERR_TIMEOUT;
+    if (read_quant_timeout_flag(&qtimeout, s) != cudaSuccess) return UFP4_ERR_CUDA;
+    if (timeout || qtimeout) return UFP4_ERR_TIMEOUT;
     if (!workspace) return UFP4_OK;
     uint32_t flag = 0;
     cudaError_t e = cudaMemcpyAsync(&flag, static_cast<const char *>(workspace) + kWsStatus,

@@ -46,15 +46,15 @@ constexpr int BM = 128, BN = 128;
 constexpr int BK_BYTES = 128;                 // 256 FP4 elements per stage
 constexpr uint32_t TILE_BYTES = 128 * 128;    // 16 KB per operand tile
 constexpr uint32_t SF_BYTES = 4 * 512;        // 4 scale atoms per operand per stage
-constexpr int kGemmThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCol = 0;               // accumulator: columns [0, 128)
-constexpr uint32_t kSfCol = 128;              // scales: 32 columns per stage
-constexpr long long kWaitBudget = 4000000000LL;
+constexpr uint32_t kSfCol = 256;              // accumulators in [0, 256), scales after
+constexpr long long kWaitBudget = 2000000000LL;
 
 template <int GRID>
 struct Cfg {
-    static constexpr int kStages = GRID == kE2M1 ? 5 : 3;
+    static constexpr int kStages = GRID == kE2M1 ? 6 : 3;
+    // warps: 0 producer, 1 MMA, 2-5 epilogue, (E1M2) 6-9 expanders
+    static constexpr int kThreads = GRID == kE2M1 ? 192 : 320;
     // stage layout: A | B | (A_lo | B_lo for E1M2) | SFA | SFB
     static constexpr uint32_t kAOff = 0;
     static constexpr uint32_t kBOff = TILE_BYTES;
@@ -74,10 +74,28 @@ struct GemmParams {
     int64_t ldc;
     int M, N;
     int nkt;      // kpad / 64: scale atoms per 128-row tile
-    int num_kb;   // ceil(nkt / 4): pipeline stages of K
+    int num_kb;   // ceil(nkt / 4): K stages per tile
+    int ntm, ntn; // tiles along M and N
 };
 
 __device__ __forceinline__ void raise_timeout() { atomicOr(&g_ufp4_timeout, 1u); }
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitBudget) {
+            *abort = 1;
+            raise_timeout();
+            return false;
+        }
+    }
+}
 
 // E1M2 nibbles -> (hi, lo) E2M1 nibbles, 8 at a time (see file header).
 __device__ __forceinline__ void split_e1m2(uint32_t w, uint32_t &hi, uint32_t &lo) {
@@ -89,8 +107,12 @@ __device__ __forceinline__ void split_e1m2(uint32_t w, uint32_t &hi, uint32_t &l
     lo = s | m0;
 }
 
+// Persistent CTA: tiles t = blockIdx.x, blockIdx.x + gridDim.x, ... in
+// row-major (M, N) tile order.  The K ring and the two TMEM accumulators are
+// carried across tiles, so the epilogue of one tile overlaps the main loop
+// of the next.
 template <int GRID>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
            GemmParams p) {
     using C = Cfg<GRID>;
@@ -98,18 +120,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
-    // bars[0..S): full (TMA landed), [S..2S): empty (MMA done with stage),
-    // [2S..3S): expanded (E1M2 planes ready), [3S]: accumulator ready
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * S + 1);
+    // bars: [0,S) full, [S,2S) empty, [2S,3S) expanded, 3S+{0,1} acc full,
+    // 3S+{2,3} acc empty, 3S+4 MMA drained
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * S + 5);
+    volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const uint32_t smem_base = ptx::smem_u32(smem);
     const uint32_t bar_base = ptx::smem_u32(bars);
     auto full = [&](int s) { return bar_base + 8u * s; };
     auto empty = [&](int s) { return bar_base + 8u * (S + s); };
     auto expd = [&](int s) { return bar_base + 8u * (2 * S + s); };
-    const uint32_t acc_bar = bar_base + 8u * (3 * S);
+    auto accf = [&](int b) { return bar_base + 8u * (3 * S + b); };
+    auto acce = [&](int b) { return bar_base + 8u * (3 * S + 2 + b); };
+    const uint32_t drained = bar_base + 8u * (3 * S + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+    const int ntiles = p.ntm * p.ntn;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -117,7 +142,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ptx::mbar_init(empty(s), 1);
             ptx::mbar_init(expd(s), 4);   // one arrival per expander warp
         }
-        ptx::mbar_init(acc_bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(accf(b), 1);
+            ptx::mbar_init(acce(b), 4);   // one arrival per epilogue warp
+        }
+        ptx::mbar_init(drained, 1);
+        *abort = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tma_a);
         ptx::prefetch_tmap(&tma_b);
@@ -132,107 +162,145 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------------ producer
+        // ---------------------------------------------------------- producer
         if (lane == 0) {
-            int issued = 0;
-            for (int kb = 0; kb < p.num_kb; ++kb) {
-                const int s = kb % S, round = kb / S;
-                if (round > 0 && !ptx::mbar_wait_bounded(empty(s), (round - 1) & 1, kWaitBudget)) {
-                    raise_timeout();
-                    break;
+            uint32_t g = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const int m0 = (t / p.ntn) * BM, n0 = (t % p.ntn) * BN;
+                for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
+                    const uint32_t s = g % S, round = g / S;
+                    if (round > 0 && !wait_or_abort(empty(s), (round - 1) & 1, abort)) { ok = false; break; }
+                    const int atoms = min(4, p.nkt - 4 * kb);
+                    const uint32_t st = smem_base + s * C::kStageBytes;
+                    ptx::mbar_arrive_expect_tx(full(s), 2 * TILE_BYTES + 2u * atoms * 512u);
+                    ptx::tma_load_2d(st + C::kAOff, &tma_a, kb * BK_BYTES, m0, full(s));
+                    ptx::tma_load_2d(st + C::kBOff, &tma_b, kb * BK_BYTES, n0, full(s));
+                    ptx::bulk_load(st + C::kSfaOff, p.sfa + ((size_t)(m0 / 128) * p.nkt + 4 * kb) * 512,
+                                   atoms * 512u, full(s));
+                    ptx::bulk_load(st + C::kSfbOff, p.sfb + ((size_t)(n0 / 128) * p.nkt + 4 * kb) * 512,
+                                   atoms * 512u, full(s));
                 }
-                const int atoms = min(4, p.nkt - 4 * kb);
-                const uint32_t st = smem_base + s * C::kStageBytes;
-                ptx::mbar_arrive_expect_tx(full(s), 2 * TILE_BYTES + 2u * atoms * 512u);
-                ptx::tma_load_2d(st + C::kAOff, &tma_a, kb * BK_BYTES, m0, full(s));
-                ptx::tma_load_2d(st + C::kBOff, &tma_b, kb * BK_BYTES, n0, full(s));
-                ptx::bulk_load(st + C::kSfaOff, p.sfa + ((size_t)(m0 / 128) * p.nkt + 4 * kb) * 512,
-                               atoms * 512u, full(s));
-                ptx::bulk_load(st + C::kSfbOff, p.sfb + ((size_t)(n0 / 128) * p.nkt + 4 * kb) * 512,
-                               atoms * 512u, full(s));
-                issued = kb + 1;
             }
-            // Drain: every copy this thread issued has landed before exit.
-            for (int kb = max(0, issued - S); kb < issued; ++kb) {
-                if (!ptx::mbar_wait_bounded(full(kb % S), (kb / S) & 1, kWaitBudget)) {
-                    raise_timeout();
-                    break;
-                }
+            // every copy this thread started has landed before the CTA exits
+            for (uint32_t h = g > (uint32_t)S ? g - S : 0; h < g; ++h) {
+                const long long t0 = clock64();
+                while (!ptx::mbar_try_wait(full(h % S), (h / S) & 1))
+                    if (clock64() - t0 > kWaitBudget) { raise_timeout(); break; }
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------ MMA issuer
+        // --------------------------------------------------------- MMA issuer
         if (lane == 0) {
             // instruction descriptor, kind::mxf4nvf4: A/B E2M1 (1), K-major,
             // N >> 3 at [17,23), UE4M3 scales (bit 23 = 0), M >> 4 at [24,29).
             const uint32_t idesc = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                                    ((uint32_t)(BM >> 4) << 24);
+            uint32_t g = 0, it = 0;
             bool ok = true;
-            for (int kb = 0; kb < p.num_kb; ++kb) {
-                const int s = kb % S, round = kb / S;
-                const uint32_t wait_bar = GRID == kE2M1 ? full(s) : expd(s);
-                if (!ptx::mbar_wait_bounded(wait_bar, round & 1, kWaitBudget)) {
-                    raise_timeout();
-                    ok = false;
-                    break;
-                }
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
+                const uint32_t b = it & 1, use = it >> 1;
+                if (use > 0 && !wait_or_abort(acce(b), (use - 1) & 1, abort)) { ok = false; break; }
                 ptx::tc_fence_after();
-                const int atoms = min(4, p.nkt - 4 * kb);
-                const uint32_t st = smem_base + s * C::kStageBytes;
-                const uint32_t sf_t = tmem + kSfCol + 32u * s;
-                for (int j = 0; j < atoms; ++j) {
-                    ptx::tc_cp_32x128b_warpx4(sf_t + 4u * j, ptx::sdesc(st + C::kSfaOff + 512u * j, 0, 128, 0));
-                    ptx::tc_cp_32x128b_warpx4(sf_t + 16u + 4u * j, ptx::sdesc(st + C::kSfbOff + 512u * j, 0, 128, 0));
+                const uint32_t acc = tmem + b * BN;
+                for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
+                    const uint32_t s = g % S, round = g / S;
+                    if (!wait_or_abort(GRID == kE2M1 ? full(s) : expd(s), round & 1, abort)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    const int atoms = min(4, p.nkt - 4 * kb);
+                    const uint32_t st = smem_base + s * C::kStageBytes;
+                    const uint32_t sf_t = tmem + kSfCol + 32u * s;
+                    for (int j = 0; j < atoms; ++j) {
+                        ptx::tc_cp_32x128b_warpx4(sf_t + 4u * j, ptx::sdesc(st + C::kSfaOff + 512u * j, 0, 128, 0));
+                        ptx::tc_cp_32x128b_warpx4(sf_t + 16u + 4u * j,
+                                                  ptx::sdesc(st + C::kSfbOff + 512u * j, 0, 128, 0));
+                    }
+                    for (int j = 0; j < atoms; ++j) {
+                        const uint32_t sfa = sf_t + 4u * j, sfb = sf_t + 16u + 4u * j;
+                        const uint32_t first = (kb == 0 && j == 0) ? 0u : 1u;
+                        const uint32_t ah = st + C::kAOff + 32u * j, bh = st + C::kBOff + 32u * j;
+                        ptx::tc_mma_nvf4(acc, ptx::sdesc(ah, 16, 1024, 2), ptx::sdesc(bh, 16, 1024, 2), idesc, sfa,
+                                         sfb, first);
+                        if (GRID == kE1M2) {
+                            const uint32_t al = st + C::kALoOff + 32u * j, bl = st + C::kBLoOff + 32u * j;
+                            ptx::tc_mma_nvf4(acc, ptx::sdesc(ah, 16, 1024, 2), ptx::sdesc(bl, 16, 1024, 2), idesc,
+                                             sfa, sfb, 1u);
+                            ptx::tc_mma_nvf4(acc, ptx::sdesc(al, 16, 1024, 2), ptx::sdesc(bh, 16, 1024, 2), idesc,
+                                             sfa, sfb, 1u);
+                            ptx::tc_mma_nvf4(acc, ptx::sdesc(al, 16, 1024, 2), ptx::sdesc(bl, 16, 1024, 2), idesc,
+                                             sfa, sfb, 1u);
+                        }
+                    }
+                    ptx::tc_commit(empty(s));
                 }
-                for (int j = 0; j < atoms; ++j) {
-                    const uint32_t sfa = sf_t + 4u * j, sfb = sf_t + 16u + 4u * j;
-                    const uint32_t first = (kb == 0 && j == 0) ? 0u : 1u;
-                    if (GRID == kE2M1) {
-                        ptx::tc_mma_nvf4(tmem + kAccCol, ptx::sdesc(st + C::kAOff + 32u * j, 16, 1024, 2),
-                                         ptx::sdesc(st + C::kBOff + 32u * j, 16, 1024, 2), idesc, sfa, sfb,
-                                         first);
+                if (ok) ptx::tc_commit(accf(b));   // fires once this tile's MMAs have completed
+            }
+            // TMEM is freed below only after every MMA issued here has finished.
+            ptx::tc_commit(drained);
+            const long long t0 = clock64();
+            while (!ptx::mbar_try_wait(drained, 0))
+                if (clock64() - t0 > kWaitBudget) { raise_timeout(); break; }
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                 // TMEM lane quadrant of this warp
+        const float alpha = __fmul_rn(*p.ts_a, *p.ts_b);
+        uint32_t it = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+            const uint32_t b = it & 1, use = it >> 1;
+            bool ok = wait_or_abort(accf(b), use & 1, abort);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const int m0 = (t / p.ntn) * BM, n0 = (t % p.ntn) * BN;
+            const int row = m0 + 32 * q + lane;
+            float *crow = p.c + (int64_t)row * p.ldc;
+#pragma unroll 1
+            for (int ch = 0; ch < BN / 32; ++ch) {
+                uint32_t r[32];
+                ptx::tc_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + b * BN + 32u * ch, r);
+                ptx::tc_wait_ld();
+                const int col0 = n0 + 32 * ch;
+                if (row < p.M) {
+                    if (col0 + 32 <= p.N) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 v = make_float4(__uint_as_float(r[i]) * alpha, __uint_as_float(r[i + 1]) * alpha,
+                                                         __uint_as_float(r[i + 2]) * alpha,
+                                                         __uint_as_float(r[i + 3]) * alpha);
+                            *reinterpret_cast<float4 *>(crow + col0 + i) = v;
+                        }
                     } else {
-                        const uint32_t ah = st + C::kAOff + 32u * j, al = st + C::kALoOff + 32u * j;
-                        const uint32_t bh = st + C::kBOff + 32u * j, bl = st + C::kBLoOff + 32u * j;
-                        ptx::tc_mma_nvf4(tmem + kAccCol, ptx::sdesc(ah, 16, 1024, 2), ptx::sdesc(bh, 16, 1024, 2),
-                                         idesc, sfa, sfb, first);
-                        ptx::tc_mma_nvf4(tmem + kAccCol, ptx::sdesc(ah, 16, 1024, 2), ptx::sdesc(bl, 16, 1024, 2),
-                                         idesc, sfa, sfb, 1u);
-                        ptx::tc_mma_nvf4(tmem + kAccCol, ptx::sdesc(al, 16, 1024, 2), ptx::sdesc(bh, 16, 1024, 2),
-                                         idesc, sfa, sfb, 1u);
-                        ptx::tc_mma_nvf4(tmem + kAccCol, ptx::sdesc(al, 16, 1024, 2), ptx::sdesc(bl, 16, 1024, 2),
-                                         idesc, sfa, sfb, 1u);
+                        for (int i = 0; i < 32; ++i)
+                            if (col0 + i < p.N) crow[col0 + i] = __uint_as_float(r[i]) * alpha;
                     }
                 }
-                ptx::tc_commit(empty(s));
             }
-            (void)ok;
-            ptx::tc_commit(acc_bar);   // fires once every MMA above has completed
-            // TMEM is freed below only after every MMA has finished with it.
-            if (!ptx::mbar_wait_bounded(acc_bar, 0, kWaitBudget)) raise_timeout();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(acce(b));
         }
     } else {
-        // ------------------------------------- expanders (E1M2) + epilogue
-        const int et = threadIdx.x - 64;   // 0..127
+        // ------------------------------------------------- E1M2 expanders
+        const int et = threadIdx.x - 192;   // 0..127
+        uint32_t g = 0;
         bool ok = true;
-        if (GRID == kE1M2) {
-            for (int kb = 0; kb < p.num_kb; ++kb) {
-                const int s = kb % S, round = kb / S;
-                if (!ptx::mbar_wait_bounded(full(s), round & 1, kWaitBudget)) {
-                    raise_timeout();
-                    ok = false;
-                    break;
-                }
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
+                const uint32_t s = g % S, round = g / S;
+                ok = wait_or_abort(full(s), round & 1, abort);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
                 uint8_t *st = smem + s * C::kStageBytes;
 #pragma unroll 4
                 for (int i = et; i < (int)(TILE_BYTES / 16); i += 128) {
                     uint4 *pa = reinterpret_cast<uint4 *>(st + C::kAOff) + i;
                     uint4 *pb = reinterpret_cast<uint4 *>(st + C::kBOff) + i;
-                    uint4 a = *pa, b = *pb, ah, alo, bh, blo;
+                    uint4 a = *pa, bv = *pb, ah, alo, bh, blo;
                     split_e1m2(a.x, ah.x, alo.x); split_e1m2(a.y, ah.y, alo.y);
                     split_e1m2(a.z, ah.z, alo.z); split_e1m2(a.w, ah.w, alo.w);
-                    split_e1m2(b.x, bh.x, blo.x); split_e1m2(b.y, bh.y, blo.y);
-                    split_e1m2(b.z, bh.z, blo.z); split_e1m2(b.w, bh.w, blo.w);
+                    split_e1m2(bv.x, bh.x, blo.x); split_e1m2(bv.y, bh.y, blo.y);
+                    split_e1m2(bv.z, bh.z, blo.z); split_e1m2(bv.w, bh.w, blo.w);
                     *pa = ah;
                     *pb = bh;
                     reinterpret_cast<uint4 *>(st + C::kALoOff)[i] = alo;
@@ -242,38 +310,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 ptx::fence_proxy_async();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(expd(s));
-            }
-        }
-        const int q = warp & 3;                 // TMEM lane quadrant of this warp
-        const int row = m0 + 32 * q + lane;
-        if (ok && !ptx::mbar_wait_bounded(acc_bar, 0, kWaitBudget)) {
-            raise_timeout();
-            ok = false;
-        }
-        ok = __all_sync(0xffffffffu, ok);
-        ptx::tc_fence_after();
-        if (ok) {
-            const float alpha = __fmul_rn(*p.ts_a, *p.ts_b);
-            float *crow = p.c + (int64_t)row * p.ldc;
-#pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
-                uint32_t r[32];
-                ptx::tc_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + kAccCol + 32u * ch, r);
-                ptx::tc_wait_ld();
-                const int col0 = n0 + 32 * ch;
-                if (row < p.M) {
-                    if (col0 + 32 <= p.N) {
-#pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            float4 v = make_float4(__uint_as_float(r[i]) * alpha, __uint_as_float(r[i + 1]) * alpha,
-                                                   __uint_as_float(r[i + 2]) * alpha, __uint_as_float(r[i + 3]) * alpha);
-                            *reinterpret_cast<float4 *>(crow + col0 + i) = v;
-                        }
-                    } else {
-                        for (int i = 0; i < 32; ++i)
-                            if (col0 + i < p.N) crow[col0 + i] = __uint_as_float(r[i]) * alpha;
-                    }
-                }
             }
         }
     }
@@ -326,8 +362,11 @@ cudaError_t run_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const GemmPar
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    dim3 grid((p.N + BN - 1) / BN, (p.M + BM - 1) / BM);
-    k_gemm<GRID><<<grid, kGemmThreads, C::kSmemBytes, s>>>(ma, mb, p);
+    static int sms = 0;
+    if (!sms) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int ntiles = p.ntm * p.ntn;
+    const int grid = ntiles < sms ? ntiles : sms;
+    k_gemm<GRID><<<grid, C::kThreads, C::kSmemBytes, s>>>(ma, mb, p);
     return cudaGetLastError();
 }
 
@@ -346,6 +385,8 @@ cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const f
     p.c = c; p.ldc = ldc; p.M = (int)M; p.N = (int)N;
     p.nkt = (int)(kpad / 64);
     p.num_kb = (p.nkt + 3) / 4;
+    p.ntm = (int)((M + BM - 1) / BM);
+    p.ntn = (int)((N + BN - 1) / BN);
     if (grid == kE2M1) return run_gemm<kE2M1>(ma, mb, p, s);
     return run_gemm<kE1M2>(ma, mb, p, s);
 }

@@ -50,5 +50,6 @@ cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const f
 // Reads and clears the sticky flag that a bounded device-side wait raises
 // when it gives up (synchronises s).
 cudaError_t read_timeout_flag(uint32_t *flag, cudaStream_t s);
+cudaError_t read_quant_timeout_flag(uint32_t *flag, cudaStream_t s);
 
 }  // namespace ufp4

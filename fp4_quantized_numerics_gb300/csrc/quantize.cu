@@ -27,12 +27,18 @@
 //    memset, deterministic).
 #include "common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 #include <algorithm>
 #include <cfloat>
+#include <mutex>
 #include <type_traits>
+#include <vector>
 
 namespace ufp4 {
+
+// Raised by a bounded wait of the staged quantization kernels that gave up.
+__device__ uint32_t g_quant_timeout;
 
 namespace {
 
@@ -122,7 +128,8 @@ __device__ __forceinline__ void advance(Pos &p, int64_t dr, int64_t dc, int64_t 
 // Tensor scale from the partial maxima (or amax_in); also fills the per-code
 // multiplier table k[e] = min(S_enc / E4M3(e), FLT_MAX) * kfold.
 __device__ __forceinline__ void tensor_scale_prologue(const Args &a, float qmax, float kfold,
-                                                      float *s_k, float *s_red, float &S_enc) {
+                                                      float *s_k, float *s_red, float &S_enc,
+                                                      bool e1m2_fold = false, bool *folded = nullptr) {
     float m = 0.0f;
     if (a.amax_in) {
         m = *a.amax_in;
@@ -144,6 +151,12 @@ __device__ __forceinline__ void tensor_scale_prologue(const Args &a, float qmax,
         sd = __fdiv_rn(A_t, num);
     }
     S_enc = se;
+    // E1M2 codes come from x = q * 2^-8 (see e1m2x8); folding 2^-8 into the
+    // table is exact while every k = S_enc / e >= S_enc / 448 stays >= 2^-118,
+    // i.e. S_enc >= 2^-109 (A_t below ~1e36).
+    const bool fold = e1m2_fold && se >= 1.5407439555097887e-33f;
+    if (folded) *folded = fold;
+    if (fold) kfold *= 0.00390625f;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         if (a.tensor_scale) *a.tensor_scale = sd;
         if (a.status) *a.status = (isfinite(A_t) ? 0u : 1u);
@@ -162,9 +175,25 @@ __device__ __forceinline__ void tensor_scale_prologue(const Args &a, float qmax,
     __syncthreads();
 }
 
-// Block scale code of a block whose magnitude maximum is amax.
+// Block scale code of a block whose magnitude maximum is amax:
+// E4M3(fl32(fl32(amax / qmax) * S_enc)).  The division uses Markstein's
+// correction of the reciprocal product (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): q = RN(a * RN(1/b)), r = RN(a - b q) (exact with FMA),
+// RN(q + r RN(1/b)) -- the correctly rounded quotient.  An exhaustive GPU
+// comparison over every finite fp32 a showed it equal to IEEE division for
+// b = 6 and b = 3.5 whenever a >= 2^-123; below that (results near the
+// subnormal range) the IEEE division is used.
+__device__ __forceinline__ float div_qmax(float a, float qmax) {
+    if (!(a >= 9.4039548e-38f)) return __fdiv_rn(a, qmax);   // 2^-123, NaN, 0
+    const float rcp = qmax == 6.0f ? 0.16666667163372040f : 0.28571429848670960f;
+    const float q = __fmul_rn(a, rcp);
+    const float r = __fmaf_rn(-qmax, q, a);
+    return __fmaf_rn(r, rcp, q);
+}
+
 __device__ __forceinline__ uint32_t block_scale(float amax, float qmax, float S_enc) {
-    return e4m3_from_f32(__fmul_rn(__fdiv_rn(amax, qmax), S_enc));
+    return e4m3_from_f32(__fmul_rn(div_qmax(amax, qmax), S_enc));
 }
 
 // Codes of 8 values q (already multiplied by k) as 8 nibbles, element j in
@@ -212,32 +241,266 @@ __device__ __forceinline__ void zero_pad_rows(const Args &a) {
 }
 
 // ======================================================= row-wise kernels
-template <class In, bool RHT>
-__global__ void __launch_bounds__(kThreads) k_amax_rowwise(Args a) {
-    __shared__ float s_red[kThreads / 32];
-    const uint32_t lane = threadIdx.x & 31;
-    const uint32_t h = lane & 1;
-    const uint32_t sflip = RHT ? ((rht_sign_mask(a.rht_seed) >> (8 * h)) & 0xFFu) : 0u;
-    const float hsign = h ? -1.0f : 1.0f;
-    const int64_t upr = a.k / 8;  // only real elements
-    const int64_t total = a.out_rows * upr;
-    const int64_t T = (int64_t)gridDim.x * blockDim.x;
-    const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-    Pos p{tid / upr, tid % upr};
-    const int64_t dr = T / upr, dc = T % upr;
-    const int64_t iters = (total + T - 1) / T;
-    float m = 0.0f;
-    for (int64_t it = 0; it < iters; ++it) {
-        const bool valid = p.r < a.out_rows;
-        float v[8];
-        unit_values<In, RHT>(static_cast<const In *>(a.x), a.ld, p.r, p.c, valid, sflip, hsign, v);
+// One thread owns one 16-block: a single 32-byte load (BF16) per block, so a
+// warp's load covers 1 KB of contiguous row.  The 16 values are held as 8
+// packed pairs P_j = (v_j, v_{j+8}); the butterflies on index bits 0..2 act
+// on both halves at once with add/sub.rn.f32x2, the bit-3 stage pairs the
+// halves.  Blocks are enumerated row-major over (row, block-in-row) with a
+// fast 32-bit divider; each thread keeps two blocks in flight.
+
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// RHT sign flips, precomputed once per thread as XOR masks on the loaded
+// words: row-wise BF16 word i holds elements (2i, 2i+1) -> bits 15 / 31;
+// row-wise FP32 word e -> bit 31; column-wise BF16 row i holds two columns
+// -> 0x80008000; column-wise FP32 row i -> bit 31 of both words.
+struct Signs {
+    uint32_t m[16];
+};
+template <class In> __device__ __forceinline__ Signs row_signs(uint32_t smask);
+template <> __device__ __forceinline__ Signs row_signs<__nv_bfloat16>(uint32_t smask) {
+    Signs s;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m = max_nan(m, fabsf(v[i]));
-        advance(p, dr, dc, upr);
+    for (int i = 0; i < 8; ++i)
+        s.m[i] = (((smask >> (2 * i)) & 1u) << 15) | (((smask >> (2 * i + 1)) & 1u) << 31);
+#pragma unroll
+    for (int i = 8; i < 16; ++i) s.m[i] = 0u;
+    return s;
+}
+template <> __device__ __forceinline__ Signs row_signs<float>(uint32_t smask) {
+    Signs s;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s.m[i] = ((smask >> i) & 1u) << 31;
+    return s;
+}
+template <class In> __device__ __forceinline__ Signs col_signs(uint32_t smask);
+template <> __device__ __forceinline__ Signs col_signs<__nv_bfloat16>(uint32_t smask) {
+    Signs s;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s.m[i] = ((smask >> i) & 1u) ? 0x80008000u : 0u;
+    return s;
+}
+template <> __device__ __forceinline__ Signs col_signs<float>(uint32_t smask) {
+    Signs s;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) s.m[i] = ((smask >> i) & 1u) << 31;
+    return s;
+}
+
+// Raw 16 elements of one block.
+template <class In> struct Raw;
+template <> struct Raw<__nv_bfloat16> {
+    uint32_t w[8];
+    __device__ __forceinline__ void load(const __nv_bfloat16 *p) {
+        asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                       "=r"(w[6]), "=r"(w[7])
+                     : "l"(p));
+    }
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = 0u;
+    }
+    __device__ __forceinline__ void load_shared(uint32_t sa) {
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(sa));
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]) : "r"(sa + 16));
+    }
+    // element e as fp32, with the row-wise sign masks applied
+    __device__ __forceinline__ float get(int e, const Signs &sg) const {
+        const uint32_t u = w[e >> 1] ^ sg.m[e >> 1];
+        return __uint_as_float((e & 1) ? (u & 0xFFFF0000u) : (u << 16));
+    }
+    __device__ __forceinline__ float get(int e) const {
+        const uint32_t u = w[e >> 1];
+        return __uint_as_float((e & 1) ? (u & 0xFFFF0000u) : (u << 16));
+    }
+};
+template <> struct Raw<float> {
+    uint32_t w[16];
+    __device__ __forceinline__ void load(const float *p) {
+        asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                       "=r"(w[6]), "=r"(w[7])
+                     : "l"(p));
+        asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(w[8]), "=r"(w[9]), "=r"(w[10]), "=r"(w[11]), "=r"(w[12]), "=r"(w[13]),
+                       "=r"(w[14]), "=r"(w[15])
+                     : "l"(p + 8));
+    }
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = 0u;
+    }
+    __device__ __forceinline__ void load_shared(uint32_t sa) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(w[4 * q]), "=r"(w[4 * q + 1]), "=r"(w[4 * q + 2]), "=r"(w[4 * q + 3])
+                         : "r"(sa + 16 * q));
+    }
+    __device__ __forceinline__ float get(int e, const Signs &sg) const { return __uint_as_float(w[e] ^ sg.m[e]); }
+    __device__ __forceinline__ float get(int e) const { return __uint_as_float(w[e]); }
+};
+
+template <class In>
+__device__ __forceinline__ void block_values_rht(const Raw<In> &raw, const Signs &sg, float lo[8], float hi[8]) {
+    uint64_t P[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) P[j] = pk2(raw.get(j, sg), raw.get(j + 8, sg));
+#pragma unroll
+    for (int s = 1; s < 8; s <<= 1) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if ((j & s) == 0) {
+                const uint64_t a = P[j], b = P[j + s];
+                P[j] = add2(a, b);
+                P[j + s] = sub2(a, b);
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float a, b;
+        upk2(P[j], a, b);
+        lo[j] = a + b;
+        hi[j] = a - b;
+    }
+}
+
+// Values of one block after the optional transform: lo[j] = v_j, hi[j] =
+// v_{j+8}; with RHT they are 4 y (H16 diag(d) x, unnormalised).
+template <class In, bool RHT>
+__device__ __forceinline__ void block_values(const Raw<In> &raw, const Signs &sg, float lo[8], float hi[8]) {
+    if (!RHT) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { lo[j] = raw.get(j); hi[j] = raw.get(j + 8); }
+    } else {
+        block_values_rht(raw, sg, lo, hi);
+    }
+}
+
+struct FastDiv {
+    uint32_t m, s;
+};
+FastDiv make_fastdiv(uint32_t d) {
+    uint32_t s = 0;
+    while ((1ull << s) < d) ++s;
+    const uint64_t m = ((1ull << 32) * ((1ull << s) - d)) / d + 1;
+    return FastDiv{(uint32_t)m, s};
+}
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, FastDiv f) {
+    return (uint32_t)(((uint64_t)__umulhi(n, f.m) + n) >> f.s);
+}
+
+// E2M1 RTNE of 8 values, element j in bits 4j..4j+3 (satfinite clamps at 6).
+__device__ __forceinline__ uint32_t e2m1x8(const float v[8]) {
+    uint32_t w;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(w)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    return w;
+}
+
+// E1M2 RTNE of 8 values x = q * 2^-8 (q in grid units), already clamped to
+// |x| <= 7 * 2^-9.  On [0, 15 * 2^-9] E4M3 is a uniform grid of step 2^-9
+// (subnormals, then the first normal binade), so the saturating E4M3 RNE of
+// x is sign << 7 | m with m = rint(2|q|), ties to even: exactly the E1M2 code.
+// The bytes are regrouped as sign << 3 | m nibbles, element j at bits 4j.
+__device__ __forceinline__ uint32_t e1m2x8(const float x[8]) {
+    uint32_t ev, od;
+    asm("{\n\t.reg .b16 h0, h1, h2, h3;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 h0, %3, %2;\n\t"    // bytes (x0, x2)
+        "cvt.rn.satfinite.e4m3x2.f32 h1, %5, %4;\n\t"    // bytes (x4, x6)
+        "cvt.rn.satfinite.e4m3x2.f32 h2, %7, %6;\n\t"    // bytes (x1, x3)
+        "cvt.rn.satfinite.e4m3x2.f32 h3, %9, %8;\n\t"    // bytes (x5, x7)
+        "mov.b32 %0, {h0, h1};\n\t"
+        "mov.b32 %1, {h2, h3};\n\t}"
+        : "=r"(ev), "=r"(od)
+        : "f"(x[0]), "f"(x[2]), "f"(x[4]), "f"(x[6]), "f"(x[1]), "f"(x[3]), "f"(x[5]), "f"(x[7]));
+    // ev bytes: x0, x2, x4, x6 ; od bytes: x1, x3, x5, x7
+    const uint32_t ne = (ev | (ev >> 4)) & 0x0F0F0F0Fu;
+    const uint32_t no = (od | (od >> 4)) & 0x0F0F0F0Fu;
+    return ne | (no << 4);
+}
+
+// Two blocks per thread per step, software-pipelined: the loads of step i+1
+// are issued before the arithmetic of step i, so every thread always has
+// 64 bytes (BF16) in flight.
+template <class In>
+struct RowFetch {
+    Raw<In> raw[2];
+    uint32_t r[2], b[2];
+    bool ok[2];
+    __device__ __forceinline__ void fetch(const In *x, int64_t ld, uint32_t u0, uint32_t T, uint32_t total,
+                                          FastDiv bdiv, uint32_t bpr, uint32_t kvb) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const uint32_t u = u0 + t * T;
+            ok[t] = u < total;
+            r[t] = fdiv(u, bdiv);
+            b[t] = u - r[t] * bpr;
+            if (ok[t] && b[t] < kvb) raw[t].load(x + (int64_t)r[t] * ld + b[t] * 16);
+            else raw[t].zero();
+        }
+    }
+};
+
+template <class In, bool RHT>
+__global__ void __launch_bounds__(kThreads) k_amax_rowwise(Args a, FastDiv bdiv, uint32_t bpr,
+                                                           uint32_t total) {
+    __shared__ float s_red[kThreads / 32];
+    const uint32_t smask = RHT ? rht_sign_mask(a.rht_seed) : 0u;
+    const Signs sg = row_signs<In>(smask);
+    const uint32_t T = gridDim.x * blockDim.x;
+    const In *x = static_cast<const In *>(a.x);
+    float m = 0.0f;
+    uint32_t u0 = blockIdx.x * blockDim.x + threadIdx.x;
+    RowFetch<In> cur;
+    cur.fetch(x, a.ld, u0, T, total, bdiv, bpr, bpr);
+    for (; u0 < total; u0 += 2 * T) {
+        RowFetch<In> nxt;
+        nxt.fetch(x, a.ld, u0 + 2 * T, T, total, bdiv, bpr, bpr);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            float lo[8], hi[8];
+            block_values<In, RHT>(cur.raw[t], sg, lo, hi);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) m = max_nan(m, max_nan(fabsf(lo[j]), fabsf(hi[j])));
+        }
+        cur = nxt;
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) s_red[threadIdx.x >> 5] = m;
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m;
     __syncthreads();
     if (threadIdx.x == 0) {
         for (int w = 1; w < kThreads / 32; ++w) m = max_nan(m, s_red[w]);
@@ -245,96 +508,280 @@ __global__ void __launch_bounds__(kThreads) k_amax_rowwise(Args a) {
     }
 }
 
+__device__ __forceinline__ uint32_t scale_offset32(uint32_t r, uint32_t b, uint32_t nkt) {
+    return (((r >> 7) * nkt + (b >> 2)) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2) + (b & 3);
+}
+
+// Rounding of one block's 16 values q (grid units, already multiplied by
+// the table's k) into two 32-bit words of nibbles.  `folded`: for E1M2 the
+// table already holds k * 2^-8.  `e` is the block's scale code: when the E4M3
+// rounding of the scale was an ordinary round-to-nearest of a normal value
+// (8 <= e < 0x7E) it moved the scale by at most 1/16 relative, so
+// |q| <= qmax * 16/15 < 3.75 and the E4M3 step of e1m2x8 cannot carry past
+// m = 7; subnormal scales (e < 8) and saturated ones (e = 448, e.g. a caller
+// amax below the true maximum) take the explicit clamp.
+template <int GRID, int ROUND>
+__device__ __forceinline__ uint2 round_block(float ql[8], float qh[8], uint32_t e, bool folded, const Args &a,
+                                             uint64_t i0) {
+    if (ROUND == kRTNE && GRID == kE2M1) return make_uint2(e2m1x8(ql), e2m1x8(qh));
+    if (ROUND == kRTNE) {
+        if (!folded) {
+            const uint64_t S8 = pk2(0.00390625f, 0.00390625f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) upk2(mul2(pk2(ql[j], qh[j]), S8), ql[j], qh[j]);
+        }
+        if (e < 8u || e >= 0x7Eu) {
+            const float c = 7.0f * 0.001953125f;   // 7 * 2^-9
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                ql[j] = fminf(fmaxf(ql[j], -c), c);
+                qh[j] = fminf(fmaxf(qh[j], -c), c);
+            }
+        }
+        return make_uint2(e1m2x8(ql), e1m2x8(qh));
+    }
+    return make_uint2(codes8<GRID, ROUND>(ql, a, i0), codes8<GRID, ROUND>(qh, a, i0 + 8));
+}
+
+__device__ __forceinline__ void store_block(const Args &a, uint32_t r, uint32_t b, uint2 w, uint32_t e,
+                                            uint32_t cstride, uint32_t nkt) {
+    if (e == 0) w = make_uint2(0u, 0u);
+    *reinterpret_cast<uint2 *>(a.codes + (size_t)r * cstride + b * 8) = w;
+    a.scales[scale_offset32(r, b, nkt)] = (uint8_t)e;
+}
+
+// Quantize one row-wise 16-block (row r, block b) from its raw elements.
 template <class In, int GRID, int ROUND, bool RHT>
-__global__ void __launch_bounds__(kThreads) k_quant_rowwise(Args a) {
+__device__ __forceinline__ void quant_block_row(const Args &a, const Raw<In> &raw, uint32_t r, uint32_t b,
+                                                const Signs &sg, float S_enc, const float *s_k,
+                                                uint32_t cstride, uint32_t nkt, bool folded) {
+    const float qmax = GRID == kE2M1 ? 6.0f : 3.5f;
+    float lo[8], hi[8];
+    block_values<In, RHT>(raw, sg, lo, hi);
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fmaxf(fabsf(lo[j]), fabsf(hi[j])));
+    if (RHT) m *= 0.25f;
+    const uint32_t e = block_scale(m, qmax, S_enc);
+    const float kk = s_k[e];
+    const uint64_t K2 = pk2(kk, kk);
+    float ql[8], qh[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) upk2(mul2(pk2(lo[j], hi[j]), K2), ql[j], qh[j]);
+    const uint64_t i0 = a.elem_base + (uint64_t)r * (uint64_t)a.k + (uint64_t)b * 16u;
+    store_block(a, r, b, round_block<GRID, ROUND>(ql, qh, e, folded, a, i0), e, cstride, nkt);
+}
+
+// Two row-wise blocks (A, B) held as packed pairs P_j = (A_j, B_j), so all
+// four butterfly stages and the scaling run on f32x2.
+template <int GRID, int ROUND, bool RHT>
+__device__ __forceinline__ void quant_pair_row(const Args &a, const Raw<__nv_bfloat16> &ra,
+                                               const Raw<__nv_bfloat16> &rb, uint32_t r0, uint32_t b0,
+                                               uint32_t r1, uint32_t b1, bool has_b, const Signs &sg,
+                                               float S_enc, const float *s_k, uint32_t cstride,
+                                               uint32_t nkt, bool folded) {
+    const float qmax = GRID == kE2M1 ? 6.0f : 3.5f;
+    uint64_t P[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) P[j] = RHT ? pk2(ra.get(j, sg), rb.get(j, sg)) : pk2(ra.get(j), rb.get(j));
+    if (RHT) {
+#pragma unroll
+        for (int st = 1; st < 16; st <<= 1) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if ((j & st) == 0) {
+                    const uint64_t x = P[j], y = P[j + st];
+                    P[j] = add2(x, y);
+                    P[j + st] = sub2(x, y);
+                }
+            }
+        }
+    }
+    float va[16], vb[16];
+    float ma = 0.0f, mb = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        upk2(P[j], va[j], vb[j]);
+        ma = fmaxf(ma, fabsf(va[j]));
+        mb = fmaxf(mb, fabsf(vb[j]));
+    }
+    if (RHT) { ma *= 0.25f; mb *= 0.25f; }
+    const uint32_t ea = block_scale(ma, qmax, S_enc), eb = block_scale(mb, qmax, S_enc);
+    const uint64_t K2 = pk2(s_k[ea], s_k[eb]);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) upk2(mul2(P[j], K2), va[j], vb[j]);
+    const uint64_t ia = a.elem_base + (uint64_t)r0 * (uint64_t)a.k + (uint64_t)b0 * 16u;
+    const uint64_t ib = a.elem_base + (uint64_t)r1 * (uint64_t)a.k + (uint64_t)b1 * 16u;
+    store_block(a, r0, b0, round_block<GRID, ROUND>(va, va + 8, ea, folded, a, ia), ea, cstride, nkt);
+    if (has_b) store_block(a, r1, b1, round_block<GRID, ROUND>(vb, vb + 8, eb, folded, a, ib), eb, cstride, nkt);
+}
+
+template <class In, int GRID, int ROUND, bool RHT>
+__global__ void __launch_bounds__(kThreads) k_quant_rowwise(Args a, FastDiv bdiv, uint32_t bpr,
+                                                            uint32_t total) {
     __shared__ float s_k[256];
     __shared__ float s_red[kThreads / 32];
     const float qmax = GRID == kE2M1 ? 6.0f : 3.5f;
     float S_enc;
-    tensor_scale_prologue(a, qmax, RHT ? 0.25f : 1.0f, s_k, s_red, S_enc);
+    bool folded = false;
+    tensor_scale_prologue(a, qmax, RHT ? 0.25f : 1.0f, s_k, s_red, S_enc, GRID == kE1M2 && ROUND == kRTNE,
+                          &folded);
 
-    const uint32_t lane = threadIdx.x & 31;
-    const uint32_t h = lane & 1;
-    const uint32_t sflip = RHT ? ((rht_sign_mask(a.rht_seed) >> (8 * h)) & 0xFFu) : 0u;
-    const float hsign = h ? -1.0f : 1.0f;
-    const int64_t upr = a.kpad / 8;   // units per row, padding included
-    const int64_t kvalid8 = a.k / 8;
-    const int64_t total = a.out_rows * upr;
-    const int64_t T = (int64_t)gridDim.x * blockDim.x;
-    const int64_t tid = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-    Pos p{tid / upr, tid % upr};
-    const int64_t dr = T / upr, dc = T % upr;
-    const int64_t iters = (total + T - 1) / T;
+    const uint32_t smask = RHT ? rht_sign_mask(a.rht_seed) : 0u;
+    const Signs sg = row_signs<In>(smask);
+    const uint32_t T = gridDim.x * blockDim.x;
+    const uint32_t kvb = (uint32_t)(a.k / 16);      // real blocks per row
+    const uint32_t nkt = (uint32_t)a.nkt;
     const In *x = static_cast<const In *>(a.x);
-    const int64_t cstride = a.kpad / 2;
-    for (int64_t it = 0; it < iters; ++it) {
-        const bool valid = p.r < a.out_rows;
-        float v[8];
-        unit_values<In, RHT>(x, a.ld, p.r, p.c, valid && p.c < kvalid8, sflip, hsign, v);
-        float m = 0.0f;
+    const uint32_t cstride = (uint32_t)(a.kpad / 2);
+    uint32_t u0 = blockIdx.x * blockDim.x + threadIdx.x;
+    RowFetch<In> cur;
+    cur.fetch(x, a.ld, u0, T, total, bdiv, bpr, kvb);
+    for (; u0 < total; u0 += 2 * T) {
+        RowFetch<In> nxt;
+        nxt.fetch(x, a.ld, u0 + 2 * T, T, total, bdiv, bpr, kvb);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        if (RHT) m *= 0.25f;
-        const uint32_t e = block_scale(m, qmax, S_enc);
-        const float kk = s_k[e];
-        float q[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(v[i], kk);
-        uint32_t w = codes8<GRID, ROUND>(q, a, a.elem_base + (uint64_t)(p.r * a.k + p.c * 8));
-        if (e == 0) w = 0;
-        if (valid) {
-            *reinterpret_cast<uint32_t *>(a.codes + p.r * cstride + p.c * 4) = w;
-            if (h == 0) a.scales[scale_offset(p.r, p.c >> 1, a.nkt)] = (uint8_t)e;
+        for (int t = 0; t < 2; ++t) {
+            if (!cur.ok[t]) continue;
+            quant_block_row<In, GRID, ROUND, RHT>(a, cur.raw[t], cur.r[t], cur.b[t], sg, S_enc, s_k,
+                                                  cstride, nkt, folded);
         }
-        advance(p, dr, dc, upr);
+        cur = nxt;
     }
     zero_pad_rows(a);
+}
+
+// Grid of exactly the CTAs that fit on the device at once (persistent).
+template <class K>
+int resident_grid(K kernel, int64_t work_ctas, size_t smem = 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    const int64_t g = std::min<int64_t>(std::max<int64_t>(work_ctas, 1), (int64_t)per_sm * num_sms());
+    return (int)std::min<int64_t>(g, kMaxPartials);
 }
 
 // ==================================================== column-wise kernels
-// Tile: 128 output rows (input columns) x 128 output k (input rows); warp w
-// owns 16-block kb = tile_k * 8 + w, lane l owns input columns 4l..4l+3.
-template <class In, bool RHT>
-__device__ __forceinline__ void col_block(const In *x, int64_t ld, int64_t r0, int64_t c,
-                                          uint32_t smask, float v[4][16]) {
+// The quantization of X^T: 16-blocks run down the columns.  A thread owns a
+// unit of 16 rows x 2 adjacent columns (two blocks, one per column); a warp's
+// 32 units are 64 adjacent columns, so each row load of the warp reads 128
+// contiguous bytes (BF16).  The two columns are held as packed pairs
+// P_i = (col0[i], col1[i]), so all four butterfly stages run on f32x2.
+// Units are enumerated (row-block, column-pair) with the column pair fastest;
+// the next unit's 16 loads are issued before the current unit's arithmetic.
+template <class In> struct ColRaw;
+template <> struct ColRaw<__nv_bfloat16> {
+    uint32_t w[16];   // row i: (col0, col1) as bf16 pair
+    __device__ __forceinline__ void load(const __nv_bfloat16 *p, int64_t ld) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        float t[4];
-        load4(x + (r0 + i) * ld + c, t);
-        const float s = (RHT && ((smask >> i) & 1u)) ? -1.0f : 1.0f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) v[j][i] = RHT ? t[j] * s : t[j];
+        for (int i = 0; i < 16; ++i) w[i] = __ldg(reinterpret_cast<const unsigned int *>(p + i * ld));
     }
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = 0u;
+    }
+    __device__ __forceinline__ void load_shared(uint32_t sa, uint32_t pitch) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w[i]) : "r"(sa + i * pitch));
+    }
+    __device__ __forceinline__ uint64_t pair(int i, const Signs &sg) const {
+        const uint32_t u = w[i] ^ sg.m[i];
+        return pk2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+    }
+    __device__ __forceinline__ uint64_t pair(int i) const {
+        const uint32_t u = w[i];
+        return pk2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+    }
+};
+template <> struct ColRaw<float> {
+    uint2 w[16];
+    __device__ __forceinline__ void load(const float *p, int64_t ld) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = __ldg(reinterpret_cast<const uint2 *>(p + i * ld));
+    }
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = make_uint2(0u, 0u);
+    }
+    __device__ __forceinline__ void load_shared(uint32_t sa, uint32_t pitch) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(w[i].x), "=r"(w[i].y) : "r"(sa + i * pitch));
+    }
+    __device__ __forceinline__ uint64_t pair(int i, const Signs &sg) const {
+        return pk2(__uint_as_float(w[i].x ^ sg.m[i]), __uint_as_float(w[i].y ^ sg.m[i]));
+    }
+    __device__ __forceinline__ uint64_t pair(int i) const {
+        return pk2(__uint_as_float(w[i].x), __uint_as_float(w[i].y));
+    }
+};
+
+// Column values after the optional transform: P[i] = (c0[i], c1[i]); with
+// RHT they are 4 y (unnormalised).
+template <class In, bool RHT>
+__device__ __forceinline__ void col_values(const ColRaw<In> &raw, const Signs &sg, uint64_t P[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) P[i] = RHT ? raw.pair(i, sg) : raw.pair(i);
     if (RHT) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) fwht16(v[j]);
+        for (int s = 1; s < 16; s <<= 1) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if ((i & s) == 0) {
+                    const uint64_t a = P[i], b = P[i + s];
+                    P[i] = add2(a, b);
+                    P[i + s] = sub2(a, b);
+                }
+            }
+        }
     }
 }
 
+template <class In>
+struct ColFetch {
+    ColRaw<In> raw;
+    uint32_t kb, cp;
+    bool ok, real;
+    __device__ __forceinline__ void fetch(const In *x, int64_t ld, uint32_t u, uint32_t total, FastDiv cdiv,
+                                          uint32_t ncp, uint32_t nkb_real) {
+        ok = u < total;
+        kb = fdiv(u, cdiv);
+        cp = u - kb * ncp;
+        real = ok && kb < nkb_real;
+        if (real) raw.load(x + (int64_t)kb * 16 * ld + cp * 2, ld);
+        else raw.zero();
+    }
+};
+
 template <class In, bool RHT>
-__global__ void __launch_bounds__(kThreads) k_amax_colwise(Args a) {
+__global__ void __launch_bounds__(kThreads) k_amax_colwise(Args a, FastDiv cdiv, uint32_t ncp,
+                                                           uint32_t total) {
     __shared__ float s_red[kThreads / 32];
-    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t smask = RHT ? rht_sign_mask(a.rht_seed) : 0u;
-    const int64_t C = a.cols, R = a.rows;
-    const int64_t ntc = (C + 127) / 128, ntk = (R + 127) / 128;
+    const Signs sg = col_signs<In>(smask);
+    const uint32_t T = gridDim.x * blockDim.x;
+    const uint32_t nkb = (uint32_t)(a.rows / 16);
+    const In *x = static_cast<const In *>(a.x);
     float m = 0.0f;
-    for (int64_t t = blockIdx.x; t < ntc * ntk; t += gridDim.x) {
-        const int64_t tk = t % ntk, tc = t / ntk;
-        const int64_t r0 = (tk * 8 + warp) * 16;
-        const int64_t c = tc * 128 + lane * 4;
-        if (r0 >= R || c >= C) continue;
-        float v[4][16];
-        col_block<In, RHT>(static_cast<const In *>(a.x), a.ld, r0, c, smask, v);
+    uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
+    ColFetch<In> cur;
+    cur.fetch(x, a.ld, u, total, cdiv, ncp, nkb);
+    for (; u < total; u += T) {
+        ColFetch<In> nxt;
+        nxt.fetch(x, a.ld, u + T, total, cdiv, ncp, nkb);
+        uint64_t P[16];
+        col_values<In, RHT>(cur.raw, sg, P);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int i = 0; i < 16; ++i) m = max_nan(m, fabsf(v[j][i]));
+        for (int i = 0; i < 16; ++i) {
+            float c0, c1;
+            upk2(P[i], c0, c1);
+            m = max_nan(m, max_nan(fabsf(c0), fabsf(c1)));
+        }
+        cur = nxt;
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) s_red[warp] = m;
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m;
     __syncthreads();
     if (threadIdx.x == 0) {
         for (int w = 1; w < kThreads / 32; ++w) m = max_nan(m, s_red[w]);
@@ -342,62 +789,330 @@ __global__ void __launch_bounds__(kThreads) k_amax_colwise(Args a) {
     }
 }
 
-template <int GRID, int ROUND>
-__device__ __forceinline__ uint2 codes16(const float q[16], const Args &a, uint64_t i0) {
-    float lo[8], hi[8];
+// Quantize one column-wise unit: 16 rows x columns (c, c+1) starting at
+// row-block kb (two output blocks: rows c and c+1 of the result, block kb).
+// `real` = false for the padding blocks past the last row (zeros written).
+template <class In, int GRID, int ROUND, bool RHT>
+__device__ __forceinline__ void quant_unit_col(const Args &a, const ColRaw<In> &raw, uint32_t kb, uint32_t c,
+                                               bool real, const Signs &sg, float S_enc, const float *s_k,
+                                               uint32_t cstride, uint32_t nkt, bool folded) {
+    const float qmax = GRID == kE2M1 ? 6.0f : 3.5f;
+    uint64_t P[16];
+    col_values<In, RHT>(raw, sg, P);
+    float v0[16], v1[16];
+    float m0 = 0.0f, m1 = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) { lo[i] = q[i]; hi[i] = q[8 + i]; }
-    return make_uint2(codes8<GRID, ROUND>(lo, a, i0), codes8<GRID, ROUND>(hi, a, i0 + 8));
+    for (int i = 0; i < 16; ++i) {
+        upk2(P[i], v0[i], v1[i]);
+        m0 = fmaxf(m0, fabsf(v0[i]));
+        m1 = fmaxf(m1, fabsf(v1[i]));
+    }
+    if (RHT) { m0 *= 0.25f; m1 *= 0.25f; }
+    uint32_t e0 = block_scale(m0, qmax, S_enc), e1 = block_scale(m1, qmax, S_enc);
+    if (!real) { e0 = 0u; e1 = 0u; }
+    const uint64_t K2 = pk2(s_k[e0], s_k[e1]);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) upk2(mul2(P[i], K2), v0[i], v1[i]);
+    const uint64_t R = (uint64_t)a.rows;
+    const uint64_t i0 = a.elem_base + (uint64_t)c * R + (uint64_t)kb * 16u;
+    store_block(a, c, kb, round_block<GRID, ROUND>(v0, v0 + 8, e0, folded, a, i0), e0, cstride, nkt);
+    store_block(a, c + 1, kb, round_block<GRID, ROUND>(v1, v1 + 8, e1, folded, a, i0 + R), e1, cstride, nkt);
 }
 
 template <class In, int GRID, int ROUND, bool RHT>
-__global__ void __launch_bounds__(kThreads) k_quant_colwise(Args a) {
+__global__ void __launch_bounds__(kThreads) k_quant_colwise(Args a, FastDiv cdiv, uint32_t ncp,
+                                                            uint32_t total) {
     __shared__ float s_k[256];
     __shared__ float s_red[kThreads / 32];
     const float qmax = GRID == kE2M1 ? 6.0f : 3.5f;
     float S_enc;
-    tensor_scale_prologue(a, qmax, RHT ? 0.25f : 1.0f, s_k, s_red, S_enc);
+    bool folded = false;
+    tensor_scale_prologue(a, qmax, RHT ? 0.25f : 1.0f, s_k, s_red, S_enc, GRID == kE1M2 && ROUND == kRTNE,
+                          &folded);
 
-    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t smask = RHT ? rht_sign_mask(a.rht_seed) : 0u;
-    const int64_t C = a.cols, R = a.rows;           // input; output is C x R
-    const int64_t nbk = a.kpad / 16;                 // output blocks per row (with pad)
-    const int64_t ntc = (C + 127) / 128, ntk = (nbk + 7) / 8;
-    const int64_t cstride = a.kpad / 2;
-    for (int64_t t = blockIdx.x; t < ntc * ntk; t += gridDim.x) {
-        const int64_t tk = t % ntk, tc = t / ntk;
-        const int64_t kb = tk * 8 + warp;
-        const int64_t r0 = kb * 16;
-        const int64_t c = tc * 128 + lane * 4;
-        if (kb >= nbk || c >= C) continue;
-        if (r0 >= R) {   // padding blocks along k
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                *reinterpret_cast<uint2 *>(a.codes + (c + j) * cstride + r0 / 2) = make_uint2(0, 0);
-                a.scales[scale_offset(c + j, kb, a.nkt)] = 0;
-            }
-            continue;
-        }
-        float v[4][16];
-        col_block<In, RHT>(static_cast<const In *>(a.x), a.ld, r0, c, smask, v);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float m = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[j][i]));
-            if (RHT) m *= 0.25f;
-            const uint32_t e = block_scale(m, qmax, S_enc);
-            const float kk = s_k[e];
-            float q[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) q[i] = __fmul_rn(v[j][i], kk);
-            uint2 w = codes16<GRID, ROUND>(q, a, a.elem_base + (uint64_t)((c + j) * R + r0));
-            if (e == 0) w = make_uint2(0, 0);
-            *reinterpret_cast<uint2 *>(a.codes + (c + j) * cstride + r0 / 2) = w;
-            a.scales[scale_offset(c + j, kb, a.nkt)] = (uint8_t)e;
-        }
+    const Signs sg = col_signs<In>(smask);
+    const uint32_t T = gridDim.x * blockDim.x;
+    const uint32_t nkb = (uint32_t)(a.rows / 16);   // real blocks along k
+    const uint32_t nkt = (uint32_t)a.nkt;
+    const In *x = static_cast<const In *>(a.x);
+    const uint32_t cstride = (uint32_t)(a.kpad / 2);
+    uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
+    ColFetch<In> cur;
+    cur.fetch(x, a.ld, u, total, cdiv, ncp, nkb);
+    for (; u < total; u += T) {
+        ColFetch<In> nxt;
+        nxt.fetch(x, a.ld, u + T, total, cdiv, ncp, nkb);
+        if (cur.ok)
+            quant_unit_col<In, GRID, ROUND, RHT>(a, cur.raw, cur.kb, cur.cp * 2, cur.real, sg, S_enc, s_k,
+                                                 cstride, nkt, folded);
+        cur = nxt;
     }
     zero_pad_rows(a);
+}
+
+// ================================================ TMA-staged (bulk copy) path
+// For inputs whose bytes can be streamed in 16-byte-aligned pieces (row-wise:
+// the whole tensor is contiguous; column-wise: every row segment of a chunk
+// is a multiple of 16 bytes), one thread per CTA streams 16 KB chunks into a
+// 4-deep shared-memory ring with cp.async.bulk (mbarrier completion), so each
+// CTA keeps up to 64 KB of loads in flight independent of the register
+// budget, and all 256 threads compute from shared memory.
+constexpr int kRing = 4;
+constexpr uint32_t kChunk = 16384;
+constexpr uint32_t kRingSmem = kRing * kChunk + 64;
+constexpr long long kRingWait = 4000000000LL;
+
+struct RingCtl {
+    uint32_t buf;    // shared address of stage 0
+    uint32_t bars;   // shared address of the kRing mbarriers
+};
+
+__device__ __forceinline__ RingCtl ring_init(uint8_t *dsm) {
+    RingCtl r;
+    r.buf = ptx::smem_u32(dsm);
+    r.bars = ptx::smem_u32(dsm + kRing * kChunk);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRing; ++s) ptx::mbar_init(r.bars + 8u * s, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    return r;
+}
+
+// Waits for chunk j's stage; false (for every thread) if any thread gave up.
+__device__ __forceinline__ bool ring_wait(const RingCtl &r, uint32_t j) {
+    const bool ok = ptx::mbar_wait_bounded(r.bars + 8u * (j % kRing), (j / kRing) & 1u, kRingWait);
+    return __syncthreads_and(ok) != 0;
+}
+
+// After an early exit: the issuing thread waits (bounded) for every copy it
+// started and that nobody consumed, so none lands in freed shared memory.
+__device__ __forceinline__ void ring_drain(const RingCtl &r, uint32_t consumed, uint32_t issued) {
+    if (threadIdx.x != 0) return;
+    for (uint32_t j = consumed; j < issued; ++j)
+        if (!ptx::mbar_wait_bounded(r.bars + 8u * (j % kRing), (j / kRing) & 1u, kRingWait)) break;
+}
+
+// Row-wise chunks: chunk i = bytes [i * kChunk, ...) of the contiguous input.
+template <class In>
+__device__ __forceinline__ void row_issue(const RingCtl &r, const Args &a, uint32_t j, uint32_t nchunks,
+                                          uint64_t total_bytes, uint32_t &issued) {
+    const uint32_t i = blockIdx.x + j * gridDim.x;
+    if (i >= nchunks) return;
+    const uint64_t off = (uint64_t)i * kChunk;
+    const uint64_t rem = total_bytes - off;
+    const uint32_t bytes = rem < kChunk ? (uint32_t)rem : kChunk;
+    const uint32_t bar = r.bars + 8u * (j % kRing);
+    ptx::mbar_arrive_expect_tx(bar, bytes);
+    ptx::bulk_load(r.buf + (j % kRing) * kChunk, static_cast<const uint8_t *>(a.x) + off, bytes, bar);
+    issued = j + 1;
+}
+
+template <class In, int GRID, int ROUND, bool RHT, bool AMAX>
+__global__ void __launch_bounds__(kThreads) k_row_staged(Args a, FastDiv bdiv, uint32_t kvb,
+                                                         uint32_t nchunks, uint64_t total_bytes) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ float s_k[256];
+    __shared__ float s_red[kThreads / 32];
+    // start streaming before the tensor-scale prologue so its latency overlaps
+    const RingCtl ring = ring_init(dsm);
+    uint32_t issued = 0, j = 0;
+    if (threadIdx.x == 0)
+        for (uint32_t t = 0; t < kRing; ++t) row_issue<In>(ring, a, t, nchunks, total_bytes, issued);
+    float S_enc = 1.0f;
+    bool folded = false;
+    if (!AMAX)
+        tensor_scale_prologue(a, GRID == kE2M1 ? 6.0f : 3.5f, RHT ? 0.25f : 1.0f, s_k, s_red, S_enc,
+                              GRID == kE1M2 && ROUND == kRTNE, &folded);
+    const uint32_t smask = RHT ? rht_sign_mask(a.rht_seed) : 0u;
+    const Signs sg = row_signs<In>(smask);
+    const uint32_t total_blocks = (uint32_t)(total_bytes / (16 * sizeof(In)));
+    constexpr uint32_t BPC = kChunk / (16 * sizeof(In));
+    const uint32_t nloc = nchunks > blockIdx.x ? (nchunks - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const uint32_t cstride = (uint32_t)(a.kpad / 2), nkt = (uint32_t)a.nkt;
+    float m = 0.0f;
+    bool ok = true;
+    for (; j < nloc; ++j) {
+        if (!ring_wait(ring, j)) { ok = false; break; }
+        const uint32_t i = blockIdx.x + j * gridDim.x;
+        const uint32_t st = ring.buf + (j % kRing) * kChunk;
+        if (sizeof(In) == 2) {
+            // BF16: 512 blocks per chunk, thread t owns blocks t and t + 256 as a packed pair
+            const uint32_t k0 = threadIdx.x, k1 = threadIdx.x + kThreads;
+            const uint32_t g0 = i * BPC + k0, g1 = i * BPC + k1;
+            if (g0 < total_blocks) {
+                const bool has1 = g1 < total_blocks;
+                Raw<__nv_bfloat16> r0, r1;
+                r0.load_shared(st + k0 * 32);
+                if (has1) r1.load_shared(st + k1 * 32); else r1.zero();
+                if (AMAX) {
+                    uint64_t P[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) P[q] = RHT ? pk2(r0.get(q, sg), r1.get(q, sg)) : pk2(r0.get(q), r1.get(q));
+                    if (RHT) {
+#pragma unroll
+                        for (int sg = 1; sg < 16; sg <<= 1) {
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) {
+                                if ((q & sg) == 0) {
+                                    const uint64_t xx = P[q], yy = P[q + sg];
+                                    P[q] = add2(xx, yy);
+                                    P[q + sg] = sub2(xx, yy);
+                                }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        float u0, u1;
+                        upk2(P[q], u0, u1);
+                        m = max_nan(m, max_nan(fabsf(u0), fabsf(u1)));
+                    }
+                } else {
+                    const uint32_t rr0 = fdiv(g0, bdiv), rr1 = fdiv(g1, bdiv);
+                    quant_pair_row<GRID, ROUND, RHT>(a, r0, r1, rr0, g0 - rr0 * kvb, rr1, g1 - rr1 * kvb, has1,
+                                                     sg, S_enc, s_k, cstride, nkt, folded);
+                }
+            }
+        } else {
+            for (uint32_t k = threadIdx.x; k < BPC; k += kThreads) {
+                const uint32_t gb = i * BPC + k;
+                if (gb >= total_blocks) break;
+                Raw<In> raw;
+                raw.load_shared(st + k * 16 * sizeof(In));
+                if (AMAX) {
+                    float lo[8], hi[8];
+                    block_values<In, RHT>(raw, sg, lo, hi);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) m = max_nan(m, max_nan(fabsf(lo[q]), fabsf(hi[q])));
+                } else {
+                    const uint32_t r = fdiv(gb, bdiv);
+                    quant_block_row<In, GRID, ROUND, RHT>(a, raw, r, gb - r * kvb, sg, S_enc, s_k, cstride,
+                                                          nkt, folded);
+                }
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) row_issue<In>(ring, a, j + kRing, nchunks, total_bytes, issued);
+    }
+    if (!ok) {
+        if (threadIdx.x == 0) atomicOr(&g_quant_timeout, 1u);
+        ring_drain(ring, j, issued);
+    }
+    if (AMAX) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int w = 1; w < kThreads / 32; ++w) m = max_nan(m, s_red[w]);
+            a.partials_out[blockIdx.x] = RHT ? m * 0.25f : m;
+        }
+    } else {
+        // padding blocks k/16 .. kpad/16 - 1 of every row, and padding rows
+        const uint32_t nbp = (uint32_t)(a.kpad / 16) - kvb;
+        const uint32_t npad = (uint32_t)a.out_rows * nbp;
+        for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < npad; t += gridDim.x * blockDim.x) {
+            const uint32_t r = t / nbp, b = kvb + (t - r * nbp);
+            *reinterpret_cast<uint2 *>(a.codes + (size_t)r * cstride + b * 8) = make_uint2(0u, 0u);
+            a.scales[scale_offset32(r, b, nkt)] = 0;
+        }
+        zero_pad_rows(a);
+    }
+}
+
+// Column-wise chunks: chunk i = (row block kb, column chunk cc) = 16 rows x
+// CW columns, CW = kChunk / (16 * sizeof(In)); column chunk fastest.
+template <class In>
+__device__ __forceinline__ void col_issue(const RingCtl &r, const Args &a, uint32_t j, uint32_t nchunks,
+                                          uint32_t ncc, uint32_t &issued) {
+    constexpr uint32_t CW = kChunk / (16 * sizeof(In));
+    const uint32_t i = blockIdx.x + j * gridDim.x;
+    if (i >= nchunks) return;
+    const uint32_t kb = i / ncc, cc = i - kb * ncc;
+    const uint32_t c0 = cc * CW;
+    const int64_t left = a.cols - (int64_t)c0;
+    const uint32_t ncols = left < (int64_t)CW ? (uint32_t)left : CW;
+    const uint32_t rowbytes = ncols * sizeof(In);
+    const uint32_t bar = r.bars + 8u * (j % kRing);
+    const uint32_t st = r.buf + (j % kRing) * kChunk;
+    ptx::mbar_arrive_expect_tx(bar, 16 * rowbytes);
+    const In *src = static_cast<const In *>(a.x) + (int64_t)kb * 16 * a.ld + c0;
+    for (int q = 0; q < 16; ++q)
+        ptx::bulk_load(st + q * (CW * sizeof(In)), src + (int64_t)q * a.ld, rowbytes, bar);
+    issued = j + 1;
+}
+
+template <class In, int GRID, int ROUND, bool RHT, bool AMAX>
+__global__ void __launch_bounds__(kThreads) k_col_staged(Args a, uint32_t ncc, uint32_t nchunks) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ float s_k[256];
+    __shared__ float s_red[kThreads / 32];
+    constexpr uint32_t CW = kChunk / (16 * sizeof(In));
+    const RingCtl ring = ring_init(dsm);
+    uint32_t issued = 0, j = 0;
+    if (threadIdx.x == 0)
+        for (uint32_t t = 0; t < kRing; ++t) col_issue<In>(ring, a, t, nchunks, ncc, issued);
+    float S_enc = 1.0f;
+    bool folded = false;
+    if (!AMAX)
+        tensor_scale_prologue(a, GRID == kE2M1 ? 6.0f : 3.5f, RHT ? 0.25f : 1.0f, s_k, s_red, S_enc,
+                              GRID == kE1M2 && ROUND == kRTNE, &folded);
+    const uint32_t smask = RHT ? rht_sign_mask(a.rht_seed) : 0u;
+    const Signs sg = col_signs<In>(smask);
+    const uint32_t nloc = nchunks > blockIdx.x ? (nchunks - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const uint32_t cstride = (uint32_t)(a.kpad / 2), nkt = (uint32_t)a.nkt;
+    float m = 0.0f;
+    bool ok = true;
+    for (; j < nloc; ++j) {
+        if (!ring_wait(ring, j)) { ok = false; break; }
+        const uint32_t i = blockIdx.x + j * gridDim.x;
+        const uint32_t kb = i / ncc, cc = i - kb * ncc;
+        const uint32_t c = cc * CW + 2 * threadIdx.x;
+        if (2 * threadIdx.x < CW && c < (uint32_t)a.cols) {
+            ColRaw<In> raw;
+            raw.load_shared(ring.buf + (j % kRing) * kChunk + 2 * threadIdx.x * sizeof(In), CW * sizeof(In));
+            if (AMAX) {
+                uint64_t P[16];
+                col_values<In, RHT>(raw, sg, P);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    float c0, c1;
+                    upk2(P[q], c0, c1);
+                    m = max_nan(m, max_nan(fabsf(c0), fabsf(c1)));
+                }
+            } else {
+                quant_unit_col<In, GRID, ROUND, RHT>(a, raw, kb, c, true, sg, S_enc, s_k, cstride, nkt, folded);
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) col_issue<In>(ring, a, j + kRing, nchunks, ncc, issued);
+    }
+    if (!ok) {
+        if (threadIdx.x == 0) atomicOr(&g_quant_timeout, 1u);
+        ring_drain(ring, j, issued);
+    }
+    if (AMAX) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int w = 1; w < kThreads / 32; ++w) m = max_nan(m, s_red[w]);
+            a.partials_out[blockIdx.x] = RHT ? m * 0.25f : m;
+        }
+    } else {
+        // padding blocks past the last input row, for every output row
+        const uint32_t kvb = (uint32_t)(a.rows / 16), nbp = (uint32_t)(a.kpad / 16) - kvb;
+        const uint32_t npad = (uint32_t)a.out_rows * nbp;
+        for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < npad; t += gridDim.x * blockDim.x) {
+            const uint32_t r = t / nbp, b = kvb + (t - r * nbp);
+            *reinterpret_cast<uint2 *>(a.codes + (size_t)r * cstride + b * 8) = make_uint2(0u, 0u);
+            a.scales[scale_offset32(r, b, nkt)] = 0;
+        }
+        zero_pad_rows(a);
+    }
 }
 
 // ============================================================= statistics
@@ -484,27 +1199,28 @@ template <class In, bool RHT>
 __global__ void __launch_bounds__(kThreads) k_stats_colwise(Args a, int grid) {
     const float qmax = grid_qmax(grid);
     const float S_dec = *a.tensor_scale;
-    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t smask = RHT ? rht_sign_mask(a.rht_seed) : 0u;
-    const int64_t C = a.cols, R = a.rows;
-    const int64_t ntc = (C + 127) / 128, ntk = (R + 127) / 128;
-    const int64_t cstride = a.kpad / 2;
+    const Signs sg = col_signs<In>(smask);
+    const uint32_t ncp = (uint32_t)(a.cols / 2), nkb = (uint32_t)(a.rows / 16);
+    const uint32_t total = ncp * nkb, cstride = (uint32_t)(a.kpad / 2), nkt = (uint32_t)a.nkt;
+    const In *x = static_cast<const In *>(a.x);
     Acc acc;
-    for (int64_t t = blockIdx.x; t < ntc * ntk; t += gridDim.x) {
-        const int64_t tk = t % ntk, tc = t / ntk;
-        const int64_t kb = tk * 8 + warp;
-        const int64_t r0 = kb * 16;
-        const int64_t c = tc * 128 + lane * 4;
-        if (r0 >= R || c >= C) continue;
-        float v[4][16];
-        col_block<In, RHT>(static_cast<const In *>(a.x), a.ld, r0, c, smask, v);
+    for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < total; u += gridDim.x * blockDim.x) {
+        const uint32_t kb = u / ncp, c = (u - kb * ncp) * 2;
+        ColRaw<In> raw;
+        raw.load(x + (int64_t)kb * 16 * a.ld + c, a.ld);
+        uint64_t P[16];
+        col_values<In, RHT>(raw, sg, P);
+        float v[2][16];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (RHT)
+        for (int i = 0; i < 16; ++i) {
+            upk2(P[i], v[0][i], v[1][i]);
+            if (RHT) { v[0][i] *= 0.25f; v[1][i] *= 0.25f; }
+        }
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[j][i] *= 0.25f;
-            const uint2 w = *reinterpret_cast<const uint2 *>(a.codes + (c + j) * cstride + r0 / 2);
-            const float e = e4m3_to_f32(a.scales[scale_offset(c + j, kb, a.nkt)]);
+        for (int j = 0; j < 2; ++j) {
+            const uint2 w = *reinterpret_cast<const uint2 *>(a.codes + (size_t)(c + j) * cstride + kb * 8);
+            const float e = e4m3_to_f32(a.scales[scale_offset32(c + j, kb, nkt)]);
             acc_block8(acc, &v[j][0], w.x, e, S_dec, grid, qmax);
             acc_block8(acc, &v[j][8], w.y, e, S_dec, grid, qmax);
         }
@@ -565,49 +1281,108 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t *codes, cons
 }
 
 // ================================================================ dispatch
+// Launch of a staged kernel: opt in to the ring's dynamic shared memory once
+// per kernel, persistent grid of the CTAs that fit at once.
+template <class K, class... P>
+cudaError_t launch_staged(K kern, int64_t work_ctas, int *grid_out, cudaStream_t s, P... args) {
+    static std::mutex mu;
+    static std::vector<const void *> done;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (std::find(done.begin(), done.end(), (const void *)kern) == done.end()) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingSmem);
+            if (e != cudaSuccess) return e;
+            done.push_back((const void *)kern);
+        }
+    }
+    const int g = resident_grid(kern, work_ctas, kRingSmem);
+    if (grid_out) *grid_out = g;
+    kern<<<g, kThreads, kRingSmem, s>>>(args...);
+    return cudaGetLastError();
+}
+
+template <class In, int GRID, int ROUND, bool RHT>
+cudaError_t quant_pass(const QuantLaunch &q, const Args &a, bool staged, cudaStream_t s) {
+    const bool col = q.colwise != 0;
+    if (!col) {
+        if (staged) {
+            const uint32_t kvb = (uint32_t)(a.k / 16);
+            const uint64_t tb = (uint64_t)a.rows * a.cols * sizeof(In);
+            const uint32_t nch = (uint32_t)((tb + kChunk - 1) / kChunk);
+            return launch_staged(k_row_staged<In, GRID, ROUND, RHT, false>, nch, nullptr, s, a,
+                                 make_fastdiv(kvb), kvb, nch, tb);
+        }
+        const uint32_t bpr = (uint32_t)(a.kpad / 16), total = (uint32_t)(a.out_rows * bpr);
+        auto kern = k_quant_rowwise<In, GRID, ROUND, RHT>;
+        kern<<<resident_grid(kern, (total + 2 * kThreads - 1) / (2 * kThreads)), kThreads, 0, s>>>(
+            a, make_fastdiv(bpr), bpr, total);
+        return cudaGetLastError();
+    }
+    if (staged) {
+        constexpr uint32_t CW = kChunk / (16 * sizeof(In));
+        const uint32_t ncc = (uint32_t)((a.cols + CW - 1) / CW), nch = (uint32_t)(a.rows / 16) * ncc;
+        return launch_staged(k_col_staged<In, GRID, ROUND, RHT, false>, nch, nullptr, s, a, ncc, nch);
+    }
+    const uint32_t ncp = (uint32_t)(a.cols / 2), ctotal = (uint32_t)((a.kpad / 16) * ncp);
+    auto kern = k_quant_colwise<In, GRID, ROUND, RHT>;
+    kern<<<resident_grid(kern, (ctotal + kThreads - 1) / kThreads), kThreads, 0, s>>>(a, make_fastdiv(ncp), ncp,
+                                                                                        ctotal);
+    return cudaGetLastError();
+}
+
+template <class In, bool RHT>
+cudaError_t amax_pass(const QuantLaunch &q, Args &a, bool staged, cudaStream_t s) {
+    const bool col = q.colwise != 0;
+    int g = 1;
+    cudaError_t e;
+    if (!col) {
+        if (staged) {
+            const uint64_t tb = (uint64_t)a.rows * a.cols * sizeof(In);
+            const uint32_t nch = (uint32_t)((tb + kChunk - 1) / kChunk);
+            e = launch_staged(k_row_staged<In, 0, 0, RHT, true>, nch, &g, s, a, FastDiv{0, 0}, 0u, nch, tb);
+        } else {
+            const uint32_t bpr = (uint32_t)(a.k / 16), total = (uint32_t)(a.out_rows * bpr);
+            auto kern = k_amax_rowwise<In, RHT>;
+            g = resident_grid(kern, (total + 2 * kThreads - 1) / (2 * kThreads));
+            kern<<<g, kThreads, 0, s>>>(a, make_fastdiv(bpr), bpr, total);
+            e = cudaGetLastError();
+        }
+    } else {
+        if (staged) {
+            constexpr uint32_t CW = kChunk / (16 * sizeof(In));
+            const uint32_t ncc = (uint32_t)((a.cols + CW - 1) / CW), nch = (uint32_t)(a.rows / 16) * ncc;
+            e = launch_staged(k_col_staged<In, 0, 0, RHT, true>, nch, &g, s, a, ncc, nch);
+        } else {
+            const uint32_t ncp = (uint32_t)(a.cols / 2), total = (uint32_t)((a.rows / 16) * ncp);
+            auto kern = k_amax_colwise<In, RHT>;
+            g = resident_grid(kern, (total + kThreads - 1) / kThreads);
+            kern<<<g, kThreads, 0, s>>>(a, make_fastdiv(ncp), ncp, total);
+            e = cudaGetLastError();
+        }
+    }
+    a.n_partials = g;
+    return e;
+}
+
 template <class In>
 cudaError_t quantize_typed(const QuantLaunch &q, Args &a, void *ws, cudaStream_t s) {
-    const int sms = num_sms();
     const bool col = q.colwise != 0;
-    // pass 1: tensor amax
+    // The bulk-copy path needs 16-byte pieces: the whole (contiguous) tensor
+    // row-wise, each row segment column-wise.
+    const bool staged = col ? ((a.cols * (int64_t)sizeof(In)) % 16 == 0) : (a.ld == a.cols);
     if (!q.amax_in) {
-        int64_t work;
-        if (!col) work = (a.out_rows * (a.k / 8) + kThreads - 1) / kThreads;
-        else work = ((a.cols + 127) / 128) * ((a.rows + 127) / 128);
-        int g = (int)std::min<int64_t>(std::max<int64_t>(work, 1), (int64_t)sms * 8);
-        if (g > kMaxPartials) g = kMaxPartials;
         a.partials_out = reinterpret_cast<float *>(static_cast<char *>(ws) + kWsPartials);
         a.partials = a.partials_out;
-        a.n_partials = g;
-        if (!col) {
-            if (q.rht) k_amax_rowwise<In, true><<<g, kThreads, 0, s>>>(a);
-            else k_amax_rowwise<In, false><<<g, kThreads, 0, s>>>(a);
-        } else {
-            if (q.rht) k_amax_colwise<In, true><<<g, kThreads, 0, s>>>(a);
-            else k_amax_colwise<In, false><<<g, kThreads, 0, s>>>(a);
-        }
-        cudaError_t err = cudaGetLastError();
-        if (err != cudaSuccess) return err;
+        cudaError_t e = q.rht ? amax_pass<In, true>(q, a, staged, s) : amax_pass<In, false>(q, a, staged, s);
+        if (e != cudaSuccess) return e;
     }
-    // pass 2: quantize
-    int64_t work;
-    if (!col) work = (a.out_rows * (a.kpad / 8) + kThreads - 1) / kThreads;
-    else work = ((a.cols + 127) / 128) * ((a.kpad / 16 + 7) / 8);
-    const int g = (int)std::min<int64_t>(std::max<int64_t>(work, 1), (int64_t)sms * 8);
-#define UFP4_Q(COLW, GRID, ROUND, RHT)                                        \
-    if (col == COLW && q.grid == GRID && q.round == ROUND && (q.rht != 0) == RHT) { \
-        if (COLW) k_quant_colwise<In, GRID, ROUND, RHT><<<g, kThreads, 0, s>>>(a); \
-        else k_quant_rowwise<In, GRID, ROUND, RHT><<<g, kThreads, 0, s>>>(a);     \
-        return cudaGetLastError();                                              \
-    }
-    UFP4_Q(false, kE2M1, kRTNE, false) UFP4_Q(false, kE2M1, kRTNE, true)
-    UFP4_Q(false, kE2M1, kSR, false)   UFP4_Q(false, kE2M1, kSR, true)
-    UFP4_Q(false, kE1M2, kRTNE, false) UFP4_Q(false, kE1M2, kRTNE, true)
-    UFP4_Q(false, kE1M2, kSR, false)   UFP4_Q(false, kE1M2, kSR, true)
-    UFP4_Q(true, kE2M1, kRTNE, false)  UFP4_Q(true, kE2M1, kRTNE, true)
-    UFP4_Q(true, kE2M1, kSR, false)    UFP4_Q(true, kE2M1, kSR, true)
-    UFP4_Q(true, kE1M2, kRTNE, false)  UFP4_Q(true, kE1M2, kRTNE, true)
-    UFP4_Q(true, kE1M2, kSR, false)    UFP4_Q(true, kE1M2, kSR, true)
+#define UFP4_Q(GRID, ROUND, RHT)                                                   \
+    if (q.grid == GRID && q.round == ROUND && (q.rht != 0) == RHT)                 \
+        return quant_pass<In, GRID, ROUND, RHT>(q, a, staged, s);
+    UFP4_Q(kE2M1, kRTNE, false) UFP4_Q(kE2M1, kRTNE, true)
+    UFP4_Q(kE2M1, kSR, false)   UFP4_Q(kE2M1, kSR, true)
+    UFP4_Q(kE1M2, kRTNE, false) UFP4_Q(kE1M2, kRTNE, true)
+    UFP4_Q(kE1M2, kSR, false)   UFP4_Q(kE1M2, kSR, true)
 #undef UFP4_Q
     return cudaErrorInvalidValue;
 }
@@ -640,6 +1415,18 @@ int num_sms() {
     return cached[dev];
 }
 
+cudaError_t read_quant_timeout_flag(uint32_t *flag, cudaStream_t s) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(flag, g_quant_timeout, sizeof(uint32_t), 0,
+                                              cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && *flag) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_quant_timeout, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    return e;
+}
+
 cudaError_t launch_quantize(const QuantLaunch &q, void *ws, cudaStream_t s) {
     Args a = make_args(q, ws);
     if (q.dtype == 0) return quantize_typed<__nv_bfloat16>(q, a, ws, s);
@@ -662,7 +1449,7 @@ cudaError_t launch_stats(const QuantLaunch &q, void *ws, int *n_ctas, cudaStream
     const bool col = q.colwise != 0;
     int64_t work;
     if (!col) work = (a.out_rows * (a.k / 8) + kThreads - 1) / kThreads;
-    else work = ((a.cols + 127) / 128) * ((a.rows + 127) / 128);
+    else work = ((a.cols / 2) * (a.rows / 16) + kThreads - 1) / kThreads;
     const int g = (int)std::min<int64_t>(std::max<int64_t>(work, 1),
                                          std::min<int64_t>((int64_t)num_sms() * 4, kMaxStatsCtas));
     *n_ctas = g;
