@@ -470,6 +470,49 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_kernel(args):
+    """One kernel of the step in isolation, for profiling: `steps` launches
+    of the fwd_y GEMM (8192 x 5632 x 2048) or of the RHT quantization of X
+    (8192 x 2048), after `warmup` launches.  Prints the mean event time."""
+    import torch
+    from fp4_quantized_numerics_gb300 import build, inputs, ufp4 as U
+    build.build()
+    dev = torch.device("cuda", 0)
+    T, H, F = WORKLOAD["tokens"], WORKLOAD["hidden"], WORKLOAD["ffn"]
+    x = inputs.device_normal((T, H), 1.0, 21, dev)
+    kind = args.kernel
+    if kind.startswith("gemm"):
+        grid = U.UFP4_E2M1 if kind == "gemm_e2m1" else U.UFP4_E1M2
+        w = inputs.device_normal((F, H), 0.02, 22, dev)
+        a, b = U.ufp4_quantize(x, grid, rht=True), U.ufp4_quantize(w, grid, rht=True)
+        c = torch.empty(T, F, dtype=torch.float32, device=dev)
+        fn = lambda: U.ufp4_gemm(a, b, out=c)
+        work = 2.0 * T * F * H
+        unit = "TFLOP/s"
+    else:
+        grid = U.UFP4_E2M1 if kind.endswith("e2m1") else U.UFP4_E1M2
+        col = kind.startswith("quant_col")
+        q = U.QTensor.empty(H if col else T, T if col else H, grid, dev)
+        am = torch.tensor([float(x.float().abs().max()) * 1.5], device=dev)
+        fn = lambda: U.ufp4_quantize(x, grid, rht=True, colwise=col, out=q, amax_in=am)
+        work = x.numel() * Q_BYTES_PER_ELEM
+        unit = "GB/s"
+    flush = L2Flush(dev)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    tot = 0.0
+    for _ in range(args.steps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(); fn(); e1.record()
+        torch.cuda.synchronize()
+        tot += e0.elapsed_time(e1)
+    ms = tot / args.steps
+    rate = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+    print(json.dumps({"kernel": kind, "ms": round(ms, 4), "rate": round(rate, 1), "unit": unit}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -479,11 +522,17 @@ def main():
     ap.add_argument("--quick", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", default=None,
+                    choices=["gemm_e2m1", "gemm_e1m2", "quant_row_e1m2", "quant_col_e1m2",
+                             "quant_row_e2m1", "quant_col_e2m1"],
+                    help="time one kernel of the step in isolation (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.kernel:
+        run_kernel(args)
     else:
         run_gpu(args)
 

@@ -52,9 +52,13 @@ constexpr long long kWaitBudget = 2000000000LL;
 
 template <int GRID>
 struct Cfg {
-    static constexpr int kStages = GRID == kE2M1 ? 6 : 3;
-    // warps: 0 producer, 1 MMA, 2-5 epilogue, (E1M2) 6-9 expanders
-    static constexpr int kThreads = GRID == kE2M1 ? 192 : 320;
+    static constexpr int kStages = GRID == kE2M1 ? 5 : 3;
+    // warps: 0 producer, 1 MMA, 2-5 epilogue, (E1M2) 6-13 expanders
+    static constexpr int kThreads = GRID == kE2M1 ? 192 : 448;
+    static constexpr int kExpThreads = kThreads - 192;
+    // epilogue staging: per epilogue warp, kEpiBufs buffers of 32 rows x 32
+    // fp32 columns (4 KB, 128-byte swizzled rows) feeding TMA stores
+    static constexpr int kEpiBufs = GRID == kE2M1 ? 2 : 1;
     // stage layout: A | B | (A_lo | B_lo for E1M2) | SFA | SFB
     static constexpr uint32_t kAOff = 0;
     static constexpr uint32_t kBOff = TILE_BYTES;
@@ -63,7 +67,8 @@ struct Cfg {
     static constexpr uint32_t kSfaOff = (GRID == kE2M1 ? 2 : 4) * TILE_BYTES;
     static constexpr uint32_t kSfbOff = kSfaOff + SF_BYTES;
     static constexpr uint32_t kStageBytes = kSfbOff + SF_BYTES;  // multiple of 1024
-    static constexpr uint32_t kBarOff = kStages * kStageBytes;
+    static constexpr uint32_t kEpiOff = kStages * kStageBytes;
+    static constexpr uint32_t kBarOff = kEpiOff + 4 * kEpiBufs * 4096;
     static constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;  // + barriers + alignment slack
 };
 
@@ -97,14 +102,13 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     }
 }
 
-// E1M2 nibbles -> (hi, lo) E2M1 nibbles, 8 at a time (see file header).
+// E1M2 nibbles s|m2 m1 m0 -> (hi, lo) E2M1 nibbles, 8 at a time.  With
+// a = m >> 1, the E2M1 code of a in {0,1,2,3} is {0,2,4,5} = 2a - [a == 3];
+// 2a sits in bits 2..1 already, so hi = (w & 0xE...) - (m1 & m2) (no borrow
+// leaves a nibble); lo keeps the sign and m0 (E2M1 code 1 = 0.5).
 __device__ __forceinline__ void split_e1m2(uint32_t w, uint32_t &hi, uint32_t &lo) {
-    const uint32_t s = w & 0x88888888u;
-    const uint32_t m2 = (w >> 2) & 0x11111111u;
-    const uint32_t m1 = (w >> 1) & 0x11111111u;
-    const uint32_t m0 = w & 0x11111111u;
-    hi = s | (m2 << 2) | ((m1 & ~m2) << 1) | (m1 & m2);
-    lo = s | m0;
+    hi = (w & 0xEEEEEEEEu) - ((w >> 1) & (w >> 2) & 0x11111111u);
+    lo = w & 0x99999999u;
 }
 
 // Persistent CTA: tiles t = blockIdx.x, blockIdx.x + gridDim.x, ... in
@@ -114,7 +118,7 @@ __device__ __forceinline__ void split_e1m2(uint32_t w, uint32_t &hi, uint32_t &l
 template <int GRID>
 __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-           GemmParams p) {
+           const __grid_constant__ CUtensorMap tma_c, GemmParams p) {
     using C = Cfg<GRID>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -140,7 +144,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(full(s), 1);
             ptx::mbar_init(empty(s), 1);
-            ptx::mbar_init(expd(s), 4);   // one arrival per expander warp
+            ptx::mbar_init(expd(s), GRID == kE1M2 ? C::kExpThreads / 32 : 1);   // one arrival per expander warp
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accf(b), 1);
@@ -151,6 +155,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tma_a);
         ptx::prefetch_tmap(&tma_b);
+        ptx::prefetch_tmap(&tma_c);
     }
     if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
@@ -243,9 +248,14 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         }
     } else if (warp < 6) {
         // ------------------------------------------------------------ epilogue
+        // TMEM -> registers (x alpha) -> swizzled shared staging -> TMA store.
+        // Each warp owns 32 accumulator rows; a 32 x 32 fp32 box per store, so
+        // global writes are whole lines and ragged tile edges are clipped by
+        // the tensor map.
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
         const float alpha = __fmul_rn(*p.ts_a, *p.ts_b);
-        uint32_t it = 0;
+        const uint32_t ebase = smem_base + C::kEpiOff + (uint32_t)(warp - 2) * C::kEpiBufs * 4096u;
+        uint32_t it = 0, nst = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
             const uint32_t b = it & 1, use = it >> 1;
             bool ok = wait_or_abort(accf(b), use & 1, abort);
@@ -253,36 +263,45 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
             if (!ok) break;
             ptx::tc_fence_after();
             const int m0 = (t / p.ntn) * BM, n0 = (t % p.ntn) * BN;
-            const int row = m0 + 32 * q + lane;
-            float *crow = p.c + (int64_t)row * p.ldc;
 #pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch) {
+            for (int ch = 0; ch < BN / 32; ++ch, ++nst) {
                 uint32_t r[32];
                 ptx::tc_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + b * BN + 32u * ch, r);
+                const uint32_t buf = ebase + (nst % C::kEpiBufs) * 4096u;
+                // the store that last read this buffer must be done reading it
+                if (lane == 0) {
+                    if (C::kEpiBufs == 2) ptx::bulk_wait_read<1>();
+                    else ptx::bulk_wait_read<0>();
+                }
+                __syncwarp();
                 ptx::tc_wait_ld();
-                const int col0 = n0 + 32 * ch;
-                if (row < p.M) {
-                    if (col0 + 32 <= p.N) {
+                if (ch == BN / 32 - 1) {   // accumulator fully read: hand it back to the MMA warp
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(acce(b));
+                }
+                const uint32_t rowb = buf + (uint32_t)lane * 128u;
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            const float4 v = make_float4(__uint_as_float(r[i]) * alpha, __uint_as_float(r[i + 1]) * alpha,
-                                                         __uint_as_float(r[i + 2]) * alpha,
-                                                         __uint_as_float(r[i + 3]) * alpha);
-                            *reinterpret_cast<float4 *>(crow + col0 + i) = v;
-                        }
-                    } else {
-                        for (int i = 0; i < 32; ++i)
-                            if (col0 + i < p.N) crow[col0 + i] = __uint_as_float(r[i]) * alpha;
-                    }
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t addr = rowb + (uint32_t)((c ^ (lane & 7)) << 4);
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                                 "f"(__uint_as_float(r[4 * c]) * alpha), "f"(__uint_as_float(r[4 * c + 1]) * alpha),
+                                 "f"(__uint_as_float(r[4 * c + 2]) * alpha), "f"(__uint_as_float(r[4 * c + 3]) * alpha)
+                                 : "memory");
+                }
+                ptx::fence_proxy_async();
+                __syncwarp();
+                if (lane == 0 && m0 + 32 * q < p.M && n0 + 32 * ch < p.N) {   // boxes wholly outside C: skip
+                    ptx::tma_store_2d(&tma_c, n0 + 32 * ch, m0 + 32 * q, buf);
+                    ptx::bulk_commit();
                 }
             }
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(acce(b));
         }
-    } else {
+        if (lane == 0) ptx::bulk_wait_all();
+        __syncwarp();
+    } else if constexpr (GRID == kE1M2) {
         // ------------------------------------------------- E1M2 expanders
-        const int et = threadIdx.x - 192;   // 0..127
+        const int et = threadIdx.x - 192;   // 0 .. kExpThreads-1
         uint32_t g = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
@@ -293,7 +312,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                 if (!ok) break;
                 uint8_t *st = smem + s * C::kStageBytes;
 #pragma unroll 4
-                for (int i = et; i < (int)(TILE_BYTES / 16); i += 128) {
+                for (int i = et; i < (int)(TILE_BYTES / 16); i += C::kExpThreads) {
                     uint4 *pa = reinterpret_cast<uint4 *>(st + C::kAOff) + i;
                     uint4 *pb = reinterpret_cast<uint4 *>(st + C::kBOff) + i;
                     uint4 a = *pa, bv = *pb, ah, alo, bh, blo;
@@ -350,8 +369,22 @@ bool make_code_map(CUtensorMap *m, const uint8_t *codes, int64_t rows, int64_t k
     return r == CUDA_SUCCESS;
 }
 
+bool make_out_map(CUtensorMap *m, float *c, int64_t M, int64_t N, int64_t ldc) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)(ldc * 4)};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, c, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <int GRID>
-cudaError_t run_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const GemmParams &p, cudaStream_t s) {
+cudaError_t run_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc, const GemmParams &p,
+                     cudaStream_t s) {
     using C = Cfg<GRID>;
     static bool attr_set[64] = {false};
     int dev = 0;
@@ -366,7 +399,7 @@ cudaError_t run_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const GemmPar
     if (!sms) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int ntiles = p.ntm * p.ntn;
     const int grid = ntiles < sms ? ntiles : sms;
-    k_gemm<GRID><<<grid, C::kThreads, C::kSmemBytes, s>>>(ma, mb, p);
+    k_gemm<GRID><<<grid, C::kThreads, C::kSmemBytes, s>>>(ma, mb, mc, p);
     return cudaGetLastError();
 }
 
@@ -377,8 +410,9 @@ cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const f
                         int64_t N, int64_t K, int grid, float *c, int64_t ldc, cudaStream_t s) {
     if (K == 0) return cudaMemset2DAsync(c, ldc * sizeof(float), 0, N * sizeof(float), M, s);
     const int64_t kpad = kpad_of(K);
-    CUtensorMap ma, mb;
-    if (!make_code_map(&ma, a_codes, M, kpad) || !make_code_map(&mb, b_codes, N, kpad))
+    CUtensorMap ma, mb, mc;
+    if (!make_code_map(&ma, a_codes, M, kpad) || !make_code_map(&mb, b_codes, N, kpad) ||
+        !make_out_map(&mc, c, M, N, ldc))
         return cudaErrorInvalidValue;
     GemmParams p{};
     p.sfa = a_scales; p.sfb = b_scales; p.ts_a = a_ts; p.ts_b = b_ts;
@@ -387,8 +421,8 @@ cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const f
     p.num_kb = (p.nkt + 3) / 4;
     p.ntm = (int)((M + BM - 1) / BM);
     p.ntn = (int)((N + BN - 1) / BN);
-    if (grid == kE2M1) return run_gemm<kE2M1>(ma, mb, p, s);
-    return run_gemm<kE1M2>(ma, mb, p, s);
+    if (grid == kE2M1) return run_gemm<kE2M1>(ma, mb, mc, p, s);
+    return run_gemm<kE1M2>(ma, mb, mc, p, s);
 }
 
 cudaError_t read_timeout_flag(uint32_t *flag, cudaStream_t s) {
