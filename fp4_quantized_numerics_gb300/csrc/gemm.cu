@@ -196,11 +196,17 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         }
     } else if (warp == 1) {
         // --------------------------------------------------------- MMA issuer
+        // One thread issues every tcgen05 op of the CTA, so its instruction
+        // stream is kept short: descriptors are built once per stage and
+        // advanced by integer adds (start address field = bytes >> 4).
         if (lane == 0) {
             // instruction descriptor, kind::mxf4nvf4: A/B E2M1 (1), K-major,
             // N >> 3 at [17,23), UE4M3 scales (bit 23 = 0), M >> 4 at [24,29).
             const uint32_t idesc = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                                    ((uint32_t)(BM >> 4) << 24);
+            const uint64_t hi_op = ptx::sdesc(0, 16, 1024, 2);   // 128B-swizzled K-major operand
+            const uint64_t hi_sf = ptx::sdesc(0, 0, 128, 0);     // 32 rows x 16 B scale atom
+            auto mk = [](uint64_t hi, uint32_t addr) { return hi | (uint64_t)((addr & 0x3FFFFu) >> 4); };
             uint32_t g = 0, it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
@@ -215,26 +221,34 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                     const int atoms = min(4, p.nkt - 4 * kb);
                     const uint32_t st = smem_base + s * C::kStageBytes;
                     const uint32_t sf_t = tmem + kSfCol + 32u * s;
-                    for (int j = 0; j < atoms; ++j) {
-                        ptx::tc_cp_32x128b_warpx4(sf_t + 4u * j, ptx::sdesc(st + C::kSfaOff + 512u * j, 0, 128, 0));
-                        ptx::tc_cp_32x128b_warpx4(sf_t + 16u + 4u * j,
-                                                  ptx::sdesc(st + C::kSfbOff + 512u * j, 0, 128, 0));
-                    }
-                    for (int j = 0; j < atoms; ++j) {
+                    const uint64_t dsa = mk(hi_sf, st + C::kSfaOff), dsb = mk(hi_sf, st + C::kSfbOff);
+                    const uint64_t dah = mk(hi_op, st + C::kAOff), dbh = mk(hi_op, st + C::kBOff);
+                    const uint64_t dal = mk(hi_op, st + C::kALoOff), dbl = mk(hi_op, st + C::kBLoOff);
+                    auto step = [&](int j) {
                         const uint32_t sfa = sf_t + 4u * j, sfb = sf_t + 16u + 4u * j;
                         const uint32_t first = (kb == 0 && j == 0) ? 0u : 1u;
-                        const uint32_t ah = st + C::kAOff + 32u * j, bh = st + C::kBOff + 32u * j;
-                        ptx::tc_mma_nvf4(acc, ptx::sdesc(ah, 16, 1024, 2), ptx::sdesc(bh, 16, 1024, 2), idesc, sfa,
-                                         sfb, first);
+                        const uint64_t o = 2u * (uint32_t)j;   // +32 bytes per 64-element K step
+                        ptx::tc_mma_nvf4(acc, dah + o, dbh + o, idesc, sfa, sfb, first);
                         if (GRID == kE1M2) {
-                            const uint32_t al = st + C::kALoOff + 32u * j, bl = st + C::kBLoOff + 32u * j;
-                            ptx::tc_mma_nvf4(acc, ptx::sdesc(ah, 16, 1024, 2), ptx::sdesc(bl, 16, 1024, 2), idesc,
-                                             sfa, sfb, 1u);
-                            ptx::tc_mma_nvf4(acc, ptx::sdesc(al, 16, 1024, 2), ptx::sdesc(bh, 16, 1024, 2), idesc,
-                                             sfa, sfb, 1u);
-                            ptx::tc_mma_nvf4(acc, ptx::sdesc(al, 16, 1024, 2), ptx::sdesc(bl, 16, 1024, 2), idesc,
-                                             sfa, sfb, 1u);
+                            ptx::tc_mma_nvf4(acc, dah + o, dbl + o, idesc, sfa, sfb, 1u);
+                            ptx::tc_mma_nvf4(acc, dal + o, dbh + o, idesc, sfa, sfb, 1u);
+                            ptx::tc_mma_nvf4(acc, dal + o, dbl + o, idesc, sfa, sfb, 1u);
                         }
+                    };
+                    if (atoms == 4) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            ptx::tc_cp_32x128b_warpx4(sf_t + 4u * j, dsa + 32u * j);
+                            ptx::tc_cp_32x128b_warpx4(sf_t + 16u + 4u * j, dsb + 32u * j);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) step(j);
+                    } else {
+                        for (int j = 0; j < atoms; ++j) {
+                            ptx::tc_cp_32x128b_warpx4(sf_t + 4u * j, dsa + 32u * j);
+                            ptx::tc_cp_32x128b_warpx4(sf_t + 16u + 4u * j, dsb + 32u * j);
+                        }
+                        for (int j = 0; j < atoms; ++j) step(j);
                     }
                     ptx::tc_commit(empty(s));
                 }
