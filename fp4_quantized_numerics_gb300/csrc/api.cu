@@ -10,6 +10,8 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstring>
+#include <memory>
 #include <mutex>
 #include <vector>
 
@@ -150,6 +152,122 @@ ufp4_status ufp4_gemm(const ufp4_qtensor *a, const ufp4_qtensor *b, float *c, in
     return from_cuda(launch_gemm(a->codes, a->scales, a->tensor_scale, b->codes, b->scales,
                                  b->tensor_scale, M, N, K, a->grid, c, ldc,
                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int64_t ufp4_grouped_rows(const int64_t *seg_rows, int32_t n_seg) {
+    if (!seg_rows || n_seg <= 0) return 0;
+    int64_t t = 0;
+    for (int i = 0; i < n_seg; ++i) t += seg_rows[i] > 0 ? rpad_of(seg_rows[i]) : 0;
+    return t;
+}
+
+int64_t ufp4_grouped_kpad(const int64_t *seg_rows, int32_t n_seg) {
+    if (!seg_rows || n_seg <= 0) return 0;
+    int64_t t = 0;
+    for (int i = 0; i < n_seg; ++i) t += seg_rows[i] > 0 ? kpad_of(seg_rows[i]) : 0;
+    return t;
+}
+
+ufp4_status ufp4_quantize_grouped(const void *x, int32_t dtype, int64_t cols, int64_t ld,
+                                  const int64_t *seg_rows, int32_t n_seg, const ufp4_qparams *p,
+                                  const ufp4_qtensor *out, void *workspace, size_t workspace_bytes,
+                                  ufp4_stream_t stream) {
+    if (!p || !out || !seg_rows || n_seg < 1 || n_seg > kMaxGroups) return UFP4_ERR_INVALID;
+    if (p->amax_in) return UFP4_ERR_INVALID;
+    int64_t total = 0;
+    for (int i = 0; i < n_seg; ++i) {
+        if (seg_rows[i] < 0) return UFP4_ERR_INVALID;
+        total += seg_rows[i];
+    }
+    // shape checks through the common validator (k = Σ kpad for column-wise)
+    const int64_t kcol = ufp4_grouped_kpad(seg_rows, n_seg);
+    const int64_t out_rows = p->colwise ? cols : ufp4_grouped_rows(seg_rows, n_seg);
+    const int64_t k = p->colwise ? kcol : cols;
+    if (!valid_qtensor(out) || out->grid != p->grid || out->rows != out_rows || out->k != k)
+        return UFP4_ERR_INVALID;
+    if (dtype != UFP4_BF16 && dtype != UFP4_FP32) return UFP4_ERR_INVALID;
+    if (p->block != UFP4_BLOCK) return UFP4_ERR_UNSUPPORTED;
+    if (p->grid != UFP4_E2M1 && p->grid != UFP4_E1M2) return UFP4_ERR_INVALID;
+    if (p->round != UFP4_RTNE && p->round != UFP4_SR) return UFP4_ERR_INVALID;
+    if ((p->rht != 0 && p->rht != 1) || (p->colwise != 0 && p->colwise != 1) || p->reserved != 0)
+        return UFP4_ERR_INVALID;
+    if (cols < 0 || ld < cols) return UFP4_ERR_INVALID;
+    if (!p->colwise && cols % UFP4_BLOCK != 0) return UFP4_ERR_INVALID;
+    if (p->colwise && cols % 4 != 0) return UFP4_ERR_INVALID;
+    const size_t esz = dtype == UFP4_BF16 ? 2 : 4;
+    if (total > 0 && cols > 0 && (!x || !aligned(x, 16) || (ld * (int64_t)esz) % 16 != 0)) return UFP4_ERR_INVALID;
+    if (!valid_workspace(workspace, workspace_bytes)) return UFP4_ERR_INVALID;
+    if (kWsPartials + (size_t)n_seg * 4 > kWsStats) return UFP4_ERR_INVALID;
+    if (total == 0 || cols == 0 || out_rows == 0 || k == 0) return UFP4_OK;
+    if (total > (int64_t)INT32_MAX) return UFP4_ERR_UNSUPPORTED;
+
+    GroupQuant gt;
+    memset(&gt, 0, sizeof gt);
+    gt.n = n_seg;
+    gt.colwise = p->colwise;
+    const int64_t kpadc = kpad_of(cols);
+    for (int i = 0; i < n_seg; ++i) {
+        const int64_t T = seg_rows[i];
+        gt.in_row[i + 1] = gt.in_row[i] + T;
+        if (!p->colwise) {
+            gt.out_off[i] = i == 0 ? 0 : gt.out_off[i - 1] + (seg_rows[i - 1] > 0 ? rpad_of(seg_rows[i - 1]) : 0);
+            gt.units[i + 1] = gt.units[i] + (T > 0 ? rpad_of(T) : 0) * (kpadc / 16);
+        } else {
+            gt.out_off[i] = i == 0 ? 0 : gt.out_off[i - 1] + (seg_rows[i - 1] > 0 ? kpad_of(seg_rows[i - 1]) : 0);
+            gt.units[i + 1] = gt.units[i] + (T > 0 ? kpad_of(T) / 16 : 0) * (cols / 2);
+        }
+    }
+    if (gt.units[n_seg] > (int64_t)INT32_MAX * 2) return UFP4_ERR_UNSUPPORTED;
+    QuantLaunch q{};
+    q.x = x; q.dtype = dtype; q.rows = total; q.cols = cols; q.ld = ld;
+    q.grid = p->grid; q.rht = p->rht; q.round = p->round; q.colwise = p->colwise;
+    q.rht_seed = p->rht_seed; q.sr_seed = p->sr_seed; q.sr_counter = p->sr_counter;
+    q.codes = out->codes; q.scales = out->scales; q.tensor_scale = out->tensor_scale;
+    q.out_rows = out_rows; q.k = k;
+    return from_cuda(launch_quantize_grouped(q, gt, workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ufp4_status ufp4_gemm_grouped(const ufp4_qtensor *a, const ufp4_qtensor *b, const ufp4_gemm_group *groups,
+                              int32_t n, ufp4_stream_t stream) {
+    if (!valid_qtensor(a) || !valid_qtensor(b) || !groups || n < 0 || n > kMaxGroups) return UFP4_ERR_INVALID;
+    if (a->grid != b->grid) return UFP4_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    std::unique_ptr<GroupGemmTab> tab(new GroupGemmTab());
+    memset(tab.get(), 0, sizeof(GroupGemmTab));
+    int m = 0;
+    int64_t tiles = 0;
+    for (int i = 0; i < n; ++i) {
+        const ufp4_gemm_group &g = groups[i];
+        if (g.M < 0 || g.N < 0 || g.K < 0 || g.K % UFP4_BLOCK != 0) return UFP4_ERR_INVALID;
+        if (g.M == 0 || g.N == 0) continue;
+        if (!g.c || !aligned(g.c, 16) || g.ldc < g.N || g.ldc % 4 != 0) return UFP4_ERR_INVALID;
+        if (g.a_row % 128 || g.b_row % 128 || g.a_k % 64 || g.b_k % 64) return UFP4_ERR_INVALID;
+        if (g.a_row < 0 || g.b_row < 0 || g.a_k < 0 || g.b_k < 0) return UFP4_ERR_INVALID;
+        if (g.a_row + g.M > a->rows || g.b_row + g.N > b->rows) return UFP4_ERR_INVALID;
+        if (g.a_k + g.K > kpad_of(a->k) || g.b_k + g.K > kpad_of(b->k)) return UFP4_ERR_INVALID;
+        if (g.a_seg < 0 || g.b_seg < 0) return UFP4_ERR_INVALID;
+        if (g.K == 0) {
+            cudaError_t e = cudaMemset2DAsync(g.c, g.ldc * sizeof(float), 0, g.N * sizeof(float), g.M, s);
+            if (e != cudaSuccess) return UFP4_ERR_CUDA;
+            continue;
+        }
+        GroupGemm &t = tab->g[m];
+        t.M = (int32_t)g.M; t.N = (int32_t)g.N;
+        t.nkt = (int32_t)(kpad_of(g.K) / 64);
+        t.ntn = (int32_t)((g.N + 127) / 128);
+        t.a_rt = (int32_t)(g.a_row / 128); t.a_kt = (int32_t)(g.a_k / 64);
+        t.b_rt = (int32_t)(g.b_row / 128); t.b_kt = (int32_t)(g.b_k / 64);
+        t.a_seg = g.a_seg; t.b_seg = g.b_seg;
+        t.c = g.c; t.ldc = g.ldc;
+        tiles += (int64_t)((g.M + 127) / 128) * t.ntn;
+        if (tiles > INT32_MAX) return UFP4_ERR_UNSUPPORTED;
+        ++m;
+        tab->tiles[m] = (int32_t)tiles;
+    }
+    tab->n = m;
+    if (m == 0) return UFP4_OK;
+    return from_cuda(launch_gemm_grouped(a->codes, a->scales, a->tensor_scale, a->rows, kpad_of(a->k), b->codes,
+                                         b->scales, b->tensor_scale, b->rows, kpad_of(b->k), a->grid, *tab, s));
 }
 
 ufp4_status ufp4_stats(const void *x, int32_t dtype, int64_t rows, int64_t cols, int64_t ld,

@@ -34,7 +34,9 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
+#include <type_traits>
 
 namespace ufp4 {
 
@@ -81,7 +83,65 @@ struct GemmParams {
     int nkt;      // kpad / 64: scale atoms per 128-row tile
     int num_kb;   // ceil(nkt / 4): K stages per tile
     int ntm, ntn; // tiles along M and N
+    int nkt_a, nkt_b;  // k atoms per 128-row tile of the whole A / B tensors
 };
+
+// Where one output tile lives: operand rows / k atoms in the A and B tensors,
+// its problem's sizes, output pointer and tensor scales.
+struct TileInfo {
+    int a_row, b_row, a_kt, b_kt, nkt, num_kb;
+    int m_loc, n_loc, M, N;
+    float *c;
+    int64_t ldc;
+    const float *ts_a, *ts_b;
+};
+
+struct NoGroups {};
+
+__device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const NoGroups &, int t) {
+    TileInfo ti;
+    ti.m_loc = (t / p.ntn) * BM;
+    ti.n_loc = (t % p.ntn) * BN;
+    ti.a_row = ti.m_loc;
+    ti.b_row = ti.n_loc;
+    ti.a_kt = 0;
+    ti.b_kt = 0;
+    ti.nkt = p.nkt;
+    ti.num_kb = p.num_kb;
+    ti.M = p.M;
+    ti.N = p.N;
+    ti.c = p.c;
+    ti.ldc = p.ldc;
+    ti.ts_a = p.ts_a;
+    ti.ts_b = p.ts_b;
+    return ti;
+}
+
+__device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const GroupGemmTab &tab, int t) {
+    int lo = 0, hi = tab.n;   // largest g with tiles[g] <= t
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (tab.tiles[mid] <= t) lo = mid; else hi = mid;
+    }
+    const GroupGemm &g = tab.g[lo];
+    const int lt = t - tab.tiles[lo];
+    TileInfo ti;
+    ti.m_loc = (lt / g.ntn) * BM;
+    ti.n_loc = (lt % g.ntn) * BN;
+    ti.a_row = g.a_rt * 128 + ti.m_loc;
+    ti.b_row = g.b_rt * 128 + ti.n_loc;
+    ti.a_kt = g.a_kt;
+    ti.b_kt = g.b_kt;
+    ti.nkt = g.nkt;
+    ti.num_kb = (g.nkt + 3) / 4;
+    ti.M = g.M;
+    ti.N = g.N;
+    ti.c = g.c;
+    ti.ldc = g.ldc;
+    ti.ts_a = p.ts_a + g.a_seg;
+    ti.ts_b = p.ts_b + g.b_seg;
+    return ti;
+}
 
 __device__ __forceinline__ void raise_timeout() { atomicOr(&g_ufp4_timeout, 1u); }
 
@@ -115,10 +175,11 @@ __device__ __forceinline__ void split_e1m2(uint32_t w, uint32_t &hi, uint32_t &l
 // row-major (M, N) tile order.  The K ring and the two TMEM accumulators are
 // carried across tiles, so the epilogue of one tile overlaps the main loop
 // of the next.
-template <int GRID>
+template <int GRID, class TAB>
 __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-           const __grid_constant__ CUtensorMap tma_c, GemmParams p) {
+           const __grid_constant__ CUtensorMap tma_c, GemmParams p, const __grid_constant__ TAB tab) {
+    constexpr bool kGrouped = std::is_same<TAB, GroupGemmTab>::value;
     using C = Cfg<GRID>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -138,7 +199,9 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
     const uint32_t drained = bar_base + 8u * (3 * S + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ntiles = p.ntm * p.ntn;
+    int ntiles;
+    if constexpr (kGrouped) ntiles = tab.tiles[tab.n];
+    else ntiles = p.ntm * p.ntn;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -172,18 +235,20 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
             uint32_t g = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const int m0 = (t / p.ntn) * BM, n0 = (t % p.ntn) * BN;
-                for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
+                const TileInfo ti = tile_info(p, tab, t);
+                for (int kb = 0; kb < ti.num_kb; ++kb, ++g) {
                     const uint32_t s = g % S, round = g / S;
                     if (round > 0 && !wait_or_abort(empty(s), (round - 1) & 1, abort)) { ok = false; break; }
-                    const int atoms = min(4, p.nkt - 4 * kb);
+                    const int atoms = min(4, ti.nkt - 4 * kb);
                     const uint32_t st = smem_base + s * C::kStageBytes;
                     ptx::mbar_arrive_expect_tx(full(s), 2 * TILE_BYTES + 2u * atoms * 512u);
-                    ptx::tma_load_2d(st + C::kAOff, &tma_a, kb * BK_BYTES, m0, full(s));
-                    ptx::tma_load_2d(st + C::kBOff, &tma_b, kb * BK_BYTES, n0, full(s));
-                    ptx::bulk_load(st + C::kSfaOff, p.sfa + ((size_t)(m0 / 128) * p.nkt + 4 * kb) * 512,
+                    ptx::tma_load_2d(st + C::kAOff, &tma_a, ti.a_kt * 32 + kb * BK_BYTES, ti.a_row, full(s));
+                    ptx::tma_load_2d(st + C::kBOff, &tma_b, ti.b_kt * 32 + kb * BK_BYTES, ti.b_row, full(s));
+                    ptx::bulk_load(st + C::kSfaOff,
+                                   p.sfa + ((size_t)(ti.a_row / 128) * p.nkt_a + ti.a_kt + 4 * kb) * 512,
                                    atoms * 512u, full(s));
-                    ptx::bulk_load(st + C::kSfbOff, p.sfb + ((size_t)(n0 / 128) * p.nkt + 4 * kb) * 512,
+                    ptx::bulk_load(st + C::kSfbOff,
+                                   p.sfb + ((size_t)(ti.b_row / 128) * p.nkt_b + ti.b_kt + 4 * kb) * 512,
                                    atoms * 512u, full(s));
                 }
             }
@@ -210,15 +275,16 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
             uint32_t g = 0, it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
+                const TileInfo ti = tile_info(p, tab, t);
                 const uint32_t b = it & 1, use = it >> 1;
                 if (use > 0 && !wait_or_abort(acce(b), (use - 1) & 1, abort)) { ok = false; break; }
                 ptx::tc_fence_after();
                 const uint32_t acc = tmem + b * BN;
-                for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
+                for (int kb = 0; kb < ti.num_kb; ++kb, ++g) {
                     const uint32_t s = g % S, round = g / S;
                     if (!wait_or_abort(GRID == kE2M1 ? full(s) : expd(s), round & 1, abort)) { ok = false; break; }
                     ptx::tc_fence_after();
-                    const int atoms = min(4, p.nkt - 4 * kb);
+                    const int atoms = min(4, ti.nkt - 4 * kb);
                     const uint32_t st = smem_base + s * C::kStageBytes;
                     const uint32_t sf_t = tmem + kSfCol + 32u * s;
                     const uint64_t dsa = mk(hi_sf, st + C::kSfaOff), dsb = mk(hi_sf, st + C::kSfbOff);
@@ -267,7 +333,6 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         // global writes are whole lines and ragged tile edges are clipped by
         // the tensor map.
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
-        const float alpha = __fmul_rn(*p.ts_a, *p.ts_b);
         const uint32_t ebase = smem_base + C::kEpiOff + (uint32_t)(warp - 2) * C::kEpiBufs * 4096u;
         uint32_t it = 0, nst = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
@@ -276,11 +341,37 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             ptx::tc_fence_after();
-            const int m0 = (t / p.ntn) * BM, n0 = (t % p.ntn) * BN;
+            const TileInfo ti = tile_info(p, tab, t);
+            const float alpha = __fmul_rn(*ti.ts_a, *ti.ts_b);
+            const int m0 = ti.m_loc, n0 = ti.n_loc;
 #pragma unroll 1
             for (int ch = 0; ch < BN / 32; ++ch, ++nst) {
                 uint32_t r[32];
                 ptx::tc_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + b * BN + 32u * ch, r);
+                if constexpr (kGrouped) {
+                    // masked direct stores: a group's C is not a whole tensor map
+                    ptx::tc_wait_ld();
+                    if (ch == BN / 32 - 1) {
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(acce(b));
+                    }
+                    const int row = m0 + 32 * q + lane, col0 = n0 + 32 * ch;
+                    if (row < ti.M) {
+                        float *crow = ti.c + (int64_t)row * ti.ldc;
+                        if (col0 + 32 <= ti.N) {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4)
+                                *reinterpret_cast<float4 *>(crow + col0 + i) =
+                                    make_float4(__uint_as_float(r[i]) * alpha, __uint_as_float(r[i + 1]) * alpha,
+                                                __uint_as_float(r[i + 2]) * alpha, __uint_as_float(r[i + 3]) * alpha);
+                        } else {
+                            for (int i = 0; i < 32; ++i)
+                                if (col0 + i < ti.N) crow[col0 + i] = __uint_as_float(r[i]) * alpha;
+                        }
+                    }
+                    continue;
+                }
                 const uint32_t buf = ebase + (nst % C::kEpiBufs) * 4096u;
                 // the store that last read this buffer must be done reading it
                 if (lane == 0) {
@@ -319,7 +410,8 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         uint32_t g = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-            for (int kb = 0; kb < p.num_kb; ++kb, ++g) {
+            const int nkb = tile_info(p, tab, t).num_kb;
+            for (int kb = 0; kb < nkb; ++kb, ++g) {
                 const uint32_t s = g % S, round = g / S;
                 ok = wait_or_abort(full(s), round & 1, abort);
                 ok = __all_sync(0xffffffffu, ok);
@@ -396,24 +488,23 @@ bool make_out_map(CUtensorMap *m, float *c, int64_t M, int64_t N, int64_t ldc) {
     return r == CUDA_SUCCESS;
 }
 
-template <int GRID>
+template <int GRID, class TAB>
 cudaError_t run_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc, const GemmParams &p,
-                     cudaStream_t s) {
+                     const TAB &tab, int ntiles, cudaStream_t s) {
     using C = Cfg<GRID>;
     static bool attr_set[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm<GRID>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(k_gemm<GRID, TAB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)C::kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    static int sms = 0;
-    if (!sms) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int ntiles = p.ntm * p.ntn;
+    const int sms = num_sms();
     const int grid = ntiles < sms ? ntiles : sms;
-    k_gemm<GRID><<<grid, C::kThreads, C::kSmemBytes, s>>>(ma, mb, mc, p);
+    if (grid <= 0) return cudaSuccess;
+    k_gemm<GRID, TAB><<<grid, C::kThreads, C::kSmemBytes, s>>>(ma, mb, mc, p, tab);
     return cudaGetLastError();
 }
 
@@ -435,8 +526,28 @@ cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const f
     p.num_kb = (p.nkt + 3) / 4;
     p.ntm = (int)((M + BM - 1) / BM);
     p.ntn = (int)((N + BN - 1) / BN);
-    if (grid == kE2M1) return run_gemm<kE2M1>(ma, mb, mc, p, s);
-    return run_gemm<kE1M2>(ma, mb, mc, p, s);
+    p.nkt_a = p.nkt_b = p.nkt;
+    const NoGroups none;
+    if (grid == kE2M1) return run_gemm<kE2M1>(ma, mb, mc, p, none, p.ntm * p.ntn, s);
+    return run_gemm<kE1M2>(ma, mb, mc, p, none, p.ntm * p.ntn, s);
+}
+
+cudaError_t launch_gemm_grouped(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_ts,
+                                int64_t a_rows, int64_t a_kpad, const uint8_t *b_codes, const uint8_t *b_scales,
+                                const float *b_ts, int64_t b_rows, int64_t b_kpad, int grid,
+                                const GroupGemmTab &tab, cudaStream_t s) {
+    CUtensorMap ma, mb, mc;
+    if (!make_code_map(&ma, a_codes, a_rows, a_kpad) || !make_code_map(&mb, b_codes, b_rows, b_kpad))
+        return cudaErrorInvalidValue;
+    memset(&mc, 0, sizeof mc);   // grouped epilogues store directly
+    GemmParams p{};
+    p.sfa = a_scales; p.sfb = b_scales; p.ts_a = a_ts; p.ts_b = b_ts;
+    p.nkt_a = (int)(a_kpad / 64);
+    p.nkt_b = (int)(b_kpad / 64);
+    p.M = 1; p.N = 1;
+    const int ntiles = tab.tiles[tab.n];
+    if (grid == kE2M1) return run_gemm<kE2M1>(ma, mb, mc, p, tab, ntiles, s);
+    return run_gemm<kE1M2>(ma, mb, mc, p, tab, ntiles, s);
 }
 
 cudaError_t read_timeout_flag(uint32_t *flag, cudaStream_t s) {

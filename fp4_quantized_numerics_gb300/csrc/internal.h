@@ -31,6 +31,31 @@ struct QuantLaunch {
 
 int num_sms();
 
+constexpr int kMaxGroups = 256;
+
+// Segment table of a grouped quantization (host-built, passed by value).
+struct GroupQuant {
+    int32_t n;
+    int32_t colwise;
+    int64_t in_row[kMaxGroups + 1];   // prefix sums of segment rows in x
+    int64_t out_off[kMaxGroups];      // row offset (row-wise) or k offset (column-wise) in the output
+    int64_t units[kMaxGroups + 1];    // prefix sums of work units (16-blocks / column-pair units)
+};
+
+// One group of a grouped GEMM (host-built).
+struct GroupGemm {
+    int32_t M, N, nkt, ntn;           // nkt = kpad(K) / 64, ntn = ceil(N / 128)
+    int32_t a_rt, a_kt, b_rt, b_kt;   // row offsets / 128, k offsets / 64
+    int32_t a_seg, b_seg;
+    float *c;
+    int64_t ldc;
+};
+struct GroupGemmTab {
+    int32_t n;
+    int32_t tiles[kMaxGroups + 1];    // prefix sums of 128 x 128 tiles per group
+    GroupGemm g[kMaxGroups];
+};
+
 // Tensor amax (when amax_in is null) + fused quantization.  `ws` is the
 // caller's workspace (status word + partial maxima).
 cudaError_t launch_quantize(const QuantLaunch &q, void *ws, cudaStream_t s);
@@ -41,6 +66,15 @@ cudaError_t launch_dequantize(const uint8_t *codes, const uint8_t *scales, const
 
 // Writes n_ctas x 8 double partial sums to ws + kWsStats; returns n_ctas.
 cudaError_t launch_stats(const QuantLaunch &q, void *ws, int *n_ctas, cudaStream_t s);
+
+// Grouped quantization: x holds segments in row order; ws keeps one fp32
+// maximum per segment and the status word.
+cudaError_t launch_quantize_grouped(const QuantLaunch &q, const GroupQuant &gt, void *ws, cudaStream_t s);
+
+cudaError_t launch_gemm_grouped(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_ts,
+                                int64_t a_rows, int64_t a_kpad, const uint8_t *b_codes, const uint8_t *b_scales,
+                                const float *b_ts, int64_t b_rows, int64_t b_kpad, int grid,
+                                const GroupGemmTab &tab, cudaStream_t s);
 
 cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_ts,
                         const uint8_t *b_codes, const uint8_t *b_scales, const float *b_ts,

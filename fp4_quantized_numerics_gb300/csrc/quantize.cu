@@ -196,6 +196,20 @@ __device__ __forceinline__ uint32_t block_scale(float amax, float qmax, float S_
     return e4m3_from_f32(__fmul_rn(div_qmax(amax, qmax), S_enc));
 }
 
+// k = min(S_enc / E4M3(e), FLT_MAX) (x 1/4 for RHT), the per-code multiplier
+// of the table, computed in place (grouped tensors: one S_enc per segment).
+__device__ __forceinline__ float inline_k(uint32_t e, float S_enc, bool rht) {
+    const float d = e4m3_to_f32(e);
+    float kk = 0.0f;
+    if (d > 0.0f) {
+        kk = __fdiv_rn(S_enc, d);
+        if (kk > kFltMax) kk = kFltMax;
+    } else if (!(d == 0.0f)) {
+        kk = d;
+    }
+    return rht ? kk * 0.25f : kk;
+}
+
 // Codes of 8 values q (already multiplied by k) as 8 nibbles, element j in
 // bits 4j..4j+3.  `i0` is the logical output index of element 0 (multiple of
 // 8) for stochastic rounding.
@@ -563,7 +577,7 @@ __device__ __forceinline__ void quant_block_row(const Args &a, const Raw<In> &ra
     for (int j = 0; j < 8; ++j) m = fmaxf(m, fmaxf(fabsf(lo[j]), fabsf(hi[j])));
     if (RHT) m *= 0.25f;
     const uint32_t e = block_scale(m, qmax, S_enc);
-    const float kk = s_k[e];
+    const float kk = s_k ? s_k[e] : inline_k(e, S_enc, RHT);
     const uint64_t K2 = pk2(kk, kk);
     float ql[8], qh[8];
 #pragma unroll
@@ -676,6 +690,11 @@ template <> struct ColRaw<__nv_bfloat16> {
 #pragma unroll
         for (int i = 0; i < 16; ++i) w[i] = __ldg(reinterpret_cast<const unsigned int *>(p + i * ld));
     }
+    __device__ __forceinline__ void load_rows(const __nv_bfloat16 *p, int64_t ld, int nvalid) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            w[i] = i < nvalid ? __ldg(reinterpret_cast<const unsigned int *>(p + i * ld)) : 0u;
+    }
     __device__ __forceinline__ void zero() {
 #pragma unroll
         for (int i = 0; i < 16; ++i) w[i] = 0u;
@@ -698,6 +717,11 @@ template <> struct ColRaw<float> {
     __device__ __forceinline__ void load(const float *p, int64_t ld) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) w[i] = __ldg(reinterpret_cast<const uint2 *>(p + i * ld));
+    }
+    __device__ __forceinline__ void load_rows(const float *p, int64_t ld, int nvalid) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            w[i] = i < nvalid ? __ldg(reinterpret_cast<const uint2 *>(p + i * ld)) : make_uint2(0u, 0u);
     }
     __device__ __forceinline__ void zero() {
 #pragma unroll
@@ -810,7 +834,7 @@ __device__ __forceinline__ void quant_unit_col(const Args &a, const ColRaw<In> &
     if (RHT) { m0 *= 0.25f; m1 *= 0.25f; }
     uint32_t e0 = block_scale(m0, qmax, S_enc), e1 = block_scale(m1, qmax, S_enc);
     if (!real) { e0 = 0u; e1 = 0u; }
-    const uint64_t K2 = pk2(s_k[e0], s_k[e1]);
+    const uint64_t K2 = s_k ? pk2(s_k[e0], s_k[e1]) : pk2(inline_k(e0, S_enc, RHT), inline_k(e1, S_enc, RHT));
 #pragma unroll
     for (int i = 0; i < 16; ++i) upk2(mul2(P[i], K2), v0[i], v1[i]);
     const uint64_t R = (uint64_t)a.rows;
@@ -1113,6 +1137,206 @@ __global__ void __launch_bounds__(kThreads) k_col_staged(Args a, uint32_t ncc, u
         }
         zero_pad_rows(a);
     }
+}
+
+// ====================================================== grouped (MoE) path
+// Segments are found by binary search over prefix tables copied into shared
+// memory: find_seg returns the largest e with pre[e] <= u (empty segments are
+// skipped because their start equals the next one's).
+__device__ __forceinline__ int find_seg(const int64_t *pre, int n, int64_t u) {
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pre[mid] <= u) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+struct GroupSmem {
+    int64_t in_row[kMaxGroups + 1];
+    int64_t out_off[kMaxGroups];
+    int64_t units[kMaxGroups + 1];
+    float senc[kMaxGroups];
+};
+
+__device__ __forceinline__ void load_group_tables(const GroupQuant &gt, GroupSmem &sm) {
+    for (int i = threadIdx.x; i <= gt.n; i += blockDim.x) {
+        sm.in_row[i] = gt.in_row[i];
+        sm.units[i] = gt.units[i];
+        if (i < gt.n) sm.out_off[i] = gt.out_off[i];
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ void seg_max_flush(uint32_t *slots, int e, float m) {
+    if (e >= 0 && m > 0.0f) atomicMax(slots + e, __float_as_uint(m));
+    else if (e >= 0 && !(m == m)) atomicMax(slots + e, 0x7FC00000u);   // NaN
+}
+
+// Per-segment maxima (row-wise: units are real 16-blocks, unit -> (row, block);
+// column-wise: units are 16-row x 2-column pieces, unit -> (row block, pair)).
+// Warp-contiguous chunks keep segment changes (and atomics) rare.
+template <class In, bool RHT, bool COL>
+__global__ void __launch_bounds__(kThreads) k_amax_grouped(Args a, const __grid_constant__ GroupQuant gt,
+                                                           FastDiv div, uint32_t per_row, uint32_t *slots) {
+    __shared__ GroupSmem sm;
+    load_group_tables(gt, sm);
+    const uint32_t smask = RHT ? rht_sign_mask(a.rht_seed) : 0u;
+    const Signs sg = COL ? col_signs<In>(smask) : row_signs<In>(smask);
+    const In *x = static_cast<const In *>(a.x);
+    const int64_t total = sm.units[gt.n];
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t chunk = ((total + nwarps - 1) / nwarps + 31) / 32 * 32;
+    const int lane = threadIdx.x & 31;
+    int e_cur = -1;
+    float m = 0.0f;
+    const int64_t uend = total < (wid + 1) * chunk ? total : (wid + 1) * chunk;
+    for (int64_t u = wid * chunk + lane; u < uend; u += 32) {
+        const int e = (e_cur >= 0 && u < sm.units[e_cur + 1]) ? e_cur : find_seg(sm.units, gt.n, u);
+        if (e != e_cur) {
+            seg_max_flush(slots, e_cur, RHT ? m * 0.25f : m);
+            e_cur = e;
+            m = 0.0f;
+        }
+        const uint32_t lu = (uint32_t)(u - sm.units[e]);
+        const uint32_t q = fdiv(lu, div), rem = lu - q * per_row;
+        if (!COL) {
+            Raw<In> raw;
+            raw.load(x + (sm.in_row[e] + q) * a.ld + rem * 16);
+            float lo[8], hi[8];
+            block_values<In, RHT>(raw, sg, lo, hi);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) m = max_nan(m, max_nan(fabsf(lo[j]), fabsf(hi[j])));
+        } else {
+            const int64_t seg_rows = sm.in_row[e + 1] - sm.in_row[e];
+            const int64_t left = seg_rows - 16 * (int64_t)q;
+            const int nvalid = left < 16 ? (int)left : 16;
+            ColRaw<In> raw;
+            raw.load_rows(x + (sm.in_row[e] + 16 * (int64_t)q) * a.ld + rem * 2, a.ld, nvalid);
+            uint64_t P[16];
+            col_values<In, RHT>(raw, sg, P);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float c0, c1;
+                upk2(P[i], c0, c1);
+                m = max_nan(m, max_nan(fabsf(c0), fabsf(c1)));
+            }
+        }
+    }
+    seg_max_flush(slots, e_cur, RHT ? m * 0.25f : m);
+}
+
+// Quantization of every segment with its own tensor scale.  Row-wise units
+// cover rows [0, rpad(T_e)) x all kpad/16 blocks of each segment (padding
+// rows and blocks are written as zeros); column-wise units cover the
+// segment's kpad(T_e)/16 row blocks x column pairs.
+template <class In, int GRID, int ROUND, bool RHT, bool COL>
+__global__ void __launch_bounds__(kThreads) k_quant_grouped(Args a, const __grid_constant__ GroupQuant gt,
+                                                            FastDiv div, uint32_t per_row, const uint32_t *slots) {
+    __shared__ GroupSmem sm;
+    load_group_tables(gt, sm);
+    const float qmax = GRID == kE2M1 ? 6.0f : 3.5f;
+    for (int e = threadIdx.x; e < gt.n; e += blockDim.x) {
+        const float A_t = __uint_as_float(slots[e]);
+        float se = 1.0f, sd = 1.0f;
+        if (A_t > 0.0f) {
+            const float num = 448.0f * qmax;
+            se = __fdiv_rn(num, A_t);
+            if (se > kFltMax) se = kFltMax;
+            sd = __fdiv_rn(A_t, num);
+        }
+        sm.senc[e] = se;
+        if (blockIdx.x == 0) {
+            a.tensor_scale[e] = sd;
+            if (!isfinite(A_t) && a.status) atomicOr(a.status, 1u);
+        }
+    }
+    __syncthreads();
+    const uint32_t smask = RHT ? rht_sign_mask(a.rht_seed) : 0u;
+    const Signs sg = COL ? col_signs<In>(smask) : row_signs<In>(smask);
+    const In *x = static_cast<const In *>(a.x);
+    const int64_t total = sm.units[gt.n];
+    const uint32_t cstride = (uint32_t)(a.kpad / 2), nkt = (uint32_t)a.nkt;
+    const uint32_t kvb = (uint32_t)(a.k / 16);
+    for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < total;
+         u += (int64_t)gridDim.x * blockDim.x) {
+        const int e = find_seg(sm.units, gt.n, u);
+        const uint32_t lu = (uint32_t)(u - sm.units[e]);
+        const uint32_t q = fdiv(lu, div), rem = lu - q * per_row;
+        const int64_t seg_rows = sm.in_row[e + 1] - sm.in_row[e];
+        const float S_enc = sm.senc[e];
+        if (!COL) {
+            // q: row within the segment, rem: block within the row
+            Raw<In> raw;
+            if ((int64_t)q < seg_rows && rem < kvb) raw.load(x + (sm.in_row[e] + q) * a.ld + rem * 16);
+            else raw.zero();
+            quant_block_row<In, GRID, ROUND, RHT>(a, raw, (uint32_t)(sm.out_off[e] + q), rem, sg, S_enc, nullptr,
+                                                  cstride, nkt, false);
+        } else {
+            // q: row block within the segment, rem: column pair
+            const int64_t left = seg_rows - 16 * (int64_t)q;
+            const int nvalid = left <= 0 ? 0 : (left < 16 ? (int)left : 16);
+            ColRaw<In> raw;
+            if (nvalid > 0) raw.load_rows(x + (sm.in_row[e] + 16 * (int64_t)q) * a.ld + rem * 2, a.ld, nvalid);
+            else raw.zero();
+            quant_unit_col<In, GRID, ROUND, RHT>(a, raw, (uint32_t)(sm.out_off[e] / 16 + q), rem * 2, nvalid > 0,
+                                                 sg, S_enc, nullptr, cstride, nkt, false);
+        }
+    }
+    zero_pad_rows(a);
+}
+
+template <class In>
+cudaError_t quantize_grouped_typed(const QuantLaunch &q, const GroupQuant &gt, void *ws, cudaStream_t s) {
+    Args a{};
+    a.x = q.x; a.ld = q.ld; a.cols = q.cols;
+    a.out_rows = q.out_rows; a.k = q.k; a.kpad = kpad_of(q.k); a.nkt = a.kpad / 64;
+    a.rows = q.colwise ? q.k : q.rows;   // column-wise: the SR row length is the whole k
+    a.rht_seed = q.rht_seed; a.sr_seed = q.sr_seed; a.sr_counter = q.sr_counter; a.elem_base = 0;
+    a.status = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsStatus);
+    a.codes = q.codes; a.scales = q.scales; a.tensor_scale = q.tensor_scale;
+    uint32_t *slots = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsPartials);
+    cudaError_t e = cudaMemsetAsync(ws, 0, kWsPartials + (size_t)gt.n * sizeof(uint32_t), s);
+    if (e != cudaSuccess) return e;
+    const bool col = q.colwise != 0;
+    // amax pass: units over real data only
+    GroupQuant ga = gt;
+    const uint32_t per_row_a = col ? (uint32_t)(q.cols / 2) : (uint32_t)(q.cols / 16);
+    for (int i = 0; i < gt.n; ++i) {
+        const int64_t T = gt.in_row[i + 1] - gt.in_row[i];
+        ga.units[i + 1] = ga.units[i] + (col ? (T + 15) / 16 : T) * per_row_a;
+    }
+    const int64_t ta = ga.units[gt.n];
+    const int sms = num_sms();
+    if (ta > 0) {
+        const int g = (int)std::min<int64_t>((ta + kThreads - 1) / kThreads, (int64_t)sms * 4);
+#define UFP4_GA(COL, RHT) if (col == COL && (q.rht != 0) == RHT) k_amax_grouped<In, RHT, COL><<<g, kThreads, 0, s>>>(a, ga, make_fastdiv(per_row_a), per_row_a, slots);
+        UFP4_GA(false, false) UFP4_GA(false, true) UFP4_GA(true, false) UFP4_GA(true, true)
+#undef UFP4_GA
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    // quant pass: units include the padding rows / blocks
+    const uint32_t per_row = col ? (uint32_t)(q.cols / 2) : (uint32_t)(a.kpad / 16);
+    const int64_t tq = gt.units[gt.n];
+    const int g = (int)std::min<int64_t>(std::max<int64_t>((tq + kThreads - 1) / kThreads, 1), (int64_t)sms * 8);
+    const FastDiv fd = make_fastdiv(per_row);
+#define UFP4_GQ(COL, GRID, ROUND, RHT)                                                            \
+    if (col == COL && q.grid == GRID && q.round == ROUND && (q.rht != 0) == RHT) {              \
+        k_quant_grouped<In, GRID, ROUND, RHT, COL><<<g, kThreads, 0, s>>>(a, gt, fd, per_row, slots); \
+        return cudaGetLastError();                                                               \
+    }
+    UFP4_GQ(false, kE2M1, kRTNE, false) UFP4_GQ(false, kE2M1, kRTNE, true)
+    UFP4_GQ(false, kE2M1, kSR, false)   UFP4_GQ(false, kE2M1, kSR, true)
+    UFP4_GQ(false, kE1M2, kRTNE, false) UFP4_GQ(false, kE1M2, kRTNE, true)
+    UFP4_GQ(false, kE1M2, kSR, false)   UFP4_GQ(false, kE1M2, kSR, true)
+    UFP4_GQ(true, kE2M1, kRTNE, false)  UFP4_GQ(true, kE2M1, kRTNE, true)
+    UFP4_GQ(true, kE2M1, kSR, false)    UFP4_GQ(true, kE2M1, kSR, true)
+    UFP4_GQ(true, kE1M2, kRTNE, false)  UFP4_GQ(true, kE1M2, kRTNE, true)
+    UFP4_GQ(true, kE1M2, kSR, false)    UFP4_GQ(true, kE1M2, kSR, true)
+#undef UFP4_GQ
+    return cudaErrorInvalidValue;
 }
 
 // ============================================================= statistics
@@ -1431,6 +1655,11 @@ cudaError_t launch_quantize(const QuantLaunch &q, void *ws, cudaStream_t s) {
     Args a = make_args(q, ws);
     if (q.dtype == 0) return quantize_typed<__nv_bfloat16>(q, a, ws, s);
     return quantize_typed<float>(q, a, ws, s);
+}
+
+cudaError_t launch_quantize_grouped(const QuantLaunch &q, const GroupQuant &gt, void *ws, cudaStream_t s) {
+    if (q.dtype == 0) return quantize_grouped_typed<__nv_bfloat16>(q, gt, ws, s);
+    return quantize_grouped_typed<float>(q, gt, ws, s);
 }
 
 cudaError_t launch_dequantize(const uint8_t *codes, const uint8_t *scales, const float *ts,

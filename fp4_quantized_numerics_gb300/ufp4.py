@@ -28,7 +28,8 @@ UFP4_OK, UFP4_ERR_INVALID, UFP4_ERR_UNSUPPORTED, UFP4_ERR_NONFINITE, UFP4_ERR_CU
 
 EXPORTED = ["ufp4_kpad", "ufp4_codes_bytes", "ufp4_scales_bytes", "ufp4_workspace_bytes",
             "ufp4_quantize", "ufp4_check", "ufp4_dequantize", "ufp4_gemm", "ufp4_stats",
-            "ufp4_status_string", "ufp4_quantize_noalloc"]
+            "ufp4_status_string", "ufp4_quantize_noalloc", "ufp4_grouped_rows",
+            "ufp4_grouped_kpad", "ufp4_quantize_grouped", "ufp4_gemm_grouped"]
 
 
 class QParamsC(ctypes.Structure):
@@ -48,6 +49,13 @@ class QTensorC(ctypes.Structure):
 class StatsC(ctypes.Structure):
     _fields_ = [(n, ctypes.c_double) for n in
                 ("alpha", "sqnr_db", "mean_bias", "sum_aq", "sum_aa", "sum_err2", "bias_count")]
+
+
+class GemmGroupC(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("a_row", ctypes.c_int64), ("a_k", ctypes.c_int64), ("b_row", ctypes.c_int64),
+                ("b_k", ctypes.c_int64), ("a_seg", ctypes.c_int32), ("b_seg", ctypes.c_int32),
+                ("c", ctypes.c_void_p), ("ldc", ctypes.c_int64)]
 
 
 class UFP4Error(RuntimeError):
@@ -89,6 +97,18 @@ def lib():
                                  ctypes.POINTER(QTensorC), vp, ctypes.c_size_t,
                                  ctypes.POINTER(StatsC), vp]
         L.ufp4_stats.restype = ctypes.c_int
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        L.ufp4_grouped_rows.argtypes = [i64p, ctypes.c_int32]
+        L.ufp4_grouped_rows.restype = i64
+        L.ufp4_grouped_kpad.argtypes = [i64p, ctypes.c_int32]
+        L.ufp4_grouped_kpad.restype = i64
+        L.ufp4_quantize_grouped.argtypes = [vp, ctypes.c_int32, i64, i64, i64p, ctypes.c_int32,
+                                            ctypes.POINTER(QParamsC), ctypes.POINTER(QTensorC), vp,
+                                            ctypes.c_size_t, vp]
+        L.ufp4_quantize_grouped.restype = ctypes.c_int
+        L.ufp4_gemm_grouped.argtypes = [ctypes.POINTER(QTensorC), ctypes.POINTER(QTensorC),
+                                        ctypes.POINTER(GemmGroupC), ctypes.c_int32, vp]
+        L.ufp4_gemm_grouped.restype = ctypes.c_int
         L.ufp4_status_string.argtypes = [ctypes.c_int]
         L.ufp4_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -241,3 +261,67 @@ def ufp4_stats(x, q, rht=False, rht_seed=0, round=UFP4_RTNE, sr_seed=0, sr_count
                           _stream(stream))
     _check(st, "ufp4_stats")
     return {n: getattr(out, n) for n, _ in StatsC._fields_}
+
+
+# ------------------------------------------------------------ grouped (MoE)
+def _i64_array(vals):
+    arr = (ctypes.c_int64 * len(vals))(*[int(v) for v in vals])
+    return arr
+
+
+def grouped_rows(seg_rows):
+    return int(lib().ufp4_grouped_rows(_i64_array(seg_rows), len(seg_rows)))
+
+
+def grouped_kpad(seg_rows):
+    return int(lib().ufp4_grouped_kpad(_i64_array(seg_rows), len(seg_rows)))
+
+
+def grouped_offsets(seg_rows, colwise):
+    """Row offsets (row-wise) or k offsets (column-wise) of each segment."""
+    offs, o = [], 0
+    for t in seg_rows:
+        offs.append(o)
+        if t > 0:
+            o += ((t + 63) // 64 * 64) if colwise else ((t + 127) // 128 * 128)
+    return offs
+
+
+def ufp4_quantize_grouped(x, grid, seg_rows, rht=False, rht_seed=0, round=UFP4_RTNE, sr_seed=0,
+                          sr_counter=0, colwise=False, out=None, ws=None, stream=None):
+    """Quantize the row segments of x, one tensor scale per segment (layouts:
+    include/ufp4.h, grouped tensors).  Returns a QTensor whose tensor_scale
+    holds one S_dec per segment."""
+    _cuda(x, "x")
+    cols = x.shape[1]
+    n = len(seg_rows)
+    if colwise:
+        rows, k = cols, grouped_kpad(seg_rows)
+    else:
+        rows, k = grouped_rows(seg_rows), cols
+    if out is None:
+        out = QTensor.empty(rows, k, grid, x.device)
+        out.tensor_scale = torch.empty(max(n, 1), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(x.device)
+    p = qparams(grid, rht, rht_seed, round, sr_seed, sr_counter, colwise)
+    qc = out.c()
+    st = lib().ufp4_quantize_grouped(x.data_ptr(), _dtype_code(x), cols, x.stride(0),
+                                     _i64_array(seg_rows), n, ctypes.byref(p), ctypes.byref(qc),
+                                     ws.data_ptr(), ws.numel(), _stream(stream))
+    _check(st, "ufp4_quantize_grouped")
+    out.seg_rows = list(seg_rows)
+    return out
+
+
+def ufp4_gemm_grouped(a, b, groups, stream=None):
+    """groups: list of dicts with keys M, N, K, a_row, a_k, b_row, b_k, a_seg,
+    b_seg and c (an fp32 CUDA tensor view of M x N with unit column stride)."""
+    arr = (GemmGroupC * max(len(groups), 1))()
+    for i, g in enumerate(groups):
+        c = g["c"]
+        arr[i] = GemmGroupC(g["M"], g["N"], g["K"], g["a_row"], g["a_k"], g["b_row"], g["b_k"],
+                            g["a_seg"], g["b_seg"], c.data_ptr(), c.stride(0))
+    ac, bc = a.c(), b.c()
+    st = lib().ufp4_gemm_grouped(ctypes.byref(ac), ctypes.byref(bc), arr, len(groups), _stream(stream))
+    _check(st, "ufp4_gemm_grouped")

@@ -212,6 +212,65 @@ UFP4_API ufp4_status ufp4_dequantize(const ufp4_qtensor *q, int32_t inverse_rht,
 UFP4_API ufp4_status ufp4_gemm(const ufp4_qtensor *a, const ufp4_qtensor *b, float *c, int64_t ldc,
                       ufp4_stream_t stream);
 
+/* ---------------------------------------------------------------------
+ * Grouped (mixture-of-experts) tensors.  The tokens routed to expert e form a
+ * segment of T_e consecutive rows of x ([sum T_e] x cols); every segment has
+ * its own tensor scale.  Segment layouts inside one quantized tensor:
+ *   row-wise  (blocks along cols): segment e occupies rows
+ *             [roff_e, roff_e + T_e) with roff_e = sum_{e'<e} round_up(T_e', 128),
+ *             so every segment starts on a scale-atom boundary; the tensor
+ *             has rows = ufp4_grouped_rows(...) and k = cols.
+ *   column-wise (blocks down the tokens, the quantization of x_e^T): segment e
+ *             occupies k range [koff_e, koff_e + T_e) with
+ *             koff_e = sum_{e'<e} round_up(T_e', 64); the token dimension of
+ *             each segment is zero-padded to a multiple of 16; rows = cols and
+ *             k = ufp4_grouped_kpad(...).
+ * The qtensor's tensor_scale points to n_seg floats (S_dec per segment).
+ * Stochastic rounding indexes elements by their position in the whole
+ * output tensor (row * k + col), so no two segments share a random word.
+ * ([HP] technical approach: MoE 7.9B and 124B models; [ZC] Validation
+ * results.) */
+UFP4_API int64_t ufp4_grouped_rows(const int64_t *seg_rows_host, int32_t n_seg);
+UFP4_API int64_t ufp4_grouped_kpad(const int64_t *seg_rows_host, int32_t n_seg);
+#define UFP4_MAX_GROUPS 256
+
+/* Grouped quantization of x (device, [sum seg_rows] x cols, row stride ld).
+ * seg_rows_host: host array of n_seg >= 1 segment row counts (0 allowed),
+ * n_seg <= UFP4_MAX_GROUPS.  p->colwise selects the layout above; p->amax_in
+ * must be NULL (every segment's amax is computed).  out: rows/k as above,
+ * tensor_scale -> n_seg floats.  workspace: ufp4_workspace_bytes(), 16-byte
+ * aligned (holds the per-segment maxima and the status word). */
+UFP4_API ufp4_status ufp4_quantize_grouped(const void *x, int32_t dtype, int64_t cols, int64_t ld,
+                                           const int64_t *seg_rows_host, int32_t n_seg,
+                                           const ufp4_qparams *p, const ufp4_qtensor *out,
+                                           void *workspace, size_t workspace_bytes,
+                                           ufp4_stream_t stream);
+
+/* One GEMM per group, C_g = A_g B_g^T, in a single launch.  A group's
+ * operands are views of two quantized tensors a and b (same grid):
+ *   A_g = rows [a_row[g], a_row[g] + M[g]) and k range [a_k[g], a_k[g] + K[g]) of a,
+ *   B_g = rows [b_row[g], b_row[g] + N[g]) and k range [b_k[g], b_k[g] + K[g]) of b,
+ * with tensor scales a->tensor_scale[a_seg[g]] and b->tensor_scale[b_seg[g]].
+ * Row offsets must be multiples of 128 and k offsets multiples of 64 (the
+ * grouped layouts above guarantee both).  C_g: device fp32 pointer c[g] with
+ * row stride ldc[g] (% 4 == 0, 16-byte aligned); K[g] = 0 writes zeros,
+ * M[g] = 0 or N[g] = 0 does nothing.  All arrays are host arrays of n groups,
+ * n <= UFP4_MAX_GROUPS.  The three training GEMMs of an MoE layer map onto
+ * this with the grouped layouts: fwd_y (A = X rows, B = W rows), bwd_dx
+ * (A = dY rows, B = W^T segments along k), bwd_dw (A = dY^T and B = X^T, both
+ * sharing the segment's k range). */
+typedef struct {
+    int64_t M, N, K;
+    int64_t a_row, a_k, b_row, b_k;
+    int32_t a_seg, b_seg;
+    float *c;
+    int64_t ldc;
+} ufp4_gemm_group;
+
+UFP4_API ufp4_status ufp4_gemm_grouped(const ufp4_qtensor *a, const ufp4_qtensor *b,
+                                       const ufp4_gemm_group *groups, int32_t n,
+                                       ufp4_stream_t stream);
+
 /* Quality of one quantization, in fp64 on the host ([ZC] "The cause",
  * "Compounding decay", "The RHT paradox").  A is the tensor that was
  * quantized (x, rotated when p->rht; transposed when p->colwise):

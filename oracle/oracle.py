@@ -56,6 +56,11 @@ def lib():
                                    ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64,
                                    ctypes.c_uint64, vp, vp, vp, vp, vp]
         L.ref_quantize.restype = ctypes.c_int
+        L.ref_quantize_strided.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_uint64,
+                                           ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64,
+                                           ctypes.c_uint64, ctypes.c_uint64, vp, vp, vp, vp, vp]
+        L.ref_quantize_strided.restype = ctypes.c_int
         L.ref_dequantize.argtypes = [vp, vp, ctypes.c_float, ctypes.c_int64, ctypes.c_int64,
                                      ctypes.c_int, ctypes.c_int, ctypes.c_uint64, vp]
         L.ref_gemm_f64.argtypes = [vp, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp]
@@ -121,7 +126,7 @@ def sr_word(sr_seed, sr_counter, i):
 
 # ------------------------------------------------------------------ tensors
 def quantize(x, grid, rht=False, rht_seed=0, round_mode=RTNE, sr_seed=0, sr_counter=0,
-             colwise=False, amax_in=None, elem_base=0):
+             colwise=False, amax_in=None, elem_base=0, sr_row_stride=None):
     """Quantize a 2-D fp32 array with 16-blocks along its last dim (row-wise),
     or along its first dim (colwise: the result is the quantization of x.T).
 
@@ -139,13 +144,63 @@ def quantize(x, grid, rht=False, rht_seed=0, round_mode=RTNE, sr_seed=0, sr_coun
     ts = np.zeros(1, dtype=np.float32)
     y = np.zeros((rows, k), dtype=np.float32)
     am = None if amax_in is None else np.array([amax_in], dtype=np.float32)
-    rc = lib().ref_quantize(_p(x), rows, k, k, grid, int(bool(rht)), ctypes.c_uint64(rht_seed),
-                            round_mode, ctypes.c_uint64(sr_seed), ctypes.c_uint64(sr_counter),
-                            ctypes.c_uint64(elem_base), _p(am), _p(codes), _p(scales), _p(ts),
-                            _p(y))
+    stride = k if sr_row_stride is None else sr_row_stride
+    rc = lib().ref_quantize_strided(_p(x), rows, k, k, grid, int(bool(rht)), ctypes.c_uint64(rht_seed),
+                                    round_mode, ctypes.c_uint64(sr_seed), ctypes.c_uint64(sr_counter),
+                                    ctypes.c_uint64(elem_base), ctypes.c_uint64(stride), _p(am), _p(codes),
+                                    _p(scales), _p(ts), _p(y))
     if rc != 0:
         raise ValueError("ref_quantize failed (%d): k must be a multiple of 16" % rc)
     return dict(codes=codes, scales=scales, tensor_scale=float(ts[0]), y=y)
+
+
+def rpad128(t):
+    return (t + 127) // 128 * 128
+
+
+def kpad64(t):
+    return (t + 63) // 64 * 64
+
+
+def quantize_grouped(x, seg_rows, grid, rht=False, rht_seed=0, round_mode=RTNE, sr_seed=0,
+                     sr_counter=0, colwise=False):
+    """Per-segment quantization of the row segments of x, each with its own
+    tensor scale (mixture-of-experts tokens).  Row-wise: segment e is the
+    quantization of its rows, placed at row offset roff_e = sum rpad128 of the
+    earlier segments in an output of row length cols.  Column-wise: segment e
+    (T_e x cols) is zero-padded to a multiple of 16 rows and becomes cols x
+    T16_e at k offset koff_e = sum kpad64 of the earlier segments, in an
+    output of row length Ktot = sum kpad64.  Stochastic rounding indexes each
+    element by its place in that whole output.  Returns a list of per-segment
+    dicts (as quantize) plus 'off' (roff_e or koff_e)."""
+    x = np.asarray(x, dtype=np.float32)
+    rows, cols = x.shape
+    starts = np.concatenate([[0], np.cumsum(seg_rows)]).astype(np.int64)
+    ktot = int(sum(kpad64(int(t)) for t in seg_rows if t > 0))
+    out, off = [], 0
+    for e, T in enumerate(seg_rows):
+        T = int(T)
+        seg = x[starts[e]:starts[e] + T]
+        if not colwise:
+            r = quantize(seg, grid, rht, rht_seed, round_mode, sr_seed, sr_counter,
+                         elem_base=off * cols) if T > 0 else None
+            if r is not None:
+                r["off"] = off
+            out.append(r)
+            off += rpad128(T) if T > 0 else 0
+        else:
+            if T == 0:
+                out.append(None)
+                continue
+            t16 = (T + 15) // 16 * 16
+            padded = np.zeros((t16, cols), np.float32)
+            padded[:T] = seg
+            r = quantize(padded, grid, rht, rht_seed, round_mode, sr_seed, sr_counter, colwise=True,
+                         elem_base=off, sr_row_stride=ktot)
+            r["off"] = off
+            out.append(r)
+            off += kpad64(T)
+    return out
 
 
 def pack_codes(codes):

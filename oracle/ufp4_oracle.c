@@ -229,12 +229,34 @@ uint32_t ref_sr_word(uint64_t sr_seed, uint64_t sr_counter, uint64_t i)
  * element index (i = elem_base + r * k + j).
  * Returns 0, or -1 on k % 16 != 0.
  * ---------------------------------------------------------------------- */
+int ref_quantize_strided(const float *x, int64_t rows, int64_t k, int64_t ld,
+                         int grid, int rht, uint64_t rht_seed,
+                         int round_mode, uint64_t sr_seed, uint64_t sr_counter,
+                         uint64_t elem_base, uint64_t sr_row_stride, const float *amax_in,
+                         uint8_t *codes, uint8_t *scales, float *tensor_scale,
+                         float *y_out);
+
 int ref_quantize(const float *x, int64_t rows, int64_t k, int64_t ld,
                  int grid, int rht, uint64_t rht_seed,
                  int round_mode, uint64_t sr_seed, uint64_t sr_counter,
                  uint64_t elem_base, const float *amax_in,
                  uint8_t *codes, uint8_t *scales, float *tensor_scale,
                  float *y_out)
+{
+    return ref_quantize_strided(x, rows, k, ld, grid, rht, rht_seed, round_mode, sr_seed,
+                                sr_counter, elem_base, (uint64_t)k, amax_in, codes, scales,
+                                tensor_scale, y_out);
+}
+
+/* As ref_quantize; the SR element index is elem_base + r * sr_row_stride + j
+ * (a segment that is one piece of a larger output tensor uses that tensor's
+ * row length, so its random words are those of its place in the whole). */
+int ref_quantize_strided(const float *x, int64_t rows, int64_t k, int64_t ld,
+                         int grid, int rht, uint64_t rht_seed,
+                         int round_mode, uint64_t sr_seed, uint64_t sr_counter,
+                         uint64_t elem_base, uint64_t sr_row_stride, const float *amax_in,
+                         uint8_t *codes, uint8_t *scales, float *tensor_scale,
+                         float *y_out)
 {
     if (k % 16 != 0) return -1;
     const float qmax = (float)ref_grid_qmax(grid);
@@ -284,7 +306,7 @@ int ref_quantize(const float *x, int64_t rows, int64_t k, int64_t ld,
                 if (a > qmax) a = qmax;
                 int m;
                 if (round_mode == REF_SR) {
-                    const uint64_t i = elem_base + (uint64_t)(r * k + b * 16 + j);
+                    const uint64_t i = elem_base + (uint64_t)r * sr_row_stride + (uint64_t)(b * 16 + j);
                     m = ref_round_sr(grid, a, ref_sr_word(sr_seed, sr_counter, i));
                 } else {
                     m = ref_round_rtne(grid, a);

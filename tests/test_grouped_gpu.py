@@ -1,0 +1,151 @@
+"""GPU parity of the grouped (mixture-of-experts) quantization and GEMMs.
+
+A small MoE layer with ragged, tiny and zero-token experts: X [sum T_e x H],
+W [E * F x H] (expert e = rows eF..eF+F-1), dY [sum T_e x F].  Every segment
+is checked against the oracle's per-segment quantization (bit-exact with RHT
+off, within the RHT tolerance with it on), and the three grouped GEMMs
+(fwd_y, bwd_dx, bwd_dw) against the oracle's fp64 per-expert products.
+"""
+import numpy as np
+import pytest
+import torch
+
+from fp4_quantized_numerics_gb300 import inputs
+from tests import layouts
+
+pytestmark = pytest.mark.gpu
+
+COUNTS = [37, 0, 130, 5, 256, 64, 1]
+H, F = 96, 80
+
+
+@pytest.fixture(scope="module")
+def U():
+    from fp4_quantized_numerics_gb300 import build, ufp4
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return ufp4
+
+
+def _data():
+    g = np.random.default_rng(7)
+    T = sum(COUNTS)
+    x = inputs.to_bf16_f32(g.standard_normal((T, H), dtype=np.float32))
+    w = inputs.to_bf16_f32(g.standard_normal((len(COUNTS) * F, H), dtype=np.float32) * np.float32(0.02))
+    dy = inputs.to_bf16_f32(g.standard_normal((T, F), dtype=np.float32) * np.float32(1e-3))
+    return x, w, dy
+
+
+def _gpu_segments(U, q, seg_rows, colwise):
+    """Per-segment (codes, scales, tensor_scale) views of a grouped QTensor."""
+    torch.cuda.synchronize()
+    codes = layouts.unpack_codes(q.codes.cpu().numpy(), q.rows, q.k)
+    scales, _ = layouts.unpack_scales(q.scales.cpu().numpy(), q.rows, q.k)
+    ts = q.tensor_scale.cpu().numpy()
+    offs = U.grouped_offsets(seg_rows, colwise)
+    out = []
+    for e, T in enumerate(seg_rows):
+        if T == 0:
+            out.append(None)
+            continue
+        o = offs[e]
+        if not colwise:
+            out.append((codes[o:o + T], scales[o:o + T], float(ts[e])))
+        else:
+            t16 = (T + 15) // 16 * 16
+            out.append((codes[:, o:o + t16], scales[:, o // 16:(o + t16) // 16], float(ts[e])))
+    return out
+
+
+def _check_segments(got, ref, rht):
+    for g, r in zip(got, ref):
+        if r is None:
+            assert g is None
+            continue
+        codes, scales, ts = g
+        if not rht:
+            np.testing.assert_array_equal(scales, r["scales"])
+            np.testing.assert_array_equal(codes, r["codes"])
+            assert ts == np.float32(r["tensor_scale"])
+        else:
+            assert abs(ts / r["tensor_scale"] - 1) <= 1e-6
+            si = lambda c: np.where(c & 8, -(c.astype(np.int32) & 7), c.astype(np.int32) & 7)
+            d = np.abs(si(codes) - si(r["codes"]))
+            assert d.max() <= 1 and (d > 0).mean() <= 1e-3
+
+
+@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("rht", [False, True])
+@pytest.mark.parametrize("colwise", [False, True])
+def test_grouped_quantize_matches_oracle(U, oracle, grid, rht, colwise):
+    x, w, dy = _data()
+    for arr, seg, rnd in ((x, COUNTS, 0), (dy, COUNTS, 1), (w, [F] * len(COUNTS), 0)):
+        t = torch.from_numpy(arr).to(torch.bfloat16).cuda()
+        q = U.ufp4_quantize_grouped(t, grid, seg, rht=rht, rht_seed=2, round=rnd, sr_seed=3,
+                                    colwise=colwise)
+        got = _gpu_segments(U, q, seg, colwise)
+        ref = oracle.quantize_grouped(arr, seg, grid, rht=rht, rht_seed=2, round_mode=rnd, sr_seed=3,
+                                      colwise=colwise)
+        _check_segments(got, ref, rht)
+
+
+def _deq(oracle, r, grid):
+    return oracle.dequantize(r["codes"], r["scales"], r["tensor_scale"], grid)
+
+
+@pytest.mark.parametrize("grid", [0, 1])
+def test_grouped_training_gemms(U, oracle, grid):
+    x, w, dy = _data()
+    E = len(COUNTS)
+    tx, tw, tdy = (torch.from_numpy(a).to(torch.bfloat16).cuda() for a in (x, w, dy))
+    wseg = [F] * E
+    qx_r = U.ufp4_quantize_grouped(tx, grid, COUNTS)
+    qx_c = U.ufp4_quantize_grouped(tx, grid, COUNTS, colwise=True)
+    qdy_r = U.ufp4_quantize_grouped(tdy, grid, COUNTS, round=1, sr_seed=3)
+    qdy_c = U.ufp4_quantize_grouped(tdy, grid, COUNTS, round=1, sr_seed=3, colwise=True)
+    qw_r = U.ufp4_quantize_grouped(tw, grid, wseg)
+    qw_c = U.ufp4_quantize_grouped(tw, grid, wseg, colwise=True)
+    rx_r = oracle.quantize_grouped(x, COUNTS, grid)
+    rx_c = oracle.quantize_grouped(x, COUNTS, grid, colwise=True)
+    rdy_r = oracle.quantize_grouped(dy, COUNTS, grid, round_mode=1, sr_seed=3)
+    rdy_c = oracle.quantize_grouped(dy, COUNTS, grid, round_mode=1, sr_seed=3, colwise=True)
+    rw_r = oracle.quantize_grouped(w, wseg, grid)
+    rw_c = oracle.quantize_grouped(w, wseg, grid, colwise=True)
+
+    T = sum(COUNTS)
+    y = torch.full((T, F), 9.0, device="cuda")
+    dx = torch.full((T, H), 9.0, device="cuda")
+    dw = torch.full((E * F, H), 9.0, device="cuda")
+    xo = U.grouped_offsets(COUNTS, False)
+    ko = U.grouped_offsets(COUNTS, True)
+    wo = U.grouped_offsets(wseg, False)
+    wk = U.grouped_offsets(wseg, True)
+    starts = np.concatenate([[0], np.cumsum(COUNTS)])
+    fy, fdx, fdw = [], [], []
+    for e, Te in enumerate(COUNTS):
+        s0 = int(starts[e])
+        fy.append(dict(M=Te, N=F, K=H, a_row=xo[e], a_k=0, b_row=wo[e], b_k=0, a_seg=e, b_seg=e,
+                       c=y[s0:s0 + Te] if Te else y[:1]))
+        fdx.append(dict(M=Te, N=H, K=F, a_row=xo[e], a_k=0, b_row=0, b_k=wk[e], a_seg=e, b_seg=e,
+                        c=dx[s0:s0 + Te] if Te else dx[:1]))
+        k16 = (Te + 15) // 16 * 16
+        fdw.append(dict(M=F, N=H, K=k16, a_row=0, a_k=ko[e], b_row=0, b_k=ko[e], a_seg=e, b_seg=e,
+                        c=dw[e * F:(e + 1) * F]))
+    U.ufp4_gemm_grouped(qx_r, qw_r, fy)
+    U.ufp4_gemm_grouped(qdy_r, qw_c, fdx)
+    U.ufp4_gemm_grouped(qdy_c, qx_c, fdw)
+    torch.cuda.synchronize()
+    y, dx, dw = y.cpu().numpy(), dx.cpu().numpy(), dw.cpu().numpy()
+    for e, Te in enumerate(COUNTS):
+        s0 = int(starts[e])
+        if Te == 0:
+            np.testing.assert_array_equal(dw[e * F:(e + 1) * F], 0.0)   # K = 0: zeros
+            continue
+        ref = oracle.gemm_f64(_deq(oracle, rx_r[e], grid), _deq(oracle, rw_r[e], grid))
+        assert np.linalg.norm(y[s0:s0 + Te] - ref) <= 1e-5 * np.linalg.norm(ref)
+        ref = oracle.gemm_f64(_deq(oracle, rdy_r[e], grid), _deq(oracle, rw_c[e], grid))
+        assert np.linalg.norm(dx[s0:s0 + Te] - ref) <= 1e-5 * np.linalg.norm(ref)
+        ref = oracle.gemm_f64(_deq(oracle, rdy_c[e], grid), _deq(oracle, rx_c[e], grid))
+        assert np.linalg.norm(dw[e * F:(e + 1) * F] - ref) <= 1e-5 * np.linalg.norm(ref)
+    # rows of y / dx that belong to no expert do not exist (sum T_e rows); all written
+    assert not np.any(y == 9.0) and not np.any(dx == 9.0)
