@@ -61,6 +61,9 @@ def lib():
                                            ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64,
                                            ctypes.c_uint64, ctypes.c_uint64, vp, vp, vp, vp, vp]
         L.ref_quantize_strided.restype = ctypes.c_int
+        L.ref_tensor_amax.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                      ctypes.c_uint64]
+        L.ref_tensor_amax.restype = ctypes.c_float
         L.ref_dequantize.argtypes = [vp, vp, ctypes.c_float, ctypes.c_int64, ctypes.c_int64,
                                      ctypes.c_int, ctypes.c_int, ctypes.c_uint64, vp]
         L.ref_gemm_f64.argtypes = [vp, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp]
@@ -152,6 +155,17 @@ def quantize(x, grid, rht=False, rht_seed=0, round_mode=RTNE, sr_seed=0, sr_coun
     if rc != 0:
         raise ValueError("ref_quantize failed (%d): k must be a multiple of 16" % rc)
     return dict(codes=codes, scales=scales, tensor_scale=float(ts[0]), y=y)
+
+
+def tensor_amax(x, rht=False, rht_seed=0, colwise=False):
+    """A_t of the quantization of x (of x.T when colwise), the step of
+    quantize() that needs the whole tensor."""
+    x = np.asarray(x, dtype=np.float32)
+    if colwise:
+        x = x.T
+    x = np.ascontiguousarray(x)
+    rows, k = x.shape
+    return float(lib().ref_tensor_amax(_p(x), rows, k, k, int(bool(rht)), ctypes.c_uint64(rht_seed)))
 
 
 def rpad128(t):

@@ -91,13 +91,19 @@ int32_t ref_hadamard16(int32_t i, int32_t j)
 
 /* y = (1/4) * H * diag(d) * x for one 16-block, in fp64, rounded to fp32
  * once.  READING: the 1/4 normalisation makes the transform orthonormal, so
- * two operands rotated with the same d along K keep their inner products. */
-static void rht16_forward(const float x[16], const int32_t d[16], float y[16])
+ * two operands rotated with the same d along K keep their inner products.
+ * hd[i][j] = H[i][j] * d[j] (+-1), built once per tensor by rht16_matrix. */
+static void rht16_matrix(const int32_t d[16], double hd[16][16])
+{
+    for (int i = 0; i < 16; ++i)
+        for (int j = 0; j < 16; ++j) hd[i][j] = (double)ref_hadamard16(i, j) * (double)d[j];
+}
+
+static void rht16_forward(const float x[16], const double hd[16][16], float y[16])
 {
     for (int i = 0; i < 16; ++i) {
         double s = 0.0;
-        for (int j = 0; j < 16; ++j)
-            s += (double)ref_hadamard16(i, j) * (double)d[j] * (double)x[j];
+        for (int j = 0; j < 16; ++j) s += hd[i][j] * (double)x[j];
         y[i] = (float)(0.25 * s);
     }
 }
@@ -262,7 +268,9 @@ int ref_quantize_strided(const float *x, int64_t rows, int64_t k, int64_t ld,
     const float qmax = (float)ref_grid_qmax(grid);
     const int64_t nb = k / 16;
     int32_t d[16];
+    double hd[16][16];
     ref_rht_signs(rht_seed, d);
+    rht16_matrix(d, hd);
 
     float *y = (float *)malloc(sizeof(float) * (size_t)(rows * k > 0 ? rows * k : 1));
     if (!y) return -2;
@@ -270,7 +278,7 @@ int ref_quantize_strided(const float *x, int64_t rows, int64_t k, int64_t ld,
         for (int64_t b = 0; b < nb; ++b) {
             const float *src = x + r * ld + b * 16;
             float *dst = y + r * k + b * 16;
-            if (rht) rht16_forward(src, d, dst);
+            if (rht) rht16_forward(src, hd, dst);
             else memcpy(dst, src, 16 * sizeof(float));
         }
 
@@ -317,6 +325,27 @@ int ref_quantize_strided(const float *x, int64_t rows, int64_t k, int64_t ld,
     if (y_out) memcpy(y_out, y, sizeof(float) * (size_t)(rows * k));
     free(y);
     return 0;
+}
+
+/* A_t = max |y| over a rows x k matrix (blocks along k), y the rotated blocks
+ * when rht is set -- the tensor amax step of ref_quantize on its own, so a
+ * sample of rows can be quantized against the whole tensor's scale. */
+float ref_tensor_amax(const float *x, int64_t rows, int64_t k, int64_t ld, int rht, uint64_t rht_seed)
+{
+    int32_t d[16];
+    double hd[16][16];
+    ref_rht_signs(rht_seed, d);
+    rht16_matrix(d, hd);
+    float A_t = 0.0f;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < k / 16; ++b) {
+            float y[16];
+            const float *src = x + r * ld + b * 16;
+            if (rht) rht16_forward(src, hd, y);
+            else memcpy(y, src, sizeof y);
+            for (int j = 0; j < 16; ++j) if (fabsf(y[j]) > A_t) A_t = fabsf(y[j]);
+        }
+    return A_t;
 }
 
 /* ------------------------------------------------------------------------

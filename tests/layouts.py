@@ -51,3 +51,24 @@ def unpack_scales(scale_bytes, rows, k):
     full = s[idx]
     pad = np.concatenate([full[rows:, :].ravel(), full[:rows, k // 16:].ravel()])
     return full[:rows, : k // 16], pad
+
+
+def rows_of(q, rows):
+    """Codes (one per element, [len(rows), k]) and row-major scales
+    ([len(rows), k/16]) of selected rows of a device QTensor."""
+    import torch
+    rows = np.asarray(rows, dtype=np.int64)
+    kp = kpad(q.k)
+    c2 = q.codes_2d()
+    idx = torch.as_tensor(rows, device=c2.device)
+    b = c2.index_select(0, idx).cpu().numpy()
+    codes = np.empty((len(rows), kp), dtype=np.uint8)
+    codes[:, 0::2] = b & 0xF
+    codes[:, 1::2] = b >> 4
+    nkt = kp // 64
+    bb = np.arange(q.k // 16)[None, :]
+    r = rows[:, None]
+    off = ((r // 128) * nkt + bb // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + (bb % 4)
+    s_all = q.scales
+    sc = s_all[torch.as_tensor(off.ravel(), device=s_all.device)].cpu().numpy().reshape(off.shape)
+    return codes[:, : q.k], sc

@@ -426,3 +426,15 @@ def test_compounding_chain_small(oracle):
     assert np.all(deltas > 0)                       # E2M1 attenuates every step
     lhs = math.log(np.prod(etas))
     assert abs(lhs + deltas.sum()) <= np.sum(deltas ** 2) + 1e-12
+
+
+def test_tensor_amax_is_quantize_step(oracle):
+    # the standalone amax gives the scale quantize() derives from the whole tensor
+    x = inputs.normal(27, (32, 64))
+    for rht in (False, True):
+        for col in (False, True):
+            a = oracle.tensor_amax(x, rht=rht, rht_seed=2, colwise=col)
+            q = oracle.quantize(x, 1, rht=rht, rht_seed=2, colwise=col)
+            assert q["tensor_scale"] == np.float32(np.float32(a) / np.float32(448 * 3.5))
+            assert a == np.abs(q["y"]).max()
+    assert oracle.tensor_amax(x) == np.abs(x).max()
