@@ -65,6 +65,23 @@ def peaks():
     return dict(FALLBACK, source="fallback")
 
 
+def reduce_max(v, world, device="cpu"):
+    """Max of a per-rank float over all ranks (one all-reduce; no-op at 1)."""
+    if world == 1:
+        return float(v)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_rate(units_per_rank, world, steps, max_ms, scale=1e9):
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time (each rank runs its own copy of the workload)."""
+    return world * steps * units_per_rank / (max_ms * 1e-3) / scale
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -237,17 +254,13 @@ def run_gpu(args):
     tq, tg, tstep = sum(q_ms), sum(sum(g) for g in g_ms), sum(step_ms)
 
     def allmax(v):
-        if ws_n == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(v, ws_n, dev)
 
     tq, tg, tstep = allmax(tq), allmax(tg), allmax(tstep)
     q_bytes = step.q_elems * Q_BYTES_PER_ELEM
-    q_gbs = ws_n * args.steps * q_bytes / (tq * 1e-3) / 1e9
+    q_gbs = weak_scaling_rate(q_bytes, ws_n, args.steps, tq)
     flops = sum(step.flops_each)
-    gemm_tflops = ws_n * args.steps * flops / (tg * 1e-3) / 1e12
+    gemm_tflops = weak_scaling_rate(flops, ws_n, args.steps, tg, 1e12)
     per_gpu_tflops = gemm_tflops / ws_n
     fp8_peak = pk["bf16_tflops"] * 2.0    # nominal dense ratio fp8:bf16 = 4.5 : 2.25
     fp4_peak = pk["bf16_tflops"] * 6.0    # nominal dense ratio fp4:bf16 = 13.5 : 2.25
@@ -513,6 +526,187 @@ def run_kernel(args):
     print(json.dumps({"kernel": kind, "ms": round(ms, 4), "rate": round(rate, 1), "unit": unit}))
 
 
+
+# ------------------------------------------------------------ all workloads
+def _ev_time(fn, flush, reps=10):
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    tot = 0.0
+    for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(); fn(); b.record()
+        torch.cuda.synchronize()
+        tot += a.elapsed_time(b)
+    return tot / reps
+
+
+def run_workloads(args):
+    """Every synthetic workload at 1 GPU: quantizer GB/s, GEMM TFLOP/s and the
+    numerics the pages discuss (alpha, SQNR, bias, prod eta).  One JSON line
+    per workload."""
+    import torch
+    from fp4_quantized_numerics_gb300 import build, inputs, ufp4 as U
+    build.build()
+    dev = torch.device("cuda", 0)
+    pk = peaks()
+    flush = L2Flush(dev)
+    out = []
+
+    def emit(d):
+        print(json.dumps(d), flush=True)
+        out.append(d)
+
+    def stats_of(x, grid, rht):
+        q = U.ufp4_quantize(x, grid, rht=rht, rht_seed=2)
+        st = U.ufp4_stats(x, q, rht=rht, rht_seed=2)
+        return {k: round(st[k], 6) for k in ("alpha", "sqnr_db", "mean_bias")}
+
+    # smoke: 256 x 1024 tensor, 256^3 GEMM
+    d = inputs.smoke(0)
+    x = torch.from_numpy(d["x"]).to(torch.bfloat16).to(dev)
+    a = torch.from_numpy(d["a"]).to(torch.bfloat16).to(dev)
+    b = torch.from_numpy(d["b"]).to(torch.bfloat16).to(dev)
+    r = {"workload": "smoke_256x1024", "numerics": {}}
+    for g, gn in ((0, "e2m1"), (1, "e1m2")):
+        for rht in (False, True):
+            r["numerics"]["%s_rht_%s" % (gn, "on" if rht else "off")] = stats_of(x, g, rht)
+        qa, qb = U.ufp4_quantize(a, g), U.ufp4_quantize(b, g)
+        c = torch.empty(256, 256, device=dev)
+        ms = _ev_time(lambda: U.ufp4_gemm(qa, qb, out=c), flush)
+        r["gemm_%s_tflops" % gn] = round(2 * 256 ** 3 / (ms * 1e-3) / 1e12, 3)
+    emit(r)
+
+    # outlier: 4096 x 4096, RHT on/off, both grids
+    d = inputs.outlier(0)
+    x = torch.from_numpy(d["x"]).to(torch.bfloat16).to(dev)
+    r = {"workload": "outlier_4096x4096", "numerics": {}, "quantize_gbs": {}}
+    for g, gn in ((0, "e2m1"), (1, "e1m2")):
+        for rht in (False, True):
+            key = "%s_rht_%s" % (gn, "on" if rht else "off")
+            r["numerics"][key] = stats_of(x, g, rht)
+            q = U.QTensor.empty(4096, 4096, g, dev)
+            ms = _ev_time(lambda: U.ufp4_quantize(x, g, rht=rht, rht_seed=2, out=q), flush)
+            r["quantize_gbs"][key] = round(x.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
+    n = r["numerics"]
+    r["sqnr_ranking"] = {
+        "before_rht_e2m1_minus_e1m2_db": round(n["e2m1_rht_off"]["sqnr_db"] - n["e1m2_rht_off"]["sqnr_db"], 3),
+        "after_rht_e2m1_minus_e1m2_db": round(n["e2m1_rht_on"]["sqnr_db"] - n["e1m2_rht_on"]["sqnr_db"], 3)}
+    emit(r)
+
+    # dense 1.5B training step (both grids)
+    dd = inputs.device_dense(seed=0, device=dev)
+    for g, gn in ((1, "e1m2"), (0, "e2m1")):
+        st = Step(U, dd["x"], dd["w"], dd["dy"], g)
+        mq = _ev_time(st.quantize_all, flush)
+        mg = _ev_time(st.gemms, flush)
+        emit({"workload": "dense1p5b_step_" + gn, "quantize_ms": round(mq, 4),
+              "quantize_gbs": round(st.q_elems * Q_BYTES_PER_ELEM / (mq * 1e-3) / 1e9, 1),
+              "gemm_ms": round(mg, 4), "gemm_tflops": round(sum(st.flops_each) / (mg * 1e-3) / 1e12, 1)})
+    del dd
+
+    # MoE 7.9B grouped step
+    m = inputs.moe(seed=0)
+    counts = [int(c) for c in m["counts"]]
+    E, H, F = len(counts), 2048, 1408
+    tx = torch.from_numpy(m["x"]).to(torch.bfloat16).to(dev)
+    tw = torch.from_numpy(m["w"]).to(torch.bfloat16).to(dev)
+    tdy = torch.from_numpy(m["dy"]).to(torch.bfloat16).to(dev)
+    T = sum(counts)
+    starts = np.concatenate([[0], np.cumsum(counts)])
+    for g, gn in ((1, "e1m2"), (0, "e2m1")):
+        kw = dict(rht=True, rht_seed=2)
+        qs = {}
+
+        def quant_all():
+            qs["xr"] = U.ufp4_quantize_grouped(tx, g, counts, out=qs.get("xr"), **kw)
+            qs["xc"] = U.ufp4_quantize_grouped(tx, g, counts, colwise=True, out=qs.get("xc"), **kw)
+            qs["dr"] = U.ufp4_quantize_grouped(tdy, g, counts, round=1, sr_seed=3, out=qs.get("dr"), **kw)
+            qs["dc"] = U.ufp4_quantize_grouped(tdy, g, counts, round=1, sr_seed=3, colwise=True,
+                                               out=qs.get("dc"), **kw)
+            qs["wr"] = U.ufp4_quantize_grouped(tw, g, [F] * E, out=qs.get("wr"), **kw)
+            qs["wc"] = U.ufp4_quantize_grouped(tw, g, [F] * E, colwise=True, out=qs.get("wc"), **kw)
+        quant_all()
+        y = torch.empty(T, F, device=dev)
+        dx = torch.empty(T, H, device=dev)
+        dw = torch.empty(E * F, H, device=dev)
+        xo, ko = U.grouped_offsets(counts, False), U.grouped_offsets(counts, True)
+        wo, wk = U.grouped_offsets([F] * E, False), U.grouped_offsets([F] * E, True)
+        gy = [dict(M=counts[e], N=F, K=H, a_row=xo[e], a_k=0, b_row=wo[e], b_k=0, a_seg=e, b_seg=e,
+                   c=y[starts[e]:starts[e] + counts[e]] if counts[e] else y[:1]) for e in range(E)]
+        gx = [dict(M=counts[e], N=H, K=F, a_row=xo[e], a_k=0, b_row=0, b_k=wk[e], a_seg=e, b_seg=e,
+                   c=dx[starts[e]:starts[e] + counts[e]] if counts[e] else dx[:1]) for e in range(E)]
+        gw = [dict(M=F, N=H, K=(counts[e] + 15) // 16 * 16, a_row=0, a_k=ko[e], b_row=0, b_k=ko[e],
+                   a_seg=e, b_seg=e, c=dw[e * F:(e + 1) * F]) for e in range(E)]
+
+        def gemm_all():
+            U.ufp4_gemm_grouped(qs["xr"], qs["wr"], gy)
+            U.ufp4_gemm_grouped(qs["dr"], qs["wc"], gx)
+            U.ufp4_gemm_grouped(qs["dc"], qs["xc"], gw)
+        mq = _ev_time(quant_all, flush, 5)
+        mg = _ev_time(gemm_all, flush, 5)
+        elems = 2 * (tx.numel() + tw.numel() + tdy.numel())
+        flops = 3 * 2.0 * T * F * H
+        emit({"workload": "moe7p9b_grouped_step_" + gn, "experts": E, "routed_tokens": T,
+              "zero_token_experts": int(sum(1 for c in counts if c == 0)),
+              "quantize_ms": round(mq, 4), "quantize_gbs": round(elems * Q_BYTES_PER_ELEM / (mq * 1e-3) / 1e9, 1),
+              "gemm_ms": round(mg, 4), "gemm_tflops": round(flops / (mg * 1e-3) / 1e12, 1)})
+    del tx, tw, tdy, m
+
+    # MoE 124B large layer
+    x = inputs.device_normal((65536, 8192), 1.0, 31, dev)
+    w = inputs.device_normal((2048, 8192), 0.01, 32, dev)
+    dy = inputs.device_normal((65536, 2048), 1e-3, 33, dev)
+    for g, gn in ((1, "e1m2"), (0, "e2m1")):
+        st = Step(U, x, w, dy, g)
+        mq = _ev_time(st.quantize_all, flush, 3)
+        mg = _ev_time(st.gemms, flush, 3)
+        emit({"workload": "moe124b_layer_" + gn, "quantize_ms": round(mq, 4),
+              "quantize_gbs": round(st.q_elems * Q_BYTES_PER_ELEM / (mq * 1e-3) / 1e9, 1),
+              "gemm_ms": round(mg, 4), "gemm_tflops": round(sum(st.flops_each) / (mg * 1e-3) / 1e12, 1)})
+        del st
+    del x, w, dy
+    torch.cuda.empty_cache()
+
+    # compounding-attenuation chain: 100 x (4096^3), fresh W_k ~ N(0, 1/64)
+    n, steps = 4096, 100
+    rows = torch.arange(0, n, n // 64, device=dev)
+    for g, gn in ((0, "e2m1"), (1, "e1m2")):
+        for rht in (False, True):
+            X = inputs.device_normal((n, n), 1.0, 50, dev, dtype=torch.float32)
+            norm0 = float(X.double().norm())
+            ln_prod, sum_delta, ln_alpha = 0.0, 0.0, 0.0
+            qx = U.QTensor.empty(n, n, g, dev)
+            qw = U.QTensor.empty(n, n, g, dev)
+            Y = torch.empty(n, n, device=dev)
+            t_gpu = 0.0
+            for k in range(steps):
+                W = inputs.device_normal((n, n), 1.0 / 64, 1000 + k, dev)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                U.ufp4_quantize(X, g, rht=rht, rht_seed=2, out=qx)
+                U.ufp4_quantize(W, g, rht=rht, rht_seed=2, out=qw)
+                U.ufp4_gemm(qx, qw, out=Y)
+                e1.record()
+                torch.cuda.synchronize()
+                t_gpu += e0.elapsed_time(e1)
+                yref = X[rows].double() @ W.double().t()
+                eta = float((Y[rows].double() * yref).sum() / (yref * yref).sum())
+                ax = U.ufp4_stats(X, qx, rht=rht, rht_seed=2)["alpha"]
+                aw = U.ufp4_stats(W, qw, rht=rht, rht_seed=2)["alpha"]
+                ln_prod += float(np.log(eta))
+                sum_delta += 1.0 - eta
+                ln_alpha += float(np.log(ax * aw))
+                X, Y = Y, X
+            emit({"workload": "attenuation_chain_4096_x100_%s_rht_%s" % (gn, "on" if rht else "off"),
+                  "prod_eta": round(float(np.exp(ln_prod)), 6), "exp_minus_sum_delta": round(float(np.exp(-sum_delta)), 6),
+                  "prod_alpha_x_alpha_w": round(float(np.exp(ln_alpha)), 6),
+                  "norm_ratio": round(float(X.double().norm()) / norm0, 6),
+                  "gpu_ms_per_layer": round(t_gpu / steps, 4),
+                  "layer_tflops": round(2.0 * n ** 3 / (t_gpu / steps * 1e-3) / 1e12, 1)})
+    return out
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -522,6 +716,8 @@ def main():
     ap.add_argument("--quick", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workloads", action="store_true",
+                    help="measure every synthetic workload (one JSON line each) instead of the step")
     ap.add_argument("--kernel", default=None,
                     choices=["gemm_e2m1", "gemm_e1m2", "quant_row_e1m2", "quant_col_e1m2",
                              "quant_row_e2m1", "quant_col_e2m1"],
@@ -533,6 +729,8 @@ def main():
         run_reference(args)
     elif args.kernel:
         run_kernel(args)
+    elif args.workloads:
+        run_workloads(args)
     else:
         run_gpu(args)
 

@@ -1,0 +1,53 @@
+"""The benchmark's multi-rank host logic on CPU: two gloo ranks (127.0.0.1)
+agree on the slowest rank's time and report the whole-job weak-scaling rate.
+No GPU: the data path has no collective; only this timing reduction does."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    ws, r, _ = bench.dist_env()
+    my_ms = 10.0 + 5.0 * rank           # rank 1 is the slow one
+    mx = bench.reduce_max(my_ms, ws)
+    rate = bench.weak_scaling_rate(1e9, ws, 4, mx)
+    dist.barrier()
+    q.put((r, ws, mx, rate))
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_reduce_max_and_rate():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, ws, mx, rate in res:
+        assert ws == 2 and mx == 15.0
+        assert rate == pytest.approx(2 * 4 * 1e9 / 15e-3 / 1e9)
+
+
+def test_single_rank_is_identity():
+    import bench
+    assert bench.reduce_max(3.5, 1) == 3.5
+    assert bench.weak_scaling_rate(2e9, 1, 10, 1000.0) == pytest.approx(20.0)
