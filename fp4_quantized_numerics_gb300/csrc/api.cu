@@ -254,12 +254,12 @@ ufp4_status ufp4_gemm_grouped(const ufp4_qtensor *a, const ufp4_qtensor *b, cons
         GroupGemm &t = tab->g[m];
         t.M = (int32_t)g.M; t.N = (int32_t)g.N;
         t.nkt = (int32_t)(kpad_of(g.K) / 64);
-        t.ntn = (int32_t)((g.N + 127) / 128);
+        t.ntn = (int32_t)((g.N + kGemmBN - 1) / kGemmBN);
         t.a_rt = (int32_t)(g.a_row / 128); t.a_kt = (int32_t)(g.a_k / 64);
         t.b_rt = (int32_t)(g.b_row / 128); t.b_kt = (int32_t)(g.b_k / 64);
         t.a_seg = g.a_seg; t.b_seg = g.b_seg;
         t.c = g.c; t.ldc = g.ldc;
-        tiles += (int64_t)((g.M + 127) / 128) * t.ntn;
+        tiles += (int64_t)((g.M + kGemmBM - 1) / kGemmBM) * t.ntn;
         if (tiles > INT32_MAX) return UFP4_ERR_UNSUPPORTED;
         ++m;
         tab->tiles[m] = (int32_t)tiles;

@@ -11,21 +11,24 @@
 // E2M1: the codes ARE the tensor cores' E2M1 elements and the block scales
 //   are UE4M3 scale_vec::4X factors, so each 64-wide K step is one
 //   tcgen05.mma.kind::mxf4nvf4.block_scale.
-// E1M2: not a tensor-core format.  Each magnitude m/2 splits exactly as
-//   a + b/2 with a = m >> 1 in {0,1,2,3} and b = m & 1, both representable in
-//   E2M1 (a -> 0,1,2,3; b/2 -> 0 or 0.5), with the sign copied to both parts
-//   and the block scale shared.  Warps expand each staged tile into a "hi"
-//   and a "lo" E2M1 plane in shared memory and four MMAs (hi*hi, hi*lo,
-//   lo*hi, lo*lo) accumulate into the same TMEM accumulator -- exact, since
-//   every product and partial sum of the dequantized values is what the
-//   single E1M2 product would give.
+// E1M2: not a tensor-core format.  Read as an E2M1 code, an E1M2 nibble m has
+//   the value R(m) in {0,.5,1,1.5,2,3,4,6}; the E1M2 value m/2 equals
+//   (R(m) + E(m)) / 2 with E(m) in {0,.5,1,1.5,2,2,2,1}, also E2M1.  The raw
+//   tile is therefore used as it was loaded, expander warps write one extra
+//   E plane per operand, and four MMAs (R*R, R*E, E*R, E*E) with the shared
+//   block scales accumulate 4 * A B^T, the factor 1/4 being applied (exactly)
+//   in the epilogue.
 //
-// CTA: 192 threads.  Warp 0 = TMA producer, warp 1 = TMEM owner + single-
-// thread MMA issuer, warps 2-5 = epilogue (and, for E1M2, the expanders).
-// Tile 128 x 128, K step per stage 256 (128 bytes per row, one 128-byte
-// swizzle atom), multi-stage mbarrier ring, accumulator in TMEM.
-// Every wait is bounded: on timeout the kernel raises g_ufp4_timeout, drains
-// its own copies, frees TMEM and returns.
+// CTA tile 128 x 256 (one M=128, N=256 MMA per K step); the K stage depth
+// and the rings differ per grid (Cfg below).  Warp 0 = TMA producer, warp 1
+// = TMEM owner + single-thread MMA issuer, warps 2-9 = epilogue (two per TMEM
+// lane quadrant, 128 columns each), warps 10-15 (E1M2) = expanders.  The
+// accumulator (256 TMEM columns) is single-buffered: the epilogue pulls the
+// whole tile out (registers and shared staging) and hands the columns back
+// before it stores, so the stores overlap the next tile's MMAs.  Block scales
+// are staged in TMEM after the accumulator, 12 columns per MMA K step.  Every
+// wait is bounded: on timeout the kernel raises g_ufp4_timeout, drains its
+// own copies, frees TMEM and returns.
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -44,34 +47,52 @@ __device__ uint32_t g_ufp4_timeout;
 
 namespace {
 
-constexpr int BM = 128, BN = 128;
-constexpr int BK_BYTES = 128;                 // 256 FP4 elements per stage
-constexpr uint32_t TILE_BYTES = 128 * 128;    // 16 KB per operand tile
-constexpr uint32_t SF_BYTES = 4 * 512;        // 4 scale atoms per operand per stage
+constexpr int BM = kGemmBM, BN = kGemmBN;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfCol = 256;              // accumulators in [0, 256), scales after
+constexpr uint32_t kSfCol = 256;                   // accumulator in [0, 256), scales after
+constexpr int kEpiWarps = 8;
 constexpr long long kWaitBudget = 2000000000LL;
 
+// Per-grid pipeline geometry.
+//  E2M1: K stage of 128 bytes (4 MMA K steps, 128-byte swizzle) so that the
+//        issuing thread's per-stage wait/commit latency stays below the
+//        stage's tensor-core time; 3 stages.
+//  E1M2: K stage of 64 bytes (2 K steps, 64-byte swizzle, 8 MMAs); a 3-deep
+//        ring of raw tiles fed by TMA and a 3-slot ring of E planes written
+//        by six expander warps (16 warps in all: the 128 registers a thread
+//        then gets still hold the epilogue's accumulator chunks).
 template <int GRID>
 struct Cfg {
-    static constexpr int kStages = GRID == kE2M1 ? 5 : 3;
-    // warps: 0 producer, 1 MMA, 2-5 epilogue, (E1M2) 6-13 expanders
-    static constexpr int kThreads = GRID == kE2M1 ? 192 : 448;
-    static constexpr int kExpThreads = kThreads - 192;
-    // epilogue staging: per epilogue warp, kEpiBufs buffers of 32 rows x 32
-    // fp32 columns (4 KB, 128-byte swizzled rows) feeding TMA stores
-    static constexpr int kEpiBufs = GRID == kE2M1 ? 2 : 1;
-    // stage layout: A | B | (A_lo | B_lo for E1M2) | SFA | SFB
+    static constexpr int kBK = GRID == kE2M1 ? 128 : 64;            // bytes of K per stage
+    static constexpr int kKS = kBK / 32;                             // MMA K steps per stage
+    static constexpr uint32_t kSwz = GRID == kE2M1 ? 2 : 4;          // descriptor swizzle: 128B / 64B
+    static constexpr uint32_t kSbo = 8 * kBK;                        // 8-row core-matrix group stride
+    static constexpr uint32_t kABytes = BM * kBK, kBBytes = BN * kBK;
+    static constexpr uint32_t kSfaBytes = kKS * 512;                 // one 128-row atom per K step
+    static constexpr uint32_t kSfbBytes = 2 * kKS * 512;             // two 128-row halves
+    static constexpr uint32_t kSfColsPerStage = 12 * kKS;            // SFA 4 + SFB 8 columns per K step
+    static constexpr int kStages = 3;
+    static constexpr int kESlots = GRID == kE2M1 ? 0 : 3;
+    static constexpr int kExpWarps = GRID == kE2M1 ? 0 : 6;
+    // E2M1: one extra warp issues the block-scale copies
+    static constexpr int kScaleWarps = GRID == kE2M1 ? 1 : 0;
+    static constexpr int kThreads = 32 * (2 + kEpiWarps + kScaleWarps + kExpWarps);
+    // epilogue staging buffers (32 x 32 fp32, 4 KB) per epilogue warp
+    static constexpr int kEpiBufs = GRID == kE2M1 ? 1 : 2;
+    // stage layout: A | B | SFA | SFB;  E slots: E_A | E_B
     static constexpr uint32_t kAOff = 0;
-    static constexpr uint32_t kBOff = TILE_BYTES;
-    static constexpr uint32_t kALoOff = 2 * TILE_BYTES;
-    static constexpr uint32_t kBLoOff = 3 * TILE_BYTES;
-    static constexpr uint32_t kSfaOff = (GRID == kE2M1 ? 2 : 4) * TILE_BYTES;
-    static constexpr uint32_t kSfbOff = kSfaOff + SF_BYTES;
-    static constexpr uint32_t kStageBytes = kSfbOff + SF_BYTES;  // multiple of 1024
-    static constexpr uint32_t kEpiOff = kStages * kStageBytes;
-    static constexpr uint32_t kBarOff = kEpiOff + 4 * kEpiBufs * 4096;
-    static constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;  // + barriers + alignment slack
+    static constexpr uint32_t kBOff = kABytes;
+    static constexpr uint32_t kSfaOff = kABytes + kBBytes;
+    static constexpr uint32_t kSfbOff = kSfaOff + kSfaBytes;
+    static constexpr uint32_t kStageBytes = kSfbOff + kSfbBytes;     // multiple of 1024
+    static constexpr uint32_t kESlotBytes = kABytes + kBBytes;
+    static constexpr uint32_t kEOff = kStages * kStageBytes;
+    static constexpr uint32_t kEpiOff = kEOff + kESlots * kESlotBytes;
+    static constexpr uint32_t kBarOff = kEpiOff + kEpiWarps * kEpiBufs * 4096;
+    static constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;   // + barriers + alignment slack
+    static_assert(kStageBytes % 1024 == 0 && kESlotBytes % 1024 == 0, "tile alignment");
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+    static_assert(kSfCol + kStages * kSfColsPerStage <= kTmemCols, "TMEM columns");
 };
 
 struct GemmParams {
@@ -81,9 +102,10 @@ struct GemmParams {
     int64_t ldc;
     int M, N;
     int nkt;      // kpad / 64: scale atoms per 128-row tile
-    int num_kb;   // ceil(nkt / 4): K stages per tile
+    int num_kb;   // ceil(nkt / K steps per stage): K stages per tile
     int ntm, ntn; // tiles along M and N
     int nkt_a, nkt_b;  // k atoms per 128-row tile of the whole A / B tensors
+    int b_rt;     // 128-row scale tiles in the whole B tensor
 };
 
 // Where one output tile lives: operand rows / k atoms in the A and B tensors,
@@ -98,6 +120,7 @@ struct TileInfo {
 
 struct NoGroups {};
 
+template <int KS>
 __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const NoGroups &, int t) {
     TileInfo ti;
     ti.m_loc = (t / p.ntn) * BM;
@@ -117,6 +140,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const NoGroup
     return ti;
 }
 
+template <int KS>
 __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const GroupGemmTab &tab, int t) {
     int lo = 0, hi = tab.n;   // largest g with tiles[g] <= t
     while (hi - lo > 1) {
@@ -133,7 +157,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const GroupGe
     ti.a_kt = g.a_kt;
     ti.b_kt = g.b_kt;
     ti.nkt = g.nkt;
-    ti.num_kb = (g.nkt + 3) / 4;
+    ti.num_kb = (g.nkt + KS - 1) / KS;
     ti.M = g.M;
     ti.N = g.N;
     ti.c = g.c;
@@ -162,19 +186,19 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     }
 }
 
-// E1M2 nibbles s|m2 m1 m0 -> (hi, lo) E2M1 nibbles, 8 at a time.  With
-// a = m >> 1, the E2M1 code of a in {0,1,2,3} is {0,2,4,5} = 2a - [a == 3];
-// 2a sits in bits 2..1 already, so hi = (w & 0xE...) - (m1 & m2) (no borrow
-// leaves a nibble); lo keeps the sign and m0 (E2M1 code 1 = 0.5).
-__device__ __forceinline__ void split_e1m2(uint32_t w, uint32_t &hi, uint32_t &lo) {
-    hi = (w & 0xEEEEEEEEu) - ((w >> 1) & (w >> 2) & 0x11111111u);
-    lo = w & 0x99999999u;
+// E plane of 8 E1M2 nibbles s|b2 b1 b0 (m = 4 b2 + 2 b1 + b0): E2M1 code m
+// for m < 4, 4 (value 2) for m in {4,5,6}, 2 (value 1) for m = 7; sign kept.
+// Per nibble the E code is the input masked by: bit 0 kept iff !b2, bit 1
+// iff (!b2 | b0), bit 2 iff !(b0 & b1), bit 3 (sign) always -- the shifted
+// copies line the other bits up with each position.
+__device__ __forceinline__ uint32_t e1m2_eplane(uint32_t w) {
+    const uint32_t u = w >> 1, v = w << 1, t = w >> 2, x = w << 2;
+    const uint32_t keep = (~t & 0x11111111u) | ((~u | v) & 0x22222222u) | (~(x & v) & 0x44444444u) | 0x88888888u;
+    return w & keep;
 }
 
 // Persistent CTA: tiles t = blockIdx.x, blockIdx.x + gridDim.x, ... in
-// row-major (M, N) tile order.  The K ring and the two TMEM accumulators are
-// carried across tiles, so the epilogue of one tile overlaps the main loop
-// of the next.
+// row-major (M, N) tile order; the K ring is carried across tiles.
 template <int GRID, class TAB>
 __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
@@ -185,18 +209,24 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
-    // bars: [0,S) full, [S,2S) empty, [2S,3S) expanded, 3S+{0,1} acc full,
-    // 3S+{2,3} acc empty, 3S+4 MMA drained
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * S + 5);
+    constexpr int ES = C::kESlots > 0 ? C::kESlots : 1;
+    // bars: [0,S) full, [S,2S) empty, [2S,2S+ES) E slot written, [2S+ES,2S+2ES)
+    // E slot free, then acc full, acc empty, MMA drained, then [.., +S) scales
+    // of a stage copied into TMEM
+    constexpr int kNBars = 3 * S + 2 * ES + 3;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNBars);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    static_assert(kNBars * 8 + 8 <= 256, "barrier area");
     const uint32_t smem_base = ptx::smem_u32(smem);
     const uint32_t bar_base = ptx::smem_u32(bars);
     auto full = [&](int s) { return bar_base + 8u * s; };
     auto empty = [&](int s) { return bar_base + 8u * (S + s); };
-    auto expd = [&](int s) { return bar_base + 8u * (2 * S + s); };
-    auto accf = [&](int b) { return bar_base + 8u * (3 * S + b); };
-    auto acce = [&](int b) { return bar_base + 8u * (3 * S + 2 + b); };
-    const uint32_t drained = bar_base + 8u * (3 * S + 4);
+    auto expd = [&](int e) { return bar_base + 8u * (2 * S + e); };
+    auto efree = [&](int e) { return bar_base + 8u * (2 * S + ES + e); };
+    const uint32_t accf = bar_base + 8u * (2 * S + 2 * ES);
+    const uint32_t acce = accf + 8u;
+    const uint32_t drained = accf + 16u;
+    auto sfr = [&](int s) { return accf + 24u + 8u * s; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int ntiles;
@@ -207,12 +237,14 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         for (int s = 0; s < S; ++s) {
             ptx::mbar_init(full(s), 1);
             ptx::mbar_init(empty(s), 1);
-            ptx::mbar_init(expd(s), GRID == kE1M2 ? C::kExpThreads / 32 : 1);   // one arrival per expander warp
+            ptx::mbar_init(sfr(s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(accf(b), 1);
-            ptx::mbar_init(acce(b), 4);   // one arrival per epilogue warp
+        for (int e = 0; e < ES; ++e) {
+            ptx::mbar_init(expd(e), GRID == kE1M2 ? C::kExpWarps : 1);   // one arrival per expander warp
+            ptx::mbar_init(efree(e), 1);
         }
+        ptx::mbar_init(accf, 1);
+        ptx::mbar_init(acce, kEpiWarps);   // one arrival per epilogue warp
         ptx::mbar_init(drained, 1);
         *abort = 0;
         ptx::fence_mbar_init();
@@ -229,27 +261,61 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // Block-scale copies of stage s into its TMEM columns: SFA 4 columns per
+    // K step at [0, 4 KS), SFB 8 columns per K step (rows 0-127, then
+    // 128-255) at [4 KS, 12 KS).  E2M1 issues them from their own warp so
+    // that they overlap the MMAs (completion signalled on sfr(s)); E1M2,
+    // with 4x the MMAs per stage, issues them in line from the MMA thread.
+    auto copy_scales = [&](uint32_t s, int atoms, bool signal) {
+        const uint64_t hi_sf = ptx::sdesc(0, 0, 128, 0);   // 32 rows x 16 B scale atom
+        const uint32_t st = smem_base + s * C::kStageBytes;
+        const uint64_t dsa = hi_sf | (uint64_t)(((st + C::kSfaOff) & 0x3FFFFu) >> 4);
+        const uint64_t dsb = hi_sf | (uint64_t)(((st + C::kSfbOff) & 0x3FFFFu) >> 4);
+        const uint32_t sf_t = tmem + kSfCol + C::kSfColsPerStage * s;
+        const uint32_t sfa0 = sf_t, sfb0 = sf_t + 4u * C::kKS;
+        ptx::tc_fence_after();
+        for (int j = 0; j < atoms; ++j) {
+            ptx::tc_cp_32x128b_warpx4(sfa0 + 4u * j, dsa + 32u * j);
+            ptx::tc_cp_32x128b_warpx4(sfb0 + 8u * j, dsb + 32u * j);
+            ptx::tc_cp_32x128b_warpx4(sfb0 + 8u * j + 4u, dsb + 32u * (C::kKS + j));
+        }
+        if (signal) ptx::tc_commit(sfr(s));
+    };
+    // The copy thread's last commits must complete before TMEM is freed.
+    auto drain_scales = [&](uint32_t g) {
+        for (uint32_t h = g > (uint32_t)S ? g - S : 0; h < g; ++h) {
+            const long long t0 = clock64();
+            while (!ptx::mbar_try_wait(sfr(h % S), (h / S) & 1))
+                if (clock64() - t0 > kWaitBudget) { raise_timeout(); break; }
+        }
+    };
+
     if (warp == 0) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
             uint32_t g = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const TileInfo ti = tile_info(p, tab, t);
+                const TileInfo ti = tile_info<C::kKS>(p, tab, t);
+                // the B tile's second 128 rows have scales only inside the tensor
+                const bool b_hi = ti.b_row / 128 + 1 < p.b_rt;
                 for (int kb = 0; kb < ti.num_kb; ++kb, ++g) {
                     const uint32_t s = g % S, round = g / S;
                     if (round > 0 && !wait_or_abort(empty(s), (round - 1) & 1, abort)) { ok = false; break; }
-                    const int atoms = min(4, ti.nkt - 4 * kb);
+                    const uint32_t atoms = (uint32_t)min(C::kKS, ti.nkt - C::kKS * kb);
                     const uint32_t st = smem_base + s * C::kStageBytes;
-                    ptx::mbar_arrive_expect_tx(full(s), 2 * TILE_BYTES + 2u * atoms * 512u);
-                    ptx::tma_load_2d(st + C::kAOff, &tma_a, ti.a_kt * 32 + kb * BK_BYTES, ti.a_row, full(s));
-                    ptx::tma_load_2d(st + C::kBOff, &tma_b, ti.b_kt * 32 + kb * BK_BYTES, ti.b_row, full(s));
+                    ptx::mbar_arrive_expect_tx(full(s), C::kABytes + C::kBBytes + atoms * 512u * (b_hi ? 3u : 2u));
+                    ptx::tma_load_2d(st + C::kAOff, &tma_a, ti.a_kt * 32 + kb * C::kBK, ti.a_row, full(s));
+                    ptx::tma_load_2d(st + C::kBOff, &tma_b, ti.b_kt * 32 + kb * C::kBK, ti.b_row, full(s));
                     ptx::bulk_load(st + C::kSfaOff,
-                                   p.sfa + ((size_t)(ti.a_row / 128) * p.nkt_a + ti.a_kt + 4 * kb) * 512,
+                                   p.sfa + ((size_t)(ti.a_row / 128) * p.nkt_a + ti.a_kt + C::kKS * kb) * 512,
                                    atoms * 512u, full(s));
-                    ptx::bulk_load(st + C::kSfbOff,
-                                   p.sfb + ((size_t)(ti.b_row / 128) * p.nkt_b + ti.b_kt + 4 * kb) * 512,
-                                   atoms * 512u, full(s));
+                    const uint8_t *sfb =
+                        p.sfb + ((size_t)(ti.b_row / 128) * p.nkt_b + ti.b_kt + C::kKS * kb) * 512;
+                    ptx::bulk_load(st + C::kSfbOff, sfb, atoms * 512u, full(s));
+                    if (b_hi)
+                        ptx::bulk_load(st + C::kSfbOff + C::kKS * 512u, sfb + (size_t)p.nkt_b * 512, atoms * 512u,
+                                       full(s));
                 }
             }
             // every copy this thread started has landed before the CTA exits
@@ -261,64 +327,59 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         }
     } else if (warp == 1) {
         // --------------------------------------------------------- MMA issuer
-        // One thread issues every tcgen05 op of the CTA, so its instruction
-        // stream is kept short: descriptors are built once per stage and
-        // advanced by integer adds (start address field = bytes >> 4).
+        // One thread issues every MMA of the CTA; descriptors are built once
+        // per stage and advanced by integer adds (address field = bytes >> 4).
         if (lane == 0) {
             // instruction descriptor, kind::mxf4nvf4: A/B E2M1 (1), K-major,
             // N >> 3 at [17,23), UE4M3 scales (bit 23 = 0), M >> 4 at [24,29).
             const uint32_t idesc = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                                    ((uint32_t)(BM >> 4) << 24);
-            const uint64_t hi_op = ptx::sdesc(0, 16, 1024, 2);   // 128B-swizzled K-major operand
-            const uint64_t hi_sf = ptx::sdesc(0, 0, 128, 0);     // 32 rows x 16 B scale atom
+            const uint64_t hi_op = ptx::sdesc(0, 16, C::kSbo, C::kSwz);   // swizzled K-major operand
             auto mk = [](uint64_t hi, uint32_t addr) { return hi | (uint64_t)((addr & 0x3FFFFu) >> 4); };
             uint32_t g = 0, it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
-                const TileInfo ti = tile_info(p, tab, t);
-                const uint32_t b = it & 1, use = it >> 1;
-                if (use > 0 && !wait_or_abort(acce(b), (use - 1) & 1, abort)) { ok = false; break; }
+                const TileInfo ti = tile_info<C::kKS>(p, tab, t);
+                // the epilogue must have read the previous tile out of the accumulator
+                if (it > 0 && !wait_or_abort(acce, (it - 1) & 1, abort)) { ok = false; break; }
                 ptx::tc_fence_after();
-                const uint32_t acc = tmem + b * BN;
                 for (int kb = 0; kb < ti.num_kb; ++kb, ++g) {
                     const uint32_t s = g % S, round = g / S;
-                    if (!wait_or_abort(GRID == kE2M1 ? full(s) : expd(s), round & 1, abort)) { ok = false; break; }
+                    const uint32_t e = g % ES, eround = g / ES;
+                    // operands landed (E1M2: E planes written) and scales in TMEM
+                    if (!wait_or_abort(GRID == kE2M1 ? full(s) : expd(e), (GRID == kE2M1 ? round : eround) & 1,
+                                       abort) ||
+                        (GRID == kE2M1 && !wait_or_abort(sfr(s), round & 1, abort))) { ok = false; break; }
                     ptx::tc_fence_after();
-                    const int atoms = min(4, ti.nkt - 4 * kb);
+                    const int atoms = min(C::kKS, ti.nkt - C::kKS * kb);
+                    if (GRID == kE1M2) copy_scales(s, atoms, false);
                     const uint32_t st = smem_base + s * C::kStageBytes;
-                    const uint32_t sf_t = tmem + kSfCol + 32u * s;
-                    const uint64_t dsa = mk(hi_sf, st + C::kSfaOff), dsb = mk(hi_sf, st + C::kSfbOff);
-                    const uint64_t dah = mk(hi_op, st + C::kAOff), dbh = mk(hi_op, st + C::kBOff);
-                    const uint64_t dal = mk(hi_op, st + C::kALoOff), dbl = mk(hi_op, st + C::kBLoOff);
+                    const uint32_t es = smem_base + C::kEOff + e * C::kESlotBytes;
+                    const uint32_t sf_t = tmem + kSfCol + C::kSfColsPerStage * s;
+                    const uint64_t da = mk(hi_op, st + C::kAOff), db = mk(hi_op, st + C::kBOff);
+                    const uint64_t dea = mk(hi_op, es), deb = mk(hi_op, es + C::kABytes);
+                    const uint32_t sfa0 = sf_t, sfb0 = sf_t + 4u * C::kKS;
                     auto step = [&](int j) {
-                        const uint32_t sfa = sf_t + 4u * j, sfb = sf_t + 16u + 4u * j;
+                        const uint32_t sfa = sfa0 + 4u * j, sfb = sfb0 + 8u * j;
                         const uint32_t first = (kb == 0 && j == 0) ? 0u : 1u;
                         const uint64_t o = 2u * (uint32_t)j;   // +32 bytes per 64-element K step
-                        ptx::tc_mma_nvf4(acc, dah + o, dbh + o, idesc, sfa, sfb, first);
+                        ptx::tc_mma_nvf4(tmem, da + o, db + o, idesc, sfa, sfb, first);
                         if (GRID == kE1M2) {
-                            ptx::tc_mma_nvf4(acc, dah + o, dbl + o, idesc, sfa, sfb, 1u);
-                            ptx::tc_mma_nvf4(acc, dal + o, dbh + o, idesc, sfa, sfb, 1u);
-                            ptx::tc_mma_nvf4(acc, dal + o, dbl + o, idesc, sfa, sfb, 1u);
+                            ptx::tc_mma_nvf4(tmem, da + o, deb + o, idesc, sfa, sfb, 1u);
+                            ptx::tc_mma_nvf4(tmem, dea + o, db + o, idesc, sfa, sfb, 1u);
+                            ptx::tc_mma_nvf4(tmem, dea + o, deb + o, idesc, sfa, sfb, 1u);
                         }
                     };
-                    if (atoms == 4) {
+                    if (atoms == C::kKS) {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            ptx::tc_cp_32x128b_warpx4(sf_t + 4u * j, dsa + 32u * j);
-                            ptx::tc_cp_32x128b_warpx4(sf_t + 16u + 4u * j, dsb + 32u * j);
-                        }
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) step(j);
+                        for (int j = 0; j < C::kKS; ++j) step(j);
                     } else {
-                        for (int j = 0; j < atoms; ++j) {
-                            ptx::tc_cp_32x128b_warpx4(sf_t + 4u * j, dsa + 32u * j);
-                            ptx::tc_cp_32x128b_warpx4(sf_t + 16u + 4u * j, dsb + 32u * j);
-                        }
                         for (int j = 0; j < atoms; ++j) step(j);
                     }
                     ptx::tc_commit(empty(s));
+                    if (GRID == kE1M2) ptx::tc_commit(efree(e));
                 }
-                if (ok) ptx::tc_commit(accf(b));   // fires once this tile's MMAs have completed
+                if (ok) ptx::tc_commit(accf);   // fires once this tile's MMAs have completed
             }
             // TMEM is freed below only after every MMA issued here has finished.
             ptx::tc_commit(drained);
@@ -326,115 +387,155 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
             while (!ptx::mbar_try_wait(drained, 0))
                 if (clock64() - t0 > kWaitBudget) { raise_timeout(); break; }
         }
-    } else if (warp < 6) {
+    } else if (warp < 2 + kEpiWarps) {
         // ------------------------------------------------------------ epilogue
-        // TMEM -> registers (x alpha) -> swizzled shared staging -> TMA store.
-        // Each warp owns 32 accumulator rows; a 32 x 32 fp32 box per store, so
-        // global writes are whole lines and ragged tile edges are clipped by
-        // the tensor map.
-        const int q = warp & 3;                 // TMEM lane quadrant of this warp
-        const uint32_t ebase = smem_base + C::kEpiOff + (uint32_t)(warp - 2) * C::kEpiBufs * 4096u;
-        uint32_t it = 0, nst = 0;
+        // Each warp owns 32 accumulator rows x 128 columns (four 32 x 32
+        // chunks).  The first kEpiBufs chunks go TMEM -> registers (x alpha) ->
+        // swizzled shared staging, the rest into registers; then the
+        // accumulator is handed back to the MMA warp and the chunks leave as
+        // TMA stores of 32 x 32 fp32 boxes (whole lines; ragged edges clipped
+        // by the tensor map).  Grouped problems copy each staged chunk out
+        // with masked, row-coalesced stores instead.
+        constexpr int NB = C::kEpiBufs;
+        const int q = warp & 3;                  // TMEM lane quadrant of this warp
+        const int ew = warp - 2;
+        const int h = ew >> 2;                   // column half of the tile
+        const uint32_t buf0 = smem_base + C::kEpiOff + (uint32_t)ew * NB * 4096u;
+        // E1M2 accumulates (R + E)(R + E) = 4 A B^T
+        const float kfix = GRID == kE1M2 ? 0.25f : 1.0f;
+        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
+        uint32_t it = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
-            const uint32_t b = it & 1, use = it >> 1;
-            bool ok = wait_or_abort(accf(b), use & 1, abort);
+            bool ok = wait_or_abort(accf, it & 1, abort);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             ptx::tc_fence_after();
-            const TileInfo ti = tile_info(p, tab, t);
+            const TileInfo ti = tile_info<C::kKS>(p, tab, t);
             const float alpha = __fmul_rn(*ti.ts_a, *ti.ts_b);
-            const int m0 = ti.m_loc, n0 = ti.n_loc;
-#pragma unroll 1
-            for (int ch = 0; ch < BN / 32; ++ch, ++nst) {
-                uint32_t r[32];
-                ptx::tc_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + b * BN + 32u * ch, r);
-                if constexpr (kGrouped) {
-                    // masked direct stores: a group's C is not a whole tensor map
-                    ptx::tc_wait_ld();
-                    if (ch == BN / 32 - 1) {
-                        ptx::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(acce(b));
-                    }
-                    const int row = m0 + 32 * q + lane, col0 = n0 + 32 * ch;
-                    if (row < ti.M) {
-                        float *crow = ti.c + (int64_t)row * ti.ldc;
-                        if (col0 + 32 <= ti.N) {
-#pragma unroll
-                            for (int i = 0; i < 32; i += 4)
-                                *reinterpret_cast<float4 *>(crow + col0 + i) =
-                                    make_float4(__uint_as_float(r[i]) * alpha, __uint_as_float(r[i + 1]) * alpha,
-                                                __uint_as_float(r[i + 2]) * alpha, __uint_as_float(r[i + 3]) * alpha);
-                        } else {
-                            for (int i = 0; i < 32; ++i)
-                                if (col0 + i < ti.N) crow[col0 + i] = __uint_as_float(r[i]) * alpha;
-                        }
-                    }
-                    continue;
-                }
-                const uint32_t buf = ebase + (nst % C::kEpiBufs) * 4096u;
-                // the store that last read this buffer must be done reading it
-                if (lane == 0) {
-                    if (C::kEpiBufs == 2) ptx::bulk_wait_read<1>();
-                    else ptx::bulk_wait_read<0>();
-                }
-                __syncwarp();
-                ptx::tc_wait_ld();
-                if (ch == BN / 32 - 1) {   // accumulator fully read: hand it back to the MMA warp
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(acce(b));
-                }
-                const uint32_t rowb = buf + (uint32_t)lane * 128u;
+            const int m0 = ti.m_loc + 32 * q, n0 = ti.n_loc + 128 * h;
+            auto stage = [&](uint32_t b, const uint32_t (&v)[32]) {
+                const uint32_t rowb = b + (uint32_t)lane * 128u;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const uint32_t addr = rowb + (uint32_t)((c ^ (lane & 7)) << 4);
                     asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                                 "f"(__uint_as_float(r[4 * c]) * alpha), "f"(__uint_as_float(r[4 * c + 1]) * alpha),
-                                 "f"(__uint_as_float(r[4 * c + 2]) * alpha), "f"(__uint_as_float(r[4 * c + 3]) * alpha)
+                                 "f"(__uint_as_float(v[4 * c]) * kfix * alpha),
+                                 "f"(__uint_as_float(v[4 * c + 1]) * kfix * alpha),
+                                 "f"(__uint_as_float(v[4 * c + 2]) * kfix * alpha),
+                                 "f"(__uint_as_float(v[4 * c + 3]) * kfix * alpha)
                                  : "memory");
                 }
-                ptx::fence_proxy_async();
-                __syncwarp();
-                if (lane == 0 && m0 + 32 * q < p.M && n0 + 32 * ch < p.N) {   // boxes wholly outside C: skip
-                    ptx::tma_store_2d(&tma_c, n0 + 32 * ch, m0 + 32 * q, buf);
-                    ptx::bulk_commit();
+            };
+            auto flush = [&](uint32_t b, int ch) {
+                if constexpr (!kGrouped) {
+                    ptx::fence_proxy_async();
+                    __syncwarp();
+                    // one bulk group per chunk, empty for boxes wholly outside C, so
+                    // that the wait_group.read counts below see every chunk
+                    if (lane == 0) {
+                        if (m0 < p.M && n0 + 32 * ch < p.N) ptx::tma_store_2d(&tma_c, n0 + 32 * ch, m0, b);
+                        ptx::bulk_commit();
+                    }
+                } else {
+                    __syncwarp();
+                    const int col = n0 + 32 * ch + 4 * (lane & 7);
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const int rr = i + (lane >> 3), row = m0 + rr;
+                        float4 v;
+                        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                     : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                                     : "r"(b + (uint32_t)rr * 128u + (uint32_t)(((lane & 7) ^ (rr & 7)) << 4))
+                                     : "memory");
+                        if (row < ti.M && col < ti.N) {
+                            float *cp = ti.c + (int64_t)row * ti.ldc + col;
+                            if (col + 4 <= ti.N) {
+                                *reinterpret_cast<float4 *>(cp) = v;
+                            } else {
+                                cp[0] = v.x;
+                                if (col + 1 < ti.N) cp[1] = v.y;
+                                if (col + 2 < ti.N) cp[2] = v.z;
+                            }
+                        }
+                    }
+                    __syncwarp();
                 }
+            };
+            // the previous tile's stores must be done reading the staging buffers
+            if (!kGrouped && lane == 0) ptx::bulk_wait_read<0>();
+            __syncwarp();
+#pragma unroll
+            for (int ch = 0; ch < NB; ++ch) {
+                uint32_t v[32];
+                ptx::tc_ld_32x32b_x32(taddr + 32u * ch, v);
+                ptx::tc_wait_ld();
+                stage(buf0 + 4096u * ch, v);
+            }
+            uint32_t rest[4 - NB][32];
+#pragma unroll
+            for (int ch = NB; ch < 4; ++ch) ptx::tc_ld_32x32b_x32(taddr + 32u * ch, rest[ch - NB]);
+            ptx::tc_wait_ld();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(acce);   // accumulator fully read
+#pragma unroll
+            for (int ch = 0; ch < NB; ++ch) flush(buf0 + 4096u * ch, ch);
+#pragma unroll
+            for (int ch = NB; ch < 4; ++ch) {
+                const uint32_t b = buf0 + 4096u * (ch % NB);
+                if (!kGrouped && lane == 0) ptx::bulk_wait_read<NB - 1>();
+                __syncwarp();
+                stage(b, rest[ch - NB]);
+                flush(b, ch);
             }
         }
         if (lane == 0) ptx::bulk_wait_all();
         __syncwarp();
+    } else if (GRID == kE2M1 && warp == 2 + kEpiWarps) {
+        // ------------------------------------------------- E2M1 scale copies
+        if (lane == 0) {
+            uint32_t g = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const TileInfo ti = tile_info<C::kKS>(p, tab, t);
+                for (int kb = 0; kb < ti.num_kb; ++kb, ++g) {
+                    const uint32_t s = g % S, round = g / S;
+                    if (!wait_or_abort(full(s), round & 1, abort)) { ok = false; break; }
+                    copy_scales(s, min(C::kKS, ti.nkt - C::kKS * kb), true);
+                }
+            }
+            drain_scales(g);
+        }
     } else if constexpr (GRID == kE1M2) {
         // ------------------------------------------------- E1M2 expanders
-        const int et = threadIdx.x - 192;   // 0 .. kExpThreads-1
+        // E planes of the staged A | B tiles, 16 bytes per thread and step;
+        // the swizzle is a byte permutation within rows, so the elementwise
+        // plane keeps the tile's layout.
+        const int et = threadIdx.x - 32 * (2 + kEpiWarps);
+        constexpr int kExpThreads = 32 * C::kExpWarps;
         uint32_t g = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-            const int nkb = tile_info(p, tab, t).num_kb;
+            const int nkb = tile_info<C::kKS>(p, tab, t).num_kb;
             for (int kb = 0; kb < nkb; ++kb, ++g) {
                 const uint32_t s = g % S, round = g / S;
+                const uint32_t e = g % ES, eround = g / ES;
                 ok = wait_or_abort(full(s), round & 1, abort);
+                // the MMAs that last read this E slot have completed
+                if (ok && eround > 0) ok = wait_or_abort(efree(e), (eround - 1) & 1, abort);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                uint8_t *st = smem + s * C::kStageBytes;
+                const uint4 *src = reinterpret_cast<const uint4 *>(smem + s * C::kStageBytes + C::kAOff);
+                uint4 *dst = reinterpret_cast<uint4 *>(smem + C::kEOff + e * C::kESlotBytes);
 #pragma unroll 4
-                for (int i = et; i < (int)(TILE_BYTES / 16); i += C::kExpThreads) {
-                    uint4 *pa = reinterpret_cast<uint4 *>(st + C::kAOff) + i;
-                    uint4 *pb = reinterpret_cast<uint4 *>(st + C::kBOff) + i;
-                    uint4 a = *pa, bv = *pb, ah, alo, bh, blo;
-                    split_e1m2(a.x, ah.x, alo.x); split_e1m2(a.y, ah.y, alo.y);
-                    split_e1m2(a.z, ah.z, alo.z); split_e1m2(a.w, ah.w, alo.w);
-                    split_e1m2(bv.x, bh.x, blo.x); split_e1m2(bv.y, bh.y, blo.y);
-                    split_e1m2(bv.z, bh.z, blo.z); split_e1m2(bv.w, bh.w, blo.w);
-                    *pa = ah;
-                    *pb = bh;
-                    reinterpret_cast<uint4 *>(st + C::kALoOff)[i] = alo;
-                    reinterpret_cast<uint4 *>(st + C::kBLoOff)[i] = blo;
+                for (int i = et; i < (int)(C::kESlotBytes / 16); i += kExpThreads) {
+                    const uint4 w = src[i];
+                    dst[i] = make_uint4(e1m2_eplane(w.x), e1m2_eplane(w.y), e1m2_eplane(w.z), e1m2_eplane(w.w));
                 }
                 // generic-proxy writes -> visible to the tensor cores (async proxy)
                 ptx::fence_proxy_async();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(expd(s));
+                if (lane == 0) ptx::mbar_arrive(expd(e));
             }
         }
     }
@@ -462,15 +563,19 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
-bool make_code_map(CUtensorMap *m, const uint8_t *codes, int64_t rows, int64_t kpad) {
+// K-major packed codes, rows x kpad/2 bytes; box = one K stage x box_rows
+// rows, swizzled as the MMA operand descriptors expect.
+bool make_code_map(CUtensorMap *m, const uint8_t *codes, int64_t rows, int64_t kpad, int box_rows, int grid) {
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)(kpad / 2), (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(kpad / 2)};
-    cuuint32_t box[2] = {(cuuint32_t)BK_BYTES, 128};
+    const int bk = grid == kE2M1 ? Cfg<kE2M1>::kBK : Cfg<kE1M2>::kBK;
+    cuuint32_t box[2] = {(cuuint32_t)bk, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), dims, strides, box,
-                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     bk == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -516,17 +621,19 @@ cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const f
     if (K == 0) return cudaMemset2DAsync(c, ldc * sizeof(float), 0, N * sizeof(float), M, s);
     const int64_t kpad = kpad_of(K);
     CUtensorMap ma, mb, mc;
-    if (!make_code_map(&ma, a_codes, M, kpad) || !make_code_map(&mb, b_codes, N, kpad) ||
+    if (!make_code_map(&ma, a_codes, M, kpad, BM, grid) || !make_code_map(&mb, b_codes, N, kpad, BN, grid) ||
         !make_out_map(&mc, c, M, N, ldc))
         return cudaErrorInvalidValue;
     GemmParams p{};
     p.sfa = a_scales; p.sfb = b_scales; p.ts_a = a_ts; p.ts_b = b_ts;
     p.c = c; p.ldc = ldc; p.M = (int)M; p.N = (int)N;
     p.nkt = (int)(kpad / 64);
-    p.num_kb = (p.nkt + 3) / 4;
+    const int ks = grid == kE2M1 ? Cfg<kE2M1>::kKS : Cfg<kE1M2>::kKS;
+    p.num_kb = (p.nkt + ks - 1) / ks;
     p.ntm = (int)((M + BM - 1) / BM);
     p.ntn = (int)((N + BN - 1) / BN);
     p.nkt_a = p.nkt_b = p.nkt;
+    p.b_rt = (int)((N + 127) / 128);
     const NoGroups none;
     if (grid == kE2M1) return run_gemm<kE2M1>(ma, mb, mc, p, none, p.ntm * p.ntn, s);
     return run_gemm<kE1M2>(ma, mb, mc, p, none, p.ntm * p.ntn, s);
@@ -537,13 +644,15 @@ cudaError_t launch_gemm_grouped(const uint8_t *a_codes, const uint8_t *a_scales,
                                 const float *b_ts, int64_t b_rows, int64_t b_kpad, int grid,
                                 const GroupGemmTab &tab, cudaStream_t s) {
     CUtensorMap ma, mb, mc;
-    if (!make_code_map(&ma, a_codes, a_rows, a_kpad) || !make_code_map(&mb, b_codes, b_rows, b_kpad))
+    if (!make_code_map(&ma, a_codes, a_rows, a_kpad, BM, grid) ||
+        !make_code_map(&mb, b_codes, b_rows, b_kpad, BN, grid))
         return cudaErrorInvalidValue;
     memset(&mc, 0, sizeof mc);   // grouped epilogues store directly
     GemmParams p{};
     p.sfa = a_scales; p.sfb = b_scales; p.ts_a = a_ts; p.ts_b = b_ts;
     p.nkt_a = (int)(a_kpad / 64);
     p.nkt_b = (int)(b_kpad / 64);
+    p.b_rt = (int)((b_rows + 127) / 128);
     p.M = 1; p.N = 1;
     const int ntiles = tab.tiles[tab.n];
     if (grid == kE2M1) return run_gemm<kE2M1>(ma, mb, mc, p, tab, ntiles, s);

@@ -42,9 +42,13 @@ struct GroupQuant {
     int64_t units[kMaxGroups + 1];    // prefix sums of work units (16-blocks / column-pair units)
 };
 
+// GEMM output tile (rows of A x rows of B per CTA tile).
+constexpr int kGemmBM = 128;
+constexpr int kGemmBN = 256;
+
 // One group of a grouped GEMM (host-built).
 struct GroupGemm {
-    int32_t M, N, nkt, ntn;           // nkt = kpad(K) / 64, ntn = ceil(N / 128)
+    int32_t M, N, nkt, ntn;           // nkt = kpad(K) / 64, ntn = ceil(N / kGemmBN)
     int32_t a_rt, a_kt, b_rt, b_kt;   // row offsets / 128, k offsets / 64
     int32_t a_seg, b_seg;
     float *c;
@@ -52,7 +56,7 @@ struct GroupGemm {
 };
 struct GroupGemmTab {
     int32_t n;
-    int32_t tiles[kMaxGroups + 1];    // prefix sums of 128 x 128 tiles per group
+    int32_t tiles[kMaxGroups + 1];    // prefix sums of kGemmBM x kGemmBN tiles per group
     GroupGemm g[kMaxGroups];
 };
 
