@@ -162,7 +162,7 @@ class Step:
     """Buffers and launches of one UFP4 training step (E1M2 + RHT on all
     GEMM operands, SR on dY), all through the libufp4 binding."""
 
-    def __init__(self, U, x, w, dy, grid):
+    def __init__(self, U, x, w, dy, grid, dual=True):
         import torch
         self.U, self.torch = U, torch
         self.x, self.w, self.dy = x, w, dy
@@ -178,12 +178,22 @@ class Step:
         self.dw = torch.empty(F, H, dtype=torch.float32, device=dev)
         self.ws = U.workspace(dev)
         self.counter = 0
+        self.dual = dual
+        self.launches_per_step = (3 if dual else 6) * 2 + 3
         self.q_elems = 2 * (x.numel() + w.numel() + dy.numel())
         self.flops_each = [2 * T * F * H, 2 * T * H * F, 2 * F * H * T]
 
     def quantize_all(self):
         U, g = self.U, self.grid
         kw = dict(rht=True, rht_seed=2, ws=self.ws)
+        if self.dual:
+            # each operand in both orientations from one read per pass
+            U.ufp4_quantize_dual(self.x, g, out_row=self.qx_r, out_col=self.qx_c, **kw)
+            U.ufp4_quantize_dual(self.w, g, out_row=self.qw_r, out_col=self.qw_c, **kw)
+            U.ufp4_quantize_dual(self.dy, g, round=U.UFP4_SR, sr_seed=3, sr_counter_row=self.counter,
+                                 sr_counter_col=self.counter, out_row=self.qdy_r, out_col=self.qdy_c, **kw)
+            self.counter += 1
+            return
         sr = dict(round=U.UFP4_SR, sr_seed=3, sr_counter=self.counter)
         U.ufp4_quantize(self.x, g, out=self.qx_r, **kw)
         U.ufp4_quantize(self.w, g, out=self.qw_r, **kw)
@@ -202,7 +212,6 @@ class Step:
             if events is not None:
                 events[i + 1].record()
 
-    launches_per_step = 6 * 2 + 3
 
 
 def run_gpu(args):
@@ -277,6 +286,22 @@ def run_gpu(args):
     extra = {}
     if not args.quick:
         extra = side_measurements(U, torch, dev, pk, flush)
+        # the same quantize phase with one pass per orientation (six
+        # single-orientation calls instead of three dual ones)
+        single = Step(U, d["x"], d["w"], d["dy"], U.UFP4_E1M2, dual=False)
+        for _ in range(3):
+            single.quantize_all()
+        tot = 0.0
+        for _ in range(20):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(); single.quantize_all(); b.record()
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b)
+        extra["quantize_step_single_orientation"] = {
+            "gbs": round(q_bytes / (tot / 20 * 1e-3) / 1e9, 1), "ms": round(tot / 20, 4),
+            "launches": single.launches_per_step - 3}
+        del single
 
     if rank == 0:
         clocks = clk.summary()
@@ -294,7 +319,8 @@ def run_gpu(args):
                        "parallelism": "replicas" if ws_n > 1 else "single"},
             "quantize": {"gbs": round(q_gbs, 1), "frac_hbm": round(q_gbs / ws_n / pk["hbm_gbs"], 4),
                          "ms_per_step": round(tq / args.steps, 4),
-                         "elements_per_step": step.q_elems, "launches_per_step": 12},
+                         "elements_per_step": step.q_elems,
+                         "launches_per_step": step.launches_per_step - 3},
             "gemm": {"tflops": round(gemm_tflops, 1), "ms_per_step": round(tg / args.steps, 4),
                      "ms_each": [round(v, 4) for v in gemm_each],
                      "frac_fp8_peak": round(per_gpu_tflops / fp8_peak, 4),
@@ -304,7 +330,7 @@ def run_gpu(args):
                          "unit": "TFLOP/s", "frac": round(per_gpu_tflops / fp8_peak, 4),
                          "traffic": traffic_for("k_gemm_e1m2_dense1p5b"),
                          "peak_kind": "dense FP8 = %s bf16 x 2 (%s)" % ("measured" if pk["source"] == "measured" else "fallback", pk["source"])},
-            "gpu_launches": Step.launches_per_step * args.steps,
+            "gpu_launches": step.launches_per_step * args.steps,
             "clocks": clocks,
             "peaks": pk,
         }
@@ -485,8 +511,10 @@ def run_reference(args):
 
 def run_kernel(args):
     """One kernel of the step in isolation, for profiling: `steps` launches
-    of the fwd_y GEMM (8192 x 5632 x 2048) or of the RHT quantization of X
-    (8192 x 2048), after `warmup` launches.  Prints the mean event time."""
+    of the fwd_y GEMM (8192 x 5632 x 2048), of the RHT quantization of X
+    (8192 x 2048) in one orientation or both (quant_dual_*; the SR variant
+    quantizes dY, 8192 x 5632), after `warmup` launches, the tensor amax
+    given.  Prints the mean event time."""
     import torch
     from fp4_quantized_numerics_gb300 import build, inputs, ufp4 as U
     build.build()
@@ -502,6 +530,19 @@ def run_kernel(args):
         fn = lambda: U.ufp4_gemm(a, b, out=c)
         work = 2.0 * T * F * H
         unit = "TFLOP/s"
+    elif kind.startswith("quant_dual"):
+        # both orientations from one read; SR variant on the dY shape
+        grid = U.UFP4_E1M2
+        sr = kind.startswith("quant_dual_sr")
+        src = inputs.device_normal((T, F), 1e-3, 23, dev) if sr else x
+        am = torch.tensor([float(src.float().abs().max()) * 1.5], device=dev)
+        qr = U.QTensor.empty(src.shape[0], src.shape[1], grid, dev)
+        qc = U.QTensor.empty(src.shape[1], src.shape[0], grid, dev)
+        kw = dict(round=U.UFP4_SR, sr_seed=3) if sr else {}
+        fn = lambda: U.ufp4_quantize_dual(src, grid, rht=True, amax_row=am, amax_col=am, out_row=qr,
+                                          out_col=qc, **kw)
+        work = 2 * src.numel() * Q_BYTES_PER_ELEM
+        unit = "GB/s"
     else:
         grid = U.UFP4_E2M1 if kind.endswith("e2m1") else U.UFP4_E1M2
         col = kind.startswith("quant_col")
@@ -719,7 +760,8 @@ def main():
     ap.add_argument("--workloads", action="store_true",
                     help="measure every synthetic workload (one JSON line each) instead of the step")
     ap.add_argument("--kernel", default=None,
-                    choices=["gemm_e2m1", "gemm_e1m2", "quant_row_e1m2", "quant_col_e1m2",
+                    choices=["gemm_e2m1", "gemm_e1m2", "quant_row_e1m2", "quant_col_e1m2", "quant_dual_e1m2",
+                             "quant_dual_sr_e1m2",
                              "quant_row_e2m1", "quant_col_e2m1"],
                     help="time one kernel of the step in isolation (profiling)")
     args = ap.parse_args()

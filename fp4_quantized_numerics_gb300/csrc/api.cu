@@ -113,6 +113,23 @@ ufp4_status ufp4_quantize(const void *x, int32_t dtype, int64_t rows, int64_t co
     return from_cuda(launch_quantize(q, workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+ufp4_status ufp4_quantize_dual(const void *x, int32_t dtype, int64_t rows, int64_t cols, int64_t ld,
+                               const ufp4_qparams *p_row, const ufp4_qparams *p_col, const ufp4_qtensor *out_row,
+                               const ufp4_qtensor *out_col, void *workspace, size_t workspace_bytes,
+                               ufp4_stream_t stream) {
+    if (!p_row || !p_col || p_row->colwise != 0 || p_col->colwise != 1) return UFP4_ERR_INVALID;
+    QuantLaunch qr, qc;
+    ufp4_status st = check_quant_args(x, dtype, rows, cols, ld, p_row, out_row, &qr);
+    if (st != UFP4_OK) return st;
+    st = check_quant_args(x, dtype, rows, cols, ld, p_col, out_col, &qc);
+    if (st != UFP4_OK) return st;
+    if ((!p_row->amax_in || !p_col->amax_in) && !valid_workspace(workspace, workspace_bytes))
+        return UFP4_ERR_INVALID;
+    if (workspace && !aligned(workspace, 16)) return UFP4_ERR_INVALID;
+    if (rows == 0 || cols == 0) return UFP4_OK;
+    return from_cuda(launch_quantize_dual(qr, qc, workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 ufp4_status ufp4_check(const void *workspace, ufp4_stream_t stream) {
     if (workspace && !aligned(workspace, 16)) return UFP4_ERR_INVALID;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -107,25 +107,27 @@ __device__ __forceinline__ uint32_t e1m2_rn(float q) {
 // p = (a - lo) / (hi - lo) against u = (r >> 8) * 2^-24.  Returns the code.
 template <int GRID>
 __device__ __forceinline__ uint32_t sr_code(float q, uint32_t r) {
+    // The decision "up iff (r >> 8) 2^-24 < p", p the position of |q| between
+    // its grid neighbours, is taken in fixed point: with t = |q| scaled so
+    // that the neighbours are consecutive integers, T = ceil(t 2^24) holds
+    // the lower neighbour's index in its top bits and ceil(p 2^24) in its low
+    // 24 bits, and (r >> 8) < ceil(p 2^24) iff r < (T << 8) mod 2^32.  Exact:
+    // t 2^24 is an fp32 value below 2^27 and the conversion rounds up; one
+    // conversion per element instead of three.
     const uint32_t sgn = (__float_as_uint(q) >> 28) & 8u;
-    const float u = __fmul_rn(__uint2float_rn(r >> 8), 5.9604644775390625e-8f);
     if (GRID == kE1M2) {
-        const float a2 = fminf(fabsf(q) * 2.0f, 7.0f);   // 2a, exact
-        const float fl = floorf(a2);
-        const float p = __fsub_rn(a2, fl);               // exact
-        uint32_t m = (uint32_t)fl + (u < p ? 1u : 0u);
-        return sgn | m;
+        const float t = fminf(fabsf(q) * 33554432.0f, 117440512.0f);   // 2|q| 2^24, at most 7 2^24
+        const uint32_t T = __float2uint_ru(t);
+        return sgn | ((T >> 24) + (r < (T << 8) ? 1u : 0u));
     } else {
-        const float a = fminf(fabsf(q), 6.0f);
-        if (a >= 6.0f) return sgn | 7u;
-        const float step = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
-        const float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
-        const float lo = __fmul_rn(floorf(__fmul_rn(a, inv)), step);  // exact
-        const float p = __fmul_rn(__fsub_rn(a, lo), inv);             // exact
-        // index of lo: 0,.5,1,1.5 -> 0..3 ; 2 -> 4 ; 3 -> 5 ; 4 -> 6
-        uint32_t m = lo < 2.0f ? (uint32_t)(lo * 2.0f) : (lo < 4.0f ? (uint32_t)lo + 2u : 6u);
-        m += (u < p ? 1u : 0u);
-        return sgn | m;
+        const float a = fabsf(q);
+        if (!(a < 6.0f)) return sgn | 7u;   // also NaN (non-finite input)
+        // neighbours 0.5 apart below 2, 1 apart below 4, 2 apart above
+        const float mul = a < 2.0f ? 33554432.0f : (a < 4.0f ? 16777216.0f : 8388608.0f);
+        const uint32_t T = __float2uint_ru(a * mul);
+        const uint32_t ip = T >> 24;
+        const uint32_t base = a < 2.0f ? ip : (a < 4.0f ? ip + 2u : 6u);   // E2M1 index of the lower neighbour
+        return sgn | (base + (r < (T << 8) ? 1u : 0u));
     }
 }
 

@@ -71,6 +71,11 @@ cudaError_t launch_dequantize(const uint8_t *codes, const uint8_t *scales, const
 // Writes n_ctas x 8 double partial sums to ws + kWsStats; returns n_ctas.
 cudaError_t launch_stats(const QuantLaunch &q, void *ws, int *n_ctas, cudaStream_t s);
 
+// Row-wise (qr) and column-wise (qc) quantization of the same x in one pass
+// over x (falls back to two passes when the parameters or the layout do not
+// allow it).
+cudaError_t launch_quantize_dual(const QuantLaunch &qr, const QuantLaunch &qc, void *ws, cudaStream_t s);
+
 // Grouped quantization: x holds segments in row order; ws keeps one fp32
 // maximum per segment and the status word.
 cudaError_t launch_quantize_grouped(const QuantLaunch &q, const GroupQuant &gt, void *ws, cudaStream_t s);

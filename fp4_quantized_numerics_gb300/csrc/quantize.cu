@@ -129,7 +129,8 @@ __device__ __forceinline__ void advance(Pos &p, int64_t dr, int64_t dc, int64_t 
 // multiplier table k[e] = min(S_enc / E4M3(e), FLT_MAX) * kfold.
 __device__ __forceinline__ void tensor_scale_prologue(const Args &a, float qmax, float kfold,
                                                       float *s_k, float *s_red, float &S_enc,
-                                                      bool e1m2_fold = false, bool *folded = nullptr) {
+                                                      bool e1m2_fold = false, bool *folded = nullptr,
+                                                      float *amax_out = nullptr) {
     float m = 0.0f;
     if (a.amax_in) {
         m = *a.amax_in;
@@ -143,6 +144,7 @@ __device__ __forceinline__ void tensor_scale_prologue(const Args &a, float qmax,
         for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = max_nan(m, s_red[w]);
     }
     const float A_t = m;
+    if (amax_out) *amax_out = A_t;
     float se = 1.0f, sd = 1.0f;
     if (A_t > 0.0f) {
         const float num = 448.0f * qmax;
@@ -1139,6 +1141,166 @@ __global__ void __launch_bounds__(kThreads) k_col_staged(Args a, uint32_t ncc, u
     }
 }
 
+// ================================================ dual orientation (X and X^T)
+// A training step quantizes every operand both ways (X row-wise for one GEMM,
+// X^T for another).  One read serves both: the column-wise ring of 16 rows x
+// CW columns is staged as above, and each chunk is quantized as CW/2 column
+// pairs (one unit per thread, output X^T) and as 16 x CW/16 row-wise blocks
+// (two per thread for BF16, packed pairs; output X).  The two results keep
+// their own tensor scale, SR counter and element numbering.  With AMAX the
+// kernel only writes one partial maximum per CTA for each orientation (the
+// row-wise and the column-wise transforms see different blocks).
+template <class In, int GRID, int ROUND, bool RHT, bool AMAX>
+__global__ void __launch_bounds__(kThreads) k_dual_staged(Args ar, Args ac, uint32_t ncc, uint32_t nchunks) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ float s_kr[256], s_kc[256];
+    __shared__ float s_red[kThreads / 32];
+    constexpr uint32_t CW = kChunk / (16 * sizeof(In));
+    constexpr uint32_t BPR = CW / 16;   // row-wise blocks per chunk row
+    const RingCtl ring = ring_init(dsm);
+    uint32_t issued = 0, j = 0;
+    if (threadIdx.x == 0)
+        for (uint32_t t = 0; t < kRing; ++t) col_issue<In>(ring, ar, t, nchunks, ncc, issued);
+    const float qmax = GRID == kE2M1 ? 6.0f : 3.5f;
+    float Sr = 1.0f, Sc = 1.0f;
+    bool fr = false, fc = false;
+    if (!AMAX) {
+        float amr = 0.0f, amc = 0.0f;
+        tensor_scale_prologue(ar, qmax, RHT ? 0.25f : 1.0f, s_kr, s_red, Sr, GRID == kE1M2 && ROUND == kRTNE, &fr,
+                              &amr);
+        tensor_scale_prologue(ac, qmax, RHT ? 0.25f : 1.0f, s_kc, s_red, Sc, GRID == kE1M2 && ROUND == kRTNE, &fc,
+                              &amc);
+        if (blockIdx.x == 0 && threadIdx.x == 0 && ar.status && !isfinite(amc)) *ar.status = 1u;
+    }
+    const uint32_t smask = RHT ? rht_sign_mask(ar.rht_seed) : 0u;
+    const Signs sgr = row_signs<In>(smask), sgc = col_signs<In>(smask);
+    const uint32_t nloc = nchunks > blockIdx.x ? (nchunks - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const uint32_t csr = (uint32_t)(ar.kpad / 2), nktr = (uint32_t)ar.nkt;
+    const uint32_t csc = (uint32_t)(ac.kpad / 2), nktc = (uint32_t)ac.nkt;
+    const uint32_t cols = (uint32_t)ar.cols;
+    float mr = 0.0f, mc = 0.0f;
+    bool ok = true;
+    for (; j < nloc; ++j) {
+        if (!ring_wait(ring, j)) { ok = false; break; }
+        const uint32_t i = blockIdx.x + j * gridDim.x;
+        const uint32_t kb = i / ncc, cc = i - kb * ncc;
+        const uint32_t c0 = cc * CW;
+        const uint32_t st = ring.buf + (j % kRing) * kChunk;
+        // column-wise unit: columns (c, c + 1), rows kb*16 .. +15
+        const uint32_t c = c0 + 2 * threadIdx.x;
+        if (2 * threadIdx.x < CW && c < cols) {
+            ColRaw<In> raw;
+            raw.load_shared(st + 2 * threadIdx.x * sizeof(In), CW * sizeof(In));
+            if (AMAX) {
+                uint64_t P[16];
+                col_values<In, RHT>(raw, sgc, P);
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    float v0, v1;
+                    upk2(P[q], v0, v1);
+                    mc = max_nan(mc, max_nan(fabsf(v0), fabsf(v1)));
+                }
+            } else {
+                quant_unit_col<In, GRID, ROUND, RHT>(ac, raw, kb, c, true, sgc, Sc, s_kc, csc, nktc, fc);
+            }
+        }
+        // row-wise blocks of the chunk: (row q, block bc) for k = q * BPR + bc
+        if (sizeof(In) == 2) {
+            // BF16: 512 blocks, thread t owns k = t and t + 256 (rows q and
+            // q + 8, the same block column) as a packed pair
+            const uint32_t q0 = threadIdx.x / BPR, bc = threadIdx.x % BPR;
+            if (c0 + bc * 16 < cols) {
+                Raw<__nv_bfloat16> r0, r1;
+                r0.load_shared(st + q0 * (CW * 2) + bc * 32);
+                r1.load_shared(st + (q0 + 8) * (CW * 2) + bc * 32);
+                if (AMAX) {
+                    uint64_t P[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) P[q] = RHT ? pk2(r0.get(q, sgr), r1.get(q, sgr)) : pk2(r0.get(q), r1.get(q));
+                    if (RHT) {
+#pragma unroll
+                        for (int sgs = 1; sgs < 16; sgs <<= 1) {
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) {
+                                if ((q & sgs) == 0) {
+                                    const uint64_t xx = P[q], yy = P[q + sgs];
+                                    P[q] = add2(xx, yy);
+                                    P[q + sgs] = sub2(xx, yy);
+                                }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        float u0, u1;
+                        upk2(P[q], u0, u1);
+                        mr = max_nan(mr, max_nan(fabsf(u0), fabsf(u1)));
+                    }
+                } else {
+                    const uint32_t b = cc * BPR + bc, r = kb * 16 + q0;
+                    quant_pair_row<GRID, ROUND, RHT>(ar, r0, r1, r, b, r + 8, b, true, sgr, Sr, s_kr, csr, nktr, fr);
+                }
+            }
+        } else {
+            for (uint32_t k = threadIdx.x; k < 16 * BPR; k += kThreads) {
+                const uint32_t q0 = k / BPR, bc = k % BPR;
+                if (c0 + bc * 16 >= cols) continue;
+                Raw<In> raw;
+                raw.load_shared(st + q0 * (CW * sizeof(In)) + bc * 16 * sizeof(In));
+                if (AMAX) {
+                    float lo[8], hi[8];
+                    block_values<In, RHT>(raw, sgr, lo, hi);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) mr = max_nan(mr, max_nan(fabsf(lo[q]), fabsf(hi[q])));
+                } else {
+                    quant_block_row<In, GRID, ROUND, RHT>(ar, raw, kb * 16 + q0, cc * BPR + bc, sgr, Sr, s_kr, csr,
+                                                          nktr, fr);
+                }
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) col_issue<In>(ring, ar, j + kRing, nchunks, ncc, issued);
+    }
+    if (!ok) {
+        if (threadIdx.x == 0) atomicOr(&g_quant_timeout, 1u);
+        ring_drain(ring, j, issued);
+    }
+    if (AMAX) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            mr = max_nan(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+            mc = max_nan(mc, __shfl_xor_sync(0xffffffffu, mc, o));
+        }
+        __shared__ float s_red2[kThreads / 32];
+        if ((threadIdx.x & 31) == 0) { s_red[threadIdx.x >> 5] = mr; s_red2[threadIdx.x >> 5] = mc; }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int w = 1; w < kThreads / 32; ++w) { mr = max_nan(mr, s_red[w]); mc = max_nan(mc, s_red2[w]); }
+            ar.partials_out[blockIdx.x] = RHT ? mr * 0.25f : mr;
+            ac.partials_out[blockIdx.x] = RHT ? mc * 0.25f : mc;
+        }
+    } else {
+        // row-wise result: padding blocks cols/16 .. kpad/16 - 1 of every row
+        const uint32_t kvr = cols / 16, nbr = (uint32_t)(ar.kpad / 16) - kvr;
+        const uint32_t npr = (uint32_t)ar.out_rows * nbr;
+        for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < npr; t += gridDim.x * blockDim.x) {
+            const uint32_t r = t / nbr, b = kvr + (t - r * nbr);
+            *reinterpret_cast<uint2 *>(ar.codes + (size_t)r * csr + b * 8) = make_uint2(0u, 0u);
+            ar.scales[scale_offset32(r, b, nktr)] = 0;
+        }
+        zero_pad_rows(ar);
+        // column-wise result: padding blocks past the last input row
+        const uint32_t kvc = (uint32_t)(ac.rows / 16), nbc = (uint32_t)(ac.kpad / 16) - kvc;
+        const uint32_t npc = (uint32_t)ac.out_rows * nbc;
+        for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < npc; t += gridDim.x * blockDim.x) {
+            const uint32_t r = t / nbc, b = kvc + (t - r * nbc);
+            *reinterpret_cast<uint2 *>(ac.codes + (size_t)r * csc + b * 8) = make_uint2(0u, 0u);
+            ac.scales[scale_offset32(r, b, nktc)] = 0;
+        }
+        zero_pad_rows(ac);
+    }
+}
+
 // ====================================================== grouped (MoE) path
 // Segments are found by binary search over prefix tables copied into shared
 // memory: find_seg returns the largest e with pre[e] <= u (empty segments are
@@ -1611,6 +1773,38 @@ cudaError_t quantize_typed(const QuantLaunch &q, Args &a, void *ws, cudaStream_t
     return cudaErrorInvalidValue;
 }
 
+// Both orientations of one tensor from one read per pass (k_dual_staged).
+// The row-wise and column-wise partial maxima take the two halves of the
+// workspace's partial area.
+template <class In>
+cudaError_t quantize_dual_typed(const QuantLaunch &qr, const QuantLaunch &qc, Args &ar, Args &ac, void *ws,
+                                cudaStream_t s) {
+    constexpr uint32_t CW = kChunk / (16 * sizeof(In));
+    const uint32_t ncc = (uint32_t)((ar.cols + CW - 1) / CW), nch = (uint32_t)(ar.rows / 16) * ncc;
+    ac.status = nullptr;   // the row-wise prologue reports both
+    if (!qr.amax_in || !qc.amax_in) {
+        ar.partials_out = reinterpret_cast<float *>(static_cast<char *>(ws) + kWsPartials);
+        ac.partials_out = ar.partials_out + kMaxPartials / 2;
+        auto kern = qr.rht ? k_dual_staged<In, 0, 0, true, true> : k_dual_staged<In, 0, 0, false, true>;
+        if (resident_grid(kern, nch, kRingSmem) > kMaxPartials / 2) return cudaErrorInvalidValue;
+        int g = 1;
+        cudaError_t e = launch_staged(kern, nch, &g, s, ar, ac, ncc, nch);
+        if (e != cudaSuccess) return e;
+        ar.partials = ar.partials_out;
+        ac.partials = ac.partials_out;
+        ar.n_partials = ac.n_partials = g;
+    }
+#define UFP4_D(GRID, ROUND, RHT)                                                                         \
+    if (qr.grid == GRID && qr.round == ROUND && (qr.rht != 0) == RHT)                                    \
+        return launch_staged(k_dual_staged<In, GRID, ROUND, RHT, false>, nch, nullptr, s, ar, ac, ncc, nch);
+    UFP4_D(kE2M1, kRTNE, false) UFP4_D(kE2M1, kRTNE, true)
+    UFP4_D(kE2M1, kSR, false)   UFP4_D(kE2M1, kSR, true)
+    UFP4_D(kE1M2, kRTNE, false) UFP4_D(kE1M2, kRTNE, true)
+    UFP4_D(kE1M2, kSR, false)   UFP4_D(kE1M2, kSR, true)
+#undef UFP4_D
+    return cudaErrorInvalidValue;
+}
+
 Args make_args(const QuantLaunch &q, void *ws) {
     Args a{};
     a.x = q.x;
@@ -1655,6 +1849,21 @@ cudaError_t launch_quantize(const QuantLaunch &q, void *ws, cudaStream_t s) {
     Args a = make_args(q, ws);
     if (q.dtype == 0) return quantize_typed<__nv_bfloat16>(q, a, ws, s);
     return quantize_typed<float>(q, a, ws, s);
+}
+
+cudaError_t launch_quantize_dual(const QuantLaunch &qr, const QuantLaunch &qc, void *ws, cudaStream_t s) {
+    const int64_t esz = qr.dtype == 0 ? 2 : 4;
+    const bool same = qr.grid == qc.grid && qr.round == qc.round && qr.rht == qc.rht &&
+                      (!qr.rht || qr.rht_seed == qc.rht_seed);
+    // one read serves both when every 16-row chunk row is a whole number of
+    // 16-byte pieces; otherwise two ordinary quantizations
+    if (!same || (qr.cols * esz) % 16 != 0 || qr.rows % 16 != 0) {
+        cudaError_t e = launch_quantize(qr, ws, s);
+        return e != cudaSuccess ? e : launch_quantize(qc, ws, s);
+    }
+    Args ar = make_args(qr, ws), ac = make_args(qc, ws);
+    if (qr.dtype == 0) return quantize_dual_typed<__nv_bfloat16>(qr, qc, ar, ac, ws, s);
+    return quantize_dual_typed<float>(qr, qc, ar, ac, ws, s);
 }
 
 cudaError_t launch_quantize_grouped(const QuantLaunch &q, const GroupQuant &gt, void *ws, cudaStream_t s) {

@@ -29,7 +29,7 @@ UFP4_OK, UFP4_ERR_INVALID, UFP4_ERR_UNSUPPORTED, UFP4_ERR_NONFINITE, UFP4_ERR_CU
 EXPORTED = ["ufp4_kpad", "ufp4_codes_bytes", "ufp4_scales_bytes", "ufp4_workspace_bytes",
             "ufp4_quantize", "ufp4_check", "ufp4_dequantize", "ufp4_gemm", "ufp4_stats",
             "ufp4_status_string", "ufp4_quantize_noalloc", "ufp4_grouped_rows",
-            "ufp4_grouped_kpad", "ufp4_quantize_grouped", "ufp4_gemm_grouped"]
+            "ufp4_grouped_kpad", "ufp4_quantize_grouped", "ufp4_gemm_grouped", "ufp4_quantize_dual"]
 
 
 class QParamsC(ctypes.Structure):
@@ -86,6 +86,10 @@ def lib():
         L.ufp4_quantize.argtypes = [vp, ctypes.c_int32, i64, i64, i64, ctypes.POINTER(QParamsC),
                                     ctypes.POINTER(QTensorC), vp, ctypes.c_size_t, vp]
         L.ufp4_quantize.restype = ctypes.c_int
+        L.ufp4_quantize_dual.argtypes = [vp, ctypes.c_int32, i64, i64, i64, ctypes.POINTER(QParamsC),
+                                         ctypes.POINTER(QParamsC), ctypes.POINTER(QTensorC),
+                                         ctypes.POINTER(QTensorC), vp, ctypes.c_size_t, vp]
+        L.ufp4_quantize_dual.restype = ctypes.c_int
         L.ufp4_check.argtypes = [vp, vp]
         L.ufp4_check.restype = ctypes.c_int
         L.ufp4_dequantize.argtypes = [ctypes.POINTER(QTensorC), ctypes.c_int32, ctypes.c_uint64,
@@ -215,6 +219,31 @@ def ufp4_quantize(x, grid, rht=False, rht_seed=0, round=UFP4_RTNE, sr_seed=0, sr
                              ctypes.byref(qc), ws.data_ptr(), ws.numel(), _stream(stream))
     _check(st, "ufp4_quantize")
     return out
+
+
+def ufp4_quantize_dual(x, grid, rht=False, rht_seed=0, round=UFP4_RTNE, sr_seed=0, sr_counter_row=0,
+                       sr_counter_col=0, amax_row=None, amax_col=None, out_row=None, out_col=None, ws=None,
+                       stream=None):
+    """Row-wise and column-wise quantization of x (results x and x.T
+    quantized along their last dim) from one read of x per pass."""
+    _cuda(x, "x")
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit stride in its last dim")
+    rows, cols = x.shape
+    if out_row is None:
+        out_row = QTensor.empty(rows, cols, grid, x.device)
+    if out_col is None:
+        out_col = QTensor.empty(cols, rows, grid, x.device)
+    if ws is None:
+        ws = workspace(x.device)
+    pr = qparams(grid, rht, rht_seed, round, sr_seed, sr_counter_row, False, amax_row)
+    pc = qparams(grid, rht, rht_seed, round, sr_seed, sr_counter_col, True, amax_col)
+    qr, qc = out_row.c(), out_col.c()
+    st = lib().ufp4_quantize_dual(x.data_ptr(), _dtype_code(x), rows, cols, x.stride(0), ctypes.byref(pr),
+                                  ctypes.byref(pc), ctypes.byref(qr), ctypes.byref(qc), ws.data_ptr(),
+                                  ws.numel(), _stream(stream))
+    _check(st, "ufp4_quantize_dual")
+    return out_row, out_col
 
 
 def ufp4_check(ws=None, stream=None):

@@ -161,6 +161,29 @@ UFP4_API ufp4_status ufp4_quantize(const void *x, int32_t dtype, int64_t rows, i
                           const ufp4_qparams *p, const ufp4_qtensor *out,
                           void *workspace, size_t workspace_bytes, ufp4_stream_t stream);
 
+/* Both quantizations of one matrix that a training step needs -- row-wise
+ * (blocks along the rows, result rows x cols) and column-wise (the
+ * quantization of X^T, result cols x rows) -- from one read of x per pass
+ * (the tensor amax pass and the quantization pass each read x once instead
+ * of twice).  The three training GEMMs consume every operand in both
+ * orientations ([ZC] zhichai.net post, Key points "The fix -- UFP4": the
+ * transform and quantization are applied to the operands of fwd_y, bwd_dx
+ * and bwd_dw).
+ *   p_row, out_row: as for ufp4_quantize with p_row->colwise == 0;
+ *   p_col, out_col: as for ufp4_quantize with p_col->colwise == 1;
+ *   x, dtype, rows, cols, ld, workspace: as for ufp4_quantize, and every
+ *   constraint of both orientations applies.
+ * Each result is bit-identical to its own ufp4_quantize call (own tensor
+ * scale, amax_in, SR seed and counter).  One pass serves both when the two
+ * parameter sets share grid, rounding mode and transform (seed included)
+ * and cols * sizeof(elem) is a multiple of 16; otherwise the call runs the
+ * two quantizations one after the other.  The non-finite flag in the
+ * workspace covers both. */
+UFP4_API ufp4_status ufp4_quantize_dual(const void *x, int32_t dtype, int64_t rows, int64_t cols, int64_t ld,
+                                        const ufp4_qparams *p_row, const ufp4_qparams *p_col,
+                                        const ufp4_qtensor *out_row, const ufp4_qtensor *out_col,
+                                        void *workspace, size_t workspace_bytes, ufp4_stream_t stream);
+
 /* ufp4_quantize without a caller workspace, for callers that cannot
  * allocate device memory when they quantize (a frozen memory pool, a custom
  * allocator that owns all device memory, code that must not risk an
