@@ -20,7 +20,7 @@ import numpy as np
 
 from . import build as _build
 
-E2M1, E1M2 = 0, 1
+E2M1, E1M2, E2M1C = 0, 1, 2
 RTNE, SR = 0, 1
 
 _lib = None
@@ -44,6 +44,8 @@ def lib():
         L.ref_grid_value.restype = ctypes.c_double
         L.ref_grid_qmax.argtypes = [ctypes.c_int]
         L.ref_grid_qmax.restype = ctypes.c_double
+        L.ref_grid_levels.argtypes = [ctypes.c_int]
+        L.ref_grid_levels.restype = ctypes.c_int
         L.ref_round_rtne.argtypes = [ctypes.c_int, ctypes.c_float]
         L.ref_round_rtne.restype = ctypes.c_int
         L.ref_round_sr.argtypes = [ctypes.c_int, ctypes.c_float, ctypes.c_uint32]
@@ -113,6 +115,10 @@ def grid_value(grid, m):
 
 def grid_qmax(grid):
     return lib().ref_grid_qmax(grid)
+
+
+def grid_levels(grid):
+    return lib().ref_grid_levels(grid)
 
 
 def round_rtne(grid, a):

@@ -33,6 +33,7 @@
 
 #define REF_E2M1 0
 #define REF_E1M2 1
+#define REF_E2M1C 2
 #define REF_RTNE 0
 #define REF_SR   1
 
@@ -154,29 +155,34 @@ uint8_t ref_e4m3_encode(float v)
 }
 
 /* ------------------------------------------------------------------------
- * The two 4-bit grids.  [ZC] Key points, "The cause" (E2M1 values) and
+ * The 4-bit grids.  [ZC] Key points, "The cause" (E2M1 values) and
  * "The fix -- UFP4" (E1M2 values).  Both grids carry a sign bit and use all
- * 16 codes; the pages stress that a uniform grid emulated by clamping E2M1
- * does not work ([ZC] Key points, Validation results).
- * A code is (sign << 3) | m, m the magnitude index 0..7.
+ * 16 codes.  The third is the ablation the pages report as failing: a
+ * uniform grid emulated by clamping E2M1's range ([ZC] Key points,
+ * "Validation results") -- READING: E2M1 restricted to its largest uniform
+ * part {0, .5, 1, 1.5, 2} (codes 0..4 with sign), qmax = 2.
+ * A code is (sign << 3) | m, m the magnitude index.
  * ---------------------------------------------------------------------- */
 double ref_grid_value(int grid, int m)
 {
     static const double e2m1[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
-    if (grid == REF_E2M1) return e2m1[m & 7];
+    if (grid == REF_E2M1 || grid == REF_E2M1C) return e2m1[m & 7];
     return 0.5 * (double)(m & 7);
 }
 
-double ref_grid_qmax(int grid) { return grid == REF_E2M1 ? 6.0 : 3.5; }
+double ref_grid_qmax(int grid) { return grid == REF_E2M1 ? 6.0 : (grid == REF_E1M2 ? 3.5 : 2.0); }
 
-/* Round-to-nearest-even onto the grid: brute-force argmin over the eight
+/* Number of magnitudes of the grid (8, or 5 for clamped E2M1). */
+int ref_grid_levels(int grid) { return grid == REF_E2M1C ? 5 : 8; }
+
+/* Round-to-nearest-even onto the grid: brute-force argmin over the grid's
  * magnitudes, ties to the even index (IEEE RNE for E2M1's bit layout; even
- * integer 2a for E1M2).  a >= 0, already clamped to qmax. */
+ * integer 2a for E1M2 and clamped E2M1).  a >= 0, already clamped to qmax. */
 int ref_round_rtne(int grid, float a)
 {
     int best = 0;
     double best_err = INFINITY;
-    for (int m = 0; m < 8; ++m) {
+    for (int m = 0; m < ref_grid_levels(grid); ++m) {
         const double err = fabs((double)a - ref_grid_value(grid, m));
         if (err < best_err || (err == best_err && (m & 1) == 0)) { best = m; best_err = err; }
     }
@@ -190,9 +196,10 @@ int ref_round_rtne(int grid, float a)
  * both sides are exact in fp32, so the rounding is exactly unbiased. */
 int ref_round_sr(int grid, float a, uint32_t r)
 {
-    if ((double)a >= ref_grid_qmax(grid)) return 7;
+    const int top = ref_grid_levels(grid) - 1;
+    if ((double)a >= ref_grid_qmax(grid)) return top;
     int m = 0;
-    while (m < 7 && ref_grid_value(grid, m + 1) <= (double)a) ++m;
+    while (m < top && ref_grid_value(grid, m + 1) <= (double)a) ++m;
     const float lo = (float)ref_grid_value(grid, m);
     const float hi = (float)ref_grid_value(grid, m + 1);
     const float p = (a - lo) / (hi - lo);

@@ -191,13 +191,50 @@ def test_e1m2_rtne_vs_rint(oracle):
         assert m == int(min(np.rint(2.0 * float(a)), 7.0)), float(a)
 
 
+def test_e2m1c_rtne_vs_rint(oracle):
+    # clamped E2M1: nearest of {0, .5, 1, 1.5, 2}, ties to the even index
+    for a in _grid_probe(2.0, [0.25 * i for i in range(9)]):
+        m = oracle.round_rtne(oracle.E2M1C, a)
+        assert m == int(min(np.rint(2.0 * float(a)), 4.0)), float(a)
+
+
 def test_grids_have_all_codes(oracle):
     e2 = [oracle.grid_value(oracle.E2M1, m) for m in range(8)]
     e1 = [oracle.grid_value(oracle.E1M2, m) for m in range(8)]
+    ec = [oracle.grid_value(oracle.E2M1C, m) for m in range(oracle.grid_levels(oracle.E2M1C))]
     assert e2 == [0, 0.5, 1, 1.5, 2, 3, 4, 6]
     assert e1 == [0.5 * m for m in range(8)]
     assert np.allclose(np.diff(e1), 0.5)          # uniform
     assert len(set(np.diff(e2))) == 3             # non-uniform
+    # clamped E2M1 is the uniform part of E2M1: the same codes, qmax 2
+    assert ec == e2[:5] and np.allclose(np.diff(ec), 0.5)
+    assert oracle.grid_qmax(oracle.E2M1C) == 2.0
+    assert [oracle.grid_levels(g) for g in (0, 1, 2)] == [8, 8, 5]
+
+
+def test_e2m1c_codes_decode_as_e2m1(oracle):
+    # a clamped-E2M1 tensor is a valid E2M1 tensor: same dequantized values
+    x = inputs.normal(24, (16, 64))
+    q = oracle.quantize(x, oracle.E2M1C, rht=True, rht_seed=2)
+    assert (q["codes"] & 7).max() <= 4
+    a = oracle.dequantize(q["codes"], q["scales"], q["tensor_scale"], oracle.E2M1C)
+    b = oracle.dequantize(q["codes"], q["scales"], q["tensor_scale"], oracle.E2M1)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_e2m1c_interior_bins_unbiased_and_fewer_levels(oracle):
+    for q0 in [0.5, 1.0, 1.5]:
+        a = np.linspace(q0 - 0.25, q0 + 0.25, 4001)[1:-1].astype(np.float32)
+        err = np.mean([oracle.grid_value(oracle.E2M1C, oracle.round_rtne(oracle.E2M1C, v)) - v for v in a])
+        assert abs(err) < 1e-6, q0
+    # 9 signed levels instead of E1M2's 15: lower SQNR on Gaussian data
+    x = inputs.normal(25, (64, 256))
+    sq = {}
+    for g in (oracle.E1M2, oracle.E2M1C):
+        q = oracle.quantize(x, g)
+        deq = oracle.dequantize(q["codes"], q["scales"], q["tensor_scale"], g)
+        sq[g] = 10 * np.log10(np.sum(x.astype(np.float64) ** 2) / np.sum((x - deq) ** 2))
+    assert sq[oracle.E2M1C] < sq[oracle.E1M2] - 3.0
 
 
 # ------------------------------------------------------ worked example: bias
@@ -238,7 +275,7 @@ def test_attenuation_closed_form():
 
 
 # ---------------------------------------------------- stochastic rounding
-@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("grid", [0, 1, 2])
 def test_sr_is_unbiased_within_5_sigma(oracle, grid):
     qmax = oracle.grid_qmax(grid)
     g = np.random.default_rng(4)
@@ -246,7 +283,7 @@ def test_sr_is_unbiased_within_5_sigma(oracle, grid):
     for a in g.uniform(0, qmax, 24).astype(np.float32):
         m0 = oracle.round_sr(grid, a, 0xFFFFFFFF)  # never rounds up: the floor
         lo = oracle.grid_value(grid, m0)
-        hi = oracle.grid_value(grid, min(m0 + 1, 7))
+        hi = oracle.grid_value(grid, min(m0 + 1, oracle.grid_levels(grid) - 1))
         vals = [oracle.grid_value(grid, oracle.round_sr(grid, a, oracle.sr_word(3, 0, i)))
                 for i in range(N)]
         p = (float(a) - lo) / (hi - lo) if hi > lo else 0.0
@@ -256,8 +293,8 @@ def test_sr_is_unbiased_within_5_sigma(oracle, grid):
 
 
 def test_sr_exact_points_and_edges(oracle):
-    for grid in (0, 1):
-        for m in range(8):
+    for grid in (0, 1, 2):
+        for m in range(oracle.grid_levels(grid)):
             v = oracle.grid_value(grid, m)
             for r in (0, 0x7FFFFFFF, 0xFFFFFFFF):
                 assert oracle.round_sr(grid, v, r) == m
@@ -267,13 +304,13 @@ def test_sr_exact_points_and_edges(oracle):
 
 
 # -------------------------------------------------- quantization end to end
-@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("grid", [0, 1, 2])
 def test_quantize_scale_path_exact_case(oracle, grid):
     qmax = oracle.grid_qmax(grid)
     x = np.full((1, 16), qmax / 8, np.float32)  # A_t = qmax/8: every step exact
     q = oracle.quantize(x, grid)
     assert q["scales"][0, 0] == 0x7E                      # E4M3 448
-    assert np.all(q["codes"] == 7)
+    assert np.all(q["codes"] == oracle.grid_levels(grid) - 1)
     assert q["tensor_scale"] == np.float32(qmax / 8) / np.float32(448 * qmax)
 
 
@@ -289,7 +326,7 @@ def test_quantize_zero_and_single_spike(oracle):
         assert np.all((others & 7) == 0)
 
 
-@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("grid", [0, 1, 2])
 def test_quantize_sign_and_power_of_two_invariance(oracle, grid):
     x = inputs.normal(21, (16, 64))
     q = oracle.quantize(x, grid)
@@ -301,7 +338,7 @@ def test_quantize_sign_and_power_of_two_invariance(oracle, grid):
     assert q2["tensor_scale"] == q["tensor_scale"] * 8
 
 
-@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("grid", [0, 1, 2])
 def test_quantize_picks_nearest_representable(oracle, grid):
     """Brute force: with the block scale fixed, every code is (to within the
     rounding of k = S_enc/e_b) the nearest of the 16 representable values."""
@@ -314,7 +351,7 @@ def test_quantize_picks_nearest_representable(oracle, grid):
             e = oracle.e4m3_decode(q["scales"][r, b])
             unit = e * q["tensor_scale"]
             cand = np.array([s * oracle.grid_value(grid, m) * unit
-                             for s in (1, -1) for m in range(8)])
+                             for s in (1, -1) for m in range(oracle.grid_levels(grid))])
             for j in range(16):
                 y = float(x[r, 16 * b + j])
                 best = np.min(np.abs(cand - y))
