@@ -162,7 +162,7 @@ class Step:
     """Buffers and launches of one UFP4 training step (E1M2 + RHT on all
     GEMM operands, SR on dY), all through the libufp4 binding."""
 
-    def __init__(self, U, x, w, dy, grid, dual=True):
+    def __init__(self, U, x, w, dy, grid, dual=True, policy="ufp4"):
         import torch
         self.U, self.torch = U, torch
         self.x, self.w, self.dy = x, w, dy
@@ -178,8 +178,11 @@ class Step:
         self.dw = torch.empty(F, H, dtype=torch.float32, device=dev)
         self.ws = U.workspace(dev)
         self.counter = 0
-        self.dual = dual
-        self.launches_per_step = (3 if dual else 6) * 2 + 3
+        # "nvfp4": the transform only on the bwd_dw operands (dY^T, X^T); the
+        # two orientations then differ and are quantized one pass each
+        self.policy = policy
+        self.dual = dual and policy == "ufp4"
+        self.launches_per_step = (3 if self.dual else 6) * 2 + 3
         self.q_elems = 2 * (x.numel() + w.numel() + dy.numel())
         self.flops_each = [2 * T * F * H, 2 * T * H * F, 2 * F * H * T]
 
@@ -195,10 +198,11 @@ class Step:
             self.counter += 1
             return
         sr = dict(round=U.UFP4_SR, sr_seed=3, sr_counter=self.counter)
-        U.ufp4_quantize(self.x, g, out=self.qx_r, **kw)
-        U.ufp4_quantize(self.w, g, out=self.qw_r, **kw)
-        U.ufp4_quantize(self.dy, g, out=self.qdy_r, **kw, **sr)
-        U.ufp4_quantize(self.w, g, colwise=True, out=self.qw_c, **kw)
+        kn = dict(kw, rht=False) if self.policy == "nvfp4" else kw   # fwd_y / bwd_dx operands
+        U.ufp4_quantize(self.x, g, out=self.qx_r, **kn)
+        U.ufp4_quantize(self.w, g, out=self.qw_r, **kn)
+        U.ufp4_quantize(self.dy, g, out=self.qdy_r, **kn, **sr)
+        U.ufp4_quantize(self.w, g, colwise=True, out=self.qw_c, **kn)
         U.ufp4_quantize(self.dy, g, colwise=True, out=self.qdy_c, **kw, **sr)
         U.ufp4_quantize(self.x, g, colwise=True, out=self.qx_c, **kw)
         self.counter += 1
@@ -610,7 +614,7 @@ def run_workloads(args):
     a = torch.from_numpy(d["a"]).to(torch.bfloat16).to(dev)
     b = torch.from_numpy(d["b"]).to(torch.bfloat16).to(dev)
     r = {"workload": "smoke_256x1024", "numerics": {}}
-    for g, gn in ((0, "e2m1"), (1, "e1m2")):
+    for g, gn in ((0, "e2m1"), (1, "e1m2"), (2, "e2m1c")):
         for rht in (False, True):
             r["numerics"]["%s_rht_%s" % (gn, "on" if rht else "off")] = stats_of(x, g, rht)
         qa, qb = U.ufp4_quantize(a, g), U.ufp4_quantize(b, g)
@@ -623,7 +627,7 @@ def run_workloads(args):
     d = inputs.outlier(0)
     x = torch.from_numpy(d["x"]).to(torch.bfloat16).to(dev)
     r = {"workload": "outlier_4096x4096", "numerics": {}, "quantize_gbs": {}}
-    for g, gn in ((0, "e2m1"), (1, "e1m2")):
+    for g, gn in ((0, "e2m1"), (1, "e1m2"), (2, "e2m1c")):
         for rht in (False, True):
             key = "%s_rht_%s" % (gn, "on" if rht else "off")
             r["numerics"][key] = stats_of(x, g, rht)
@@ -636,10 +640,11 @@ def run_workloads(args):
         "after_rht_e2m1_minus_e1m2_db": round(n["e2m1_rht_on"]["sqnr_db"] - n["e1m2_rht_on"]["sqnr_db"], 3)}
     emit(r)
 
-    # dense 1.5B training step (both grids)
+    # dense 1.5B training step: UFP4 on both grids, and the NVFP4 policy
+    # (E2M1, the transform only on the bwd_dw operands) the pages compare with
     dd = inputs.device_dense(seed=0, device=dev)
-    for g, gn in ((1, "e1m2"), (0, "e2m1")):
-        st = Step(U, dd["x"], dd["w"], dd["dy"], g)
+    for g, gn, pol in ((1, "e1m2", "ufp4"), (0, "e2m1", "ufp4"), (0, "nvfp4_policy", "nvfp4")):
+        st = Step(U, dd["x"], dd["w"], dd["dy"], g, policy=pol)
         mq = _ev_time(st.quantize_all, flush)
         mg = _ev_time(st.gemms, flush)
         emit({"workload": "dense1p5b_step_" + gn, "quantize_ms": round(mq, 4),
@@ -713,7 +718,7 @@ def run_workloads(args):
     # compounding-attenuation chain: 100 x (4096^3), fresh W_k ~ N(0, 1/64)
     n, steps = 4096, 100
     rows = torch.arange(0, n, n // 64, device=dev)
-    for g, gn in ((0, "e2m1"), (1, "e1m2")):
+    for g, gn in ((0, "e2m1"), (1, "e1m2"), (2, "e2m1c")):
         for rht in (False, True):
             X = inputs.device_normal((n, n), 1.0, 50, dev, dtype=torch.float32)
             norm0 = float(X.double().norm())

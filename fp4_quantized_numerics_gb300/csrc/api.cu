@@ -28,7 +28,7 @@ inline ufp4_status from_cuda(cudaError_t e) {
 bool valid_qtensor(const ufp4_qtensor *q) {
     if (!q || q->reserved != 0) return false;
     if (q->rows < 0 || q->k < 0 || q->k % UFP4_BLOCK != 0) return false;
-    if (q->grid != UFP4_E2M1 && q->grid != UFP4_E1M2) return false;
+    if (q->grid != UFP4_E2M1 && q->grid != UFP4_E1M2 && q->grid != UFP4_E2M1C) return false;
     if (q->rows == 0 || q->k == 0) return true;
     if (!q->codes || !q->scales || !q->tensor_scale) return false;
     return aligned(q->codes, 16) && aligned(q->scales, 16) && aligned(q->tensor_scale, 4);
@@ -40,7 +40,7 @@ ufp4_status check_quant_args(const void *x, int32_t dtype, int64_t rows, int64_t
     if (!p || !out) return UFP4_ERR_INVALID;
     if (dtype != UFP4_BF16 && dtype != UFP4_FP32) return UFP4_ERR_INVALID;
     if (p->block != UFP4_BLOCK) return UFP4_ERR_UNSUPPORTED;
-    if (p->grid != UFP4_E2M1 && p->grid != UFP4_E1M2) return UFP4_ERR_INVALID;
+    if (p->grid != UFP4_E2M1 && p->grid != UFP4_E1M2 && p->grid != UFP4_E2M1C) return UFP4_ERR_INVALID;
     if (p->round != UFP4_RTNE && p->round != UFP4_SR) return UFP4_ERR_INVALID;
     if ((p->rht != 0 && p->rht != 1) || (p->colwise != 0 && p->colwise != 1) || p->reserved != 0)
         return UFP4_ERR_INVALID;
@@ -204,7 +204,7 @@ ufp4_status ufp4_quantize_grouped(const void *x, int32_t dtype, int64_t cols, in
         return UFP4_ERR_INVALID;
     if (dtype != UFP4_BF16 && dtype != UFP4_FP32) return UFP4_ERR_INVALID;
     if (p->block != UFP4_BLOCK) return UFP4_ERR_UNSUPPORTED;
-    if (p->grid != UFP4_E2M1 && p->grid != UFP4_E1M2) return UFP4_ERR_INVALID;
+    if (p->grid != UFP4_E2M1 && p->grid != UFP4_E1M2 && p->grid != UFP4_E2M1C) return UFP4_ERR_INVALID;
     if (p->round != UFP4_RTNE && p->round != UFP4_SR) return UFP4_ERR_INVALID;
     if ((p->rht != 0 && p->rht != 1) || (p->colwise != 0 && p->colwise != 1) || p->reserved != 0)
         return UFP4_ERR_INVALID;

@@ -14,11 +14,19 @@ namespace ufp4 {
 
 constexpr int kE2M1 = 0;
 constexpr int kE1M2 = 1;
+// E2M1 restricted to its uniform part {0, .5, 1, 1.5, 2} (codes 0..4): the
+// clamped-E2M1 ablation.  It quantizes through the uniform-grid (E1M2)
+// kernels with qmax 2 and top index 4; its codes are E2M1 codes.
+constexpr int kE2M1C = 2;
 constexpr int kRTNE = 0;
 constexpr int kSR = 1;
 constexpr float kFltMax = 3.402823466e38f;
 
-__host__ __device__ __forceinline__ float grid_qmax(int grid) { return grid == kE2M1 ? 6.0f : 3.5f; }
+__host__ __device__ __forceinline__ float grid_qmax(int grid) {
+    return grid == kE2M1 ? 6.0f : (grid == kE1M2 ? 3.5f : 2.0f);
+}
+// Largest magnitude index of the grid.
+__host__ __device__ __forceinline__ uint32_t grid_top(int grid) { return grid == kE2M1C ? 4u : 7u; }
 
 __host__ __device__ __forceinline__ int64_t kpad_of(int64_t k) { return (k + 63) / 64 * 64; }
 __host__ __device__ __forceinline__ int64_t rpad_of(int64_t r) { return (r + 127) / 128 * 128; }
@@ -96,8 +104,8 @@ __device__ __forceinline__ uint32_t e2m1x2_rn(float lo, float hi) {
 // E1M2 round-to-nearest-even of q (grid units): m = rint(min(2|q|, 7)); 2|q|
 // is exact (or +inf, which clamps to 7).  Adding 2^23 rounds a value in
 // [0, 8) to an integer with ties to even, leaving it in the low mantissa bits.
-__device__ __forceinline__ uint32_t e1m2_rn(float q) {
-    const float a2 = fminf(fabsf(q) * 2.0f, 7.0f);
+__device__ __forceinline__ uint32_t e1m2_rn(float q, float top = 7.0f) {
+    const float a2 = fminf(fabsf(q) * 2.0f, top);
     const uint32_t m = __float_as_uint(__fadd_rn(a2, 8388608.0f)) & 7u;
     return m | ((__float_as_uint(q) >> 28) & 8u);
 }
@@ -106,7 +114,7 @@ __device__ __forceinline__ uint32_t e1m2_rn(float q) {
 // the grid point below |q| (clamped to qmax), then up with probability
 // p = (a - lo) / (hi - lo) against u = (r >> 8) * 2^-24.  Returns the code.
 template <int GRID>
-__device__ __forceinline__ uint32_t sr_code(float q, uint32_t r) {
+__device__ __forceinline__ uint32_t sr_code(float q, uint32_t r, uint32_t top = 7u) {
     // The decision "up iff (r >> 8) 2^-24 < p", p the position of |q| between
     // its grid neighbours, is taken in fixed point: with t = |q| scaled so
     // that the neighbours are consecutive integers, T = ceil(t 2^24) holds
@@ -116,7 +124,7 @@ __device__ __forceinline__ uint32_t sr_code(float q, uint32_t r) {
     // conversion per element instead of three.
     const uint32_t sgn = (__float_as_uint(q) >> 28) & 8u;
     if (GRID == kE1M2) {
-        const float t = fminf(fabsf(q) * 33554432.0f, 117440512.0f);   // 2|q| 2^24, at most 7 2^24
+        const float t = fminf(fabsf(q) * 33554432.0f, (float)(top << 24));   // 2|q| 2^24, at most top 2^24
         const uint32_t T = __float2uint_ru(t);
         return sgn | ((T >> 24) + (r < (T << 8) ? 1u : 0u));
     } else {

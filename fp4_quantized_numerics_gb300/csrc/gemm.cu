@@ -570,7 +570,7 @@ bool make_code_map(CUtensorMap *m, const uint8_t *codes, int64_t rows, int64_t k
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)(kpad / 2), (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(kpad / 2)};
-    const int bk = grid == kE2M1 ? Cfg<kE2M1>::kBK : Cfg<kE1M2>::kBK;
+    const int bk = grid == kE1M2 ? Cfg<kE1M2>::kBK : Cfg<kE2M1>::kBK;
     cuuint32_t box[2] = {(cuuint32_t)bk, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), dims, strides, box,
@@ -628,14 +628,15 @@ cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const f
     p.sfa = a_scales; p.sfb = b_scales; p.ts_a = a_ts; p.ts_b = b_ts;
     p.c = c; p.ldc = ldc; p.M = (int)M; p.N = (int)N;
     p.nkt = (int)(kpad / 64);
-    const int ks = grid == kE2M1 ? Cfg<kE2M1>::kKS : Cfg<kE1M2>::kKS;
+    const int ks = grid == kE1M2 ? Cfg<kE1M2>::kKS : Cfg<kE2M1>::kKS;
     p.num_kb = (p.nkt + ks - 1) / ks;
     p.ntm = (int)((M + BM - 1) / BM);
     p.ntn = (int)((N + BN - 1) / BN);
     p.nkt_a = p.nkt_b = p.nkt;
     p.b_rt = (int)((N + 127) / 128);
     const NoGroups none;
-    if (grid == kE2M1) return run_gemm<kE2M1>(ma, mb, mc, p, none, p.ntm * p.ntn, s);
+    // clamped-E2M1 codes are E2M1 codes
+    if (grid != kE1M2) return run_gemm<kE2M1>(ma, mb, mc, p, none, p.ntm * p.ntn, s);
     return run_gemm<kE1M2>(ma, mb, mc, p, none, p.ntm * p.ntn, s);
 }
 
@@ -655,7 +656,7 @@ cudaError_t launch_gemm_grouped(const uint8_t *a_codes, const uint8_t *a_scales,
     p.b_rt = (int)((b_rows + 127) / 128);
     p.M = 1; p.N = 1;
     const int ntiles = tab.tiles[tab.n];
-    if (grid == kE2M1) return run_gemm<kE2M1>(ma, mb, mc, p, tab, ntiles, s);
+    if (grid != kE1M2) return run_gemm<kE2M1>(ma, mb, mc, p, tab, ntiles, s);
     return run_gemm<kE1M2>(ma, mb, mc, p, tab, ntiles, s);
 }
 

@@ -58,6 +58,10 @@ struct Args {
     uint8_t *codes, *scales;
     float *tensor_scale;
     double *stats_out;
+    // uniform grids (E1M2 kernels): qmax and the largest magnitude index,
+    // 3.5 / 7 for E1M2, 2 / 4 for clamped E2M1
+    float uqmax;
+    uint32_t utop;
 };
 
 // ------------------------------------------------------------------ loads
@@ -187,6 +191,7 @@ __device__ __forceinline__ void tensor_scale_prologue(const Args &a, float qmax,
 // b = 6 and b = 3.5 whenever a >= 2^-123; below that (results near the
 // subnormal range) the IEEE division is used.
 __device__ __forceinline__ float div_qmax(float a, float qmax) {
+    if (qmax == 2.0f) return a * 0.5f;                        // exact
     if (!(a >= 9.4039548e-38f)) return __fdiv_rn(a, qmax);   // 2^-123, NaN, 0
     const float rcp = qmax == 6.0f ? 0.16666667163372040f : 0.28571429848670960f;
     const float q = __fmul_rn(a, rcp);
@@ -224,7 +229,7 @@ __device__ __forceinline__ uint32_t codes8(const float q[8], const Args &a, uint
             for (int j = 0; j < 4; ++j) w |= e2m1x2_rn(q[2 * j], q[2 * j + 1]) << (8 * j);
         } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) w |= e1m2_rn(q[j]) << (4 * j);
+            for (int j = 0; j < 8; ++j) w |= e1m2_rn(q[j], (float)a.utop) << (4 * j);
         }
     } else {
         const uint2 key = make_uint2((uint32_t)a.sr_seed, (uint32_t)(a.sr_seed >> 32));
@@ -235,10 +240,10 @@ __device__ __forceinline__ uint32_t codes8(const float q[8], const Args &a, uint
             const uint4 r = philox4x32_10(
                 make_uint4((uint32_t)c, (uint32_t)(c >> 32), (uint32_t)a.sr_counter,
                            (uint32_t)(a.sr_counter >> 32)), key);
-            w |= sr_code<GRID>(q[4 * t + 0], r.x) << (16 * t + 0);
-            w |= sr_code<GRID>(q[4 * t + 1], r.y) << (16 * t + 4);
-            w |= sr_code<GRID>(q[4 * t + 2], r.z) << (16 * t + 8);
-            w |= sr_code<GRID>(q[4 * t + 3], r.w) << (16 * t + 12);
+            w |= sr_code<GRID>(q[4 * t + 0], r.x, a.utop) << (16 * t + 0);
+            w |= sr_code<GRID>(q[4 * t + 1], r.y, a.utop) << (16 * t + 4);
+            w |= sr_code<GRID>(q[4 * t + 2], r.z, a.utop) << (16 * t + 8);
+            w |= sr_code<GRID>(q[4 * t + 3], r.w, a.utop) << (16 * t + 12);
         }
     }
     return w;
@@ -547,7 +552,7 @@ __device__ __forceinline__ uint2 round_block(float ql[8], float qh[8], uint32_t 
             for (int j = 0; j < 8; ++j) upk2(mul2(pk2(ql[j], qh[j]), S8), ql[j], qh[j]);
         }
         if (e < 8u || e >= 0x7Eu) {
-            const float c = 7.0f * 0.001953125f;   // 7 * 2^-9
+            const float c = (float)a.utop * 0.001953125f;   // top index * 2^-9
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 ql[j] = fminf(fmaxf(ql[j], -c), c);
@@ -571,7 +576,7 @@ template <class In, int GRID, int ROUND, bool RHT>
 __device__ __forceinline__ void quant_block_row(const Args &a, const Raw<In> &raw, uint32_t r, uint32_t b,
                                                 const Signs &sg, float S_enc, const float *s_k,
                                                 uint32_t cstride, uint32_t nkt, bool folded) {
-    const float qmax = GRID == kE2M1 ? 6.0f : 3.5f;
+    const float qmax = GRID == kE2M1 ? 6.0f : a.uqmax;
     float lo[8], hi[8];
     block_values<In, RHT>(raw, sg, lo, hi);
     float m = 0.0f;
@@ -596,7 +601,7 @@ __device__ __forceinline__ void quant_pair_row(const Args &a, const Raw<__nv_bfl
                                                uint32_t r1, uint32_t b1, bool has_b, const Signs &sg,
                                                float S_enc, const float *s_k, uint32_t cstride,
                                                uint32_t nkt, bool folded) {
-    const float qmax = GRID == kE2M1 ? 6.0f : 3.5f;
+    const float qmax = GRID == kE2M1 ? 6.0f : a.uqmax;
     uint64_t P[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) P[j] = RHT ? pk2(ra.get(j, sg), rb.get(j, sg)) : pk2(ra.get(j), rb.get(j));
@@ -637,7 +642,7 @@ __global__ void __launch_bounds__(kThreads) k_quant_rowwise(Args a, FastDiv bdiv
                                                             uint32_t total) {
     __shared__ float s_k[256];
     __shared__ float s_red[kThreads / 32];
-    const float qmax = GRID == kE2M1 ? 6.0f : 3.5f;
+    const float qmax = GRID == kE2M1 ? 6.0f : a.uqmax;
     float S_enc;
     bool folded = false;
     tensor_scale_prologue(a, qmax, RHT ? 0.25f : 1.0f, s_k, s_red, S_enc, GRID == kE1M2 && ROUND == kRTNE,
@@ -822,7 +827,7 @@ template <class In, int GRID, int ROUND, bool RHT>
 __device__ __forceinline__ void quant_unit_col(const Args &a, const ColRaw<In> &raw, uint32_t kb, uint32_t c,
                                                bool real, const Signs &sg, float S_enc, const float *s_k,
                                                uint32_t cstride, uint32_t nkt, bool folded) {
-    const float qmax = GRID == kE2M1 ? 6.0f : 3.5f;
+    const float qmax = GRID == kE2M1 ? 6.0f : a.uqmax;
     uint64_t P[16];
     col_values<In, RHT>(raw, sg, P);
     float v0[16], v1[16];
@@ -850,7 +855,7 @@ __global__ void __launch_bounds__(kThreads) k_quant_colwise(Args a, FastDiv cdiv
                                                             uint32_t total) {
     __shared__ float s_k[256];
     __shared__ float s_red[kThreads / 32];
-    const float qmax = GRID == kE2M1 ? 6.0f : 3.5f;
+    const float qmax = GRID == kE2M1 ? 6.0f : a.uqmax;
     float S_enc;
     bool folded = false;
     tensor_scale_prologue(a, qmax, RHT ? 0.25f : 1.0f, s_k, s_red, S_enc, GRID == kE1M2 && ROUND == kRTNE,
@@ -952,7 +957,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_row_staged(Args a,
     float S_enc = 1.0f;
     bool folded = false;
     if (!AMAX)
-        tensor_scale_prologue(a, GRID == kE2M1 ? 6.0f : 3.5f, RHT ? 0.25f : 1.0f, s_k, s_red, S_enc,
+        tensor_scale_prologue(a, GRID == kE2M1 ? 6.0f : a.uqmax, RHT ? 0.25f : 1.0f, s_k, s_red, S_enc,
                               GRID == kE1M2 && ROUND == kRTNE, &folded);
     const uint32_t smask = RHT ? rht_sign_mask(a.rht_seed) : 0u;
     const Signs sg = row_signs<In>(smask);
@@ -1086,7 +1091,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_col_staged(Args a,
     float S_enc = 1.0f;
     bool folded = false;
     if (!AMAX)
-        tensor_scale_prologue(a, GRID == kE2M1 ? 6.0f : 3.5f, RHT ? 0.25f : 1.0f, s_k, s_red, S_enc,
+        tensor_scale_prologue(a, GRID == kE2M1 ? 6.0f : a.uqmax, RHT ? 0.25f : 1.0f, s_k, s_red, S_enc,
                               GRID == kE1M2 && ROUND == kRTNE, &folded);
     const uint32_t smask = RHT ? rht_sign_mask(a.rht_seed) : 0u;
     const Signs sg = col_signs<In>(smask);
@@ -1164,7 +1169,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_dual_staged(Args a
     uint32_t issued = 0, j = 0;
     if (threadIdx.x == 0)
         for (uint32_t t = 0; t < kRing; ++t) col_issue<In>(ring, ar, t, nchunks, ncc, issued);
-    const float qmax = GRID == kE2M1 ? 6.0f : 3.5f;
+    const float qmax = GRID == kE2M1 ? 6.0f : ar.uqmax;
     float Sr = 1.0f, Sc = 1.0f;
     bool fr = false, fc = false;
     if (!AMAX) {
@@ -1401,7 +1406,7 @@ __global__ void __launch_bounds__(kThreads) k_quant_grouped(Args a, const __grid
                                                             FastDiv div, uint32_t per_row, const uint32_t *slots) {
     __shared__ GroupSmem sm;
     load_group_tables(gt, sm);
-    const float qmax = GRID == kE2M1 ? 6.0f : 3.5f;
+    const float qmax = GRID == kE2M1 ? 6.0f : a.uqmax;
     for (int e = threadIdx.x; e < gt.n; e += blockDim.x) {
         const float A_t = __uint_as_float(slots[e]);
         float se = 1.0f, sd = 1.0f;
@@ -1461,6 +1466,8 @@ cudaError_t quantize_grouped_typed(const QuantLaunch &q, const GroupQuant &gt, v
     a.rht_seed = q.rht_seed; a.sr_seed = q.sr_seed; a.sr_counter = q.sr_counter; a.elem_base = 0;
     a.status = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsStatus);
     a.codes = q.codes; a.scales = q.scales; a.tensor_scale = q.tensor_scale;
+    a.uqmax = q.grid == kE2M1C ? 2.0f : 3.5f;
+    a.utop = grid_top(q.grid);
     uint32_t *slots = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsPartials);
     cudaError_t e = cudaMemsetAsync(ws, 0, kWsPartials + (size_t)gt.n * sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
@@ -1487,8 +1494,9 @@ cudaError_t quantize_grouped_typed(const QuantLaunch &q, const GroupQuant &gt, v
     const int64_t tq = gt.units[gt.n];
     const int g = (int)std::min<int64_t>(std::max<int64_t>((tq + kThreads - 1) / kThreads, 1), (int64_t)sms * 8);
     const FastDiv fd = make_fastdiv(per_row);
+    const int kgrid = q.grid == kE2M1 ? kE2M1 : kE1M2;   // clamped E2M1 runs the uniform-grid kernels
 #define UFP4_GQ(COL, GRID, ROUND, RHT)                                                            \
-    if (col == COL && q.grid == GRID && q.round == ROUND && (q.rht != 0) == RHT) {              \
+    if (col == COL && kgrid == GRID && q.round == ROUND && (q.rht != 0) == RHT) {              \
         k_quant_grouped<In, GRID, ROUND, RHT, COL><<<g, kThreads, 0, s>>>(a, gt, fd, per_row, slots); \
         return cudaGetLastError();                                                               \
     }
@@ -1765,8 +1773,9 @@ cudaError_t quantize_typed(const QuantLaunch &q, Args &a, void *ws, cudaStream_t
         cudaError_t e = q.rht ? amax_pass<In, true>(q, a, staged, s) : amax_pass<In, false>(q, a, staged, s);
         if (e != cudaSuccess) return e;
     }
+    const int kgrid = q.grid == kE2M1 ? kE2M1 : kE1M2;   // clamped E2M1 runs the uniform-grid kernels
 #define UFP4_Q(GRID, ROUND, RHT)                                                   \
-    if (q.grid == GRID && q.round == ROUND && (q.rht != 0) == RHT)                 \
+    if (kgrid == GRID && q.round == ROUND && (q.rht != 0) == RHT)                  \
         return quant_pass<In, GRID, ROUND, RHT>(q, a, staged, s);
     UFP4_Q(kE2M1, kRTNE, false) UFP4_Q(kE2M1, kRTNE, true)
     UFP4_Q(kE2M1, kSR, false)   UFP4_Q(kE2M1, kSR, true)
@@ -1797,8 +1806,9 @@ cudaError_t quantize_dual_typed(const QuantLaunch &qr, const QuantLaunch &qc, Ar
         ac.partials = ac.partials_out;
         ar.n_partials = ac.n_partials = g;
     }
+    const int kgrid = qr.grid == kE2M1 ? kE2M1 : kE1M2;   // clamped E2M1 runs the uniform-grid kernels
 #define UFP4_D(GRID, ROUND, RHT)                                                                         \
-    if (qr.grid == GRID && qr.round == ROUND && (qr.rht != 0) == RHT)                                    \
+    if (kgrid == GRID && qr.round == ROUND && (qr.rht != 0) == RHT)                                      \
         return launch_staged(k_dual_staged<In, GRID, ROUND, RHT, false>, nch, nullptr, s, ar, ac, ncc, nch);
     UFP4_D(kE2M1, kRTNE, false) UFP4_D(kE2M1, kRTNE, true)
     UFP4_D(kE2M1, kSR, false)   UFP4_D(kE2M1, kSR, true)
@@ -1818,6 +1828,8 @@ Args make_args(const QuantLaunch &q, void *ws) {
     a.amax_in = q.amax_in;
     a.status = ws ? reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsStatus) : nullptr;
     a.codes = q.codes; a.scales = q.scales; a.tensor_scale = q.tensor_scale;
+    a.uqmax = q.grid == kE2M1C ? 2.0f : 3.5f;
+    a.utop = grid_top(q.grid);
     return a;
 }
 

@@ -20,7 +20,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libufp4.so")
 
-UFP4_E2M1, UFP4_E1M2 = 0, 1
+UFP4_E2M1, UFP4_E1M2, UFP4_E2M1C = 0, 1, 2
 UFP4_RTNE, UFP4_SR = 0, 1
 UFP4_BF16, UFP4_FP32 = 0, 1
 UFP4_OK, UFP4_ERR_INVALID, UFP4_ERR_UNSUPPORTED, UFP4_ERR_NONFINITE, UFP4_ERR_CUDA, \

@@ -59,11 +59,19 @@ typedef enum {
 } ufp4_status;
 
 /* 4-bit grids.  A code is (sign << 3) | m with magnitude index m = 0..7.
- *   UFP4_E2M1: magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6} -- the non-uniform
- *              Blackwell FP4 format ([ZC] "The cause").
- *   UFP4_E1M2: magnitudes {0, .5, 1, ..., 3.5} = m/2 -- the uniform grid of
- *              UFP4 ([ZC] "The fix -- UFP4"; [AN] "The UFP4 Recipe"). */
-typedef enum { UFP4_E2M1 = 0, UFP4_E1M2 = 1 } ufp4_grid;
+ *   UFP4_E2M1:  magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6} -- the non-uniform
+ *               Blackwell FP4 format ([ZC] "The cause").
+ *   UFP4_E1M2:  magnitudes {0, .5, 1, ..., 3.5} = m/2 -- the uniform grid of
+ *               UFP4 ([ZC] "The fix -- UFP4"; [AN] "The UFP4 Recipe").
+ *   UFP4_E2M1C: E2M1 clamped to its uniform part {0, .5, 1, 1.5, 2} (m <= 4,
+ *               qmax = 2): the "clamp E2M1 to emulate a uniform grid"
+ *               ablation that the pages report as failing ([ZC] Key points,
+ *               "Validation results").  Its codes are E2M1 codes, so its
+ *               GEMM is the native E2M1 one.
+ * A symmetric uniform INT4 grid {-7..7} needs no entry: with the same
+ * two-level scaling its codes and block scales equal E1M2's bit for bit and
+ * only the tensor scale (x 1/2) and the value of a code (x 2) differ. */
+typedef enum { UFP4_E2M1 = 0, UFP4_E1M2 = 1, UFP4_E2M1C = 2 } ufp4_grid;
 
 /* Rounding onto the grid: round-to-nearest-even, or stochastic rounding
  * (the pages apply SR to dY only: [HP] key contributions; [ZC] "The fix"). */

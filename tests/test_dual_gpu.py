@@ -42,7 +42,7 @@ def _single(U, x, grid, rht, rnd, sr_counter, colwise, amax=None):
                                  colwise=colwise, amax_in=amax))
 
 
-DUAL_CASES = [(dt, grid, rht, rnd) for dt in (torch.bfloat16, torch.float32) for grid in (0, 1)
+DUAL_CASES = [(dt, grid, rht, rnd) for dt in (torch.bfloat16, torch.float32) for grid in (0, 1, 2)
               for rht in (False, True) for rnd in (0, 1)]
 
 
@@ -86,7 +86,8 @@ def test_dual_fallback_mixed_parameters(U):
     _assert_same(_host(out_c), _single(U, x, 0, True, 1, 5, True))
 
 
-@pytest.mark.parametrize("grid,rht,rnd", [(0, False, 0), (1, False, 1), (1, True, 0), (0, True, 1)])
+@pytest.mark.parametrize("grid,rht,rnd", [(0, False, 0), (1, False, 1), (1, True, 0), (0, True, 1), (2, False, 1),
+                                          (2, True, 0)])
 def test_dual_matches_oracle(U, oracle, grid, rht, rnd):
     xn = inputs.smoke(0)["x"]   # 256 x 1024 N(0,1), BF16-representable
     x = torch.from_numpy(np.ascontiguousarray(xn)).to(torch.bfloat16).cuda()

@@ -43,14 +43,14 @@ def _gemm_case(U, oracle, a, b, grid, rht=False, col_a=False, col_b=False, round
     return c.cpu().numpy().astype(np.float64), ref
 
 
-@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("grid", [0, 1, 2])
 def test_smoke_gemm_256(U, oracle, grid):
     d = inputs.smoke(0)
     c, ref = _gemm_case(U, oracle, d["a"], d["b"], grid)
     assert _rel_fro(c, ref) <= TOL
 
 
-@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("grid", [0, 1, 2])
 @pytest.mark.parametrize("M,N,K", [(128, 128, 64), (300, 200, 320), (129, 257, 1040),
                                    (64, 48, 16), (256, 384, 2048), (130, 140, 4160)])
 def test_ragged_and_multistage(U, oracle, grid, M, N, K):

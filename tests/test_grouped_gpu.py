@@ -74,7 +74,7 @@ def _check_segments(got, ref, rht):
             assert d.max() <= 1 and (d > 0).mean() <= 1e-3
 
 
-@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("grid", [0, 1, 2])
 @pytest.mark.parametrize("rht", [False, True])
 @pytest.mark.parametrize("colwise", [False, True])
 def test_grouped_quantize_matches_oracle(U, oracle, grid, rht, colwise):

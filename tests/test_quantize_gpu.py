@@ -67,7 +67,8 @@ def _compare(g, r, rht):
         assert (g["scales"] != r["scales"]).mean() <= 1e-3
 
 
-CASES = [(grid, rht, rnd, col) for grid in (0, 1) for rht in (False, True)
+# grid 2 = clamped E2M1 ({0, .5, 1, 1.5, 2}, the pages' failed uniform-grid ablation)
+CASES = [(grid, rht, rnd, col) for grid in (0, 1, 2) for rht in (False, True)
          for rnd in (0, 1) for col in (False, True)]
 
 
@@ -82,7 +83,7 @@ def test_smoke_config_all_modes(U, oracle, grid, rht, rnd, col):
 
 @pytest.mark.parametrize("shape,col", [((300, 80), False), ((37, 208), False), ((48, 12), True),
                                        ((144, 260), True), ((16, 16), False), ((16, 4), True)])
-@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("grid", [0, 1, 2])
 def test_ragged_shapes(U, oracle, shape, col, grid):
     x = inputs.normal(31, shape)
     for rht in (False, True):
@@ -92,7 +93,7 @@ def test_ragged_shapes(U, oracle, shape, col, grid):
             _compare(g, r, rht)
 
 
-@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("grid", [0, 1, 2])
 def test_fp32_input(U, oracle, grid):
     x = np.random.default_rng(5).standard_normal((96, 160)).astype(np.float32)
     for col in (False, True):
@@ -102,7 +103,7 @@ def test_fp32_input(U, oracle, grid):
             _compare(g, r, False)
 
 
-@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("grid", [0, 1, 2])
 def test_outlier_config(U, oracle, grid):
     x = inputs.outlier(0)["x"]
     for rht in (False, True):
@@ -113,7 +114,7 @@ def test_outlier_config(U, oracle, grid):
 
 def test_amax_in_and_special_tensors(U, oracle):
     x = inputs.normal(32, (64, 64))
-    for grid in (0, 1):
+    for grid in (0, 1, 2):
         g = _gpu_quant(U, x, grid, False, 0, False, amax_in=3.0)
         r = oracle.quantize(x, grid, amax_in=3.0)
         _compare(g, r, False)
@@ -160,7 +161,7 @@ def test_nonfinite_input_is_reported(U):
     assert U.ufp4_check(ws) == U.UFP4_OK
 
 
-@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("grid", [0, 1, 2])
 def test_dequantize_matches_oracle(U, oracle, grid):
     """Codes from the RHT-off path are bit-exact, so both sides decode the
     same codes; the inverse transform (fp32 butterflies vs fp64) must agree
@@ -178,7 +179,7 @@ def test_dequantize_matches_oracle(U, oracle, grid):
     assert np.abs(out - ref).max() <= 1e-6 * np.abs(ref).max()
 
 
-@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("grid", [0, 1, 2])
 def test_stats_match_oracle(U, oracle, grid):
     x = inputs.smoke(0)["x"]
     for rht in (False, True):
