@@ -660,6 +660,20 @@ cudaError_t launch_gemm_grouped(const uint8_t *a_codes, const uint8_t *a_scales,
     return run_gemm<kE1M2>(ma, mb, mc, p, tab, ntiles, s);
 }
 
+bool make_input_tile_map(void *tmap, const void *x, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                         int box_rows) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(static_cast<CUtensorMap *>(tmap), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x),
+                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 cudaError_t read_timeout_flag(uint32_t *flag, cudaStream_t s) {
     cudaError_t e = cudaMemcpyFromSymbolAsync(flag, g_ufp4_timeout, sizeof(uint32_t), 0,
                                               cudaMemcpyDeviceToHost, s);

@@ -71,6 +71,12 @@ cudaError_t launch_dequantize(const uint8_t *codes, const uint8_t *scales, const
 // Writes n_ctas x 8 double partial sums to ws + kWsStats; returns n_ctas.
 cudaError_t launch_stats(const QuantLaunch &q, void *ws, int *n_ctas, cudaStream_t s);
 
+// 2-D TMA tensor map (CUtensorMap, 128 bytes) of a BF16 matrix rows x cols
+// with row stride ld elements; tiles of box_cols x box_rows, no swizzle, out
+// of range elements read as zero.
+bool make_input_tile_map(void *tmap, const void *x, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                         int box_rows);
+
 // Row-wise (qr) and column-wise (qc) quantization of the same x in one pass
 // over x (falls back to two passes when the parameters or the layout do not
 // allow it).

@@ -29,6 +29,8 @@
 #include "internal.h"
 #include "ptx.cuh"
 
+#include <cuda.h>
+
 #include <algorithm>
 #include <cfloat>
 #include <mutex>
@@ -824,9 +826,10 @@ __global__ void __launch_bounds__(kThreads) k_amax_colwise(Args a, FastDiv cdiv,
 // row-block kb (two output blocks: rows c and c+1 of the result, block kb).
 // `real` = false for the padding blocks past the last row (zeros written).
 template <class In, int GRID, int ROUND, bool RHT>
-__device__ __forceinline__ void quant_unit_col(const Args &a, const ColRaw<In> &raw, uint32_t kb, uint32_t c,
+__device__ __forceinline__ void col_unit_words(const Args &a, const ColRaw<In> &raw, uint32_t kb, uint32_t c,
                                                bool real, const Signs &sg, float S_enc, const float *s_k,
-                                               uint32_t cstride, uint32_t nkt, bool folded) {
+                                               bool folded, uint2 &w0, uint2 &w1, uint32_t &e0_out,
+                                               uint32_t &e1_out) {
     const float qmax = GRID == kE2M1 ? 6.0f : a.uqmax;
     uint64_t P[16];
     col_values<In, RHT>(raw, sg, P);
@@ -846,8 +849,23 @@ __device__ __forceinline__ void quant_unit_col(const Args &a, const ColRaw<In> &
     for (int i = 0; i < 16; ++i) upk2(mul2(P[i], K2), v0[i], v1[i]);
     const uint64_t R = (uint64_t)a.rows;
     const uint64_t i0 = a.elem_base + (uint64_t)c * R + (uint64_t)kb * 16u;
-    store_block(a, c, kb, round_block<GRID, ROUND>(v0, v0 + 8, e0, folded, a, i0), e0, cstride, nkt);
-    store_block(a, c + 1, kb, round_block<GRID, ROUND>(v1, v1 + 8, e1, folded, a, i0 + R), e1, cstride, nkt);
+    w0 = round_block<GRID, ROUND>(v0, v0 + 8, e0, folded, a, i0);
+    w1 = round_block<GRID, ROUND>(v1, v1 + 8, e1, folded, a, i0 + R);
+    if (e0 == 0) w0 = make_uint2(0u, 0u);
+    if (e1 == 0) w1 = make_uint2(0u, 0u);
+    e0_out = e0;
+    e1_out = e1;
+}
+
+template <class In, int GRID, int ROUND, bool RHT>
+__device__ __forceinline__ void quant_unit_col(const Args &a, const ColRaw<In> &raw, uint32_t kb, uint32_t c,
+                                               bool real, const Signs &sg, float S_enc, const float *s_k,
+                                               uint32_t cstride, uint32_t nkt, bool folded) {
+    uint2 w0, w1;
+    uint32_t e0, e1;
+    col_unit_words<In, GRID, ROUND, RHT>(a, raw, kb, c, real, sg, S_enc, s_k, folded, w0, w1, e0, e1);
+    store_block(a, c, kb, w0, e0, cstride, nkt);
+    store_block(a, c + 1, kb, w1, e1, cstride, nkt);
 }
 
 template <class In, int GRID, int ROUND, bool RHT>
@@ -886,22 +904,24 @@ __global__ void __launch_bounds__(kThreads) k_quant_colwise(Args a, FastDiv cdiv
 // For inputs whose bytes can be streamed in 16-byte-aligned pieces (row-wise:
 // the whole tensor is contiguous; column-wise: every row segment of a chunk
 // is a multiple of 16 bytes), one thread per CTA streams 16 KB chunks into a
-// 3-deep shared-memory ring with cp.async.bulk (mbarrier completion), so each
-// CTA keeps up to 48 KB of loads in flight independent of the register
-// budget, and all 256 threads compute from shared memory.  The kernels are
-// issue-bound, so they are compiled for at least 3 resident CTAs per SM
-// (registers <= 80; measured: 23 % faster RTNE, 17 % faster SR than 2 CTAs).
-constexpr int kRing = 3;
+// shared-memory ring with cp.async.bulk (mbarrier completion), so each CTA
+// keeps its loads in flight independent of the register budget, and all 256
+// threads compute from shared memory.  Quantization passes are issue-bound:
+// a 3-deep ring (48 KB) and at least 3 resident CTAs per SM (registers <= 80;
+// measured 17-25 % faster than 2 CTAs); the amax passes stream with little
+// arithmetic and keep a 4-deep ring (64 KB in flight per CTA).
+template <bool AMAX> constexpr int ring_depth() { return AMAX ? 4 : 3; }
 constexpr int kStagedMinCtas = 3;
 constexpr uint32_t kChunk = 16384;
-constexpr uint32_t kRingSmem = kRing * kChunk + 64;
+template <bool AMAX> constexpr uint32_t ring_smem() { return ring_depth<AMAX>() * kChunk + 64; }
 constexpr long long kRingWait = 4000000000LL;
 
 struct RingCtl {
     uint32_t buf;    // shared address of stage 0
-    uint32_t bars;   // shared address of the kRing mbarriers
+    uint32_t bars;   // shared address of the ring's mbarriers
 };
 
+template <int kRing>
 __device__ __forceinline__ RingCtl ring_init(uint8_t *dsm) {
     RingCtl r;
     r.buf = ptx::smem_u32(dsm);
@@ -915,6 +935,7 @@ __device__ __forceinline__ RingCtl ring_init(uint8_t *dsm) {
 }
 
 // Waits for chunk j's stage; false (for every thread) if any thread gave up.
+template <int kRing>
 __device__ __forceinline__ bool ring_wait(const RingCtl &r, uint32_t j) {
     const bool ok = ptx::mbar_wait_bounded(r.bars + 8u * (j % kRing), (j / kRing) & 1u, kRingWait);
     return __syncthreads_and(ok) != 0;
@@ -922,6 +943,7 @@ __device__ __forceinline__ bool ring_wait(const RingCtl &r, uint32_t j) {
 
 // After an early exit: the issuing thread waits (bounded) for every copy it
 // started and that nobody consumed, so none lands in freed shared memory.
+template <int kRing>
 __device__ __forceinline__ void ring_drain(const RingCtl &r, uint32_t consumed, uint32_t issued) {
     if (threadIdx.x != 0) return;
     for (uint32_t j = consumed; j < issued; ++j)
@@ -929,7 +951,7 @@ __device__ __forceinline__ void ring_drain(const RingCtl &r, uint32_t consumed, 
 }
 
 // Row-wise chunks: chunk i = bytes [i * kChunk, ...) of the contiguous input.
-template <class In>
+template <class In, int kRing>
 __device__ __forceinline__ void row_issue(const RingCtl &r, const Args &a, uint32_t j, uint32_t nchunks,
                                           uint64_t total_bytes, uint32_t &issued) {
     const uint32_t i = blockIdx.x + j * gridDim.x;
@@ -946,14 +968,15 @@ __device__ __forceinline__ void row_issue(const RingCtl &r, const Args &a, uint3
 template <class In, int GRID, int ROUND, bool RHT, bool AMAX>
 __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_row_staged(Args a, FastDiv bdiv, uint32_t kvb,
                                                          uint32_t nchunks, uint64_t total_bytes) {
+    constexpr int kRing = ring_depth<AMAX>();
     extern __shared__ __align__(128) uint8_t dsm[];
     __shared__ float s_k[256];
     __shared__ float s_red[kThreads / 32];
     // start streaming before the tensor-scale prologue so its latency overlaps
-    const RingCtl ring = ring_init(dsm);
+    const RingCtl ring = ring_init<kRing>(dsm);
     uint32_t issued = 0, j = 0;
     if (threadIdx.x == 0)
-        for (uint32_t t = 0; t < kRing; ++t) row_issue<In>(ring, a, t, nchunks, total_bytes, issued);
+        for (uint32_t t = 0; t < kRing; ++t) row_issue<In, kRing>(ring, a, t, nchunks, total_bytes, issued);
     float S_enc = 1.0f;
     bool folded = false;
     if (!AMAX)
@@ -968,7 +991,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_row_staged(Args a,
     float m = 0.0f;
     bool ok = true;
     for (; j < nloc; ++j) {
-        if (!ring_wait(ring, j)) { ok = false; break; }
+        if (!ring_wait<kRing>(ring, j)) { ok = false; break; }
         const uint32_t i = blockIdx.x + j * gridDim.x;
         const uint32_t st = ring.buf + (j % kRing) * kChunk;
         if (sizeof(In) == 2) {
@@ -1028,11 +1051,11 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_row_staged(Args a,
             }
         }
         __syncthreads();
-        if (threadIdx.x == 0) row_issue<In>(ring, a, j + kRing, nchunks, total_bytes, issued);
+        if (threadIdx.x == 0) row_issue<In, kRing>(ring, a, j + kRing, nchunks, total_bytes, issued);
     }
     if (!ok) {
         if (threadIdx.x == 0) atomicOr(&g_quant_timeout, 1u);
-        ring_drain(ring, j, issued);
+        ring_drain<kRing>(ring, j, issued);
     }
     if (AMAX) {
 #pragma unroll
@@ -1058,7 +1081,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_row_staged(Args a,
 
 // Column-wise chunks: chunk i = (row block kb, column chunk cc) = 16 rows x
 // CW columns, CW = kChunk / (16 * sizeof(In)); column chunk fastest.
-template <class In>
+template <class In, int kRing>
 __device__ __forceinline__ void col_issue(const RingCtl &r, const Args &a, uint32_t j, uint32_t nchunks,
                                           uint32_t ncc, uint32_t &issued) {
     constexpr uint32_t CW = kChunk / (16 * sizeof(In));
@@ -1080,14 +1103,15 @@ __device__ __forceinline__ void col_issue(const RingCtl &r, const Args &a, uint3
 
 template <class In, int GRID, int ROUND, bool RHT, bool AMAX>
 __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_col_staged(Args a, uint32_t ncc, uint32_t nchunks) {
+    constexpr int kRing = ring_depth<AMAX>();
     extern __shared__ __align__(128) uint8_t dsm[];
     __shared__ float s_k[256];
     __shared__ float s_red[kThreads / 32];
     constexpr uint32_t CW = kChunk / (16 * sizeof(In));
-    const RingCtl ring = ring_init(dsm);
+    const RingCtl ring = ring_init<kRing>(dsm);
     uint32_t issued = 0, j = 0;
     if (threadIdx.x == 0)
-        for (uint32_t t = 0; t < kRing; ++t) col_issue<In>(ring, a, t, nchunks, ncc, issued);
+        for (uint32_t t = 0; t < kRing; ++t) col_issue<In, kRing>(ring, a, t, nchunks, ncc, issued);
     float S_enc = 1.0f;
     bool folded = false;
     if (!AMAX)
@@ -1100,7 +1124,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_col_staged(Args a,
     float m = 0.0f;
     bool ok = true;
     for (; j < nloc; ++j) {
-        if (!ring_wait(ring, j)) { ok = false; break; }
+        if (!ring_wait<kRing>(ring, j)) { ok = false; break; }
         const uint32_t i = blockIdx.x + j * gridDim.x;
         const uint32_t kb = i / ncc, cc = i - kb * ncc;
         const uint32_t c = cc * CW + 2 * threadIdx.x;
@@ -1121,11 +1145,11 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_col_staged(Args a,
             }
         }
         __syncthreads();
-        if (threadIdx.x == 0) col_issue<In>(ring, a, j + kRing, nchunks, ncc, issued);
+        if (threadIdx.x == 0) col_issue<In, kRing>(ring, a, j + kRing, nchunks, ncc, issued);
     }
     if (!ok) {
         if (threadIdx.x == 0) atomicOr(&g_quant_timeout, 1u);
-        ring_drain(ring, j, issued);
+        ring_drain<kRing>(ring, j, issued);
     }
     if (AMAX) {
 #pragma unroll
@@ -1160,15 +1184,16 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_col_staged(Args a,
 // row-wise and the column-wise transforms see different blocks).
 template <class In, int GRID, int ROUND, bool RHT, bool AMAX>
 __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_dual_staged(Args ar, Args ac, uint32_t ncc, uint32_t nchunks) {
+    constexpr int kRing = ring_depth<AMAX>();
     extern __shared__ __align__(128) uint8_t dsm[];
     __shared__ float s_kr[256], s_kc[256];
     __shared__ float s_red[kThreads / 32];
     constexpr uint32_t CW = kChunk / (16 * sizeof(In));
     constexpr uint32_t BPR = CW / 16;   // row-wise blocks per chunk row
-    const RingCtl ring = ring_init(dsm);
+    const RingCtl ring = ring_init<kRing>(dsm);
     uint32_t issued = 0, j = 0;
     if (threadIdx.x == 0)
-        for (uint32_t t = 0; t < kRing; ++t) col_issue<In>(ring, ar, t, nchunks, ncc, issued);
+        for (uint32_t t = 0; t < kRing; ++t) col_issue<In, kRing>(ring, ar, t, nchunks, ncc, issued);
     const float qmax = GRID == kE2M1 ? 6.0f : ar.uqmax;
     float Sr = 1.0f, Sc = 1.0f;
     bool fr = false, fc = false;
@@ -1189,7 +1214,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_dual_staged(Args a
     float mr = 0.0f, mc = 0.0f;
     bool ok = true;
     for (; j < nloc; ++j) {
-        if (!ring_wait(ring, j)) { ok = false; break; }
+        if (!ring_wait<kRing>(ring, j)) { ok = false; break; }
         const uint32_t i = blockIdx.x + j * gridDim.x;
         const uint32_t kb = i / ncc, cc = i - kb * ncc;
         const uint32_t c0 = cc * CW;
@@ -1267,11 +1292,11 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_dual_staged(Args a
             }
         }
         __syncthreads();
-        if (threadIdx.x == 0) col_issue<In>(ring, ar, j + kRing, nchunks, ncc, issued);
+        if (threadIdx.x == 0) col_issue<In, kRing>(ring, ar, j + kRing, nchunks, ncc, issued);
     }
     if (!ok) {
         if (threadIdx.x == 0) atomicOr(&g_quant_timeout, 1u);
-        ring_drain(ring, j, issued);
+        ring_drain<kRing>(ring, j, issued);
     }
     if (AMAX) {
 #pragma unroll
@@ -1306,6 +1331,206 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_dual_staged(Args a
             ac.scales[scale_offset32(r, b, nktc)] = 0;
         }
         zero_pad_rows(ac);
+    }
+}
+
+// BF16 inputs use square-ish tiles instead: 128 rows x 64 columns (16 KB) per
+// ring stage, one TMA tile copy each.  Each tile is 8 row blocks deep, so the
+// column-wise result of a column is 8 consecutive blocks (64 contiguous code
+// bytes, two 4-byte scale words): the codes are staged in shared memory and
+// leave as 16-byte stores, instead of 8-byte stores to 32 different rows per
+// warp instruction.  Row-wise, a tile row is 4 blocks (32 code bytes).
+constexpr uint32_t kTileRows = 128, kTileCols = 64;
+constexpr uint32_t kTileBytes = kTileRows * kTileCols * 2;   // BF16
+static_assert(kTileBytes == kChunk, "a tile fills one ring stage");
+constexpr uint32_t kColStageBytes = 8 * kTileCols * 8 + 8 * kTileCols;   // codes [8][64] x 8 B + scales [8][64]
+template <bool AMAX> constexpr uint32_t tile_smem() { return ring_smem<AMAX>() + (AMAX ? 0u : kColStageBytes); }
+
+template <int GRID, int ROUND, bool RHT, bool AMAX>
+__global__ void __launch_bounds__(kThreads, kStagedMinCtas)
+    k_dual_tile(const __grid_constant__ CUtensorMap tmx, Args ar, Args ac, uint32_t nct, uint32_t ntiles) {
+    constexpr int kRing = ring_depth<AMAX>();
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ float s_kr[256], s_kc[256];
+    __shared__ float s_red[kThreads / 32], s_red2[kThreads / 32];
+    const RingCtl ring = ring_init<kRing>(dsm);
+    uint8_t *stage_codes = dsm + kRing * kChunk + 64;            // [rb][cl] uint2 (quantization pass only)
+    uint8_t *stage_scales = stage_codes + 8 * kTileCols * 8;    // [rb][cl] byte
+    uint32_t issued = 0, j = 0;
+    auto issue = [&](uint32_t jj) {
+        const uint32_t i = blockIdx.x + jj * gridDim.x;
+        if (i >= ntiles) return;
+        const uint32_t rt = i / nct, ct = i - rt * nct;
+        const uint32_t bar = ring.bars + 8u * (jj % kRing);
+        ptx::mbar_arrive_expect_tx(bar, kTileBytes);   // out-of-range elements arrive as zeros
+        ptx::tma_load_2d(ring.buf + (jj % kRing) * kChunk, &tmx, (int32_t)(ct * kTileCols),
+                         (int32_t)(rt * kTileRows), bar);
+        issued = jj + 1;
+    };
+    if (threadIdx.x == 0) {
+        ptx::prefetch_tmap(&tmx);
+        for (uint32_t t = 0; t < kRing; ++t) issue(t);
+    }
+    const float qmax = GRID == kE2M1 ? 6.0f : ar.uqmax;
+    float Sr = 1.0f, Sc = 1.0f;
+    bool fr = false, fc = false;
+    if (!AMAX) {
+        float amr = 0.0f, amc = 0.0f;
+        tensor_scale_prologue(ar, qmax, RHT ? 0.25f : 1.0f, s_kr, s_red, Sr, GRID == kE1M2 && ROUND == kRTNE, &fr,
+                              &amr);
+        tensor_scale_prologue(ac, qmax, RHT ? 0.25f : 1.0f, s_kc, s_red, Sc, GRID == kE1M2 && ROUND == kRTNE, &fc,
+                              &amc);
+        if (blockIdx.x == 0 && threadIdx.x == 0 && ar.status && !isfinite(amc)) *ar.status = 1u;
+    }
+    const uint32_t smask = RHT ? rht_sign_mask(ar.rht_seed) : 0u;
+    const Signs sgr = row_signs<__nv_bfloat16>(smask), sgc = col_signs<__nv_bfloat16>(smask);
+    const uint32_t nloc = ntiles > blockIdx.x ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const uint32_t csr = (uint32_t)(ar.kpad / 2), nktr = (uint32_t)ar.nkt;
+    const uint32_t csc = (uint32_t)(ac.kpad / 2), nktc = (uint32_t)ac.nkt;
+    const uint32_t cols = (uint32_t)ar.cols, rows = (uint32_t)ar.rows;
+    const uint32_t kvr = cols / 16;               // real row-wise blocks per row
+    const uint32_t kbr = rows / 16;               // real column-wise blocks per column
+    const uint32_t kbp = (uint32_t)(ac.kpad / 16);   // column-wise blocks incl. padding
+    // column-wise unit of this thread: column pair cp, row block rb of the tile
+    const uint32_t cp = threadIdx.x % 32, rb = threadIdx.x / 32;
+    // row-wise pair of this thread: rows q and q + 64, block column bc of the tile
+    const uint32_t q = threadIdx.x / 4, bc = threadIdx.x % 4;
+    float mr = 0.0f, mc = 0.0f;
+    bool ok = true;
+    for (; j < nloc; ++j) {
+        if (!ring_wait<kRing>(ring, j)) { ok = false; break; }
+        const uint32_t i = blockIdx.x + j * gridDim.x;
+        const uint32_t rt = i / nct, ct = i - rt * nct;
+        const uint32_t r0 = rt * kTileRows, c0 = ct * kTileCols;
+        const uint32_t st = ring.buf + (j % kRing) * kChunk;
+        // ---- column-wise: columns c0 + 2cp, +1; rows r0 + 16 rb .. + 15
+        {
+            const uint32_t c = c0 + 2 * cp, kb = rt * 8 + rb;
+            ColRaw<__nv_bfloat16> raw;
+            raw.load_shared(st + 16 * rb * (kTileCols * 2) + cp * 4, kTileCols * 2);
+            if (AMAX) {
+                if (c < cols && kb < kbr) {
+                    uint64_t P[16];
+                    col_values<__nv_bfloat16, RHT>(raw, sgc, P);
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        float v0, v1;
+                        upk2(P[k], v0, v1);
+                        mc = max_nan(mc, max_nan(fabsf(v0), fabsf(v1)));
+                    }
+                }
+            } else {
+                uint2 w0 = make_uint2(0u, 0u), w1 = make_uint2(0u, 0u);
+                uint32_t e0 = 0, e1 = 0;
+                if (c < cols && kb < kbr)
+                    col_unit_words<__nv_bfloat16, GRID, ROUND, RHT>(ac, raw, kb, c, true, sgc, Sc, s_kc, fc, w0, w1,
+                                                                    e0, e1);
+                // staging [rb][column] (consecutive columns -> consecutive words)
+                reinterpret_cast<uint2 *>(stage_codes)[rb * kTileCols + 2 * cp] = w0;
+                reinterpret_cast<uint2 *>(stage_codes)[rb * kTileCols + 2 * cp + 1] = w1;
+                stage_scales[rb * kTileCols + 2 * cp] = (uint8_t)e0;
+                stage_scales[rb * kTileCols + 2 * cp + 1] = (uint8_t)e1;
+            }
+        }
+        // ---- row-wise: rows r0 + q and r0 + q + 64, block c0 / 16 + bc
+        {
+            const uint32_t r = r0 + q, b = ct * (kTileCols / 16) + bc;
+            if (r < rows && b < kvr) {
+                Raw<__nv_bfloat16> ra, rbw;
+                ra.load_shared(st + q * (kTileCols * 2) + bc * 32);
+                rbw.load_shared(st + (q + 64) * (kTileCols * 2) + bc * 32);
+                if (AMAX) {
+                    const bool has1 = r + 64 < rows;
+                    uint64_t P[16];
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        P[k] = RHT ? pk2(ra.get(k, sgr), rbw.get(k, sgr)) : pk2(ra.get(k), rbw.get(k));
+                    if (RHT) {
+#pragma unroll
+                        for (int sgs = 1; sgs < 16; sgs <<= 1) {
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) {
+                                if ((k & sgs) == 0) {
+                                    const uint64_t xx = P[k], yy = P[k + sgs];
+                                    P[k] = add2(xx, yy);
+                                    P[k + sgs] = sub2(xx, yy);
+                                }
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        float u0, u1;
+                        upk2(P[k], u0, u1);
+                        mr = max_nan(mr, fabsf(u0));
+                        if (has1) mr = max_nan(mr, fabsf(u1));   // rows past the end are zeros anyway
+                    }
+                } else {
+                    // one block at a time (measured faster here than the packed
+                    // pair, which holds twice the registers)
+                    quant_block_row<__nv_bfloat16, GRID, ROUND, RHT>(ar, ra, r, b, sgr, Sr, s_kr, csr, nktr, fr);
+                    if (r + 64 < rows)
+                        quant_block_row<__nv_bfloat16, GRID, ROUND, RHT>(ar, rbw, r + 64, b, sgr, Sr, s_kr, csr, nktr,
+                                                                         fr);
+                }
+            }
+        }
+        __syncthreads();   // tile consumed; column-wise results staged
+        if (threadIdx.x == 0) issue(j + kRing);
+        if (!AMAX) {
+            // column-wise codes: column c, blocks kb0 .. kb0 + 7 = 64 contiguous bytes
+            const uint32_t kb0 = rt * 8;
+            {
+                const uint32_t cl = threadIdx.x / 4, part = threadIdx.x % 4;   // 16 bytes each
+                const uint32_t c = c0 + cl, kb = kb0 + 2 * part;
+                if (c < cols && kb < kbp) {
+                    const uint2 a0 = reinterpret_cast<const uint2 *>(stage_codes)[(2 * part) * kTileCols + cl];
+                    const uint2 a1 = reinterpret_cast<const uint2 *>(stage_codes)[(2 * part + 1) * kTileCols + cl];
+                    *reinterpret_cast<uint4 *>(ac.codes + (size_t)c * csc + kb * 8) = make_uint4(a0.x, a0.y, a1.x, a1.y);
+                }
+            }
+            // column-wise scales: column c, blocks kb0 + 4h .. + 3 = one 4-byte word of an atom
+            if (threadIdx.x < 2 * kTileCols) {
+                const uint32_t cl = threadIdx.x / 2, h = threadIdx.x % 2;
+                const uint32_t c = c0 + cl, kb = kb0 + 4 * h;
+                if (c < cols && kb < kbp) {
+                    uint32_t w = 0;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) w |= (uint32_t)stage_scales[(4 * h + k) * kTileCols + cl] << (8 * k);
+                    *reinterpret_cast<uint32_t *>(ac.scales + scale_offset32(c, kb, nktc)) = w;
+                }
+            }
+            __syncthreads();   // staging buffers free for the next tile
+        }
+    }
+    if (!ok) {
+        if (threadIdx.x == 0) atomicOr(&g_quant_timeout, 1u);
+        ring_drain<kRing>(ring, j, issued);
+    }
+    if (AMAX) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            mr = max_nan(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+            mc = max_nan(mc, __shfl_xor_sync(0xffffffffu, mc, o));
+        }
+        if ((threadIdx.x & 31) == 0) { s_red[threadIdx.x >> 5] = mr; s_red2[threadIdx.x >> 5] = mc; }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int w = 1; w < kThreads / 32; ++w) { mr = max_nan(mr, s_red[w]); mc = max_nan(mc, s_red2[w]); }
+            ar.partials_out[blockIdx.x] = RHT ? mr * 0.25f : mr;
+            ac.partials_out[blockIdx.x] = RHT ? mc * 0.25f : mc;
+        }
+    } else {
+        // row-wise result: padding blocks cols/16 .. kpad/16 - 1 of every row
+        const uint32_t nbr = (uint32_t)(ar.kpad / 16) - kvr;
+        const uint32_t npr = (uint32_t)ar.out_rows * nbr;
+        for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < npr; t += gridDim.x * blockDim.x) {
+            const uint32_t r = t / nbr, b = kvr + (t - r * nbr);
+            *reinterpret_cast<uint2 *>(ar.codes + (size_t)r * csr + b * 8) = make_uint2(0u, 0u);
+            ar.scales[scale_offset32(r, b, nktr)] = 0;
+        }
+        zero_pad_rows(ar);
+        zero_pad_rows(ac);   // column-wise padding blocks were written from zero tiles above
     }
 }
 
@@ -1681,21 +1906,25 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t *codes, cons
 // Launch of a staged kernel: opt in to the ring's dynamic shared memory once
 // per kernel, persistent grid of the CTAs that fit at once.
 template <class K, class... P>
-cudaError_t launch_staged(K kern, int64_t work_ctas, int *grid_out, cudaStream_t s, P... args) {
+cudaError_t launch_staged_smem(K kern, size_t smem, int64_t work_ctas, int *grid_out, cudaStream_t s, P... args) {
     static std::mutex mu;
     static std::vector<const void *> done;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (std::find(done.begin(), done.end(), (const void *)kern) == done.end()) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingSmem);
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
             done.push_back((const void *)kern);
         }
     }
-    const int g = resident_grid(kern, work_ctas, kRingSmem);
+    const int g = resident_grid(kern, work_ctas, smem);
     if (grid_out) *grid_out = g;
-    kern<<<g, kThreads, kRingSmem, s>>>(args...);
+    kern<<<g, kThreads, smem, s>>>(args...);
     return cudaGetLastError();
+}
+template <bool AMAX, class K, class... P>
+cudaError_t launch_staged(K kern, int64_t work_ctas, int *grid_out, cudaStream_t s, P... args) {
+    return launch_staged_smem(kern, ring_smem<AMAX>(), work_ctas, grid_out, s, args...);
 }
 
 template <class In, int GRID, int ROUND, bool RHT>
@@ -1706,7 +1935,7 @@ cudaError_t quant_pass(const QuantLaunch &q, const Args &a, bool staged, cudaStr
             const uint32_t kvb = (uint32_t)(a.k / 16);
             const uint64_t tb = (uint64_t)a.rows * a.cols * sizeof(In);
             const uint32_t nch = (uint32_t)((tb + kChunk - 1) / kChunk);
-            return launch_staged(k_row_staged<In, GRID, ROUND, RHT, false>, nch, nullptr, s, a,
+            return launch_staged<false>(k_row_staged<In, GRID, ROUND, RHT, false>, nch, nullptr, s, a,
                                  make_fastdiv(kvb), kvb, nch, tb);
         }
         const uint32_t bpr = (uint32_t)(a.kpad / 16), total = (uint32_t)(a.out_rows * bpr);
@@ -1718,7 +1947,7 @@ cudaError_t quant_pass(const QuantLaunch &q, const Args &a, bool staged, cudaStr
     if (staged) {
         constexpr uint32_t CW = kChunk / (16 * sizeof(In));
         const uint32_t ncc = (uint32_t)((a.cols + CW - 1) / CW), nch = (uint32_t)(a.rows / 16) * ncc;
-        return launch_staged(k_col_staged<In, GRID, ROUND, RHT, false>, nch, nullptr, s, a, ncc, nch);
+        return launch_staged<false>(k_col_staged<In, GRID, ROUND, RHT, false>, nch, nullptr, s, a, ncc, nch);
     }
     const uint32_t ncp = (uint32_t)(a.cols / 2), ctotal = (uint32_t)((a.kpad / 16) * ncp);
     auto kern = k_quant_colwise<In, GRID, ROUND, RHT>;
@@ -1736,7 +1965,7 @@ cudaError_t amax_pass(const QuantLaunch &q, Args &a, bool staged, cudaStream_t s
         if (staged) {
             const uint64_t tb = (uint64_t)a.rows * a.cols * sizeof(In);
             const uint32_t nch = (uint32_t)((tb + kChunk - 1) / kChunk);
-            e = launch_staged(k_row_staged<In, 0, 0, RHT, true>, nch, &g, s, a, FastDiv{0, 0}, 0u, nch, tb);
+            e = launch_staged<true>(k_row_staged<In, 0, 0, RHT, true>, nch, &g, s, a, FastDiv{0, 0}, 0u, nch, tb);
         } else {
             const uint32_t bpr = (uint32_t)(a.k / 16), total = (uint32_t)(a.out_rows * bpr);
             auto kern = k_amax_rowwise<In, RHT>;
@@ -1748,7 +1977,7 @@ cudaError_t amax_pass(const QuantLaunch &q, Args &a, bool staged, cudaStream_t s
         if (staged) {
             constexpr uint32_t CW = kChunk / (16 * sizeof(In));
             const uint32_t ncc = (uint32_t)((a.cols + CW - 1) / CW), nch = (uint32_t)(a.rows / 16) * ncc;
-            e = launch_staged(k_col_staged<In, 0, 0, RHT, true>, nch, &g, s, a, ncc, nch);
+            e = launch_staged<true>(k_col_staged<In, 0, 0, RHT, true>, nch, &g, s, a, ncc, nch);
         } else {
             const uint32_t ncp = (uint32_t)(a.cols / 2), total = (uint32_t)((a.rows / 16) * ncp);
             auto kern = k_amax_colwise<In, RHT>;
@@ -1791,6 +2020,38 @@ cudaError_t quantize_typed(const QuantLaunch &q, Args &a, void *ws, cudaStream_t
 template <class In>
 cudaError_t quantize_dual_typed(const QuantLaunch &qr, const QuantLaunch &qc, Args &ar, Args &ac, void *ws,
                                 cudaStream_t s) {
+    if constexpr (std::is_same<In, __nv_bfloat16>::value) {
+        // BF16: 128 x 64 tiles by TMA (k_dual_tile)
+        alignas(64) CUtensorMap tm;
+        if (!make_input_tile_map(&tm, ar.x, ar.rows, ar.cols, ar.ld, kTileCols, kTileRows))
+            return cudaErrorInvalidValue;
+        const uint32_t nct = (uint32_t)((ar.cols + kTileCols - 1) / kTileCols);
+        const uint32_t ntiles = (uint32_t)((ar.rows + kTileRows - 1) / kTileRows) * nct;
+        ac.status = nullptr;   // the row-wise prologue reports both
+        if (!qr.amax_in || !qc.amax_in) {
+            ar.partials_out = reinterpret_cast<float *>(static_cast<char *>(ws) + kWsPartials);
+            ac.partials_out = ar.partials_out + kMaxPartials / 2;
+            auto kern = qr.rht ? k_dual_tile<0, 0, true, true> : k_dual_tile<0, 0, false, true>;
+            if (resident_grid(kern, ntiles, tile_smem<true>()) > kMaxPartials / 2) return cudaErrorInvalidValue;
+            int g = 1;
+            cudaError_t e = launch_staged_smem(kern, tile_smem<true>(), ntiles, &g, s, tm, ar, ac, nct, ntiles);
+            if (e != cudaSuccess) return e;
+            ar.partials = ar.partials_out;
+            ac.partials = ac.partials_out;
+            ar.n_partials = ac.n_partials = g;
+        }
+        const int kgrid = qr.grid == kE2M1 ? kE2M1 : kE1M2;   // clamped E2M1 runs the uniform-grid kernels
+#define UFP4_T(GRID, ROUND, RHT)                                                                          \
+        if (kgrid == GRID && qr.round == ROUND && (qr.rht != 0) == RHT)                                   \
+            return launch_staged_smem(k_dual_tile<GRID, ROUND, RHT, false>, tile_smem<false>(), ntiles, nullptr, s, tm, ar, \
+                                      ac, nct, ntiles);
+        UFP4_T(kE2M1, kRTNE, false) UFP4_T(kE2M1, kRTNE, true)
+        UFP4_T(kE2M1, kSR, false)   UFP4_T(kE2M1, kSR, true)
+        UFP4_T(kE1M2, kRTNE, false) UFP4_T(kE1M2, kRTNE, true)
+        UFP4_T(kE1M2, kSR, false)   UFP4_T(kE1M2, kSR, true)
+#undef UFP4_T
+        return cudaErrorInvalidValue;
+    } else {
     constexpr uint32_t CW = kChunk / (16 * sizeof(In));
     const uint32_t ncc = (uint32_t)((ar.cols + CW - 1) / CW), nch = (uint32_t)(ar.rows / 16) * ncc;
     ac.status = nullptr;   // the row-wise prologue reports both
@@ -1798,9 +2059,9 @@ cudaError_t quantize_dual_typed(const QuantLaunch &qr, const QuantLaunch &qc, Ar
         ar.partials_out = reinterpret_cast<float *>(static_cast<char *>(ws) + kWsPartials);
         ac.partials_out = ar.partials_out + kMaxPartials / 2;
         auto kern = qr.rht ? k_dual_staged<In, 0, 0, true, true> : k_dual_staged<In, 0, 0, false, true>;
-        if (resident_grid(kern, nch, kRingSmem) > kMaxPartials / 2) return cudaErrorInvalidValue;
+        if (resident_grid(kern, nch, ring_smem<true>()) > kMaxPartials / 2) return cudaErrorInvalidValue;
         int g = 1;
-        cudaError_t e = launch_staged(kern, nch, &g, s, ar, ac, ncc, nch);
+        cudaError_t e = launch_staged<true>(kern, nch, &g, s, ar, ac, ncc, nch);
         if (e != cudaSuccess) return e;
         ar.partials = ar.partials_out;
         ac.partials = ac.partials_out;
@@ -1809,13 +2070,14 @@ cudaError_t quantize_dual_typed(const QuantLaunch &qr, const QuantLaunch &qc, Ar
     const int kgrid = qr.grid == kE2M1 ? kE2M1 : kE1M2;   // clamped E2M1 runs the uniform-grid kernels
 #define UFP4_D(GRID, ROUND, RHT)                                                                         \
     if (kgrid == GRID && qr.round == ROUND && (qr.rht != 0) == RHT)                                      \
-        return launch_staged(k_dual_staged<In, GRID, ROUND, RHT, false>, nch, nullptr, s, ar, ac, ncc, nch);
+        return launch_staged<false>(k_dual_staged<In, GRID, ROUND, RHT, false>, nch, nullptr, s, ar, ac, ncc, nch);
     UFP4_D(kE2M1, kRTNE, false) UFP4_D(kE2M1, kRTNE, true)
     UFP4_D(kE2M1, kSR, false)   UFP4_D(kE2M1, kSR, true)
     UFP4_D(kE1M2, kRTNE, false) UFP4_D(kE1M2, kRTNE, true)
     UFP4_D(kE1M2, kSR, false)   UFP4_D(kE1M2, kSR, true)
 #undef UFP4_D
     return cudaErrorInvalidValue;
+    }
 }
 
 Args make_args(const QuantLaunch &q, void *ws) {
