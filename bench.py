@@ -382,16 +382,17 @@ def side_measurements(U, torch, dev, pk, flush):
     from fp4_quantized_numerics_gb300 import inputs
 
     def timeit(fn, n=30):
+        # median of n timed runs (each after an L2 flush)
         fn(); fn(); fn()
         torch.cuda.synchronize()
-        tot = 0.0
+        ts = []
         for _ in range(n):
             flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(); fn(); b.record()
             torch.cuda.synchronize()
-            tot += a.elapsed_time(b)
-        return tot / n
+            ts.append(a.elapsed_time(b))
+        return sorted(ts)[len(ts) // 2]
 
     out = {}
     x = inputs.device_normal((8192, 2048), 1.0, 11, dev)
@@ -407,6 +408,27 @@ def side_measurements(U, torch, dev, pk, flush):
     r["rht_overhead_amax_given"] = round(r["rht_off_amax_given"] / r["rht_on_amax_given"] - 1, 4)
     r["frac_hbm_rht_on_amax_given"] = round(r["rht_on_amax_given"] / pk["hbm_gbs"], 4)
     out["quantize_x_8192x2048_gbs"] = r
+
+    # steady state on a large operand (512 MB of BF16): one orientation and
+    # both, transform on, E1M2 RTNE
+    xl = inputs.device_normal((32768, 8192), 1.0, 15, dev)
+    ql = U.QTensor.empty(32768, 8192, U.UFP4_E1M2, dev)
+    qlc = U.QTensor.empty(8192, 32768, U.UFP4_E1M2, dev)
+    aml = torch.tensor([float(xl.float().abs().max()) * 1.25], device=dev)
+    L = {}
+    ms = timeit(lambda: U.ufp4_quantize(xl, U.UFP4_E1M2, rht=True, out=ql, ws=ws, amax_in=aml), 10)
+    L["single_amax_given"] = round(xl.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
+    ms = timeit(lambda: U.ufp4_quantize(xl, U.UFP4_E1M2, rht=True, out=ql, ws=ws), 10)
+    L["single_with_amax_pass"] = round(xl.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
+    ms = timeit(lambda: U.ufp4_quantize_dual(xl, U.UFP4_E1M2, rht=True, amax_row=aml, amax_col=aml, out_row=ql,
+                                             out_col=qlc, ws=ws), 10)
+    L["dual_amax_given"] = round(2 * xl.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
+    L["dual_amax_given_dram_gbs"] = round(xl.numel() * (2 + 2 * 0.5625) / (ms * 1e-3) / 1e9, 1)
+    ms = timeit(lambda: U.ufp4_quantize_dual(xl, U.UFP4_E1M2, rht=True, out_row=ql, out_col=qlc, ws=ws), 10)
+    L["dual_with_amax_pass"] = round(2 * xl.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
+    L["frac_hbm_single_amax_given"] = round(L["single_amax_given"] / pk["hbm_gbs"], 4)
+    out["quantize_large_32768x8192_e1m2_rht_gbs"] = L
+    del xl, ql, qlc
 
     xo = inputs.device_normal((4096, 4096), 1.0, 12, dev)
     qo = U.QTensor.empty(4096, 4096, U.UFP4_E2M1, dev)

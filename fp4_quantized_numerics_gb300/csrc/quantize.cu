@@ -2029,12 +2029,17 @@ cudaError_t quantize_dual_typed(const QuantLaunch &qr, const QuantLaunch &qc, Ar
         const uint32_t ntiles = (uint32_t)((ar.rows + kTileRows - 1) / kTileRows) * nct;
         ac.status = nullptr;   // the row-wise prologue reports both
         if (!qr.amax_in || !qc.amax_in) {
+            // the amax pass streams with little arithmetic: 16-row x 1 KB
+            // chunks (contiguous kilobyte rows) read faster than 128-byte
+            // tile rows, and the maxima do not depend on the traversal
+            constexpr uint32_t CW = kChunk / 32;
+            const uint32_t ncc = (uint32_t)((ar.cols + CW - 1) / CW), nch = (uint32_t)(ar.rows / 16) * ncc;
             ar.partials_out = reinterpret_cast<float *>(static_cast<char *>(ws) + kWsPartials);
             ac.partials_out = ar.partials_out + kMaxPartials / 2;
-            auto kern = qr.rht ? k_dual_tile<0, 0, true, true> : k_dual_tile<0, 0, false, true>;
-            if (resident_grid(kern, ntiles, tile_smem<true>()) > kMaxPartials / 2) return cudaErrorInvalidValue;
+            auto kern = qr.rht ? k_dual_staged<In, 0, 0, true, true> : k_dual_staged<In, 0, 0, false, true>;
+            if (resident_grid(kern, nch, ring_smem<true>()) > kMaxPartials / 2) return cudaErrorInvalidValue;
             int g = 1;
-            cudaError_t e = launch_staged_smem(kern, tile_smem<true>(), ntiles, &g, s, tm, ar, ac, nct, ntiles);
+            cudaError_t e = launch_staged<true>(kern, nch, &g, s, ar, ac, ncc, nch);
             if (e != cudaSuccess) return e;
             ar.partials = ar.partials_out;
             ac.partials = ac.partials_out;
