@@ -418,6 +418,9 @@ def side_measurements(U, torch, dev, pk, flush):
     L = {}
     ms = timeit(lambda: U.ufp4_quantize(xl, U.UFP4_E1M2, rht=True, out=ql, ws=ws, amax_in=aml), 10)
     L["single_amax_given"] = round(xl.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
+    ms = timeit(lambda: U.ufp4_quantize(xl, U.UFP4_E1M2, rht=False, out=ql, ws=ws, amax_in=aml), 10)
+    L["single_amax_given_rht_off"] = round(xl.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
+    L["rht_overhead_amax_given"] = round(L["single_amax_given_rht_off"] / L["single_amax_given"] - 1, 4)
     ms = timeit(lambda: U.ufp4_quantize(xl, U.UFP4_E1M2, rht=True, out=ql, ws=ws), 10)
     L["single_with_amax_pass"] = round(xl.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
     ms = timeit(lambda: U.ufp4_quantize_dual(xl, U.UFP4_E1M2, rht=True, amax_row=aml, amax_col=aml, out_row=ql,
