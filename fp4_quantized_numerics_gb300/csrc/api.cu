@@ -25,6 +25,13 @@ inline ufp4_status from_cuda(cudaError_t e) {
     return e == cudaSuccess ? UFP4_OK : (e == cudaErrorNotSupported ? UFP4_ERR_UNSUPPORTED : UFP4_ERR_CUDA);
 }
 
+// Within the 32-bit indexing of the kernels (UFP4_MAX_DIM, UFP4_MAX_BLOCKS).
+bool within_limits(int64_t rows, int64_t k) {
+    if (rows > UFP4_MAX_DIM || k > UFP4_MAX_DIM) return false;
+    if (rows <= 0 || k <= 0) return true;
+    return rows <= UFP4_MAX_BLOCKS / (kpad_of(k) / 16);
+}
+
 bool valid_qtensor(const ufp4_qtensor *q) {
     if (!q || q->reserved != 0) return false;
     if (q->rows < 0 || q->k < 0 || q->k % UFP4_BLOCK != 0) return false;
@@ -47,6 +54,8 @@ ufp4_status check_quant_args(const void *x, int32_t dtype, int64_t rows, int64_t
     if (rows < 0 || cols < 0 || ld < cols) return UFP4_ERR_INVALID;
     const int64_t out_rows = p->colwise ? cols : rows;
     const int64_t k = p->colwise ? rows : cols;
+    if (!within_limits(out_rows, k) || !within_limits(rows, cols) || ld > UFP4_MAX_DIM)
+        return UFP4_ERR_UNSUPPORTED;
     if (!valid_qtensor(out) || out->grid != p->grid || out->rows != out_rows || out->k != k)
         return UFP4_ERR_INVALID;
     if (k % UFP4_BLOCK != 0) return UFP4_ERR_INVALID;
@@ -150,6 +159,7 @@ ufp4_status ufp4_dequantize(const ufp4_qtensor *q, int32_t inverse_rht, uint64_t
                             float *out, int64_t ld_out, ufp4_stream_t stream) {
     if (!valid_qtensor(q) || (inverse_rht != 0 && inverse_rht != 1)) return UFP4_ERR_INVALID;
     if (q->rows == 0 || q->k == 0) return UFP4_OK;
+    if (!within_limits(q->rows, q->k)) return UFP4_ERR_UNSUPPORTED;
     if (!out || !aligned(out, 16) || ld_out < q->k || ld_out % 4 != 0) return UFP4_ERR_INVALID;
     return from_cuda(launch_dequantize(q->codes, q->scales, q->tensor_scale, q->rows, q->k,
                                        q->grid, inverse_rht, rht_seed, out, ld_out,
@@ -164,8 +174,7 @@ ufp4_status ufp4_gemm(const ufp4_qtensor *a, const ufp4_qtensor *b, float *c, in
     const int64_t M = a->rows, N = b->rows, K = a->k;
     if (M == 0 || N == 0) return UFP4_OK;
     if (!c || !aligned(c, 16) || ldc < N || ldc % 4 != 0) return UFP4_ERR_INVALID;
-    if (M > (int64_t)INT32_MAX || N > (int64_t)INT32_MAX || K > (int64_t)INT32_MAX)
-        return UFP4_ERR_INVALID;
+    if (!within_limits(M, K) || !within_limits(N, K)) return UFP4_ERR_UNSUPPORTED;
     return from_cuda(launch_gemm(a->codes, a->scales, a->tensor_scale, b->codes, b->scales,
                                  b->tensor_scale, M, N, K, a->grid, c, ldc,
                                  reinterpret_cast<cudaStream_t>(stream)));
@@ -209,6 +218,8 @@ ufp4_status ufp4_quantize_grouped(const void *x, int32_t dtype, int64_t cols, in
     if ((p->rht != 0 && p->rht != 1) || (p->colwise != 0 && p->colwise != 1) || p->reserved != 0)
         return UFP4_ERR_INVALID;
     if (cols < 0 || ld < cols) return UFP4_ERR_INVALID;
+    if (!within_limits(out_rows, k) || !within_limits(total, cols) || ld > UFP4_MAX_DIM)
+        return UFP4_ERR_UNSUPPORTED;
     if (!p->colwise && cols % UFP4_BLOCK != 0) return UFP4_ERR_INVALID;
     if (p->colwise && cols % 4 != 0) return UFP4_ERR_INVALID;
     const size_t esz = dtype == UFP4_BF16 ? 2 : 4;
@@ -256,6 +267,7 @@ ufp4_status ufp4_gemm_grouped(const ufp4_qtensor *a, const ufp4_qtensor *b, cons
     for (int i = 0; i < n; ++i) {
         const ufp4_gemm_group &g = groups[i];
         if (g.M < 0 || g.N < 0 || g.K < 0 || g.K % UFP4_BLOCK != 0) return UFP4_ERR_INVALID;
+        if (!within_limits(g.M, g.K) || !within_limits(g.N, g.K)) return UFP4_ERR_UNSUPPORTED;
         if (g.M == 0 || g.N == 0) continue;
         if (!g.c || !aligned(g.c, 16) || g.ldc < g.N || g.ldc % 4 != 0) return UFP4_ERR_INVALID;
         if (g.a_row % 128 || g.b_row % 128 || g.a_k % 64 || g.b_k % 64) return UFP4_ERR_INVALID;

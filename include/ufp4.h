@@ -82,6 +82,15 @@ typedef enum { UFP4_BF16 = 0, UFP4_FP32 = 1 } ufp4_dtype;
 
 #define UFP4_BLOCK 16
 
+/* Size limits of this build (32-bit block and tile indexing inside the
+ * kernels).  A request beyond them returns UFP4_ERR_UNSUPPORTED before any
+ * launch:
+ *   quantize / stats / dequantize: rows, cols (k) < 2^31 and the quantized
+ *   tensor's blocks, rows x kpad(k)/16, < 2^31 (about 3.4e10 elements);
+ *   GEMM: M, N < 2^31 and every operand within the quantize limit. */
+#define UFP4_MAX_DIM 2147483647LL
+#define UFP4_MAX_BLOCKS 2147483647LL
+
 /* Quantization parameters.
  *   grid, round  : see above.
  *   block        : must be 16.

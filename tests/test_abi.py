@@ -144,3 +144,34 @@ def test_binding_refuses_cpu_tensors():
     from fp4_quantized_numerics_gb300 import ufp4
     with pytest.raises(TypeError):
         ufp4.ufp4_quantize(torch.zeros(16, 16, dtype=torch.bfloat16), 0)
+
+
+def test_sizes_beyond_the_index_limits_are_refused_on_host(L):
+    """Tensors past the kernels' 32-bit block indexing (UFP4_MAX_DIM,
+    UFP4_MAX_BLOCKS in include/ufp4.h) return UFP4_ERR_UNSUPPORTED before
+    any launch; the pointers are never touched."""
+    from fp4_quantized_numerics_gb300 import ufp4
+    UNS = ufp4.UFP4_ERR_UNSUPPORTED
+    ws, x, wsb = 0x10000, 0x20000, L.ufp4_workspace_bytes()
+    # 2^20 rows x 2^16 cols: 2^32 blocks of 16
+    rows, cols = 1 << 20, 1 << 16
+    p = _q()
+    assert L.ufp4_quantize(x, 0, rows, cols, cols, ctypes.byref(p), ctypes.byref(_qt(rows, cols)), ws, wsb,
+                           None) == UNS
+    pc = _q(colwise=True)
+    assert L.ufp4_quantize(x, 0, rows, cols, cols, ctypes.byref(pc), ctypes.byref(_qt(cols, rows)), ws, wsb,
+                           None) == UNS
+    # one dimension past 2^31
+    big = 1 << 31
+    assert L.ufp4_quantize(x, 0, 16, big, big, ctypes.byref(p), ctypes.byref(_qt(16, big)), ws, wsb,
+                           None) == UNS
+    q = _qt(rows, cols)
+    assert L.ufp4_dequantize(ctypes.byref(q), 0, 0, 0x4000, cols, None) == UNS
+    a, b = _qt(rows, cols), _qt(128, cols)
+    assert L.ufp4_gemm(ctypes.byref(a), ctypes.byref(b), 0x4000, 128, None) == UNS
+    # just inside the limit still passes validation (it then fails on the fake
+    # pointers only if it reached the GPU, which a CPU test must not do: use a
+    # too-small workspace to stop it one check later)
+    rows_ok = (1 << 31) // (kpad(cols) // 16) - 1
+    assert L.ufp4_quantize(x, 0, rows_ok, cols, cols, ctypes.byref(p), ctypes.byref(_qt(rows_ok, cols)), ws, 16,
+                           None) == ufp4.UFP4_ERR_INVALID
