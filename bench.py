@@ -329,7 +329,7 @@ def run_gpu(args):
                      "ms_each": [round(v, 4) for v in gemm_each],
                      "frac_fp8_peak": round(per_gpu_tflops / fp8_peak, 4),
                      "frac_fp4_peak": round(per_gpu_tflops / fp4_peak, 4)},
-            "roofline": {"bound": "tensor", "kernel": "k_gemm<E1M2>",
+            "roofline": {"bound": "tensor", "kernel": "k_gemm<E1M2, E planes loaded>",
                          "achieved": round(per_gpu_tflops, 1), "peak": round(fp8_peak, 1),
                          "unit": "TFLOP/s", "frac": round(per_gpu_tflops / fp8_peak, 4),
                          "traffic": traffic_for("k_gemm_e1m2_dense1p5b"),
@@ -428,7 +428,8 @@ def side_measurements(U, torch, dev, pk, flush):
 
     out = {}
     x = inputs.device_normal((8192, 2048), 1.0, 11, dev)
-    q = U.QTensor.empty(8192, 2048, U.UFP4_E1M2, dev)
+    # the quantizer alone (codes and scales, no E1M2 correction plane)
+    q = U.QTensor.empty(8192, 2048, U.UFP4_E1M2, dev, eplane=False)
     amax = torch.ones(1, device=dev)
     ws = U.workspace(dev)
     el = x.numel()
@@ -444,8 +445,8 @@ def side_measurements(U, torch, dev, pk, flush):
     # steady state on a large operand (512 MB of BF16): one orientation and
     # both, transform on, E1M2 RTNE
     xl = inputs.device_normal((32768, 8192), 1.0, 15, dev)
-    ql = U.QTensor.empty(32768, 8192, U.UFP4_E1M2, dev)
-    qlc = U.QTensor.empty(8192, 32768, U.UFP4_E1M2, dev)
+    ql = U.QTensor.empty(32768, 8192, U.UFP4_E1M2, dev, eplane=False)
+    qlc = U.QTensor.empty(8192, 32768, U.UFP4_E1M2, dev, eplane=False)
     aml = torch.tensor([float(xl.float().abs().max()) * 1.25], device=dev)
     L = {}
     ms = timeit(lambda: U.ufp4_quantize(xl, U.UFP4_E1M2, rht=True, out=ql, ws=ws, amax_in=aml), 10)
@@ -462,12 +463,17 @@ def side_measurements(U, torch, dev, pk, flush):
     ms = timeit(lambda: U.ufp4_quantize_dual(xl, U.UFP4_E1M2, rht=True, out_row=ql, out_col=qlc, ws=ws), 10)
     L["dual_with_amax_pass"] = round(2 * xl.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
     L["frac_hbm_single_amax_given"] = round(L["single_amax_given"] / pk["hbm_gbs"], 4)
+    # the same with the correction plane written too (+0.5 B/elem, not counted)
+    qle = U.QTensor.empty(32768, 8192, U.UFP4_E1M2, dev)
+    ms = timeit(lambda: U.ufp4_quantize(xl, U.UFP4_E1M2, rht=True, out=qle, ws=ws, amax_in=aml), 10)
+    L["single_amax_given_with_eplane"] = round(xl.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
+    del qle
     out["quantize_large_32768x8192_e1m2_rht_gbs"] = L
     del xl, ql, qlc
 
     xo = inputs.device_normal((4096, 4096), 1.0, 12, dev)
     qo = U.QTensor.empty(4096, 4096, U.UFP4_E2M1, dev)
-    qo1 = U.QTensor.empty(4096, 4096, U.UFP4_E1M2, dev)
+    qo1 = U.QTensor.empty(4096, 4096, U.UFP4_E1M2, dev, eplane=False)
     o = {}
     for g, qq in ((U.UFP4_E2M1, qo), (U.UFP4_E1M2, qo1)):
         ms = timeit(lambda: U.ufp4_quantize(xo, g, rht=True, out=qq, ws=ws))
@@ -482,6 +488,16 @@ def side_measurements(U, torch, dev, pk, flush):
     tf = 2 * 8192 * 5632 * 2048 / (ms * 1e-3) / 1e12
     out["gemm_e2m1_fwd_y"] = {"tflops": round(tf, 1), "frac_fp4_peak": round(tf / (pk["bf16_tflops"] * 6), 4),
                               "output_bytes_bound_tflops": round(2 * 2048 / 4 * pk["hbm_gbs"] / 1e3, 1)}
+    # E1M2 at the fwd_y shape: correction planes loaded vs expanded on chip
+    a = U.ufp4_quantize(inputs.device_normal((8192, 2048), 1.0, 13, dev), U.UFP4_E1M2, rht=True)
+    b = U.ufp4_quantize(inputs.device_normal((5632, 2048), 0.02, 14, dev), U.UFP4_E1M2, rht=True)
+    e = {}
+    for name, (qa, qb) in (("eplanes_loaded", (a, b)),
+                           ("expanded_on_chip", tuple(U.QTensor(t.codes, t.scales, t.tensor_scale, t.rows, t.k,
+                                                                t.grid) for t in (a, b)))):
+        ms = timeit(lambda: U.ufp4_gemm(qa, qb, out=c))
+        e[name] = round(2 * 8192 * 5632 * 2048 / (ms * 1e-3) / 1e12, 1)
+    out["gemm_e1m2_fwd_y_tflops"] = e
     return out
 
 

@@ -38,6 +38,7 @@ bool valid_qtensor(const ufp4_qtensor *q) {
     if (q->grid != UFP4_E2M1 && q->grid != UFP4_E1M2 && q->grid != UFP4_E2M1C) return false;
     if (q->rows == 0 || q->k == 0) return true;
     if (!q->codes || !q->scales || !q->tensor_scale) return false;
+    if (q->eplane && (q->grid != UFP4_E1M2 || !aligned(q->eplane, 16))) return false;
     return aligned(q->codes, 16) && aligned(q->scales, 16) && aligned(q->tensor_scale, 4);
 }
 
@@ -71,6 +72,7 @@ ufp4_status check_quant_args(const void *x, int32_t dtype, int64_t rows, int64_t
     q.rht_seed = p->rht_seed; q.sr_seed = p->sr_seed; q.sr_counter = p->sr_counter;
     q.amax_in = p->amax_in;
     q.codes = out->codes; q.scales = out->scales; q.tensor_scale = out->tensor_scale;
+    q.eplane = out->eplane;
     q.out_rows = out_rows; q.k = k; q.elem_base = 0;
     *ql = q;
     return UFP4_OK;
@@ -175,7 +177,7 @@ ufp4_status ufp4_gemm(const ufp4_qtensor *a, const ufp4_qtensor *b, float *c, in
     if (M == 0 || N == 0) return UFP4_OK;
     if (!c || !aligned(c, 16) || ldc < N || ldc % 4 != 0) return UFP4_ERR_INVALID;
     if (!within_limits(M, K) || !within_limits(N, K)) return UFP4_ERR_UNSUPPORTED;
-    return from_cuda(launch_gemm(a->codes, a->scales, a->tensor_scale, b->codes, b->scales,
+    return from_cuda(launch_gemm(a->codes, a->eplane, a->scales, a->tensor_scale, b->codes, b->eplane, b->scales,
                                  b->tensor_scale, M, N, K, a->grid, c, ldc,
                                  reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -251,6 +253,7 @@ ufp4_status ufp4_quantize_grouped(const void *x, int32_t dtype, int64_t cols, in
     q.grid = p->grid; q.rht = p->rht; q.round = p->round; q.colwise = p->colwise;
     q.rht_seed = p->rht_seed; q.sr_seed = p->sr_seed; q.sr_counter = p->sr_counter;
     q.codes = out->codes; q.scales = out->scales; q.tensor_scale = out->tensor_scale;
+    q.eplane = out->eplane;
     q.out_rows = out_rows; q.k = k;
     return from_cuda(launch_quantize_grouped(q, gt, workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -295,8 +298,9 @@ ufp4_status ufp4_gemm_grouped(const ufp4_qtensor *a, const ufp4_qtensor *b, cons
     }
     tab->n = m;
     if (m == 0) return UFP4_OK;
-    return from_cuda(launch_gemm_grouped(a->codes, a->scales, a->tensor_scale, a->rows, kpad_of(a->k), b->codes,
-                                         b->scales, b->tensor_scale, b->rows, kpad_of(b->k), a->grid, *tab, s));
+    return from_cuda(launch_gemm_grouped(a->codes, a->eplane, a->scales, a->tensor_scale, a->rows, kpad_of(a->k),
+                                         b->codes, b->eplane, b->scales, b->tensor_scale, b->rows, kpad_of(b->k),
+                                         a->grid, *tab, s));
 }
 
 ufp4_status ufp4_stats(const void *x, int32_t dtype, int64_t rows, int64_t cols, int64_t ld,

@@ -147,6 +147,20 @@ __device__ __forceinline__ float grid_value(int grid, uint32_t m) {
     return m == 7u ? 6.0f : (float)(m - 2u);
 }
 
+// E1M2 as two E2M1 planes: the value m/2 of an E1M2 code equals (R + E)/2,
+// R the code's nibble read as an E2M1 code ({0,.5,1,1.5,2,3,4,6}[m]) and E
+// the correction plane {0,.5,1,1.5,2,2,2,1}[m] as E2M1 codes, sign kept.
+// E plane of 8 packed nibbles s|b2 b1 b0 (m = 4 b2 + 2 b1 + b0): E2M1 code m
+// for m < 4, 4 (value 2) for m in {4,5,6}, 2 (value 1) for m = 7.  Per
+// nibble the E code is the input masked by: bit 0 kept iff !b2, bit 1 iff
+// (!b2 | b0), bit 2 iff !(b0 & b1), bit 3 (sign) always -- the shifted
+// copies line the other bits up with each position.
+__device__ __forceinline__ uint32_t e1m2_eplane(uint32_t w) {
+    const uint32_t u = w >> 1, v = w << 1, t = w >> 2, x = w << 2;
+    const uint32_t keep = (~t & 0x11111111u) | ((~u | v) & 0x22222222u) | (~(x & v) & 0x44444444u) | 0x88888888u;
+    return w & keep;
+}
+
 // ---------------------------------------------------------- in-register FWHT
 // Unnormalised 8-point Walsh-Hadamard butterflies (Sylvester order):
 // v_i <- sum_j (-1)^popcount(i&j) v_j.

@@ -53,7 +53,12 @@ constexpr uint32_t kSfCol = 256;                   // accumulator in [0, 256), s
 constexpr int kEpiWarps = 8;
 constexpr long long kWaitBudget = 2000000000LL;
 
-// Per-grid pipeline geometry.
+// Kernel variants (the template argument GRID): kE2M1 (also clamped E2M1,
+// whose codes are E2M1 codes), kE1M2 (E planes expanded on chip) and kE1M2Pl
+// (E1M2 whose E planes the quantizer wrote next to the codes).
+constexpr int kE1M2Pl = 3;
+
+// Per-variant pipeline geometry.
 //  E2M1: K stage of 128 bytes (4 MMA K steps, 128-byte swizzle) so that the
 //        issuing thread's per-stage wait/commit latency stays below the
 //        stage's tensor-core time; 3 stages.
@@ -61,8 +66,13 @@ constexpr long long kWaitBudget = 2000000000LL;
 //        ring of raw tiles fed by TMA and a 3-slot ring of E planes written
 //        by six expander warps (16 warps in all: the 128 registers a thread
 //        then gets still hold the epilogue's accumulator chunks).
+//  E1M2Pl: the same 8 MMAs per 64-byte stage, all four tiles (R_A, R_B,
+//        E_A, E_B) loaded by TMA into a 3-deep ring; scale copies from their
+//        own warp as for E2M1.
 template <int GRID>
 struct Cfg {
+    static constexpr bool kFour = GRID != kE2M1;                     // E1M2: 4 MMAs per K step
+    static constexpr bool kPl = GRID == kE1M2Pl;                     // E planes loaded by TMA
     static constexpr int kBK = GRID == kE2M1 ? 128 : 64;            // bytes of K per stage
     static constexpr int kKS = kBK / 32;                             // MMA K steps per stage
     static constexpr uint32_t kSwz = GRID == kE2M1 ? 2 : 4;          // descriptor swizzle: 128B / 64B
@@ -72,17 +82,20 @@ struct Cfg {
     static constexpr uint32_t kSfbBytes = 2 * kKS * 512;             // two 128-row halves
     static constexpr uint32_t kSfColsPerStage = 12 * kKS;            // SFA 4 + SFB 8 columns per K step
     static constexpr int kStages = 3;
-    static constexpr int kESlots = GRID == kE2M1 ? 0 : 3;
-    static constexpr int kExpWarps = GRID == kE2M1 ? 0 : 6;
-    // E2M1: one extra warp issues the block-scale copies
-    static constexpr int kScaleWarps = GRID == kE2M1 ? 1 : 0;
+    static constexpr int kESlots = GRID == kE1M2 ? 3 : 0;
+    static constexpr int kExpWarps = GRID == kE1M2 ? 6 : 0;
+    // E2M1 and E1M2Pl: one extra warp issues the block-scale copies
+    static constexpr int kScaleWarps = GRID == kE1M2 ? 0 : 1;
     static constexpr int kThreads = 32 * (2 + kEpiWarps + kScaleWarps + kExpWarps);
     // epilogue staging buffers (32 x 32 fp32, 4 KB) per epilogue warp
-    static constexpr int kEpiBufs = GRID == kE2M1 ? 1 : 2;
-    // stage layout: A | B | SFA | SFB;  E slots: E_A | E_B
+    static constexpr int kEpiBufs = GRID == kE1M2 ? 2 : 1;
+    // stage layout: A | B | (E1M2Pl: E_A | E_B) | SFA | SFB;  E slots: E_A | E_B
+    static constexpr uint32_t kPlaneBytes = kPl ? kABytes + kBBytes : 0;
     static constexpr uint32_t kAOff = 0;
     static constexpr uint32_t kBOff = kABytes;
-    static constexpr uint32_t kSfaOff = kABytes + kBBytes;
+    static constexpr uint32_t kEAOff = kABytes + kBBytes;
+    static constexpr uint32_t kEBOff = kEAOff + kABytes;
+    static constexpr uint32_t kSfaOff = kABytes + kBBytes + kPlaneBytes;
     static constexpr uint32_t kSfbOff = kSfaOff + kSfaBytes;
     static constexpr uint32_t kStageBytes = kSfbOff + kSfbBytes;     // multiple of 1024
     static constexpr uint32_t kESlotBytes = kABytes + kBBytes;
@@ -186,22 +199,12 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     }
 }
 
-// E plane of 8 E1M2 nibbles s|b2 b1 b0 (m = 4 b2 + 2 b1 + b0): E2M1 code m
-// for m < 4, 4 (value 2) for m in {4,5,6}, 2 (value 1) for m = 7; sign kept.
-// Per nibble the E code is the input masked by: bit 0 kept iff !b2, bit 1
-// iff (!b2 | b0), bit 2 iff !(b0 & b1), bit 3 (sign) always -- the shifted
-// copies line the other bits up with each position.
-__device__ __forceinline__ uint32_t e1m2_eplane(uint32_t w) {
-    const uint32_t u = w >> 1, v = w << 1, t = w >> 2, x = w << 2;
-    const uint32_t keep = (~t & 0x11111111u) | ((~u | v) & 0x22222222u) | (~(x & v) & 0x44444444u) | 0x88888888u;
-    return w & keep;
-}
-
 // Persistent CTA: tiles t = blockIdx.x, blockIdx.x + gridDim.x, ... in
 // row-major (M, N) tile order; the K ring is carried across tiles.
 template <int GRID, class TAB>
 __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+           const __grid_constant__ CUtensorMap tma_ea, const __grid_constant__ CUtensorMap tma_eb,
            const __grid_constant__ CUtensorMap tma_c, GemmParams p, const __grid_constant__ TAB tab) {
     constexpr bool kGrouped = std::is_same<TAB, GroupGemmTab>::value;
     using C = Cfg<GRID>;
@@ -250,6 +253,10 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tma_a);
         ptx::prefetch_tmap(&tma_b);
+        if (C::kPl) {
+            ptx::prefetch_tmap(&tma_ea);
+            ptx::prefetch_tmap(&tma_eb);
+        }
         ptx::prefetch_tmap(&tma_c);
     }
     if (warp == 1) {
@@ -304,9 +311,14 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                     if (round > 0 && !wait_or_abort(empty(s), (round - 1) & 1, abort)) { ok = false; break; }
                     const uint32_t atoms = (uint32_t)min(C::kKS, ti.nkt - C::kKS * kb);
                     const uint32_t st = smem_base + s * C::kStageBytes;
-                    ptx::mbar_arrive_expect_tx(full(s), C::kABytes + C::kBBytes + atoms * 512u * (b_hi ? 3u : 2u));
+                    ptx::mbar_arrive_expect_tx(full(s), C::kABytes + C::kBBytes + C::kPlaneBytes +
+                                                            atoms * 512u * (b_hi ? 3u : 2u));
                     ptx::tma_load_2d(st + C::kAOff, &tma_a, ti.a_kt * 32 + kb * C::kBK, ti.a_row, full(s));
                     ptx::tma_load_2d(st + C::kBOff, &tma_b, ti.b_kt * 32 + kb * C::kBK, ti.b_row, full(s));
+                    if (C::kPl) {
+                        ptx::tma_load_2d(st + C::kEAOff, &tma_ea, ti.a_kt * 32 + kb * C::kBK, ti.a_row, full(s));
+                        ptx::tma_load_2d(st + C::kEBOff, &tma_eb, ti.b_kt * 32 + kb * C::kBK, ti.b_row, full(s));
+                    }
                     ptx::bulk_load(st + C::kSfaOff,
                                    p.sfa + ((size_t)(ti.a_row / 128) * p.nkt_a + ti.a_kt + C::kKS * kb) * 512,
                                    atoms * 512u, full(s));
@@ -346,35 +358,47 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                 for (int kb = 0; kb < ti.num_kb; ++kb, ++g) {
                     const uint32_t s = g % S, round = g / S;
                     const uint32_t e = g % ES, eround = g / ES;
-                    // operands landed (E1M2: E planes written) and scales in TMEM
-                    if (!wait_or_abort(GRID == kE2M1 ? full(s) : expd(e), (GRID == kE2M1 ? round : eround) & 1,
-                                       abort) ||
-                        (GRID == kE2M1 && !wait_or_abort(sfr(s), round & 1, abort))) { ok = false; break; }
+                    // operands landed and (scale warp) scales in TMEM
+                    if (!wait_or_abort(full(s), round & 1, abort) ||
+                        (C::kScaleWarps > 0 && !wait_or_abort(sfr(s), round & 1, abort))) { ok = false; break; }
                     ptx::tc_fence_after();
                     const int atoms = min(C::kKS, ti.nkt - C::kKS * kb);
-                    if (GRID == kE1M2) copy_scales(s, atoms, false);
+                    if constexpr (GRID == kE1M2) {
+                        // scale copies queued while the expanders finish the E planes
+                        copy_scales(s, atoms, false);
+                        if (!wait_or_abort(expd(e), eround & 1, abort)) { ok = false; break; }
+                        ptx::tc_fence_after();
+                    }
                     const uint32_t st = smem_base + s * C::kStageBytes;
                     const uint32_t es = smem_base + C::kEOff + e * C::kESlotBytes;
                     const uint32_t sf_t = tmem + kSfCol + C::kSfColsPerStage * s;
                     const uint64_t da = mk(hi_op, st + C::kAOff), db = mk(hi_op, st + C::kBOff);
-                    const uint64_t dea = mk(hi_op, es), deb = mk(hi_op, es + C::kABytes);
+                    const uint64_t dea = mk(hi_op, C::kPl ? st + C::kEAOff : es);
+                    const uint64_t deb = mk(hi_op, C::kPl ? st + C::kEBOff : es + C::kABytes);
                     const uint32_t sfa0 = sf_t, sfb0 = sf_t + 4u * C::kKS;
-                    auto step = [&](int j) {
-                        const uint32_t sfa = sfa0 + 4u * j, sfb = sfb0 + 8u * j;
-                        const uint32_t first = (kb == 0 && j == 0) ? 0u : 1u;
-                        const uint64_t o = 2u * (uint32_t)j;   // +32 bytes per 64-element K step
-                        ptx::tc_mma_nvf4(tmem, da + o, db + o, idesc, sfa, sfb, first);
-                        if (GRID == kE1M2) {
-                            ptx::tc_mma_nvf4(tmem, da + o, deb + o, idesc, sfa, sfb, 1u);
-                            ptx::tc_mma_nvf4(tmem, dea + o, db + o, idesc, sfa, sfb, 1u);
-                            ptx::tc_mma_nvf4(tmem, dea + o, deb + o, idesc, sfa, sfb, 1u);
-                        }
+                    // E1M2 per K step: R*R, R*E, E*R, E*E, each A plane read
+                    // from shared memory once and reused by the next MMA from
+                    // the tensor core's collector
+                    using ptx::CollA;
+                    auto mma = [&](auto u, uint64_t a, uint64_t b, int j, uint32_t acc) {
+                        ptx::tc_mma_nvf4<decltype(u)::value>(tmem, a + 2u * (uint32_t)j, b + 2u * (uint32_t)j, idesc,
+                                                             sfa0 + 4u * j, sfb0 + 8u * j, acc);
                     };
-                    if (atoms == C::kKS) {
+                    using None = std::integral_constant<CollA, CollA::kNone>;
+                    using Fill = std::integral_constant<CollA, CollA::kFill>;
+                    using Last = std::integral_constant<CollA, CollA::kLastUse>;
+                    auto first = [&](int j) { return (kb == 0 && j == 0) ? 0u : 1u; };
 #pragma unroll
-                        for (int j = 0; j < C::kKS; ++j) step(j);
-                    } else {
-                        for (int j = 0; j < atoms; ++j) step(j);
+                    for (int j = 0; j < C::kKS; ++j) {
+                        if (j >= atoms) break;
+                        if constexpr (C::kFour) {
+                            mma(Fill{}, da, db, j, first(j));
+                            mma(Last{}, da, deb, j, 1u);
+                            mma(Fill{}, dea, db, j, 1u);
+                            mma(Last{}, dea, deb, j, 1u);
+                        } else {
+                            mma(None{}, da, db, j, first(j));
+                        }
                     }
                     ptx::tc_commit(empty(s));
                     if (GRID == kE1M2) ptx::tc_commit(efree(e));
@@ -402,7 +426,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         const int h = ew >> 2;                   // column half of the tile
         const uint32_t buf0 = smem_base + C::kEpiOff + (uint32_t)ew * NB * 4096u;
         // E1M2 accumulates (R + E)(R + E) = 4 A B^T
-        const float kfix = GRID == kE1M2 ? 0.25f : 1.0f;
+        const float kfix = C::kFour ? 0.25f : 1.0f;
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
         uint32_t it = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
@@ -491,7 +515,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         }
         if (lane == 0) ptx::bulk_wait_all();
         __syncwarp();
-    } else if (GRID == kE2M1 && warp == 2 + kEpiWarps) {
+    } else if (C::kScaleWarps > 0 && warp == 2 + kEpiWarps) {
         // ------------------------------------------------- E2M1 scale copies
         if (lane == 0) {
             uint32_t g = 0;
@@ -594,8 +618,8 @@ bool make_out_map(CUtensorMap *m, float *c, int64_t M, int64_t N, int64_t ldc) {
 }
 
 template <int GRID, class TAB>
-cudaError_t run_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc, const GemmParams &p,
-                     const TAB &tab, int ntiles, cudaStream_t s) {
+cudaError_t run_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mea, const CUtensorMap &meb,
+                     const CUtensorMap &mc, const GemmParams &p, const TAB &tab, int ntiles, cudaStream_t s) {
     using C = Cfg<GRID>;
     static bool attr_set[64] = {false};
     int dev = 0;
@@ -609,21 +633,30 @@ cudaError_t run_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const CUtenso
     const int sms = num_sms();
     const int grid = ntiles < sms ? ntiles : sms;
     if (grid <= 0) return cudaSuccess;
-    k_gemm<GRID, TAB><<<grid, C::kThreads, C::kSmemBytes, s>>>(ma, mb, mc, p, tab);
+    k_gemm<GRID, TAB><<<grid, C::kThreads, C::kSmemBytes, s>>>(ma, mb, mea, meb, mc, p, tab);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_ts,
-                        const uint8_t *b_codes, const uint8_t *b_scales, const float *b_ts, int64_t M,
-                        int64_t N, int64_t K, int grid, float *c, int64_t ldc, cudaStream_t s) {
+cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_eplane, const uint8_t *a_scales,
+                        const float *a_ts, const uint8_t *b_codes, const uint8_t *b_eplane,
+                        const uint8_t *b_scales, const float *b_ts, int64_t M, int64_t N, int64_t K, int grid,
+                        float *c, int64_t ldc, cudaStream_t s) {
     if (K == 0) return cudaMemset2DAsync(c, ldc * sizeof(float), 0, N * sizeof(float), M, s);
     const int64_t kpad = kpad_of(K);
-    CUtensorMap ma, mb, mc;
+    const bool planes = grid == kE1M2 && a_eplane && b_eplane;
+    CUtensorMap ma, mb, mea, meb, mc;
     if (!make_code_map(&ma, a_codes, M, kpad, BM, grid) || !make_code_map(&mb, b_codes, N, kpad, BN, grid) ||
         !make_out_map(&mc, c, M, N, ldc))
         return cudaErrorInvalidValue;
+    if (planes) {
+        if (!make_code_map(&mea, a_eplane, M, kpad, BM, grid) || !make_code_map(&meb, b_eplane, N, kpad, BN, grid))
+            return cudaErrorInvalidValue;
+    } else {
+        mea = ma;   // unused
+        meb = mb;
+    }
     GemmParams p{};
     p.sfa = a_scales; p.sfb = b_scales; p.ts_a = a_ts; p.ts_b = b_ts;
     p.c = c; p.ldc = ldc; p.M = (int)M; p.N = (int)N;
@@ -636,18 +669,29 @@ cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const f
     p.b_rt = (int)((N + 127) / 128);
     const NoGroups none;
     // clamped-E2M1 codes are E2M1 codes
-    if (grid != kE1M2) return run_gemm<kE2M1>(ma, mb, mc, p, none, p.ntm * p.ntn, s);
-    return run_gemm<kE1M2>(ma, mb, mc, p, none, p.ntm * p.ntn, s);
+    if (grid != kE1M2) return run_gemm<kE2M1>(ma, mb, mea, meb, mc, p, none, p.ntm * p.ntn, s);
+    if (planes) return run_gemm<kE1M2Pl>(ma, mb, mea, meb, mc, p, none, p.ntm * p.ntn, s);
+    return run_gemm<kE1M2>(ma, mb, mea, meb, mc, p, none, p.ntm * p.ntn, s);
 }
 
-cudaError_t launch_gemm_grouped(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_ts,
-                                int64_t a_rows, int64_t a_kpad, const uint8_t *b_codes, const uint8_t *b_scales,
-                                const float *b_ts, int64_t b_rows, int64_t b_kpad, int grid,
-                                const GroupGemmTab &tab, cudaStream_t s) {
-    CUtensorMap ma, mb, mc;
+cudaError_t launch_gemm_grouped(const uint8_t *a_codes, const uint8_t *a_eplane, const uint8_t *a_scales,
+                                const float *a_ts, int64_t a_rows, int64_t a_kpad, const uint8_t *b_codes,
+                                const uint8_t *b_eplane, const uint8_t *b_scales, const float *b_ts,
+                                int64_t b_rows, int64_t b_kpad, int grid, const GroupGemmTab &tab,
+                                cudaStream_t s) {
+    const bool planes = grid == kE1M2 && a_eplane && b_eplane;
+    CUtensorMap ma, mb, mea, meb, mc;
     if (!make_code_map(&ma, a_codes, a_rows, a_kpad, BM, grid) ||
         !make_code_map(&mb, b_codes, b_rows, b_kpad, BN, grid))
         return cudaErrorInvalidValue;
+    if (planes) {
+        if (!make_code_map(&mea, a_eplane, a_rows, a_kpad, BM, grid) ||
+            !make_code_map(&meb, b_eplane, b_rows, b_kpad, BN, grid))
+            return cudaErrorInvalidValue;
+    } else {
+        mea = ma;   // unused
+        meb = mb;
+    }
     memset(&mc, 0, sizeof mc);   // grouped epilogues store directly
     GemmParams p{};
     p.sfa = a_scales; p.sfb = b_scales; p.ts_a = a_ts; p.ts_b = b_ts;
@@ -656,8 +700,9 @@ cudaError_t launch_gemm_grouped(const uint8_t *a_codes, const uint8_t *a_scales,
     p.b_rt = (int)((b_rows + 127) / 128);
     p.M = 1; p.N = 1;
     const int ntiles = tab.tiles[tab.n];
-    if (grid != kE1M2) return run_gemm<kE2M1>(ma, mb, mc, p, tab, ntiles, s);
-    return run_gemm<kE1M2>(ma, mb, mc, p, tab, ntiles, s);
+    if (grid != kE1M2) return run_gemm<kE2M1>(ma, mb, mea, meb, mc, p, tab, ntiles, s);
+    if (planes) return run_gemm<kE1M2Pl>(ma, mb, mea, meb, mc, p, tab, ntiles, s);
+    return run_gemm<kE1M2>(ma, mb, mea, meb, mc, p, tab, ntiles, s);
 }
 
 bool make_input_tile_map(void *tmap, const void *x, int64_t rows, int64_t cols, int64_t ld, int box_cols,

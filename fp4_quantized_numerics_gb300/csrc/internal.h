@@ -23,6 +23,7 @@ struct QuantLaunch {
     uint64_t rht_seed, sr_seed, sr_counter;
     const float *amax_in;      // device or null
     uint8_t *codes;
+    uint8_t *eplane;           // E1M2 correction plane (codes' layout) or null
     uint8_t *scales;
     float *tensor_scale;
     int64_t out_rows, k;       // result shape
@@ -86,15 +87,18 @@ cudaError_t launch_quantize_dual(const QuantLaunch &qr, const QuantLaunch &qc, v
 // maximum per segment and the status word.
 cudaError_t launch_quantize_grouped(const QuantLaunch &q, const GroupQuant &gt, void *ws, cudaStream_t s);
 
-cudaError_t launch_gemm_grouped(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_ts,
-                                int64_t a_rows, int64_t a_kpad, const uint8_t *b_codes, const uint8_t *b_scales,
-                                const float *b_ts, int64_t b_rows, int64_t b_kpad, int grid,
-                                const GroupGemmTab &tab, cudaStream_t s);
+cudaError_t launch_gemm_grouped(const uint8_t *a_codes, const uint8_t *a_eplane, const uint8_t *a_scales,
+                                const float *a_ts, int64_t a_rows, int64_t a_kpad, const uint8_t *b_codes,
+                                const uint8_t *b_eplane, const uint8_t *b_scales, const float *b_ts,
+                                int64_t b_rows, int64_t b_kpad, int grid, const GroupGemmTab &tab,
+                                cudaStream_t s);
 
-cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_ts,
-                        const uint8_t *b_codes, const uint8_t *b_scales, const float *b_ts,
-                        int64_t M, int64_t N, int64_t K, int grid, float *c, int64_t ldc,
-                        cudaStream_t s);
+// a_eplane / b_eplane: E1M2 correction planes (same layout as the codes) or
+// NULL; with both given the GEMM loads them instead of expanding on chip.
+cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_eplane, const uint8_t *a_scales,
+                        const float *a_ts, const uint8_t *b_codes, const uint8_t *b_eplane,
+                        const uint8_t *b_scales, const float *b_ts, int64_t M, int64_t N, int64_t K, int grid,
+                        float *c, int64_t ldc, cudaStream_t s);
 
 // Reads and clears the sticky flag that a bounded device-side wait raises
 // when it gives up (synchronises s).

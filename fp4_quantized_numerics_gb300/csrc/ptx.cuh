@@ -143,16 +143,26 @@ __device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t de
 
 // D[tmem] (+)= A[smem] * B[smem]^T with E2M1 elements and one UE4M3 scale per
 // 16 K-elements per row (scale_vec::4X), MMA-K = 64.
+// Use of the tensor core's A-operand collector: kFill reads A from shared
+// memory and keeps it; the next MMA of this thread with the same A takes it
+// from the collector with kLastUse (and releases it) instead of re-reading.
+enum class CollA { kNone, kFill, kLastUse };
+
+template <CollA U = CollA::kNone>
 __device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                             uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
                                             uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
-        " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
-        : "memory");
+#define UFP4_MMA_NVF4(Q)                                                                              \
+    asm volatile("{\n\t.reg .pred p;\n\t"                                                          \
+                 "setp.ne.b32 p, %4, 0;\n\t"                                                        \
+                 "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X" Q               \
+                 " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),                             \
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem) \
+                 : "memory")
+    if constexpr (U == CollA::kFill) UFP4_MMA_NVF4(".collector::a::fill");
+    else if constexpr (U == CollA::kLastUse) UFP4_MMA_NVF4(".collector::a::lastuse");
+    else UFP4_MMA_NVF4("");
+#undef UFP4_MMA_NVF4
 }
 
 // Arrive on an mbarrier once every previously issued tcgen05 op of this

@@ -58,6 +58,7 @@ struct Args {
     int n_partials;
     uint32_t *status;
     uint8_t *codes, *scales;
+    uint8_t *eplane;            // E1M2 correction plane beside the codes, or null
     float *tensor_scale;
     double *stats_out;
     // uniform grids (E1M2 kernels): qmax and the largest magnitude index,
@@ -566,10 +567,23 @@ __device__ __forceinline__ uint2 round_block(float ql[8], float qh[8], uint32_t 
     return make_uint2(codes8<GRID, ROUND>(ql, a, i0), codes8<GRID, ROUND>(qh, a, i0 + 8));
 }
 
+// Packed codes at byte offset `off` of the code buffer, and their E1M2
+// correction plane at the same offset of the plane when the tensor has one.
+__device__ __forceinline__ void put_codes(const Args &a, size_t off, uint2 w) {
+    *reinterpret_cast<uint2 *>(a.codes + off) = w;
+    if (a.eplane) *reinterpret_cast<uint2 *>(a.eplane + off) = make_uint2(e1m2_eplane(w.x), e1m2_eplane(w.y));
+}
+__device__ __forceinline__ void put_codes(const Args &a, size_t off, uint4 w) {
+    *reinterpret_cast<uint4 *>(a.codes + off) = w;
+    if (a.eplane)
+        *reinterpret_cast<uint4 *>(a.eplane + off) =
+            make_uint4(e1m2_eplane(w.x), e1m2_eplane(w.y), e1m2_eplane(w.z), e1m2_eplane(w.w));
+}
+
 __device__ __forceinline__ void store_block(const Args &a, uint32_t r, uint32_t b, uint2 w, uint32_t e,
                                             uint32_t cstride, uint32_t nkt) {
     if (e == 0) w = make_uint2(0u, 0u);
-    *reinterpret_cast<uint2 *>(a.codes + (size_t)r * cstride + b * 8) = w;
+    put_codes(a, (size_t)r * cstride + b * 8, w);
     a.scales[scale_offset32(r, b, nkt)] = (uint8_t)e;
 }
 
@@ -1068,7 +1082,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_row_staged(Args a,
         const uint32_t npad = (uint32_t)a.out_rows * nbp;
         for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < npad; t += gridDim.x * blockDim.x) {
             const uint32_t r = t / nbp, b = kvb + (t - r * nbp);
-            *reinterpret_cast<uint2 *>(a.codes + (size_t)r * cstride + b * 8) = make_uint2(0u, 0u);
+            put_codes(a, (size_t)r * cstride + b * 8, make_uint2(0u, 0u));
             a.scales[scale_offset32(r, b, nkt)] = 0;
         }
         zero_pad_rows(a);
@@ -1162,7 +1176,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_col_staged(Args a,
         const uint32_t npad = (uint32_t)a.out_rows * nbp;
         for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < npad; t += gridDim.x * blockDim.x) {
             const uint32_t r = t / nbp, b = kvb + (t - r * nbp);
-            *reinterpret_cast<uint2 *>(a.codes + (size_t)r * cstride + b * 8) = make_uint2(0u, 0u);
+            put_codes(a, (size_t)r * cstride + b * 8, make_uint2(0u, 0u));
             a.scales[scale_offset32(r, b, nkt)] = 0;
         }
         zero_pad_rows(a);
@@ -1314,7 +1328,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_dual_staged(Args a
         const uint32_t npr = (uint32_t)ar.out_rows * nbr;
         for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < npr; t += gridDim.x * blockDim.x) {
             const uint32_t r = t / nbr, b = kvr + (t - r * nbr);
-            *reinterpret_cast<uint2 *>(ar.codes + (size_t)r * csr + b * 8) = make_uint2(0u, 0u);
+            put_codes(ar, (size_t)r * csr + b * 8, make_uint2(0u, 0u));
             ar.scales[scale_offset32(r, b, nktr)] = 0;
         }
         zero_pad_rows(ar);
@@ -1323,7 +1337,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_dual_staged(Args a
         const uint32_t npc = (uint32_t)ac.out_rows * nbc;
         for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < npc; t += gridDim.x * blockDim.x) {
             const uint32_t r = t / nbc, b = kvc + (t - r * nbc);
-            *reinterpret_cast<uint2 *>(ac.codes + (size_t)r * csc + b * 8) = make_uint2(0u, 0u);
+            put_codes(ac, (size_t)r * csc + b * 8, make_uint2(0u, 0u));
             ac.scales[scale_offset32(r, b, nktc)] = 0;
         }
         zero_pad_rows(ac);
@@ -1482,7 +1496,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas)
                 if (c < cols && kb < kbp) {
                     const uint2 a0 = reinterpret_cast<const uint2 *>(stage_codes)[(2 * part) * kTileCols + cl];
                     const uint2 a1 = reinterpret_cast<const uint2 *>(stage_codes)[(2 * part + 1) * kTileCols + cl];
-                    *reinterpret_cast<uint4 *>(ac.codes + (size_t)c * csc + kb * 8) = make_uint4(a0.x, a0.y, a1.x, a1.y);
+                    put_codes(ac, (size_t)c * csc + kb * 8, make_uint4(a0.x, a0.y, a1.x, a1.y));
                 }
             }
             // column-wise scales: column c, blocks kb0 + 4h .. + 3 = one 4-byte word of an atom
@@ -1522,7 +1536,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas)
         const uint32_t npr = (uint32_t)ar.out_rows * nbr;
         for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < npr; t += gridDim.x * blockDim.x) {
             const uint32_t r = t / nbr, b = kvr + (t - r * nbr);
-            *reinterpret_cast<uint2 *>(ar.codes + (size_t)r * csr + b * 8) = make_uint2(0u, 0u);
+            put_codes(ar, (size_t)r * csr + b * 8, make_uint2(0u, 0u));
             ar.scales[scale_offset32(r, b, nktr)] = 0;
         }
         zero_pad_rows(ar);
@@ -1687,6 +1701,7 @@ cudaError_t quantize_grouped_typed(const QuantLaunch &q, const GroupQuant &gt, v
     a.rht_seed = q.rht_seed; a.sr_seed = q.sr_seed; a.sr_counter = q.sr_counter; a.elem_base = 0;
     a.status = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsStatus);
     a.codes = q.codes; a.scales = q.scales; a.tensor_scale = q.tensor_scale;
+    a.eplane = q.grid == kE1M2 ? q.eplane : nullptr;
     a.uqmax = q.grid == kE2M1C ? 2.0f : 3.5f;
     a.utop = grid_top(q.grid);
     uint32_t *slots = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsPartials);
@@ -2091,6 +2106,7 @@ Args make_args(const QuantLaunch &q, void *ws) {
     a.amax_in = q.amax_in;
     a.status = ws ? reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsStatus) : nullptr;
     a.codes = q.codes; a.scales = q.scales; a.tensor_scale = q.tensor_scale;
+    a.eplane = q.grid == kE1M2 ? q.eplane : nullptr;
     a.uqmax = q.grid == kE2M1C ? 2.0f : 3.5f;
     a.utop = grid_top(q.grid);
     return a;

@@ -43,7 +43,8 @@ class QParamsC(ctypes.Structure):
 class QTensorC(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("tensor_scale", ctypes.c_void_p), ("rows", ctypes.c_int64),
-                ("k", ctypes.c_int64), ("grid", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("k", ctypes.c_int64), ("grid", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("eplane", ctypes.c_void_p)]
 
 
 class StatsC(ctypes.Structure):
@@ -157,19 +158,25 @@ def workspace(device=None):
 
 class QTensor:
     """Quantized tensor: device codes / scales / tensor scale in the layouts
-    of include/ufp4.h, logical shape rows x k."""
+    of include/ufp4.h, logical shape rows x k; E1M2 tensors may carry the
+    correction plane (eplane) that the quantizer writes and the GEMM loads."""
 
-    def __init__(self, codes, scales, tensor_scale, rows, k, grid):
+    def __init__(self, codes, scales, tensor_scale, rows, k, grid, eplane=None):
         self.codes, self.scales, self.tensor_scale = codes, scales, tensor_scale
         self.rows, self.k, self.grid = int(rows), int(k), int(grid)
+        self.eplane = eplane
 
     @classmethod
-    def empty(cls, rows, k, grid, device="cuda"):
+    def empty(cls, rows, k, grid, device="cuda", eplane=None):
+        """eplane: allocate the E1M2 correction plane (default: for E1M2)."""
         L = lib()
         codes = torch.empty(max(int(L.ufp4_codes_bytes(rows, k)), 1), dtype=torch.uint8, device=device)
         scales = torch.empty(max(int(L.ufp4_scales_bytes(rows, k)), 1), dtype=torch.uint8, device=device)
         ts = torch.empty(1, dtype=torch.float32, device=device)
-        return cls(codes, scales, ts, rows, k, grid)
+        if eplane is None:
+            eplane = int(grid) == UFP4_E1M2
+        ep = torch.empty_like(codes) if eplane and int(grid) == UFP4_E1M2 else None
+        return cls(codes, scales, ts, rows, k, grid, ep)
 
     @property
     def kpad(self):
@@ -177,7 +184,8 @@ class QTensor:
 
     def c(self):
         return QTensorC(self.codes.data_ptr(), self.scales.data_ptr(), self.tensor_scale.data_ptr(),
-                        self.rows, self.k, self.grid, 0)
+                        self.rows, self.k, self.grid, 0,
+                        None if self.eplane is None else self.eplane.data_ptr())
 
     def codes_2d(self):
         """codes as uint8 [rows, kpad/2] (a view)."""

@@ -143,7 +143,19 @@ typedef struct {
  *            blocks >= k/16 are written as 0.
  *   tensor_scale : 1 fp32, S_dec.
  *   Values: x ~= v(m) * e_b * S_dec (then the inverse RHT when rht was on).
- *   Alignment: codes and scales 16-byte aligned, tensor_scale 4-byte.  */
+ *   eplane : optional, UFP4_E1M2 only (NULL otherwise): a buffer of the
+ *            codes' size and layout holding the E1M2 correction plane.  An
+ *            E1M2 value m/2 equals (R + E)/2 with R the code's nibble read as
+ *            an E2M1 code and E = {0,.5,1,1.5,2,2,2,1}[m] (sign kept), stored
+ *            here as E2M1 codes; a padding code 0 has E code 0.  Every
+ *            quantize call that writes the tensor writes the plane too, and
+ *            ufp4_gemm / ufp4_gemm_grouped load it (instead of expanding E
+ *            on chip, which is slower) when both operands carry one.  The
+ *            plane must stay in step with the codes: a caller that writes
+ *            codes by other means sets eplane to NULL.  Costs 0.5 byte per
+ *            element of device memory and of quantizer writes.
+ *   Alignment: codes, scales and eplane 16-byte aligned, tensor_scale
+ *   4-byte.  */
 typedef struct {
     uint8_t *codes;
     uint8_t *scales;
@@ -152,6 +164,7 @@ typedef struct {
     int64_t k;
     int32_t grid;
     int32_t reserved;          /* must be 0 */
+    uint8_t *eplane;           /* E1M2 correction plane or NULL */
 } ufp4_qtensor;
 
 /* Host-side size helpers (no GPU needed). */
@@ -245,8 +258,11 @@ UFP4_API ufp4_status ufp4_dequantize(const ufp4_qtensor *q, int32_t inverse_rht,
  * This is fwd_y (Y = X W^T: A = X rows, B = W rows), bwd_dx (dX = dY W:
  * A = dY rows, B = W columns) or bwd_dw (dW = dY^T X: A = dY columns,
  * B = X columns) ([ZC] "The fix -- UFP4"; [HP] technical approach).
- * E2M1 runs natively on tcgen05 block-scaled FP4 MMAs; E1M2 codes are split
- * exactly into two E2M1 planes per operand in shared memory.
+ * E2M1 runs natively on tcgen05 block-scaled FP4 MMAs; E1M2 runs as the
+ * exact split into two E2M1 planes per operand (R, the codes, and E, the
+ * correction plane): four MMAs per K step.  The E planes are loaded from
+ * a->eplane and b->eplane when both are given, else expanded from the codes
+ * in shared memory (slower); both give the same result bit for bit.
  * Requirements: a->k == b->k, a->grid == b->grid; c 16-byte aligned,
  * ldc >= N and ldc % 4 == 0.  K = 0 writes zeros. */
 UFP4_API ufp4_status ufp4_gemm(const ufp4_qtensor *a, const ufp4_qtensor *b, float *c, int64_t ldc,

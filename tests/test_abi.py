@@ -92,6 +92,12 @@ def test_quantize_rejects_bad_arguments_on_host(L):
     assert call(_q(), _qt(32, 64), w=0) == INV                         # no workspace
     assert call(_q(), _qt(32, 64), wb=16) == INV                       # workspace too small
     assert call(_q(), _qt(32, 64, ptr=0x1001)) == INV                  # misaligned codes
+    q = _qt(32, 64)
+    q.eplane = 0x4000
+    assert call(_q(), q) == INV                                        # E plane on an E2M1 tensor
+    q = _qt(32, 64, grid=1)
+    q.eplane = 0x4008
+    assert call(_q(grid=1), q) == INV                                  # misaligned E plane
     assert call(_q(colwise=True), _qt(64, 30), rows=30) == INV         # colwise rows % 16
     assert call(_q(colwise=True), _qt(62, 32), rows=32, cols=62, ld=64) == INV  # colwise cols % 4
     p = _q()
@@ -121,6 +127,9 @@ def test_gemm_and_dequant_reject_bad_arguments_on_host(L):
     assert L.ufp4_gemm(ctypes.byref(a), ctypes.byref(b), 0x4000, 32, None) == INV   # ldc < N
     assert L.ufp4_gemm(ctypes.byref(a), ctypes.byref(b), 0x4004, 64, None) == INV   # c alignment
     assert L.ufp4_gemm(ctypes.byref(a), ctypes.byref(b), 0, 64, None) == INV        # no C
+    a, b = _qt(128, 256, grid=1), _qt(64, 256, grid=1)
+    a.eplane = 0x4001
+    assert L.ufp4_gemm(ctypes.byref(a), ctypes.byref(b), 0x4000, 64, None) == INV   # E plane alignment
     q = _qt(16, 32)
     assert L.ufp4_dequantize(ctypes.byref(q), 2, 0, 0x4000, 32, None) == INV
     assert L.ufp4_dequantize(ctypes.byref(q), 0, 0, 0x4000, 30, None) == INV
