@@ -1043,9 +1043,13 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_row_staged(Args a,
                 }
             }
         } else {
-            for (uint32_t k = threadIdx.x; k < BPC; k += kThreads) {
+            // a thread's blocks of the chunk unrolled, so that their independent
+            // arithmetic interleaves (2 % faster with the transform)
+#pragma unroll
+            for (uint32_t kk = 0; kk < (BPC + kThreads - 1) / kThreads; ++kk) {
+                const uint32_t k = threadIdx.x + kk * kThreads;
                 const uint32_t gb = i * BPC + k;
-                if (gb >= total_blocks) break;
+                if (k >= BPC || gb >= total_blocks) continue;
                 Raw<In> raw;
                 raw.load_shared(st + k * 16 * sizeof(In));
                 if (AMAX) {
