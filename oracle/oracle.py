@@ -21,6 +21,7 @@ import numpy as np
 from . import build as _build
 
 E2M1, E1M2, E2M1C = 0, 1, 2
+MXFP4 = 3      # E2M1 elements, E8M0 scale per 32 elements (see quantize_mx)
 RTNE, SR = 0, 1
 
 _lib = None
@@ -72,6 +73,17 @@ def lib():
         L.ref_gemm_entries.argtypes = [vp, vp, ctypes.c_int64, vp, vp, ctypes.c_int64, vp]
         L.ref_stats.argtypes = [vp, vp, vp, ctypes.c_float, ctypes.c_int64, ctypes.c_int64,
                                 ctypes.c_int, vp]
+        L.ref_e8m0_decode.argtypes = [ctypes.c_uint8]
+        L.ref_e8m0_decode.restype = ctypes.c_double
+        L.ref_mx_shared_exp.argtypes = [ctypes.c_float]
+        L.ref_mx_shared_exp.restype = ctypes.c_int
+        L.ref_quantize_mx.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                      ctypes.c_uint64, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64,
+                                      vp, vp, vp]
+        L.ref_quantize_mx.restype = ctypes.c_int
+        L.ref_dequantize_mx.argtypes = [vp, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                        ctypes.c_uint64, vp]
+        L.ref_stats_mx.argtypes = [vp, vp, vp, ctypes.c_int64, ctypes.c_int64, vp]
         _lib = L
     return _lib
 
@@ -270,5 +282,56 @@ def stats(y, codes, scales, tensor_scale, grid):
     out = np.zeros(7, dtype=np.float64)
     lib().ref_stats(_p(y), _p(codes), _p(scales), ctypes.c_float(tensor_scale), rows, k,
                     grid, _p(out))
+    keys = ["alpha", "sqnr_db", "mean_bias", "sum_aq", "sum_aa", "sum_err2", "bias_count"]
+    return dict(zip(keys, [float(v) for v in out]))
+
+
+# ------------------------------------------------------------------- MXFP4
+def e8m0_decode(b):
+    return lib().ref_e8m0_decode(int(b))
+
+
+def mx_shared_exp(a):
+    return int(lib().ref_mx_shared_exp(float(a)))
+
+
+def quantize_mx(x, rht=False, rht_seed=0, round_mode=RTNE, sr_seed=0, sr_counter=0, colwise=False):
+    """MXFP4 quantization (E2M1 elements, one E8M0 scale per 32 elements along
+    the last dim, or along the first when colwise; see ufp4_oracle.c).
+    Returns dict(codes=u8[rows_out, k], scales=u8[rows_out, k//32] (biased
+    exponents), y=f32[rows_out, k])."""
+    x = np.asarray(x, dtype=np.float32)
+    if colwise:
+        x = x.T
+    x = np.ascontiguousarray(x)
+    rows, k = x.shape
+    codes = np.zeros((rows, k), dtype=np.uint8)
+    scales = np.zeros((rows, max(k // 32, 0)), dtype=np.uint8)
+    y = np.zeros((rows, k), dtype=np.float32)
+    rc = lib().ref_quantize_mx(_p(x), rows, k, k, int(bool(rht)), ctypes.c_uint64(rht_seed), round_mode,
+                               ctypes.c_uint64(sr_seed), ctypes.c_uint64(sr_counter), _p(codes), _p(scales),
+                               _p(y))
+    if rc != 0:
+        raise ValueError("ref_quantize_mx failed (%d): k must be a multiple of 32" % rc)
+    return dict(codes=codes, scales=scales, y=y)
+
+
+def dequantize_mx(codes, scales, inverse_rht=False, rht_seed=0):
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    rows, k = codes.shape
+    out = np.zeros((rows, k), dtype=np.float64)
+    lib().ref_dequantize_mx(_p(codes), _p(scales), rows, k, int(bool(inverse_rht)), ctypes.c_uint64(rht_seed),
+                            _p(out))
+    return out
+
+
+def stats_mx(y, codes, scales):
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    rows, k = codes.shape
+    out = np.zeros(7, dtype=np.float64)
+    lib().ref_stats_mx(_p(y), _p(codes), _p(scales), rows, k, _p(out))
     keys = ["alpha", "sqnr_db", "mean_bias", "sum_aq", "sum_aa", "sum_err2", "bias_count"]
     return dict(zip(keys, [float(v) for v in out]))

@@ -454,3 +454,132 @@ void ref_stats(const float *A, const uint8_t *codes, const uint8_t *scales,
     out[2] = cnt > 0 ? bias / cnt : 0.0;
     out[3] = saq; out[4] = saa; out[5] = se2; out[6] = cnt;
 }
+
+/* ------------------------------------------------------------------------
+ * MXFP4, a comparison format of the pages ([HP] technical approach, the
+ * "comparison formats" line: E2M1-based NVFP4 and MXFP4); the pages give no
+ * details.  READING: the OCP Microscaling (MX) definition of MXFP4 --
+ *   blocks of 32 elements along k share one E8M0 scale X = 2^s with
+ *   s = floor(log2(max |y|)) - 2  (2 = the exponent of E2M1's largest
+ *   normal, 6 = 1.5 * 2^2), clamped to the E8M0 range [-127, 127]; a block
+ *   whose max is 0 stores s = -127;
+ *   q = y / X (exact: a power-of-two scaling, rounded once to fp32);
+ *   code = signbit(q) << 3 | E2M1 rounding of min(|q|, 6): RTNE, or SR with
+ *   the same Philox words as ref_quantize;
+ *   no tensor-level scale.
+ * With rht set each 16-element half of a block is rotated as in
+ * ref_quantize.  Outputs: codes rows x k (one code per byte), scales
+ * rows x k/32 (biased exponent bytes s + 127).  SR element index r * k + j.
+ * Returns 0, or -1 on k % 32 != 0.
+ * ---------------------------------------------------------------------- */
+double ref_e8m0_decode(uint8_t b)
+{
+    if (b == 255) return NAN;
+    return ldexp(1.0, (int)b - 127);
+}
+
+/* floor(log2(a)) - 2 clamped to [-127, 127]; -127 for a == 0. */
+int ref_mx_shared_exp(float a)
+{
+    if (!(a > 0.0f)) return -127;
+    int e;
+    frexp((double)a, &e);          /* a = f 2^e, f in [0.5, 1): floor(log2 a) = e - 1 */
+    int s = (e - 1) - 2;
+    if (s < -127) s = -127;
+    if (s > 127) s = 127;
+    return s;
+}
+
+int ref_quantize_mx(const float *x, int64_t rows, int64_t k, int64_t ld, int rht, uint64_t rht_seed,
+                    int round_mode, uint64_t sr_seed, uint64_t sr_counter,
+                    uint8_t *codes, uint8_t *scales, float *y_out)
+{
+    if (k % 32 != 0) return -1;
+    const int64_t nb = k / 32;
+    int32_t d[16];
+    double hd[16][16];
+    ref_rht_signs(rht_seed, d);
+    rht16_matrix(d, hd);
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            float blk[32];
+            for (int h = 0; h < 2; ++h) {
+                const float *src = x + r * ld + b * 32 + 16 * h;
+                if (rht) rht16_forward(src, hd, blk + 16 * h);
+                else memcpy(blk + 16 * h, src, 16 * sizeof(float));
+            }
+            float amax = 0.0f;
+            for (int j = 0; j < 32; ++j) if (fabsf(blk[j]) > amax) amax = fabsf(blk[j]);
+            const int s = ref_mx_shared_exp(amax);
+            scales[r * nb + b] = (uint8_t)(s + 127);
+            for (int j = 0; j < 32; ++j) {
+                const float q = (float)ldexp((double)blk[j], -s);
+                float a = fabsf(q);
+                if (a > 6.0f) a = 6.0f;
+                int m;
+                if (round_mode == REF_SR) {
+                    const uint64_t i = (uint64_t)r * (uint64_t)k + (uint64_t)(b * 32 + j);
+                    m = ref_round_sr(REF_E2M1, a, ref_sr_word(sr_seed, sr_counter, i));
+                } else {
+                    m = ref_round_rtne(REF_E2M1, a);
+                }
+                codes[r * k + b * 32 + j] = (uint8_t)((signbit(q) ? 8 : 0) | m);
+            }
+            if (y_out) memcpy(y_out + r * k + b * 32, blk, sizeof blk);
+        }
+    return 0;
+}
+
+/* MXFP4 dequantization: v(m) * 2^s, exact in fp64; inverse_rht rotates each
+ * 16-element half back.  Output fp64 rows x k. */
+void ref_dequantize_mx(const uint8_t *codes, const uint8_t *scales, int64_t rows, int64_t k,
+                       int inverse_rht, uint64_t rht_seed, double *out)
+{
+    const int64_t nb = k / 32;
+    int32_t d[16];
+    ref_rht_signs(rht_seed, d);
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            const double X = ref_e8m0_decode(scales[r * nb + b]);
+            double blk[32];
+            for (int j = 0; j < 32; ++j) {
+                const uint8_t c = codes[r * k + b * 32 + j];
+                const double v = ref_grid_value(REF_E2M1, c & 7);
+                blk[j] = ((c & 8) ? -v : v) * X;
+            }
+            if (inverse_rht)
+                for (int h = 0; h < 2; ++h) {
+                    double xb[16];
+                    rht16_inverse(blk + 16 * h, d, xb);
+                    memcpy(blk + 16 * h, xb, sizeof xb);
+                }
+            memcpy(out + r * k + b * 32, blk, sizeof blk);
+        }
+}
+
+/* ref_stats for MXFP4: the grid-unit magnitude is a = min(|A| / X, 6). */
+void ref_stats_mx(const float *A, const uint8_t *codes, const uint8_t *scales, int64_t rows, int64_t k,
+                  double out[7])
+{
+    const int64_t nb = k / 32;
+    double saq = 0, saa = 0, se2 = 0, bias = 0, cnt = 0;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            const double X = ref_e8m0_decode(scales[r * nb + b]);
+            for (int j = 0; j < 32; ++j) {
+                const int64_t i = r * k + b * 32 + j;
+                const uint8_t c = codes[i];
+                const double v = ref_grid_value(REF_E2M1, c & 7);
+                const double dq = ((c & 8) ? -v : v) * X;
+                const double a = (double)A[i];
+                saq += dq * a; saa += a * a; se2 += (a - dq) * (a - dq);
+                double g = fabs(a) / X;
+                if (g > 6.0) g = 6.0;
+                if (g != 0.0) { bias += v - g; cnt += 1.0; }
+            }
+        }
+    out[0] = saa > 0 ? saq / saa : 1.0;
+    out[1] = se2 > 0 ? 10.0 * log10(saa / se2) : INFINITY;
+    out[2] = cnt > 0 ? bias / cnt : 0.0;
+    out[3] = saq; out[4] = saa; out[5] = se2; out[6] = cnt;
+}
