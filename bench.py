@@ -694,19 +694,23 @@ def run_workloads(args):
         c = torch.empty(256, 256, device=dev)
         ms = _ev_time(lambda: U.ufp4_gemm(qa, qb, out=c), flush)
         r["gemm_%s_tflops" % gn] = round(2 * 256 ** 3 / (ms * 1e-3) / 1e12, 3)
+    for rht in (False, True):   # MXFP4: quantization numerics only (no GEMM)
+        r["numerics"]["mxfp4_rht_%s" % ("on" if rht else "off")] = stats_of(x, U.UFP4_MXFP4, rht)
     emit(r)
 
     # outlier: 4096 x 4096, RHT on/off, both grids
     d = inputs.outlier(0)
     x = torch.from_numpy(d["x"]).to(torch.bfloat16).to(dev)
     r = {"workload": "outlier_4096x4096", "numerics": {}, "quantize_gbs": {}}
-    for g, gn in ((0, "e2m1"), (1, "e1m2"), (2, "e2m1c")):
+    for g, gn in ((0, "e2m1"), (1, "e1m2"), (2, "e2m1c"), (3, "mxfp4")):
+        # MXFP4 moves 2 + 0.5 + 1/32 B/elem (one E8M0 byte per 32 elements)
+        bpe = 2.53125 if g == U.UFP4_MXFP4 else Q_BYTES_PER_ELEM
         for rht in (False, True):
             key = "%s_rht_%s" % (gn, "on" if rht else "off")
             r["numerics"][key] = stats_of(x, g, rht)
             q = U.QTensor.empty(4096, 4096, g, dev)
             ms = _ev_time(lambda: U.ufp4_quantize(x, g, rht=rht, rht_seed=2, out=q), flush)
-            r["quantize_gbs"][key] = round(x.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
+            r["quantize_gbs"][key] = round(x.numel() * bpe / (ms * 1e-3) / 1e9, 1)
     n = r["numerics"]
     r["sqnr_ranking"] = {
         "before_rht_e2m1_minus_e1m2_db": round(n["e2m1_rht_off"]["sqnr_db"] - n["e1m2_rht_off"]["sqnr_db"], 3),

@@ -35,7 +35,9 @@ bool within_limits(int64_t rows, int64_t k) {
 bool valid_qtensor(const ufp4_qtensor *q) {
     if (!q || q->reserved != 0) return false;
     if (q->rows < 0 || q->k < 0 || q->k % UFP4_BLOCK != 0) return false;
-    if (q->grid != UFP4_E2M1 && q->grid != UFP4_E1M2 && q->grid != UFP4_E2M1C) return false;
+    if (q->grid != UFP4_E2M1 && q->grid != UFP4_E1M2 && q->grid != UFP4_E2M1C && q->grid != UFP4_MXFP4)
+        return false;
+    if (q->grid == UFP4_MXFP4 && q->k % UFP4_MX_BLOCK != 0) return false;
     if (q->rows == 0 || q->k == 0) return true;
     if (!q->codes || !q->scales || !q->tensor_scale) return false;
     if (q->eplane && (q->grid != UFP4_E1M2 || !aligned(q->eplane, 16))) return false;
@@ -47,14 +49,16 @@ ufp4_status check_quant_args(const void *x, int32_t dtype, int64_t rows, int64_t
                              const ufp4_qparams *p, const ufp4_qtensor *out, QuantLaunch *ql) {
     if (!p || !out) return UFP4_ERR_INVALID;
     if (dtype != UFP4_BF16 && dtype != UFP4_FP32) return UFP4_ERR_INVALID;
-    if (p->block != UFP4_BLOCK) return UFP4_ERR_UNSUPPORTED;
-    if (p->grid != UFP4_E2M1 && p->grid != UFP4_E1M2 && p->grid != UFP4_E2M1C) return UFP4_ERR_INVALID;
+    if (p->grid != UFP4_E2M1 && p->grid != UFP4_E1M2 && p->grid != UFP4_E2M1C && p->grid != UFP4_MXFP4)
+        return UFP4_ERR_INVALID;
+    if (p->block != (p->grid == UFP4_MXFP4 ? UFP4_MX_BLOCK : UFP4_BLOCK)) return UFP4_ERR_UNSUPPORTED;
     if (p->round != UFP4_RTNE && p->round != UFP4_SR) return UFP4_ERR_INVALID;
     if ((p->rht != 0 && p->rht != 1) || (p->colwise != 0 && p->colwise != 1) || p->reserved != 0)
         return UFP4_ERR_INVALID;
     if (rows < 0 || cols < 0 || ld < cols) return UFP4_ERR_INVALID;
     const int64_t out_rows = p->colwise ? cols : rows;
     const int64_t k = p->colwise ? rows : cols;
+    if (p->grid == UFP4_MXFP4 && (k % UFP4_MX_BLOCK != 0 || p->amax_in)) return UFP4_ERR_INVALID;
     if (!within_limits(out_rows, k) || !within_limits(rows, cols) || ld > UFP4_MAX_DIM)
         return UFP4_ERR_UNSUPPORTED;
     if (!valid_qtensor(out) || out->grid != p->grid || out->rows != out_rows || out->k != k)
@@ -129,6 +133,7 @@ ufp4_status ufp4_quantize_dual(const void *x, int32_t dtype, int64_t rows, int64
                                const ufp4_qtensor *out_col, void *workspace, size_t workspace_bytes,
                                ufp4_stream_t stream) {
     if (!p_row || !p_col || p_row->colwise != 0 || p_col->colwise != 1) return UFP4_ERR_INVALID;
+    if (p_row->grid == UFP4_MXFP4 || p_col->grid == UFP4_MXFP4) return UFP4_ERR_UNSUPPORTED;
     QuantLaunch qr, qc;
     ufp4_status st = check_quant_args(x, dtype, rows, cols, ld, p_row, out_row, &qr);
     if (st != UFP4_OK) return st;
@@ -172,7 +177,7 @@ ufp4_status ufp4_gemm(const ufp4_qtensor *a, const ufp4_qtensor *b, float *c, in
                       ufp4_stream_t stream) {
     if (!valid_qtensor(a) || !valid_qtensor(b)) return UFP4_ERR_INVALID;
     if (a->k != b->k) return UFP4_ERR_INVALID;
-    if (a->grid != b->grid) return UFP4_ERR_UNSUPPORTED;
+    if (a->grid != b->grid || a->grid == UFP4_MXFP4) return UFP4_ERR_UNSUPPORTED;
     const int64_t M = a->rows, N = b->rows, K = a->k;
     if (M == 0 || N == 0) return UFP4_OK;
     if (!c || !aligned(c, 16) || ldc < N || ldc % 4 != 0) return UFP4_ERR_INVALID;
@@ -201,6 +206,7 @@ ufp4_status ufp4_quantize_grouped(const void *x, int32_t dtype, int64_t cols, in
                                   const ufp4_qtensor *out, void *workspace, size_t workspace_bytes,
                                   ufp4_stream_t stream) {
     if (!p || !out || !seg_rows || n_seg < 1 || n_seg > kMaxGroups) return UFP4_ERR_INVALID;
+    if (p->grid == UFP4_MXFP4) return UFP4_ERR_UNSUPPORTED;
     if (p->amax_in) return UFP4_ERR_INVALID;
     int64_t total = 0;
     for (int i = 0; i < n_seg; ++i) {
@@ -261,7 +267,7 @@ ufp4_status ufp4_quantize_grouped(const void *x, int32_t dtype, int64_t cols, in
 ufp4_status ufp4_gemm_grouped(const ufp4_qtensor *a, const ufp4_qtensor *b, const ufp4_gemm_group *groups,
                               int32_t n, ufp4_stream_t stream) {
     if (!valid_qtensor(a) || !valid_qtensor(b) || !groups || n < 0 || n > kMaxGroups) return UFP4_ERR_INVALID;
-    if (a->grid != b->grid) return UFP4_ERR_UNSUPPORTED;
+    if (a->grid != b->grid || a->grid == UFP4_MXFP4) return UFP4_ERR_UNSUPPORTED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     std::unique_ptr<GroupGemmTab> tab(new GroupGemmTab());
     memset(tab.get(), 0, sizeof(GroupGemmTab));

@@ -18,12 +18,15 @@ constexpr int kE1M2 = 1;
 // clamped-E2M1 ablation.  It quantizes through the uniform-grid (E1M2)
 // kernels with qmax 2 and top index 4; its codes are E2M1 codes.
 constexpr int kE2M1C = 2;
+// MXFP4 (OCP microscaling): E2M1 elements, one E8M0 scale 2^s per 32
+// elements (stored at both of its 16-blocks' places), no tensor scale.
+constexpr int kMXFP4 = 3;
 constexpr int kRTNE = 0;
 constexpr int kSR = 1;
 constexpr float kFltMax = 3.402823466e38f;
 
 __host__ __device__ __forceinline__ float grid_qmax(int grid) {
-    return grid == kE2M1 ? 6.0f : (grid == kE1M2 ? 3.5f : 2.0f);
+    return (grid == kE2M1 || grid == kMXFP4) ? 6.0f : (grid == kE1M2 ? 3.5f : 2.0f);
 }
 // Largest magnitude index of the grid.
 __host__ __device__ __forceinline__ uint32_t grid_top(int grid) { return grid == kE2M1C ? 4u : 7u; }
@@ -76,6 +79,18 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
     const uint16_t in = (uint16_t)(c & 0xFFu);
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
     return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+
+// E8M0 -> fp32: 2^(b - 127) (b = 0 is 2^-127, a subnormal; 255, NaN, is
+// never written).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
+    b &= 0xFFu;
+    return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
+}
+
+// Value of a stored block-scale byte: E8M0 for MXFP4, E4M3 otherwise.
+__device__ __forceinline__ float scale_value(int grid, uint32_t c) {
+    return grid == kMXFP4 ? e8m0_to_f32(c) : e4m3_to_f32(c);
 }
 
 // --------------------------------------------------------------- bf16 bits

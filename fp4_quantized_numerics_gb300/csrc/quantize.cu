@@ -1824,7 +1824,7 @@ __global__ void __launch_bounds__(kThreads) k_stats_rowwise(Args a, int grid) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) v[i] *= 0.25f;
             const uint32_t w = *reinterpret_cast<const uint32_t *>(a.codes + p.r * (a.kpad / 2) + p.c * 4);
-            const float e = e4m3_to_f32(a.scales[scale_offset(p.r, p.c >> 1, a.nkt)]);
+            const float e = scale_value(grid, a.scales[scale_offset(p.r, p.c >> 1, a.nkt)]);
             acc_block8(acc, v, w, e, S_dec, grid, qmax);
         }
         advance(p, dr, dc, upr);
@@ -1857,12 +1857,136 @@ __global__ void __launch_bounds__(kThreads) k_stats_colwise(Args a, int grid) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const uint2 w = *reinterpret_cast<const uint2 *>(a.codes + (size_t)(c + j) * cstride + kb * 8);
-            const float e = e4m3_to_f32(a.scales[scale_offset32(c + j, kb, nkt)]);
+            const float e = scale_value(grid, a.scales[scale_offset32(c + j, kb, nkt)]);
             acc_block8(acc, &v[j][0], w.x, e, S_dec, grid, qmax);
             acc_block8(acc, &v[j][8], w.y, e, S_dec, grid, qmax);
         }
     }
     stats_reduce(acc, a.stats_out);
+}
+
+// ================================================================== MXFP4
+// The OCP microscaling format MXFP4: blocks of 32 elements along k share one
+// E8M0 scale 2^s, s = floor(log2(max |y|)) - 2 (2 = the exponent of E2M1's
+// largest normal 6), clamped to [-127, 127] (-127 for an all-zero block);
+// elements are E2M1 codes of y * 2^-s (RTNE saturating at 6, or SR).  No
+// tensor scale (tensor_scale is written as 1).  The scale byte s + 127 is
+// stored at both of the block's 16-block places of the scale layout, so the
+// dequantizer and the statistics read it like any block scale.  One thread
+// per block; with the transform, each 16-element half is rotated.
+
+// Scale byte s + 127 of a block maximum: the fp32 exponent field minus 2,
+// at least 0 (zero or subnormal maxima, and exponents below -125, clamp to
+// s = -127).
+__device__ __forceinline__ uint32_t mx_scale_byte(float amax) {
+    const uint32_t ef = (__float_as_uint(amax) >> 23) & 0xFFu;
+    return ef > 2u ? ef - 2u : 0u;
+}
+
+template <int ROUND>
+__device__ __forceinline__ void mx_store(const Args &a, float v[32], uint32_t r, uint32_t b, uint64_t i0,
+                                         uint32_t cstride, uint32_t nkt) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) amax = max_nan(amax, fabsf(v[j]));
+    if (!(amax <= kFltMax) && a.status) atomicOr(a.status, 1u);
+    const uint32_t sb = mx_scale_byte(amax);
+    const float f = __uint_as_float((254u - min(sb, 253u)) << 23);   // 2^-s, exact
+    uint32_t w[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        float q[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) q[j] = __fmul_rn(v[8 * t + j], f);
+        w[t] = codes8<kE2M1, ROUND>(q, a, i0 + 8 * t);
+    }
+    *reinterpret_cast<uint4 *>(a.codes + (size_t)r * cstride + b * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint16_t *>(a.scales + scale_offset32(r, 2 * b, nkt)) = (uint16_t)(sb | (sb << 8));
+}
+
+__device__ __forceinline__ void mx_store_zero(const Args &a, uint32_t r, uint32_t b, uint32_t cstride,
+                                              uint32_t nkt) {
+    *reinterpret_cast<uint4 *>(a.codes + (size_t)r * cstride + b * 16) = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint16_t *>(a.scales + scale_offset32(r, 2 * b, nkt)) = 0;
+}
+
+// Row-wise: unit u = r * (kpad / 32) + b; blocks b >= k / 32 are padding.
+template <class In, int ROUND, bool RHT>
+__global__ void __launch_bounds__(kThreads) k_quant_mx_row(Args a) {
+    const uint32_t nbp = (uint32_t)(a.kpad / 32), nbk = (uint32_t)(a.k / 32);
+    const uint32_t cstride = (uint32_t)(a.kpad / 2), nkt = (uint32_t)a.nkt;
+    const uint64_t total = (uint64_t)a.out_rows * nbp;
+    const uint32_t smask = RHT ? rht_sign_mask(a.rht_seed) : 0u;
+    const In *x = static_cast<const In *>(a.x);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.tensor_scale = 1.0f;
+    for (uint64_t u = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; u < total;
+         u += (uint64_t)gridDim.x * blockDim.x) {
+        const uint32_t r = (uint32_t)(u / nbp), b = (uint32_t)(u - (uint64_t)r * nbp);
+        if (b >= nbk) { mx_store_zero(a, r, b, cstride, nkt); continue; }
+        float v[32];
+        const In *p = x + (int64_t)r * a.ld + (int64_t)b * 32;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) load8(p + 8 * t, RHT ? (smask >> (8 * (t & 1))) & 0xFFu : 0u, v + 8 * t);
+        if (RHT) {
+            fwht16(v);
+            fwht16(v + 16);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] *= 0.25f;
+        }
+        mx_store<ROUND>(a, v, r, b, ((uint64_t)r * a.k + (uint64_t)b * 32), cstride, nkt);
+    }
+    zero_pad_rows(a);
+}
+
+// Column-wise (the quantization of X^T): unit u = b * cols + c, column c of
+// the input is output row c, and rows 32b..32b+31 its block b; adjacent
+// threads read adjacent columns.
+template <class In, int ROUND, bool RHT>
+__global__ void __launch_bounds__(kThreads) k_quant_mx_col(Args a) {
+    const uint32_t cols = (uint32_t)a.cols;
+    const uint32_t nbp = (uint32_t)(a.kpad / 32), nbk = (uint32_t)(a.k / 32);
+    const uint32_t cstride = (uint32_t)(a.kpad / 2), nkt = (uint32_t)a.nkt;
+    const uint64_t total = (uint64_t)nbp * cols;
+    const uint32_t smask = RHT ? rht_sign_mask(a.rht_seed) : 0u;
+    const In *x = static_cast<const In *>(a.x);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.tensor_scale = 1.0f;
+    for (uint64_t u = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; u < total;
+         u += (uint64_t)gridDim.x * blockDim.x) {
+        const uint32_t b = (uint32_t)(u / cols), c = (uint32_t)(u - (uint64_t)b * cols);
+        if (b >= nbk) { mx_store_zero(a, c, b, cstride, nkt); continue; }
+        float v[32];
+        const In *p = x + (int64_t)b * 32 * a.ld + c;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float e = (float)p[(int64_t)i * a.ld];
+            v[i] = (RHT && ((smask >> (i & 15)) & 1u)) ? -e : e;
+        }
+        if (RHT) {
+            fwht16(v);
+            fwht16(v + 16);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] *= 0.25f;
+        }
+        mx_store<ROUND>(a, v, c, b, ((uint64_t)c * a.k + (uint64_t)b * 32), cstride, nkt);
+    }
+    zero_pad_rows(a);
+}
+
+template <class In>
+cudaError_t quantize_mx_typed(const QuantLaunch &q, const Args &a, cudaStream_t s) {
+    const uint64_t units = (uint64_t)q.out_rows * (uint64_t)(a.kpad / 32);
+    const int g = (int)std::min<uint64_t>(std::max<uint64_t>((units + kThreads - 1) / kThreads, 1),
+                                          (uint64_t)num_sms() * 8);
+#define UFP4_MX(COL, RND, R)                                                                     \
+    if (q.colwise == COL && q.round == RND && (q.rht != 0) == R) {                               \
+        if (COL) k_quant_mx_col<In, RND, R><<<g, kThreads, 0, s>>>(a);                           \
+        else k_quant_mx_row<In, RND, R><<<g, kThreads, 0, s>>>(a);                               \
+        return cudaGetLastError();                                                               \
+    }
+    UFP4_MX(0, kRTNE, false) UFP4_MX(0, kRTNE, true) UFP4_MX(0, kSR, false) UFP4_MX(0, kSR, true)
+    UFP4_MX(1, kRTNE, false) UFP4_MX(1, kRTNE, true) UFP4_MX(1, kSR, false) UFP4_MX(1, kSR, true)
+#undef UFP4_MX
+    return cudaErrorInvalidValue;
 }
 
 // ========================================================== dequantization
@@ -1888,7 +2012,7 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t *codes, cons
         float v[8];
         if (valid) {
             const uint32_t w = *reinterpret_cast<const uint32_t *>(codes + p.r * (kpad / 2) + p.c * 4);
-            const float e = e4m3_to_f32(scales[scale_offset(p.r, p.c >> 1, nkt)]);
+            const float e = scale_value(grid, scales[scale_offset(p.r, p.c >> 1, nkt)]);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const uint32_t c = (w >> (4 * j)) & 0xFu;
@@ -2145,6 +2269,14 @@ cudaError_t read_quant_timeout_flag(uint32_t *flag, cudaStream_t s) {
 
 cudaError_t launch_quantize(const QuantLaunch &q, void *ws, cudaStream_t s) {
     Args a = make_args(q, ws);
+    if (q.grid == kMXFP4) {
+        // status word only (no tensor amax): clear it like the other passes do
+        if (a.status) {
+            cudaError_t e = cudaMemsetAsync(a.status, 0, sizeof(uint32_t), s);
+            if (e != cudaSuccess) return e;
+        }
+        return q.dtype == 0 ? quantize_mx_typed<__nv_bfloat16>(q, a, s) : quantize_mx_typed<float>(q, a, s);
+    }
     if (q.dtype == 0) return quantize_typed<__nv_bfloat16>(q, a, ws, s);
     return quantize_typed<float>(q, a, ws, s);
 }

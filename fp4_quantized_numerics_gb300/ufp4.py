@@ -20,7 +20,8 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libufp4.so")
 
-UFP4_E2M1, UFP4_E1M2, UFP4_E2M1C = 0, 1, 2
+UFP4_E2M1, UFP4_E1M2, UFP4_E2M1C, UFP4_MXFP4 = 0, 1, 2, 3
+UFP4_BLOCK, UFP4_MX_BLOCK = 16, 32
 UFP4_RTNE, UFP4_SR = 0, 1
 UFP4_BF16, UFP4_FP32 = 0, 1
 UFP4_OK, UFP4_ERR_INVALID, UFP4_ERR_UNSUPPORTED, UFP4_ERR_NONFINITE, UFP4_ERR_CUDA, \
@@ -202,7 +203,8 @@ def _dtype_code(x):
 
 def qparams(grid, rht=False, rht_seed=0, round=UFP4_RTNE, sr_seed=0, sr_counter=0,
             colwise=False, amax_in=None):
-    return QParamsC(int(grid), 16, int(bool(rht)), int(round), int(rht_seed) & (2**64 - 1),
+    block = UFP4_MX_BLOCK if int(grid) == UFP4_MXFP4 else UFP4_BLOCK
+    return QParamsC(int(grid), block, int(bool(rht)), int(round), int(rht_seed) & (2**64 - 1),
                     int(sr_seed) & (2**64 - 1), int(sr_counter) & (2**64 - 1), int(bool(colwise)), 0,
                     None if amax_in is None else amax_in.data_ptr())
 

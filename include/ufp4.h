@@ -68,10 +68,21 @@ typedef enum {
  *               ablation that the pages report as failing ([ZC] Key points,
  *               "Validation results").  Its codes are E2M1 codes, so its
  *               GEMM is the native E2M1 one.
+ *   UFP4_MXFP4: the OCP microscaling format MXFP4, a comparison format of
+ *               the pages ([HP] technical approach): E2M1 elements, blocks of
+ *               32 along k sharing one E8M0 scale 2^s with
+ *               s = floor(log2(max |y|)) - 2 clamped to [-127, 127] (-127
+ *               for an all-zero block), elements RTNE (saturating at 6) or SR
+ *               of y * 2^-s, and no tensor scale (tensor_scale is written as
+ *               1).  The scale byte s + 127 is stored at both of the block's
+ *               16-block places of the scale layout below.  Supported by
+ *               ufp4_quantize (block = UFP4_MX_BLOCK, k a multiple of 32,
+ *               amax_in NULL), ufp4_dequantize and ufp4_stats; the dual,
+ *               grouped and GEMM calls return UFP4_ERR_UNSUPPORTED for it.
  * A symmetric uniform INT4 grid {-7..7} needs no entry: with the same
  * two-level scaling its codes and block scales equal E1M2's bit for bit and
  * only the tensor scale (x 1/2) and the value of a code (x 2) differ. */
-typedef enum { UFP4_E2M1 = 0, UFP4_E1M2 = 1, UFP4_E2M1C = 2 } ufp4_grid;
+typedef enum { UFP4_E2M1 = 0, UFP4_E1M2 = 1, UFP4_E2M1C = 2, UFP4_MXFP4 = 3 } ufp4_grid;
 
 /* Rounding onto the grid: round-to-nearest-even, or stochastic rounding
  * (the pages apply SR to dY only: [HP] key contributions; [ZC] "The fix"). */
@@ -81,6 +92,7 @@ typedef enum { UFP4_RTNE = 0, UFP4_SR = 1 } ufp4_round;
 typedef enum { UFP4_BF16 = 0, UFP4_FP32 = 1 } ufp4_dtype;
 
 #define UFP4_BLOCK 16
+#define UFP4_MX_BLOCK 32
 
 /* Size limits of this build (32-bit block and tile indexing inside the
  * kernels).  A request beyond them returns UFP4_ERR_UNSUPPORTED before any
@@ -93,7 +105,7 @@ typedef enum { UFP4_BF16 = 0, UFP4_FP32 = 1 } ufp4_dtype;
 
 /* Quantization parameters.
  *   grid, round  : see above.
- *   block        : must be 16.
+ *   block        : must be 16 (UFP4_BLOCK); UFP4_MX_BLOCK (32) for UFP4_MXFP4.
  *   rht          : 1 = rotate every 16-block along K by y = (1/4) H16 diag(d) x
  *                  before quantizing ([ZC] "The RHT paradox"; UFP4 applies it
  *                  on all three GEMMs).  H16 is the Sylvester Hadamard matrix,
@@ -110,7 +122,8 @@ typedef enum { UFP4_BF16 = 0, UFP4_FP32 = 1 } ufp4_dtype;
  *                  run down the columns and the result is the quantization of
  *                  X^T (cols x rows), as the bwd_dx / bwd_dw GEMMs need.
  *   amax_in      : optional device pointer to the tensor amax A_t of the
- *                  (rotated) input; NULL = computed by the call.
+ *                  (rotated) input; NULL = computed by the call.  Must be
+ *                  NULL for UFP4_MXFP4 (no tensor scale).
  * Tensor scale: S_enc = fl32(448 qmax / A_t) (clamped to FLT_MAX), stored
  * S_dec = fl32(A_t / (448 qmax)); A_t = 0 gives S_enc = S_dec = 1.
  * Block scale:  e_b = E4M3_rne_satfinite(fl32(fl32(amax_b / qmax) * S_enc)).

@@ -98,6 +98,13 @@ def test_quantize_rejects_bad_arguments_on_host(L):
     q = _qt(32, 64, grid=1)
     q.eplane = 0x4008
     assert call(_q(grid=1), q) == INV                                  # misaligned E plane
+    p = _q(grid=3)                                                     # MXFP4 wants block 32
+    p.block = 16
+    assert call(p, _qt(32, 64, grid=3)) == ufp4.UFP4_ERR_UNSUPPORTED
+    assert call(_q(grid=3), _qt(32, 48, grid=3), cols=48, ld=48) == INV   # MXFP4: k % 32
+    p = _q(grid=3)
+    p.amax_in = 0x4000
+    assert call(p, _qt(32, 64, grid=3)) == INV                         # MXFP4: no tensor amax
     assert call(_q(colwise=True), _qt(64, 30), rows=30) == INV         # colwise rows % 16
     assert call(_q(colwise=True), _qt(62, 32), rows=32, cols=62, ld=64) == INV  # colwise cols % 4
     p = _q()
