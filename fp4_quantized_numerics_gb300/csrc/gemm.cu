@@ -67,21 +67,26 @@ constexpr int kE1M2Pl = 3;
 //        by six expander warps (16 warps in all: the 128 registers a thread
 //        then gets still hold the epilogue's accumulator chunks).
 //  E1M2Pl: the same 8 MMAs per 64-byte stage, all four tiles (R_A, R_B,
-//        E_A, E_B) loaded by TMA into a 3-deep ring; scale copies from their
-//        own warp as for E2M1.
+//        E_A, E_B) loaded by TMA into a 4-deep ring (the epilogue stages
+//        16-column halves through 2 KB per warp to make room); scale copies
+//        from their own warp as for E2M1.
 template <int GRID>
 struct Cfg {
     static constexpr bool kFour = GRID != kE2M1;                     // E1M2: 4 MMAs per K step
     static constexpr bool kPl = GRID == kE1M2Pl;                     // E planes loaded by TMA
+    // columns of a staged TMA-store box: E1M2Pl stages 16-column halves
+    // through a 2 KB buffer per epilogue warp, which leaves room for a 4th stage
+    static constexpr int kEpiCols = kPl ? 16 : 32;
+    static constexpr uint32_t kEpiBufBytes = 32u * kEpiCols * 4u;
     static constexpr int kBK = GRID == kE2M1 ? 128 : 64;            // bytes of K per stage
     static constexpr int kKS = kBK / 32;                             // MMA K steps per stage
-    static constexpr uint32_t kSwz = GRID == kE2M1 ? 2 : 4;          // descriptor swizzle: 128B / 64B
+    static constexpr uint32_t kSwz = kBK == 128 ? 2 : 4;             // descriptor swizzle: 128B / 64B
     static constexpr uint32_t kSbo = 8 * kBK;                        // 8-row core-matrix group stride
     static constexpr uint32_t kABytes = BM * kBK, kBBytes = BN * kBK;
     static constexpr uint32_t kSfaBytes = kKS * 512;                 // one 128-row atom per K step
     static constexpr uint32_t kSfbBytes = 2 * kKS * 512;             // two 128-row halves
     static constexpr uint32_t kSfColsPerStage = 12 * kKS;            // SFA 4 + SFB 8 columns per K step
-    static constexpr int kStages = 3;
+    static constexpr int kStages = kPl ? 4 : 3;
     static constexpr int kESlots = GRID == kE1M2 ? 3 : 0;
     static constexpr int kExpWarps = GRID == kE1M2 ? 6 : 0;
     // E2M1 and E1M2Pl: one extra warp issues the block-scale copies
@@ -101,7 +106,7 @@ struct Cfg {
     static constexpr uint32_t kESlotBytes = kABytes + kBBytes;
     static constexpr uint32_t kEOff = kStages * kStageBytes;
     static constexpr uint32_t kEpiOff = kEOff + kESlots * kESlotBytes;
-    static constexpr uint32_t kBarOff = kEpiOff + kEpiWarps * kEpiBufs * 4096;
+    static constexpr uint32_t kBarOff = kEpiOff + kEpiWarps * kEpiBufs * kEpiBufBytes;
     static constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;   // + barriers + alignment slack
     static_assert(kStageBytes % 1024 == 0 && kESlotBytes % 1024 == 0, "tile alignment");
     static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -424,7 +429,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         const int q = warp & 3;                  // TMEM lane quadrant of this warp
         const int ew = warp - 2;
         const int h = ew >> 2;                   // column half of the tile
-        const uint32_t buf0 = smem_base + C::kEpiOff + (uint32_t)ew * NB * 4096u;
+        const uint32_t buf0 = smem_base + C::kEpiOff + (uint32_t)ew * NB * C::kEpiBufBytes;
         // E1M2 accumulates (R + E)(R + E) = 4 A B^T
         const float kfix = C::kFour ? 0.25f : 1.0f;
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
@@ -437,6 +442,77 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
             const TileInfo ti = tile_info<C::kKS>(p, tab, t);
             const float alpha = __fmul_rn(*ti.ts_a, *ti.ts_b);
             const int m0 = ti.m_loc + 32 * q, n0 = ti.n_loc + 128 * h;
+            if constexpr (C::kEpiCols == 16 && kGrouped) {
+                // grouped E1M2Pl: all four chunks into registers, accumulator
+                // handed back, then each lane stores its row's 128 columns
+                // (512 contiguous bytes) with the group's bounds
+                uint32_t v[4][32];
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) ptx::tc_ld_32x32b_x32(taddr + 32u * ch, v[ch]);
+                ptx::tc_wait_ld();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(acce);
+                const int row = m0 + lane;
+                if (row < ti.M) {
+                    float *crow = ti.c + (int64_t)row * ti.ldc;
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int col = n0 + 32 * ch + 4 * j;
+                            const float4 o = make_float4(__uint_as_float(v[ch][4 * j]) * kfix * alpha,
+                                                         __uint_as_float(v[ch][4 * j + 1]) * kfix * alpha,
+                                                         __uint_as_float(v[ch][4 * j + 2]) * kfix * alpha,
+                                                         __uint_as_float(v[ch][4 * j + 3]) * kfix * alpha);
+                            if (col + 4 <= ti.N) {
+                                *reinterpret_cast<float4 *>(crow + col) = o;
+                            } else if (col < ti.N) {
+                                crow[col] = o.x;
+                                if (col + 1 < ti.N) crow[col + 1] = o.y;
+                                if (col + 2 < ti.N) crow[col + 2] = o.z;
+                            }
+                        }
+                }
+                continue;
+            } else if constexpr (C::kEpiCols == 16) {
+                // all four chunks into registers, accumulator handed back, then
+                // 16-column halves through one 2 KB staging buffer (64-byte
+                // swizzle) and TMA stores of 32 x 16 boxes
+                uint32_t v[4][32];
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) ptx::tc_ld_32x32b_x32(taddr + 32u * ch, v[ch]);
+                ptx::tc_wait_ld();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(acce);
+                const uint32_t rowb = buf0 + (uint32_t)lane * 64u;
+#pragma unroll
+                for (int hc = 0; hc < 8; ++hc) {
+                    // the previous store has read the buffer
+                    if (lane == 0) ptx::bulk_wait_read<0>();
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t* w = &v[hc >> 1][16 * (hc & 1) + 4 * c];
+                        const uint32_t addr = rowb + (uint32_t)((c ^ ((lane >> 1) & 3)) << 4);
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                                     "f"(__uint_as_float(w[0]) * kfix * alpha),
+                                     "f"(__uint_as_float(w[1]) * kfix * alpha),
+                                     "f"(__uint_as_float(w[2]) * kfix * alpha),
+                                     "f"(__uint_as_float(w[3]) * kfix * alpha)
+                                     : "memory");
+                    }
+                    ptx::fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int col = n0 + 16 * hc;
+                        if (m0 < ti.M && col < ti.N) ptx::tma_store_2d(&tma_c, col, m0, buf0);
+                        ptx::bulk_commit();
+                    }
+                }
+                continue;
+            } else {
             auto stage = [&](uint32_t b, const uint32_t (&v)[32]) {
                 const uint32_t rowb = b + (uint32_t)lane * 128u;
 #pragma unroll
@@ -511,6 +587,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                 __syncwarp();
                 stage(b, rest[ch - NB]);
                 flush(b, ch);
+            }
             }
         }
         if (lane == 0) ptx::bulk_wait_all();
@@ -589,12 +666,11 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 // K-major packed codes, rows x kpad/2 bytes; box = one K stage x box_rows
 // rows, swizzled as the MMA operand descriptors expect.
-bool make_code_map(CUtensorMap *m, const uint8_t *codes, int64_t rows, int64_t kpad, int box_rows, int grid) {
+bool make_code_map(CUtensorMap *m, const uint8_t *codes, int64_t rows, int64_t kpad, int box_rows, int bk) {
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)(kpad / 2), (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(kpad / 2)};
-    const int bk = grid == kE1M2 ? Cfg<kE1M2>::kBK : Cfg<kE2M1>::kBK;
     cuuint32_t box[2] = {(cuuint32_t)bk, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), dims, strides, box,
@@ -604,15 +680,18 @@ bool make_code_map(CUtensorMap *m, const uint8_t *codes, int64_t rows, int64_t k
     return r == CUDA_SUCCESS;
 }
 
-bool make_out_map(CUtensorMap *m, float *c, int64_t M, int64_t N, int64_t ldc) {
+// Output map: boxes of 32 rows x box_cols fp32 (32: 128-byte rows, 16:
+// 64-byte rows), swizzled like the epilogue's staging buffers.
+bool make_out_map(CUtensorMap *m, float *c, int64_t M, int64_t N, int64_t ldc, int box_cols) {
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
     cuuint64_t strides[1] = {(cuuint64_t)(ldc * 4)};
-    cuuint32_t box[2] = {32, 32};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, 32};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, c, dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                      CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -646,12 +725,14 @@ cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_eplane, const u
     if (K == 0) return cudaMemset2DAsync(c, ldc * sizeof(float), 0, N * sizeof(float), M, s);
     const int64_t kpad = kpad_of(K);
     const bool planes = grid == kE1M2 && a_eplane && b_eplane;
+    // K bytes per stage of the kernel that runs: the tensor maps' box width
+    const int bk = planes ? Cfg<kE1M2Pl>::kBK : (grid == kE1M2 ? Cfg<kE1M2>::kBK : Cfg<kE2M1>::kBK);
     CUtensorMap ma, mb, mea, meb, mc;
-    if (!make_code_map(&ma, a_codes, M, kpad, BM, grid) || !make_code_map(&mb, b_codes, N, kpad, BN, grid) ||
-        !make_out_map(&mc, c, M, N, ldc))
+    if (!make_code_map(&ma, a_codes, M, kpad, BM, bk) || !make_code_map(&mb, b_codes, N, kpad, BN, bk) ||
+        !make_out_map(&mc, c, M, N, ldc, planes ? Cfg<kE1M2Pl>::kEpiCols : 32))
         return cudaErrorInvalidValue;
     if (planes) {
-        if (!make_code_map(&mea, a_eplane, M, kpad, BM, grid) || !make_code_map(&meb, b_eplane, N, kpad, BN, grid))
+        if (!make_code_map(&mea, a_eplane, M, kpad, BM, bk) || !make_code_map(&meb, b_eplane, N, kpad, BN, bk))
             return cudaErrorInvalidValue;
     } else {
         mea = ma;   // unused
@@ -661,7 +742,7 @@ cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_eplane, const u
     p.sfa = a_scales; p.sfb = b_scales; p.ts_a = a_ts; p.ts_b = b_ts;
     p.c = c; p.ldc = ldc; p.M = (int)M; p.N = (int)N;
     p.nkt = (int)(kpad / 64);
-    const int ks = grid == kE1M2 ? Cfg<kE1M2>::kKS : Cfg<kE2M1>::kKS;
+    const int ks = bk / 32;   // MMA K steps per stage
     p.num_kb = (p.nkt + ks - 1) / ks;
     p.ntm = (int)((M + BM - 1) / BM);
     p.ntn = (int)((N + BN - 1) / BN);
@@ -680,13 +761,14 @@ cudaError_t launch_gemm_grouped(const uint8_t *a_codes, const uint8_t *a_eplane,
                                 int64_t b_rows, int64_t b_kpad, int grid, const GroupGemmTab &tab,
                                 cudaStream_t s) {
     const bool planes = grid == kE1M2 && a_eplane && b_eplane;
+    const int bk = planes ? Cfg<kE1M2Pl>::kBK : (grid == kE1M2 ? Cfg<kE1M2>::kBK : Cfg<kE2M1>::kBK);
     CUtensorMap ma, mb, mea, meb, mc;
-    if (!make_code_map(&ma, a_codes, a_rows, a_kpad, BM, grid) ||
-        !make_code_map(&mb, b_codes, b_rows, b_kpad, BN, grid))
+    if (!make_code_map(&ma, a_codes, a_rows, a_kpad, BM, bk) ||
+        !make_code_map(&mb, b_codes, b_rows, b_kpad, BN, bk))
         return cudaErrorInvalidValue;
     if (planes) {
-        if (!make_code_map(&mea, a_eplane, a_rows, a_kpad, BM, grid) ||
-            !make_code_map(&meb, b_eplane, b_rows, b_kpad, BN, grid))
+        if (!make_code_map(&mea, a_eplane, a_rows, a_kpad, BM, bk) ||
+            !make_code_map(&meb, b_eplane, b_rows, b_kpad, BN, bk))
             return cudaErrorInvalidValue;
     } else {
         mea = ma;   // unused
