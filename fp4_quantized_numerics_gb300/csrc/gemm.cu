@@ -74,9 +74,10 @@ template <int GRID>
 struct Cfg {
     static constexpr bool kFour = GRID != kE2M1;                     // E1M2: 4 MMAs per K step
     static constexpr bool kPl = GRID == kE1M2Pl;                     // E planes loaded by TMA
-    // columns of a staged TMA-store box: E1M2Pl stages 16-column halves
-    // through a 2 KB buffer per epilogue warp, which leaves room for a 4th stage
-    static constexpr int kEpiCols = kPl ? 16 : 32;
+    // columns of a staged TMA-store box: E1M2Pl stages 16-column pieces
+    // through a 2 KB buffer per epilogue warp, E2M1 8-column pieces through
+    // 1 KB, which leaves room for a 4th operand stage
+    static constexpr int kEpiCols = kPl ? 16 : (GRID == kE2M1 ? 8 : 32);
     static constexpr uint32_t kEpiBufBytes = 32u * kEpiCols * 4u;
     static constexpr int kBK = GRID == kE2M1 ? 128 : 64;            // bytes of K per stage
     static constexpr int kKS = kBK / 32;                             // MMA K steps per stage
@@ -86,7 +87,7 @@ struct Cfg {
     static constexpr uint32_t kSfaBytes = kKS * 512;                 // one 128-row atom per K step
     static constexpr uint32_t kSfbBytes = 2 * kKS * 512;             // two 128-row halves
     static constexpr uint32_t kSfColsPerStage = 12 * kKS;            // SFA 4 + SFB 8 columns per K step
-    static constexpr int kStages = kPl ? 4 : 3;
+    static constexpr int kStages = GRID == kE1M2 ? 3 : 4;
     static constexpr int kESlots = GRID == kE1M2 ? 3 : 0;
     static constexpr int kExpWarps = GRID == kE1M2 ? 6 : 0;
     // E2M1 and E1M2Pl: one extra warp issues the block-scale copies
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
             const TileInfo ti = tile_info<C::kKS>(p, tab, t);
             const float alpha = __fmul_rn(*ti.ts_a, *ti.ts_b);
             const int m0 = ti.m_loc + 32 * q, n0 = ti.n_loc + 128 * h;
-            if constexpr (C::kEpiCols == 16 && kGrouped) {
+            if constexpr (C::kEpiCols < 32 && kGrouped) {
                 // grouped E1M2Pl: all four chunks into registers, accumulator
                 // handed back, then each lane stores its row's 128 columns
                 // (512 contiguous bytes) with the group's bounds
@@ -475,10 +476,11 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                         }
                 }
                 continue;
-            } else if constexpr (C::kEpiCols == 16) {
+            } else if constexpr (C::kEpiCols < 32) {
                 // all four chunks into registers, accumulator handed back, then
-                // 16-column halves through one 2 KB staging buffer (64-byte
-                // swizzle) and TMA stores of 32 x 16 boxes
+                // kEpiCols-column pieces through one staging buffer (rows of
+                // 4 kEpiCols bytes, swizzled as the output map) and TMA stores
+                // of 32 x kEpiCols boxes
                 uint32_t v[4][32];
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) ptx::tc_ld_32x32b_x32(taddr + 32u * ch, v[ch]);
@@ -486,16 +488,18 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(acce);
-                const uint32_t rowb = buf0 + (uint32_t)lane * 64u;
+                constexpr int EC = C::kEpiCols, RB = 4 * EC, NC = RB / 16;   // row bytes, 16-byte pieces
+                const uint32_t rowb = buf0 + (uint32_t)lane * RB;
+                const uint32_t sw = (uint32_t)(lane * RB / 128) & (NC - 1);  // swizzle of this row
 #pragma unroll
-                for (int hc = 0; hc < 8; ++hc) {
+                for (int hc = 0; hc < 128 / EC; ++hc) {
                     // the previous store has read the buffer
                     if (lane == 0) ptx::bulk_wait_read<0>();
                     __syncwarp();
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint32_t* w = &v[hc >> 1][16 * (hc & 1) + 4 * c];
-                        const uint32_t addr = rowb + (uint32_t)((c ^ ((lane >> 1) & 3)) << 4);
+                    for (int c = 0; c < NC; ++c) {
+                        const uint32_t *w = &v[(hc * EC) / 32][(hc * EC) % 32 + 4 * c];
+                        const uint32_t addr = rowb + (uint32_t)((c ^ sw) << 4);
                         asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
                                      "f"(__uint_as_float(w[0]) * kfix * alpha),
                                      "f"(__uint_as_float(w[1]) * kfix * alpha),
@@ -506,7 +510,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                     ptx::fence_proxy_async();
                     __syncwarp();
                     if (lane == 0) {
-                        const int col = n0 + 16 * hc;
+                        const int col = n0 + EC * hc;
                         if (m0 < ti.M && col < ti.N) ptx::tma_store_2d(&tma_c, col, m0, buf0);
                         ptx::bulk_commit();
                     }
@@ -680,8 +684,8 @@ bool make_code_map(CUtensorMap *m, const uint8_t *codes, int64_t rows, int64_t k
     return r == CUDA_SUCCESS;
 }
 
-// Output map: boxes of 32 rows x box_cols fp32 (32: 128-byte rows, 16:
-// 64-byte rows), swizzled like the epilogue's staging buffers.
+// Output map: boxes of 32 rows x box_cols fp32 (32, 16, 8: rows of 128,
+// 64, 32 bytes), swizzled like the epilogue's staging buffers.
 bool make_out_map(CUtensorMap *m, float *c, int64_t M, int64_t N, int64_t ldc, int box_cols) {
     auto enc = get_encode();
     if (!enc) return false;
@@ -691,7 +695,8 @@ bool make_out_map(CUtensorMap *m, float *c, int64_t M, int64_t N, int64_t ldc, i
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, c, dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                     box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                    : (box_cols == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B),
                      CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -729,7 +734,8 @@ cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_eplane, const u
     const int bk = planes ? Cfg<kE1M2Pl>::kBK : (grid == kE1M2 ? Cfg<kE1M2>::kBK : Cfg<kE2M1>::kBK);
     CUtensorMap ma, mb, mea, meb, mc;
     if (!make_code_map(&ma, a_codes, M, kpad, BM, bk) || !make_code_map(&mb, b_codes, N, kpad, BN, bk) ||
-        !make_out_map(&mc, c, M, N, ldc, planes ? Cfg<kE1M2Pl>::kEpiCols : 32))
+        !make_out_map(&mc, c, M, N, ldc,
+                      planes ? Cfg<kE1M2Pl>::kEpiCols : (grid == kE1M2 ? Cfg<kE1M2>::kEpiCols : Cfg<kE2M1>::kEpiCols)))
         return cudaErrorInvalidValue;
     if (planes) {
         if (!make_code_map(&mea, a_eplane, M, kpad, BM, bk) || !make_code_map(&meb, b_eplane, N, kpad, BN, bk))
