@@ -443,40 +443,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
             const TileInfo ti = tile_info<C::kKS>(p, tab, t);
             const float alpha = __fmul_rn(*ti.ts_a, *ti.ts_b);
             const int m0 = ti.m_loc + 32 * q, n0 = ti.n_loc + 128 * h;
-            if constexpr (C::kEpiCols < 32 && kGrouped) {
-                // grouped E1M2Pl: all four chunks into registers, accumulator
-                // handed back, then each lane stores its row's 128 columns
-                // (512 contiguous bytes) with the group's bounds
-                uint32_t v[4][32];
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) ptx::tc_ld_32x32b_x32(taddr + 32u * ch, v[ch]);
-                ptx::tc_wait_ld();
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(acce);
-                const int row = m0 + lane;
-                if (row < ti.M) {
-                    float *crow = ti.c + (int64_t)row * ti.ldc;
-#pragma unroll
-                    for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int col = n0 + 32 * ch + 4 * j;
-                            const float4 o = make_float4(__uint_as_float(v[ch][4 * j]) * kfix * alpha,
-                                                         __uint_as_float(v[ch][4 * j + 1]) * kfix * alpha,
-                                                         __uint_as_float(v[ch][4 * j + 2]) * kfix * alpha,
-                                                         __uint_as_float(v[ch][4 * j + 3]) * kfix * alpha);
-                            if (col + 4 <= ti.N) {
-                                *reinterpret_cast<float4 *>(crow + col) = o;
-                            } else if (col < ti.N) {
-                                crow[col] = o.x;
-                                if (col + 1 < ti.N) crow[col + 1] = o.y;
-                                if (col + 2 < ti.N) crow[col + 2] = o.z;
-                            }
-                        }
-                }
-                continue;
-            } else if constexpr (C::kEpiCols < 32) {
+            if constexpr (C::kEpiCols < 32) {
                 // all four chunks into registers, accumulator handed back, then
                 // kEpiCols-column pieces through one staging buffer (rows of
                 // 4 kEpiCols bytes, swizzled as the output map) and TMA stores
@@ -494,7 +461,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
 #pragma unroll
                 for (int hc = 0; hc < 128 / EC; ++hc) {
                     // the previous store has read the buffer
-                    if (lane == 0) ptx::bulk_wait_read<0>();
+                    if (!kGrouped && lane == 0) ptx::bulk_wait_read<0>();
                     __syncwarp();
 #pragma unroll
                     for (int c = 0; c < NC; ++c) {
@@ -507,12 +474,41 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                                      "f"(__uint_as_float(w[3]) * kfix * alpha)
                                      : "memory");
                     }
-                    ptx::fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0) {
-                        const int col = n0 + EC * hc;
-                        if (m0 < ti.M && col < ti.N) ptx::tma_store_2d(&tma_c, col, m0, buf0);
-                        ptx::bulk_commit();
+                    if constexpr (!kGrouped) {
+                        ptx::fence_proxy_async();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const int col = n0 + EC * hc;
+                            if (m0 < ti.M && col < ti.N) ptx::tma_store_2d(&tma_c, col, m0, buf0);
+                            ptx::bulk_commit();
+                        }
+                    } else {
+                        // grouped: masked, row-coalesced stores within the group's bounds
+                        __syncwarp();
+                        constexpr int LPR = EC / 4, RPI = 32 / LPR;   // lanes per row, rows per pass
+                        const int pc = lane % LPR;
+#pragma unroll
+                        for (int it = 0; it < LPR; ++it) {
+                            const int rr = it * RPI + lane / LPR;
+                            const uint32_t swr = (uint32_t)(rr * RB / 128) & (NC - 1);
+                            float4 o;
+                            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                         : "=f"(o.x), "=f"(o.y), "=f"(o.z), "=f"(o.w)
+                                         : "r"(buf0 + (uint32_t)rr * RB + ((pc ^ swr) << 4))
+                                         : "memory");
+                            const int row = m0 + rr, col = n0 + EC * hc + 4 * pc;
+                            if (row < ti.M && col < ti.N) {
+                                float *cp = ti.c + (int64_t)row * ti.ldc + col;
+                                if (col + 4 <= ti.N) {
+                                    *reinterpret_cast<float4 *>(cp) = o;
+                                } else {
+                                    cp[0] = o.x;
+                                    if (col + 1 < ti.N) cp[1] = o.y;
+                                    if (col + 2 < ti.N) cp[2] = o.z;
+                                }
+                            }
+                        }
+                        __syncwarp();
                     }
                 }
                 continue;
