@@ -49,12 +49,19 @@ FALLBACK = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
-        with open(p) as f:
-            d = json.load(f)
+        try:
+            with open(p) as f:
+                d = json.load(f)
+        except (OSError, ValueError):
+            d = {}
+        # the figures may sit at the top level or one level down
+        dicts = [d] + [v for v in d.values() if isinstance(v, dict)] if isinstance(d, dict) else []
+
         def pick(*keys):
-            for k in keys:
-                if k in d and isinstance(d[k], (int, float)):
-                    return float(d[k])
+            for dd in dicts:
+                for k in keys:
+                    if k in dd and isinstance(dd[k], (int, float)) and not isinstance(dd[k], bool) and dd[k] > 0:
+                        return float(dd[k])
             return None
         hbm = pick("hbm_gbs", "hbm_GBps", "copy_gbs")
         bf = pick("bf16_tflops", "bf16_tflops_burst")
