@@ -51,3 +51,21 @@ def test_single_rank_is_identity():
     import bench
     assert bench.reduce_max(3.5, 1) == 3.5
     assert bench.weak_scaling_rate(2e9, 1, 10, 1000.0) == pytest.approx(20.0)
+
+
+def test_peaks_file_forms(tmp_path, monkeypatch):
+    """bench.peaks(): measured figures at the top level or one level down; a
+    malformed or partial file falls back to the recipe's figures."""
+    import bench
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    f = tmp_path / "MEASURED_PEAKS.json"
+    assert bench.peaks()["source"] == "fallback"
+    f.write_text('{"hbm_gbs": 7000, "bf16_tflops": 2000, "bf16_tflops_sustained": 1750}')
+    p = bench.peaks()
+    assert p["source"] == "measured" and p["hbm_gbs"] == 7000 and p["bf16_tflops_sustained"] == 1750
+    f.write_text('{"gb300": {"hbm_gbs": 7100, "bf16_tflops": 1950}}')
+    p = bench.peaks()
+    assert p["source"] == "measured" and p["bf16_tflops_sustained"] == 1950
+    for bad in ("not json", "[1, 2]", '{"hbm_gbs": 7000}', '{"hbm_gbs": true, "bf16_tflops": 1}'):
+        f.write_text(bad)
+        assert bench.peaks()["source"] == "fallback", bad
