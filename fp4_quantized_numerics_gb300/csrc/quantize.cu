@@ -1696,6 +1696,128 @@ __global__ void __launch_bounds__(kThreads) k_quant_grouped(Args a, const __grid
     zero_pad_rows(a);
 }
 
+// Row-wise grouped quantization of a contiguous input through the staged
+// ring: the segments are consecutive rows of one [sum T_e x cols] tensor, so
+// its 16 KB chunks stream as in k_row_staged.  Each block finds its segment
+// by input row (binary search over the prefix table in shared memory, cached
+// between blocks), takes that segment's tensor scale and lands in the
+// segment's output rows.  AMAX: per-segment maxima by atomicMax on the bit
+// patterns; a CTA takes a contiguous run of chunks, so a thread meets one or
+// two segments and flushes once per segment (strided chunks would visit every
+// segment and flush per chunk).  The quantization pass then zeroes the
+// padding blocks of every output row and every block of the segments'
+// padding rows.
+template <class In, int GRID, int ROUND, bool RHT, bool AMAX>
+__global__ void __launch_bounds__(kThreads, kStagedMinCtas)
+    k_row_grouped_staged(Args a, const __grid_constant__ GroupQuant gt, FastDiv bdiv, uint32_t kvb,
+                         uint32_t nchunks, uint64_t total_bytes, uint32_t *slots) {
+    constexpr int kRing = ring_depth<AMAX>();
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ GroupSmem sm;
+    const RingCtl ring = ring_init<kRing>(dsm);
+    // chunk of local step j: contiguous runs (AMAX) or strided (quantization)
+    const uint32_t per = AMAX ? (nchunks + gridDim.x - 1) / gridDim.x : 0u;
+    const uint32_t nloc = AMAX ? (blockIdx.x * per < nchunks ? min(per, nchunks - blockIdx.x * per) : 0u)
+                               : (nchunks > blockIdx.x ? (nchunks - blockIdx.x + gridDim.x - 1) / gridDim.x : 0u);
+    auto chunk_of = [&](uint32_t jj) { return AMAX ? blockIdx.x * per + jj : blockIdx.x + jj * gridDim.x; };
+    uint32_t issued = 0, j = 0;
+    auto issue = [&](uint32_t jj) {
+        if (jj >= nloc) return;
+        const uint64_t off = (uint64_t)chunk_of(jj) * kChunk;
+        const uint64_t rem = total_bytes - off;
+        const uint32_t bytes = rem < kChunk ? (uint32_t)rem : kChunk;
+        const uint32_t bar = ring.bars + 8u * (jj % kRing);
+        ptx::mbar_arrive_expect_tx(bar, bytes);
+        ptx::bulk_load(ring.buf + (jj % kRing) * kChunk, static_cast<const uint8_t *>(a.x) + off, bytes, bar);
+        issued = jj + 1;
+    };
+    if (threadIdx.x == 0)
+        for (uint32_t t = 0; t < kRing; ++t) issue(t);
+    load_group_tables(gt, sm);
+    if (!AMAX) {
+        const float qmax = GRID == kE2M1 ? 6.0f : a.uqmax;
+        for (int e = threadIdx.x; e < gt.n; e += blockDim.x) {
+            const float A_t = __uint_as_float(slots[e]);
+            float se = 1.0f, sd = 1.0f;
+            if (A_t > 0.0f) {
+                const float num = 448.0f * qmax;
+                se = __fdiv_rn(num, A_t);
+                if (se > kFltMax) se = kFltMax;
+                sd = __fdiv_rn(A_t, num);
+            }
+            sm.senc[e] = se;
+            if (blockIdx.x == 0) {
+                a.tensor_scale[e] = sd;
+                if (!isfinite(A_t) && a.status) atomicOr(a.status, 1u);
+            }
+        }
+        __syncthreads();
+    }
+    const uint32_t smask = RHT ? rht_sign_mask(a.rht_seed) : 0u;
+    const Signs sg = row_signs<In>(smask);
+    const uint32_t total_blocks = (uint32_t)(total_bytes / (16 * sizeof(In)));
+    constexpr uint32_t BPC = kChunk / (16 * sizeof(In));
+    const uint32_t cstride = (uint32_t)(a.kpad / 2), nkt = (uint32_t)a.nkt;
+    int e_cur = -1;
+    float m = 0.0f;
+    bool ok = true;
+    for (; j < nloc; ++j) {
+        if (!ring_wait<kRing>(ring, j)) { ok = false; break; }
+        const uint32_t i = chunk_of(j);
+        const uint32_t st = ring.buf + (j % kRing) * kChunk;
+#pragma unroll
+        for (uint32_t kk = 0; kk < (BPC + kThreads - 1) / kThreads; ++kk) {
+            const uint32_t k = threadIdx.x + kk * kThreads;
+            const uint32_t gb = i * BPC + k;
+            if (k >= BPC || gb >= total_blocks) continue;
+            const uint32_t r = fdiv(gb, bdiv);   // input row
+            const bool same = e_cur >= 0 && (int64_t)r >= sm.in_row[e_cur] && (int64_t)r < sm.in_row[e_cur + 1];
+            const int e = same ? e_cur : find_seg(sm.in_row, gt.n, (int64_t)r);
+            Raw<In> raw;
+            raw.load_shared(st + k * 16 * sizeof(In));
+            if (AMAX) {
+                if (e != e_cur) {
+                    seg_max_flush(slots, e_cur, RHT ? m * 0.25f : m);
+                    e_cur = e;
+                    m = 0.0f;
+                }
+                float lo[8], hi[8];
+                block_values<In, RHT>(raw, sg, lo, hi);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) m = max_nan(m, max_nan(fabsf(lo[t]), fabsf(hi[t])));
+            } else {
+                e_cur = e;
+                const uint32_t orow = (uint32_t)(sm.out_off[e] + ((int64_t)r - sm.in_row[e]));
+                quant_block_row<In, GRID, ROUND, RHT>(a, raw, orow, gb - r * kvb, sg, sm.senc[e], nullptr,
+                                                      cstride, nkt, false);
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) issue(j + kRing);
+    }
+    if (!ok) {
+        if (threadIdx.x == 0) atomicOr(&g_quant_timeout, 1u);
+        ring_drain<kRing>(ring, j, issued);
+    }
+    if (AMAX) {
+        seg_max_flush(slots, e_cur, RHT ? m * 0.25f : m);
+    } else {
+        const uint32_t nbk = (uint32_t)(a.kpad / 16);
+        for (uint32_t ro = blockIdx.x * blockDim.x + threadIdx.x; ro < (uint32_t)a.out_rows;
+             ro += gridDim.x * blockDim.x) {
+            const int e = find_seg(sm.out_off, gt.n, (int64_t)ro);
+            const bool pad_row = (int64_t)ro - sm.out_off[e] >= sm.in_row[e + 1] - sm.in_row[e];
+            for (uint32_t b = pad_row ? 0u : kvb; b < nbk; ++b) {
+                put_codes(a, (size_t)ro * cstride + b * 8, make_uint2(0u, 0u));
+                a.scales[scale_offset32(ro, b, nkt)] = 0;
+            }
+        }
+    }
+}
+
+template <bool AMAX, class K, class... P>
+cudaError_t launch_staged(K kern, int64_t work_ctas, int *grid_out, cudaStream_t s, P... args);
+
 template <class In>
 cudaError_t quantize_grouped_typed(const QuantLaunch &q, const GroupQuant &gt, void *ws, cudaStream_t s) {
     Args a{};
@@ -1712,6 +1834,24 @@ cudaError_t quantize_grouped_typed(const QuantLaunch &q, const GroupQuant &gt, v
     cudaError_t e = cudaMemsetAsync(ws, 0, kWsPartials + (size_t)gt.n * sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
     const bool col = q.colwise != 0;
+    if (!col && q.ld == q.cols) {
+        // contiguous row-wise: both passes stream the tensor through the staged ring
+        const uint32_t kvb = (uint32_t)(q.cols / 16);
+        const uint64_t tb = (uint64_t)q.rows * (uint64_t)q.cols * sizeof(In);
+        const uint32_t nch = (uint32_t)((tb + kChunk - 1) / kChunk);
+        const FastDiv bd = make_fastdiv(kvb);
+        e = q.rht ? launch_staged<true>(k_row_grouped_staged<In, kE2M1, kRTNE, true, true>, nch, nullptr, s, a, gt,
+                                        bd, kvb, nch, tb, slots)
+                  : launch_staged<true>(k_row_grouped_staged<In, kE2M1, kRTNE, false, true>, nch, nullptr, s, a,
+                                        gt, bd, kvb, nch, tb, slots);
+        if (e != cudaSuccess) return e;
+        const int kg = q.grid == kE2M1 ? kE2M1 : kE1M2;   // clamped E2M1 runs the uniform-grid kernels
+#define UFP4_GR(GRID, ROUND, RHT)                                                                                 if (kg == GRID && q.round == ROUND && (q.rht != 0) == RHT)                                                    return launch_staged<false>(k_row_grouped_staged<In, GRID, ROUND, RHT, false>, nch, nullptr, s, a,                                         gt, bd, kvb, nch, tb, slots);
+        UFP4_GR(kE2M1, kRTNE, false) UFP4_GR(kE2M1, kRTNE, true) UFP4_GR(kE2M1, kSR, false) UFP4_GR(kE2M1, kSR, true)
+        UFP4_GR(kE1M2, kRTNE, false) UFP4_GR(kE1M2, kRTNE, true) UFP4_GR(kE1M2, kSR, false) UFP4_GR(kE1M2, kSR, true)
+#undef UFP4_GR
+        return cudaErrorInvalidValue;
+    }
     // amax pass: units over real data only
     GroupQuant ga = gt;
     const uint32_t per_row_a = col ? (uint32_t)(q.cols / 2) : (uint32_t)(q.cols / 16);
