@@ -14,15 +14,17 @@
 // E1M2: not a tensor-core format.  Read as an E2M1 code, an E1M2 nibble m has
 //   the value R(m) in {0,.5,1,1.5,2,3,4,6}; the E1M2 value m/2 equals
 //   (R(m) + E(m)) / 2 with E(m) in {0,.5,1,1.5,2,2,2,1}, also E2M1.  The raw
-//   tile is therefore used as it was loaded, expander warps write one extra
-//   E plane per operand, and four MMAs (R*R, R*E, E*R, E*E) with the shared
-//   block scales accumulate 4 * A B^T, the factor 1/4 being applied (exactly)
-//   in the epilogue.
+//   tile is therefore used as it was loaded, the E plane of each operand is
+//   either loaded (the quantizer wrote it beside the codes) or written by
+//   expander warps, and four MMAs (R*R, R*E, E*R, E*E) with the shared block
+//   scales accumulate 4 * A B^T, the factor 1/4 being applied (exactly) in
+//   the epilogue.
 //
 // CTA tile 128 x 256 (one M=128, N=256 MMA per K step); the K stage depth
 // and the rings differ per grid (Cfg below).  Warp 0 = TMA producer, warp 1
 // = TMEM owner + single-thread MMA issuer, warps 2-9 = epilogue (two per TMEM
-// lane quadrant, 128 columns each), warps 10-15 (E1M2) = expanders.  The
+// lane quadrant, 128 columns each), warp 10 = scale copies (E2M1, E1M2 with
+// loaded planes) or warps 10-15 = expanders (E1M2 without planes).  The
 // accumulator (256 TMEM columns) is single-buffered: the epilogue pulls the
 // whole tile out (registers and shared staging) and hands the columns back
 // before it stores, so the stores overlap the next tile's MMAs.  Block scales
@@ -61,7 +63,8 @@ constexpr int kE1M2Pl = 3;
 // Per-variant pipeline geometry.
 //  E2M1: K stage of 128 bytes (4 MMA K steps, 128-byte swizzle) so that the
 //        issuing thread's per-stage wait/commit latency stays below the
-//        stage's tensor-core time; 3 stages.
+//        stage's tensor-core time; 4 stages (the epilogue stages 8-column
+//        pieces through 1 KB per warp to make room).
 //  E1M2: K stage of 64 bytes (2 K steps, 64-byte swizzle, 8 MMAs); a 3-deep
 //        ring of raw tiles fed by TMA and a 3-slot ring of E planes written
 //        by six expander warps (16 warps in all: the 128 registers a thread
@@ -93,7 +96,7 @@ struct Cfg {
     // E2M1 and E1M2Pl: one extra warp issues the block-scale copies
     static constexpr int kScaleWarps = GRID == kE1M2 ? 0 : 1;
     static constexpr int kThreads = 32 * (2 + kEpiWarps + kScaleWarps + kExpWarps);
-    // epilogue staging buffers (32 x 32 fp32, 4 KB) per epilogue warp
+    // epilogue staging buffers (32 rows x kEpiCols fp32) per epilogue warp
     static constexpr int kEpiBufs = GRID == kE1M2 ? 2 : 1;
     // stage layout: A | B | (E1M2Pl: E_A | E_B) | SFA | SFB;  E slots: E_A | E_B
     static constexpr uint32_t kPlaneBytes = kPl ? kABytes + kBBytes : 0;
@@ -420,12 +423,13 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
     } else if (warp < 2 + kEpiWarps) {
         // ------------------------------------------------------------ epilogue
         // Each warp owns 32 accumulator rows x 128 columns (four 32 x 32
-        // chunks).  The first kEpiBufs chunks go TMEM -> registers (x alpha) ->
-        // swizzled shared staging, the rest into registers; then the
-        // accumulator is handed back to the MMA warp and the chunks leave as
-        // TMA stores of 32 x 32 fp32 boxes (whole lines; ragged edges clipped
-        // by the tensor map).  Grouped problems copy each staged chunk out
-        // with masked, row-coalesced stores instead.
+        // chunks), handed back to the MMA warp once read out of TMEM; the
+        // values leave through swizzled shared staging as TMA stores (whole
+        // lines; ragged edges clipped by the tensor map), or, for grouped
+        // problems, as masked row-coalesced stores from the staging buffer.
+        // E2M1 / E1M2Pl: all four chunks into registers, then 8- / 16-column
+        // pieces through one small buffer.  E1M2: the first kEpiBufs chunks
+        // staged before the hand-back, the rest held in registers.
         constexpr int NB = C::kEpiBufs;
         const int q = warp & 3;                  // TMEM lane quadrant of this warp
         const int ew = warp - 2;
