@@ -69,3 +69,11 @@ def test_peaks_file_forms(tmp_path, monkeypatch):
     for bad in ("not json", "[1, 2]", '{"hbm_gbs": 7000}', '{"hbm_gbs": true, "bf16_tflops": 1}'):
         f.write_text(bad)
         assert bench.peaks()["source"] == "fallback", bad
+
+
+def test_gemm_traffic_record_matches_source():
+    """The roofline's DRAM traffic comes from a committed ncu record keyed by
+    the GEMM source's hash; it must still match the source in the tree."""
+    import bench
+    t = bench.traffic_for("k_gemm_e1m2_dense1p5b")
+    assert isinstance(t, int) and t > 0
