@@ -191,3 +191,60 @@ def test_sizes_beyond_the_index_limits_are_refused_on_host(L):
     rows_ok = (1 << 31) // (kpad(cols) // 16) - 1
     assert L.ufp4_quantize(x, 0, rows_ok, cols, cols, ctypes.byref(p), ctypes.byref(_qt(rows_ok, cols)), ws, 16,
                            None) == ufp4.UFP4_ERR_INVALID
+
+
+def test_dual_and_grouped_reject_bad_arguments_on_host(L):
+    from fp4_quantized_numerics_gb300 import ufp4
+    INV, UNS = ufp4.UFP4_ERR_INVALID, ufp4.UFP4_ERR_UNSUPPORTED
+    ws, x, wsb = 0x10000, 0x20000, L.ufp4_workspace_bytes()
+
+    def dual(pr, pc, qr, qc, rows=64, cols=128):
+        return L.ufp4_quantize_dual(x, 0, rows, cols, cols, ctypes.byref(pr) if pr else None,
+                                    ctypes.byref(pc) if pc else None, ctypes.byref(qr), ctypes.byref(qc),
+                                    ws, wsb, None)
+
+    qr, qc = _qt(64, 128), _qt(128, 64)
+    assert dual(None, _q(colwise=True), qr, qc) == INV                     # no row params
+    assert dual(_q(colwise=True), _q(colwise=True), qr, qc) == INV         # row params must be row-wise
+    assert dual(_q(), _q(), qr, qc) == INV                                 # column params must be column-wise
+    assert dual(_q(), _q(colwise=True), _qt(64, 128), _qt(64, 128)) == INV   # column result shape
+    assert dual(_q(grid=3), _q(grid=3, colwise=True), _qt(64, 128, 3), _qt(128, 64, 3)) == UNS   # MXFP4
+
+    def seg(v):
+        return (ctypes.c_int64 * len(v))(*v)
+
+    # grouped row counts: rows round up to 128 per segment, k to 64 (empty segments take none)
+    assert L.ufp4_grouped_rows(seg([100, 0, 37]), 3) == 256
+    assert L.ufp4_grouped_kpad(seg([100, 0, 37]), 3) == 192
+
+    def grouped(p, out, counts, cols=128, n=None):
+        return L.ufp4_quantize_grouped(x, 0, cols, cols, seg(counts), len(counts) if n is None else n,
+                                       ctypes.byref(p), ctypes.byref(out), ws, wsb, None)
+
+    out = _qt(256, 128)
+    assert grouped(_q(), out, [100, 0, 37], n=0) == INV                    # no segments
+    assert grouped(_q(), out, [100, 0, 37], n=300) == INV                  # too many segments
+    assert grouped(_q(), out, [100, -1, 37]) == INV                        # negative count
+    assert grouped(_q(), _qt(200, 128), [100, 0, 37]) == INV               # rows != sum of rpad
+    p = _q()
+    p.amax_in = 0x4000
+    assert grouped(p, out, [100, 0, 37]) == INV                            # amax is per segment
+    assert grouped(_q(grid=3), _qt(256, 128, 3), [100, 0, 37]) == UNS      # MXFP4
+
+    def ggemm(a, b, groups, n=None):
+        arr = (ufp4.GemmGroupC * max(len(groups), 1))(*groups)
+        return L.ufp4_gemm_grouped(ctypes.byref(a), ctypes.byref(b), arr, len(groups) if n is None else n, None)
+
+    a, b = _qt(256, 128), _qt(256, 128)
+    g = ufp4.GemmGroupC(100, 64, 128, 0, 0, 0, 0, 0, 0, 0x4000, 64)
+    assert ggemm(a, b, [g], n=300) == INV                                  # too many groups
+    assert ggemm(a, _qt(256, 128, 1), [g]) == UNS                          # grids differ
+    assert ggemm(_qt(256, 128, 3), _qt(256, 128, 3), [g]) == UNS          # MXFP4
+    bad = [ufp4.GemmGroupC(100, 64, 128, 64, 0, 0, 0, 0, 0, 0x4000, 64),   # a_row not on a 128-row tile
+           ufp4.GemmGroupC(100, 64, 120, 0, 0, 0, 0, 0, 0, 0x4000, 64),    # K % 16
+           ufp4.GemmGroupC(300, 64, 128, 0, 0, 0, 0, 0, 0, 0x4000, 64),    # rows past A
+           ufp4.GemmGroupC(100, 64, 128, 0, 32, 0, 0, 0, 0, 0x4000, 64),   # a_k not on a 64 boundary
+           ufp4.GemmGroupC(100, 64, 128, 0, 0, 0, 0, 0, 0, 0x4004, 64),    # C alignment
+           ufp4.GemmGroupC(100, 64, 128, 0, 0, 0, 0, 0, 0, 0x4000, 32)]    # ldc < N
+    for gg in bad:
+        assert ggemm(a, b, [gg]) == INV, (gg.M, gg.K, gg.a_row, gg.a_k, gg.c, gg.ldc)
