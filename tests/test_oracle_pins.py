@@ -475,3 +475,93 @@ def test_tensor_amax_is_quantize_step(oracle):
             assert q["tensor_scale"] == np.float32(np.float32(a) / np.float32(448 * 3.5))
             assert a == np.abs(q["y"]).max()
     assert oracle.tensor_amax(x) == np.abs(x).max()
+
+
+# ------------------------------------------------- pins added for mean_bias
+# E2M1 / E1M2 magnitudes as the pages print them ([ZC] Key points, "The
+# cause" and "The fix -- UFP4"), typed here so the checks below use no oracle
+# table.
+_E2M1_VALUES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+_E1M2_VALUES = [m / 2 for m in range(8)]
+
+
+def _e4m3_value(code):
+    import torch
+    return float(torch.tensor([code], dtype=torch.uint8).view(torch.float8_e4m3fn).float()[0])
+
+
+def _mean_bias_by_definition(A, codes, scales, ts, grid):
+    """mean over elements with a != 0 of (v(m) - a), a = min(|A| / (e_b S_dec),
+    qmax), blocks with e_b = 0 skipped -- written from the header's
+    definition with torch's E4M3 decoding and the pages' grid values."""
+    vals = _E2M1_VALUES if grid == 0 else _E1M2_VALUES
+    qmax = vals[-1]
+    tot, cnt = 0.0, 0
+    rows, k = codes.shape
+    for r in range(rows):
+        for b in range(k // 16):
+            e = _e4m3_value(int(scales[r, b]))
+            if e == 0.0:
+                continue
+            for j in range(b * 16, b * 16 + 16):
+                a = min(abs(float(A[r, j])) / (e * float(np.float32(ts))), qmax)
+                if a != 0.0:
+                    tot += vals[int(codes[r, j]) & 7] - a
+                    cnt += 1
+    return tot / cnt if cnt else 0.0, cnt
+
+
+@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("rht", [False, True])
+def test_mean_bias_from_its_definition(oracle, grid, rht):
+    """ref_stats' mean_bias against its definition recomputed element by
+    element.  Catches: dividing by every element instead of the a != 0 count,
+    the unclamped a, counting blocks with e_b = 0, the wrong grid table."""
+    x = inputs.normal(28, (8, 64))
+    x[3, :16] = 0.0                     # an all-zero block: e_b = 0
+    x[5, 7] = 0.0                       # a single zero element: a = 0
+    x[6, 33] = 40.0                     # the tensor max: its block saturates
+    q = oracle.quantize(x, grid, rht=rht, rht_seed=2)
+    st = oracle.stats(q["y"], q["codes"], q["scales"], q["tensor_scale"], grid)
+    want, cnt = _mean_bias_by_definition(q["y"], q["codes"], q["scales"], q["tensor_scale"], grid)
+    assert st["bias_count"] == cnt
+    assert abs(st["mean_bias"] - want) <= 1e-12
+
+
+def test_mean_bias_hand_built_block(oracle):
+    """A hand-built E2M1 input with S_dec = 1 and block scale 1.0 (E4M3 0x38):
+    8 values 1.75 and 7 values 2.4 coded as 2.0, one exact zero; a second
+    block with e_b = 0 whose codes are nonzero; a third block with |A| = 7
+    above qmax coded 6.0.  Expected bias by hand:
+    (8 (2 - 1.75) + 7 (2 - 2.4) + 16 (6 - 6)) / 31, about -0.0258."""
+    A = np.zeros((1, 48), np.float32)
+    codes = np.zeros((1, 48), np.uint8)
+    scales = np.array([[0x38, 0x00, 0x38]], np.uint8)
+    A[0, :8] = 1.75
+    A[0, 8:15] = 2.4
+    A[0, 15] = 0.0
+    codes[0, :15] = 4                    # E2M1 index 4 = 2.0
+    A[0, 16:32] = 3.0                    # skipped block (e_b = 0), nonzero codes
+    codes[0, 16:32] = 5
+    A[0, 32:48] = -7.0                   # clamped to qmax = 6, coded -6
+    codes[0, 32:48] = 8 | 7
+    st = oracle.stats(A, codes, scales, 1.0, 0)
+    assert st["bias_count"] == 31
+    v24 = float(np.float32(2.4))         # the stored input, not the decimal 2.4
+    assert math.isclose(st["mean_bias"], (8 * 0.25 + 7 * (2.0 - v24)) / 31, rel_tol=1e-12)
+
+
+# ------------------------------------------------ pin added for rht_signs
+def test_rht_signs_seed0_from_philox_kat(oracle):
+    """d for seed 0 is fixed by the first Philox known-answer row (key 0,
+    counter 0 -> word 0 = 0x6627e8d5): d_j = -1 iff bit j is set.  Catches a
+    wrong word, a wrong bit order or an inverted sign convention."""
+    row = _read_rows("philox4x32_10_kat.txt")[0]
+    assert [int(t, 16) for t in row[:6]] == [0] * 6
+    w0 = int(row[6], 16)
+    want = np.array([-1 if (w0 >> j) & 1 else 1 for j in range(16)], dtype=np.int32)
+    np.testing.assert_array_equal(oracle.rht_signs(0), want)
+    # the 64-bit seed is the key (low word first): seed 2**32 is key (0, 1)
+    w = oracle.philox4x32_10([0, 0, 0, 0], [0, 1])[0]
+    np.testing.assert_array_equal(oracle.rht_signs(2 ** 32),
+                                  [-1 if (w >> j) & 1 else 1 for j in range(16)])
