@@ -12,7 +12,6 @@
 #include <cmath>
 #include <cstring>
 #include <memory>
-#include <mutex>
 #include <vector>
 
 using namespace ufp4;
@@ -361,23 +360,21 @@ ufp4_status ufp4_stats(const void *x, int32_t dtype, int64_t rows, int64_t cols,
 // streams, or different host threads without ordering) race on it.
 namespace {
 constexpr size_t kNoAllocBytes = kWsPartials + size_t(kMaxPartials) * sizeof(float);  // 16,640 B
+// The amax pass's grid is capped at kMaxPartials CTAs (resident_grid in
+// quantize.cu), one partial maximum each, so the array holds every call's
+// scratch whatever the tensor's size.
+static_assert(kNoAllocBytes >= kWsPartials + size_t(kMaxPartials) * sizeof(float),
+              "the no-allocation scratch must hold the status word and kMaxPartials partial maxima");
 static __device__ __align__(256) unsigned char g_ufp4_noalloc_scratch[kNoAllocBytes];
 
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[64] = {nullptr};
-
-// Device address of the scratch array for the current device, looked up once
-// per device (host code only holds a stand-in for the array's name).
+// Device address of the scratch array on the current device.  Host code only
+// holds a stand-in for the array's name, so the address is looked up on every
+// call (a cheap runtime query): nothing is cached that a device reset or a
+// reload of the module could leave stale.
 ufp4_status noalloc_scratch(void **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return UFP4_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_ufp4_noalloc_scratch) != cudaSuccess || !p) return UFP4_ERR_CUDA;
-        g_noalloc_ptr[dev] = p;
-    }
-    *out = g_noalloc_ptr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_ufp4_noalloc_scratch) != cudaSuccess || !p) return UFP4_ERR_CUDA;
+    *out = p;
     return UFP4_OK;
 }
 }  // namespace
@@ -389,10 +386,6 @@ extern "C" ufp4_status ufp4_quantize_noalloc(const void *x, int32_t dtype, int64
     ufp4_status st = check_quant_args(x, dtype, rows, cols, ld, p, out, &q);
     if (st != UFP4_OK) return st;
     if (rows == 0 || cols == 0) return UFP4_OK;
-    // The amax pass never launches more than min(8 x SMs, kMaxPartials) CTAs;
-    // refuse a call whose partial maxima would not fit the array.
-    const int64_t slots = std::min<int64_t>((int64_t)num_sms() * 8, kMaxPartials);
-    if (kWsPartials + (size_t)slots * sizeof(float) > kNoAllocBytes) return UFP4_ERR_INVALID;
     void *scratch = nullptr;
     st = noalloc_scratch(&scratch);
     if (st != UFP4_OK) return st;

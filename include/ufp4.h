@@ -180,11 +180,17 @@ typedef struct {
     uint8_t *eplane;           /* E1M2 correction plane or NULL */
 } ufp4_qtensor;
 
-/* Host-side size helpers (no GPU needed). */
+/* Host-side size helpers (no GPU needed): bytes of the buffers of a
+ * quantized tensor in the layout above.  The pages fix no storage layout;
+ * the sizes follow from the 16-element E4M3 block scaling of the NVFP4
+ * recipe the pages start from ([ZC] Key points, "The symptom") and the
+ * tensor cores' operand and scale layouts. */
 UFP4_API int64_t ufp4_kpad(int64_t k);
 UFP4_API int64_t ufp4_codes_bytes(int64_t rows, int64_t k);
 UFP4_API int64_t ufp4_scales_bytes(int64_t rows, int64_t k);
-/* Bytes of the scratch buffer that ufp4_quantize and ufp4_stats take. */
+/* Bytes of the scratch buffer that ufp4_quantize and ufp4_stats take (the
+ * tensor amax of the two-level scaling needs every element before the first
+ * code, [ZC] "The symptom"; its partial maxima live there). */
 UFP4_API size_t ufp4_workspace_bytes(void);
 
 /* Fused (RHT +) block quantization of one BF16 or FP32 matrix.
@@ -235,11 +241,12 @@ UFP4_API ufp4_status ufp4_quantize_dual(const void *x, int32_t dtype, int64_t ro
  * Arguments and results are exactly those of ufp4_quantize, minus the
  * workspace.  Its scratch -- the amax pass's partial maxima and a status
  * word, 16,640 bytes -- is a fixed array inside the library that every GPU
- * using libufp4 holds until the process exits; it fits every tensor that
- * ufp4_quantize accepts (the amax pass launches at most 4096 CTAs), and a
- * call that would need more is refused with UFP4_ERR_INVALID.  The first call
- * on each device looks up the array's device address, so make that first call
- * before capturing any stream into a CUDA graph.  All calls on a device share
+ * using libufp4 holds until the process exits.  The array always fits: the
+ * amax pass never launches more than 4096 CTAs, one partial maximum each,
+ * whatever the tensor's size, so no size is refused for lack of scratch.
+ * Every call looks up the array's device address on the current device
+ * (cudaGetSymbolAddress; a failure returns UFP4_ERR_CUDA), so a device reset
+ * between calls leaves nothing stale.  All calls on a device share
  * the array and it keeps the last call's contents: calls that overlap on the
  * GPU (other streams, unordered host threads) race and give wrong results.
  * Allocates nothing.  The non-finite status of this variant is not
@@ -248,7 +255,9 @@ UFP4_API ufp4_status ufp4_quantize_noalloc(const void *x, int32_t dtype, int64_t
                                            int64_t ld, const ufp4_qparams *p, const ufp4_qtensor *out,
                                            ufp4_stream_t stream);
 
-/* Reports device-side problems (synchronises `stream`):
+/* Reports device-side problems (synchronises `stream`).  The pages have no
+ * counterpart: this is the library's failure reporting for the kernels of
+ * the calls above.  Returns the first that applies:
  *   UFP4_ERR_TIMEOUT   -- a bounded wait inside a GEMM kernel gave up since
  *                         the last check (the flag is then cleared); that
  *                         GEMM's output is unspecified;
@@ -258,7 +267,11 @@ UFP4_API ufp4_status ufp4_quantize_noalloc(const void *x, int32_t dtype, int64_t
  * `workspace` may be NULL to check only the timeout flag. */
 UFP4_API ufp4_status ufp4_check(const void *workspace, ufp4_stream_t stream);
 
-/* out[r][c] = v(m) * e_b * S_dec as fp32, computed as fl32(fl32(v e_b) S_dec);
+/* Dequantization: the value a code stands for under the two-level scaling,
+ * v(m) the grid value of its magnitude index ([ZC] Key points, "The cause"
+ * for E2M1, "The fix -- UFP4" for E1M2), then, optionally, the inverse of
+ * the orthonormal transform ([ZC] "The RHT paradox").
+ * out[r][c] = v(m) * e_b * S_dec as fp32, computed as fl32(fl32(v e_b) S_dec);
  * with inverse_rht = 1, each 16-block is then rotated back with the signs of
  * rht_seed: x = diag(d) (1/4) H16 y.  out: device fp32, q->rows x q->k, row
  * stride ld_out >= q->k elements, 16-byte aligned, ld_out % 4 == 0. */
@@ -364,7 +377,7 @@ UFP4_API ufp4_status ufp4_stats(const void *x, int32_t dtype, int64_t rows, int6
                        void *workspace, size_t workspace_bytes,
                        ufp4_stats_t *host_out, ufp4_stream_t stream);
 
-/* Static description of a status code. */
+/* Static description of a status code (no counterpart on the pages). */
 UFP4_API const char *ufp4_status_string(ufp4_status s);
 
 #ifdef __cplusplus
