@@ -1,23 +1,31 @@
 """Benchmark of the UFP4 hot path on GB300.
 
-One step = one UFP4 training step of the dense-1.5B-shaped linear layer
-(X 8192 x 2048, W 5632 x 2048, dY 8192 x 5632, BF16, seeded synthetic data):
-six fused RHT + E1M2 quantizations (X, W, dY, each row-wise and
-column-wise; stochastic rounding on dY only) followed by the three training
-GEMMs fwd_y = X W^T, bwd_dx = dY W and bwd_dw = dY^T X.
+Headline (the JSON line's value): one UFP4 training step of the MoE-124B-
+shaped large layer -- X 65536 x 8192, W 2048 x 8192, dY 65536 x 2048, BF16,
+seeded synthetic data -- six fused RHT + E1M2 quantizations (X, W, dY, each
+row-wise and column-wise from one read per pass; stochastic rounding on dY
+only) followed by the three training GEMMs fwd_y = X W^T, bwd_dx = dY W and
+bwd_dw = dY^T X (K = 65536).
 
 Reported (one JSON line from rank 0):
   value         fused RHT+quantize throughput, GB/s of algorithmic traffic
-                (2 B read + 0.5625 B written per element) over the
-                quantization launches of the step (tensor-amax pass included
-                in the time, not in the bytes);
+                (2 B read + 0.5625 B written per element and orientation)
+                over the quantization launches of the step (the tensor-amax
+                pass is in the time, not in the bytes);
   gemm          GEMM TFLOP/s (2 M N K logical flops) and fractions of the
-                FP8 / FP4 dense peaks;
-  roofline      for the dominant kernel by time (the E1M2 GEMM);
+                dense FP8 / FP4 peaks;
+  roofline      the dominant kernel by time (the E1M2 GEMM);
   e2e           the same metric through the public API with the inputs
                 copied from pinned host memory each step and the three GEMM
                 outputs read back;
-  cpu_baseline  the CPU oracle on a bounded sample of the same step.
+  cpu_baseline  the CPU oracle on a bounded sample of the same step;
+  quantizer_x   the single- and dual-orientation quantizer on the layer's X
+                with the transform on and off (the RHT overhead);
+  workloads     every synthetic workload (smoke, outlier, dense-1.5B step,
+                MoE-7.9B grouped step, MoE-124B layer and its compounding
+                chain) with quantizer GB/s and GEMM TFLOP/s as fractions of
+                their rooflines, the numerics the pages discuss, and the
+                oracle timed beside each on a stated sample.
 L2 is flushed before every timed step, outside the events: a 256 MiB buffer
 is written and then read back, so the timed kernels start with an L2 that
 holds none of their data and no dirty lines whose write-back would compete
@@ -40,7 +48,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = dict(name="dense1p5b_linear_train_step", tokens=8192, hidden=2048, ffn=5632)
+WORKLOAD = dict(name="moe124b_layer_train_step", tokens=65536, hidden=8192, ffn=2048)
+DENSE = dict(tokens=8192, hidden=2048, ffn=5632)
 METRIC = ("fused RHT+quantize GB/s (% HBM peak); FP4 GEMM TFLOPS (% tensor peak)")
 Q_BYTES_PER_ELEM = 2.0 + 0.5 + 1.0 / 16.0
 FALLBACK = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
@@ -87,6 +96,16 @@ def weak_scaling_rate(units_per_rank, world, steps, max_ms, scale=1e9):
     """Whole-job throughput: the units all ranks processed over the slowest
     rank's time (each rank runs its own copy of the workload)."""
     return world * steps * units_per_rank / (max_ms * 1e-3) / scale
+
+
+def moe124b_inputs(device, seed=0):
+    """The MoE-124B large layer's operands, drawn on the device from seeded
+    generators: X 65536 x 8192 N(0,1), W 2048 x 8192 N(0,0.01),
+    dY 65536 x 2048 N(0,1e-3), all BF16."""
+    from fp4_quantized_numerics_gb300 import inputs
+    return dict(x=inputs.device_normal((65536, 8192), 1.0, 31 + 10 * seed, device),
+                w=inputs.device_normal((2048, 8192), 0.01, 32 + 10 * seed, device),
+                dy=inputs.device_normal((65536, 2048), 1e-3, 33 + 10 * seed, device))
 
 
 def dist_env():
@@ -225,9 +244,27 @@ class Step:
 
 
 
+def time_steps(step, steps, flush, stream=None):
+    """Times `steps` steps on the current stream (L2 flushed before each,
+    outside the events).  Returns per-step (quantize ms, [gemm ms x 3])."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        e = evs[i]
+        e[0].record()
+        step.quantize_all()
+        e[1].record()
+        step.gemms(events=[None, e[2], e[3], e[4]])
+    torch.cuda.synchronize()
+    q_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    g_ms = [[e[1 + j].elapsed_time(e[2 + j]) for j in range(3)] for e in evs]
+    return q_ms, g_ms
+
+
 def run_gpu(args):
     import torch
-    from fp4_quantized_numerics_gb300 import build, inputs, ufp4 as U
+    from fp4_quantized_numerics_gb300 import build, ufp4 as U
 
     ws_n, rank, local = dist_env()
     if ws_n > 1:
@@ -239,39 +276,24 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     pk = peaks()
 
-    d = inputs.device_dense(seed=rank, tokens=WORKLOAD["tokens"], hidden=WORKLOAD["hidden"],
-                            ffn=WORKLOAD["ffn"], device=dev)
+    d = moe124b_inputs(dev, seed=rank)
     step = Step(U, d["x"], d["w"], d["dy"], U.UFP4_E1M2)
     flush = L2Flush(dev)
-    stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
         step.quantize_all()
         step.gemms()
     torch.cuda.synchronize()
 
-    # per-step events: [start, after quantize, after gemm0, gemm1, gemm2]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     if ws_n > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        t_wall = time.perf_counter()
-        for i in range(args.steps):
-            flush()
-            e = evs[i]
-            e[0].record()
-            step.quantize_all()
-            e[1].record()
-            step.gemms(events=[None, e[2], e[3], e[4]])
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall
+        q_ms, g_ms = time_steps(step, args.steps, flush)
     if ws_n > 1:
         torch.distributed.barrier()
-    q_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    g_ms = [[e[1 + j].elapsed_time(e[2 + j]) for j in range(3)] for e in evs]
-    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
-    tq, tg, tstep = sum(q_ms), sum(sum(g) for g in g_ms), sum(step_ms)
+    tq, tg = sum(q_ms), sum(sum(g) for g in g_ms)
+    tstep = tq + tg
 
     def allmax(v):
         return reduce_max(v, ws_n, dev)
@@ -282,9 +304,14 @@ def run_gpu(args):
     flops = sum(step.flops_each)
     gemm_tflops = weak_scaling_rate(flops, ws_n, args.steps, tg, 1e12)
     per_gpu_tflops = gemm_tflops / ws_n
-    fp8_peak = pk["bf16_tflops"] * 2.0    # nominal dense ratio fp8:bf16 = 4.5 : 2.25
-    fp4_peak = pk["bf16_tflops"] * 6.0    # nominal dense ratio fp4:bf16 = 13.5 : 2.25
+    fp8_sus = pk["bf16_tflops_sustained"] * 2.0   # nominal dense ratio fp8:bf16 = 4.5 : 2.25
+    fp8_burst = pk["bf16_tflops"] * 2.0
+    fp4_sus = pk["bf16_tflops_sustained"] * 6.0   # nominal dense ratio fp4:bf16 = 13.5 : 2.25
     gemm_each = [sum(g[j] for g in g_ms) / args.steps for j in range(3)]
+    launch_ms = tg / (3 * args.steps)             # mean duration of one E1M2 GEMM launch
+    flops_launch = step.flops_each[0]             # the three GEMMs have the same M N K
+    assert all(f == flops_launch for f in step.flops_each)
+    per_launch_tf = flops_launch / (launch_ms * 1e-3) / 1e12
 
     # ---------------------------------------------------- e2e through the API
     e2e = None
@@ -295,24 +322,14 @@ def run_gpu(args):
         del e2e["time_s"]
 
     extra = {}
-    if not args.quick:
-        extra = side_measurements(U, torch, dev, pk, flush)
-        # the same quantize phase with one pass per orientation (six
-        # single-orientation calls instead of three dual ones)
-        single = Step(U, d["x"], d["w"], d["dy"], U.UFP4_E1M2, dual=False)
-        for _ in range(3):
-            single.quantize_all()
-        tot = 0.0
-        for _ in range(20):
-            flush()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(); single.quantize_all(); b.record()
-            torch.cuda.synchronize()
-            tot += a.elapsed_time(b)
-        extra["quantize_step_single_orientation"] = {
-            "gbs": round(q_bytes / (tot / 20 * 1e-3) / 1e9, 1), "ms": round(tot / 20, 4),
-            "launches": single.launches_per_step - 3}
-        del single
+    if not args.quick and rank == 0:
+        extra["quantizer_x_65536x8192"] = quantizer_on_x(U, torch, dev, pk, flush, d["x"])
+    del step, d
+    torch.cuda.empty_cache()
+    if not args.quick and rank == 0:
+        extra["workloads"] = all_workloads(U, torch, dev, pk, flush, with_oracle=not args.no_cpu_baseline)
+    if ws_n > 1:
+        torch.distributed.barrier()
 
     if rank == 0:
         clocks = clk.summary()
@@ -321,27 +338,32 @@ def run_gpu(args):
             "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(tstep / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp32 quantize / e2m1-plane MMA, f32 accumulate",
-            "data": "synthetic (seeded N(0,1)/N(0,0.02)/N(0,1e-3) BF16; 1 outlier column x50)",
+            "data": "synthetic (seeded N(0,1) / N(0,0.01) / N(0,1e-3) BF16, drawn on the device)",
             "config": {"workload": WORKLOAD["name"], "X": [WORKLOAD["tokens"], WORKLOAD["hidden"]],
                        "W": [WORKLOAD["ffn"], WORKLOAD["hidden"]],
                        "dY": [WORKLOAD["tokens"], WORKLOAD["ffn"]],
-                       "recipe": "UFP4: E1M2, RHT16 on all GEMM operands, SR on dY",
+                       "recipe": "UFP4: E1M2, RHT16 on all GEMM operands, SR on dY, both orientations per read",
                        "l2": "flushed before every timed step (256 MiB write, then read back)",
                        "parallelism": "replicas" if ws_n > 1 else "single"},
             "quantize": {"gbs": round(q_gbs, 1), "frac_hbm": round(q_gbs / ws_n / pk["hbm_gbs"], 4),
                          "ms_per_step": round(tq / args.steps, 4),
-                         "elements_per_step": step.q_elems,
-                         "launches_per_step": step.launches_per_step - 3},
+                         "elements_per_step": step_elems(WORKLOAD),
+                         "launches_per_step": 6},
             "gemm": {"tflops": round(gemm_tflops, 1), "ms_per_step": round(tg / args.steps, 4),
                      "ms_each": [round(v, 4) for v in gemm_each],
-                     "frac_fp8_peak": round(per_gpu_tflops / fp8_peak, 4),
-                     "frac_fp4_peak": round(per_gpu_tflops / fp4_peak, 4)},
+                     "frac_fp8_peak_sustained": round(per_gpu_tflops / fp8_sus, 4),
+                     "frac_fp8_peak_burst": round(per_gpu_tflops / fp8_burst, 4),
+                     "frac_fp4_peak_sustained": round(per_gpu_tflops / fp4_sus, 4)},
             "roofline": {"bound": "tensor", "kernel": "k_gemm<E1M2, E planes loaded>",
-                         "achieved": round(per_gpu_tflops, 1), "peak": round(fp8_peak, 1),
-                         "unit": "TFLOP/s", "frac": round(per_gpu_tflops / fp8_peak, 4),
-                         "traffic": traffic_for("k_gemm_e1m2_dense1p5b"),
-                         "peak_kind": "dense FP8 = %s bf16 x 2 (%s)" % ("measured" if pk["source"] == "measured" else "fallback", pk["source"])},
-            "gpu_launches": step.launches_per_step * args.steps,
+                         "achieved": round(per_launch_tf, 1), "peak": round(fp8_sus, 1),
+                         "unit": "TFLOP/s", "frac": round(per_launch_tf / fp8_sus, 4),
+                         "frac_of_burst_peak": round(per_launch_tf / fp8_burst, 4),
+                         "flops_per_launch": flops_launch,
+                         "mean_launch_ms": round(launch_ms, 4),
+                         "traffic": traffic_for("k_gemm_e1m2_moe124b"),
+                         "peak_kind": "dense FP8 = %s sustained bf16 x 2 (timed inside a seconds-long loop of "
+                                      "steps)" % pk["source"]},
+            "gpu_launches": 9 * args.steps,
             "clocks": clocks,
             "peaks": pk,
         }
@@ -353,6 +375,11 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
     if ws_n > 1:
         torch.distributed.destroy_process_group()
+
+
+def step_elems(wl):
+    T, H, F = wl["tokens"], wl["hidden"], wl["ffn"]
+    return 2 * (T * H + F * H + T * F)
 
 
 def run_e2e(args, U, step, d, dev, q_bytes):
@@ -415,97 +442,58 @@ def run_e2e(args, U, step, d, dev, q_bytes):
             "overlap": "2 buffer sets, copy-in / compute / copy-out streams"}
 
 
-def side_measurements(U, torch, dev, pk, flush):
-    """Secondary numbers: RHT on/off overhead of the E1M2 quantizer, the
-    outlier-heavy 4096 x 4096 quantization, and the E2M1 GEMM."""
-    from fp4_quantized_numerics_gb300 import inputs
-
-    def timeit(fn, n=30):
-        # median of n timed runs (each after an L2 flush)
-        fn(); fn(); fn()
+def _timeit(torch, fn, flush, n=10):
+    """Median of n timed runs (each after an L2 flush), after 3 untimed."""
+    fn(); fn(); fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(n):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(); fn(); b.record()
         torch.cuda.synchronize()
-        ts = []
-        for _ in range(n):
-            flush()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(); fn(); b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        return sorted(ts)[len(ts) // 2]
+        ts.append(a.elapsed_time(b))
+    return sorted(ts)[len(ts) // 2]
 
-    out = {}
-    x = inputs.device_normal((8192, 2048), 1.0, 11, dev)
-    # the quantizer alone (codes and scales, no E1M2 correction plane)
-    q = U.QTensor.empty(8192, 2048, U.UFP4_E1M2, dev, eplane=False)
-    amax = torch.ones(1, device=dev)
-    ws = U.workspace(dev)
+
+def quantizer_on_x(U, torch, dev, pk, flush, x):
+    """The fused quantizer on the MoE-124B layer's X (65536 x 8192 BF16,
+    1 GiB), E1M2 RTNE: one orientation with the tensor amax given, transform
+    on and off (the RHT overhead), with the amax pass, with the correction
+    plane written; and both orientations from one read."""
+    R, C = x.shape
     el = x.numel()
+    q = U.QTensor.empty(R, C, U.UFP4_E1M2, dev, eplane=False)
+    qc = U.QTensor.empty(C, R, U.UFP4_E1M2, dev, eplane=False)
+    am = (x.abs().max().float() * 1.25).reshape(1)   # a valid amax, above the rotated maximum
+    ws = U.workspace(dev)
+    gbs = lambda ms, n=1: round(n * el * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
     r = {}
-    for rht in (False, True):
-        for name, am in (("with_amax_pass", None), ("amax_given", amax)):
-            ms = timeit(lambda: U.ufp4_quantize(x, U.UFP4_E1M2, rht=rht, out=q, ws=ws, amax_in=am))
-            r["rht_%s_%s" % ("on" if rht else "off", name)] = round(el * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
-    r["rht_overhead_amax_given"] = round(r["rht_off_amax_given"] / r["rht_on_amax_given"] - 1, 4)
-    r["frac_hbm_rht_on_amax_given"] = round(r["rht_on_amax_given"] / pk["hbm_gbs"], 4)
-    out["quantize_x_8192x2048_gbs"] = r
-
-    # steady state on a large operand (512 MB of BF16): one orientation and
-    # both, transform on, E1M2 RTNE
-    xl = inputs.device_normal((32768, 8192), 1.0, 15, dev)
-    ql = U.QTensor.empty(32768, 8192, U.UFP4_E1M2, dev, eplane=False)
-    qlc = U.QTensor.empty(8192, 32768, U.UFP4_E1M2, dev, eplane=False)
-    aml = torch.tensor([float(xl.float().abs().max()) * 1.25], device=dev)
-    L = {}
-    ms = timeit(lambda: U.ufp4_quantize(xl, U.UFP4_E1M2, rht=True, out=ql, ws=ws, amax_in=aml), 10)
-    L["single_amax_given"] = round(xl.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
-    ms = timeit(lambda: U.ufp4_quantize(xl, U.UFP4_E1M2, rht=False, out=ql, ws=ws, amax_in=aml), 10)
-    L["single_amax_given_rht_off"] = round(xl.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
-    L["rht_overhead_amax_given"] = round(L["single_amax_given_rht_off"] / L["single_amax_given"] - 1, 4)
-    ms = timeit(lambda: U.ufp4_quantize(xl, U.UFP4_E1M2, rht=True, out=ql, ws=ws), 10)
-    L["single_with_amax_pass"] = round(xl.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
-    ms = timeit(lambda: U.ufp4_quantize_dual(xl, U.UFP4_E1M2, rht=True, amax_row=aml, amax_col=aml, out_row=ql,
-                                             out_col=qlc, ws=ws), 10)
-    L["dual_amax_given"] = round(2 * xl.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
-    L["dual_amax_given_dram_gbs"] = round(xl.numel() * (2 + 2 * 0.5625) / (ms * 1e-3) / 1e9, 1)
-    ms = timeit(lambda: U.ufp4_quantize_dual(xl, U.UFP4_E1M2, rht=True, out_row=ql, out_col=qlc, ws=ws), 10)
-    L["dual_with_amax_pass"] = round(2 * xl.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
-    L["frac_hbm_single_amax_given"] = round(L["single_amax_given"] / pk["hbm_gbs"], 4)
-    # the same with the correction plane written too (+0.5 B/elem, not counted)
-    qle = U.QTensor.empty(32768, 8192, U.UFP4_E1M2, dev)
-    ms = timeit(lambda: U.ufp4_quantize(xl, U.UFP4_E1M2, rht=True, out=qle, ws=ws, amax_in=aml), 10)
-    L["single_amax_given_with_eplane"] = round(xl.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
-    del qle
-    out["quantize_large_32768x8192_e1m2_rht_gbs"] = L
-    del xl, ql, qlc
-
-    xo = inputs.device_normal((4096, 4096), 1.0, 12, dev)
-    qo = U.QTensor.empty(4096, 4096, U.UFP4_E2M1, dev)
-    qo1 = U.QTensor.empty(4096, 4096, U.UFP4_E1M2, dev, eplane=False)
-    o = {}
-    for g, qq in ((U.UFP4_E2M1, qo), (U.UFP4_E1M2, qo1)):
-        ms = timeit(lambda: U.ufp4_quantize(xo, g, rht=True, out=qq, ws=ws))
-        o["e2m1" if g == 0 else "e1m2"] = round(xo.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 1)
-    out["quantize_outlier_4096x4096_rht_gbs"] = o
-
-    # E2M1 GEMM at the fwd_y shape
-    a = U.ufp4_quantize(inputs.device_normal((8192, 2048), 1.0, 13, dev), U.UFP4_E2M1)
-    b = U.ufp4_quantize(inputs.device_normal((5632, 2048), 0.02, 14, dev), U.UFP4_E2M1)
-    c = torch.empty(8192, 5632, dtype=torch.float32, device=dev)
-    ms = timeit(lambda: U.ufp4_gemm(a, b, out=c))
-    tf = 2 * 8192 * 5632 * 2048 / (ms * 1e-3) / 1e12
-    out["gemm_e2m1_fwd_y"] = {"tflops": round(tf, 1), "frac_fp4_peak": round(tf / (pk["bf16_tflops"] * 6), 4),
-                              "output_bytes_bound_tflops": round(2 * 2048 / 4 * pk["hbm_gbs"] / 1e3, 1)}
-    # E1M2 at the fwd_y shape: correction planes loaded vs expanded on chip
-    a = U.ufp4_quantize(inputs.device_normal((8192, 2048), 1.0, 13, dev), U.UFP4_E1M2, rht=True)
-    b = U.ufp4_quantize(inputs.device_normal((5632, 2048), 0.02, 14, dev), U.UFP4_E1M2, rht=True)
-    e = {}
-    for name, (qa, qb) in (("eplanes_loaded", (a, b)),
-                           ("expanded_on_chip", tuple(U.QTensor(t.codes, t.scales, t.tensor_scale, t.rows, t.k,
-                                                                t.grid) for t in (a, b)))):
-        ms = timeit(lambda: U.ufp4_gemm(qa, qb, out=c))
-        e[name] = round(2 * 8192 * 5632 * 2048 / (ms * 1e-3) / 1e12, 1)
-    out["gemm_e1m2_fwd_y_tflops"] = e
-    return out
+    r["single_amax_given_rht_on"] = gbs(_timeit(torch, lambda: U.ufp4_quantize(
+        x, U.UFP4_E1M2, rht=True, out=q, ws=ws, amax_in=am), flush))
+    r["single_amax_given_rht_off"] = gbs(_timeit(torch, lambda: U.ufp4_quantize(
+        x, U.UFP4_E1M2, rht=False, out=q, ws=ws, amax_in=am), flush))
+    r["rht_overhead_amax_given"] = round(r["single_amax_given_rht_off"] / r["single_amax_given_rht_on"] - 1, 4)
+    r["frac_hbm_single_amax_given_rht_on"] = round(r["single_amax_given_rht_on"] / pk["hbm_gbs"], 4)
+    r["single_with_amax_pass_rht_on"] = gbs(_timeit(torch, lambda: U.ufp4_quantize(
+        x, U.UFP4_E1M2, rht=True, out=q, ws=ws), flush))
+    r["single_amax_given_rht_off_colwise"] = gbs(_timeit(torch, lambda: U.ufp4_quantize(
+        x, U.UFP4_E1M2, rht=False, colwise=True, out=qc, ws=ws, amax_in=am), flush))
+    r["single_amax_given_rht_on_colwise"] = gbs(_timeit(torch, lambda: U.ufp4_quantize(
+        x, U.UFP4_E1M2, rht=True, colwise=True, out=qc, ws=ws, amax_in=am), flush))
+    r["dual_amax_given_rht_on"] = gbs(_timeit(torch, lambda: U.ufp4_quantize_dual(
+        x, U.UFP4_E1M2, rht=True, amax_row=am, amax_col=am, out_row=q, out_col=qc, ws=ws), flush), 2)
+    r["dual_amax_given_rht_off"] = gbs(_timeit(torch, lambda: U.ufp4_quantize_dual(
+        x, U.UFP4_E1M2, rht=False, amax_row=am, amax_col=am, out_row=q, out_col=qc, ws=ws), flush), 2)
+    r["dual_with_amax_pass_rht_on"] = gbs(_timeit(torch, lambda: U.ufp4_quantize_dual(
+        x, U.UFP4_E1M2, rht=True, out_row=q, out_col=qc, ws=ws), flush), 2)
+    del q, qc
+    qe = U.QTensor.empty(R, C, U.UFP4_E1M2, dev)
+    r["single_amax_given_rht_on_with_eplane"] = gbs(_timeit(torch, lambda: U.ufp4_quantize(
+        x, U.UFP4_E1M2, rht=True, out=qe, ws=ws, amax_in=am), flush))
+    r["note"] = ("GB/s of algorithmic traffic (2.5625 B per element and result); the amax pass's "
+                 "second read and the correction plane's writes are not counted")
+    return r
 
 
 def traffic_for(key):
@@ -527,16 +515,34 @@ def traffic_for(key):
 
 
 # ------------------------------------------------------------ CPU oracle
-def cpu_sample(rows_x=2048, rows_dy=2048, gemm_rows=32):
-    """The oracle on a bounded sample of the step: RHT + E1M2 row-wise
-    quantization of the first rows of X and of dY (SR), and gemm_rows rows of
-    fwd_y in fp64.  Returns (quantize GB/s, GEMM GFLOP/s, seconds, desc)."""
+def _oracle_quant_rate(fn, elems):
+    t0 = time.perf_counter()
+    fn()
+    dt = time.perf_counter() - t0
+    return elems * Q_BYTES_PER_ELEM / dt / 1e9, dt
+
+
+def _oracle_gemm_rate(a, b):
+    from oracle import oracle
+    t0 = time.perf_counter()
+    oracle.gemm_f64(a, b)
+    dt = time.perf_counter() - t0
+    return 2.0 * a.shape[0] * b.shape[0] * a.shape[1] / dt / 1e9, dt
+
+
+def cpu_sample(rows_x=8192, rows_dy=16384, gemm_rows=16, seed=0):
+    """The oracle on a bounded sample of the MoE-124B step: RHT + E1M2
+    row-wise quantization of rows_x rows of X (65536 x 8192 in full) and of
+    rows_dy rows of dY (SR), and gemm_rows rows of fwd_y in fp64 against the
+    whole quantized W.  Returns (quantize GB/s, GEMM GFLOP/s, seconds, desc,
+    extrapolated seconds of the full step)."""
     from fp4_quantized_numerics_gb300 import inputs
     from oracle import oracle
-    g = np.random.default_rng(0)
-    x = inputs.to_bf16_f32(g.standard_normal((rows_x, WORKLOAD["hidden"]), dtype=np.float32))
-    dy = inputs.to_bf16_f32(g.standard_normal((rows_dy, WORKLOAD["ffn"]), dtype=np.float32) * np.float32(1e-3))
-    w = inputs.to_bf16_f32(g.standard_normal((WORKLOAD["ffn"], WORKLOAD["hidden"]), dtype=np.float32) * np.float32(0.02))
+    T, H, F = WORKLOAD["tokens"], WORKLOAD["hidden"], WORKLOAD["ffn"]
+    g = inputs.rng(seed)
+    x = inputs.to_bf16_f32(g.standard_normal((rows_x, H), dtype=np.float32))
+    dy = inputs.to_bf16_f32(g.standard_normal((rows_dy, F), dtype=np.float32) * np.float32(1e-3))
+    w = inputs.to_bf16_f32(g.standard_normal((F, H), dtype=np.float32) * np.float32(0.01))
     t0 = time.perf_counter()
     rx = oracle.quantize(x, oracle.E1M2, rht=True, rht_seed=2)
     oracle.quantize(dy, oracle.E1M2, rht=True, rht_seed=2, round_mode=oracle.SR, sr_seed=3)
@@ -544,27 +550,35 @@ def cpu_sample(rows_x=2048, rows_dy=2048, gemm_rows=32):
     rw = oracle.quantize(w, oracle.E1M2, rht=True, rht_seed=2)
     A = oracle.dequantize(rx["codes"][:gemm_rows], rx["scales"][:gemm_rows], rx["tensor_scale"], oracle.E1M2)
     B = oracle.dequantize(rw["codes"], rw["scales"], rw["tensor_scale"], oracle.E1M2)
-    t1 = time.perf_counter()
-    oracle.gemm_f64(A, B)
-    tg = time.perf_counter() - t1
+    gflops, tg = _oracle_gemm_rate(A, B)
     el = x.size + dy.size
-    flops = 2.0 * gemm_rows * w.shape[0] * w.shape[1]
+    qgbs = el * Q_BYTES_PER_ELEM / tq / 1e9
+    full = step_elems(WORKLOAD) * Q_BYTES_PER_ELEM / (qgbs * 1e9) + 3 * 2.0 * T * H * F / (gflops * 1e9)
     desc = ("RHT+E1M2 row-wise quantization of %d x %d of X and %d x %d of dY (SR), "
-            "plus %d rows of fwd_y in fp64" % (rows_x, WORKLOAD["hidden"], rows_dy, WORKLOAD["ffn"], gemm_rows))
-    return el * Q_BYTES_PER_ELEM / tq / 1e9, flops / tg / 1e9, tq + tg, desc
+            "plus %d rows of fwd_y in fp64 (K = %d)" % (rows_x, H, rows_dy, F, gemm_rows, H))
+    return qgbs, gflops, tq + tg, desc, full
 
 
 def cpu_baseline(args):
-    gbs, gflops, secs, desc = cpu_sample()
+    gbs, gflops, secs, desc, full = cpu_sample()
     return {"value": round(gbs, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": desc, "gemm_gflops": round(gflops, 3), "seconds": round(secs, 2),
-            "host": host_desc()}
+            "full_step_seconds_extrapolated": round(full, 1), "host": host_desc()}
 
 
 def host_desc():
     try:
         import platform
-        return "%s, %d logical cores" % (platform.machine(), os.cpu_count() or 0)
+        model = ""
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+            for l in out.splitlines():
+                if l.startswith("Model name"):
+                    model = l.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+        return "%s %s, %d logical cores (the oracle uses 1)" % (platform.machine(), model, os.cpu_count() or 0)
     except Exception:
         return None
 
@@ -576,7 +590,7 @@ def run_reference(args):
     t_all = 0.0
     vals = []
     for i in range(args.warmup + args.steps):
-        gbs, gflops, secs, desc = cpu_sample(rows_x=256, rows_dy=256, gemm_rows=4)
+        gbs, gflops, secs, desc, _ = cpu_sample(rows_x=256, rows_dy=512, gemm_rows=4, seed=i)
         if i >= args.warmup:
             t_all += secs
             vals.append(gbs)
@@ -587,23 +601,25 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32 (CPU oracle)",
             "data": "synthetic", "config": {"workload": WORKLOAD["name"]},
             "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": desc},
+                             "sample": desc, "host": host_desc()},
             "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 def run_kernel(args):
-    """One kernel of the step in isolation, for profiling: `steps` launches
-    of the fwd_y GEMM (8192 x 5632 x 2048), of the RHT quantization of X
-    (8192 x 2048) in one orientation or both (quant_dual_*; the SR variant
-    quantizes dY, 8192 x 5632), after `warmup` launches, the tensor amax
-    given.  Prints the mean event time."""
+    """One kernel of a step in isolation, for profiling: `steps` launches of
+    the fwd_y GEMM (T x F x H), of the RHT quantization of X (T x H) in one
+    orientation or both (quant_dual_*; the SR variant quantizes dY, T x F),
+    after `warmup` launches, the tensor amax given.  --shape dense: T, H, F =
+    8192, 2048, 5632; moe124b: 65536, 8192, 2048.  Prints the mean event
+    time."""
     import torch
     from fp4_quantized_numerics_gb300 import build, inputs, ufp4 as U
     build.build()
     dev = torch.device("cuda", 0)
-    T, H, F = WORKLOAD["tokens"], WORKLOAD["hidden"], WORKLOAD["ffn"]
+    wl = WORKLOAD if args.shape == "moe124b" else DENSE
+    T, H, F = wl["tokens"], wl["hidden"], wl["ffn"]
     x = inputs.device_normal((T, H), 1.0, 21, dev)
     kind = args.kernel
     if kind.startswith("gemm"):
@@ -619,7 +635,7 @@ def run_kernel(args):
         grid = U.UFP4_E1M2
         sr = kind.startswith("quant_dual_sr")
         src = inputs.device_normal((T, F), 1e-3, 23, dev) if sr else x
-        am = torch.tensor([float(src.float().abs().max()) * 1.5], device=dev)
+        am = (src.abs().max().float() * 1.5).reshape(1)
         qr = U.QTensor.empty(src.shape[0], src.shape[1], grid, dev)
         qc = U.QTensor.empty(src.shape[1], src.shape[0], grid, dev)
         kw = dict(round=U.UFP4_SR, sr_seed=3) if sr else {}
@@ -631,7 +647,7 @@ def run_kernel(args):
         grid = U.UFP4_E2M1 if kind.endswith("e2m1") else U.UFP4_E1M2
         col = kind.startswith("quant_col")
         q = U.QTensor.empty(H if col else T, T if col else H, grid, dev)
-        am = torch.tensor([float(x.float().abs().max()) * 1.5], device=dev)
+        am = (x.abs().max().float() * 1.5).reshape(1)
         fn = lambda: U.ufp4_quantize(x, grid, rht=True, colwise=col, out=q, amax_in=am)
         work = x.numel() * Q_BYTES_PER_ELEM
         unit = "GB/s"
@@ -655,45 +671,71 @@ def run_kernel(args):
 # ------------------------------------------------------------ all workloads
 def _ev_time(fn, flush, reps=10):
     import torch
-    fn()
-    torch.cuda.synchronize()
-    tot = 0.0
-    for _ in range(reps):
-        flush()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(); fn(); b.record()
-        torch.cuda.synchronize()
-        tot += a.elapsed_time(b)
-    return tot / reps
+    return _timeit(torch, fn, flush, reps)
 
 
-def run_workloads(args):
-    """Every synthetic workload at 1 GPU: quantizer GB/s, GEMM TFLOP/s and the
-    numerics the pages discuss (alpha, SQNR, bias, prod eta).  One JSON line
-    per workload."""
-    import torch
-    from fp4_quantized_numerics_gb300 import build, inputs, ufp4 as U
-    build.build()
-    dev = torch.device("cuda", 0)
-    pk = peaks()
-    flush = L2Flush(dev)
-    out = []
+def _fracs(pk, q_gbs=None, tflops=None, grid=None, gemm_bytes=None, gemm_flops=None):
+    """Roofline fractions: the quantizer against HBM, a GEMM against the
+    dense tensor peak of its grid's MMA (E1M2: FP8, as the recipe's target
+    states; E2M1: FP4) and, for E2M1, against max(flop time, byte time)."""
+    out = {}
+    if q_gbs is not None:
+        out["quantize_frac_hbm"] = round(q_gbs / pk["hbm_gbs"], 4)
+    if tflops is not None:
+        fp8, fp4 = 2.0 * pk["bf16_tflops"], 6.0 * pk["bf16_tflops"]
+        if grid == 1:
+            out["gemm_frac_fp8_dense"] = round(tflops / fp8, 4)
+        else:
+            out["gemm_frac_fp4_dense"] = round(tflops / fp4, 4)
+            if gemm_bytes and gemm_flops:
+                # the fastest the GEMM could run: tensor time or HBM time, whichever is longer
+                t_min = max(gemm_flops / (fp4 * 1e12), gemm_bytes / (pk["hbm_gbs"] * 1e9))
+                t_run = gemm_flops / (tflops * 1e12)
+                out["gemm_combined_roofline_tflops"] = round(gemm_flops / t_min / 1e12, 1)
+                out["gemm_frac_combined_roofline"] = round(t_min / t_run, 4)
+    return out
 
-    def emit(d):
-        print(json.dumps(d), flush=True)
-        out.append(d)
+
+def _gemm_bytes(M, N, K):
+    """Algorithmic bytes of one GEMM: both quantized operands (0.5 B codes +
+    1/16 B scale per element) and the fp32 output."""
+    return (M + N) * K * 0.5625 + 4.0 * M * N
+
+
+def all_workloads(U, torch, dev, pk, flush, with_oracle=True):
+    """Every synthetic workload at 1 GPU: quantizer GB/s and GEMM TFLOP/s
+    with their roofline fractions, the numerics the pages discuss (alpha,
+    SQNR, mean bias, prod eta), and the CPU oracle timed beside each on the
+    stated sample (1 core; full-workload time extrapolated from the sample's
+    rate)."""
+    from fp4_quantized_numerics_gb300 import inputs
+    out = {}
+    o = None
+    if with_oracle:
+        from oracle import oracle as o
+
+    def oracle_q(x, elems_full, desc, **kw):
+        if o is None:
+            return None
+        gbs, dt = _oracle_quant_rate(lambda: o.quantize(x, **kw), x.size)
+        return {"quantize_gbs": round(gbs, 5), "seconds": round(dt, 2), "cores": 1, "sample": desc,
+                "full_quantize_seconds_extrapolated": round(elems_full * Q_BYTES_PER_ELEM / (gbs * 1e9), 1)}
 
     def stats_of(x, grid, rht):
         q = U.ufp4_quantize(x, grid, rht=rht, rht_seed=2)
         st = U.ufp4_stats(x, q, rht=rht, rht_seed=2)
         return {k: round(st[k], 6) for k in ("alpha", "sqnr_db", "mean_bias")}
 
-    # smoke: 256 x 1024 tensor, 256^3 GEMM
+    # ---- smoke: 256 x 1024 tensor, 256^3 GEMM (launch-bound; reported)
     d = inputs.smoke(0)
     x = torch.from_numpy(d["x"]).to(torch.bfloat16).to(dev)
     a = torch.from_numpy(d["a"]).to(torch.bfloat16).to(dev)
     b = torch.from_numpy(d["b"]).to(torch.bfloat16).to(dev)
-    r = {"workload": "smoke_256x1024", "numerics": {}}
+    r = {"config": "BF16 256 x 1024 N(0,1); GEMM 256^3", "numerics": {}}
+    q = U.QTensor.empty(256, 1024, U.UFP4_E1M2, dev)
+    ms = _ev_time(lambda: U.ufp4_quantize(x, U.UFP4_E1M2, rht=True, rht_seed=2, out=q), flush)
+    r["quantize_e1m2_rht_gbs"] = round(x.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 2)
+    r.update(_fracs(pk, q_gbs=r["quantize_e1m2_rht_gbs"]))
     for g, gn in ((0, "e2m1"), (1, "e1m2"), (2, "e2m1c")):
         for rht in (False, True):
             r["numerics"]["%s_rht_%s" % (gn, "on" if rht else "off")] = stats_of(x, g, rht)
@@ -703,40 +745,74 @@ def run_workloads(args):
         r["gemm_%s_tflops" % gn] = round(2 * 256 ** 3 / (ms * 1e-3) / 1e12, 3)
     for rht in (False, True):   # MXFP4: quantization numerics only (no GEMM)
         r["numerics"]["mxfp4_rht_%s" % ("on" if rht else "off")] = stats_of(x, U.UFP4_MXFP4, rht)
-    emit(r)
+    r["note"] = "0.67 MB of input: launch latency, not HBM, bounds it"
+    if o is not None:
+        r["oracle"] = oracle_q(d["x"], d["x"].size, "the whole 256 x 1024 tensor, RHT + E1M2",
+                               grid=1, rht=True, rht_seed=2)
+        qa, qb = o.quantize(d["a"], 1), o.quantize(d["b"], 1)
+        gf, dt = _oracle_gemm_rate(o.dequantize(qa["codes"], qa["scales"], qa["tensor_scale"], 1),
+                                   o.dequantize(qb["codes"], qb["scales"], qb["tensor_scale"], 1))
+        r["oracle"]["gemm_gflops"] = round(gf, 3)
+    out["smoke_256x1024"] = r
 
-    # outlier: 4096 x 4096, RHT on/off, both grids
+    # ---- outlier: 4096 x 4096, RHT on/off, every grid
     d = inputs.outlier(0)
     x = torch.from_numpy(d["x"]).to(torch.bfloat16).to(dev)
-    r = {"workload": "outlier_4096x4096", "numerics": {}, "quantize_gbs": {}}
+    r = {"config": "BF16 4096 x 4096 N(0,1) + column offsets N(0,0.5), 4 columns x100", "numerics": {},
+         "quantize_gbs": {}}
     for g, gn in ((0, "e2m1"), (1, "e1m2"), (2, "e2m1c"), (3, "mxfp4")):
         # MXFP4 moves 2 + 0.5 + 1/32 B/elem (one E8M0 byte per 32 elements)
         bpe = 2.53125 if g == U.UFP4_MXFP4 else Q_BYTES_PER_ELEM
         for rht in (False, True):
             key = "%s_rht_%s" % (gn, "on" if rht else "off")
             r["numerics"][key] = stats_of(x, g, rht)
-            q = U.QTensor.empty(4096, 4096, g, dev)
-            ms = _ev_time(lambda: U.ufp4_quantize(x, g, rht=rht, rht_seed=2, out=q), flush)
+            qq = U.QTensor.empty(4096, 4096, g, dev, eplane=False)
+            ms = _ev_time(lambda: U.ufp4_quantize(x, g, rht=rht, rht_seed=2, out=qq), flush)
             r["quantize_gbs"][key] = round(x.numel() * bpe / (ms * 1e-3) / 1e9, 1)
+    r["quantize_frac_hbm"] = {k: round(v / pk["hbm_gbs"], 4) for k, v in r["quantize_gbs"].items()}
     n = r["numerics"]
     r["sqnr_ranking"] = {
         "before_rht_e2m1_minus_e1m2_db": round(n["e2m1_rht_off"]["sqnr_db"] - n["e1m2_rht_off"]["sqnr_db"], 3),
         "after_rht_e2m1_minus_e1m2_db": round(n["e2m1_rht_on"]["sqnr_db"] - n["e1m2_rht_on"]["sqnr_db"], 3)}
-    emit(r)
+    r["note"] = "43 MB of input (amax pass + quantization pass per call): the whole call's time"
+    if o is not None:
+        r["oracle"] = oracle_q(d["x"][:512], d["x"].size, "512 of the 4096 rows, RHT + E1M2",
+                               grid=1, rht=True, rht_seed=2)
+    out["outlier_4096x4096"] = r
 
-    # dense 1.5B training step: UFP4 on both grids, and the NVFP4 policy
-    # (E2M1, the transform only on the bwd_dw operands) the pages compare with
+    # ---- dense 1.5B training step: UFP4 on both grids, and the NVFP4 policy
+    T, H, F = DENSE["tokens"], DENSE["hidden"], DENSE["ffn"]
     dd = inputs.device_dense(seed=0, device=dev)
+    r = {"config": "X 8192 x 2048 (1 column x50), W 5632 x 2048, dY 8192 x 5632; 3 GEMMs of 189 GFLOP"}
     for g, gn, pol in ((1, "e1m2", "ufp4"), (0, "e2m1", "ufp4"), (0, "nvfp4_policy", "nvfp4")):
         st = Step(U, dd["x"], dd["w"], dd["dy"], g, policy=pol)
         mq = _ev_time(st.quantize_all, flush)
         mg = _ev_time(st.gemms, flush)
-        emit({"workload": "dense1p5b_step_" + gn, "quantize_ms": round(mq, 4),
-              "quantize_gbs": round(st.q_elems * Q_BYTES_PER_ELEM / (mq * 1e-3) / 1e9, 1),
-              "gemm_ms": round(mg, 4), "gemm_tflops": round(sum(st.flops_each) / (mg * 1e-3) / 1e12, 1)})
+        qg = st.q_elems * Q_BYTES_PER_ELEM / (mq * 1e-3) / 1e9
+        tf = sum(st.flops_each) / (mg * 1e-3) / 1e12
+        e = {"quantize_ms": round(mq, 4), "quantize_gbs": round(qg, 1), "gemm_ms": round(mg, 4),
+             "gemm_tflops": round(tf, 1)}
+        e.update(_fracs(pk, qg, tf, g, 3 * _gemm_bytes(T, F, H), sum(st.flops_each)))
+        r[gn] = e
+        del st
     del dd
+    if o is not None:
+        g = inputs.rng(0)
+        xs = inputs.to_bf16_f32(g.standard_normal((1024, H), dtype=np.float32))
+        dys = inputs.to_bf16_f32(g.standard_normal((1024, F), dtype=np.float32) * np.float32(1e-3))
+        full = 2 * (T * H + F * H + T * F)
+        r["oracle"] = oracle_q(xs, full, "1024 rows of X, RHT + E1M2 (and the GEMM: 8 rows of fwd_y)",
+                               grid=1, rht=True, rht_seed=2)
+        ws_ = inputs.to_bf16_f32(g.standard_normal((F, H), dtype=np.float32) * np.float32(0.02))
+        qa, qb = o.quantize(xs[:8], 1, rht=True, rht_seed=2), o.quantize(ws_, 1, rht=True, rht_seed=2)
+        gf, _ = _oracle_gemm_rate(o.dequantize(qa["codes"], qa["scales"], qa["tensor_scale"], 1),
+                                  o.dequantize(qb["codes"], qb["scales"], qb["tensor_scale"], 1))
+        r["oracle"]["gemm_gflops"] = round(gf, 3)
+        r["oracle"]["full_gemm_seconds_extrapolated"] = round(3 * 2.0 * T * H * F / (gf * 1e9), 1)
+        del dys
+    out["dense1p5b_step"] = r
 
-    # MoE 7.9B grouped step
+    # ---- MoE 7.9B grouped step
     m = inputs.moe(seed=0)
     counts = [int(c) for c in m["counts"]]
     E, H, F = len(counts), 2048, 1408
@@ -745,6 +821,9 @@ def run_workloads(args):
     tdy = torch.from_numpy(m["dy"]).to(torch.bfloat16).to(dev)
     T = sum(counts)
     starts = np.concatenate([[0], np.cumsum(counts)])
+    r = {"config": "64 experts, 16384 tokens x top-6 = %d routed rows (Dirichlet(1) routing, %d empty experts); "
+                   "per expert X_e [T_e x 2048], W_e [1408 x 2048], dY_e [T_e x 1408]"
+                   % (T, sum(1 for c in counts if c == 0))}
     for g, gn in ((1, "e1m2"), (0, "e2m1")):
         kw = dict(rht=True, rht_seed=2)
         qs = {}
@@ -778,30 +857,42 @@ def run_workloads(args):
         mg = _ev_time(gemm_all, flush, 5)
         elems = 2 * (tx.numel() + tw.numel() + tdy.numel())
         flops = 3 * 2.0 * T * F * H
-        emit({"workload": "moe7p9b_grouped_step_" + gn, "experts": E, "routed_tokens": T,
-              "zero_token_experts": int(sum(1 for c in counts if c == 0)),
-              "quantize_ms": round(mq, 4), "quantize_gbs": round(elems * Q_BYTES_PER_ELEM / (mq * 1e-3) / 1e9, 1),
-              "gemm_ms": round(mg, 4), "gemm_tflops": round(flops / (mg * 1e-3) / 1e12, 1)})
+        qg = elems * Q_BYTES_PER_ELEM / (mq * 1e-3) / 1e9
+        tf = flops / (mg * 1e-3) / 1e12
+        e = {"quantize_ms": round(mq, 4), "quantize_gbs": round(qg, 1), "gemm_ms": round(mg, 4),
+             "gemm_tflops": round(tf, 1)}
+        e.update(_fracs(pk, qg, tf, g, 3 * sum(_gemm_bytes(c, F, H) for c in counts), flops))
+        r[gn] = e
+        del qs, y, dx, dw
+    if o is not None:
+        seg = m["x"][:4096]
+        full = 2 * (tx.numel() + tw.numel() + tdy.numel())
+        r["oracle"] = oracle_q(seg, full, "4096 routed rows of X (the first segments), RHT + E1M2",
+                               grid=1, rht=True, rht_seed=2)
     del tx, tw, tdy, m
+    torch.cuda.empty_cache()
+    out["moe7p9b_grouped_step"] = r
 
-    # MoE 124B large layer
-    x = inputs.device_normal((65536, 8192), 1.0, 31, dev)
-    w = inputs.device_normal((2048, 8192), 0.01, 32, dev)
-    dy = inputs.device_normal((65536, 2048), 1e-3, 33, dev)
-    for g, gn in ((1, "e1m2"), (0, "e2m1")):
-        st = Step(U, x, w, dy, g)
-        mq = _ev_time(st.quantize_all, flush, 3)
-        mg = _ev_time(st.gemms, flush, 3)
-        emit({"workload": "moe124b_layer_" + gn, "quantize_ms": round(mq, 4),
-              "quantize_gbs": round(st.q_elems * Q_BYTES_PER_ELEM / (mq * 1e-3) / 1e9, 1),
-              "gemm_ms": round(mg, 4), "gemm_tflops": round(sum(st.flops_each) / (mg * 1e-3) / 1e12, 1)})
-        del st
-    del x, w, dy
+    # ---- MoE 124B large layer on the E2M1 grid (the E1M2 step is the headline)
+    d = moe124b_inputs(dev)
+    T, H, F = WORKLOAD["tokens"], WORKLOAD["hidden"], WORKLOAD["ffn"]
+    st = Step(U, d["x"], d["w"], d["dy"], U.UFP4_E2M1)
+    mq = _ev_time(st.quantize_all, flush, 3)
+    mg = _ev_time(st.gemms, flush, 3)
+    qg = st.q_elems * Q_BYTES_PER_ELEM / (mq * 1e-3) / 1e9
+    tf = sum(st.flops_each) / (mg * 1e-3) / 1e12
+    e = {"quantize_ms": round(mq, 4), "quantize_gbs": round(qg, 1), "gemm_ms": round(mg, 4),
+         "gemm_tflops": round(tf, 1)}
+    e.update(_fracs(pk, qg, tf, 0, 3 * _gemm_bytes(T, F, H), sum(st.flops_each)))
+    out["moe124b_layer_e2m1"] = dict(config="the headline layer on the E2M1 grid (UFP4 recipe otherwise)", **e)
+    del st, d
     torch.cuda.empty_cache()
 
-    # compounding-attenuation chain: 100 x (4096^3), fresh W_k ~ N(0, 1/64)
+    # ---- compounding-attenuation chain: 100 x (4096^3), fresh W_k ~ N(0, 1/64)
     n, steps = 4096, 100
     rows = torch.arange(0, n, n // 64, device=dev)
+    r = {"config": "100 sequential 4096^3 GEMMs, X_0 N(0,1), W_k N(0,1/64) BF16, each output re-quantized "
+                   "from fp32; eta on 64 sampled rows against the fp64 product"}
     for g, gn in ((0, "e2m1"), (1, "e1m2"), (2, "e2m1c")):
         for rht in (False, True):
             X = inputs.device_normal((n, n), 1.0, 50, dev, dtype=torch.float32)
@@ -829,13 +920,22 @@ def run_workloads(args):
                 sum_delta += 1.0 - eta
                 ln_alpha += float(np.log(ax * aw))
                 X, Y = Y, X
-            emit({"workload": "attenuation_chain_4096_x100_%s_rht_%s" % (gn, "on" if rht else "off"),
-                  "prod_eta": round(float(np.exp(ln_prod)), 6), "exp_minus_sum_delta": round(float(np.exp(-sum_delta)), 6),
-                  "prod_alpha_x_alpha_w": round(float(np.exp(ln_alpha)), 6),
-                  "norm_ratio": round(float(X.double().norm()) / norm0, 6),
-                  "gpu_ms_per_layer": round(t_gpu / steps, 4),
-                  "layer_tflops": round(2.0 * n ** 3 / (t_gpu / steps * 1e-3) / 1e12, 1)})
+            r["%s_rht_%s" % (gn, "on" if rht else "off")] = {
+                "prod_eta": round(float(np.exp(ln_prod)), 6),
+                "exp_minus_sum_delta": round(float(np.exp(-sum_delta)), 6),
+                "prod_alpha_x_alpha_w": round(float(np.exp(ln_alpha)), 6),
+                "norm_ratio": round(float(X.double().norm()) / norm0, 6),
+                "gpu_ms_per_layer": round(t_gpu / steps, 4),
+                "layer_tflops": round(2.0 * n ** 3 / (t_gpu / steps * 1e-3) / 1e12, 1)}
+            del X, Y, qx, qw
+    if o is not None:
+        Xh = inputs.rng(50).standard_normal((512, n), dtype=np.float32)
+        r["oracle"] = oracle_q(Xh, steps * 2 * n * n, "512 rows of an fp32 4096-wide X, RHT + E1M2",
+                               grid=1, rht=True, rht_seed=2)
+    out["attenuation_chain_4096_x100"] = r
+    torch.cuda.empty_cache()
     return out
+
 
 def main():
     ap = argparse.ArgumentParser()
@@ -843,11 +943,12 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--quick", action="store_true", help="skip the secondary measurements")
+    ap.add_argument("--quick", action="store_true",
+                    help="skip the secondary measurements (the quantizer on X and the five workloads)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workloads", action="store_true",
-                    help="measure every synthetic workload (one JSON line each) instead of the step")
+    ap.add_argument("--shape", default="dense", choices=["dense", "moe124b"],
+                    help="layer shape of --kernel")
     ap.add_argument("--kernel", default=None,
                     choices=["gemm_e2m1", "gemm_e1m2", "quant_row_e1m2", "quant_col_e1m2", "quant_dual_e1m2",
                              "quant_dual_sr_e1m2",
@@ -860,8 +961,6 @@ def main():
         run_reference(args)
     elif args.kernel:
         run_kernel(args)
-    elif args.workloads:
-        run_workloads(args)
     else:
         run_gpu(args)
 

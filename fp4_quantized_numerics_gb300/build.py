@@ -44,13 +44,21 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src, extra):
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-    if _stale(obj, [src] + _headers()):
+def _compile(src, extra, build_dir=BUILD, deps=()):
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
+    if _stale(obj, [src] + _headers() + list(deps)):
         cmd = [nvcc(), *NVCC_FLAGS, *extra, "-c", src, "-o", obj + ".tmp"]
         subprocess.check_call(cmd)
         os.replace(obj + ".tmp", obj)
     return obj
+
+
+def _link(lib, objs):
+    if _stale(lib, objs):
+        tmp = lib + ".tmp.%d" % os.getpid()
+        subprocess.check_call([nvcc(), *ARCH, "-shared", "-o", tmp, *objs])
+        os.replace(tmp, lib)
+    return lib
 
 
 def build(verbose=False, extra_flags=()):
@@ -59,13 +67,30 @@ def build(verbose=False, extra_flags=()):
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(lambda s: _compile(s, list(extra_flags)), srcs))
-    if _stale(LIB, objs):
-        tmp = LIB + ".tmp.%d" % os.getpid()
-        subprocess.check_call([nvcc(), *ARCH, "-shared", "-o", tmp, *objs])
-        os.replace(tmp, LIB)
+    _link(LIB, objs)
     if verbose:
         print(LIB)
     return LIB
+
+
+def build_variant(lib, build_dir, flags, sources, include_dir):
+    """A test-only variant of the library: `sources` (file names under csrc/)
+    recompiled with `flags` and -I include_dir (whose files they may include)
+    into build_dir, linked with the library's other objects into `lib`.
+    Builds the library's objects first.  Returns the variant's path."""
+    os.makedirs(build_dir, exist_ok=True)
+    deps = glob.glob(os.path.join(include_dir, "*"))
+    extra = list(flags) + ["-I", include_dir]
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    mine = [s for s in srcs if os.path.basename(s) in sources]
+    # the library and the variant's own objects compile side by side
+    with cf.ThreadPoolExecutor(max_workers=1 + len(mine)) as ex:
+        lib_job = ex.submit(build)
+        jobs = {s: ex.submit(_compile, s, extra, build_dir, deps) for s in mine}
+        lib_job.result()
+        objs = [jobs[s].result() if s in jobs else os.path.join(BUILD, os.path.basename(s) + ".o")
+                for s in srcs]
+    return _link(lib, objs)
 
 
 if __name__ == "__main__":

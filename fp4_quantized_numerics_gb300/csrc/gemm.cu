@@ -128,6 +128,8 @@ struct GemmParams {
     int ntm, ntn; // tiles along M and N
     int nkt_a, nkt_b;  // k atoms per 128-row tile of the whole A / B tensors
     int b_rt;     // 128-row scale tiles in the whole B tensor
+    long long budget;  // clock cycles a role waits for another before it gives up
+    int stall;         // test-only build: the MMA thread waits on a barrier nobody arrives on
 };
 
 // Where one output tile lives: operand rows / k atoms in the A and B tensors,
@@ -192,7 +194,8 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const GroupGe
 __device__ __forceinline__ void raise_timeout() { atomicOr(&g_ufp4_timeout, 1u); }
 
 // Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort) {
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort,
+                                              long long budget) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
@@ -200,7 +203,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
         for (int i = 0; i < 64; ++i)
             if (ptx::mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (clock64() - t0 > kWaitBudget) {
+        if (clock64() - t0 > budget) {
             *abort = 1;
             raise_timeout();
             return false;
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                 const bool b_hi = ti.b_row / 128 + 1 < p.b_rt;
                 for (int kb = 0; kb < ti.num_kb; ++kb, ++g) {
                     const uint32_t s = g % S, round = g / S;
-                    if (round > 0 && !wait_or_abort(empty(s), (round - 1) & 1, abort)) { ok = false; break; }
+                    if (round > 0 && !wait_or_abort(empty(s), (round - 1) & 1, abort, p.budget)) { ok = false; break; }
                     const uint32_t atoms = (uint32_t)min(C::kKS, ti.nkt - C::kKS * kb);
                     const uint32_t st = smem_base + s * C::kStageBytes;
                     ptx::mbar_arrive_expect_tx(full(s), C::kABytes + C::kBBytes + C::kPlaneBytes +
@@ -359,23 +362,28 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
             auto mk = [](uint64_t hi, uint32_t addr) { return hi | (uint64_t)((addr & 0x3FFFFu) >> 4); };
             uint32_t g = 0, it = 0;
             bool ok = true;
+#ifdef UFP4_PROBE
+            // test-only build: a wait that nothing ends ("drained" is committed
+            // only below), so the timeout path runs
+            if (p.stall && !wait_or_abort(drained, 0u, abort, p.budget)) ok = false;
+#endif
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
                 const TileInfo ti = tile_info<C::kKS>(p, tab, t);
                 // the epilogue must have read the previous tile out of the accumulator
-                if (it > 0 && !wait_or_abort(acce, (it - 1) & 1, abort)) { ok = false; break; }
+                if (it > 0 && !wait_or_abort(acce, (it - 1) & 1, abort, p.budget)) { ok = false; break; }
                 ptx::tc_fence_after();
                 for (int kb = 0; kb < ti.num_kb; ++kb, ++g) {
                     const uint32_t s = g % S, round = g / S;
                     const uint32_t e = g % ES, eround = g / ES;
                     // operands landed and (scale warp) scales in TMEM
-                    if (!wait_or_abort(full(s), round & 1, abort) ||
-                        (C::kScaleWarps > 0 && !wait_or_abort(sfr(s), round & 1, abort))) { ok = false; break; }
+                    if (!wait_or_abort(full(s), round & 1, abort, p.budget) ||
+                        (C::kScaleWarps > 0 && !wait_or_abort(sfr(s), round & 1, abort, p.budget))) { ok = false; break; }
                     ptx::tc_fence_after();
                     const int atoms = min(C::kKS, ti.nkt - C::kKS * kb);
                     if constexpr (GRID == kE1M2) {
                         // scale copies queued while the expanders finish the E planes
                         copy_scales(s, atoms, false);
-                        if (!wait_or_abort(expd(e), eround & 1, abort)) { ok = false; break; }
+                        if (!wait_or_abort(expd(e), eround & 1, abort, p.budget)) { ok = false; break; }
                         ptx::tc_fence_after();
                     }
                     const uint32_t st = smem_base + s * C::kStageBytes;
@@ -440,7 +448,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
         uint32_t it = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
-            bool ok = wait_or_abort(accf, it & 1, abort);
+            bool ok = wait_or_abort(accf, it & 1, abort, p.budget);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             ptx::tc_fence_after();
@@ -605,7 +613,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                 const TileInfo ti = tile_info<C::kKS>(p, tab, t);
                 for (int kb = 0; kb < ti.num_kb; ++kb, ++g) {
                     const uint32_t s = g % S, round = g / S;
-                    if (!wait_or_abort(full(s), round & 1, abort)) { ok = false; break; }
+                    if (!wait_or_abort(full(s), round & 1, abort, p.budget)) { ok = false; break; }
                     copy_scales(s, min(C::kKS, ti.nkt - C::kKS * kb), true);
                 }
             }
@@ -625,9 +633,9 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
             for (int kb = 0; kb < nkb; ++kb, ++g) {
                 const uint32_t s = g % S, round = g / S;
                 const uint32_t e = g % ES, eround = g / ES;
-                ok = wait_or_abort(full(s), round & 1, abort);
+                ok = wait_or_abort(full(s), round & 1, abort, p.budget);
                 // the MMAs that last read this E slot have completed
-                if (ok && eround > 0) ok = wait_or_abort(efree(e), (eround - 1) & 1, abort);
+                if (ok && eround > 0) ok = wait_or_abort(efree(e), (eround - 1) & 1, abort, p.budget);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 const uint4 *src = reinterpret_cast<const uint4 *>(smem + s * C::kStageBytes + C::kAOff);
@@ -654,6 +662,11 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
 }
 
 // ------------------------------------------------------------ host side
+// Wait budget of the GEMM roles (and the test-only stall switch); a test-only
+// build of the library can change them, libufp4 keeps the defaults.
+long long g_wait_budget = kWaitBudget;
+int g_stall = 0;
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -754,6 +767,8 @@ cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_eplane, const u
     p.ntn = (int)((N + BN - 1) / BN);
     p.nkt_a = p.nkt_b = p.nkt;
     p.b_rt = (int)((N + 127) / 128);
+    p.budget = g_wait_budget;
+    p.stall = g_stall;
     const NoGroups none;
     // clamped-E2M1 codes are E2M1 codes
     if (grid != kE1M2) return run_gemm<kE2M1>(ma, mb, mea, meb, mc, p, none, p.ntm * p.ntn, s);
@@ -787,6 +802,8 @@ cudaError_t launch_gemm_grouped(const uint8_t *a_codes, const uint8_t *a_eplane,
     p.nkt_b = (int)(b_kpad / 64);
     p.b_rt = (int)((b_rows + 127) / 128);
     p.M = 1; p.N = 1;
+    p.budget = g_wait_budget;
+    p.stall = g_stall;
     const int ntiles = tab.tiles[tab.n];
     if (grid != kE1M2) return run_gemm<kE2M1>(ma, mb, mea, meb, mc, p, tab, ntiles, s);
     if (planes) return run_gemm<kE1M2Pl>(ma, mb, mea, meb, mc, p, tab, ntiles, s);
@@ -820,3 +837,7 @@ cudaError_t read_timeout_flag(uint32_t *flag, cudaStream_t s) {
 }
 
 }  // namespace ufp4
+
+#ifdef UFP4_PROBE
+#include "probe_gemm.inc"
+#endif

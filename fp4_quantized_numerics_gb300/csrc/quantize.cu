@@ -67,6 +67,18 @@ struct Args {
     uint32_t utop;
 };
 
+// A test-only build (-DUFP4_PROBE, tests/probe) records the values each
+// quantization path hands to its block scale -- the rotated y when the
+// transform is on -- so that tests can compare them element by element; in
+// the library these hooks are empty.
+#ifdef UFP4_PROBE
+#include "probe_hooks.inc"
+#else
+#define UFP4_PROBE_ROW8(a, r, b, lo, hi, rht) ((void)0)
+#define UFP4_PROBE_ROW16(a, r, b, v, rht) ((void)0)
+#define UFP4_PROBE_COL16(a, c, kb, v, rht) ((void)0)
+#endif
+
 // ------------------------------------------------------------------ loads
 // 8 consecutive elements as fp32, sign-flipped by the 8-bit mask `sflip`
 // (bit j set: negate element j).
@@ -86,17 +98,6 @@ __device__ __forceinline__ void load8(const float *p, uint32_t sflip, float v[8]
     const float t[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(__float_as_uint(t[i]) ^ (((sflip >> i) & 1u) << 31));
-}
-
-// 4 consecutive columns of one row as fp32 (no sign flip: column-wise signs
-// depend on the row, applied by the caller).
-__device__ __forceinline__ void load4(const __nv_bfloat16 *p, float v[4]) {
-    const uint2 w = *reinterpret_cast<const uint2 *>(p);
-    v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2] = bf16lo(w.y); v[3] = bf16hi(w.y);
-}
-__device__ __forceinline__ void load4(const float *p, float v[4]) {
-    const float4 a = *reinterpret_cast<const float4 *>(p);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
 }
 
 // Row-wise unit values: the lane pair (2i, 2i+1) holds one 16-block, lane
@@ -337,11 +338,12 @@ template <> __device__ __forceinline__ Signs col_signs<float>(uint32_t smask) {
 template <class In> struct Raw;
 template <> struct Raw<__nv_bfloat16> {
     uint32_t w[8];
+    // 16-byte loads: a row of a strided input is only 16-byte aligned
     __device__ __forceinline__ void load(const __nv_bfloat16 *p) {
-        asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
-                       "=r"(w[6]), "=r"(w[7])
-                     : "l"(p));
+        asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "l"(p));
+        asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]) : "l"(p + 8));
     }
     __device__ __forceinline__ void zero() {
 #pragma unroll
@@ -365,15 +367,13 @@ template <> struct Raw<__nv_bfloat16> {
 };
 template <> struct Raw<float> {
     uint32_t w[16];
+    // 16-byte loads: a row of a strided input is only 16-byte aligned
     __device__ __forceinline__ void load(const float *p) {
-        asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
-                       "=r"(w[6]), "=r"(w[7])
-                     : "l"(p));
-        asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                     : "=r"(w[8]), "=r"(w[9]), "=r"(w[10]), "=r"(w[11]), "=r"(w[12]), "=r"(w[13]),
-                       "=r"(w[14]), "=r"(w[15])
-                     : "l"(p + 8));
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            asm volatile("ld.global.nc.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(w[4 * q]), "=r"(w[4 * q + 1]), "=r"(w[4 * q + 2]), "=r"(w[4 * q + 3])
+                         : "l"(p + 4 * q));
     }
     __device__ __forceinline__ void zero() {
 #pragma unroll
@@ -595,6 +595,7 @@ __device__ __forceinline__ void quant_block_row(const Args &a, const Raw<In> &ra
     const float qmax = GRID == kE2M1 ? 6.0f : a.uqmax;
     float lo[8], hi[8];
     block_values<In, RHT>(raw, sg, lo, hi);
+    UFP4_PROBE_ROW8(a, r, b, lo, hi, RHT);
     float m = 0.0f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) m = fmaxf(m, fmaxf(fabsf(lo[j]), fabsf(hi[j])));
@@ -642,6 +643,8 @@ __device__ __forceinline__ void quant_pair_row(const Args &a, const Raw<__nv_bfl
         ma = fmaxf(ma, fabsf(va[j]));
         mb = fmaxf(mb, fabsf(vb[j]));
     }
+    UFP4_PROBE_ROW16(a, r0, b0, va, RHT);
+    if (has_b) UFP4_PROBE_ROW16(a, r1, b1, vb, RHT);
     if (RHT) { ma *= 0.25f; mb *= 0.25f; }
     const uint32_t ea = block_scale(ma, qmax, S_enc), eb = block_scale(mb, qmax, S_enc);
     const uint64_t K2 = pk2(s_k[ea], s_k[eb]);
@@ -854,6 +857,10 @@ __device__ __forceinline__ void col_unit_words(const Args &a, const ColRaw<In> &
         upk2(P[i], v0[i], v1[i]);
         m0 = fmaxf(m0, fabsf(v0[i]));
         m1 = fmaxf(m1, fabsf(v1[i]));
+    }
+    if (real) {
+        UFP4_PROBE_COL16(a, c, kb, v0, RHT);
+        UFP4_PROBE_COL16(a, c + 1, kb, v1, RHT);
     }
     if (RHT) { m0 *= 0.25f; m1 *= 0.25f; }
     uint32_t e0 = block_scale(m0, qmax, S_enc), e1 = block_scale(m1, qmax, S_enc);
@@ -2478,3 +2485,7 @@ cudaError_t launch_stats(const QuantLaunch &q, void *ws, int *n_ctas, cudaStream
 }
 
 }  // namespace ufp4
+
+#ifdef UFP4_PROBE
+#include "probe_entry.inc"
+#endif

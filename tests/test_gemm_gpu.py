@@ -1,15 +1,19 @@
 """GPU parity of the block-scaled FP4 GEMMs against the oracle's fp64 product.
 
-Both sides quantize the same inputs (the oracle with its own code); with RHT
+Both sides quantize the same inputs (the oracle with its own code).  With RHT
 off the codes are bit-exact, so the oracle's fp64 product of its dequantized
-operands is the exact value of the GPU's product.  Bar: relative Frobenius
-error <= 1e-5 (fp32 accumulation in the tensor cores).
+operands is the exact value of the GPU's product.  With RHT on, the GPU's
+codes first pass the code bar against the oracle's (at most 1e-4 one grid
+step apart), and the GEMM is compared with the fp64 product of the operands
+it consumed: the GPU's codes and scales, dequantized by the oracle.  Bar:
+relative Frobenius error <= 1e-5 (fp32 accumulation in the tensor cores).
 """
 import numpy as np
 import pytest
 import torch
 
 from fp4_quantized_numerics_gb300 import inputs
+from tests import layouts, parity
 
 pytestmark = pytest.mark.gpu
 
@@ -28,6 +32,15 @@ def _rel_fro(c, ref):
     return float(np.linalg.norm(c - ref) / max(np.linalg.norm(ref), 1e-300))
 
 
+def consumed(oracle, q):
+    """fp64 values of the operand a GPU GEMM consumed: the GPU's codes,
+    scales and tensor scale, dequantized by the oracle."""
+    torch.cuda.synchronize()
+    codes = layouts.unpack_codes(q.codes.cpu().numpy(), q.rows, q.k)
+    scales, _ = layouts.unpack_scales(q.scales.cpu().numpy(), q.rows, q.k)
+    return codes, oracle.dequantize(codes, scales, float(q.tensor_scale[0].item()), q.grid)
+
+
 def _gemm_case(U, oracle, a, b, grid, rht=False, col_a=False, col_b=False, round_a=0):
     ta = torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).cuda()
     tb = torch.from_numpy(np.ascontiguousarray(b)).to(torch.bfloat16).cuda()
@@ -37,8 +50,17 @@ def _gemm_case(U, oracle, a, b, grid, rht=False, col_a=False, col_b=False, round
     torch.cuda.synchronize()
     ra = oracle.quantize(a, grid, rht=rht, rht_seed=2, colwise=col_a, round_mode=round_a, sr_seed=3)
     rb = oracle.quantize(b, grid, rht=rht, rht_seed=2, colwise=col_b)
-    A = oracle.dequantize(ra["codes"], ra["scales"], ra["tensor_scale"], grid)
-    B = oracle.dequantize(rb["codes"], rb["scales"], rb["tensor_scale"], grid)
+    if rht:
+        # the codes the kernel consumed, at the code bar against the oracle's
+        ca, A = consumed(oracle, qa)
+        cb, B = consumed(oracle, qb)
+        tally = parity.CodeTally()
+        tally.add(ca, ra["codes"])
+        tally.add(cb, rb["codes"])
+        tally.check()
+    else:
+        A = oracle.dequantize(ra["codes"], ra["scales"], ra["tensor_scale"], grid)
+        B = oracle.dequantize(rb["codes"], rb["scales"], rb["tensor_scale"], grid)
     ref = oracle.gemm_f64(A, B)
     return c.cpu().numpy().astype(np.float64), ref
 
@@ -61,31 +83,35 @@ def test_ragged_and_multistage(U, oracle, grid, M, N, K):
 
 
 @pytest.mark.parametrize("grid", [0, 1])
-def test_training_orientations(U, oracle, grid):
+@pytest.mark.parametrize("rht", [False, True])
+def test_training_orientations(U, oracle, grid, rht):
     """fwd_y = X W^T, bwd_dx = dY W (B = W column-wise), bwd_dw = dY^T X
-    (both operands column-wise), with SR on dY as in the recipe."""
+    (both operands column-wise), with SR on dY as in the recipe, the
+    transform off and on (UFP4 rotates the operands of all three GEMMs)."""
     T, H, F = 192, 256, 320
     x = inputs.normal(43, (T, H))
     w = inputs.normal(44, (F, H), std=0.02)
     dy = inputs.normal(45, (T, F), std=1e-3)
-    c, ref = _gemm_case(U, oracle, x, w, grid)                                   # fwd_y
+    c, ref = _gemm_case(U, oracle, x, w, grid, rht=rht)                                   # fwd_y
     assert c.shape == (T, F) and _rel_fro(c, ref) <= TOL
-    c, ref = _gemm_case(U, oracle, dy, w, grid, col_b=True, round_a=1)          # bwd_dx
+    c, ref = _gemm_case(U, oracle, dy, w, grid, rht=rht, col_b=True, round_a=1)          # bwd_dx
     assert c.shape == (T, H) and _rel_fro(c, ref) <= TOL
-    c, ref = _gemm_case(U, oracle, dy, x, grid, col_a=True, col_b=True, round_a=1)  # bwd_dw
+    c, ref = _gemm_case(U, oracle, dy, x, grid, rht=rht, col_a=True, col_b=True, round_a=1)  # bwd_dw
     assert c.shape == (F, H) and _rel_fro(c, ref) <= TOL
 
 
-@pytest.mark.parametrize("grid", [0, 1])
-def test_rht_gemm_close_to_unrotated_product(U, oracle, grid):
-    """With the same signs on both operands the rotation cancels in A B^T; the
-    GPU result must stay close to the oracle's quantized RHT product (codes
-    may differ in <= 1e-4 of the elements)."""
-    d = inputs.smoke(0)
-    c, ref = _gemm_case(U, oracle, d["a"], d["b"], grid, rht=True)
-    assert _rel_fro(c, ref) <= 1e-3
-    exact = d["a"].astype(np.float64) @ d["b"].astype(np.float64).T
-    assert _rel_fro(c, exact) <= (0.2 if grid == 0 else 0.15)
+@pytest.mark.parametrize("grid", [0, 1, 2])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (300, 200, 320), (130, 140, 4160)])
+def test_rht_gemm_matches_consumed_operands(U, oracle, grid, M, N, K):
+    """RHT on: 1e-5 against the fp64 product of the operands consumed, and,
+    since the same signs rotate both operands, close to the unrotated
+    product of the BF16 inputs (the quantization error only)."""
+    a = inputs.normal(46, (M, K))
+    b = inputs.normal(47, (N, K))
+    c, ref = _gemm_case(U, oracle, a, b, grid, rht=True)
+    assert _rel_fro(c, ref) <= TOL
+    exact = a.astype(np.float64) @ b.astype(np.float64).T
+    assert _rel_fro(c, exact) <= {0: 0.2, 1: 0.15, 2: 0.3}[grid]
 
 
 def test_gemm_k_zero_writes_zeros(U):
