@@ -630,12 +630,13 @@ def run_kernel(args):
         fn = lambda: U.ufp4_gemm(a, b, out=c)
         work = 2.0 * T * F * H
         unit = "TFLOP/s"
-    elif kind.startswith("quant_dual"):
-        # both orientations from one read; SR variant on the dY shape
+    elif kind.startswith("quant_dual") or kind == "amax_dual_e1m2":
+        # both orientations from one read; SR variant on the dY shape; the
+        # amax variant computes the tensor maxima (its amax pass is profiled)
         grid = U.UFP4_E1M2
         sr = kind.startswith("quant_dual_sr")
         src = inputs.device_normal((T, F), 1e-3, 23, dev) if sr else x
-        am = (src.abs().max().float() * 1.5).reshape(1)
+        am = None if kind == "amax_dual_e1m2" else (src.abs().max().float() * 1.5).reshape(1)
         qr = U.QTensor.empty(src.shape[0], src.shape[1], grid, dev)
         qc = U.QTensor.empty(src.shape[1], src.shape[0], grid, dev)
         kw = dict(round=U.UFP4_SR, sr_seed=3) if sr else {}
@@ -892,7 +893,8 @@ def all_workloads(U, torch, dev, pk, flush, with_oracle=True):
     n, steps = 4096, 100
     rows = torch.arange(0, n, n // 64, device=dev)
     r = {"config": "100 sequential 4096^3 GEMMs, X_0 N(0,1), W_k N(0,1/64) BF16, each output re-quantized "
-                   "from fp32; eta on 64 sampled rows against the fp64 product"}
+                   "from fp32 with its tensor amax taken from the GEMM epilogue (ufp4_gemm_amax); eta on 64 "
+                   "sampled rows against the fp64 product"}
     for g, gn in ((0, "e2m1"), (1, "e1m2"), (2, "e2m1c")):
         for rht in (False, True):
             X = inputs.device_normal((n, n), 1.0, 50, dev, dtype=torch.float32)
@@ -901,14 +903,16 @@ def all_workloads(U, torch, dev, pk, flush, with_oracle=True):
             qx = U.QTensor.empty(n, n, g, dev)
             qw = U.QTensor.empty(n, n, g, dev)
             Y = torch.empty(n, n, device=dev)
+            amax = torch.empty(1, device=dev)
             t_gpu = 0.0
             for k in range(steps):
                 W = inputs.device_normal((n, n), 1.0 / 64, 1000 + k, dev)
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
-                U.ufp4_quantize(X, g, rht=rht, rht_seed=2, out=qx)
+                # each output's amax comes from the GEMM epilogue that wrote it
+                U.ufp4_quantize(X, g, rht=rht, rht_seed=2, out=qx, amax_in=amax if k > 0 else None)
                 U.ufp4_quantize(W, g, rht=rht, rht_seed=2, out=qw)
-                U.ufp4_gemm(qx, qw, out=Y)
+                U.ufp4_gemm_amax(qx, qw, rht=rht, rht_seed=2, out=Y, amax=amax)
                 e1.record()
                 torch.cuda.synchronize()
                 t_gpu += e0.elapsed_time(e1)
@@ -951,7 +955,7 @@ def main():
                     help="layer shape of --kernel")
     ap.add_argument("--kernel", default=None,
                     choices=["gemm_e2m1", "gemm_e1m2", "quant_row_e1m2", "quant_col_e1m2", "quant_dual_e1m2",
-                             "quant_dual_sr_e1m2",
+                             "quant_dual_sr_e1m2", "amax_dual_e1m2",
                              "quant_row_e2m1", "quant_col_e2m1"],
                     help="time one kernel of the step in isolation (profiling)")
     args = ap.parse_args()

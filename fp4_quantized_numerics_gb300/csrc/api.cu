@@ -186,6 +186,23 @@ ufp4_status ufp4_gemm(const ufp4_qtensor *a, const ufp4_qtensor *b, float *c, in
                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
+ufp4_status ufp4_gemm_amax(const ufp4_qtensor *a, const ufp4_qtensor *b, float *c, int64_t ldc, int32_t rht,
+                           uint64_t rht_seed, float *c_amax, ufp4_stream_t stream) {
+    if (!valid_qtensor(a) || !valid_qtensor(b)) return UFP4_ERR_INVALID;
+    if (a->k != b->k || (rht != 0 && rht != 1) || !c_amax || !aligned(c_amax, 4)) return UFP4_ERR_INVALID;
+    if (a->grid != b->grid || a->grid == UFP4_MXFP4) return UFP4_ERR_UNSUPPORTED;
+    const int64_t M = a->rows, N = b->rows, K = a->k;
+    if (rht && N % UFP4_BLOCK != 0) return UFP4_ERR_INVALID;
+    if (M == 0 || N == 0) {
+        return from_cuda(cudaMemsetAsync(c_amax, 0, sizeof(float), reinterpret_cast<cudaStream_t>(stream)));
+    }
+    if (!c || !aligned(c, 16) || ldc < N || ldc % 4 != 0) return UFP4_ERR_INVALID;
+    if (!within_limits(M, K) || !within_limits(N, K)) return UFP4_ERR_UNSUPPORTED;
+    return from_cuda(launch_gemm(a->codes, a->eplane, a->scales, a->tensor_scale, b->codes, b->eplane, b->scales,
+                                 b->tensor_scale, M, N, K, a->grid, c, ldc,
+                                 reinterpret_cast<cudaStream_t>(stream), c_amax, rht, rht_seed));
+}
+
 int64_t ufp4_grouped_rows(const int64_t *seg_rows, int32_t n_seg) {
     if (!seg_rows || n_seg <= 0) return 0;
     int64_t t = 0;
@@ -308,6 +325,43 @@ ufp4_status ufp4_gemm_grouped(const ufp4_qtensor *a, const ufp4_qtensor *b, cons
                                          a->grid, *tab, s));
 }
 
+// Host fp64 reduction of n sets of 8 partial sums into the statistics.
+static ufp4_stats_t reduce_stats(const double *part, int n) {
+    double s[5] = {0, 0, 0, 0, 0};
+    for (int i = 0; i < n; ++i)
+        for (int j = 0; j < 5; ++j) s[j] += part[(size_t)i * 8 + j];
+    ufp4_stats_t r{};
+    r.sum_aq = s[0]; r.sum_aa = s[1]; r.sum_err2 = s[2]; r.bias_count = s[4];
+    r.alpha = s[1] > 0 ? s[0] / s[1] : 1.0;
+    r.sqnr_db = s[2] > 0 ? 10.0 * std::log10(s[1] / s[2]) : INFINITY;
+    r.mean_bias = s[4] > 0 ? s[3] / s[4] : 0.0;
+    return r;
+}
+
+ufp4_status ufp4_quantize_stats(const void *x, int32_t dtype, int64_t rows, int64_t cols, int64_t ld,
+                                const ufp4_qparams *p, const ufp4_qtensor *out, void *workspace,
+                                size_t workspace_bytes, ufp4_stats_t *host_out, ufp4_stream_t stream) {
+    if (!host_out) return UFP4_ERR_INVALID;
+    QuantLaunch q;
+    ufp4_status st = check_quant_args(x, dtype, rows, cols, ld, p, out, &q);
+    if (st != UFP4_OK) return st;
+    if (!valid_workspace(workspace, workspace_bytes)) return UFP4_ERR_INVALID;
+    std::vector<double> part;
+    int n = 0;
+    if (rows > 0 && cols > 0) {
+        cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+        cudaError_t e = launch_quantize_stats(q, workspace, &n, cs);
+        if (e != cudaSuccess) return from_cuda(e);
+        part.resize((size_t)n * 8);
+        e = cudaMemcpyAsync(part.data(), static_cast<char *>(workspace) + kWsStats, part.size() * sizeof(double),
+                            cudaMemcpyDeviceToHost, cs);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+        if (e != cudaSuccess) return UFP4_ERR_CUDA;
+    }
+    *host_out = reduce_stats(part.data(), n);
+    return UFP4_OK;
+}
+
 ufp4_status ufp4_stats(const void *x, int32_t dtype, int64_t rows, int64_t cols, int64_t ld,
                        const ufp4_qparams *p, const ufp4_qtensor *qt, void *workspace,
                        size_t workspace_bytes, ufp4_stats_t *host_out, ufp4_stream_t stream) {
@@ -316,26 +370,19 @@ ufp4_status ufp4_stats(const void *x, int32_t dtype, int64_t rows, int64_t cols,
     ufp4_status st = check_quant_args(x, dtype, rows, cols, ld, p, qt, &q);
     if (st != UFP4_OK) return st;
     if (!valid_workspace(workspace, workspace_bytes)) return UFP4_ERR_INVALID;
-    double s[5] = {0, 0, 0, 0, 0};
+    std::vector<double> part;
+    int n = 0;
     if (rows > 0 && cols > 0) {
         cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-        int n = 0;
         cudaError_t e = launch_stats(q, workspace, &n, cs);
         if (e != cudaSuccess) return from_cuda(e);
-        std::vector<double> part((size_t)n * 8);
+        part.resize((size_t)n * 8);
         e = cudaMemcpyAsync(part.data(), static_cast<char *>(workspace) + kWsStats,
                             part.size() * sizeof(double), cudaMemcpyDeviceToHost, cs);
         if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
         if (e != cudaSuccess) return UFP4_ERR_CUDA;
-        for (int i = 0; i < n; ++i)
-            for (int j = 0; j < 5; ++j) s[j] += part[(size_t)i * 8 + j];
     }
-    ufp4_stats_t r{};
-    r.sum_aq = s[0]; r.sum_aa = s[1]; r.sum_err2 = s[2]; r.bias_count = s[4];
-    r.alpha = s[1] > 0 ? s[0] / s[1] : 1.0;
-    r.sqnr_db = s[2] > 0 ? 10.0 * std::log10(s[1] / s[2]) : INFINITY;
-    r.mean_bias = s[4] > 0 ? s[3] / s[4] : 0.0;
-    *host_out = r;
+    *host_out = reduce_stats(part.data(), n);
     return UFP4_OK;
 }
 

@@ -130,12 +130,18 @@ struct GemmParams {
     int b_rt;     // 128-row scale tiles in the whole B tensor
     long long budget;  // clock cycles a role waits for another before it gives up
     int stall;         // test-only build: the MMA thread waits on a barrier nobody arrives on
+    int splits;        // K halves per output tile (1 or 2); 2: partial sums added into a zeroed C
+    int col_major;     // tile order: 1 = down the M tiles first (when M < N), 0 = along the N tiles first
+    float *c_amax;     // or null: raised to the tensor amax of C's row-wise quantization
+    int amax_rht;      // ... of the rotated C (16-blocks along N)
+    uint64_t amax_seed;
 };
 
 // Where one output tile lives: operand rows / k atoms in the A and B tensors,
 // its problem's sizes, output pointer and tensor scales.
 struct TileInfo {
     int a_row, b_row, a_kt, b_kt, nkt, num_kb;
+    int kb0, kb1;   // the K stages [kb0, kb1) of this work unit
     int m_loc, n_loc, M, N;
     float *c;
     int64_t ldc;
@@ -144,11 +150,23 @@ struct TileInfo {
 
 struct NoGroups {};
 
+// Work unit u of a dense GEMM: K part u / tiles (outermost, so that one
+// round of the persistent grid covers twice the tiles of a K half), then the
+// tile, numbered along the dimension whose operand is smaller: a round of
+// CTAs then shares the bigger operand's few tiles through L2 and re-reads only
+// the smaller one (row-major tiles when M >= N, column-major when M < N).
 template <int KS>
-__device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const NoGroups &, int t) {
+__device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const NoGroups &, int u) {
     TileInfo ti;
-    ti.m_loc = (t / p.ntn) * BM;
-    ti.n_loc = (t % p.ntn) * BN;
+    const int ntiles = p.ntm * p.ntn;
+    const int part = u / ntiles, t = u - part * ntiles;
+    const int per = (p.num_kb + p.splits - 1) / p.splits;
+    ti.kb0 = part * per;
+    ti.kb1 = min(p.num_kb, ti.kb0 + per);
+    const int mt = p.col_major ? t % p.ntm : t / p.ntn;
+    const int nt = p.col_major ? t / p.ntm : t % p.ntn;
+    ti.m_loc = mt * BM;
+    ti.n_loc = nt * BN;
     ti.a_row = ti.m_loc;
     ti.b_row = ti.n_loc;
     ti.a_kt = 0;
@@ -182,6 +200,8 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const GroupGe
     ti.b_kt = g.b_kt;
     ti.nkt = g.nkt;
     ti.num_kb = (g.nkt + KS - 1) / KS;
+    ti.kb0 = 0;
+    ti.kb1 = ti.num_kb;
     ti.M = g.M;
     ti.N = g.N;
     ti.c = g.c;
@@ -192,6 +212,67 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const GroupGe
 }
 
 __device__ __forceinline__ void raise_timeout() { atomicOr(&g_ufp4_timeout, 1u); }
+
+// Epilogue amax: the running maximum over 16 consecutive output values of a
+// row, c_j = (acc_j * kfix) * alpha exactly as stored.  Without the transform
+// max |c_j|; with it max |4 y| for y = (1/4) H16 diag(d) c, computed with the
+// same fp32 butterflies in the same order as the quantizer's row-wise path
+// (pairs (c_j, c_{j+8}), index bits 0..2 on f32x2, then the halves), so that
+// 0.25 * the maximum is bit for bit the tensor amax that ufp4_quantize of C
+// would compute.  NaN propagates.
+__device__ __forceinline__ float max_nan2(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float out_block_amax(const uint32_t *w, float kfix, float alpha, bool rht,
+                                                uint32_t smask, float m) {
+    float c[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) c[j] = __uint_as_float(w[j]) * kfix * alpha;
+    if (!rht) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) m = max_nan2(m, fabsf(c[j]));
+        return m;
+    }
+    float a[8], b[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        a[j] = __uint_as_float(__float_as_uint(c[j]) ^ (((smask >> j) & 1u) << 31));
+        b[j] = __uint_as_float(__float_as_uint(c[j + 8]) ^ (((smask >> (j + 8)) & 1u) << 31));
+    }
+#pragma unroll
+    for (int st = 1; st < 8; st <<= 1) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if ((j & st) == 0) {
+                const float a0 = a[j], a1 = a[j + st], b0 = b[j], b1 = b[j + st];
+                a[j] = __fadd_rn(a0, a1);
+                a[j + st] = __fsub_rn(a0, a1);
+                b[j] = __fadd_rn(b0, b1);
+                b[j + st] = __fsub_rn(b0, b1);
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        m = max_nan2(m, fabsf(__fadd_rn(a[j], b[j])));
+        m = max_nan2(m, fabsf(__fsub_rn(a[j], b[j])));
+    }
+    return m;
+}
+
+// Warp maximum of the lanes' running maxima into *dst (a non-negative float,
+// or NaN, as int bits: the order of non-negative IEEE floats is that of their
+// bit patterns).
+__device__ __forceinline__ void flush_amax(float *dst, float m, bool rht, int lane) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = max_nan2(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) {
+        const float v = rht ? m * 0.25f : m;
+        atomicMax(reinterpret_cast<int *>(dst), v != v ? 0x7FFFFFFF : __float_as_int(v));
+    }
+}
 
 // Bounded wait that also gives up as soon as another role has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort,
@@ -246,7 +327,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int ntiles;
     if constexpr (kGrouped) ntiles = tab.tiles[tab.n];
-    else ntiles = p.ntm * p.ntn;
+    else ntiles = p.ntm * p.ntn * p.splits;   // work units
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -318,7 +399,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                 const TileInfo ti = tile_info<C::kKS>(p, tab, t);
                 // the B tile's second 128 rows have scales only inside the tensor
                 const bool b_hi = ti.b_row / 128 + 1 < p.b_rt;
-                for (int kb = 0; kb < ti.num_kb; ++kb, ++g) {
+                for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++g) {
                     const uint32_t s = g % S, round = g / S;
                     if (round > 0 && !wait_or_abort(empty(s), (round - 1) & 1, abort, p.budget)) { ok = false; break; }
                     const uint32_t atoms = (uint32_t)min(C::kKS, ti.nkt - C::kKS * kb);
@@ -372,7 +453,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                 // the epilogue must have read the previous tile out of the accumulator
                 if (it > 0 && !wait_or_abort(acce, (it - 1) & 1, abort, p.budget)) { ok = false; break; }
                 ptx::tc_fence_after();
-                for (int kb = 0; kb < ti.num_kb; ++kb, ++g) {
+                for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++g) {
                     const uint32_t s = g % S, round = g / S;
                     const uint32_t e = g % ES, eround = g / ES;
                     // operands landed and (scale warp) scales in TMEM
@@ -404,7 +485,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                     using None = std::integral_constant<CollA, CollA::kNone>;
                     using Fill = std::integral_constant<CollA, CollA::kFill>;
                     using Last = std::integral_constant<CollA, CollA::kLastUse>;
-                    auto first = [&](int j) { return (kb == 0 && j == 0) ? 0u : 1u; };
+                    auto first = [&](int j) { return (kb == ti.kb0 && j == 0) ? 0u : 1u; };
 #pragma unroll
                     for (int j = 0; j < C::kKS; ++j) {
                         if (j >= atoms) break;
@@ -445,6 +526,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         const uint32_t buf0 = smem_base + C::kEpiOff + (uint32_t)ew * NB * C::kEpiBufBytes;
         // E1M2 accumulates (R + E)(R + E) = 4 A B^T
         const float kfix = C::kFour ? 0.25f : 1.0f;
+        const uint32_t smask = (!kGrouped && p.c_amax && p.amax_rht) ? rht_sign_mask(p.amax_seed) : 0u;
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
         uint32_t it = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
@@ -467,6 +549,14 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(acce);
+                if (!kGrouped && p.c_amax) {
+                    // rows and columns outside C hold zeros (zero-filled operands)
+                    float am = 0.0f;
+#pragma unroll
+                    for (int blk = 0; blk < 8; ++blk)
+                        am = out_block_amax(&v[blk >> 1][(blk & 1) * 16], kfix, alpha, p.amax_rht != 0, smask, am);
+                    flush_amax(p.c_amax, am, p.amax_rht != 0, lane);
+                }
                 constexpr int EC = C::kEpiCols, RB = 4 * EC, NC = RB / 16;   // row bytes, 16-byte pieces
                 const uint32_t rowb = buf0 + (uint32_t)lane * RB;
                 const uint32_t sw = (uint32_t)(lane * RB / 128) & (NC - 1);  // swizzle of this row
@@ -491,7 +581,10 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                         __syncwarp();
                         if (lane == 0) {
                             const int col = n0 + EC * hc;
-                            if (m0 < ti.M && col < ti.N) ptx::tma_store_2d(&tma_c, col, m0, buf0);
+                            if (m0 < ti.M && col < ti.N) {
+                                if (p.splits > 1) ptx::tma_reduce_add_2d(&tma_c, col, m0, buf0);
+                                else ptx::tma_store_2d(&tma_c, col, m0, buf0);
+                            }
                             ptx::bulk_commit();
                         }
                     } else {
@@ -526,6 +619,11 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                 continue;
             } else {
             auto stage = [&](uint32_t b, const uint32_t (&v)[32]) {
+                if (!kGrouped && p.c_amax) {
+                    float am = out_block_amax(&v[0], kfix, alpha, p.amax_rht != 0, smask, 0.0f);
+                    am = out_block_amax(&v[16], kfix, alpha, p.amax_rht != 0, smask, am);
+                    flush_amax(p.c_amax, am, p.amax_rht != 0, lane);
+                }
                 const uint32_t rowb = b + (uint32_t)lane * 128u;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -545,7 +643,10 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                     // one bulk group per chunk, empty for boxes wholly outside C, so
                     // that the wait_group.read counts below see every chunk
                     if (lane == 0) {
-                        if (m0 < p.M && n0 + 32 * ch < p.N) ptx::tma_store_2d(&tma_c, n0 + 32 * ch, m0, b);
+                        if (m0 < p.M && n0 + 32 * ch < p.N) {
+                            if (p.splits > 1) ptx::tma_reduce_add_2d(&tma_c, n0 + 32 * ch, m0, b);
+                            else ptx::tma_store_2d(&tma_c, n0 + 32 * ch, m0, b);
+                        }
                         ptx::bulk_commit();
                     }
                 } else {
@@ -611,7 +712,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
             bool ok = true;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
                 const TileInfo ti = tile_info<C::kKS>(p, tab, t);
-                for (int kb = 0; kb < ti.num_kb; ++kb, ++g) {
+                for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++g) {
                     const uint32_t s = g % S, round = g / S;
                     if (!wait_or_abort(full(s), round & 1, abort, p.budget)) { ok = false; break; }
                     copy_scales(s, min(C::kKS, ti.nkt - C::kKS * kb), true);
@@ -629,8 +730,8 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         uint32_t g = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-            const int nkb = tile_info<C::kKS>(p, tab, t).num_kb;
-            for (int kb = 0; kb < nkb; ++kb, ++g) {
+            const TileInfo ti = tile_info<C::kKS>(p, tab, t);
+            for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++g) {
                 const uint32_t s = g % S, round = g / S;
                 const uint32_t e = g % ES, eround = g / ES;
                 ok = wait_or_abort(full(s), round & 1, abort, p.budget);
@@ -739,7 +840,12 @@ cudaError_t run_gemm(const CUtensorMap &ma, const CUtensorMap &mb, const CUtenso
 cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_eplane, const uint8_t *a_scales,
                         const float *a_ts, const uint8_t *b_codes, const uint8_t *b_eplane,
                         const uint8_t *b_scales, const float *b_ts, int64_t M, int64_t N, int64_t K, int grid,
-                        float *c, int64_t ldc, cudaStream_t s) {
+                        float *c, int64_t ldc, cudaStream_t s, float *c_amax, int amax_rht, uint64_t amax_seed) {
+    if (c_amax) {
+        // the epilogue raises it from zero (and a K = 0 product is all zeros)
+        cudaError_t e = cudaMemsetAsync(c_amax, 0, sizeof(float), s);
+        if (e != cudaSuccess) return e;
+    }
     if (K == 0) return cudaMemset2DAsync(c, ldc * sizeof(float), 0, N * sizeof(float), M, s);
     const int64_t kpad = kpad_of(K);
     const bool planes = grid == kE1M2 && a_eplane && b_eplane;
@@ -769,11 +875,32 @@ cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_eplane, const u
     p.b_rt = (int)((N + 127) / 128);
     p.budget = g_wait_budget;
     p.stall = g_stall;
+    // Split K in two when the tiles leave the last round of the persistent
+    // grid mostly idle (e.g. 512 tiles on 152 SMs: 4 rounds for 3.4 rounds of
+    // work) and two half-K units per tile fill the rounds better.  The halves
+    // are added into a zeroed C by TMA reduce-add; with two terms the sum
+    // does not depend on their order, so the result is deterministic.
+    p.splits = 1;
+    {
+        const int64_t tiles = (int64_t)p.ntm * p.ntn, sms = num_sms();
+        const int64_t w1 = (tiles + sms - 1) / sms, w2 = (2 * tiles + sms - 1) / sms;
+        // (not with the output amax: the epilogue then sees only partial sums)
+        if (!c_amax && p.num_kb >= 8 && (double)w2 < 0.92 * 2.0 * (double)w1) p.splits = 2;
+    }
+    p.c_amax = c_amax;
+    p.amax_rht = amax_rht;
+    p.amax_seed = amax_seed;
+    p.col_major = M < N ? 1 : 0;
+    if (p.splits > 1) {
+        cudaError_t e = cudaMemset2DAsync(c, ldc * sizeof(float), 0, N * sizeof(float), M, s);
+        if (e != cudaSuccess) return e;
+    }
     const NoGroups none;
+    const int units = p.ntm * p.ntn * p.splits;
     // clamped-E2M1 codes are E2M1 codes
-    if (grid != kE1M2) return run_gemm<kE2M1>(ma, mb, mea, meb, mc, p, none, p.ntm * p.ntn, s);
-    if (planes) return run_gemm<kE1M2Pl>(ma, mb, mea, meb, mc, p, none, p.ntm * p.ntn, s);
-    return run_gemm<kE1M2>(ma, mb, mea, meb, mc, p, none, p.ntm * p.ntn, s);
+    if (grid != kE1M2) return run_gemm<kE2M1>(ma, mb, mea, meb, mc, p, none, units, s);
+    if (planes) return run_gemm<kE1M2Pl>(ma, mb, mea, meb, mc, p, none, units, s);
+    return run_gemm<kE1M2>(ma, mb, mea, meb, mc, p, none, units, s);
 }
 
 cudaError_t launch_gemm_grouped(const uint8_t *a_codes, const uint8_t *a_eplane, const uint8_t *a_scales,
@@ -804,6 +931,7 @@ cudaError_t launch_gemm_grouped(const uint8_t *a_codes, const uint8_t *a_eplane,
     p.M = 1; p.N = 1;
     p.budget = g_wait_budget;
     p.stall = g_stall;
+    p.splits = 1;
     const int ntiles = tab.tiles[tab.n];
     if (grid != kE1M2) return run_gemm<kE2M1>(ma, mb, mea, meb, mc, p, tab, ntiles, s);
     if (planes) return run_gemm<kE1M2Pl>(ma, mb, mea, meb, mc, p, tab, ntiles, s);

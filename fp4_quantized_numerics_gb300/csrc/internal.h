@@ -72,6 +72,12 @@ cudaError_t launch_dequantize(const uint8_t *codes, const uint8_t *scales, const
 // Writes n_ctas x 8 double partial sums to ws + kWsStats; returns n_ctas.
 cudaError_t launch_stats(const QuantLaunch &q, void *ws, int *n_ctas, cudaStream_t s);
 
+// Quantization and the statistics of its result: one pass over x where the
+// staged row-wise kernel applies (it accumulates the partial sums as it
+// writes the codes), else launch_quantize then launch_stats.  Partial sums
+// as launch_stats.
+cudaError_t launch_quantize_stats(const QuantLaunch &q, void *ws, int *n_ctas, cudaStream_t s);
+
 // 2-D TMA tensor map (CUtensorMap, 128 bytes) of a BF16 matrix rows x cols
 // with row stride ld elements; tiles of box_cols x box_rows, no swizzle, out
 // of range elements read as zero.
@@ -95,10 +101,13 @@ cudaError_t launch_gemm_grouped(const uint8_t *a_codes, const uint8_t *a_eplane,
 
 // a_eplane / b_eplane: E1M2 correction planes (same layout as the codes) or
 // NULL; with both given the GEMM loads them instead of expanding on chip.
+// c_amax (or NULL): set to the tensor amax of C's row-wise quantization
+// (amax_rht: of the rotated C with the signs of amax_seed).
 cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_eplane, const uint8_t *a_scales,
                         const float *a_ts, const uint8_t *b_codes, const uint8_t *b_eplane,
                         const uint8_t *b_scales, const float *b_ts, int64_t M, int64_t N, int64_t K, int grid,
-                        float *c, int64_t ldc, cudaStream_t s);
+                        float *c, int64_t ldc, cudaStream_t s, float *c_amax = nullptr, int amax_rht = 0,
+                        uint64_t amax_seed = 0);
 
 // Reads and clears the sticky flag that a bounded device-side wait raises
 // when it gives up (synchronises s).

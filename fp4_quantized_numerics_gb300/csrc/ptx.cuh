@@ -89,6 +89,14 @@ __device__ __forceinline__ void tma_store_2d(const void *tmap, int32_t x, int32_
                  "r"(x), "r"(y), "r"(src)
                  : "memory");
 }
+// Element-wise fp32 add of a shared-memory box into global memory (the
+// reduction happens at L2; boxes partly outside the tensor are clipped).
+__device__ __forceinline__ void tma_reduce_add_2d(const void *tmap, int32_t x, int32_t y, uint32_t src) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N committed bulk groups are still reading shared memory.
 template <int N>

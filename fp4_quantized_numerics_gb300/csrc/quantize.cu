@@ -610,6 +610,85 @@ __device__ __forceinline__ void quant_block_row(const Args &a, const Raw<In> &ra
     store_block(a, r, b, round_block<GRID, ROUND>(ql, qh, e, folded, a, i0), e, cstride, nkt);
 }
 
+// Per element: deq = fl32(fl32(v e) S_dec), A = y (rotated input);
+// sums of deq*A, A*A, (A-deq)^2, (v - a) over a != 0, count.
+struct Acc {
+    double aq = 0, aa = 0, e2 = 0, bias = 0, cnt = 0;
+};
+
+__device__ __forceinline__ void acc_block8(Acc &acc, const float y[8], uint32_t w, float e,
+                                           float S_dec, int grid, float qmax) {
+    float aq = 0, aa = 0, e2 = 0, bias = 0, cnt = 0;
+    const float unit = __fmul_rn(e, S_dec);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t c = (w >> (4 * j)) & 0xFu;
+        const float v = grid_value(grid, c);
+        const float sv = (c & 8u) ? -v : v;
+        const float dq = __fmul_rn(__fmul_rn(sv, e), S_dec);
+        aq += dq * y[j];
+        aa += y[j] * y[j];
+        e2 += (y[j] - dq) * (y[j] - dq);
+        if (e > 0.0f) {
+            const float g = fminf(fabsf(y[j]) / unit, qmax);
+            if (g != 0.0f) { bias += v - g; cnt += 1.0f; }
+        }
+    }
+    acc.aq += aq; acc.aa += aa; acc.e2 += e2; acc.bias += bias; acc.cnt += cnt;
+}
+
+__device__ void stats_reduce(Acc acc, double *out) {
+    __shared__ double s[kThreads / 32][5];
+    double v[5] = {acc.aq, acc.aa, acc.e2, acc.bias, acc.cnt};
+#pragma unroll
+    for (int i = 0; i < 5; ++i)
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0)
+        for (int i = 0; i < 5; ++i) s[warp][i] = v[i];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 5; ++i) {
+            double t = 0;
+            for (int w = 0; w < kThreads / 32; ++w) t += s[w][i];
+            out[blockIdx.x * 8 + i] = t;
+        }
+    }
+}
+
+// quant_block_row, and the block's terms of the quality statistics (the
+// sums of ufp4_stats over the result actually stored) added to acc.
+template <class In, int GRID, int ROUND, bool RHT>
+__device__ __forceinline__ void quant_block_row_stats(const Args &a, const Raw<In> &raw, uint32_t r, uint32_t b,
+                                                      const Signs &sg, float S_enc, float S_dec, const float *s_k,
+                                                      uint32_t cstride, uint32_t nkt, bool folded, Acc &acc) {
+    const float qmax = GRID == kE2M1 ? 6.0f : a.uqmax;
+    float lo[8], hi[8];
+    block_values<In, RHT>(raw, sg, lo, hi);
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fmaxf(fabsf(lo[j]), fabsf(hi[j])));
+    if (RHT) m *= 0.25f;
+    const uint32_t e = block_scale(m, qmax, S_enc);
+    const float kk = s_k ? s_k[e] : inline_k(e, S_enc, RHT);
+    const uint64_t K2 = pk2(kk, kk);
+    float ql[8], qh[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) upk2(mul2(pk2(lo[j], hi[j]), K2), ql[j], qh[j]);
+    const uint64_t i0 = a.elem_base + (uint64_t)r * (uint64_t)a.k + (uint64_t)b * 16u;
+    uint2 w = round_block<GRID, ROUND>(ql, qh, e, folded, a, i0);
+    if (e == 0) w = make_uint2(0u, 0u);
+    store_block(a, r, b, w, e, cstride, nkt);
+    if (RHT) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { lo[j] *= 0.25f; hi[j] *= 0.25f; }
+    }
+    const float ev = e4m3_to_f32(e);
+    acc_block8(acc, lo, w.x, ev, S_dec, GRID, qmax);
+    acc_block8(acc, hi, w.y, ev, S_dec, GRID, qmax);
+}
+
 // Two row-wise blocks (A, B) held as packed pairs P_j = (A_j, B_j), so all
 // four butterfly stages and the scaling run on f32x2.
 template <int GRID, int ROUND, bool RHT>
@@ -986,7 +1065,10 @@ __device__ __forceinline__ void row_issue(const RingCtl &r, const Args &a, uint3
     issued = j + 1;
 }
 
-template <class In, int GRID, int ROUND, bool RHT, bool AMAX>
+// STATS (quantization pass only): also accumulate the quality statistics of
+// the result -- the sums of ufp4_stats -- and write one set of partial sums
+// per CTA to a.stats_out, so that quantization and statistics take one read.
+template <class In, int GRID, int ROUND, bool RHT, bool AMAX, bool STATS = false>
 __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_row_staged(Args a, FastDiv bdiv, uint32_t kvb,
                                                          uint32_t nchunks, uint64_t total_bytes) {
     constexpr int kRing = ring_depth<AMAX>();
@@ -998,11 +1080,16 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_row_staged(Args a,
     uint32_t issued = 0, j = 0;
     if (threadIdx.x == 0)
         for (uint32_t t = 0; t < kRing; ++t) row_issue<In, kRing>(ring, a, t, nchunks, total_bytes, issued);
-    float S_enc = 1.0f;
+    float S_enc = 1.0f, S_dec = 1.0f;
     bool folded = false;
-    if (!AMAX)
-        tensor_scale_prologue(a, GRID == kE2M1 ? 6.0f : a.uqmax, RHT ? 0.25f : 1.0f, s_k, s_red, S_enc,
-                              GRID == kE1M2 && ROUND == kRTNE, &folded);
+    if (!AMAX) {
+        const float qmax = GRID == kE2M1 ? 6.0f : a.uqmax;
+        float A_t = 0.0f;
+        tensor_scale_prologue(a, qmax, RHT ? 0.25f : 1.0f, s_k, s_red, S_enc, GRID == kE1M2 && ROUND == kRTNE,
+                              &folded, &A_t);
+        if (STATS && A_t > 0.0f) S_dec = __fdiv_rn(A_t, 448.0f * qmax);   // as the prologue stores it
+    }
+    Acc acc;
     const uint32_t smask = RHT ? rht_sign_mask(a.rht_seed) : 0u;
     const Signs sg = row_signs<In>(smask);
     const uint32_t total_blocks = (uint32_t)(total_bytes / (16 * sizeof(In)));
@@ -1066,8 +1153,12 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_row_staged(Args a,
                     for (int q = 0; q < 8; ++q) m = max_nan(m, max_nan(fabsf(lo[q]), fabsf(hi[q])));
                 } else {
                     const uint32_t r = fdiv(gb, bdiv);
-                    quant_block_row<In, GRID, ROUND, RHT>(a, raw, r, gb - r * kvb, sg, S_enc, s_k, cstride,
-                                                          nkt, folded);
+                    if (STATS)
+                        quant_block_row_stats<In, GRID, ROUND, RHT>(a, raw, r, gb - r * kvb, sg, S_enc, S_dec, s_k,
+                                                                    cstride, nkt, folded, acc);
+                    else
+                        quant_block_row<In, GRID, ROUND, RHT>(a, raw, r, gb - r * kvb, sg, S_enc, s_k, cstride,
+                                                              nkt, folded);
                 }
             }
         }
@@ -1097,6 +1188,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_row_staged(Args a,
             a.scales[scale_offset32(r, b, nkt)] = 0;
         }
         zero_pad_rows(a);
+        if (STATS) stats_reduce(acc, a.stats_out);
     }
 }
 
@@ -1900,53 +1992,6 @@ cudaError_t quantize_grouped_typed(const QuantLaunch &q, const GroupQuant &gt, v
 }
 
 // ============================================================= statistics
-// Per element: deq = fl32(fl32(v e) S_dec), A = y (rotated input);
-// sums of deq*A, A*A, (A-deq)^2, (v - a) over a != 0, count.
-struct Acc {
-    double aq = 0, aa = 0, e2 = 0, bias = 0, cnt = 0;
-};
-
-__device__ __forceinline__ void acc_block8(Acc &acc, const float y[8], uint32_t w, float e,
-                                           float S_dec, int grid, float qmax) {
-    float aq = 0, aa = 0, e2 = 0, bias = 0, cnt = 0;
-    const float unit = __fmul_rn(e, S_dec);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint32_t c = (w >> (4 * j)) & 0xFu;
-        const float v = grid_value(grid, c);
-        const float sv = (c & 8u) ? -v : v;
-        const float dq = __fmul_rn(__fmul_rn(sv, e), S_dec);
-        aq += dq * y[j];
-        aa += y[j] * y[j];
-        e2 += (y[j] - dq) * (y[j] - dq);
-        if (e > 0.0f) {
-            const float g = fminf(fabsf(y[j]) / unit, qmax);
-            if (g != 0.0f) { bias += v - g; cnt += 1.0f; }
-        }
-    }
-    acc.aq += aq; acc.aa += aa; acc.e2 += e2; acc.bias += bias; acc.cnt += cnt;
-}
-
-__device__ void stats_reduce(Acc acc, double *out) {
-    __shared__ double s[kThreads / 32][5];
-    double v[5] = {acc.aq, acc.aa, acc.e2, acc.bias, acc.cnt};
-#pragma unroll
-    for (int i = 0; i < 5; ++i)
-#pragma unroll
-        for (int o = 16; o; o >>= 1) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0)
-        for (int i = 0; i < 5; ++i) s[warp][i] = v[i];
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < 5; ++i) {
-            double t = 0;
-            for (int w = 0; w < kThreads / 32; ++w) t += s[w][i];
-            out[blockIdx.x * 8 + i] = t;
-        }
-    }
-}
-
 template <class In, bool RHT>
 __global__ void __launch_bounds__(kThreads) k_stats_rowwise(Args a, int grid) {
     const float qmax = grid_qmax(grid);
@@ -2426,6 +2471,50 @@ cudaError_t launch_quantize(const QuantLaunch &q, void *ws, cudaStream_t s) {
     }
     if (q.dtype == 0) return quantize_typed<__nv_bfloat16>(q, a, ws, s);
     return quantize_typed<float>(q, a, ws, s);
+}
+
+cudaError_t launch_quantize_stats(const QuantLaunch &q, void *ws, int *n_ctas, cudaStream_t s) {
+    const int64_t esz = q.dtype == 0 ? 2 : 4;
+    *n_ctas = 0;
+    // one pass: the staged row-wise quantization (contiguous input), whose
+    // CTAs fit the workspace's partial sums
+    if (q.grid != kMXFP4 && !q.colwise && q.ld == q.cols) {
+        Args a = make_args(q, ws);
+        a.stats_out = reinterpret_cast<double *>(static_cast<char *>(ws) + kWsStats);
+        if (!q.amax_in) {
+            a.partials_out = reinterpret_cast<float *>(static_cast<char *>(ws) + kWsPartials);
+            a.partials = a.partials_out;
+            cudaError_t e = q.rht ? (esz == 2 ? amax_pass<__nv_bfloat16, true>(q, a, true, s)
+                                              : amax_pass<float, true>(q, a, true, s))
+                                  : (esz == 2 ? amax_pass<__nv_bfloat16, false>(q, a, true, s)
+                                              : amax_pass<float, false>(q, a, true, s));
+            if (e != cudaSuccess) return e;
+        }
+        const uint32_t kvb = (uint32_t)(a.k / 16);
+        const uint64_t tb = (uint64_t)a.rows * a.cols * esz;
+        const uint32_t nch = (uint32_t)((tb + kChunk - 1) / kChunk);
+        const int kgrid = q.grid == kE2M1 ? kE2M1 : kE1M2;
+#define UFP4_QS(IN, GRID, ROUND, RHT)                                                                        \
+        if ((esz == sizeof(IN)) && kgrid == GRID && q.round == ROUND && (q.rht != 0) == RHT) {              \
+            auto kern = k_row_staged<IN, GRID, ROUND, RHT, false, true>;                                     \
+            if (resident_grid(kern, nch, ring_smem<false>()) <= kMaxStatsCtas)                               \
+                return launch_staged<false>(kern, nch, n_ctas, s, a, make_fastdiv(kvb), kvb, nch, tb);      \
+        }
+        UFP4_QS(__nv_bfloat16, kE2M1, kRTNE, false) UFP4_QS(__nv_bfloat16, kE2M1, kRTNE, true)
+        UFP4_QS(__nv_bfloat16, kE2M1, kSR, false)   UFP4_QS(__nv_bfloat16, kE2M1, kSR, true)
+        UFP4_QS(__nv_bfloat16, kE1M2, kRTNE, false) UFP4_QS(__nv_bfloat16, kE1M2, kRTNE, true)
+        UFP4_QS(__nv_bfloat16, kE1M2, kSR, false)   UFP4_QS(__nv_bfloat16, kE1M2, kSR, true)
+        UFP4_QS(float, kE2M1, kRTNE, false) UFP4_QS(float, kE2M1, kRTNE, true)
+        UFP4_QS(float, kE2M1, kSR, false)   UFP4_QS(float, kE2M1, kSR, true)
+        UFP4_QS(float, kE1M2, kRTNE, false) UFP4_QS(float, kE1M2, kRTNE, true)
+        UFP4_QS(float, kE1M2, kSR, false)   UFP4_QS(float, kE1M2, kSR, true)
+#undef UFP4_QS
+        // (the amax pass, if any, has run: the two-pass route below repeats it)
+    }
+    // two passes: quantization, then the statistics kernels
+    cudaError_t e = launch_quantize(q, ws, s);
+    if (e != cudaSuccess) return e;
+    return launch_stats(q, ws, n_ctas, s);
 }
 
 cudaError_t launch_quantize_dual(const QuantLaunch &qr, const QuantLaunch &qc, void *ws, cudaStream_t s) {

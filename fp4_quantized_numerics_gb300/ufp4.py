@@ -30,7 +30,8 @@ UFP4_OK, UFP4_ERR_INVALID, UFP4_ERR_UNSUPPORTED, UFP4_ERR_NONFINITE, UFP4_ERR_CU
 EXPORTED = ["ufp4_kpad", "ufp4_codes_bytes", "ufp4_scales_bytes", "ufp4_workspace_bytes",
             "ufp4_quantize", "ufp4_check", "ufp4_dequantize", "ufp4_gemm", "ufp4_stats",
             "ufp4_status_string", "ufp4_quantize_noalloc", "ufp4_grouped_rows",
-            "ufp4_grouped_kpad", "ufp4_quantize_grouped", "ufp4_gemm_grouped", "ufp4_quantize_dual"]
+            "ufp4_grouped_kpad", "ufp4_quantize_grouped", "ufp4_gemm_grouped", "ufp4_quantize_dual",
+            "ufp4_gemm_amax", "ufp4_quantize_stats"]
 
 
 class QParamsC(ctypes.Structure):
@@ -99,10 +100,17 @@ def lib():
         L.ufp4_dequantize.restype = ctypes.c_int
         L.ufp4_gemm.argtypes = [ctypes.POINTER(QTensorC), ctypes.POINTER(QTensorC), vp, i64, vp]
         L.ufp4_gemm.restype = ctypes.c_int
+        L.ufp4_gemm_amax.argtypes = [ctypes.POINTER(QTensorC), ctypes.POINTER(QTensorC), vp, i64,
+                                     ctypes.c_int32, ctypes.c_uint64, vp, vp]
+        L.ufp4_gemm_amax.restype = ctypes.c_int
         L.ufp4_stats.argtypes = [vp, ctypes.c_int32, i64, i64, i64, ctypes.POINTER(QParamsC),
                                  ctypes.POINTER(QTensorC), vp, ctypes.c_size_t,
                                  ctypes.POINTER(StatsC), vp]
         L.ufp4_stats.restype = ctypes.c_int
+        L.ufp4_quantize_stats.argtypes = [vp, ctypes.c_int32, i64, i64, i64, ctypes.POINTER(QParamsC),
+                                          ctypes.POINTER(QTensorC), vp, ctypes.c_size_t,
+                                          ctypes.POINTER(StatsC), vp]
+        L.ufp4_quantize_stats.restype = ctypes.c_int
         i64p = ctypes.POINTER(ctypes.c_int64)
         L.ufp4_grouped_rows.argtypes = [i64p, ctypes.c_int32]
         L.ufp4_grouped_rows.restype = i64
@@ -283,6 +291,47 @@ def ufp4_gemm(a, b, out=None, stream=None):
                          _stream(stream))
     _check(st, "ufp4_gemm")
     return out
+
+
+def ufp4_gemm_amax(a, b, rht=False, rht_seed=0, out=None, amax=None, stream=None):
+    """C = A B^T as ufp4_gemm, and the tensor amax of C's row-wise
+    quantization (rotated with rht_seed when rht) from the epilogue.
+    Returns (C, amax); pass amax as the amax_in of ufp4_quantize(C, ...)."""
+    _cuda(a.codes, "a.codes")
+    _cuda(b.codes, "b.codes")
+    if out is None:
+        ld = (b.rows + 3) // 4 * 4
+        out = torch.empty(a.rows, ld, dtype=torch.float32, device=a.codes.device)[:, : b.rows]
+    if amax is None:
+        amax = torch.empty(1, dtype=torch.float32, device=a.codes.device)
+    ac, bc = a.c(), b.c()
+    st = lib().ufp4_gemm_amax(ctypes.byref(ac), ctypes.byref(bc), out.data_ptr(), out.stride(0),
+                              int(bool(rht)), int(rht_seed) & (2**64 - 1), amax.data_ptr(), _stream(stream))
+    _check(st, "ufp4_gemm_amax")
+    return out, amax
+
+
+def ufp4_quantize_stats(x, grid, rht=False, rht_seed=0, round=UFP4_RTNE, sr_seed=0, sr_counter=0,
+                        colwise=False, amax_in=None, out=None, ws=None, stream=None):
+    """ufp4_quantize and ufp4_stats of its result in one call (one read of x
+    where the layout allows).  Returns (QTensor, stats dict); synchronises."""
+    _cuda(x, "x")
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit stride in its last dim")
+    rows, cols = x.shape
+    out_rows, k = (cols, rows) if colwise else (rows, cols)
+    if out is None:
+        out = QTensor.empty(out_rows, k, grid, x.device)
+    if ws is None:
+        ws = workspace(x.device)
+    p = qparams(grid, rht, rht_seed, round, sr_seed, sr_counter, colwise, amax_in)
+    qc = out.c()
+    res = StatsC()
+    st = lib().ufp4_quantize_stats(x.data_ptr(), _dtype_code(x), rows, cols, x.stride(0), ctypes.byref(p),
+                                   ctypes.byref(qc), ws.data_ptr(), ws.numel(), ctypes.byref(res),
+                                   _stream(stream))
+    _check(st, "ufp4_quantize_stats")
+    return out, {n: getattr(res, n) for n, _ in StatsC._fields_}
 
 
 def ufp4_stats(x, q, rht=False, rht_seed=0, round=UFP4_RTNE, sr_seed=0, sr_counter=0,

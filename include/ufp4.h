@@ -294,6 +294,24 @@ UFP4_API ufp4_status ufp4_dequantize(const ufp4_qtensor *q, int32_t inverse_rht,
 UFP4_API ufp4_status ufp4_gemm(const ufp4_qtensor *a, const ufp4_qtensor *b, float *c, int64_t ldc,
                       ufp4_stream_t stream);
 
+/* ufp4_gemm fused with the first step of quantizing its output.  The pages'
+ * compounding chain re-quantizes every layer's output for the next layer
+ * ([ZC] Key points, "Compounding decay"); the tensor amax of that
+ * quantization needs all of C, so a plain GEMM leaves it to a second read of
+ * C.  This call writes C exactly as ufp4_gemm does and, from the epilogue's
+ * registers, the amax A_t that ufp4_quantize would compute for the row-wise
+ * quantization of C with parameters rht / rht_seed: max |C| (rht = 0), or
+ * max over C's 16-blocks along N of |(1/4) H16 diag(d) block| (rht = 1),
+ * with the quantizer's own fp32 butterflies in its order.  Passing c_amax as
+ * that quantization's amax_in gives bit for bit the codes, scales and tensor
+ * scale of the unfused call, with C read once instead of twice.
+ *   c_amax : device, 1 float, 4-byte aligned; overwritten (the call zeroes
+ *            it on `stream`, then the kernel raises it); NaN if C holds one.
+ *   rht    : 0 or 1; with rht = 1, N % 16 == 0.
+ * Other arguments and requirements as ufp4_gemm. */
+UFP4_API ufp4_status ufp4_gemm_amax(const ufp4_qtensor *a, const ufp4_qtensor *b, float *c, int64_t ldc,
+                                    int32_t rht, uint64_t rht_seed, float *c_amax, ufp4_stream_t stream);
+
 /* ---------------------------------------------------------------------
  * Grouped (mixture-of-experts) tensors.  The tokens routed to expert e form a
  * segment of T_e consecutive rows of x ([sum T_e] x cols); every segment has
@@ -376,6 +394,21 @@ UFP4_API ufp4_status ufp4_stats(const void *x, int32_t dtype, int64_t rows, int6
                        const ufp4_qparams *p, const ufp4_qtensor *q,
                        void *workspace, size_t workspace_bytes,
                        ufp4_stats_t *host_out, ufp4_stream_t stream);
+
+/* ufp4_quantize and ufp4_stats of its result in one call: the quantization
+ * kernel accumulates the statistics' partial sums as it writes the codes, so
+ * x is read once for both, where the layout allows it (row-wise, contiguous
+ * input: ld == cols); otherwise the call runs the two one after the other.
+ * The pages track the shrinkage factor and SQNR of every quantization ([ZC]
+ * "The cause", "Compounding decay", "The RHT paradox").  Arguments as
+ * ufp4_quantize (out receives the quantization) plus host_out as ufp4_stats.
+ * The quantized tensor is bit for bit ufp4_quantize's; the statistics equal
+ * ufp4_stats's up to the order of the fp32 partial sums.  Synchronises
+ * `stream`. */
+UFP4_API ufp4_status ufp4_quantize_stats(const void *x, int32_t dtype, int64_t rows, int64_t cols, int64_t ld,
+                                         const ufp4_qparams *p, const ufp4_qtensor *out,
+                                         void *workspace, size_t workspace_bytes,
+                                         ufp4_stats_t *host_out, ufp4_stream_t stream);
 
 /* Static description of a status code (no counterpart on the pages). */
 UFP4_API const char *ufp4_status_string(ufp4_status s);

@@ -124,3 +124,55 @@ def test_gemm_k_zero_writes_zeros(U):
 
 def test_gemm_no_timeout_flag(U):
     assert U.ufp4_check() == U.UFP4_OK
+
+
+@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 4096), (384, 300, 8192)])
+def test_split_k_deterministic(U, oracle, grid, M, N, K):
+    """Few output tiles and a long K: the GEMM splits K in two and adds the
+    halves into a zeroed C (TMA reduce-add).  Two terms add the same in
+    either order, so repeated runs agree bit for bit; and the result is
+    within 1e-5 of the oracle's fp64 product."""
+    a = inputs.normal(48, (M, K))
+    b = inputs.normal(49, (N, K), std=0.02)
+    ta = torch.from_numpy(a).to(torch.bfloat16).cuda()
+    tb = torch.from_numpy(b).to(torch.bfloat16).cuda()
+    qa, qb = U.ufp4_quantize(ta, grid), U.ufp4_quantize(tb, grid)
+    c1 = U.ufp4_gemm(qa, qb).clone()
+    c2 = torch.full_like(c1, 5.0)
+    U.ufp4_gemm(qa, qb, out=c2)
+    torch.cuda.synchronize()
+    assert torch.equal(c1, c2)
+    ra, rb = oracle.quantize(a, grid), oracle.quantize(b, grid)
+    ref = oracle.gemm_f64(oracle.dequantize(ra["codes"], ra["scales"], ra["tensor_scale"], grid),
+                          oracle.dequantize(rb["codes"], rb["scales"], rb["tensor_scale"], grid))
+    assert _rel_fro(c1.cpu().numpy(), ref) <= TOL
+
+
+@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("rht", [False, True])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (300, 208, 320), (128, 4096, 1024)])
+def test_gemm_amax_fuses_next_quantization(U, oracle, grid, rht, M, N, K):
+    """ufp4_gemm_amax: C as ufp4_gemm computes it, and the tensor amax of C's
+    row-wise quantization from the epilogue.  Quantizing C with that amax
+    given equals, bit for bit, quantizing C with the amax computed by the
+    quantizer's own pass; without the transform it is max |C| exactly, with
+    it the oracle's rotated amax of C within 1e-6."""
+    a = inputs.normal(50, (M, K))
+    b = inputs.normal(51, (N, K), std=0.05)
+    qa = U.ufp4_quantize(torch.from_numpy(a).to(torch.bfloat16).cuda(), grid)
+    qb = U.ufp4_quantize(torch.from_numpy(b).to(torch.bfloat16).cuda(), grid)
+    c, am = U.ufp4_gemm_amax(qa, qb, rht=rht, rht_seed=2)
+    c_plain = U.ufp4_gemm(qa, qb)
+    q_given = U.ufp4_quantize(c, grid, rht=rht, rht_seed=2, amax_in=am)
+    q_own = U.ufp4_quantize(c, grid, rht=rht, rht_seed=2)
+    torch.cuda.synchronize()
+    assert _rel_fro(c.cpu().numpy(), c_plain.cpu().numpy()) <= 1e-6   # plain may split K
+    for f in ("codes", "scales", "tensor_scale"):
+        assert torch.equal(getattr(q_given, f), getattr(q_own, f)), f
+    ch = c.cpu().numpy()
+    if not rht:
+        assert am.item() == float(np.abs(ch).max())
+    else:
+        want = oracle.tensor_amax(ch, rht=True, rht_seed=2)
+        assert abs(am.item() / want - 1) <= 1e-6

@@ -243,3 +243,35 @@ def test_rows_16_byte_aligned_only(U, oracle, dtype, rht, colwise):
                 np.testing.assert_array_equal(gc[off:off + counts[e]], rg[e]["codes"])
             else:
                 parity.assert_codes_close(gc[off:off + counts[e]], rg[e]["codes"])
+
+
+@pytest.mark.parametrize("grid", [0, 1, 2])
+@pytest.mark.parametrize("rht", [False, True])
+@pytest.mark.parametrize("layout", ["bf16", "fp32", "strided", "colwise"])
+def test_quantize_stats_fused(U, oracle, grid, rht, layout):
+    """ufp4_quantize_stats: the quantized tensor is ufp4_quantize's bit for
+    bit; the statistics agree with ufp4_stats (separate pass) and with the
+    oracle's.  BF16 / FP32 contiguous row-wise take the one-pass kernel; the
+    strided and column-wise layouts the two-pass route."""
+    dtype = torch.float32 if layout == "fp32" else torch.bfloat16
+    x = inputs.normal(72, (512, 768)) if dtype == torch.bfloat16 else \
+        inputs.rng(72).standard_normal((512, 768), dtype=np.float32)
+    xt = _strided(x, dtype, 8) if layout == "strided" else torch.from_numpy(x).to(dtype).cuda()
+    col = layout == "colwise"
+    rnd = 1 if grid == 1 else 0
+    kw = dict(rht=rht, rht_seed=2, round=rnd, sr_seed=5, colwise=col)
+    q, st = U.ufp4_quantize_stats(xt, grid, **kw)
+    q0 = U.ufp4_quantize(xt, grid, **kw)
+    s0 = U.ufp4_stats(xt, q0, **kw)
+    torch.cuda.synchronize()
+    for f in ("codes", "scales", "tensor_scale"):
+        assert torch.equal(getattr(q, f), getattr(q0, f)), f
+    assert torch.equal(q.eplane, q0.eplane) if q.eplane is not None else True
+    assert st["bias_count"] == s0["bias_count"]
+    assert abs(st["alpha"] - s0["alpha"]) <= 1e-6
+    assert abs(st["sqnr_db"] - s0["sqnr_db"]) <= 1e-4
+    assert abs(st["mean_bias"] - s0["mean_bias"]) <= 1e-5
+    r = oracle.quantize(x, grid, rht=rht, rht_seed=2, round_mode=rnd, sr_seed=5, colwise=col)
+    ro = oracle.stats(r["y"], r["codes"], r["scales"], r["tensor_scale"], grid)
+    assert abs(st["alpha"] - ro["alpha"]) <= 1e-5
+    assert abs(st["sqnr_db"] - ro["sqnr_db"]) <= 1e-3
