@@ -1019,19 +1019,33 @@ constexpr long long kRingWait = 4000000000LL;
 struct RingCtl {
     uint32_t buf;    // shared address of stage 0
     uint32_t bars;   // shared address of the ring's mbarriers
+    volatile int *abort;   // raised by a thread whose own wait gave up
 };
 
 template <int kRing>
 __device__ __forceinline__ RingCtl ring_init(uint8_t *dsm) {
+    static_assert(kRing * 8 + 4 <= 64, "the ring's barriers and abort flag fit its 64 bytes");
     RingCtl r;
     r.buf = ptx::smem_u32(dsm);
     r.bars = ptx::smem_u32(dsm + kRing * kChunk);
+    r.abort = reinterpret_cast<volatile int *>(dsm + kRing * kChunk + 60);
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRing; ++s) ptx::mbar_init(r.bars + 8u * s, 1);
+        *r.abort = 0;
         ptx::fence_mbar_init();
     }
     __syncthreads();
     return r;
+}
+
+// Each thread's own wait for chunk j's stage, without a CTA barrier: a thread
+// that gives up raises the abort flag, which every thread reads after the
+// barrier that ends the iteration.
+template <int kRing>
+__device__ __forceinline__ bool ring_wait_own(const RingCtl &r, uint32_t j) {
+    const bool ok = ptx::mbar_wait_bounded(r.bars + 8u * (j % kRing), (j / kRing) & 1u, kRingWait);
+    if (!ok) *r.abort = 1;
+    return ok;
 }
 
 // Waits for chunk j's stage; false (for every thread) if any thread gave up.
@@ -1286,6 +1300,167 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_col_staged(Args a,
     }
 }
 
+// ========================================= tensor-core amax (BF16, transform)
+// With the transform on, the tensor amax is max |y| over y = (1/4) H16
+// diag(d) x of every 16-block: a product with the constant 16 x 16 matrix
+// H16 diag(d), whose entries +-1 are exact in BF16, and only the maximum is
+// needed, not where each y lands.  So the blocks go through the tensor cores
+// as the rows of A in mma.sync m16n8k16 BF16 products with fp32 accumulation
+// (the products are exact; the tensor cores round the 16-term sums, within
+// about 1e-7 relative of the fp64 transform), A loaded by ldmatrix from
+// 16-row chunks staged in shared memory at a row pitch padded by 16 bytes, so
+// that the eight rows one ldmatrix phase reads fall in different banks.
+// ROW: the row-wise blocks (16 consecutive elements of a row, A row m = chunk
+// row m of one block column); COL: the column-wise blocks (16 consecutive
+// rows of a column, A row m = column m of a 16-column group, loaded
+// transposed); both from one read for the dual pass.  Every BF16 amax with
+// the transform runs here (when rows are 16-byte pieces), so the single- and
+// dual-orientation quantizations of a tensor agree bit for bit.
+constexpr uint32_t kMmaCW = 512;                  // columns per chunk (1 KB of BF16)
+constexpr uint32_t kMmaPitch = kMmaCW * 2 + 16;   // padded row pitch in shared memory
+constexpr uint32_t kMmaStage = 16 * kMmaPitch;    // 16,640 bytes
+constexpr int kMmaRing = 4;
+constexpr uint32_t kMmaSmem = kMmaRing * kMmaStage + 64;
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+// D = A B for A 16 x 16 (row-major fragment a), B 16 x 8 (fragment b0, b1).
+__device__ __forceinline__ void mma_bf16(const uint32_t (&a)[4], uint32_t b0, uint32_t b1, float (&d)[4]) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%10,%10,%10,%10};"
+                 : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+template <bool ROW, bool COL>
+__global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_amax_mma(Args ar, Args ac, uint32_t ncc,
+                                                                      uint32_t nchunks) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ float s_red[kThreads / 32], s_red2[kThreads / 32];
+    const Args &a = ROW ? ar : ac;   // the input as stored (both describe the same x)
+    const uint32_t buf = ptx::smem_u32(dsm);
+    const uint32_t bars = buf + kMmaRing * kMmaStage;
+    volatile int *abort = reinterpret_cast<volatile int *>(dsm + kMmaRing * kMmaStage + 60);
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < kMmaRing; ++t) ptx::mbar_init(bars + 8u * t, 1);
+        *abort = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    const uint32_t rows = (uint32_t)a.rows, cols = (uint32_t)a.cols;
+    uint32_t issued = 0, j = 0;
+    auto issue = [&](uint32_t jj) {
+        const uint32_t i = blockIdx.x + jj * gridDim.x;
+        if (i >= nchunks) return;
+        const uint32_t kb = i / ncc, cc = i - kb * ncc;
+        const uint32_t c0 = cc * kMmaCW, r0 = kb * 16;
+        const uint32_t ncols = min(kMmaCW, cols - c0), nrows = min(16u, rows - r0);
+        const uint32_t bar = bars + 8u * (jj % kMmaRing);
+        const uint32_t st = buf + (jj % kMmaRing) * kMmaStage;
+        ptx::mbar_arrive_expect_tx(bar, nrows * ncols * 2);
+        const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(a.x) + (int64_t)r0 * a.ld + c0;
+        for (uint32_t q = 0; q < nrows; ++q) ptx::bulk_load(st + q * kMmaPitch, src + (int64_t)q * a.ld, ncols * 2, bar);
+        issued = jj + 1;
+    };
+    if (threadIdx.x == 0)
+        for (uint32_t t = 0; t < kMmaRing; ++t) issue(t);
+    // B fragments of H16 diag(d): B[k][n] = (-1)^popcount(n & k) d_k as BF16 +-1;
+    // lane l holds k = 2 (l % 4) + {0, 1} (and + 8), n = l / 4 (and + 8)
+    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t smask = rht_sign_mask(a.rht_seed);
+    auto bv = [&](uint32_t n, uint32_t k) -> uint32_t {
+        return ((__popc(n & k) ^ (smask >> k)) & 1u) ? 0xBF80u : 0x3F80u;
+    };
+    const uint32_t k0 = 2 * (lane & 3), n0 = lane >> 2;
+    const uint32_t bl0 = bv(n0, k0) | (bv(n0, k0 + 1) << 16), bl1 = bv(n0, k0 + 8) | (bv(n0, k0 + 9) << 16);
+    const uint32_t bh0 = bv(n0 + 8, k0) | (bv(n0 + 8, k0 + 1) << 16);
+    const uint32_t bh1 = bv(n0 + 8, k0 + 8) | (bv(n0 + 8, k0 + 9) << 16);
+    float mr = 0.0f, mc = 0.0f;
+    // running max of |D| over the A rows that hold data (rows m = lane / 4 and lane / 4 + 8)
+    auto acc = [&](float &m, const float (&d)[4], const float (&e)[4], bool lo_ok, bool hi_ok) {
+        if (lo_ok) m = max_nan(max_nan(m, max_nan(fabsf(d[0]), fabsf(d[1]))), max_nan(fabsf(e[0]), fabsf(e[1])));
+        if (hi_ok) m = max_nan(max_nan(m, max_nan(fabsf(d[2]), fabsf(d[3]))), max_nan(fabsf(e[2]), fabsf(e[3])));
+    };
+    auto process = [&](uint32_t jj) {
+        const uint32_t i = blockIdx.x + jj * gridDim.x;
+        const uint32_t kb = i / ncc, cc = i - kb * ncc;
+        const uint32_t c0 = cc * kMmaCW, r0 = kb * 16;
+        const uint32_t ncols = min(kMmaCW, cols - c0), nrows = min(16u, rows - r0);
+        const uint32_t st = buf + (jj % kMmaRing) * kMmaStage;
+        if (ROW) {
+            // groups = block columns b (16 rows of the chunk each); partial last rows masked
+            const bool lo_ok = n0 < nrows, hi_ok = n0 + 8 < nrows;
+            const uint32_t lrow = lane & 15, lhalf = (lane >> 4) * 16;
+#pragma unroll
+            for (uint32_t t = 0; t < kMmaCW / 16 / 8; ++t) {
+                const uint32_t b = warp + 8 * t;
+                if (b * 16 >= ncols) break;
+                uint32_t af[4];
+                ldsm_x4(st + lrow * kMmaPitch + b * 32 + lhalf, af);
+                float d[4], e[4];
+                mma_bf16(af, bl0, bl1, d);
+                mma_bf16(af, bh0, bh1, e);
+                acc(mr, d, e, lo_ok, hi_ok);
+            }
+        }
+        if (COL) {
+            // groups = 16 columns (16 rows each, loaded transposed); partial last group masked
+            const uint32_t lrow = (lane & 7) + ((lane >> 4) << 3), lcol = ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (uint32_t t = 0; t < kMmaCW / 16 / 8; ++t) {
+                const uint32_t g = warp + 8 * t;
+                if (g * 16 >= ncols) break;
+                uint32_t af[4];
+                ldsm_x4_t(st + lrow * kMmaPitch + (g * 16 + lcol) * 2, af);
+                float d[4], e[4];
+                mma_bf16(af, bl0, bl1, d);
+                mma_bf16(af, bh0, bh1, e);
+                acc(mc, d, e, g * 16 + n0 < ncols, g * 16 + n0 + 8 < ncols);
+            }
+        }
+    };
+    bool ok = true;
+    while (j < nchunks && blockIdx.x + j * gridDim.x < nchunks) {
+        const uint32_t nj = (blockIdx.x + (j + 1) * gridDim.x < nchunks) ? 2u : 1u;
+        bool mine = true;
+        for (uint32_t t = 0; t < nj && mine; ++t)
+            mine = ptx::mbar_wait_bounded(bars + 8u * ((j + t) % kMmaRing), ((j + t) / kMmaRing) & 1u, kRingWait);
+        if (!mine) *abort = 1;
+        else
+            for (uint32_t t = 0; t < nj; ++t) process(j + t);
+        __syncthreads();
+        if (*abort) { ok = false; break; }
+        if (threadIdx.x == 0)
+            for (uint32_t t = 0; t < nj; ++t) issue(j + t + kMmaRing);
+        j += nj;
+    }
+    if (!ok) {
+        if (threadIdx.x == 0) {
+            atomicOr(&g_quant_timeout, 1u);
+            for (uint32_t h = j; h < issued; ++h)
+                if (!ptx::mbar_wait_bounded(bars + 8u * (h % kMmaRing), (h / kMmaRing) & 1u, kRingWait)) break;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        mr = max_nan(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+        mc = max_nan(mc, __shfl_xor_sync(0xffffffffu, mc, o));
+    }
+    if (lane == 0) { s_red[warp] = mr; s_red2[warp] = mc; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kThreads / 32; ++w) { mr = max_nan(mr, s_red[w]); mc = max_nan(mc, s_red2[w]); }
+        if (ROW) ar.partials_out[blockIdx.x] = mr * 0.25f;
+        if (COL) ac.partials_out[blockIdx.x] = mc * 0.25f;
+    }
+}
+
 // ================================================ dual orientation (X and X^T)
 // A training step quantizes every operand both ways (X row-wise for one GEMM,
 // X^T for another).  One read serves both: the column-wise ring of 16 rows x
@@ -1326,12 +1501,11 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_dual_staged(Args a
     const uint32_t cols = (uint32_t)ar.cols;
     float mr = 0.0f, mc = 0.0f;
     bool ok = true;
-    for (; j < nloc; ++j) {
-        if (!ring_wait<kRing>(ring, j)) { ok = false; break; }
-        const uint32_t i = blockIdx.x + j * gridDim.x;
+    auto process = [&](uint32_t jj) {
+        const uint32_t i = blockIdx.x + jj * gridDim.x;
         const uint32_t kb = i / ncc, cc = i - kb * ncc;
         const uint32_t c0 = cc * CW;
-        const uint32_t st = ring.buf + (j % kRing) * kChunk;
+        const uint32_t st = ring.buf + (jj % kRing) * kChunk;
         // column-wise unit: columns (c, c + 1), rows kb*16 .. +15
         const uint32_t c = c0 + 2 * threadIdx.x;
         if (2 * threadIdx.x < CW && c < cols) {
@@ -1404,8 +1578,20 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_dual_staged(Args a
                 }
             }
         }
+    };
+    // One CTA barrier per iteration (each thread waits for its chunks itself);
+    // the amax pass, light on arithmetic, takes two chunks per iteration.
+    while (j < nloc) {
+        const uint32_t nj = (AMAX && j + 1 < nloc) ? 2u : 1u;
+        bool mine = true;
+        for (uint32_t t = 0; t < nj && mine; ++t) mine = ring_wait_own<kRing>(ring, j + t);
+        if (mine)
+            for (uint32_t t = 0; t < nj; ++t) process(j + t);
         __syncthreads();
-        if (threadIdx.x == 0) col_issue<In, kRing>(ring, ar, j + kRing, nchunks, ncc, issued);
+        if (*ring.abort) { ok = false; break; }
+        if (threadIdx.x == 0)
+            for (uint32_t t = 0; t < nj; ++t) col_issue<In, kRing>(ring, ar, j + t + kRing, nchunks, ncc, issued);
+        j += nj;
     }
     if (!ok) {
         if (threadIdx.x == 0) atomicOr(&g_quant_timeout, 1u);
@@ -1511,11 +1697,13 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas)
     float mr = 0.0f, mc = 0.0f;
     bool ok = true;
     for (; j < nloc; ++j) {
-        if (!ring_wait<kRing>(ring, j)) { ok = false; break; }
+        // each thread waits for the tile itself; no CTA barrier before the work
+        const bool mine = ring_wait_own<kRing>(ring, j);
         const uint32_t i = blockIdx.x + j * gridDim.x;
         const uint32_t rt = i / nct, ct = i - rt * nct;
         const uint32_t r0 = rt * kTileRows, c0 = ct * kTileCols;
         const uint32_t st = ring.buf + (j % kRing) * kChunk;
+        if (mine) {
         // ---- column-wise: columns c0 + 2cp, +1; rows r0 + 16 rb .. + 15
         {
             const uint32_t c = c0 + 2 * cp, kb = rt * 8 + rb;
@@ -1588,7 +1776,9 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas)
                 }
             }
         }
+        }
         __syncthreads();   // tile consumed; column-wise results staged
+        if (*ring.abort) { ok = false; break; }
         if (threadIdx.x == 0) issue(j + kRing);
         if (!AMAX) {
             // column-wise codes: column c, blocks kb0 .. kb0 + 7 = 64 contiguous bytes
@@ -2292,6 +2482,17 @@ cudaError_t amax_pass(const QuantLaunch &q, Args &a, bool staged, cudaStream_t s
     const bool col = q.colwise != 0;
     int g = 1;
     cudaError_t e;
+    if constexpr (std::is_same<In, __nv_bfloat16>::value && RHT) {
+        // BF16 with the transform: the tensor-core amax (rows as 16-byte pieces)
+        if ((a.cols * 2) % 16 == 0) {
+            const uint32_t ncc = (uint32_t)((a.cols + kMmaCW - 1) / kMmaCW);
+            const uint32_t nch = (uint32_t)((a.rows + 15) / 16) * ncc;
+            e = col ? launch_staged_smem(k_amax_mma<false, true>, kMmaSmem, nch, &g, s, a, a, ncc, nch)
+                    : launch_staged_smem(k_amax_mma<true, false>, kMmaSmem, nch, &g, s, a, a, ncc, nch);
+            a.n_partials = g;
+            return e;
+        }
+    }
     if (!col) {
         if (staged) {
             const uint64_t tb = (uint64_t)a.rows * a.cols * sizeof(In);
@@ -2367,10 +2568,19 @@ cudaError_t quantize_dual_typed(const QuantLaunch &qr, const QuantLaunch &qc, Ar
             const uint32_t ncc = (uint32_t)((ar.cols + CW - 1) / CW), nch = (uint32_t)(ar.rows / 16) * ncc;
             ar.partials_out = reinterpret_cast<float *>(static_cast<char *>(ws) + kWsPartials);
             ac.partials_out = ar.partials_out + kMaxPartials / 2;
-            auto kern = qr.rht ? k_dual_staged<In, 0, 0, true, true> : k_dual_staged<In, 0, 0, false, true>;
-            if (resident_grid(kern, nch, ring_smem<true>()) > kMaxPartials / 2) return cudaErrorInvalidValue;
             int g = 1;
-            cudaError_t e = launch_staged<true>(kern, nch, &g, s, ar, ac, ncc, nch);
+            cudaError_t e;
+            if (qr.rht) {
+                // the tensor-core amax of both orientations (CW = kMmaCW: same chunking)
+                static_assert(CW == kMmaCW, "chunk widths");
+                auto kern = k_amax_mma<true, true>;
+                if (resident_grid(kern, nch, kMmaSmem) > kMaxPartials / 2) return cudaErrorInvalidValue;
+                e = launch_staged_smem(kern, kMmaSmem, nch, &g, s, ar, ac, ncc, nch);
+            } else {
+                auto kern = k_dual_staged<In, 0, 0, false, true>;
+                if (resident_grid(kern, nch, ring_smem<true>()) > kMaxPartials / 2) return cudaErrorInvalidValue;
+                e = launch_staged<true>(kern, nch, &g, s, ar, ac, ncc, nch);
+            }
             if (e != cudaSuccess) return e;
             ar.partials = ar.partials_out;
             ac.partials = ac.partials_out;
