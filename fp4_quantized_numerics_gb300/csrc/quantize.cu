@@ -297,6 +297,13 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
     return r;
 }
 
+// max(a, b, c) in one instruction (PTX three-input max; NaN as fmaxf).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // RHT sign flips, precomputed once per thread as XOR masks on the loaded
 // words: row-wise BF16 word i holds elements (2i, 2i+1) -> bits 15 / 31;
 // row-wise FP32 word e -> bit 31; column-wise BF16 row i holds two columns
@@ -306,12 +313,14 @@ struct Signs {
 };
 template <class In> __device__ __forceinline__ Signs row_signs(uint32_t smask);
 template <> __device__ __forceinline__ Signs row_signs<__nv_bfloat16>(uint32_t smask) {
+    // word i holds elements 2i (low half) and 2i + 1 (high half): m[i] is the
+    // fp32 sign bit of element 2i, m[8 + i] that of element 2i + 1
     Signs s;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        s.m[i] = (((smask >> (2 * i)) & 1u) << 15) | (((smask >> (2 * i + 1)) & 1u) << 31);
-#pragma unroll
-    for (int i = 8; i < 16; ++i) s.m[i] = 0u;
+    for (int i = 0; i < 8; ++i) {
+        s.m[i] = ((smask >> (2 * i)) & 1u) << 31;
+        s.m[8 + i] = ((smask >> (2 * i + 1)) & 1u) << 31;
+    }
     return s;
 }
 template <> __device__ __forceinline__ Signs row_signs<float>(uint32_t smask) {
@@ -322,9 +331,10 @@ template <> __device__ __forceinline__ Signs row_signs<float>(uint32_t smask) {
 }
 template <class In> __device__ __forceinline__ Signs col_signs(uint32_t smask);
 template <> __device__ __forceinline__ Signs col_signs<__nv_bfloat16>(uint32_t smask) {
+    // row i of a column unit: both columns take the fp32 sign bit m[i]
     Signs s;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) s.m[i] = ((smask >> i) & 1u) ? 0x80008000u : 0u;
+    for (int i = 0; i < 16; ++i) s.m[i] = ((smask >> i) & 1u) << 31;
     return s;
 }
 template <> __device__ __forceinline__ Signs col_signs<float>(uint32_t smask) {
@@ -333,6 +343,17 @@ template <> __device__ __forceinline__ Signs col_signs<float>(uint32_t smask) {
     for (int i = 0; i < 16; ++i) s.m[i] = ((smask >> i) & 1u) << 31;
     return s;
 }
+
+// BF16 halves of a 32-bit word as fp32 bit patterns, with the fp32 sign bit
+// `sb` (0 or 1 << 31) flipped in: the low half as w * 2^16 + sb (one
+// multiply-add: the product's low 16 bits are zero, so adding bit 31 flips
+// it), the high half as (w & 0xFFFF0000) ^ sb (one three-input logic op).
+__device__ __forceinline__ uint32_t bf16lo_s(uint32_t w, uint32_t sb) {
+    uint32_t r;
+    asm("mad.lo.u32 %0, %1, 65536, %2;" : "=r"(r) : "r"(w), "r"(sb));
+    return r;
+}
+__device__ __forceinline__ uint32_t bf16hi_s(uint32_t w, uint32_t sb) { return (w & 0xFFFF0000u) ^ sb; }
 
 // Raw 16 elements of one block.
 template <class In> struct Raw;
@@ -355,10 +376,9 @@ template <> struct Raw<__nv_bfloat16> {
         asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                      : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]) : "r"(sa + 16));
     }
-    // element e as fp32, with the row-wise sign masks applied
+    // element e as fp32, with the row-wise sign applied
     __device__ __forceinline__ float get(int e, const Signs &sg) const {
-        const uint32_t u = w[e >> 1] ^ sg.m[e >> 1];
-        return __uint_as_float((e & 1) ? (u & 0xFFFF0000u) : (u << 16));
+        return __uint_as_float((e & 1) ? bf16hi_s(w[e >> 1], sg.m[8 + (e >> 1)]) : bf16lo_s(w[e >> 1], sg.m[e >> 1]));
     }
     __device__ __forceinline__ float get(int e) const {
         const uint32_t u = w[e >> 1];
@@ -598,7 +618,7 @@ __device__ __forceinline__ void quant_block_row(const Args &a, const Raw<In> &ra
     UFP4_PROBE_ROW8(a, r, b, lo, hi, RHT);
     float m = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) m = fmaxf(m, fmaxf(fabsf(lo[j]), fabsf(hi[j])));
+    for (int j = 0; j < 8; ++j) m = max3f(m, fabsf(lo[j]), fabsf(hi[j]));
     if (RHT) m *= 0.25f;
     const uint32_t e = block_scale(m, qmax, S_enc);
     const float kk = s_k ? s_k[e] : inline_k(e, S_enc, RHT);
@@ -668,7 +688,7 @@ __device__ __forceinline__ void quant_block_row_stats(const Args &a, const Raw<I
     block_values<In, RHT>(raw, sg, lo, hi);
     float m = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) m = fmaxf(m, fmaxf(fabsf(lo[j]), fabsf(hi[j])));
+    for (int j = 0; j < 8; ++j) m = max3f(m, fabsf(lo[j]), fabsf(hi[j]));
     if (RHT) m *= 0.25f;
     const uint32_t e = block_scale(m, qmax, S_enc);
     const float kk = s_k ? s_k[e] : inline_k(e, S_enc, RHT);
@@ -717,10 +737,11 @@ __device__ __forceinline__ void quant_pair_row(const Args &a, const Raw<__nv_bfl
     float va[16], vb[16];
     float ma = 0.0f, mb = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        upk2(P[j], va[j], vb[j]);
-        ma = fmaxf(ma, fabsf(va[j]));
-        mb = fmaxf(mb, fabsf(vb[j]));
+    for (int j = 0; j < 16; ++j) upk2(P[j], va[j], vb[j]);
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+        ma = max3f(ma, fabsf(va[j]), fabsf(va[j + 1]));
+        mb = max3f(mb, fabsf(vb[j]), fabsf(vb[j + 1]));
     }
     UFP4_PROBE_ROW16(a, r0, b0, va, RHT);
     if (has_b) UFP4_PROBE_ROW16(a, r1, b1, vb, RHT);
@@ -809,8 +830,7 @@ template <> struct ColRaw<__nv_bfloat16> {
         for (int i = 0; i < 16; ++i) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w[i]) : "r"(sa + i * pitch));
     }
     __device__ __forceinline__ uint64_t pair(int i, const Signs &sg) const {
-        const uint32_t u = w[i] ^ sg.m[i];
-        return pk2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+        return pk2(__uint_as_float(bf16lo_s(w[i], sg.m[i])), __uint_as_float(bf16hi_s(w[i], sg.m[i])));
     }
     __device__ __forceinline__ uint64_t pair(int i) const {
         const uint32_t u = w[i];
@@ -932,10 +952,11 @@ __device__ __forceinline__ void col_unit_words(const Args &a, const ColRaw<In> &
     float v0[16], v1[16];
     float m0 = 0.0f, m1 = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        upk2(P[i], v0[i], v1[i]);
-        m0 = fmaxf(m0, fabsf(v0[i]));
-        m1 = fmaxf(m1, fabsf(v1[i]));
+    for (int i = 0; i < 16; ++i) upk2(P[i], v0[i], v1[i]);
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+        m0 = max3f(m0, fabsf(v0[i]), fabsf(v0[i + 1]));
+        m1 = max3f(m1, fabsf(v1[i]), fabsf(v1[i + 1]));
     }
     if (real) {
         UFP4_PROBE_COL16(a, c, kb, v0, RHT);
@@ -1355,6 +1376,9 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_amax_mma(Args ar, 
     __syncthreads();
     const uint32_t rows = (uint32_t)a.rows, cols = (uint32_t)a.cols;
     uint32_t issued = 0, j = 0;
+    // Chunk jj's 16 row copies are issued by the eight warps' lane 0, two rows
+    // each; thread 0 also posts the chunk's byte count (the barrier's phase
+    // needs that single arrival, so copies may land before or after it).
     auto issue = [&](uint32_t jj) {
         const uint32_t i = blockIdx.x + jj * gridDim.x;
         if (i >= nchunks) return;
@@ -1363,12 +1387,13 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_amax_mma(Args ar, 
         const uint32_t ncols = min(kMmaCW, cols - c0), nrows = min(16u, rows - r0);
         const uint32_t bar = bars + 8u * (jj % kMmaRing);
         const uint32_t st = buf + (jj % kMmaRing) * kMmaStage;
-        ptx::mbar_arrive_expect_tx(bar, nrows * ncols * 2);
+        if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(bar, nrows * ncols * 2);
         const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(a.x) + (int64_t)r0 * a.ld + c0;
-        for (uint32_t q = 0; q < nrows; ++q) ptx::bulk_load(st + q * kMmaPitch, src + (int64_t)q * a.ld, ncols * 2, bar);
+        for (uint32_t q = 2 * (threadIdx.x >> 5); q < min(nrows, 2 * (threadIdx.x >> 5) + 2); ++q)
+            ptx::bulk_load(st + q * kMmaPitch, src + (int64_t)q * a.ld, ncols * 2, bar);
         issued = jj + 1;
     };
-    if (threadIdx.x == 0)
+    if ((threadIdx.x & 31) == 0)
         for (uint32_t t = 0; t < kMmaRing; ++t) issue(t);
     // B fragments of H16 diag(d): B[k][n] = (-1)^popcount(n & k) d_k as BF16 +-1;
     // lane l holds k = 2 (l % 4) + {0, 1} (and + 8), n = l / 4 (and + 8)
@@ -1436,16 +1461,16 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_amax_mma(Args ar, 
             for (uint32_t t = 0; t < nj; ++t) process(j + t);
         __syncthreads();
         if (*abort) { ok = false; break; }
-        if (threadIdx.x == 0)
+        if ((threadIdx.x & 31) == 0)
             for (uint32_t t = 0; t < nj; ++t) issue(j + t + kMmaRing);
         j += nj;
     }
     if (!ok) {
-        if (threadIdx.x == 0) {
-            atomicOr(&g_quant_timeout, 1u);
+        // every copy issued and not consumed lands before the CTA exits
+        if (threadIdx.x == 0) atomicOr(&g_quant_timeout, 1u);
+        if ((threadIdx.x & 31) == 0)
             for (uint32_t h = j; h < issued; ++h)
                 if (!ptx::mbar_wait_bounded(bars + 8u * (h % kMmaRing), (h / kMmaRing) & 1u, kRingWait)) break;
-        }
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
