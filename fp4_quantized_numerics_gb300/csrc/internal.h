@@ -9,6 +9,7 @@ namespace ufp4 {
 
 // Workspace layout (bytes from the start of the caller's scratch buffer).
 constexpr size_t kWsStatus = 0;            // uint32 status word
+constexpr size_t kWsArrive = 8;            // uint32 grid-barrier counter of the single-pass quantizer
 constexpr size_t kWsPartials = 256;        // float partial maxima
 constexpr int kMaxPartials = 4096;
 constexpr size_t kWsStats = 32768;         // double partial sums, 8 per CTA

@@ -143,7 +143,7 @@ __device__ __forceinline__ void tensor_scale_prologue(const Args &a, float qmax,
     if (a.amax_in) {
         m = *a.amax_in;
     } else {
-        for (int i = threadIdx.x; i < a.n_partials; i += blockDim.x) m = max_nan(m, a.partials[i]);
+        for (int i = threadIdx.x; i < a.n_partials; i += blockDim.x) m = max_nan(m, __ldcg(a.partials + i));
 #pragma unroll
         for (int o = 16; o; o >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
         if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m;
@@ -1668,17 +1668,123 @@ constexpr uint32_t kTileRows = 128, kTileCols = 64;
 constexpr uint32_t kTileBytes = kTileRows * kTileCols * 2;   // BF16
 static_assert(kTileBytes == kChunk, "a tile fills one ring stage");
 constexpr uint32_t kColStageBytes = 8 * kTileCols * 8 + 8 * kTileCols;   // codes [8][64] x 8 B + scales [8][64]
-template <bool AMAX> constexpr uint32_t tile_smem() { return ring_smem<AMAX>() + (AMAX ? 0u : kColStageBytes); }
+constexpr uint32_t kTileSmem = ring_smem<false>() + kColStageBytes;
 
-template <int GRID, int ROUND, bool RHT, bool AMAX>
+// Geometry of the dual-orientation tile kernels, fixed per launch.
+struct DualGeom {
+    uint32_t csr, nktr, csc, nktc;   // code row strides (bytes) and k atoms of the two results
+    uint32_t cols, rows;             // the input
+    uint32_t kvr, kbr, kbp;          // real row-wise blocks per row; real and padded column-wise blocks
+    uint32_t cp, rb, q, bc;          // this thread's column pair / row block, and row / block column
+};
+__device__ __forceinline__ DualGeom dual_geom(const Args &ar, const Args &ac) {
+    DualGeom g;
+    g.csr = (uint32_t)(ar.kpad / 2); g.nktr = (uint32_t)ar.nkt;
+    g.csc = (uint32_t)(ac.kpad / 2); g.nktc = (uint32_t)ac.nkt;
+    g.cols = (uint32_t)ar.cols; g.rows = (uint32_t)ar.rows;
+    g.kvr = g.cols / 16; g.kbr = g.rows / 16; g.kbp = (uint32_t)(ac.kpad / 16);
+    g.cp = threadIdx.x % 32; g.rb = threadIdx.x / 32;
+    g.q = threadIdx.x / 4; g.bc = threadIdx.x % 4;
+    return g;
+}
+
+// Quantization of one 128 x 64 BF16 tile (rt, ct) held at shared address st,
+// both orientations.  Column-wise: this thread's unit (columns c0 + 2 cp, +1;
+// rows r0 + 16 rb .. + 15), staged in stage_codes / stage_scales when STAGE
+// (written out by dual_tile_flush), else stored directly.  Row-wise: rows
+// r0 + q and r0 + q + 64, block c0 / 16 + bc, stored directly.
+template <int GRID, int ROUND, bool RHT, bool STAGE>
+__device__ __forceinline__ void dual_tile_quant(const Args &ar, const Args &ac, const DualGeom &g, uint32_t st,
+                                                uint32_t rt, uint32_t ct, const Signs &sgr, const Signs &sgc,
+                                                float Sr, float Sc, const float *s_kr, const float *s_kc, bool fr,
+                                                bool fc, uint8_t *stage_codes, uint8_t *stage_scales) {
+    const uint32_t r0 = rt * kTileRows, c0 = ct * kTileCols;
+    {
+        const uint32_t c = c0 + 2 * g.cp, kb = rt * 8 + g.rb;
+        ColRaw<__nv_bfloat16> raw;
+        raw.load_shared(st + 16 * g.rb * (kTileCols * 2) + g.cp * 4, kTileCols * 2);
+        if (STAGE) {
+            uint2 w0 = make_uint2(0u, 0u), w1 = make_uint2(0u, 0u);
+            uint32_t e0 = 0, e1 = 0;
+            if (c < g.cols && kb < g.kbr)
+                col_unit_words<__nv_bfloat16, GRID, ROUND, RHT>(ac, raw, kb, c, true, sgc, Sc, s_kc, fc, w0, w1, e0,
+                                                                e1);
+            // staging [rb][column] (consecutive columns -> consecutive words)
+            reinterpret_cast<uint2 *>(stage_codes)[g.rb * kTileCols + 2 * g.cp] = w0;
+            reinterpret_cast<uint2 *>(stage_codes)[g.rb * kTileCols + 2 * g.cp + 1] = w1;
+            stage_scales[g.rb * kTileCols + 2 * g.cp] = (uint8_t)e0;
+            stage_scales[g.rb * kTileCols + 2 * g.cp + 1] = (uint8_t)e1;
+        } else if (c < g.cols && kb < g.kbp) {
+            // padding blocks past the last row are written as zeros
+            quant_unit_col<__nv_bfloat16, GRID, ROUND, RHT>(ac, raw, kb, c, kb < g.kbr, sgc, Sc, s_kc, g.csc, g.nktc,
+                                                            fc);
+        }
+    }
+    {
+        const uint32_t r = r0 + g.q, b = ct * (kTileCols / 16) + g.bc;
+        if (r < g.rows && b < g.kvr) {
+            Raw<__nv_bfloat16> ra, rbw;
+            ra.load_shared(st + g.q * (kTileCols * 2) + g.bc * 32);
+            rbw.load_shared(st + (g.q + 64) * (kTileCols * 2) + g.bc * 32);
+            // one block at a time (measured faster than the packed pair, which
+            // holds twice the registers)
+            quant_block_row<__nv_bfloat16, GRID, ROUND, RHT>(ar, ra, r, b, sgr, Sr, s_kr, g.csr, g.nktr, fr);
+            if (r + 64 < g.rows)
+                quant_block_row<__nv_bfloat16, GRID, ROUND, RHT>(ar, rbw, r + 64, b, sgr, Sr, s_kr, g.csr, g.nktr, fr);
+        }
+    }
+}
+
+// The staged column-wise results of tile (rt, ct): column c, blocks
+// rt * 8 .. + 7 = 64 contiguous code bytes (16 per thread), and the scales as
+// two 4-byte words of an atom.
+__device__ __forceinline__ void dual_tile_flush(const Args &ac, const DualGeom &g, uint32_t rt, uint32_t ct,
+                                                const uint8_t *stage_codes, const uint8_t *stage_scales) {
+    const uint32_t c0 = ct * kTileCols, kb0 = rt * 8;
+    {
+        const uint32_t cl = threadIdx.x / 4, part = threadIdx.x % 4;
+        const uint32_t c = c0 + cl, kb = kb0 + 2 * part;
+        if (c < g.cols && kb < g.kbp) {
+            const uint2 a0 = reinterpret_cast<const uint2 *>(stage_codes)[(2 * part) * kTileCols + cl];
+            const uint2 a1 = reinterpret_cast<const uint2 *>(stage_codes)[(2 * part + 1) * kTileCols + cl];
+            put_codes(ac, (size_t)c * g.csc + kb * 8, make_uint4(a0.x, a0.y, a1.x, a1.y));
+        }
+    }
+    if (threadIdx.x < 2 * kTileCols) {
+        const uint32_t cl = threadIdx.x / 2, h = threadIdx.x % 2;
+        const uint32_t c = c0 + cl, kb = kb0 + 4 * h;
+        if (c < g.cols && kb < g.kbp) {
+            uint32_t w = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) w |= (uint32_t)stage_scales[(4 * h + k) * kTileCols + cl] << (8 * k);
+            *reinterpret_cast<uint32_t *>(ac.scales + scale_offset32(c, kb, g.nktc)) = w;
+        }
+    }
+}
+
+// Row-wise padding blocks cols/16 .. kpad/16 - 1 of every row of a dual
+// result, and the scale entries of both results' padding rows.
+__device__ __forceinline__ void dual_padding(const Args &ar, const Args &ac, const DualGeom &g) {
+    const uint32_t nbr = (uint32_t)(ar.kpad / 16) - g.kvr;
+    const uint32_t npr = (uint32_t)ar.out_rows * nbr;
+    for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < npr; t += gridDim.x * blockDim.x) {
+        const uint32_t r = t / nbr, b = g.kvr + (t - r * nbr);
+        put_codes(ar, (size_t)r * g.csr + b * 8, make_uint2(0u, 0u));
+        ar.scales[scale_offset32(r, b, g.nktr)] = 0;
+    }
+    zero_pad_rows(ar);
+    zero_pad_rows(ac);   // column-wise padding blocks come from zero-filled tile rows
+}
+
+template <int GRID, int ROUND, bool RHT>
 __global__ void __launch_bounds__(kThreads, kStagedMinCtas)
     k_dual_tile(const __grid_constant__ CUtensorMap tmx, Args ar, Args ac, uint32_t nct, uint32_t ntiles) {
-    constexpr int kRing = ring_depth<AMAX>();
+    constexpr int kRing = ring_depth<false>();
     extern __shared__ __align__(128) uint8_t dsm[];
     __shared__ float s_kr[256], s_kc[256];
-    __shared__ float s_red[kThreads / 32], s_red2[kThreads / 32];
+    __shared__ float s_red[kThreads / 32];
     const RingCtl ring = ring_init<kRing>(dsm);
-    uint8_t *stage_codes = dsm + kRing * kChunk + 64;            // [rb][cl] uint2 (quantization pass only)
+    uint8_t *stage_codes = dsm + kRing * kChunk + 64;            // [rb][cl] uint2
     uint8_t *stage_scales = stage_codes + 8 * kTileCols * 8;    // [rb][cl] byte
     uint32_t issued = 0, j = 0;
     auto issue = [&](uint32_t jj) {
@@ -1698,168 +1804,202 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas)
     const float qmax = GRID == kE2M1 ? 6.0f : ar.uqmax;
     float Sr = 1.0f, Sc = 1.0f;
     bool fr = false, fc = false;
-    if (!AMAX) {
-        float amr = 0.0f, amc = 0.0f;
-        tensor_scale_prologue(ar, qmax, RHT ? 0.25f : 1.0f, s_kr, s_red, Sr, GRID == kE1M2 && ROUND == kRTNE, &fr,
-                              &amr);
-        tensor_scale_prologue(ac, qmax, RHT ? 0.25f : 1.0f, s_kc, s_red, Sc, GRID == kE1M2 && ROUND == kRTNE, &fc,
-                              &amc);
-        if (blockIdx.x == 0 && threadIdx.x == 0 && ar.status && !isfinite(amc)) *ar.status = 1u;
-    }
+    float amr = 0.0f, amc = 0.0f;
+    tensor_scale_prologue(ar, qmax, RHT ? 0.25f : 1.0f, s_kr, s_red, Sr, GRID == kE1M2 && ROUND == kRTNE, &fr, &amr);
+    tensor_scale_prologue(ac, qmax, RHT ? 0.25f : 1.0f, s_kc, s_red, Sc, GRID == kE1M2 && ROUND == kRTNE, &fc, &amc);
+    if (blockIdx.x == 0 && threadIdx.x == 0 && ar.status && !isfinite(amc)) *ar.status = 1u;
     const uint32_t smask = RHT ? rht_sign_mask(ar.rht_seed) : 0u;
     const Signs sgr = row_signs<__nv_bfloat16>(smask), sgc = col_signs<__nv_bfloat16>(smask);
     const uint32_t nloc = ntiles > blockIdx.x ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-    const uint32_t csr = (uint32_t)(ar.kpad / 2), nktr = (uint32_t)ar.nkt;
-    const uint32_t csc = (uint32_t)(ac.kpad / 2), nktc = (uint32_t)ac.nkt;
-    const uint32_t cols = (uint32_t)ar.cols, rows = (uint32_t)ar.rows;
-    const uint32_t kvr = cols / 16;               // real row-wise blocks per row
-    const uint32_t kbr = rows / 16;               // real column-wise blocks per column
-    const uint32_t kbp = (uint32_t)(ac.kpad / 16);   // column-wise blocks incl. padding
-    // column-wise unit of this thread: column pair cp, row block rb of the tile
-    const uint32_t cp = threadIdx.x % 32, rb = threadIdx.x / 32;
-    // row-wise pair of this thread: rows q and q + 64, block column bc of the tile
-    const uint32_t q = threadIdx.x / 4, bc = threadIdx.x % 4;
-    float mr = 0.0f, mc = 0.0f;
+    const DualGeom g = dual_geom(ar, ac);
     bool ok = true;
     for (; j < nloc; ++j) {
         // each thread waits for the tile itself; no CTA barrier before the work
         const bool mine = ring_wait_own<kRing>(ring, j);
         const uint32_t i = blockIdx.x + j * gridDim.x;
         const uint32_t rt = i / nct, ct = i - rt * nct;
-        const uint32_t r0 = rt * kTileRows, c0 = ct * kTileCols;
-        const uint32_t st = ring.buf + (j % kRing) * kChunk;
-        if (mine) {
-        // ---- column-wise: columns c0 + 2cp, +1; rows r0 + 16 rb .. + 15
-        {
-            const uint32_t c = c0 + 2 * cp, kb = rt * 8 + rb;
-            ColRaw<__nv_bfloat16> raw;
-            raw.load_shared(st + 16 * rb * (kTileCols * 2) + cp * 4, kTileCols * 2);
-            if (AMAX) {
-                if (c < cols && kb < kbr) {
-                    uint64_t P[16];
-                    col_values<__nv_bfloat16, RHT>(raw, sgc, P);
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        float v0, v1;
-                        upk2(P[k], v0, v1);
-                        mc = max_nan(mc, max_nan(fabsf(v0), fabsf(v1)));
-                    }
-                }
-            } else {
-                uint2 w0 = make_uint2(0u, 0u), w1 = make_uint2(0u, 0u);
-                uint32_t e0 = 0, e1 = 0;
-                if (c < cols && kb < kbr)
-                    col_unit_words<__nv_bfloat16, GRID, ROUND, RHT>(ac, raw, kb, c, true, sgc, Sc, s_kc, fc, w0, w1,
-                                                                    e0, e1);
-                // staging [rb][column] (consecutive columns -> consecutive words)
-                reinterpret_cast<uint2 *>(stage_codes)[rb * kTileCols + 2 * cp] = w0;
-                reinterpret_cast<uint2 *>(stage_codes)[rb * kTileCols + 2 * cp + 1] = w1;
-                stage_scales[rb * kTileCols + 2 * cp] = (uint8_t)e0;
-                stage_scales[rb * kTileCols + 2 * cp + 1] = (uint8_t)e1;
-            }
-        }
-        // ---- row-wise: rows r0 + q and r0 + q + 64, block c0 / 16 + bc
-        {
-            const uint32_t r = r0 + q, b = ct * (kTileCols / 16) + bc;
-            if (r < rows && b < kvr) {
-                Raw<__nv_bfloat16> ra, rbw;
-                ra.load_shared(st + q * (kTileCols * 2) + bc * 32);
-                rbw.load_shared(st + (q + 64) * (kTileCols * 2) + bc * 32);
-                if (AMAX) {
-                    const bool has1 = r + 64 < rows;
-                    uint64_t P[16];
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        P[k] = RHT ? pk2(ra.get(k, sgr), rbw.get(k, sgr)) : pk2(ra.get(k), rbw.get(k));
-                    if (RHT) {
-#pragma unroll
-                        for (int sgs = 1; sgs < 16; sgs <<= 1) {
-#pragma unroll
-                            for (int k = 0; k < 16; ++k) {
-                                if ((k & sgs) == 0) {
-                                    const uint64_t xx = P[k], yy = P[k + sgs];
-                                    P[k] = add2(xx, yy);
-                                    P[k + sgs] = sub2(xx, yy);
-                                }
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        float u0, u1;
-                        upk2(P[k], u0, u1);
-                        mr = max_nan(mr, fabsf(u0));
-                        if (has1) mr = max_nan(mr, fabsf(u1));   // rows past the end are zeros anyway
-                    }
-                } else {
-                    // one block at a time (measured faster here than the packed
-                    // pair, which holds twice the registers)
-                    quant_block_row<__nv_bfloat16, GRID, ROUND, RHT>(ar, ra, r, b, sgr, Sr, s_kr, csr, nktr, fr);
-                    if (r + 64 < rows)
-                        quant_block_row<__nv_bfloat16, GRID, ROUND, RHT>(ar, rbw, r + 64, b, sgr, Sr, s_kr, csr, nktr,
-                                                                         fr);
-                }
-            }
-        }
-        }
+        if (mine)
+            dual_tile_quant<GRID, ROUND, RHT, true>(ar, ac, g, ring.buf + (j % kRing) * kChunk, rt, ct, sgr, sgc, Sr,
+                                                    Sc, s_kr, s_kc, fr, fc, stage_codes, stage_scales);
         __syncthreads();   // tile consumed; column-wise results staged
         if (*ring.abort) { ok = false; break; }
         if (threadIdx.x == 0) issue(j + kRing);
-        if (!AMAX) {
-            // column-wise codes: column c, blocks kb0 .. kb0 + 7 = 64 contiguous bytes
-            const uint32_t kb0 = rt * 8;
-            {
-                const uint32_t cl = threadIdx.x / 4, part = threadIdx.x % 4;   // 16 bytes each
-                const uint32_t c = c0 + cl, kb = kb0 + 2 * part;
-                if (c < cols && kb < kbp) {
-                    const uint2 a0 = reinterpret_cast<const uint2 *>(stage_codes)[(2 * part) * kTileCols + cl];
-                    const uint2 a1 = reinterpret_cast<const uint2 *>(stage_codes)[(2 * part + 1) * kTileCols + cl];
-                    put_codes(ac, (size_t)c * csc + kb * 8, make_uint4(a0.x, a0.y, a1.x, a1.y));
-                }
-            }
-            // column-wise scales: column c, blocks kb0 + 4h .. + 3 = one 4-byte word of an atom
-            if (threadIdx.x < 2 * kTileCols) {
-                const uint32_t cl = threadIdx.x / 2, h = threadIdx.x % 2;
-                const uint32_t c = c0 + cl, kb = kb0 + 4 * h;
-                if (c < cols && kb < kbp) {
-                    uint32_t w = 0;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) w |= (uint32_t)stage_scales[(4 * h + k) * kTileCols + cl] << (8 * k);
-                    *reinterpret_cast<uint32_t *>(ac.scales + scale_offset32(c, kb, nktc)) = w;
-                }
-            }
-            __syncthreads();   // staging buffers free for the next tile
-        }
+        dual_tile_flush(ac, g, rt, ct, stage_codes, stage_scales);
+        __syncthreads();   // staging buffers free for the next tile
     }
     if (!ok) {
         if (threadIdx.x == 0) atomicOr(&g_quant_timeout, 1u);
         ring_drain<kRing>(ring, j, issued);
     }
-    if (AMAX) {
+    dual_padding(ar, ac, g);
+}
+
+// ======================================== on-chip single pass (dual, BF16)
+// For a tensor that fits in the GPU's shared memory (up to kResidentMax
+// 128 x 64 tiles per SM), one cooperative launch of one CTA per SM reads it
+// once: each CTA loads its tiles (TMA) and keeps them resident, computes both
+// orientations' maxima from them -- with the transform through the same
+// tensor-core products as k_amax_mma, so the result is bit for bit the
+// two-pass one -- and writes one partial maximum per orientation; after a
+// bounded grid barrier (a counter in the workspace that the launch zeroes)
+// every CTA reduces all partials to the two tensor scales and quantizes its
+// resident tiles.  The input's second read, and a launch, go away.
+constexpr uint32_t kResidentMax = 14;
+constexpr uint32_t kResidentSmem = kResidentMax * kTileBytes + 128;
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Maxima of |4 y| (or |x| without the transform) of one resident tile, row-wise
+// blocks into mr and column-wise blocks into mc.  Elements outside the tensor
+// arrive as zeros.
+template <bool RHT>
+__device__ __forceinline__ void tile_maxima(uint32_t st, uint32_t bl0, uint32_t bl1, uint32_t bh0, uint32_t bh1,
+                                            float &mr, float &mc) {
+    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (!RHT) {
+        // the orientations share max |x|: the thread's two row-wise blocks
+        const uint32_t q = threadIdx.x / 4, bc = threadIdx.x % 4;
+        Raw<__nv_bfloat16> ra, rb;
+        ra.load_shared(st + q * (kTileCols * 2) + bc * 32);
+        rb.load_shared(st + (q + 64) * (kTileCols * 2) + bc * 32);
 #pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            mr = max_nan(mr, __shfl_xor_sync(0xffffffffu, mr, o));
-            mc = max_nan(mc, __shfl_xor_sync(0xffffffffu, mc, o));
-        }
-        if ((threadIdx.x & 31) == 0) { s_red[threadIdx.x >> 5] = mr; s_red2[threadIdx.x >> 5] = mc; }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            for (int w = 1; w < kThreads / 32; ++w) { mr = max_nan(mr, s_red[w]); mc = max_nan(mc, s_red2[w]); }
-            ar.partials_out[blockIdx.x] = RHT ? mr * 0.25f : mr;
-            ac.partials_out[blockIdx.x] = RHT ? mc * 0.25f : mc;
-        }
-    } else {
-        // row-wise result: padding blocks cols/16 .. kpad/16 - 1 of every row
-        const uint32_t nbr = (uint32_t)(ar.kpad / 16) - kvr;
-        const uint32_t npr = (uint32_t)ar.out_rows * nbr;
-        for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < npr; t += gridDim.x * blockDim.x) {
-            const uint32_t r = t / nbr, b = kvr + (t - r * nbr);
-            put_codes(ar, (size_t)r * csr + b * 8, make_uint2(0u, 0u));
-            ar.scales[scale_offset32(r, b, nktr)] = 0;
-        }
-        zero_pad_rows(ar);
-        zero_pad_rows(ac);   // column-wise padding blocks were written from zero tiles above
+        for (int e = 0; e < 16; ++e) mr = max_nan(mr, max_nan(fabsf(ra.get(e)), fabsf(rb.get(e))));
+        mc = mr;
+        return;
     }
+#pragma unroll
+    for (uint32_t u = 0; u < 4; ++u) {
+        const uint32_t G = warp + 8 * u, band = G / 4, sft = G % 4;
+        float d[4], e[4];
+        uint32_t af[4];
+        // row-wise: A row m = tile row 16 band + m, block column (sft + m) % 4
+        {
+            const uint32_t m = lane & 15, half = lane >> 4;
+            ldsm_x4(st + (band * 16 + m) * (kTileCols * 2) + ((sft + m) & 3) * 32 + half * 16, af);
+            mma_bf16(af, bl0, bl1, d);
+            mma_bf16(af, bh0, bh1, e);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mr = max_nan(mr, max_nan(fabsf(d[k]), fabsf(e[k])));
+        }
+        // column-wise: A row m = column 16 sft + m, k = tile rows 16 band .. + 15
+        {
+            const uint32_t lrow = (lane & 7) + ((lane >> 4) << 3), lcol = ((lane >> 3) & 1) * 8;
+            ldsm_x4_t(st + (band * 16 + lrow) * (kTileCols * 2) + (sft * 16 + lcol) * 2, af);
+            mma_bf16(af, bl0, bl1, d);
+            mma_bf16(af, bh0, bh1, e);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mc = max_nan(mc, max_nan(fabsf(d[k]), fabsf(e[k])));
+        }
+    }
+}
+
+template <int GRID, int ROUND, bool RHT>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_dual_resident(const __grid_constant__ CUtensorMap tmx, Args ar, Args ac, uint32_t nct, uint32_t ntiles,
+                    uint32_t *arrive) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ float s_kr[256], s_kc[256];
+    __shared__ float s_red[kThreads / 32], s_red2[kThreads / 32];
+    __shared__ int s_go;
+    const uint32_t buf = ptx::smem_u32(dsm);
+    const uint32_t bars = buf + kResidentMax * kTileBytes;
+    const uint32_t nloc = ntiles > blockIdx.x ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    auto tile_of = [&](uint32_t t, uint32_t &rt, uint32_t &ct) {
+        const uint32_t i = blockIdx.x + t * gridDim.x;
+        rt = i / nct;
+        ct = i - rt * nct;
+    };
+    if (threadIdx.x == 0) {
+        for (uint32_t t = 0; t < nloc; ++t) ptx::mbar_init(bars + 8u * t, 1);
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tmx);
+        for (uint32_t t = 0; t < nloc; ++t) {
+            uint32_t rt, ct;
+            tile_of(t, rt, ct);
+            ptx::mbar_arrive_expect_tx(bars + 8u * t, kTileBytes);
+            ptx::tma_load_2d(buf + t * kTileBytes, &tmx, (int32_t)(ct * kTileCols), (int32_t)(rt * kTileRows),
+                             bars + 8u * t);
+        }
+    }
+    __syncthreads();
+    // 1. both orientations' maxima over the resident tiles
+    const uint32_t smask = RHT ? rht_sign_mask(ar.rht_seed) : 0u;
+    uint32_t bl0 = 0, bl1 = 0, bh0 = 0, bh1 = 0;
+    if (RHT) {
+        const uint32_t lane = threadIdx.x & 31, k0 = 2 * (lane & 3), n0 = lane >> 2;
+        auto bv = [&](uint32_t n, uint32_t k) -> uint32_t {
+            return ((__popc(n & k) ^ (smask >> k)) & 1u) ? 0xBF80u : 0x3F80u;
+        };
+        bl0 = bv(n0, k0) | (bv(n0, k0 + 1) << 16);
+        bl1 = bv(n0, k0 + 8) | (bv(n0, k0 + 9) << 16);
+        bh0 = bv(n0 + 8, k0) | (bv(n0 + 8, k0 + 1) << 16);
+        bh1 = bv(n0 + 8, k0 + 8) | (bv(n0 + 8, k0 + 9) << 16);
+    }
+    float mr = 0.0f, mc = 0.0f;
+    bool ok = true;
+    for (uint32_t t = 0; t < nloc && ok; ++t) {
+        ok = ptx::mbar_wait_bounded(bars + 8u * t, 0u, kRingWait);
+        if (ok) tile_maxima<RHT>(buf + t * kTileBytes, bl0, bl1, bh0, bh1, mr, mc);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        mr = max_nan(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+        mc = max_nan(mc, __shfl_xor_sync(0xffffffffu, mc, o));
+    }
+    if ((threadIdx.x & 31) == 0) { s_red[threadIdx.x >> 5] = mr; s_red2[threadIdx.x >> 5] = mc; }
+    ok = __syncthreads_and(ok) != 0;
+    // 2. partial maxima out (NaN from a CTA whose copies did not land in time,
+    // so that the others do not wait for it and see a non-finite amax), then
+    // the grid barrier -- every CTA is resident (cooperative launch) -- bounded
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kThreads / 32; ++w) { mr = max_nan(mr, s_red[w]); mc = max_nan(mc, s_red2[w]); }
+        ar.partials_out[blockIdx.x] = ok ? (RHT ? mr * 0.25f : mr) : __int_as_float(0x7FFFFFFF);
+        ac.partials_out[blockIdx.x] = ok ? (RHT ? mc * 0.25f : mc) : __int_as_float(0x7FFFFFFF);
+        __threadfence();
+        atomicAdd(arrive, 1u);
+    }
+    if (!ok) {
+        // wait (bounded) for every copy of this CTA before leaving
+        if (threadIdx.x == 0) {
+            atomicOr(&g_quant_timeout, 1u);
+            for (uint32_t t = 0; t < nloc; ++t)
+                if (!ptx::mbar_wait_bounded(bars + 8u * t, 0u, kRingWait)) break;
+        }
+        return;
+    }
+    if (threadIdx.x == 0) {
+        const long long t0 = clock64();
+        bool go = true;
+        while (ld_acquire_u32(arrive) < gridDim.x) {
+            if (clock64() - t0 > kRingWait) { go = false; break; }
+            __nanosleep(64);
+        }
+        s_go = go;
+        if (!go) atomicOr(&g_quant_timeout, 1u);
+    }
+    __syncthreads();
+    if (!s_go) return;
+    // 3. tensor scales from all partial maxima, then the resident tiles
+    const float qmax = GRID == kE2M1 ? 6.0f : ar.uqmax;
+    float Sr = 1.0f, Sc = 1.0f;
+    bool fr = false, fc = false;
+    float amr = 0.0f, amc = 0.0f;
+    tensor_scale_prologue(ar, qmax, RHT ? 0.25f : 1.0f, s_kr, s_red, Sr, GRID == kE1M2 && ROUND == kRTNE, &fr, &amr);
+    tensor_scale_prologue(ac, qmax, RHT ? 0.25f : 1.0f, s_kc, s_red, Sc, GRID == kE1M2 && ROUND == kRTNE, &fc, &amc);
+    if (blockIdx.x == 0 && threadIdx.x == 0 && ar.status && !isfinite(amc)) *ar.status = 1u;
+    const Signs sgr = row_signs<__nv_bfloat16>(smask), sgc = col_signs<__nv_bfloat16>(smask);
+    const DualGeom g = dual_geom(ar, ac);
+    for (uint32_t t = 0; t < nloc; ++t) {
+        uint32_t rt, ct;
+        tile_of(t, rt, ct);
+        dual_tile_quant<GRID, ROUND, RHT, false>(ar, ac, g, buf + t * kTileBytes, rt, ct, sgr, sgc, Sr, Sc, s_kr,
+                                                 s_kc, fr, fc, nullptr, nullptr);
+    }
+    dual_padding(ar, ac, g);
 }
 
 // ====================================================== grouped (MoE) path
@@ -2571,6 +2711,37 @@ cudaError_t quantize_typed(const QuantLaunch &q, Args &a, void *ws, cudaStream_t
     return cudaErrorInvalidValue;
 }
 
+// Cooperative launch of a single-pass kernel over `grid` CTAs of kThreads
+// with kResidentSmem bytes of shared memory, after zeroing its grid-barrier
+// counter.  cudaErrorNotSupported when the CTAs cannot all be resident.
+template <class K, class... P>
+cudaError_t launch_resident(K kern, uint32_t grid, uint32_t *arrive, cudaStream_t s, P... args) {
+    static std::mutex mu;
+    static std::vector<const void *> done;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (std::find(done.begin(), done.end(), (const void *)kern) == done.end()) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kResidentSmem);
+            if (e != cudaSuccess) return e;
+            done.push_back((const void *)kern);
+        }
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kResidentSmem) != cudaSuccess ||
+        (int64_t)per_sm * num_sms() < (int64_t)grid)
+        return cudaErrorNotSupported;
+    cudaError_t e = cudaMemsetAsync(arrive, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return e;
+    void *argv[] = {static_cast<void *>(&args)...};
+    e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(grid), dim3(kThreads), argv,
+                                    kResidentSmem, s);
+    if (e == cudaErrorCooperativeLaunchTooLarge) {
+        cudaGetLastError();   // not sticky: take the two-pass route
+        return cudaErrorNotSupported;
+    }
+    return e;
+}
+
 // Both orientations of one tensor from one read per pass (k_dual_staged).
 // The row-wise and column-wise partial maxima take the two halves of the
 // workspace's partial area.
@@ -2585,6 +2756,32 @@ cudaError_t quantize_dual_typed(const QuantLaunch &qr, const QuantLaunch &qc, Ar
         const uint32_t nct = (uint32_t)((ar.cols + kTileCols - 1) / kTileCols);
         const uint32_t ntiles = (uint32_t)((ar.rows + kTileRows - 1) / kTileRows) * nct;
         ac.status = nullptr;   // the row-wise prologue reports both
+        if (!qr.amax_in && !qc.amax_in) {
+            // small enough to stay in shared memory: one cooperative single pass
+            const int sms = num_sms();
+            const uint32_t grid = (uint32_t)std::min<int64_t>(sms, ntiles);
+            if ((ntiles + grid - 1) / grid <= kResidentMax) {
+                ar.partials_out = reinterpret_cast<float *>(static_cast<char *>(ws) + kWsPartials);
+                ac.partials_out = ar.partials_out + kMaxPartials / 2;
+                ar.partials = ar.partials_out;
+                ac.partials = ac.partials_out;
+                ar.n_partials = ac.n_partials = (int)grid;
+                uint32_t *arrive = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsArrive);
+                const int kgrid = qr.grid == kE2M1 ? kE2M1 : kE1M2;
+#define UFP4_R(GRID, ROUND, RHT)                                                                         \
+                if (kgrid == GRID && qr.round == ROUND && (qr.rht != 0) == RHT) {                        \
+                    cudaError_t e = launch_resident(k_dual_resident<GRID, ROUND, RHT>, grid, arrive, s, tm, \
+                                                    ar, ac, nct, ntiles, arrive);                          \
+                    if (e != cudaErrorNotSupported) return e;                                             \
+                }
+                UFP4_R(kE2M1, kRTNE, false) UFP4_R(kE2M1, kRTNE, true)
+                UFP4_R(kE2M1, kSR, false)   UFP4_R(kE2M1, kSR, true)
+                UFP4_R(kE1M2, kRTNE, false) UFP4_R(kE1M2, kRTNE, true)
+                UFP4_R(kE1M2, kSR, false)   UFP4_R(kE1M2, kSR, true)
+#undef UFP4_R
+                // (not co-resident on this device: the two-pass route below)
+            }
+        }
         if (!qr.amax_in || !qc.amax_in) {
             // the amax pass streams with little arithmetic: 16-row x 1 KB
             // chunks (contiguous kilobyte rows) read faster than 128-byte
@@ -2614,7 +2811,7 @@ cudaError_t quantize_dual_typed(const QuantLaunch &qr, const QuantLaunch &qc, Ar
         const int kgrid = qr.grid == kE2M1 ? kE2M1 : kE1M2;   // clamped E2M1 runs the uniform-grid kernels
 #define UFP4_T(GRID, ROUND, RHT)                                                                          \
         if (kgrid == GRID && qr.round == ROUND && (qr.rht != 0) == RHT)                                   \
-            return launch_staged_smem(k_dual_tile<GRID, ROUND, RHT, false>, tile_smem<false>(), ntiles, nullptr, s, tm, ar, \
+            return launch_staged_smem(k_dual_tile<GRID, ROUND, RHT>, kTileSmem, ntiles, nullptr, s, tm, ar,       \
                                       ac, nct, ntiles);
         UFP4_T(kE2M1, kRTNE, false) UFP4_T(kE2M1, kRTNE, true)
         UFP4_T(kE2M1, kSR, false)   UFP4_T(kE2M1, kSR, true)

@@ -120,3 +120,23 @@ def test_dual_nonfinite_flag(U):
     y = torch.from_numpy(inputs.normal(4, (64, 256))).to(torch.bfloat16).cuda()
     U.ufp4_quantize_dual(y, 1, rht=True, ws=ws)
     assert U.ufp4_check(ws) == 0
+
+
+@pytest.mark.parametrize("grid,rht,rnd", [(1, True, 0), (1, True, 1), (0, False, 0), (0, True, 1)])
+@pytest.mark.parametrize("rows,cols", [(3584, 4864), (3584, 4928), (64, 128)])
+def test_single_pass_capacity_boundary(U, grid, rht, rnd, rows, cols):
+    """BF16 dual quantization with both tensor maxima computed: tensors of up
+    to 14 x 128 x 64 tiles per SM (3584 x 4864 is 2128 tiles, the limit on
+    152 SMs) take the single on-chip pass; one tile column more (3584 x 4928)
+    the two-pass route.  Both equal the single-orientation calls bit for
+    bit, and a repeated call (the grid-barrier counter is re-armed) too."""
+    x = torch.from_numpy(inputs.normal(9, (rows, cols))).to(torch.bfloat16).cuda()
+    kw = dict(rht=rht, rht_seed=7, round=rnd, sr_seed=11, sr_counter_row=3, sr_counter_col=4)
+    qr, qc = U.ufp4_quantize_dual(x, grid, **kw)
+    r1, c1 = _host(qr), _host(qc)
+    _assert_same(r1, _single(U, x, grid, rht, rnd, 3, False))
+    _assert_same(c1, _single(U, x, grid, rht, rnd, 4, True))
+    qr2, qc2 = U.ufp4_quantize_dual(x, grid, **kw)
+    _assert_same(_host(qr2), r1)
+    _assert_same(_host(qc2), c1)
+    assert U.ufp4_check(U.workspace(x.device)) == U.UFP4_OK
