@@ -52,6 +52,7 @@ WORKLOAD = dict(name="moe124b_layer_train_step", tokens=65536, hidden=8192, ffn=
 DENSE = dict(tokens=8192, hidden=2048, ffn=5632)
 METRIC = ("fused RHT+quantize GB/s (% HBM peak); FP4 GEMM TFLOPS (% tensor peak)")
 Q_BYTES_PER_ELEM = 2.0 + 0.5 + 1.0 / 16.0
+MX_BYTES_PER_ELEM = 2.0 + 0.5 + 1.0 / 32.0     # one E8M0 byte per 32 elements
 FALLBACK = dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0)
 
 
@@ -623,7 +624,7 @@ def run_kernel(args):
     x = inputs.device_normal((T, H), 1.0, 21, dev)
     kind = args.kernel
     if kind.startswith("gemm"):
-        grid = U.UFP4_E2M1 if kind == "gemm_e2m1" else U.UFP4_E1M2
+        grid = {"gemm_e2m1": U.UFP4_E2M1, "gemm_mxfp4": U.UFP4_MXFP4}.get(kind, U.UFP4_E1M2)
         w = inputs.device_normal((F, H), 0.02, 22, dev)
         a, b = U.ufp4_quantize(x, grid, rht=True), U.ufp4_quantize(w, grid, rht=True)
         c = torch.empty(T, F, dtype=torch.float32, device=dev)
@@ -697,10 +698,10 @@ def _fracs(pk, q_gbs=None, tflops=None, grid=None, gemm_bytes=None, gemm_flops=N
     return out
 
 
-def _gemm_bytes(M, N, K):
+def _gemm_bytes(M, N, K, mx=False):
     """Algorithmic bytes of one GEMM: both quantized operands (0.5 B codes +
-    1/16 B scale per element) and the fp32 output."""
-    return (M + N) * K * 0.5625 + 4.0 * M * N
+    1/16 B scale per element; MXFP4 1/32 B) and the fp32 output."""
+    return (M + N) * K * (0.53125 if mx else 0.5625) + 4.0 * M * N
 
 
 def all_workloads(U, torch, dev, pk, flush, with_oracle=True):
@@ -737,15 +738,13 @@ def all_workloads(U, torch, dev, pk, flush, with_oracle=True):
     ms = _ev_time(lambda: U.ufp4_quantize(x, U.UFP4_E1M2, rht=True, rht_seed=2, out=q), flush)
     r["quantize_e1m2_rht_gbs"] = round(x.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 2)
     r.update(_fracs(pk, q_gbs=r["quantize_e1m2_rht_gbs"]))
-    for g, gn in ((0, "e2m1"), (1, "e1m2"), (2, "e2m1c")):
+    for g, gn in ((0, "e2m1"), (1, "e1m2"), (2, "e2m1c"), (3, "mxfp4")):
         for rht in (False, True):
             r["numerics"]["%s_rht_%s" % (gn, "on" if rht else "off")] = stats_of(x, g, rht)
         qa, qb = U.ufp4_quantize(a, g), U.ufp4_quantize(b, g)
         c = torch.empty(256, 256, device=dev)
         ms = _ev_time(lambda: U.ufp4_gemm(qa, qb, out=c), flush)
         r["gemm_%s_tflops" % gn] = round(2 * 256 ** 3 / (ms * 1e-3) / 1e12, 3)
-    for rht in (False, True):   # MXFP4: quantization numerics only (no GEMM)
-        r["numerics"]["mxfp4_rht_%s" % ("on" if rht else "off")] = stats_of(x, U.UFP4_MXFP4, rht)
     r["note"] = "0.67 MB of input: launch latency, not HBM, bounds it"
     if o is not None:
         r["oracle"] = oracle_q(d["x"], d["x"].size, "the whole 256 x 1024 tensor, RHT + E1M2",
@@ -762,8 +761,7 @@ def all_workloads(U, torch, dev, pk, flush, with_oracle=True):
     r = {"config": "BF16 4096 x 4096 N(0,1) + column offsets N(0,0.5), 4 columns x100", "numerics": {},
          "quantize_gbs": {}}
     for g, gn in ((0, "e2m1"), (1, "e1m2"), (2, "e2m1c"), (3, "mxfp4")):
-        # MXFP4 moves 2 + 0.5 + 1/32 B/elem (one E8M0 byte per 32 elements)
-        bpe = 2.53125 if g == U.UFP4_MXFP4 else Q_BYTES_PER_ELEM
+        bpe = MX_BYTES_PER_ELEM if g == U.UFP4_MXFP4 else Q_BYTES_PER_ELEM
         for rht in (False, True):
             key = "%s_rht_%s" % (gn, "on" if rht else "off")
             r["numerics"][key] = stats_of(x, g, rht)
@@ -785,15 +783,18 @@ def all_workloads(U, torch, dev, pk, flush, with_oracle=True):
     T, H, F = DENSE["tokens"], DENSE["hidden"], DENSE["ffn"]
     dd = inputs.device_dense(seed=0, device=dev)
     r = {"config": "X 8192 x 2048 (1 column x50), W 5632 x 2048, dY 8192 x 5632; 3 GEMMs of 189 GFLOP"}
-    for g, gn, pol in ((1, "e1m2", "ufp4"), (0, "e2m1", "ufp4"), (0, "nvfp4_policy", "nvfp4")):
-        st = Step(U, dd["x"], dd["w"], dd["dy"], g, policy=pol)
+    for g, gn, pol in ((1, "e1m2", "ufp4"), (0, "e2m1", "ufp4"), (0, "nvfp4_policy", "nvfp4"),
+                       (3, "mxfp4", "ufp4")):
+        # MXFP4 has no two-orientation pass: six single-orientation passes
+        st = Step(U, dd["x"], dd["w"], dd["dy"], g, policy=pol, dual=g != U.UFP4_MXFP4)
         mq = _ev_time(st.quantize_all, flush)
         mg = _ev_time(st.gemms, flush)
-        qg = st.q_elems * Q_BYTES_PER_ELEM / (mq * 1e-3) / 1e9
+        bpe = MX_BYTES_PER_ELEM if g == U.UFP4_MXFP4 else Q_BYTES_PER_ELEM
+        qg = st.q_elems * bpe / (mq * 1e-3) / 1e9
         tf = sum(st.flops_each) / (mg * 1e-3) / 1e12
         e = {"quantize_ms": round(mq, 4), "quantize_gbs": round(qg, 1), "gemm_ms": round(mg, 4),
              "gemm_tflops": round(tf, 1)}
-        e.update(_fracs(pk, qg, tf, g, 3 * _gemm_bytes(T, F, H), sum(st.flops_each)))
+        e.update(_fracs(pk, qg, tf, g, 3 * _gemm_bytes(T, F, H, mx=g == U.UFP4_MXFP4), sum(st.flops_each)))
         r[gn] = e
         del st
     del dd
@@ -954,7 +955,7 @@ def main():
     ap.add_argument("--shape", default="dense", choices=["dense", "moe124b"],
                     help="layer shape of --kernel")
     ap.add_argument("--kernel", default=None,
-                    choices=["gemm_e2m1", "gemm_e1m2", "quant_row_e1m2", "quant_col_e1m2", "quant_dual_e1m2",
+                    choices=["gemm_e2m1", "gemm_e1m2", "gemm_mxfp4", "quant_row_e1m2", "quant_col_e1m2", "quant_dual_e1m2",
                              "quant_dual_sr_e1m2", "amax_dual_e1m2",
                              "quant_row_e2m1", "quant_col_e2m1"],
                     help="time one kernel of the step in isolation (profiling)")

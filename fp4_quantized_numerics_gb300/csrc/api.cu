@@ -176,7 +176,7 @@ ufp4_status ufp4_gemm(const ufp4_qtensor *a, const ufp4_qtensor *b, float *c, in
                       ufp4_stream_t stream) {
     if (!valid_qtensor(a) || !valid_qtensor(b)) return UFP4_ERR_INVALID;
     if (a->k != b->k) return UFP4_ERR_INVALID;
-    if (a->grid != b->grid || a->grid == UFP4_MXFP4) return UFP4_ERR_UNSUPPORTED;
+    if (a->grid != b->grid) return UFP4_ERR_UNSUPPORTED;
     const int64_t M = a->rows, N = b->rows, K = a->k;
     if (M == 0 || N == 0) return UFP4_OK;
     if (!c || !aligned(c, 16) || ldc < N || ldc % 4 != 0) return UFP4_ERR_INVALID;

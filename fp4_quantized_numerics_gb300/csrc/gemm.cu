@@ -59,6 +59,9 @@ constexpr long long kWaitBudget = 2000000000LL;
 // whose codes are E2M1 codes), kE1M2 (E planes expanded on chip) and kE1M2Pl
 // (E1M2 whose E planes the quantizer wrote next to the codes).
 constexpr int kE1M2Pl = 3;
+// MXFP4 operands: E2M1 codes like kE2M1, one UE8M0 scale per 32 elements
+// (stored at both of its 16-block places); the MMA takes scale_vec::2X.
+constexpr int kMX = 4;
 
 // Per-variant pipeline geometry.
 //  E2M1: K stage of 128 bytes (4 MMA K steps, 128-byte swizzle) so that the
@@ -75,14 +78,15 @@ constexpr int kE1M2Pl = 3;
 //        from their own warp as for E2M1.
 template <int GRID>
 struct Cfg {
-    static constexpr bool kFour = GRID != kE2M1;                     // E1M2: 4 MMAs per K step
+    static constexpr bool kFour = GRID == kE1M2 || GRID == kE1M2Pl;  // E1M2: 4 MMAs per K step
+    static constexpr bool kE2M1Like = GRID == kE2M1 || GRID == kMX;  // one MMA per K step
     static constexpr bool kPl = GRID == kE1M2Pl;                     // E planes loaded by TMA
     // columns of a staged TMA-store box: E1M2Pl stages 16-column pieces
     // through a 2 KB buffer per epilogue warp, E2M1 8-column pieces through
     // 1 KB, which leaves room for a 4th operand stage
-    static constexpr int kEpiCols = kPl ? 16 : (GRID == kE2M1 ? 8 : 32);
+    static constexpr int kEpiCols = kPl ? 16 : (kE2M1Like ? 8 : 32);
     static constexpr uint32_t kEpiBufBytes = 32u * kEpiCols * 4u;
-    static constexpr int kBK = GRID == kE2M1 ? 128 : 64;            // bytes of K per stage
+    static constexpr int kBK = kE2M1Like ? 128 : 64;                 // bytes of K per stage
     static constexpr int kKS = kBK / 32;                             // MMA K steps per stage
     static constexpr uint32_t kSwz = kBK == 128 ? 2 : 4;             // descriptor swizzle: 128B / 64B
     static constexpr uint32_t kSbo = 8 * kBK;                        // 8-row core-matrix group stride
@@ -438,6 +442,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
             // instruction descriptor, kind::mxf4nvf4: A/B E2M1 (1), K-major,
             // N >> 3 at [17,23), UE4M3 scales (bit 23 = 0), M >> 4 at [24,29).
             const uint32_t idesc = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                                   (GRID == kMX ? (1u << 23) : 0u) |   // UE8M0 scales for MXFP4
                                    ((uint32_t)(BM >> 4) << 24);
             const uint64_t hi_op = ptx::sdesc(0, 16, C::kSbo, C::kSwz);   // swizzled K-major operand
             auto mk = [](uint64_t hi, uint32_t addr) { return hi | (uint64_t)((addr & 0x3FFFFu) >> 4); };
@@ -494,6 +499,9 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                             mma(Last{}, da, deb, j, 1u);
                             mma(Fill{}, dea, db, j, 1u);
                             mma(Last{}, dea, deb, j, 1u);
+                        } else if constexpr (GRID == kMX) {
+                            ptx::tc_mma_mxf4(tmem, da + 2u * (uint32_t)j, db + 2u * (uint32_t)j, idesc, sfa0 + 4u * j,
+                                             sfb0 + 8u * j, first(j));
                         } else {
                             mma(None{}, da, db, j, first(j));
                         }
@@ -705,6 +713,36 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         }
         if (lane == 0) ptx::bulk_wait_all();
         __syncwarp();
+    } else if (GRID == kMX && warp == 2 + kEpiWarps) {
+        // ---------------------------------------- MXFP4 scale repack + copies
+        // A staged scale word holds one row's four 16-block places of a K step,
+        // (s0, s0, s1, s1) for its two 32-blocks; scale_vec::2X reads the K
+        // step's two scales from bytes 0 and 1, so the whole warp rewrites
+        // each word to (s0, s1, s1, s1) before lane 0 copies it to TMEM.
+        uint32_t g = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            const TileInfo ti = tile_info<C::kKS>(p, tab, t);
+            for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++g) {
+                const uint32_t s = g % S, round = g / S;
+                ok = __all_sync(0xffffffffu, wait_or_abort(full(s), round & 1, abort, p.budget));
+                if (!ok) break;
+                const uint32_t st = smem_base + s * C::kStageBytes;
+                constexpr uint32_t kWords = (C::kSfaBytes + C::kSfbBytes) / 4;   // SFA | SFB, contiguous
+                for (uint32_t w = lane; w < kWords; w += 32) {
+                    const uint32_t addr = st + C::kSfaOff + 4u * w;
+                    uint32_t v;
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+                    asm("prmt.b32 %0, %0, 0, 0x3320;" : "+r"(v));
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+                }
+                ptx::fence_proxy_async();   // the rewritten bytes, to the tensor cores' copies
+                __syncwarp();
+                if (lane == 0) copy_scales(s, min(C::kKS, ti.nkt - C::kKS * kb), true);
+                __syncwarp();
+            }
+        }
+        if (lane == 0) drain_scales(g);
     } else if (C::kScaleWarps > 0 && warp == 2 + kEpiWarps) {
         // ------------------------------------------------- E2M1 scale copies
         if (lane == 0) {
@@ -851,6 +889,7 @@ cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_eplane, const u
     const bool planes = grid == kE1M2 && a_eplane && b_eplane;
     // K bytes per stage of the kernel that runs: the tensor maps' box width
     const int bk = planes ? Cfg<kE1M2Pl>::kBK : (grid == kE1M2 ? Cfg<kE1M2>::kBK : Cfg<kE2M1>::kBK);
+    static_assert(Cfg<kMX>::kBK == Cfg<kE2M1>::kBK && Cfg<kMX>::kEpiCols == Cfg<kE2M1>::kEpiCols, "MX = E2M1 geometry");
     CUtensorMap ma, mb, mea, meb, mc;
     if (!make_code_map(&ma, a_codes, M, kpad, BM, bk) || !make_code_map(&mb, b_codes, N, kpad, BN, bk) ||
         !make_out_map(&mc, c, M, N, ldc,
@@ -897,7 +936,8 @@ cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_eplane, const u
     }
     const NoGroups none;
     const int units = p.ntm * p.ntn * p.splits;
-    // clamped-E2M1 codes are E2M1 codes
+    // clamped-E2M1 codes are E2M1 codes; MXFP4 codes too, with UE8M0 scales
+    if (grid == kMXFP4) return run_gemm<kMX>(ma, mb, mea, meb, mc, p, none, units, s);
     if (grid != kE1M2) return run_gemm<kE2M1>(ma, mb, mea, meb, mc, p, none, units, s);
     if (planes) return run_gemm<kE1M2Pl>(ma, mb, mea, meb, mc, p, none, units, s);
     return run_gemm<kE1M2>(ma, mb, mea, meb, mc, p, none, units, s);

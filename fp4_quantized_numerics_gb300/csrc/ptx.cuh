@@ -173,6 +173,19 @@ __device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t adesc, uin
 #undef UFP4_MMA_NVF4
 }
 
+// The same product with one UE8M0 scale per 32 K-elements per row
+// (scale_vec::2X, MXFP4): the two scales of a K step are bytes 0 and 1 of the
+// row's scale word (scale-factor ID 0 in the instruction descriptor).
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X"
+                 " [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+                 : "memory");
+}
+
 // Arrive on an mbarrier once every previously issued tcgen05 op of this
 // thread has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {

@@ -77,8 +77,10 @@ typedef enum {
  *               1).  The scale byte s + 127 is stored at both of the block's
  *               16-block places of the scale layout below.  Supported by
  *               ufp4_quantize (block = UFP4_MX_BLOCK, k a multiple of 32,
- *               amax_in NULL), ufp4_dequantize and ufp4_stats; the dual,
- *               grouped and GEMM calls return UFP4_ERR_UNSUPPORTED for it.
+ *               amax_in NULL), ufp4_dequantize, ufp4_stats and ufp4_gemm (two
+ *               MXFP4 operands: the tensor cores' MXFP4 product, E2M1
+ *               elements with one UE8M0 scale per 32 K-elements); the dual,
+ *               grouped and GEMM-amax calls return UFP4_ERR_UNSUPPORTED.
  * A symmetric uniform INT4 grid {-7..7} needs no entry: with the same
  * two-level scaling its codes and block scales equal E1M2's bit for bit and
  * only the tensor scale (x 1/2) and the value of a code (x 2) differ. */

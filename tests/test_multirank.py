@@ -75,5 +75,5 @@ def test_gemm_traffic_record_matches_source():
     """The roofline's DRAM traffic comes from a committed ncu record keyed by
     the GEMM source's hash; it must still match the source in the tree."""
     import bench
-    t = bench.traffic_for("k_gemm_e1m2_dense1p5b")
+    t = bench.traffic_for("k_gemm_e1m2_moe124b")
     assert isinstance(t, int) and t > 0

@@ -101,8 +101,8 @@ def test_mx_dequantize_and_stats(U, oracle):
 def test_mx_refused_where_unsupported(U):
     x = torch.from_numpy(inputs.normal(41, (128, 256))).to(torch.bfloat16).cuda()
     q = U.ufp4_quantize(x, U.UFP4_MXFP4)
-    with pytest.raises(U.UFP4Error) as e:
-        U.ufp4_gemm(q, q)
+    with pytest.raises(U.UFP4Error) as e:                       # MX and NVFP4-style operands do not mix
+        U.ufp4_gemm(q, U.ufp4_quantize(x, U.UFP4_E2M1))
     assert e.value.status == U.UFP4_ERR_UNSUPPORTED
     with pytest.raises(U.UFP4Error) as e:
         U.ufp4_quantize_dual(x, U.UFP4_MXFP4)
@@ -128,3 +128,66 @@ def test_mx_nonfinite_flag(U):
     x[3, 70] = 1.0
     U.ufp4_quantize(x, U.UFP4_MXFP4, ws=ws, colwise=True)
     assert U.ufp4_check(ws) == U.UFP4_OK
+
+
+def _mx_consumed(U, oracle, q):
+    """fp64 values of a GPU MXFP4 operand (its codes and its per-32 scale
+    bytes, one of the two 16-block places each), dequantized by the oracle."""
+    torch.cuda.synchronize()
+    codes = layouts.unpack_codes(q.codes.cpu().numpy(), q.rows, q.k)
+    s16, _ = layouts.unpack_scales(q.scales.cpu().numpy(), q.rows, q.k)
+    return oracle.dequantize_mx(codes, np.ascontiguousarray(s16[:, 0::2]))
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (300, 200, 320), (130, 140, 4160), (64, 48, 32)])
+def test_mx_gemm_matches_oracle(U, oracle, M, N, K):
+    """C = A B^T of two MXFP4 operands on the tensor cores (E2M1 elements,
+    UE8M0 scale per 32, scale_vec::2X) within 1e-5 relative Frobenius of the
+    oracle's fp64 product of its own MX-dequantized operands (the codes and
+    scales are bit-exact without the transform)."""
+    a = inputs.normal(61, (M, K))
+    b = inputs.normal(62, (N, K), std=0.02)
+    qa = U.ufp4_quantize(torch.from_numpy(a).to(torch.bfloat16).cuda(), U.UFP4_MXFP4)
+    qb = U.ufp4_quantize(torch.from_numpy(b).to(torch.bfloat16).cuda(), U.UFP4_MXFP4)
+    c = U.ufp4_gemm(qa, qb).cpu().numpy().astype(np.float64)
+    ra, rb = oracle.quantize_mx(a), oracle.quantize_mx(b)
+    ref = oracle.gemm_f64(oracle.dequantize_mx(ra["codes"], ra["scales"]),
+                          oracle.dequantize_mx(rb["codes"], rb["scales"]))
+    assert np.linalg.norm(c - ref) <= 1e-5 * np.linalg.norm(ref)
+
+
+def test_mx_training_gemms_and_rht(U, oracle):
+    """fwd_y, bwd_dx (B column-wise) and bwd_dw (both column-wise, SR on dY)
+    with MXFP4 operands, transform off against the oracle's operands and on
+    against the operands the kernel consumed; and a spread of block
+    exponents across 2^40 (rows scaled 2^-20 .. 2^20) that a per-tensor
+    scale could not hold."""
+    T, H, F = 192, 256, 320
+    x = inputs.normal(63, (T, H))
+    w = inputs.normal(64, (F, H), std=0.02)
+    dy = inputs.normal(65, (T, F), std=1e-3)
+    cases = ((x, w, False, False, 0), (dy, w, False, True, 1), (dy, x, True, True, 1))
+    for rht in (False, True):
+        for a, b, ca, cb, rnd in cases:
+            qa = U.ufp4_quantize(torch.from_numpy(a).to(torch.bfloat16).cuda(), U.UFP4_MXFP4, rht=rht, rht_seed=2,
+                                 colwise=ca, round=rnd, sr_seed=3)
+            qb = U.ufp4_quantize(torch.from_numpy(b).to(torch.bfloat16).cuda(), U.UFP4_MXFP4, rht=rht, rht_seed=2,
+                                 colwise=cb)
+            c = U.ufp4_gemm(qa, qb).cpu().numpy().astype(np.float64)
+            if not rht:
+                ra = oracle.quantize_mx(a, colwise=ca, round_mode=rnd, sr_seed=3)
+                rb = oracle.quantize_mx(b, colwise=cb)
+                A = oracle.dequantize_mx(ra["codes"], ra["scales"])
+                B = oracle.dequantize_mx(rb["codes"], rb["scales"])
+            else:
+                A, B = _mx_consumed(U, oracle, qa), _mx_consumed(U, oracle, qb)
+            ref = oracle.gemm_f64(A, B)
+            assert np.linalg.norm(c - ref) <= 1e-5 * np.linalg.norm(ref)
+    wide = inputs.normal(66, (128, 256)) * np.float32(2.0) ** np.linspace(-20, 20, 128, dtype=np.float32)[:, None]
+    wide = inputs.to_bf16_f32(wide)
+    qa = U.ufp4_quantize(torch.from_numpy(wide).to(torch.bfloat16).cuda(), U.UFP4_MXFP4)
+    qb = U.ufp4_quantize(torch.from_numpy(w[:, :256]).to(torch.bfloat16).cuda(), U.UFP4_MXFP4)
+    c = U.ufp4_gemm(qa, qb).cpu().numpy().astype(np.float64)
+    ref = oracle.gemm_f64(_mx_consumed(U, oracle, qa), _mx_consumed(U, oracle, qb))
+    for r in (0, 64, 127):   # every row to 1e-5 of its own norm, small rows included
+        assert np.linalg.norm(c[r] - ref[r]) <= 1e-5 * np.linalg.norm(ref[r])
