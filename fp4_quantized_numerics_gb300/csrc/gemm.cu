@@ -153,6 +153,9 @@ struct TileInfo {
 };
 
 struct NoGroups {};
+// A plain GEMM whose epilogue also raises the tensor amax of C's row-wise
+// quantization (its own kernel, so the plain GEMM carries none of that code).
+struct NoGroupsAmax : NoGroups {};
 
 // Work unit u of a dense GEMM: K part u / tiles (outermost, so that one
 // round of the persistent grid covers twice the tiles of a K half), then the
@@ -304,6 +307,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
            const __grid_constant__ CUtensorMap tma_ea, const __grid_constant__ CUtensorMap tma_eb,
            const __grid_constant__ CUtensorMap tma_c, GemmParams p, const __grid_constant__ TAB tab) {
     constexpr bool kGrouped = std::is_same<TAB, GroupGemmTab>::value;
+    constexpr bool kAmax = std::is_same<TAB, NoGroupsAmax>::value;
     using C = Cfg<GRID>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -534,7 +538,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         const uint32_t buf0 = smem_base + C::kEpiOff + (uint32_t)ew * NB * C::kEpiBufBytes;
         // E1M2 accumulates (R + E)(R + E) = 4 A B^T
         const float kfix = C::kFour ? 0.25f : 1.0f;
-        const uint32_t smask = (!kGrouped && p.c_amax && p.amax_rht) ? rht_sign_mask(p.amax_seed) : 0u;
+        const uint32_t smask = (kAmax && p.amax_rht) ? rht_sign_mask(p.amax_seed) : 0u;
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(128 * h);
         uint32_t it = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
@@ -557,7 +561,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(acce);
-                if (!kGrouped && p.c_amax) {
+                if constexpr (kAmax) {
                     // rows and columns outside C hold zeros (zero-filled operands)
                     float am = 0.0f;
 #pragma unroll
@@ -627,7 +631,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                 continue;
             } else {
             auto stage = [&](uint32_t b, const uint32_t (&v)[32]) {
-                if (!kGrouped && p.c_amax) {
+                if constexpr (kAmax) {
                     float am = out_block_amax(&v[0], kfix, alpha, p.amax_rht != 0, smask, 0.0f);
                     am = out_block_amax(&v[16], kfix, alpha, p.amax_rht != 0, smask, am);
                     flush_amax(p.c_amax, am, p.amax_rht != 0, lane);
@@ -727,14 +731,24 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                 const uint32_t s = g % S, round = g / S;
                 ok = __all_sync(0xffffffffu, wait_or_abort(full(s), round & 1, abort, p.budget));
                 if (!ok) break;
-                const uint32_t st = smem_base + s * C::kStageBytes;
-                constexpr uint32_t kWords = (C::kSfaBytes + C::kSfbBytes) / 4;   // SFA | SFB, contiguous
-                for (uint32_t w = lane; w < kWords; w += 32) {
-                    const uint32_t addr = st + C::kSfaOff + 4u * w;
-                    uint32_t v;
-                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-                    asm("prmt.b32 %0, %0, 0, 0x3320;" : "+r"(v));
-                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+                // SFA | SFB are contiguous: 16 bytes per lane and step, all of a
+                // lane's loads in flight before its first store
+                const uint32_t st = smem_base + s * C::kStageBytes + C::kSfaOff + 16u * (uint32_t)lane;
+                constexpr int kPer = (int)((C::kSfaBytes + C::kSfbBytes) / (16 * 32));
+                static_assert((C::kSfaBytes + C::kSfbBytes) % (16 * 32) == 0, "whole 16-byte steps per lane");
+                uint32_t v[kPer][4];
+#pragma unroll
+                for (int i = 0; i < kPer; ++i)
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(v[i][0]), "=r"(v[i][1]), "=r"(v[i][2]), "=r"(v[i][3])
+                                 : "r"(st + 512u * (uint32_t)i));
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) asm("prmt.b32 %0, %0, 0, 0x3320;" : "+r"(v[i][j]));
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(st + 512u * (uint32_t)i),
+                                 "r"(v[i][0]), "r"(v[i][1]), "r"(v[i][2]), "r"(v[i][3])
+                                 : "memory");
                 }
                 ptx::fence_proxy_async();   // the rewritten bytes, to the tensor cores' copies
                 __syncwarp();
@@ -936,6 +950,13 @@ cudaError_t launch_gemm(const uint8_t *a_codes, const uint8_t *a_eplane, const u
     }
     const NoGroups none;
     const int units = p.ntm * p.ntn * p.splits;
+    if (c_amax) {
+        const NoGroupsAmax with_amax;
+        if (grid == kMXFP4) return cudaErrorInvalidValue;
+        if (grid != kE1M2) return run_gemm<kE2M1>(ma, mb, mea, meb, mc, p, with_amax, units, s);
+        if (planes) return run_gemm<kE1M2Pl>(ma, mb, mea, meb, mc, p, with_amax, units, s);
+        return run_gemm<kE1M2>(ma, mb, mea, meb, mc, p, with_amax, units, s);
+    }
     // clamped-E2M1 codes are E2M1 codes; MXFP4 codes too, with UE8M0 scales
     if (grid == kMXFP4) return run_gemm<kMX>(ma, mb, mea, meb, mc, p, none, units, s);
     if (grid != kE1M2) return run_gemm<kE2M1>(ma, mb, mea, meb, mc, p, none, units, s);
