@@ -831,13 +831,21 @@ def all_workloads(U, torch, dev, pk, flush, with_oracle=True):
         qs = {}
 
         def quant_all():
-            qs["xr"] = U.ufp4_quantize_grouped(tx, g, counts, out=qs.get("xr"), **kw)
-            qs["xc"] = U.ufp4_quantize_grouped(tx, g, counts, colwise=True, out=qs.get("xc"), **kw)
-            qs["dr"] = U.ufp4_quantize_grouped(tdy, g, counts, round=1, sr_seed=3, out=qs.get("dr"), **kw)
-            qs["dc"] = U.ufp4_quantize_grouped(tdy, g, counts, round=1, sr_seed=3, colwise=True,
-                                               out=qs.get("dc"), **kw)
-            qs["wr"] = U.ufp4_quantize_grouped(tw, g, [F] * E, out=qs.get("wr"), **kw)
-            qs["wc"] = U.ufp4_quantize_grouped(tw, g, [F] * E, colwise=True, out=qs.get("wc"), **kw)
+            # every operand in both orientations from one read per pass
+            qs["xr"], qs["xc"] = U.ufp4_quantize_grouped_dual(tx, g, counts, out_row=qs.get("xr"),
+                                                              out_col=qs.get("xc"), **kw)
+            qs["dr"], qs["dc"] = U.ufp4_quantize_grouped_dual(tdy, g, counts, round=1, sr_seed=3,
+                                                              out_row=qs.get("dr"), out_col=qs.get("dc"), **kw)
+            qs["wr"], qs["wc"] = U.ufp4_quantize_grouped_dual(tw, g, [F] * E, out_row=qs.get("wr"),
+                                                              out_col=qs.get("wc"), **kw)
+
+        def quant_all_single():
+            U.ufp4_quantize_grouped(tx, g, counts, out=qs["xr"], **kw)
+            U.ufp4_quantize_grouped(tx, g, counts, colwise=True, out=qs["xc"], **kw)
+            U.ufp4_quantize_grouped(tdy, g, counts, round=1, sr_seed=3, out=qs["dr"], **kw)
+            U.ufp4_quantize_grouped(tdy, g, counts, round=1, sr_seed=3, colwise=True, out=qs["dc"], **kw)
+            U.ufp4_quantize_grouped(tw, g, [F] * E, out=qs["wr"], **kw)
+            U.ufp4_quantize_grouped(tw, g, [F] * E, colwise=True, out=qs["wc"], **kw)
         quant_all()
         y = torch.empty(T, F, device=dev)
         dx = torch.empty(T, H, device=dev)
@@ -856,13 +864,15 @@ def all_workloads(U, torch, dev, pk, flush, with_oracle=True):
             U.ufp4_gemm_grouped(qs["dr"], qs["wc"], gx)
             U.ufp4_gemm_grouped(qs["dc"], qs["xc"], gw)
         mq = _ev_time(quant_all, flush, 5)
+        mq1 = _ev_time(quant_all_single, flush, 5)
         mg = _ev_time(gemm_all, flush, 5)
         elems = 2 * (tx.numel() + tw.numel() + tdy.numel())
         flops = 3 * 2.0 * T * F * H
         qg = elems * Q_BYTES_PER_ELEM / (mq * 1e-3) / 1e9
         tf = flops / (mg * 1e-3) / 1e12
         e = {"quantize_ms": round(mq, 4), "quantize_gbs": round(qg, 1), "gemm_ms": round(mg, 4),
-             "gemm_tflops": round(tf, 1)}
+             "gemm_tflops": round(tf, 1),
+             "quantize_ms_six_single_orientation_calls": round(mq1, 4)}
         e.update(_fracs(pk, qg, tf, g, 3 * sum(_gemm_bytes(c, F, H) for c in counts), flops))
         r[gn] = e
         del qs, y, dx, dw

@@ -217,10 +217,13 @@ int64_t ufp4_grouped_kpad(const int64_t *seg_rows, int32_t n_seg) {
     return t;
 }
 
-ufp4_status ufp4_quantize_grouped(const void *x, int32_t dtype, int64_t cols, int64_t ld,
-                                  const int64_t *seg_rows, int32_t n_seg, const ufp4_qparams *p,
-                                  const ufp4_qtensor *out, void *workspace, size_t workspace_bytes,
-                                  ufp4_stream_t stream) {
+// Validation and segment table of one grouped quantization.  `*empty` is set
+// when there is nothing to write (UFP4_OK without a launch).
+static ufp4_status grouped_prepare(const void *x, int32_t dtype, int64_t cols, int64_t ld,
+                                   const int64_t *seg_rows, int32_t n_seg, const ufp4_qparams *p,
+                                   const ufp4_qtensor *out, void *workspace, size_t workspace_bytes,
+                                   GroupQuant &gt, QuantLaunch &q, bool *empty) {
+    *empty = false;
     if (!p || !out || !seg_rows || n_seg < 1 || n_seg > kMaxGroups) return UFP4_ERR_INVALID;
     if (p->grid == UFP4_MXFP4) return UFP4_ERR_UNSUPPORTED;
     if (p->amax_in) return UFP4_ERR_INVALID;
@@ -250,10 +253,12 @@ ufp4_status ufp4_quantize_grouped(const void *x, int32_t dtype, int64_t cols, in
     if (total > 0 && cols > 0 && (!x || !aligned(x, 16) || (ld * (int64_t)esz) % 16 != 0)) return UFP4_ERR_INVALID;
     if (!valid_workspace(workspace, workspace_bytes)) return UFP4_ERR_INVALID;
     if (kWsPartials + (size_t)n_seg * 4 > kWsStats) return UFP4_ERR_INVALID;
-    if (total == 0 || cols == 0 || out_rows == 0 || k == 0) return UFP4_OK;
+    if (total == 0 || cols == 0 || out_rows == 0 || k == 0) {
+        *empty = true;
+        return UFP4_OK;
+    }
     if (total > (int64_t)INT32_MAX) return UFP4_ERR_UNSUPPORTED;
 
-    GroupQuant gt;
     memset(&gt, 0, sizeof gt);
     gt.n = n_seg;
     gt.colwise = p->colwise;
@@ -270,14 +275,66 @@ ufp4_status ufp4_quantize_grouped(const void *x, int32_t dtype, int64_t cols, in
         }
     }
     if (gt.units[n_seg] > (int64_t)INT32_MAX * 2) return UFP4_ERR_UNSUPPORTED;
-    QuantLaunch q{};
+    q = QuantLaunch{};
     q.x = x; q.dtype = dtype; q.rows = total; q.cols = cols; q.ld = ld;
     q.grid = p->grid; q.rht = p->rht; q.round = p->round; q.colwise = p->colwise;
     q.rht_seed = p->rht_seed; q.sr_seed = p->sr_seed; q.sr_counter = p->sr_counter;
     q.codes = out->codes; q.scales = out->scales; q.tensor_scale = out->tensor_scale;
     q.eplane = out->eplane;
     q.out_rows = out_rows; q.k = k;
+    return UFP4_OK;
+}
+
+ufp4_status ufp4_quantize_grouped(const void *x, int32_t dtype, int64_t cols, int64_t ld,
+                                  const int64_t *seg_rows, int32_t n_seg, const ufp4_qparams *p,
+                                  const ufp4_qtensor *out, void *workspace, size_t workspace_bytes,
+                                  ufp4_stream_t stream) {
+    GroupQuant gt;
+    QuantLaunch q;
+    bool empty = false;
+    ufp4_status st = grouped_prepare(x, dtype, cols, ld, seg_rows, n_seg, p, out, workspace, workspace_bytes, gt,
+                                     q, &empty);
+    if (st != UFP4_OK || empty) return st;
     return from_cuda(launch_quantize_grouped(q, gt, workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ufp4_status ufp4_quantize_grouped_dual(const void *x, int32_t dtype, int64_t cols, int64_t ld,
+                                       const int64_t *seg_rows, int32_t n_seg, const ufp4_qparams *p_row,
+                                       const ufp4_qparams *p_col, const ufp4_qtensor *out_row,
+                                       const ufp4_qtensor *out_col, void *workspace, size_t workspace_bytes,
+                                       ufp4_stream_t stream) {
+    if (!p_row || !p_col || p_row->colwise != 0 || p_col->colwise != 1) return UFP4_ERR_INVALID;
+    GroupQuant gr, gc;
+    QuantLaunch qr, qc;
+    bool empty_r = false, empty_c = false;
+    ufp4_status st = grouped_prepare(x, dtype, cols, ld, seg_rows, n_seg, p_row, out_row, workspace,
+                                     workspace_bytes, gr, qr, &empty_r);
+    if (st != UFP4_OK) return st;
+    st = grouped_prepare(x, dtype, cols, ld, seg_rows, n_seg, p_col, out_col, workspace, workspace_bytes, gc, qc,
+                         &empty_c);
+    if (st != UFP4_OK) return st;
+    if (empty_r || empty_c) return UFP4_OK;   // both empty together: no rows or no columns
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool same = qr.grid == qc.grid && qr.round == qc.round && qr.rht == qc.rht &&
+                      (!qr.rht || qr.rht_seed == qc.rht_seed);
+    // one read per pass serves both for BF16 input of 128 x 64 TMA tiles; the
+    // amax slots of both orientations must fit the workspace's partial area
+    if (!same || dtype != UFP4_BF16 || kWsPartials + 2 * (size_t)n_seg * 4 > kWsStats) {
+        cudaError_t e = launch_quantize_grouped(qr, gr, workspace, s);
+        return from_cuda(e != cudaSuccess ? e : launch_quantize_grouped(qc, gc, workspace, s));
+    }
+    GroupDual gd;
+    memset(&gd, 0, sizeof gd);
+    gd.n = n_seg;
+    const int64_t nct = (cols + 63) / 64;
+    for (int i = 0; i < n_seg; ++i) {
+        gd.in_row[i + 1] = gr.in_row[i + 1];
+        gd.roff[i] = gr.out_off[i];
+        gd.koff[i] = gc.out_off[i];
+        gd.tiles[i + 1] = gd.tiles[i] + (seg_rows[i] + 127) / 128 * nct;
+    }
+    if (gd.tiles[n_seg] > (int64_t)INT32_MAX) return UFP4_ERR_UNSUPPORTED;
+    return from_cuda(launch_quantize_grouped_dual(qr, qc, gd, workspace, s));
 }
 
 ufp4_status ufp4_gemm_grouped(const ufp4_qtensor *a, const ufp4_qtensor *b, const ufp4_gemm_group *groups,

@@ -44,6 +44,19 @@ struct GroupQuant {
     int64_t units[kMaxGroups + 1];    // prefix sums of work units (16-blocks / column-pair units)
 };
 
+// Segment table of a grouped quantization of both orientations (host-built,
+// passed by value): segment e's input rows [in_row[e], in_row[e + 1]), its
+// row-wise output rows from roff[e], its column-wise k range from koff[e],
+// and the prefix sums of its 128 x 64 input tiles (ceil(T_e / 128) row tiles
+// per segment times the column tiles).
+struct GroupDual {
+    int32_t n;
+    int64_t in_row[kMaxGroups + 1];
+    int64_t roff[kMaxGroups];
+    int64_t koff[kMaxGroups];
+    int64_t tiles[kMaxGroups + 1];
+};
+
 // GEMM output tile (rows of A x rows of B per CTA tile).
 constexpr int kGemmBM = 128;
 constexpr int kGemmBN = 256;
@@ -93,6 +106,12 @@ cudaError_t launch_quantize_dual(const QuantLaunch &qr, const QuantLaunch &qc, v
 // Grouped quantization: x holds segments in row order; ws keeps one fp32
 // maximum per segment and the status word.
 cudaError_t launch_quantize_grouped(const QuantLaunch &q, const GroupQuant &gt, void *ws, cudaStream_t s);
+
+// Both orientations of a grouped BF16 tensor from one read per pass (amax,
+// then quantization): qr row-wise and qc column-wise, sharing grid, rounding
+// and transform.  Each result equals its own launch_quantize_grouped.
+cudaError_t launch_quantize_grouped_dual(const QuantLaunch &qr, const QuantLaunch &qc, const GroupDual &gd,
+                                         void *ws, cudaStream_t s);
 
 cudaError_t launch_gemm_grouped(const uint8_t *a_codes, const uint8_t *a_eplane, const uint8_t *a_scales,
                                 const float *a_ts, int64_t a_rows, int64_t a_kpad, const uint8_t *b_codes,

@@ -829,6 +829,14 @@ template <> struct ColRaw<__nv_bfloat16> {
 #pragma unroll
         for (int i = 0; i < 16; ++i) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w[i]) : "r"(sa + i * pitch));
     }
+    // rows nvalid..15 read as zeros (the rows of a tile past its segment's end)
+    __device__ __forceinline__ void load_shared_rows(uint32_t sa, uint32_t pitch, int nvalid) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            w[i] = 0u;
+            if (i < nvalid) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w[i]) : "r"(sa + i * pitch));
+        }
+    }
     __device__ __forceinline__ uint64_t pair(int i, const Signs &sg) const {
         return pk2(__uint_as_float(bf16lo_s(w[i], sg.m[i])), __uint_as_float(bf16hi_s(w[i], sg.m[i])));
     }
@@ -2272,8 +2280,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas)
 template <bool AMAX, class K, class... P>
 cudaError_t launch_staged(K kern, int64_t work_ctas, int *grid_out, cudaStream_t s, P... args);
 
-template <class In>
-cudaError_t quantize_grouped_typed(const QuantLaunch &q, const GroupQuant &gt, void *ws, cudaStream_t s) {
+Args grouped_args(const QuantLaunch &q, void *ws) {
     Args a{};
     a.x = q.x; a.ld = q.ld; a.cols = q.cols;
     a.out_rows = q.out_rows; a.k = q.k; a.kpad = kpad_of(q.k); a.nkt = a.kpad / 64;
@@ -2284,6 +2291,12 @@ cudaError_t quantize_grouped_typed(const QuantLaunch &q, const GroupQuant &gt, v
     a.eplane = q.grid == kE1M2 ? q.eplane : nullptr;
     a.uqmax = q.grid == kE2M1C ? 2.0f : 3.5f;
     a.utop = grid_top(q.grid);
+    return a;
+}
+
+template <class In>
+cudaError_t quantize_grouped_typed(const QuantLaunch &q, const GroupQuant &gt, void *ws, cudaStream_t s) {
+    Args a = grouped_args(q, ws);
     uint32_t *slots = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsPartials);
     cudaError_t e = cudaMemsetAsync(ws, 0, kWsPartials + (size_t)gt.n * sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
@@ -2344,6 +2357,261 @@ cudaError_t quantize_grouped_typed(const QuantLaunch &q, const GroupQuant &gt, v
     UFP4_GQ(true, kE1M2, kSR, false)    UFP4_GQ(true, kE1M2, kSR, true)
 #undef UFP4_GQ
     return cudaErrorInvalidValue;
+}
+
+// ======================================= grouped, both orientations (BF16)
+// The segments of a grouped tensor are cut into segment-aligned 128 x 64
+// tiles: segment e's rows are split into ceil(T_e / 128) row tiles starting at
+// its first row, so no tile straddles two segments, and tile rows past the
+// segment's end are read as zeros (the zero padding of the column-wise
+// layout; padding rows of the row-wise layout).  Tiles are numbered segment
+// by segment (the GroupDual prefix table) and every CTA takes a contiguous
+// run of them through the TMA ring, so it meets few segments and the
+// segment lookup is uniform across the CTA.  AMAX: each thread keeps the
+// row-wise and column-wise block maxima of its current segment and the CTA's
+// warps flush them (atomicMax on the bit patterns) when the segment changes.
+// Otherwise both results as k_dual_tile, each block with its segment's
+// tensor scales.
+
+// Tensor-scale encode factor S_enc of a segment from its amax slot.
+__device__ __forceinline__ float senc_of(uint32_t slot, float qmax) {
+    const float A_t = __uint_as_float(slot);
+    float se = 1.0f;
+    if (A_t > 0.0f) {
+        se = __fdiv_rn(448.0f * qmax, A_t);
+        if (se > kFltMax) se = kFltMax;
+    }
+    return se;
+}
+
+// One segment-aligned tile at shared address st: `nvalid` of its rows belong
+// to the segment, its row-wise output starts at row `orow`, its column-wise
+// blocks at k-block `kb0`, of which the first `nkb` (4 or 8) lie in the
+// segment's k range.
+template <int GRID, int ROUND, bool RHT, bool AMAX>
+__device__ __forceinline__ void dual_tile_grouped(const Args &ar, const Args &ac, const DualGeom &g, uint32_t st,
+                                                  int nvalid, uint32_t orow, uint32_t kb0, uint32_t nkb, uint32_t ct,
+                                                  const Signs &sgr, const Signs &sgc, float Sr, float Sc,
+                                                  const float *s_kr, const float *s_kc, bool fr, bool fc,
+                                                  uint8_t *stage_codes, uint8_t *stage_scales, float &mr, float &mc) {
+    const uint32_t c0 = ct * kTileCols;
+    {
+        const uint32_t c = c0 + 2 * g.cp;
+        const int left = nvalid - 16 * (int)g.rb;   // rows of this unit inside the segment
+        ColRaw<__nv_bfloat16> raw;
+        const uint32_t sa = st + 16 * g.rb * (kTileCols * 2) + g.cp * 4;
+        if (left >= 16) raw.load_shared(sa, kTileCols * 2);   // (warp-uniform branches)
+        else if (left > 0) raw.load_shared_rows(sa, kTileCols * 2, left);
+        else raw.zero();
+        if (AMAX) {
+            if (c < g.cols && left > 0) {
+                uint64_t P[16];
+                col_values<__nv_bfloat16, RHT>(raw, sgc, P);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float a, b;
+                    upk2(P[i], a, b);
+                    mc = max_nan(mc, max_nan(fabsf(a), fabsf(b)));
+                }
+            }
+        } else {
+            uint2 w0 = make_uint2(0u, 0u), w1 = make_uint2(0u, 0u);
+            uint32_t e0 = 0, e1 = 0;
+            if (c < g.cols && g.rb < nkb)
+                col_unit_words<__nv_bfloat16, GRID, ROUND, RHT>(ac, raw, kb0 + g.rb, c, left > 0, sgc, Sc, s_kc, fc,
+                                                                w0, w1, e0, e1);
+            reinterpret_cast<uint2 *>(stage_codes)[g.rb * kTileCols + 2 * g.cp] = w0;
+            reinterpret_cast<uint2 *>(stage_codes)[g.rb * kTileCols + 2 * g.cp + 1] = w1;
+            stage_scales[g.rb * kTileCols + 2 * g.cp] = (uint8_t)e0;
+            stage_scales[g.rb * kTileCols + 2 * g.cp + 1] = (uint8_t)e1;
+        }
+    }
+    {
+        const uint32_t b = ct * (kTileCols / 16) + g.bc;
+        if (b < g.kvr) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = (int)g.q + 64 * h;
+                Raw<__nv_bfloat16> ra;
+                if (row < nvalid) ra.load_shared(st + (uint32_t)row * (kTileCols * 2) + g.bc * 32);
+                else ra.zero();
+                if (AMAX) {
+                    if (row < nvalid) {
+                        float lo[8], hi[8];
+                        block_values<__nv_bfloat16, RHT>(ra, sgr, lo, hi);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) mr = max_nan(mr, max_nan(fabsf(lo[j]), fabsf(hi[j])));
+                    }
+                } else {
+                    // rows past the segment's end are the layout's zero padding rows
+                    quant_block_row<__nv_bfloat16, GRID, ROUND, RHT>(ar, ra, orow + (uint32_t)row, b, sgr, Sr,
+                                                                     s_kr, g.csr, g.nktr, fr);
+                }
+            }
+        }
+    }
+}
+
+template <int GRID, int ROUND, bool RHT, bool AMAX>
+__global__ void __launch_bounds__(kThreads, kStagedMinCtas)
+    k_dual_tile_grouped(const __grid_constant__ CUtensorMap tmx, Args ar, Args ac,
+                        const __grid_constant__ GroupDual gd, uint32_t nct, uint32_t *slots) {
+    // slots: [0, n) row-wise maxima, [n, 2n) column-wise maxima (fp32 bits)
+    constexpr int kRing = ring_depth<false>();
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ float s_kr[256], s_kc[256];   // the current segment's per-code multipliers
+    const RingCtl ring = ring_init<kRing>(dsm);
+    uint8_t *stage_codes = dsm + kRing * kChunk + 64;            // [rb][cl] uint2
+    uint8_t *stage_scales = stage_codes + 8 * kTileCols * 8;    // [rb][cl] byte
+    const uint32_t total = (uint32_t)gd.tiles[gd.n];
+    const uint32_t per = (total + gridDim.x - 1) / gridDim.x;
+    const uint32_t t0 = blockIdx.x * per;
+    const uint32_t nloc = t0 < total ? min(per, total - t0) : 0u;
+    uint32_t issued = 0, j = 0;
+    // Position of the CTA's consecutive tiles (segment, row tile, column tile),
+    // advanced one tile at a time: a binary search only when a segment ends.
+    struct Cursor {
+        int e;
+        uint32_t rt, ct;
+    };
+    auto seek = [&](uint32_t i) {
+        Cursor c;
+        c.e = find_seg(gd.tiles, gd.n, (int64_t)i);
+        const uint32_t lt = (uint32_t)(i - gd.tiles[c.e]);
+        c.rt = lt / nct;
+        c.ct = lt - c.rt * nct;
+        return c;
+    };
+    auto next = [&](Cursor &c, uint32_t i_next) {   // i_next: the tile after c's
+        if (i_next >= (uint32_t)gd.tiles[c.e + 1]) {
+            if (i_next < total) c = seek(i_next);
+            return;
+        }
+        if (++c.ct == nct) { c.ct = 0; ++c.rt; }
+    };
+    Cursor icur = seek(t0);   // the issuing thread's, kRing tiles ahead
+    auto issue = [&](uint32_t jj) {
+        if (jj >= nloc) return;
+        const uint32_t bar = ring.bars + 8u * (jj % kRing);
+        ptx::mbar_arrive_expect_tx(bar, kTileBytes);   // rows past the tensor arrive as zeros
+        ptx::tma_load_2d(ring.buf + (jj % kRing) * kChunk, &tmx, (int32_t)(icur.ct * kTileCols),
+                         (int32_t)(gd.in_row[icur.e] + (int64_t)icur.rt * kTileRows), bar);
+        issued = jj + 1;
+        next(icur, t0 + jj + 1);
+    };
+    if (threadIdx.x == 0) {
+        ptx::prefetch_tmap(&tmx);
+        for (uint32_t t = 0; t < kRing; ++t) issue(t);
+    }
+    const float qmax = GRID == kE2M1 ? 6.0f : ar.uqmax;
+    if (!AMAX && blockIdx.x == 0) {
+        // every segment's S_dec, and the non-finite flag
+        for (int e = threadIdx.x; e < gd.n; e += blockDim.x) {
+            const float ar_t = __uint_as_float(slots[e]), ac_t = __uint_as_float(slots[gd.n + e]);
+            ar.tensor_scale[e] = ar_t > 0.0f ? __fdiv_rn(ar_t, 448.0f * qmax) : 1.0f;
+            ac.tensor_scale[e] = ac_t > 0.0f ? __fdiv_rn(ac_t, 448.0f * qmax) : 1.0f;
+            if ((!isfinite(ar_t) || !isfinite(ac_t)) && ar.status) atomicOr(ar.status, 1u);
+        }
+    }
+    const uint32_t smask = RHT ? rht_sign_mask(ar.rht_seed) : 0u;
+    const Signs sgr = row_signs<__nv_bfloat16>(smask), sgc = col_signs<__nv_bfloat16>(smask);
+    const DualGeom g = dual_geom(ar, ac);
+    float mr = 0.0f, mc = 0.0f;
+    int e_cur = -1;
+    float Sr = 1.0f, Sc = 1.0f;
+    bool fr = false, fc = false;
+    // a segment's tables k = min(S_enc / E4M3(e), FLT_MAX) x (1/4 with the
+    // transform) x (2^-8 where the E1M2 RTNE rounding folds it), as the
+    // single-tensor prologue builds them; rebuilt when the CTA's run of tiles
+    // enters the next segment (every thread has left the previous tile)
+    auto tables = [&](int e) {
+        Sr = senc_of(slots[e], qmax);
+        Sc = senc_of(slots[gd.n + e], qmax);
+        fr = GRID == kE1M2 && ROUND == kRTNE && Sr >= 1.5407439555097887e-33f;
+        fc = GRID == kE1M2 && ROUND == kRTNE && Sc >= 1.5407439555097887e-33f;
+        const float kf = RHT ? 0.25f : 1.0f;
+        for (int c = threadIdx.x; c < 256; c += blockDim.x) {
+            const float d = e4m3_to_f32((uint32_t)c);
+            float kr = 0.0f, kc = 0.0f;
+            if (d > 0.0f) {
+                kr = fminf(__fdiv_rn(Sr, d), kFltMax);
+                kc = fminf(__fdiv_rn(Sc, d), kFltMax);
+            } else if (!(d == 0.0f)) {
+                kr = kc = d;   // NaN code: only reachable from non-finite input
+            }
+            s_kr[c] = kr * (fr ? kf * 0.00390625f : kf);
+            s_kc[c] = kc * (fc ? kf * 0.00390625f : kf);
+        }
+        __syncthreads();
+    };
+    bool ok = true;
+    Cursor cur = seek(t0);
+    for (; j < nloc; ++j) {
+        const bool mine = ring_wait_own<kRing>(ring, j);
+        const uint32_t i = t0 + j;
+        const int e = cur.e;
+        const uint32_t rt = cur.rt, ct = cur.ct;
+        next(cur, i + 1);
+        const uint32_t T = (uint32_t)(gd.in_row[e + 1] - gd.in_row[e]);   // rows fit 32 bits (checked on the host)
+        const uint32_t left = T - rt * kTileRows;
+        const int nvalid = left < kTileRows ? (int)left : (int)kTileRows;
+        // column-wise blocks of the segment's k range (kpad(T) / 16, a multiple of 4) in this tile
+        const uint32_t kbl = (T + 63) / 64 * 4 - rt * 8;
+        const uint32_t nkb = kbl < 8 ? kbl : 8u;
+        const uint32_t kb0 = (uint32_t)(gd.koff[e] / 16) + rt * 8;
+        if (!AMAX && e != e_cur) tables(e);   // uniform across the CTA
+        e_cur = e;
+        if (mine)
+            dual_tile_grouped<GRID, ROUND, RHT, AMAX>(ar, ac, g, ring.buf + (j % kRing) * kChunk, nvalid,
+                                                      (uint32_t)gd.roff[e] + rt * kTileRows, kb0, nkb, ct, sgr, sgc,
+                                                      Sr, Sc, s_kr, s_kc, fr, fc, stage_codes, stage_scales, mr, mc);
+        __syncthreads();   // tile consumed; column-wise results staged
+        if (*ring.abort) { ok = false; break; }
+        if (threadIdx.x == 0) issue(j + kRing);
+        if (AMAX) {
+            // the segment's last tile in this CTA: flush its maxima, one atomic per warp
+            if (j + 1 == nloc || cur.e != e) {
+#pragma unroll
+                for (int o = 16; o; o >>= 1) {
+                    mr = max_nan(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+                    mc = max_nan(mc, __shfl_xor_sync(0xffffffffu, mc, o));
+                }
+                if ((threadIdx.x & 31) == 0) {
+                    seg_max_flush(slots, e, RHT ? mr * 0.25f : mr);
+                    seg_max_flush(slots + gd.n, e, RHT ? mc * 0.25f : mc);
+                }
+                mr = mc = 0.0f;
+            }
+        } else {
+            // the staged column-wise results: column c, blocks kb0 .. kb0 + nkb - 1
+            {
+                const uint32_t cl = threadIdx.x / 4, part = threadIdx.x % 4;
+                const uint32_t c = ct * kTileCols + cl;
+                if (c < g.cols && 2 * part < nkb) {
+                    const uint2 a0 = reinterpret_cast<const uint2 *>(stage_codes)[(2 * part) * kTileCols + cl];
+                    const uint2 a1 = reinterpret_cast<const uint2 *>(stage_codes)[(2 * part + 1) * kTileCols + cl];
+                    put_codes(ac, (size_t)c * g.csc + (size_t)(kb0 + 2 * part) * 8,
+                              make_uint4(a0.x, a0.y, a1.x, a1.y));
+                }
+            }
+            if (threadIdx.x < 2 * kTileCols) {
+                const uint32_t cl = threadIdx.x / 2, h = threadIdx.x % 2;
+                const uint32_t c = ct * kTileCols + cl;
+                if (c < g.cols && 4 * h < nkb) {
+                    uint32_t w = 0;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) w |= (uint32_t)stage_scales[(4 * h + k) * kTileCols + cl] << (8 * k);
+                    *reinterpret_cast<uint32_t *>(ac.scales + scale_offset32(c, kb0 + 4 * h, g.nktc)) = w;
+                }
+            }
+            __syncthreads();   // staging buffers free for the next tile
+        }
+    }
+    if (!ok) {
+        if (threadIdx.x == 0) atomicOr(&g_quant_timeout, 1u);
+        ring_drain<kRing>(ring, j, issued);
+    }
+    if (!AMAX) dual_padding(ar, ac, g);
 }
 
 // ============================================================= statistics
@@ -2864,6 +3132,37 @@ Args make_args(const QuantLaunch &q, void *ws) {
     return a;
 }
 
+// Both orientations of a grouped BF16 tensor: the amax pass and the
+// quantization pass of k_dual_tile_grouped, one read of x each.
+cudaError_t quantize_grouped_dual_bf16(const QuantLaunch &qr, const QuantLaunch &qc, const GroupDual &gd, void *ws,
+                                       cudaStream_t s) {
+    Args ar = grouped_args(qr, ws), ac = grouped_args(qc, ws);
+    ac.status = nullptr;   // the row-wise side reports both
+    alignas(64) CUtensorMap tm;
+    if (!make_input_tile_map(&tm, qr.x, qr.rows, qr.cols, qr.ld, kTileCols, kTileRows)) return cudaErrorInvalidValue;
+    const uint32_t nct = (uint32_t)((qr.cols + kTileCols - 1) / kTileCols);
+    const int64_t ntiles = gd.tiles[gd.n];
+    uint32_t *slots = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsPartials);
+    cudaError_t e = cudaMemsetAsync(ws, 0, kWsPartials + 2 * (size_t)gd.n * sizeof(uint32_t), s);
+    if (e != cudaSuccess || ntiles == 0) return e;
+    e = qr.rht ? launch_staged_smem(k_dual_tile_grouped<kE2M1, kRTNE, true, true>, kTileSmem, ntiles, nullptr, s,
+                                    tm, ar, ac, gd, nct, slots)
+               : launch_staged_smem(k_dual_tile_grouped<kE2M1, kRTNE, false, true>, kTileSmem, ntiles, nullptr, s,
+                                    tm, ar, ac, gd, nct, slots);
+    if (e != cudaSuccess) return e;
+    const int kgrid = qr.grid == kE2M1 ? kE2M1 : kE1M2;   // clamped E2M1 runs the uniform-grid kernels
+#define UFP4_GD(GRID, ROUND, RHT)                                                                             \
+    if (kgrid == GRID && qr.round == ROUND && (qr.rht != 0) == RHT)                                          \
+        return launch_staged_smem(k_dual_tile_grouped<GRID, ROUND, RHT, false>, kTileSmem, ntiles, nullptr, s, tm, \
+                                  ar, ac, gd, nct, slots);
+    UFP4_GD(kE2M1, kRTNE, false) UFP4_GD(kE2M1, kRTNE, true)
+    UFP4_GD(kE2M1, kSR, false)   UFP4_GD(kE2M1, kSR, true)
+    UFP4_GD(kE1M2, kRTNE, false) UFP4_GD(kE1M2, kRTNE, true)
+    UFP4_GD(kE1M2, kSR, false)   UFP4_GD(kE1M2, kSR, true)
+#undef UFP4_GD
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 int num_sms() {
@@ -2967,6 +3266,12 @@ cudaError_t launch_quantize_dual(const QuantLaunch &qr, const QuantLaunch &qc, v
 cudaError_t launch_quantize_grouped(const QuantLaunch &q, const GroupQuant &gt, void *ws, cudaStream_t s) {
     if (q.dtype == 0) return quantize_grouped_typed<__nv_bfloat16>(q, gt, ws, s);
     return quantize_grouped_typed<float>(q, gt, ws, s);
+}
+
+cudaError_t launch_quantize_grouped_dual(const QuantLaunch &qr, const QuantLaunch &qc, const GroupDual &gd,
+                                         void *ws, cudaStream_t s) {
+    if (qr.dtype != 0) return cudaErrorInvalidValue;
+    return quantize_grouped_dual_bf16(qr, qc, gd, ws, s);
 }
 
 cudaError_t launch_dequantize(const uint8_t *codes, const uint8_t *scales, const float *ts,

@@ -31,7 +31,7 @@ EXPORTED = ["ufp4_kpad", "ufp4_codes_bytes", "ufp4_scales_bytes", "ufp4_workspac
             "ufp4_quantize", "ufp4_check", "ufp4_dequantize", "ufp4_gemm", "ufp4_stats",
             "ufp4_status_string", "ufp4_quantize_noalloc", "ufp4_grouped_rows",
             "ufp4_grouped_kpad", "ufp4_quantize_grouped", "ufp4_gemm_grouped", "ufp4_quantize_dual",
-            "ufp4_gemm_amax", "ufp4_quantize_stats"]
+            "ufp4_gemm_amax", "ufp4_quantize_stats", "ufp4_quantize_grouped_dual"]
 
 
 class QParamsC(ctypes.Structure):
@@ -120,6 +120,11 @@ def lib():
                                             ctypes.POINTER(QParamsC), ctypes.POINTER(QTensorC), vp,
                                             ctypes.c_size_t, vp]
         L.ufp4_quantize_grouped.restype = ctypes.c_int
+        L.ufp4_quantize_grouped_dual.argtypes = [vp, ctypes.c_int32, i64, i64, i64p, ctypes.c_int32,
+                                                 ctypes.POINTER(QParamsC), ctypes.POINTER(QParamsC),
+                                                 ctypes.POINTER(QTensorC), ctypes.POINTER(QTensorC), vp,
+                                                 ctypes.c_size_t, vp]
+        L.ufp4_quantize_grouped_dual.restype = ctypes.c_int
         L.ufp4_gemm_grouped.argtypes = [ctypes.POINTER(QTensorC), ctypes.POINTER(QTensorC),
                                         ctypes.POINTER(GemmGroupC), ctypes.c_int32, vp]
         L.ufp4_gemm_grouped.restype = ctypes.c_int
@@ -400,6 +405,35 @@ def ufp4_quantize_grouped(x, grid, seg_rows, rht=False, rht_seed=0, round=UFP4_R
     _check(st, "ufp4_quantize_grouped")
     out.seg_rows = list(seg_rows)
     return out
+
+
+def ufp4_quantize_grouped_dual(x, grid, seg_rows, rht=False, rht_seed=0, round=UFP4_RTNE, sr_seed=0,
+                               sr_counter_row=0, sr_counter_col=0, out_row=None, out_col=None, ws=None,
+                               stream=None):
+    """Row-wise and column-wise grouped quantization of x from one read of x
+    per pass; each result as its own ufp4_quantize_grouped call."""
+    _cuda(x, "x")
+    cols = x.shape[1]
+    n = len(seg_rows)
+    if out_row is None:
+        out_row = QTensor.empty(grouped_rows(seg_rows), cols, grid, x.device)
+        out_row.tensor_scale = torch.empty(max(n, 1), dtype=torch.float32, device=x.device)
+    if out_col is None:
+        out_col = QTensor.empty(cols, grouped_kpad(seg_rows), grid, x.device)
+        out_col.tensor_scale = torch.empty(max(n, 1), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(x.device)
+    pr = qparams(grid, rht, rht_seed, round, sr_seed, sr_counter_row, False)
+    pc = qparams(grid, rht, rht_seed, round, sr_seed, sr_counter_col, True)
+    qr, qc = out_row.c(), out_col.c()
+    st = lib().ufp4_quantize_grouped_dual(x.data_ptr(), _dtype_code(x), cols, x.stride(0),
+                                          _i64_array(seg_rows), n, ctypes.byref(pr), ctypes.byref(pc),
+                                          ctypes.byref(qr), ctypes.byref(qc), ws.data_ptr(), ws.numel(),
+                                          _stream(stream))
+    _check(st, "ufp4_quantize_grouped_dual")
+    out_row.seg_rows = list(seg_rows)
+    out_col.seg_rows = list(seg_rows)
+    return out_row, out_col
 
 
 def ufp4_gemm_grouped(a, b, groups, stream=None):

@@ -348,6 +348,31 @@ UFP4_API ufp4_status ufp4_quantize_grouped(const void *x, int32_t dtype, int64_t
                                            void *workspace, size_t workspace_bytes,
                                            ufp4_stream_t stream);
 
+/* Both grouped quantizations of x that an MoE layer's training step needs --
+ * row-wise (p_row->colwise == 0, the row-wise grouped layout above) and
+ * column-wise (p_col->colwise == 1, the column-wise grouped layout) -- from
+ * one read of x per pass: an amax pass that takes every segment's maxima of
+ * both orientations, then one quantization pass writing both results.  The
+ * three grouped GEMMs consume every operand in both orientations ([ZC]
+ * zhichai.net post, Key points "The fix -- UFP4": the transform and
+ * quantization on the fwd_y, bwd_dx and bwd_dw operands; [HP] technical
+ * approach: the MoE models).
+ * Arguments as for ufp4_quantize_grouped, one parameter set and one result
+ * per orientation; every constraint of both orientations applies (cols % 16
+ * == 0).  Each result is bit-identical to its own ufp4_quantize_grouped call
+ * (own per-segment tensor scales, SR seed and counter).  The one-read path
+ * serves BF16 input when the two parameter sets share grid, rounding mode
+ * and transform (seed included); otherwise the call runs the two grouped
+ * quantizations one after the other.  The workspace holds both
+ * orientations' per-segment maxima (2 * n_seg floats) and the non-finite
+ * status, which covers both results.  The pages have no dual-orientation
+ * call of their own; this one reorders reads, not arithmetic. */
+UFP4_API ufp4_status ufp4_quantize_grouped_dual(const void *x, int32_t dtype, int64_t cols, int64_t ld,
+                                                const int64_t *seg_rows_host, int32_t n_seg,
+                                                const ufp4_qparams *p_row, const ufp4_qparams *p_col,
+                                                const ufp4_qtensor *out_row, const ufp4_qtensor *out_col,
+                                                void *workspace, size_t workspace_bytes, ufp4_stream_t stream);
+
 /* One GEMM per group, C_g = A_g B_g^T, in a single launch.  A group's
  * operands are views of two quantized tensors a and b (same grid):
  *   A_g = rows [a_row[g], a_row[g] + M[g]) and k range [a_k[g], a_k[g] + K[g]) of a,

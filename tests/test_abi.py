@@ -231,6 +231,21 @@ def test_dual_and_grouped_reject_bad_arguments_on_host(L):
     assert grouped(p, out, [100, 0, 37]) == INV                            # amax is per segment
     assert grouped(_q(grid=3), _qt(256, 128, 3), [100, 0, 37]) == UNS      # MXFP4
 
+    def gdual(pr, pc, qr, qc, counts, cols=128):
+        return L.ufp4_quantize_grouped_dual(x, 0, cols, cols, seg(counts), len(counts),
+                                            ctypes.byref(pr) if pr else None, ctypes.byref(pc) if pc else None,
+                                            ctypes.byref(qr), ctypes.byref(qc), ws, wsb, None)
+
+    gqr, gqc = _qt(256, 128), _qt(128, 192)
+    assert gdual(None, _q(colwise=True), gqr, gqc, [100, 0, 37]) == INV           # no row params
+    assert gdual(_q(colwise=True), _q(colwise=True), gqr, gqc, [100, 0, 37]) == INV
+    assert gdual(_q(), _q(), gqr, gqc, [100, 0, 37]) == INV                       # column params row-wise
+    assert gdual(_q(), _q(colwise=True), gqr, _qt(128, 128), [100, 0, 37]) == INV  # column k != sum of kpad
+    assert gdual(_q(), _q(colwise=True), _qt(200, 128), gqc, [100, 0, 37]) == INV  # row count
+    assert gdual(_q(grid=3), _q(grid=3, colwise=True), _qt(256, 128, 3), _qt(128, 192, 3),
+                 [100, 0, 37]) == UNS                                             # MXFP4
+    assert gdual(_q(), _q(colwise=True), _qt(0, 128), _qt(128, 0), [0, 0]) == ufp4.UFP4_OK   # nothing to do
+
     def ggemm(a, b, groups, n=None):
         arr = (ufp4.GemmGroupC * max(len(groups), 1))(*groups)
         return L.ufp4_gemm_grouped(ctypes.byref(a), ctypes.byref(b), arr, len(groups) if n is None else n, None)

@@ -164,8 +164,8 @@ def test_dense_gemms_full_size_exact_codes(U, oracle, grid):
 def test_moe7p9b_grouped_full_size(U, oracle):
     """64 experts, 16384 tokens x top-6 (Dirichlet(1) routing, zero-token
     experts allowed), the benchmark's recipe: grouped RHT + E1M2
-    quantization of X, W, dY both ways (SR on dY) and the three grouped
-    GEMMs.  Sampled codes of three experts (largest, median, smallest
+    quantization of X, W, dY both ways from one read per pass (SR on dY; each
+    result equal to its own grouped call) and the three grouped GEMMs.  Sampled codes of three experts (largest, median, smallest
     nonzero) against the oracle, row-wise X and column-wise dY; sampled GEMM
     blocks of the same experts against the consumed operands; and the
     grouped fwd_y with RHT off against the oracle's own operands."""
@@ -178,12 +178,19 @@ def test_moe7p9b_grouped_full_size(U, oracle):
     grid = 1
     kw = dict(rht=True, rht_seed=2)
     wseg = [F] * E
-    qx = U.ufp4_quantize_grouped(tx, grid, counts, **kw)
-    qxc = U.ufp4_quantize_grouped(tx, grid, counts, colwise=True, **kw)
-    qdy = U.ufp4_quantize_grouped(tdy, grid, counts, round=1, sr_seed=3, **kw)
-    qdyc = U.ufp4_quantize_grouped(tdy, grid, counts, round=1, sr_seed=3, colwise=True, **kw)
-    qw = U.ufp4_quantize_grouped(tw, grid, wseg, **kw)
-    qwc = U.ufp4_quantize_grouped(tw, grid, wseg, colwise=True, **kw)
+    # both orientations of every operand from one read per pass, as the
+    # benchmark launches them; each result equals its own grouped call
+    qx, qxc = U.ufp4_quantize_grouped_dual(tx, grid, counts, **kw)
+    qdy, qdyc = U.ufp4_quantize_grouped_dual(tdy, grid, counts, round=1, sr_seed=3, **kw)
+    qw, qwc = U.ufp4_quantize_grouped_dual(tw, grid, wseg, **kw)
+    for q, t, seg, col, extra in ((qx, tx, counts, False, {}), (qxc, tx, counts, True, {}),
+                                  (qdy, tdy, counts, False, dict(round=1, sr_seed=3)),
+                                  (qdyc, tdy, counts, True, dict(round=1, sr_seed=3)),
+                                  (qw, tw, wseg, False, {}), (qwc, tw, wseg, True, {})):
+        single = U.ufp4_quantize_grouped(t, grid, seg, colwise=col, **kw, **extra)
+        assert torch.equal(q.codes, single.codes) and torch.equal(q.scales, single.scales)
+        assert torch.equal(q.eplane, single.eplane) and torch.equal(q.tensor_scale, single.tensor_scale)
+        del single
     T = sum(counts)
     y = torch.zeros(T, F, device="cuda")
     dx = torch.zeros(T, H, device="cuda")

@@ -177,3 +177,79 @@ def test_grouped_training_gemms(U, oracle, grid, rht):
         assert np.linalg.norm(dw[e * F:(e + 1) * F] - ref) <= 1e-5 * np.linalg.norm(ref)
     # rows of y / dx that belong to no expert do not exist (sum T_e rows); all written
     assert not np.any(y == 9.0) and not np.any(dx == 9.0)
+
+
+def _filled(U, rows, k, grid, n, dev="cuda"):
+    """A grouped QTensor whose buffers hold a sentinel, so that any byte a
+    call leaves unwritten shows up in the comparison."""
+    q = U.QTensor.empty(rows, k, grid, dev)
+    q.codes.fill_(0xA5)
+    q.scales.fill_(0x5A)
+    if q.eplane is not None:
+        q.eplane.fill_(0x3C)
+    q.tensor_scale = torch.full((max(n, 1),), -7.0, device=dev)
+    return q
+
+
+def _same(a, b):
+    torch.cuda.synchronize()
+    assert torch.equal(a.codes, b.codes)
+    assert torch.equal(a.scales, b.scales)
+    assert torch.equal(a.tensor_scale, b.tensor_scale)
+    assert (a.eplane is None) == (b.eplane is None)
+    if a.eplane is not None:
+        assert torch.equal(a.eplane, b.eplane)
+
+
+@pytest.mark.parametrize("counts,cols", [(COUNTS, H), ([128, 1, 0, 255, 129, 16, 200], 80),
+                                         ([300], 208), ([0, 5], 32)])
+@pytest.mark.parametrize("grid", [0, 1, 2])
+@pytest.mark.parametrize("rht", [False, True])
+@pytest.mark.parametrize("rnd", [0, 1])
+def test_grouped_dual_equals_two_grouped_calls(U, grid, rht, rnd, counts, cols):
+    """ufp4_quantize_grouped_dual (segment-aligned 128 x 64 tiles, one read per
+    pass) gives each orientation bit for bit what its own
+    ufp4_quantize_grouped call gives: codes, scales, correction planes, every
+    segment's tensor scale, padding rows and blocks (segments of 1, 16, 128,
+    129, 255 rows, empty ones, column counts off the 64-column tile)."""
+    g = np.random.default_rng(11)
+    T = sum(counts)
+    x = inputs.to_bf16_f32(g.standard_normal((T, cols), dtype=np.float32) *
+                           np.float32(2.0) ** g.integers(-3, 4, size=(T, 1)).astype(np.float32))
+    t = torch.from_numpy(x).to(torch.bfloat16).cuda()
+    n = len(counts)
+    kw = dict(rht=rht, rht_seed=5, round=rnd, sr_seed=9)
+    rr, kc = U.grouped_rows(counts), U.grouped_kpad(counts)
+    dr, dc = _filled(U, rr, cols, grid, n), _filled(U, cols, kc, grid, n)
+    U.ufp4_quantize_grouped_dual(t, grid, counts, sr_counter_row=3, sr_counter_col=4, out_row=dr, out_col=dc, **kw)
+    sr, sc = _filled(U, rr, cols, grid, n), _filled(U, cols, kc, grid, n)
+    U.ufp4_quantize_grouped(t, grid, counts, sr_counter=3, out=sr, **kw)
+    U.ufp4_quantize_grouped(t, grid, counts, sr_counter=4, colwise=True, out=sc, **kw)
+    _same(dr, sr)
+    _same(dc, sc)
+    assert U.ufp4_check() == U.UFP4_OK
+
+
+@pytest.mark.parametrize("rht", [False, True])
+def test_grouped_dual_matches_oracle(U, oracle, rht):
+    """The grouped dual call against the oracle's per-segment quantization
+    (dY-like input with SR): bit-exact without the transform, the code bar
+    with it."""
+    x, w, dy = _data()
+    t = torch.from_numpy(dy).to(torch.bfloat16).cuda()
+    qr, qc = U.ufp4_quantize_grouped_dual(t, 1, COUNTS, rht=rht, rht_seed=2, round=1, sr_seed=3)
+    for q, col in ((qr, False), (qc, True)):
+        got = _gpu_segments(U, q, COUNTS, col)
+        ref = oracle.quantize_grouped(dy, COUNTS, 1, rht=rht, rht_seed=2, round_mode=1, sr_seed=3, colwise=col)
+        _check_segments(got, ref, rht)
+
+
+def test_grouped_dual_nonfinite_flag(U):
+    """A NaN in one segment raises the workspace's non-finite flag."""
+    x = torch.zeros(200, 64, dtype=torch.bfloat16, device="cuda")
+    x[150, 3] = float("nan")
+    ws = U.workspace()
+    U.ufp4_quantize_grouped_dual(x, 1, [100, 100], ws=ws)
+    assert U.ufp4_check(ws) == U.UFP4_ERR_NONFINITE
+    U.ufp4_quantize_grouped_dual(torch.ones(200, 64, dtype=torch.bfloat16, device="cuda"), 1, [100, 100], ws=ws)
+    assert U.ufp4_check(ws) == U.UFP4_OK
