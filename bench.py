@@ -612,17 +612,31 @@ def run_kernel(args):
     """One kernel of a step in isolation, for profiling: `steps` launches of
     the fwd_y GEMM (T x F x H), of the RHT quantization of X (T x H) in one
     orientation or both (quant_dual_*; the SR variant quantizes dY, T x F),
-    after `warmup` launches, the tensor amax given.  --shape dense: T, H, F =
-    8192, 2048, 5632; moe124b: 65536, 8192, 2048.  Prints the mean event
+    after `warmup` launches, the tensor amax given (quant_grouped_dual_e1m2:
+    the MoE-7.9B X both ways, its amax pass included).  --shape dense: T, H,
+    F = 8192, 2048, 5632; moe124b: 65536, 8192, 2048.  Prints the mean event
     time."""
     import torch
     from fp4_quantized_numerics_gb300 import build, inputs, ufp4 as U
     build.build()
     dev = torch.device("cuda", 0)
+    kind = args.kernel
+    if kind == "quant_grouped_dual_e1m2":
+        # the MoE-7.9B layer's X (64 experts, 16384 tokens x top-6, Dirichlet
+        # routing) in both orientations, amax pass included; --shape unused
+        counts = [int(c) for c in inputs.moe_counts(0)]
+        x = inputs.device_normal((sum(counts), 2048), 1.0, 21, dev)
+        qr = U.QTensor.empty(U.grouped_rows(counts), 2048, U.UFP4_E1M2, dev)
+        qc = U.QTensor.empty(2048, U.grouped_kpad(counts), U.UFP4_E1M2, dev)
+        qr.tensor_scale = torch.empty(len(counts), device=dev)
+        qc.tensor_scale = torch.empty(len(counts), device=dev)
+        fn = lambda: U.ufp4_quantize_grouped_dual(x, U.UFP4_E1M2, counts, rht=True, out_row=qr, out_col=qc)
+        work = 2 * x.numel() * Q_BYTES_PER_ELEM
+        unit = "GB/s"
+        return _run_kernel_timing(args, kind, fn, work, unit, dev)
     wl = WORKLOAD if args.shape == "moe124b" else DENSE
     T, H, F = wl["tokens"], wl["hidden"], wl["ffn"]
     x = inputs.device_normal((T, H), 1.0, 21, dev)
-    kind = args.kernel
     if kind.startswith("gemm"):
         grid = {"gemm_e2m1": U.UFP4_E2M1, "gemm_mxfp4": U.UFP4_MXFP4}.get(kind, U.UFP4_E1M2)
         w = inputs.device_normal((F, H), 0.02, 22, dev)
@@ -653,6 +667,11 @@ def run_kernel(args):
         fn = lambda: U.ufp4_quantize(x, grid, rht=True, colwise=col, out=q, amax_in=am)
         work = x.numel() * Q_BYTES_PER_ELEM
         unit = "GB/s"
+    return _run_kernel_timing(args, kind, fn, work, unit, dev)
+
+
+def _run_kernel_timing(args, kind, fn, work, unit, dev):
+    import torch
     flush = L2Flush(dev)
     for _ in range(args.warmup):
         fn()
@@ -967,7 +986,7 @@ def main():
     ap.add_argument("--kernel", default=None,
                     choices=["gemm_e2m1", "gemm_e1m2", "gemm_mxfp4", "quant_row_e1m2", "quant_col_e1m2", "quant_dual_e1m2",
                              "quant_dual_sr_e1m2", "amax_dual_e1m2",
-                             "quant_row_e2m1", "quant_col_e2m1"],
+                             "quant_row_e2m1", "quant_col_e2m1", "quant_grouped_dual_e1m2"],
                     help="time one kernel of the step in isolation (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -316,8 +316,8 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
     constexpr int ES = C::kESlots > 0 ? C::kESlots : 1;
     // bars: [0,S) full, [S,2S) empty, [2S,2S+ES) E slot written, [2S+ES,2S+2ES)
     // E slot free, then acc full, acc empty, MMA drained, then [.., +S) scales
-    // of a stage copied into TMEM
-    constexpr int kNBars = 3 * S + 2 * ES + 3;
+    // of a stage issued to the tensor cores, then the scale copies drained
+    constexpr int kNBars = 3 * S + 2 * ES + 4;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNBars);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
     static_assert(kNBars * 8 + 8 <= 256, "barrier area");
@@ -331,6 +331,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
     const uint32_t acce = accf + 8u;
     const uint32_t drained = accf + 16u;
     auto sfr = [&](int s) { return accf + 24u + 8u * s; };
+    const uint32_t sfd = accf + 24u + 8u * S;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int ntiles;
@@ -350,6 +351,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         ptx::mbar_init(accf, 1);
         ptx::mbar_init(acce, kEpiWarps);   // one arrival per epilogue warp
         ptx::mbar_init(drained, 1);
+        ptx::mbar_init(sfd, 1);
         *abort = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tma_a);
@@ -371,9 +373,10 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
 
     // Block-scale copies of stage s into its TMEM columns: SFA 4 columns per
     // K step at [0, 4 KS), SFB 8 columns per K step (rows 0-127, then
-    // 128-255) at [4 KS, 12 KS).  E2M1 issues them from their own warp so
-    // that they overlap the MMAs (completion signalled on sfr(s)); E1M2,
-    // with 4x the MMAs per stage, issues them in line from the MMA thread.
+    // 128-255) at [4 KS, 12 KS).  E2M1, MXFP4 and E1M2 with loaded planes
+    // issue them from their own warp so that their issue overlaps the MMAs'
+    // (sfr(s) says they are issued); E1M2 with expanded planes issues them in
+    // line from the MMA thread.
     auto copy_scales = [&](uint32_t s, int atoms, bool signal) {
         const uint64_t hi_sf = ptx::sdesc(0, 0, 128, 0);   // 32 rows x 16 B scale atom
         const uint32_t st = smem_base + s * C::kStageBytes;
@@ -387,15 +390,23 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
             ptx::tc_cp_32x128b_warpx4(sfb0 + 8u * j, dsb + 32u * j);
             ptx::tc_cp_32x128b_warpx4(sfb0 + 8u * j + 4u, dsb + 32u * (C::kKS + j));
         }
-        if (signal) ptx::tc_commit(sfr(s));
-    };
-    // The copy thread's last commits must complete before TMEM is freed.
-    auto drain_scales = [&](uint32_t g) {
-        for (uint32_t h = g > (uint32_t)S ? g - S : 0; h < g; ++h) {
-            const long long t0 = clock64();
-            while (!ptx::mbar_try_wait(sfr(h % S), (h / S) & 1))
-                if (clock64() - t0 > kWaitBudget) { raise_timeout(); break; }
+        if (signal) {
+            // Copies and the MMAs that read their columns form a pipelined
+            // pair in the tensor cores: ordered across threads by the fence
+            // before this arrival and the MMA thread's fence after its wait,
+            // so the MMAs need not wait for the copies to complete.
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(sfr(s));
         }
+    };
+    // Every copy the scale thread issued must complete before TMEM is freed:
+    // one commit tracks them all.
+    auto drain_scales = [&](uint32_t g) {
+        if (g == 0) return;
+        ptx::tc_commit(sfd);
+        const long long t0 = clock64();
+        while (!ptx::mbar_try_wait(sfd, 0))
+            if (clock64() - t0 > kWaitBudget) { raise_timeout(); break; }
     };
 
     if (warp == 0) {

@@ -176,3 +176,38 @@ def test_gemm_amax_fuses_next_quantization(U, oracle, grid, rht, M, N, K):
     else:
         want = oracle.tensor_amax(ch, rht=True, rht_seed=2)
         assert abs(am.item() / want - 1) <= 1e-6
+
+
+@pytest.mark.parametrize("grid", [0, 1, 3])
+def test_repeated_gemms_agree_with_varied_block_scales(U, oracle, grid):
+    """The scale warp's tensor-memory copies and the MMAs that read them are
+    ordered by fences around an mbarrier, not by waiting for the copies to
+    complete.  Rows and K blocks carry block scales spread over 2^-12..2^12,
+    so an MMA that read a stage's scales before they landed (or a previous
+    stage's) would be far off: 30 runs of a multi-tile, multi-stage GEMM in
+    each grid (E2M1, E1M2 with loaded planes, MXFP4) agree bit for bit and
+    with the oracle's fp64 product."""
+    M, N, K = 512, 1024, 2048
+    g = inputs.rng(77)
+    a = g.standard_normal((M, K), dtype=np.float32)
+    a *= np.float32(2.0) ** g.integers(-12, 13, size=(M, K // 32)).repeat(32, axis=1).astype(np.float32)
+    b = g.standard_normal((N, K), dtype=np.float32)
+    b *= np.float32(2.0) ** g.integers(-12, 13, size=(N, K // 32)).repeat(32, axis=1).astype(np.float32)
+    a, b = inputs.to_bf16_f32(a), inputs.to_bf16_f32(b)
+    ta = torch.from_numpy(a).to(torch.bfloat16).cuda()
+    tb = torch.from_numpy(b).to(torch.bfloat16).cuda()
+    qa, qb = U.ufp4_quantize(ta, grid), U.ufp4_quantize(tb, grid)
+    first = U.ufp4_gemm(qa, qb).clone()
+    for _ in range(29):
+        c = torch.full_like(first, 3.0)
+        U.ufp4_gemm(qa, qb, out=c)
+        assert torch.equal(c, first)
+    if grid == 3:
+        ra, rb = oracle.quantize_mx(a), oracle.quantize_mx(b)
+        A = oracle.dequantize_mx(ra["codes"], ra["scales"])
+        B = oracle.dequantize_mx(rb["codes"], rb["scales"])
+    else:
+        ra, rb = oracle.quantize(a, grid), oracle.quantize(b, grid)
+        A = oracle.dequantize(ra["codes"], ra["scales"], ra["tensor_scale"], grid)
+        B = oracle.dequantize(rb["codes"], rb["scales"], rb["tensor_scale"], grid)
+    assert _rel_fro(first.cpu().numpy(), oracle.gemm_f64(A, B)) <= TOL
