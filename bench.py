@@ -443,7 +443,7 @@ def run_e2e(args, U, step, d, dev, q_bytes):
             "overlap": "2 buffer sets, copy-in / compute / copy-out streams"}
 
 
-def _timeit(torch, fn, flush, n=10):
+def _timeit(torch, fn, flush, n=20):
     """Median of n timed runs (each after an L2 flush), after 3 untimed."""
     fn(); fn(); fn()
     torch.cuda.synchronize()
@@ -492,8 +492,11 @@ def quantizer_on_x(U, torch, dev, pk, flush, x):
     qe = U.QTensor.empty(R, C, U.UFP4_E1M2, dev)
     r["single_amax_given_rht_on_with_eplane"] = gbs(_timeit(torch, lambda: U.ufp4_quantize(
         x, U.UFP4_E1M2, rht=True, out=qe, ws=ws, amax_in=am), flush))
-    r["note"] = ("GB/s of algorithmic traffic (2.5625 B per element and result); the amax pass's "
-                 "second read and the correction plane's writes are not counted")
+    r["elems_per_s_single_amax_given_rht_on"] = round(r["single_amax_given_rht_on"] * 1e9 / Q_BYTES_PER_ELEM)
+    r["elems_per_s_single_with_amax_pass_rht_on"] = round(r["single_with_amax_pass_rht_on"] * 1e9 /
+                                                          Q_BYTES_PER_ELEM)
+    r["note"] = ("GB/s of algorithmic traffic (2.5625 B per element and result; elements/s = GB/s / 2.5625); "
+                 "the amax pass's second read and the correction plane's writes are not counted")
     return r
 
 
@@ -689,8 +692,86 @@ def _run_kernel_timing(args, kind, fn, work, unit, dev):
 
 
 
+def run_all_kernels(args):
+    """Every public call of the library once per timing, on the dense-1.5B
+    shapes (X 8192 x 2048, W 5632 x 2048, dY 8192 x 5632) and the MoE-7.9B
+    grouped X: medians of `steps` event-timed runs (L2 flushed, after 3
+    untimed) with each call's algorithmic bytes or FLOPs, so that an ncu
+    launch list of this command covers every kernel.  Prints one JSON line."""
+    import torch
+    from fp4_quantized_numerics_gb300 import build, inputs, ufp4 as U
+    build.build()
+    dev = torch.device("cuda", 0)
+    flush = L2Flush(dev)
+    T, H, F = DENSE["tokens"], DENSE["hidden"], DENSE["ffn"]
+    x = inputs.device_normal((T, H), 1.0, 31, dev)
+    w = inputs.device_normal((F, H), 0.02, 32, dev)
+    dy = inputs.device_normal((T, F), 1e-3, 33, dev)
+    x32 = x.float()
+    E1, E2, MX = U.UFP4_E1M2, U.UFP4_E2M1, U.UFP4_MXFP4
+    qx, qw = U.ufp4_quantize(x, E1, rht=True), U.ufp4_quantize(w, E1, rht=True)
+    qx2, qw2 = U.ufp4_quantize(x, E2, rht=True), U.ufp4_quantize(w, E2, rht=True)
+    qxn = U.QTensor.empty(T, H, E1, dev, eplane=False)
+    U.ufp4_quantize(x, E1, rht=True, out=qxn)
+    qwn = U.QTensor.empty(F, H, E1, dev, eplane=False)
+    U.ufp4_quantize(w, E1, rht=True, out=qwn)
+    qxm, qwm = U.ufp4_quantize(x, MX), U.ufp4_quantize(w, MX)
+    c = torch.empty(T, F, dtype=torch.float32, device=dev)
+    deq = torch.empty(T, H, dtype=torch.float32, device=dev)
+    counts = [int(v) for v in inputs.moe_counts(0)]
+    xg = inputs.device_normal((sum(counts), H), 1.0, 34, dev)
+    gr, gc = U.ufp4_quantize_grouped_dual(xg, E1, counts, rht=True)
+    wg = inputs.device_normal((len(counts) * 1408, H), 0.02, 35, dev)
+    gw = U.ufp4_quantize_grouped(wg, E1, [1408] * len(counts), rht=True)
+    yg = torch.empty(sum(counts), 1408, dtype=torch.float32, device=dev)
+    xo, wo = U.grouped_offsets(counts, False), U.grouped_offsets([1408] * len(counts), False)
+    starts = np.concatenate([[0], np.cumsum(counts)])
+    groups = [dict(M=counts[e], N=1408, K=H, a_row=xo[e], a_k=0, b_row=wo[e], b_k=0, a_seg=e, b_seg=e,
+                   c=yg[starts[e]:starts[e] + counts[e]] if counts[e] else yg[:1]) for e in range(len(counts))]
+    qb, gb = Q_BYTES_PER_ELEM, 2.0 * T * F * H
+    nx, ng = x.numel(), xg.numel()
+    calls = [
+        ("quantize row E1M2 RHT (amax pass + pass)", lambda: U.ufp4_quantize(x, E1, rht=True, out=qx), nx * qb, "B"),
+        ("quantize col E1M2 RHT", lambda: U.ufp4_quantize(x, E1, rht=True, colwise=True), nx * qb, "B"),
+        ("quantize row E2M1 RHT", lambda: U.ufp4_quantize(x, E2, rht=True, out=qx2), nx * qb, "B"),
+        ("quantize row E1M2 SR (dY)", lambda: U.ufp4_quantize(dy, E1, rht=True, round=U.UFP4_SR, sr_seed=3),
+         dy.numel() * qb, "B"),
+        ("quantize row E1M2 RHT, FP32 input", lambda: U.ufp4_quantize(x32, E1, rht=True), nx * 4.5625, "B"),
+        ("quantize dual E1M2 RHT X (on-chip single pass)", lambda: U.ufp4_quantize_dual(x, E1, rht=True),
+         2 * nx * qb, "B"),
+        ("quantize dual E1M2 RHT SR dY (two passes)",
+         lambda: U.ufp4_quantize_dual(dy, E1, rht=True, round=U.UFP4_SR, sr_seed=3), 2 * dy.numel() * qb, "B"),
+        ("quantize MXFP4 row", lambda: U.ufp4_quantize(x, MX), nx * MX_BYTES_PER_ELEM, "B"),
+        ("quantize MXFP4 col", lambda: U.ufp4_quantize(x, MX, colwise=True), nx * MX_BYTES_PER_ELEM, "B"),
+        ("dequantize E1M2 + inverse RHT", lambda: U.ufp4_dequantize(qx, inverse_rht=True, out=deq),
+         nx * (0.5625 + 4), "B"),
+        ("stats E1M2 RHT", lambda: U.ufp4_stats(x, qx, rht=True), nx * (2 + 0.5625), "B"),
+        ("quantize + stats E1M2 RHT (one read)", lambda: U.ufp4_quantize_stats(x, E1, rht=True), nx * qb, "B"),
+        ("quantize grouped row E1M2 RHT (MoE-7.9B X)", lambda: U.ufp4_quantize_grouped(xg, E1, counts, rht=True),
+         ng * qb, "B"),
+        ("quantize grouped col E1M2 RHT", lambda: U.ufp4_quantize_grouped(xg, E1, counts, rht=True, colwise=True),
+         ng * qb, "B"),
+        ("quantize grouped dual E1M2 RHT",
+         lambda: U.ufp4_quantize_grouped_dual(xg, E1, counts, rht=True, out_row=gr, out_col=gc), 2 * ng * qb, "B"),
+        ("GEMM E1M2 planes loaded, fwd_y", lambda: U.ufp4_gemm(qx, qw, out=c), gb, "F"),
+        ("GEMM E1M2 planes expanded on chip", lambda: U.ufp4_gemm(qxn, qwn, out=c), gb, "F"),
+        ("GEMM E2M1", lambda: U.ufp4_gemm(qx2, qw2, out=c), gb, "F"),
+        ("GEMM MXFP4", lambda: U.ufp4_gemm(qxm, qwm, out=c), gb, "F"),
+        ("GEMM E1M2 + output amax", lambda: U.ufp4_gemm_amax(qx, qw, out=c), gb, "F"),
+        ("grouped GEMM E1M2 fwd_y (MoE-7.9B)", lambda: U.ufp4_gemm_grouped(gr, gw, groups),
+         2.0 * sum(counts) * 1408 * H, "F"),
+    ]
+    out = []
+    for name, fn, work, kind in calls:
+        ms = _timeit(torch, fn, flush, max(args.steps, 1))
+        rate = work / (ms * 1e-3) / (1e12 if kind == "F" else 1e9)
+        out.append({"call": name, "ms": round(ms, 4), "rate": round(rate, 1),
+                    "unit": "TFLOP/s" if kind == "F" else "GB/s"})
+    print(json.dumps({"kernel": "all", "calls": out}))
+
+
 # ------------------------------------------------------------ all workloads
-def _ev_time(fn, flush, reps=10):
+def _ev_time(fn, flush, reps=20):
     import torch
     return _timeit(torch, fn, flush, reps)
 
@@ -882,9 +963,9 @@ def all_workloads(U, torch, dev, pk, flush, with_oracle=True):
             U.ufp4_gemm_grouped(qs["xr"], qs["wr"], gy)
             U.ufp4_gemm_grouped(qs["dr"], qs["wc"], gx)
             U.ufp4_gemm_grouped(qs["dc"], qs["xc"], gw)
-        mq = _ev_time(quant_all, flush, 5)
-        mq1 = _ev_time(quant_all_single, flush, 5)
-        mg = _ev_time(gemm_all, flush, 5)
+        mq = _ev_time(quant_all, flush)
+        mq1 = _ev_time(quant_all_single, flush)
+        mg = _ev_time(gemm_all, flush)
         elems = 2 * (tx.numel() + tw.numel() + tdy.numel())
         flops = 3 * 2.0 * T * F * H
         qg = elems * Q_BYTES_PER_ELEM / (mq * 1e-3) / 1e9
@@ -908,8 +989,8 @@ def all_workloads(U, torch, dev, pk, flush, with_oracle=True):
     d = moe124b_inputs(dev)
     T, H, F = WORKLOAD["tokens"], WORKLOAD["hidden"], WORKLOAD["ffn"]
     st = Step(U, d["x"], d["w"], d["dy"], U.UFP4_E2M1)
-    mq = _ev_time(st.quantize_all, flush, 3)
-    mg = _ev_time(st.gemms, flush, 3)
+    mq = _ev_time(st.quantize_all, flush)
+    mg = _ev_time(st.gemms, flush)
     qg = st.q_elems * Q_BYTES_PER_ELEM / (mq * 1e-3) / 1e9
     tf = sum(st.flops_each) / (mg * 1e-3) / 1e12
     e = {"quantize_ms": round(mq, 4), "quantize_gbs": round(qg, 1), "gemm_ms": round(mg, 4),
@@ -986,13 +1067,15 @@ def main():
     ap.add_argument("--kernel", default=None,
                     choices=["gemm_e2m1", "gemm_e1m2", "gemm_mxfp4", "quant_row_e1m2", "quant_col_e1m2", "quant_dual_e1m2",
                              "quant_dual_sr_e1m2", "amax_dual_e1m2",
-                             "quant_row_e2m1", "quant_col_e2m1", "quant_grouped_dual_e1m2"],
-                    help="time one kernel of the step in isolation (profiling)")
+                             "quant_row_e2m1", "quant_col_e2m1", "quant_grouped_dual_e1m2", "all"],
+                    help="time one kernel of the step in isolation (profiling); all: every public call once")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.kernel == "all":
+        run_all_kernels(args)
     elif args.kernel:
         run_kernel(args)
     else:
