@@ -632,9 +632,21 @@ __device__ __forceinline__ void quant_block_row(const Args &a, const Raw<In> &ra
 
 // Per element: deq = fl32(fl32(v e) S_dec), A = y (rotated input);
 // sums of deq*A, A*A, (A-deq)^2, (v - a) over a != 0, count.
+// Each thread keeps the five sums in fp32 with Kahan's compensation (W. Kahan,
+// "Further remarks on reducing truncation errors", CACM 8(1), 1965): the
+// error stays at a few fp32 ulps of the sum however many blocks a thread
+// adds, and the GB300's fp64 rate (a small fraction of fp32) is spent only
+// on the final cross-thread reduction.
 struct Acc {
-    double aq = 0, aa = 0, e2 = 0, bias = 0, cnt = 0;
+    float s[5] = {0, 0, 0, 0, 0};   // <deq, A>, <A, A>, ||A - deq||^2, bias sum, bias count
+    float c[5] = {0, 0, 0, 0, 0};   // compensations (the negated lost low parts)
 };
+__device__ __forceinline__ void kahan_add(float &s, float &c, float x) {
+    const float y = __fsub_rn(x, c);
+    const float t = __fadd_rn(s, y);
+    c = __fsub_rn(__fsub_rn(t, s), y);
+    s = t;
+}
 
 __device__ __forceinline__ void acc_block8(Acc &acc, const float y[8], uint32_t w, float e,
                                            float S_dec, int grid, float qmax) {
@@ -654,12 +666,18 @@ __device__ __forceinline__ void acc_block8(Acc &acc, const float y[8], uint32_t 
             if (g != 0.0f) { bias += v - g; cnt += 1.0f; }
         }
     }
-    acc.aq += aq; acc.aa += aa; acc.e2 += e2; acc.bias += bias; acc.cnt += cnt;
+    kahan_add(acc.s[0], acc.c[0], aq);
+    kahan_add(acc.s[1], acc.c[1], aa);
+    kahan_add(acc.s[2], acc.c[2], e2);
+    kahan_add(acc.s[3], acc.c[3], bias);
+    kahan_add(acc.s[4], acc.c[4], cnt);
 }
 
 __device__ void stats_reduce(Acc acc, double *out) {
     __shared__ double s[kThreads / 32][5];
-    double v[5] = {acc.aq, acc.aa, acc.e2, acc.bias, acc.cnt};
+    double v[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) v[i] = (double)acc.s[i] - (double)acc.c[i];
 #pragma unroll
     for (int i = 0; i < 5; ++i)
 #pragma unroll
