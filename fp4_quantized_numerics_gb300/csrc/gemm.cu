@@ -75,7 +75,7 @@ constexpr int kMX = 4;
 //  E1M2Pl: the same 8 MMAs per 64-byte stage, all four tiles (R_A, R_B,
 //        E_A, E_B) loaded by TMA into a 4-deep ring (the epilogue stages
 //        16-column halves through 2 KB per warp to make room); scale copies
-//        from their own warp as for E2M1.
+//        from their own warps as for E2M1.
 template <int GRID>
 struct Cfg {
     static constexpr bool kFour = GRID == kE1M2 || GRID == kE1M2Pl;  // E1M2: 4 MMAs per K step
@@ -98,7 +98,13 @@ struct Cfg {
     static constexpr int kESlots = GRID == kE1M2 ? 3 : 0;
     static constexpr int kExpWarps = GRID == kE1M2 ? 6 : 0;
     // E2M1 and E1M2Pl: one extra warp issues the block-scale copies
-    static constexpr int kScaleWarps = GRID == kE1M2 ? 0 : 1;
+    // Block-scale copies cost their issuing thread ~45 cycles each: E2M1 and
+    // MXFP4 need 12 per 512-cycle stage, more than one warp can issue, so two
+    // warps take alternate stages (E2M1 4.2 -> 4.8 PFLOP/s, MXFP4 3.3 -> 4.6
+    // at fwd_y of the MoE-124B layer); E1M2Pl, 6 per 1024 cycles, gains ~1 %
+    // from the second.  A third warp would cap the registers below what the
+    // epilogue holds.
+    static constexpr int kScaleWarps = GRID == kE1M2 ? 0 : 2;
     static constexpr int kThreads = 32 * (2 + kEpiWarps + kScaleWarps + kExpWarps);
     // epilogue staging buffers (32 rows x kEpiCols fp32) per epilogue warp
     static constexpr int kEpiBufs = GRID == kE1M2 ? 2 : 1;
@@ -332,6 +338,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
     const uint32_t drained = accf + 16u;
     auto sfr = [&](int s) { return accf + 24u + 8u * s; };
     const uint32_t sfd = accf + 24u + 8u * S;
+    constexpr uint32_t kSW = C::kScaleWarps > 0 ? C::kScaleWarps : 1;   // stage stride of a scale warp
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int ntiles;
@@ -351,7 +358,7 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         ptx::mbar_init(accf, 1);
         ptx::mbar_init(acce, kEpiWarps);   // one arrival per epilogue warp
         ptx::mbar_init(drained, 1);
-        ptx::mbar_init(sfd, 1);
+        ptx::mbar_init(sfd, C::kScaleWarps > 0 ? C::kScaleWarps : 1);   // one commit per scale warp
         *abort = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tma_a);
@@ -374,9 +381,9 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
     // Block-scale copies of stage s into its TMEM columns: SFA 4 columns per
     // K step at [0, 4 KS), SFB 8 columns per K step (rows 0-127, then
     // 128-255) at [4 KS, 12 KS).  E2M1, MXFP4 and E1M2 with loaded planes
-    // issue them from their own warp so that their issue overlaps the MMAs'
-    // (sfr(s) says they are issued); E1M2 with expanded planes issues them in
-    // line from the MMA thread.
+    // issue them from two warps of their own, alternate stages each, so that
+    // their issue overlaps the MMAs' (sfr(s) says they are issued); E1M2 with
+    // expanded planes issues them in line from the MMA thread.
     auto copy_scales = [&](uint32_t s, int atoms, bool signal) {
         const uint64_t hi_sf = ptx::sdesc(0, 0, 128, 0);   // 32 rows x 16 B scale atom
         const uint32_t st = smem_base + s * C::kStageBytes;
@@ -401,9 +408,8 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
     };
     // Every copy the scale thread issued must complete before TMEM is freed:
     // one commit tracks them all.
-    auto drain_scales = [&](uint32_t g) {
-        if (g == 0) return;
-        ptx::tc_commit(sfd);
+    auto drain_scales = [&]() {
+        ptx::tc_commit(sfd);   // (with nothing issued it arrives at once)
         const long long t0 = clock64();
         while (!ptx::mbar_try_wait(sfd, 0))
             if (clock64() - t0 > kWaitBudget) { raise_timeout(); break; }
@@ -728,17 +734,20 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
         }
         if (lane == 0) ptx::bulk_wait_all();
         __syncwarp();
-    } else if (GRID == kMX && warp == 2 + kEpiWarps) {
+    } else if (GRID == kMX && warp >= 2 + kEpiWarps && warp < 2 + kEpiWarps + C::kScaleWarps) {
         // ---------------------------------------- MXFP4 scale repack + copies
         // A staged scale word holds one row's four 16-block places of a K step,
         // (s0, s0, s1, s1) for its two 32-blocks; scale_vec::2X reads the K
         // step's two scales from bytes 0 and 1, so the whole warp rewrites
         // each word to (s0, s1, s1, s1) before lane 0 copies it to TMEM.
+        // The scale warps take alternate stages.
+        const uint32_t sw = (uint32_t)(warp - 2 - kEpiWarps);
         uint32_t g = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
             const TileInfo ti = tile_info<C::kKS>(p, tab, t);
             for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++g) {
+                if (g % kSW != sw) continue;
                 const uint32_t s = g % S, round = g / S;
                 ok = __all_sync(0xffffffffu, wait_or_abort(full(s), round & 1, abort, p.budget));
                 if (!ok) break;
@@ -767,21 +776,24 @@ __global__ void __launch_bounds__(Cfg<GRID>::kThreads, 1)
                 __syncwarp();
             }
         }
-        if (lane == 0) drain_scales(g);
-    } else if (C::kScaleWarps > 0 && warp == 2 + kEpiWarps) {
+        if (lane == 0) drain_scales();
+    } else if (C::kScaleWarps > 0 && warp >= 2 + kEpiWarps && warp < 2 + kEpiWarps + C::kScaleWarps) {
         // ------------------------------------------------- E2M1 scale copies
+        // (two warps, alternate stages)
+        const uint32_t sw = (uint32_t)(warp - 2 - kEpiWarps);
         if (lane == 0) {
             uint32_t g = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
                 const TileInfo ti = tile_info<C::kKS>(p, tab, t);
                 for (int kb = ti.kb0; kb < ti.kb1; ++kb, ++g) {
+                    if (g % kSW != sw) continue;
                     const uint32_t s = g % S, round = g / S;
                     if (!wait_or_abort(full(s), round & 1, abort, p.budget)) { ok = false; break; }
                     copy_scales(s, min(C::kKS, ti.nkt - C::kKS * kb), true);
                 }
             }
-            drain_scales(g);
+            drain_scales();
         }
     } else if constexpr (GRID == kE1M2) {
         // ------------------------------------------------- E1M2 expanders
