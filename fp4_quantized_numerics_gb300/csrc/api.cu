@@ -107,7 +107,7 @@ const char *ufp4_status_string(ufp4_status s) {
     switch (s) {
         case UFP4_OK: return "ok";
         case UFP4_ERR_INVALID: return "invalid argument";
-        case UFP4_ERR_UNSUPPORTED: return "unsupported by this build";
+        case UFP4_ERR_UNSUPPORTED: return "unsupported by this library";
         case UFP4_ERR_NONFINITE: return "non-finite input";
         case UFP4_ERR_CUDA: return "CUDA runtime error";
         case UFP4_ERR_TIMEOUT: return "device-side wait timed out";

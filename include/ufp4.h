@@ -26,7 +26,7 @@
  *     where a call is documented to synchronise (it returns host values).
  *   - Argument errors are found on the host before anything is launched and
  *     return UFP4_ERR_INVALID (or UFP4_ERR_UNSUPPORTED for a valid request
- *     this build does not implement); a failed launch returns UFP4_ERR_CUDA.
+ *     this library does not implement); a failed launch returns UFP4_ERR_CUDA.
  *     Faults inside an already-launched kernel surface through the CUDA
  *     runtime on a later synchronisation, as for any CUDA library.
  *   - Zero-sized tensors are a no-op returning UFP4_OK.
@@ -52,7 +52,7 @@ typedef struct CUstream_st *ufp4_stream_t; /* a cudaStream_t; NULL = legacy defa
 typedef enum {
     UFP4_OK = 0,
     UFP4_ERR_INVALID = 1,      /* bad pointer, size, alignment or enum */
-    UFP4_ERR_UNSUPPORTED = 2,  /* valid request not implemented by this build */
+    UFP4_ERR_UNSUPPORTED = 2,  /* valid request not implemented by this library */
     UFP4_ERR_NONFINITE = 3,    /* NaN/Inf input seen (reported by ufp4_check) */
     UFP4_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
     UFP4_ERR_TIMEOUT = 5       /* a bounded device-side wait gave up */
@@ -96,7 +96,7 @@ typedef enum { UFP4_BF16 = 0, UFP4_FP32 = 1 } ufp4_dtype;
 #define UFP4_BLOCK 16
 #define UFP4_MX_BLOCK 32
 
-/* Size limits of this build (32-bit block and tile indexing inside the
+/* Size limits of this library (32-bit block and tile indexing inside the
  * kernels).  A request beyond them returns UFP4_ERR_UNSUPPORTED before any
  * launch:
  *   quantize / stats / dequantize: rows, cols (k) < 2^31 and the quantized
