@@ -6,6 +6,8 @@ is checked against the oracle's per-segment quantization (bit-exact with RHT
 off, within the RHT tolerance with it on), and the three grouped GEMMs
 (fwd_y, bwd_dx, bwd_dw) against the oracle's fp64 per-expert products.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -253,3 +255,32 @@ def test_grouped_dual_nonfinite_flag(U):
     assert U.ufp4_check(ws) == U.UFP4_ERR_NONFINITE
     U.ufp4_quantize_grouped_dual(torch.ones(200, 64, dtype=torch.bfloat16, device="cuda"), 1, [100, 100], ws=ws)
     assert U.ufp4_check(ws) == U.UFP4_OK
+
+
+@pytest.mark.parametrize("case", ["fp32", "mixed_round", "mixed_rht"])
+def test_grouped_dual_two_call_route(U, case):
+    """Where one read cannot serve both orientations (FP32 input, different
+    rounding modes or transforms) the grouped dual call runs the two grouped
+    quantizations in turn: each result still equals its own call."""
+    counts = [37, 0, 130, 5]
+    g = np.random.default_rng(13)
+    x = inputs.to_bf16_f32(g.standard_normal((sum(counts), 96), dtype=np.float32))
+    dtype = torch.float32 if case == "fp32" else torch.bfloat16
+    t = torch.from_numpy(x).to(dtype).cuda()
+    n = len(counts)
+    rr, kc = U.grouped_rows(counts), U.grouped_kpad(counts)
+    dr, dc = _filled(U, rr, 96, 1, n), _filled(U, 96, kc, 1, n)
+    pr = U.qparams(1, True, 2, 0, 3, 0, False)
+    pc = U.qparams(1, case != "mixed_rht", 2, 1 if case == "mixed_round" else 0, 3, 0, True)
+    qr, qc = dr.c(), dc.c()
+    ws = U.workspace()
+    st = U.lib().ufp4_quantize_grouped_dual(t.data_ptr(), U._dtype_code(t), 96, t.stride(0), U._i64_array(counts), n,
+                                            ctypes.byref(pr), ctypes.byref(pc), ctypes.byref(qr), ctypes.byref(qc),
+                                            ws.data_ptr(), ws.numel(), U._stream(None))
+    assert st == U.UFP4_OK
+    sr, sc = _filled(U, rr, 96, 1, n), _filled(U, 96, kc, 1, n)
+    U.ufp4_quantize_grouped(t, 1, counts, rht=True, rht_seed=2, sr_seed=3, out=sr)
+    U.ufp4_quantize_grouped(t, 1, counts, rht=case != "mixed_rht", rht_seed=2,
+                            round=1 if case == "mixed_round" else 0, sr_seed=3, colwise=True, out=sc)
+    _same(dr, sr)
+    _same(dc, sc)
