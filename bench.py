@@ -209,9 +209,29 @@ class Step:
         # two orientations then differ and are quantized one pass each
         self.policy = policy
         self.dual = dual and policy == "ufp4"
-        self.launches_per_step = (3 if self.dual else 6) * 2 + 3
+        self.launches_per_step = self.count_launches(x.device) + 3
         self.q_elems = 2 * (x.numel() + w.numel() + dy.numel())
         self.flops_each = [2 * T * F * H, 2 * T * H * F, 2 * F * H * T]
+
+    def count_launches(self, dev):
+        """Kernels the quantize phase launches, by the library's routing: a
+        dual-orientation BF16 call whose tensor fits on chip (at most 14
+        128 x 64 tiles per SM) is one cooperative launch that takes its own
+        maxima; any other quantization is an amax pass and a quantize pass."""
+        import torch
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        n = 0
+        for t in (self.x, self.w, self.dy):
+            if self.grid == self.U.UFP4_MXFP4:   # no tensor amax: one pass per orientation
+                n += 2
+                continue
+            rows, cols = t.shape
+            tiles = -(-rows // 128) * -(-cols // 64)
+            if self.dual and t.dtype == torch.bfloat16 and -(-tiles // min(sms, tiles)) <= 14:
+                n += 1
+            else:
+                n += 2 * (1 if self.dual else 2)
+        return n
 
     def quantize_all(self):
         U, g = self.U, self.grid
@@ -349,7 +369,7 @@ def run_gpu(args):
             "quantize": {"gbs": round(q_gbs, 1), "frac_hbm": round(q_gbs / ws_n / pk["hbm_gbs"], 4),
                          "ms_per_step": round(tq / args.steps, 4),
                          "elements_per_step": step_elems(WORKLOAD),
-                         "launches_per_step": 6},
+                         "launches_per_step": step.launches_per_step - 3},
             "gemm": {"tflops": round(gemm_tflops, 1), "ms_per_step": round(tg / args.steps, 4),
                      "ms_each": [round(v, 4) for v in gemm_each],
                      "frac_fp8_peak_sustained": round(per_gpu_tflops / fp8_sus, 4),
@@ -364,7 +384,7 @@ def run_gpu(args):
                          "traffic": traffic_for("k_gemm_e1m2_moe124b"),
                          "peak_kind": "dense FP8 = %s sustained bf16 x 2 (timed inside a seconds-long loop of "
                                       "steps)" % pk["source"]},
-            "gpu_launches": 9 * args.steps,
+            "gpu_launches": step.launches_per_step * args.steps,
             "clocks": clocks,
             "peaks": pk,
         }
