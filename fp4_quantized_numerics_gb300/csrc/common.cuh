@@ -141,7 +141,10 @@ __device__ __forceinline__ uint32_t sr_code(float q, uint32_t r, uint32_t top = 
     if (GRID == kE1M2) {
         const float t = fminf(fabsf(q) * 33554432.0f, (float)(top << 24));   // 2|q| 2^24, at most top 2^24
         const uint32_t T = __float2uint_ru(t);
-        return sgn | ((T >> 24) + (r < (T << 8) ? 1u : 0u));
+        // the same decision as an addition: with P = T mod 2^24 and R = r >> 8,
+        // T + (2^24 - 1 - R) carries into bit 24 iff R < P, and 2^24 - 1 - R
+        // is (~r) >> 8 (T < 2^27, so nothing overflows)
+        return sgn | ((T + (~r >> 8)) >> 24);
     } else {
         const float a = fabsf(q);
         if (!(a < 6.0f)) return sgn | 7u;   // also NaN (non-finite input)

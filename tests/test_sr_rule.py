@@ -6,9 +6,11 @@ The kernels take the same decision in fixed point: with t = a scaled so
 that the neighbours are consecutive integers, T = ceil(t * 2^24) holds the
 lower neighbour's index in its top bits and ceil(p * 2^24) in its low 24,
 and the decision is r < (T << 8) mod 2^32 (one rounding-up conversion per
-code).  This test restates that rule and compares it with the oracle's
-float decision for random magnitudes, grid points, the clamp, and for every
-r next to each threshold.
+code); the E1M2 kernels take it as the carry of an addition, the index
+(T + ((~r) >> 8)) >> 24.  This test restates those rules, checks that the
+two E1M2 forms agree, and compares them with the oracle's float decision for
+random magnitudes, grid points, the clamp, and for every r next to each
+threshold.
 """
 import math
 
@@ -25,7 +27,10 @@ def fixed_point_code(grid, a, r):
     if grid == 1:   # E1M2: neighbours 0.5 apart
         t = min(F32(a * F32(2.0 ** 25)), F32(7 << 24))
         T = int(math.ceil(float(t)))
-        return (T >> 24) + (1 if r < ((T << 8) & 0xFFFFFFFF) else 0)
+        compare = (T >> 24) + (1 if r < ((T << 8) & 0xFFFFFFFF) else 0)
+        carry = ((T + ((~r & 0xFFFFFFFF) >> 8)) & 0xFFFFFFFF) >> 24
+        assert carry == compare, (float(a), r)
+        return carry
     if not a < F32(6.0):
         return 7
     mul = F32(2.0 ** 25) if a < 2 else (F32(2.0 ** 24) if a < 4 else F32(2.0 ** 23))
