@@ -142,9 +142,9 @@ __device__ __forceinline__ uint32_t sr_code(float q, uint32_t r, uint32_t top = 
         const float t = fminf(fabsf(q) * 33554432.0f, (float)(top << 24));   // 2|q| 2^24, at most top 2^24
         const uint32_t T = __float2uint_ru(t);
         // the same decision as an addition: with P = T mod 2^24 and R = r >> 8,
-        // T + (2^24 - 1 - R) carries into bit 24 iff R < P, and 2^24 - 1 - R
-        // is (~r) >> 8 (T < 2^27, so nothing overflows)
-        return sgn | ((T + (~r >> 8)) >> 24);
+        // T + (2^24 - 1 - R) carries into bit 24 iff R < P (one three-input
+        // add; T < 2^27, so nothing overflows)
+        return sgn | ((T + 0xFFFFFFu - (r >> 8)) >> 24);
     } else {
         const float a = fabsf(q);
         if (!(a < 6.0f)) return sgn | 7u;   // also NaN (non-finite input)
@@ -155,6 +155,14 @@ __device__ __forceinline__ uint32_t sr_code(float q, uint32_t r, uint32_t top = 
         const uint32_t base = a < 2.0f ? ip : (a < 4.0f ? ip + 2u : 6u);   // E2M1 index of the lower neighbour
         return sgn | (base + (r < (T << 8) ? 1u : 0u));
     }
+}
+
+// sr_code<kE1M2> of q given as qs = q 2^25 (the caller's packed multiply;
+// exact: a power-of-two factor, and an overflow to inf clamps the same).
+__device__ __forceinline__ uint32_t sr_code_e1m2_scaled(float qs, uint32_t r, uint32_t top) {
+    const uint32_t sgn = (__float_as_uint(qs) >> 28) & 8u;
+    const uint32_t T = __float2uint_ru(fminf(fabsf(qs), (float)(top << 24)));
+    return sgn | ((T + 0xFFFFFFu - (r >> 8)) >> 24);
 }
 
 // Grid value of a magnitude index.

@@ -221,6 +221,31 @@ __device__ __forceinline__ float inline_k(uint32_t e, float S_enc, bool rht) {
     return rht ? kk * 0.25f : kk;
 }
 
+// Packed fp32 pairs (f32x2): two values per register pair and instruction.
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 // Codes of 8 values q (already multiplied by k) as 8 nibbles, element j in
 // bits 4j..4j+3.  `i0` is the logical output index of element 0 (multiple of
 // 8) for stochastic rounding.
@@ -238,16 +263,26 @@ __device__ __forceinline__ uint32_t codes8(const float q[8], const Args &a, uint
     } else {
         const uint2 key = make_uint2((uint32_t)a.sr_seed, (uint32_t)(a.sr_seed >> 32));
         const uint64_t c0 = i0 >> 2;
+        float qs[8];
+        if (GRID == kE1M2) {
+            // the decision's 2^25 scaling, two values per packed multiply
+            const uint64_t S25 = pk2(33554432.0f, 33554432.0f);
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) upk2(mul2(pk2(q[j], q[j + 1]), S25), qs[j], qs[j + 1]);
+        }
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             const uint64_t c = c0 + t;
             const uint4 r = philox4x32_10(
                 make_uint4((uint32_t)c, (uint32_t)(c >> 32), (uint32_t)a.sr_counter,
                            (uint32_t)(a.sr_counter >> 32)), key);
-            w |= sr_code<GRID>(q[4 * t + 0], r.x, a.utop) << (16 * t + 0);
-            w |= sr_code<GRID>(q[4 * t + 1], r.y, a.utop) << (16 * t + 4);
-            w |= sr_code<GRID>(q[4 * t + 2], r.z, a.utop) << (16 * t + 8);
-            w |= sr_code<GRID>(q[4 * t + 3], r.w, a.utop) << (16 * t + 12);
+            const uint32_t rr[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t code = GRID == kE1M2 ? sr_code_e1m2_scaled(qs[4 * t + j], rr[j], a.utop)
+                                                    : sr_code<GRID>(q[4 * t + j], rr[j], a.utop);
+                w |= code << (16 * t + 4 * j);
+            }
         }
     }
     return w;
@@ -272,30 +307,6 @@ __device__ __forceinline__ void zero_pad_rows(const Args &a) {
 // on both halves at once with add/sub.rn.f32x2, the bit-3 stage pairs the
 // halves.  Blocks are enumerated row-major over (row, block-in-row) with a
 // fast 32-bit divider; each thread keeps two blocks in flight.
-
-__device__ __forceinline__ uint64_t pk2(float a, float b) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ void upk2(uint64_t r, float &a, float &b) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
-}
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
 
 // max(a, b, c) in one instruction (PTX three-input max; NaN as fmaxf).
 __device__ __forceinline__ float max3f(float a, float b, float c) {
