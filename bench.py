@@ -31,8 +31,9 @@ is written and then read back, so the timed kernels start with an L2 that
 holds none of their data and no dirty lines whose write-back would compete
 with their reads.
 
---impl reference runs the CPU oracle (the reference arm of this tier) on a
-bounded sample of the same workload and prints the same line shape.
+--impl reference runs the CPU oracle (the paper released no code, so the
+oracle is the reference arm) on a bounded sample of the same workload and
+prints the same line shape.
 """
 import argparse
 import hashlib
