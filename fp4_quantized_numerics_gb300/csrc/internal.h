@@ -10,7 +10,10 @@ namespace ufp4 {
 // Workspace layout (bytes from the start of the caller's scratch buffer).
 constexpr size_t kWsStatus = 0;            // uint32 status word
 constexpr size_t kWsArrive = 8;            // uint32 grid-barrier counter of the single-pass quantizer
+constexpr size_t kWsTileNext = 16;         // uint32 tile counters of a batched dual quantization, one per tensor
+constexpr int kMaxDualBatch = 32;
 constexpr size_t kWsPartials = 256;        // float partial maxima
+static_assert(kWsTileNext + kMaxDualBatch * sizeof(uint32_t) <= kWsPartials, "tile counters end before the partials");
 constexpr int kMaxPartials = 4096;
 constexpr size_t kWsStats = 32768;         // double partial sums, 8 per CTA
 constexpr int kMaxStatsCtas = 1024;
@@ -29,6 +32,7 @@ struct QuantLaunch {
     float *tensor_scale;
     int64_t out_rows, k;       // result shape
     uint64_t elem_base;        // SR element offset (grouped segments)
+    int status_or = 0;         // 1: only raise the workspace's status flag, never clear it
 };
 
 int num_sms();
@@ -102,6 +106,14 @@ bool make_input_tile_map(void *tmap, const void *x, int64_t rows, int64_t cols, 
 // over x (falls back to two passes when the parameters or the layout do not
 // allow it).
 cudaError_t launch_quantize_dual(const QuantLaunch &qr, const QuantLaunch &qc, void *ws, cudaStream_t s);
+
+// Both orientations of n tensors, in order, each result equal to its own
+// launch_quantize_dual.  The workspace's status flag is cleared once and
+// raised by any tensor's non-finite maximum.  Where tensor j and tensor
+// j + 1 both take the tile route and j + 1 has the transform on and needs
+// its maxima, j + 1's amax pass runs inside j's quantization launch.
+cudaError_t launch_quantize_dual_batch(const QuantLaunch *qr, const QuantLaunch *qc, int n, void *ws,
+                                       cudaStream_t s);
 
 // Grouped quantization: x holds segments in row order; ws keeps one fp32
 // maximum per segment and the status word.

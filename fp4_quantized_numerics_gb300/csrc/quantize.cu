@@ -57,6 +57,7 @@ struct Args {
     float *partials_out;
     int n_partials;
     uint32_t *status;
+    uint32_t status_or;         // 1: the pass only raises the status flag (batched calls)
     uint8_t *codes, *scales;
     uint8_t *eplane;            // E1M2 correction plane beside the codes, or null
     float *tensor_scale;
@@ -169,7 +170,7 @@ __device__ __forceinline__ void tensor_scale_prologue(const Args &a, float qmax,
     if (fold) kfold *= 0.00390625f;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         if (a.tensor_scale) *a.tensor_scale = sd;
-        if (a.status) *a.status = (isfinite(A_t) ? 0u : 1u);
+        if (a.status && (!a.status_or || !isfinite(A_t))) *a.status = (isfinite(A_t) ? 0u : 1u);
     }
     for (int c = threadIdx.x; c < 256; c += blockDim.x) {
         const float d = e4m3_to_f32((uint32_t)c);
@@ -1396,11 +1397,12 @@ __device__ __forceinline__ void mma_bf16(const uint32_t (&a)[4], uint32_t b0, ui
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
+// The amax pass over chunks cta, cta + ncta, ... of x, staged in `dsm`
+// (kMmaSmem bytes); writes this CTA's partial maxima to partials_out[cta].
 template <bool ROW, bool COL>
-__global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_amax_mma(Args ar, Args ac, uint32_t ncc,
-                                                                      uint32_t nchunks) {
-    extern __shared__ __align__(128) uint8_t dsm[];
-    __shared__ float s_red[kThreads / 32], s_red2[kThreads / 32];
+__device__ __forceinline__ void amax_mma_run(const Args &ar, const Args &ac, uint32_t ncc, uint32_t nchunks,
+                                             uint32_t cta, uint32_t ncta, uint8_t *dsm, float *s_red,
+                                             float *s_red2) {
     const Args &a = ROW ? ar : ac;   // the input as stored (both describe the same x)
     const uint32_t buf = ptx::smem_u32(dsm);
     const uint32_t bars = buf + kMmaRing * kMmaStage;
@@ -1417,7 +1419,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_amax_mma(Args ar, 
     // each; thread 0 also posts the chunk's byte count (the barrier's phase
     // needs that single arrival, so copies may land before or after it).
     auto issue = [&](uint32_t jj) {
-        const uint32_t i = blockIdx.x + jj * gridDim.x;
+        const uint32_t i = cta + jj * ncta;
         if (i >= nchunks) return;
         const uint32_t kb = i / ncc, cc = i - kb * ncc;
         const uint32_t c0 = cc * kMmaCW, r0 = kb * 16;
@@ -1450,7 +1452,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_amax_mma(Args ar, 
         if (hi_ok) m = max_nan(max_nan(m, max_nan(fabsf(d[2]), fabsf(d[3]))), max_nan(fabsf(e[2]), fabsf(e[3])));
     };
     auto process = [&](uint32_t jj) {
-        const uint32_t i = blockIdx.x + jj * gridDim.x;
+        const uint32_t i = cta + jj * ncta;
         const uint32_t kb = i / ncc, cc = i - kb * ncc;
         const uint32_t c0 = cc * kMmaCW, r0 = kb * 16;
         const uint32_t ncols = min(kMmaCW, cols - c0), nrows = min(16u, rows - r0);
@@ -1488,8 +1490,8 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_amax_mma(Args ar, 
         }
     };
     bool ok = true;
-    while (j < nchunks && blockIdx.x + j * gridDim.x < nchunks) {
-        const uint32_t nj = (blockIdx.x + (j + 1) * gridDim.x < nchunks) ? 2u : 1u;
+    while (j < nchunks && cta + j * ncta < nchunks) {
+        const uint32_t nj = (cta + (j + 1) * ncta < nchunks) ? 2u : 1u;
         bool mine = true;
         for (uint32_t t = 0; t < nj && mine; ++t)
             mine = ptx::mbar_wait_bounded(bars + 8u * ((j + t) % kMmaRing), ((j + t) / kMmaRing) & 1u, kRingWait);
@@ -1518,9 +1520,17 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_amax_mma(Args ar, 
     __syncthreads();
     if (threadIdx.x == 0) {
         for (int w = 1; w < kThreads / 32; ++w) { mr = max_nan(mr, s_red[w]); mc = max_nan(mc, s_red2[w]); }
-        if (ROW) ar.partials_out[blockIdx.x] = mr * 0.25f;
-        if (COL) ac.partials_out[blockIdx.x] = mc * 0.25f;
+        if (ROW) ar.partials_out[cta] = mr * 0.25f;
+        if (COL) ac.partials_out[cta] = mc * 0.25f;
     }
+}
+
+template <bool ROW, bool COL>
+__global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_amax_mma(Args ar, Args ac, uint32_t ncc,
+                                                                      uint32_t nchunks) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ float s_red[kThreads / 32], s_red2[kThreads / 32];
+    amax_mma_run<ROW, COL>(ar, ac, ncc, nchunks, blockIdx.x, gridDim.x, dsm, s_red, s_red2);
 }
 
 // ================================================ dual orientation (X and X^T)
@@ -1813,53 +1823,92 @@ __device__ __forceinline__ void dual_padding(const Args &ar, const Args &ac, con
     zero_pad_rows(ac);   // column-wise padding blocks come from zero-filled tile rows
 }
 
-template <int GRID, int ROUND, bool RHT>
-__global__ void __launch_bounds__(kThreads, kStagedMinCtas)
-    k_dual_tile(const __grid_constant__ CUtensorMap tmx, Args ar, Args ac, uint32_t nct, uint32_t ntiles) {
-    constexpr int kRing = ring_depth<false>();
-    extern __shared__ __align__(128) uint8_t dsm[];
-    __shared__ float s_kr[256], s_kc[256];
-    __shared__ float s_red[kThreads / 32];
-    const RingCtl ring = ring_init<kRing>(dsm);
-    uint8_t *stage_codes = dsm + kRing * kChunk + 64;            // [rb][cl] uint2
-    uint8_t *stage_scales = stage_codes + 8 * kTileCols * 8;    // [rb][cl] byte
-    uint32_t issued = 0, j = 0;
-    auto issue = [&](uint32_t jj) {
-        const uint32_t i = blockIdx.x + jj * gridDim.x;
-        if (i >= ntiles) return;
-        const uint32_t rt = i / nct, ct = i - rt * nct;
-        const uint32_t bar = ring.bars + 8u * (jj % kRing);
-        ptx::mbar_arrive_expect_tx(bar, kTileBytes);   // out-of-range elements arrive as zeros
-        ptx::tma_load_2d(ring.buf + (jj % kRing) * kChunk, &tmx, (int32_t)(ct * kTileCols),
-                         (int32_t)(rt * kTileRows), bar);
-        issued = jj + 1;
-    };
-    if (threadIdx.x == 0) {
-        ptx::prefetch_tmap(&tmx);
-        for (uint32_t t = 0; t < kRing; ++t) issue(t);
+// Where the tiles of a dual tile loop come from: a fixed stride (tiles
+// first, first + stride, ... below n), or one at a time from a counter in
+// global memory that several CTAs share (a CTA that joins late takes what is
+// left).  kNoTile once the tiles are exhausted; a claim never returns a tile
+// after returning kNoTile.
+constexpr uint32_t kNoTile = 0xFFFFFFFFu;
+struct StrideTiles {
+    uint32_t first, stride, n;
+    __device__ __forceinline__ uint32_t claim(uint32_t jj) const {
+        const uint64_t i = first + (uint64_t)jj * stride;
+        return i < n ? (uint32_t)i : kNoTile;
     }
+};
+struct SharedTiles {
+    uint32_t *next, n;
+    __device__ __forceinline__ uint32_t claim(uint32_t) const {
+        const uint32_t i = atomicAdd(next, 1u);
+        return i < n ? i : kNoTile;
+    }
+};
+
+// The quantization loop of the dual tile kernels: tiles from `src` through
+// a 3-deep TMA ring in dsm (kTileSmem bytes).  Thread 0 claims each ring
+// slot's tile as it refills the slot and records it in the ring's control
+// area before arriving on the slot's barrier, so every thread reads the
+// same tile (or kNoTile, with no copy in flight) after its wait.  The
+// tensor scales and multiplier tables are computed by dual_tile_scales while
+// the first copies are in flight.
+template <int GRID, int ROUND, bool RHT>
+__device__ __forceinline__ void dual_tile_scales(const Args &ar, const Args &ac, float *s_kr, float *s_kc,
+                                                 float *s_red, float &Sr, float &Sc, bool &fr, bool &fc) {
     const float qmax = GRID == kE2M1 ? 6.0f : ar.uqmax;
-    float Sr = 1.0f, Sc = 1.0f;
-    bool fr = false, fc = false;
     float amr = 0.0f, amc = 0.0f;
     tensor_scale_prologue(ar, qmax, RHT ? 0.25f : 1.0f, s_kr, s_red, Sr, GRID == kE1M2 && ROUND == kRTNE, &fr, &amr);
     tensor_scale_prologue(ac, qmax, RHT ? 0.25f : 1.0f, s_kc, s_red, Sc, GRID == kE1M2 && ROUND == kRTNE, &fc, &amc);
     if (blockIdx.x == 0 && threadIdx.x == 0 && ar.status && !isfinite(amc)) *ar.status = 1u;
+}
+
+template <int GRID, int ROUND, bool RHT, class Src>
+__device__ __forceinline__ void dual_tile_loop(const CUtensorMap *tmx, const Args &ar, const Args &ac, uint32_t nct,
+                                               const Src &src, uint8_t *dsm, float *s_kr, float *s_kc,
+                                               float *s_red) {
+    constexpr int kRing = ring_depth<false>();
+    const RingCtl ring = ring_init<kRing>(dsm);
+    volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(dsm + kRing * kChunk + 32);
+    static_assert(kRing * 8 <= 32 && 32 + kRing * 4 <= 60, "slot tiles fit the ring's control area");
+    uint8_t *stage_codes = dsm + kRing * kChunk + 64;            // [rb][cl] uint2
+    uint8_t *stage_scales = stage_codes + 8 * kTileCols * 8;    // [rb][cl] byte
+    uint32_t issued = 0;
+    auto issue = [&](uint32_t jj) {
+        const uint32_t i = src.claim(jj);
+        const uint32_t bar = ring.bars + 8u * (jj % kRing);
+        slot[jj % kRing] = i;
+        if (i == kNoTile) {
+            ptx::mbar_arrive(bar);   // completes the phase: "no more tiles"
+            return;
+        }
+        const uint32_t rt = i / nct, ct = i - rt * nct;
+        ptx::mbar_arrive_expect_tx(bar, kTileBytes);   // out-of-range elements arrive as zeros
+        ptx::tma_load_2d(ring.buf + (jj % kRing) * kChunk, tmx, (int32_t)(ct * kTileCols),
+                         (int32_t)(rt * kTileRows), bar);
+        issued = jj + 1;
+    };
+    if (threadIdx.x == 0) {
+        ptx::prefetch_tmap(tmx);
+        for (uint32_t t = 0; t < kRing; ++t) issue(t);
+    }
+    float Sr = 1.0f, Sc = 1.0f;
+    bool fr = false, fc = false;
+    dual_tile_scales<GRID, ROUND, RHT>(ar, ac, s_kr, s_kc, s_red, Sr, Sc, fr, fc);
     const uint32_t smask = RHT ? rht_sign_mask(ar.rht_seed) : 0u;
     const Signs sgr = row_signs<__nv_bfloat16>(smask), sgc = col_signs<__nv_bfloat16>(smask);
-    const uint32_t nloc = ntiles > blockIdx.x ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     const DualGeom g = dual_geom(ar, ac);
     bool ok = true;
-    for (; j < nloc; ++j) {
+    uint32_t j = 0;
+    for (;; ++j) {
         // each thread waits for the tile itself; no CTA barrier before the work
         const bool mine = ring_wait_own<kRing>(ring, j);
-        const uint32_t i = blockIdx.x + j * gridDim.x;
+        const uint32_t i = slot[j % kRing];
         const uint32_t rt = i / nct, ct = i - rt * nct;
-        if (mine)
+        if (mine && i != kNoTile)
             dual_tile_quant<GRID, ROUND, RHT, true>(ar, ac, g, ring.buf + (j % kRing) * kChunk, rt, ct, sgr, sgc, Sr,
                                                     Sc, s_kr, s_kc, fr, fc, stage_codes, stage_scales);
         __syncthreads();   // tile consumed; column-wise results staged
         if (*ring.abort) { ok = false; break; }
+        if (i == kNoTile) break;   // (no abort: every thread read the same slot)
         if (threadIdx.x == 0) issue(j + kRing);
         dual_tile_flush(ac, g, rt, ct, stage_codes, stage_scales);
         __syncthreads();   // staging buffers free for the next tile
@@ -1868,8 +1917,46 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas)
         if (threadIdx.x == 0) atomicOr(&g_quant_timeout, 1u);
         ring_drain<kRing>(ring, j, issued);
     }
-    dual_padding(ar, ac, g);
 }
+
+template <int GRID, int ROUND, bool RHT>
+__global__ void __launch_bounds__(kThreads, kStagedMinCtas)
+    k_dual_tile(const __grid_constant__ CUtensorMap tmx, Args ar, Args ac, uint32_t nct, uint32_t ntiles) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ float s_kr[256], s_kc[256];
+    __shared__ float s_red[kThreads / 32];
+    dual_tile_loop<GRID, ROUND, RHT>(&tmx, ar, ac, nct, StrideTiles{blockIdx.x, gridDim.x, ntiles}, dsm, s_kr, s_kc,
+                                     s_red);
+    dual_padding(ar, ac, dual_geom(ar, ac));
+}
+
+// The quantization pass of one tensor (as k_dual_tile) with the tensor-amax
+// pass of the next one (as k_amax_mma<true, true>, both orientations of
+// x_next) in the same launch, so that the amax pass, which streams at HBM
+// speed with little arithmetic, runs beside a quantization pass that is
+// bound by instruction issue.  CTAs 0 .. namax-1 first take the amax chunks
+// (a fixed stride over namax CTAs; partial maxima in br / bc.partials_out
+// [0, namax)); then they, and from the start every other CTA, claim the
+// quantization tiles from the shared counter `next_tile` (zero before the
+// launch).  The amax ring and the tile ring share dynamic shared memory: the
+// amax run has consumed every copy it started when it returns.  Every
+// result equals that of the two separate launches.
+template <int GRID, int ROUND, bool RHT>
+__global__ void __launch_bounds__(kThreads, kStagedMinCtas)
+    k_dual_tile_amax(const __grid_constant__ CUtensorMap tmx, Args ar, Args ac, uint32_t nct, uint32_t ntiles,
+                     Args br, Args bc, uint32_t ncc, uint32_t nch, uint32_t namax, uint32_t *next_tile) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ float s_kr[256], s_kc[256];
+    __shared__ float s_red[kThreads / 32], s_red2[kThreads / 32];
+    if (blockIdx.x < namax) {
+        amax_mma_run<true, true>(br, bc, ncc, nch, blockIdx.x, namax, dsm, s_red, s_red2);
+        ptx::fence_proxy_async();   // the amax stages' bytes are reused by the tile ring's copies
+        __syncthreads();
+    }
+    dual_tile_loop<GRID, ROUND, RHT>(&tmx, ar, ac, nct, SharedTiles{next_tile, ntiles}, dsm, s_kr, s_kc, s_red);
+    dual_padding(ar, ac, dual_geom(ar, ac));
+}
+constexpr uint32_t kTileAmaxSmem = kTileSmem > kMmaSmem ? kTileSmem : kMmaSmem;
 
 // ======================================== on-chip single pass (dual, BF16)
 // For a tensor that fits in the GPU's shared memory (up to kResidentMax
@@ -2888,18 +2975,22 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t *codes, cons
 // ================================================================ dispatch
 // Launch of a staged kernel: opt in to the ring's dynamic shared memory once
 // per kernel, persistent grid of the CTAs that fit at once.
-template <class K, class... P>
-cudaError_t launch_staged_smem(K kern, size_t smem, int64_t work_ctas, int *grid_out, cudaStream_t s, P... args) {
+template <class K>
+cudaError_t opt_in_smem(K kern, size_t smem) {
     static std::mutex mu;
     static std::vector<const void *> done;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (std::find(done.begin(), done.end(), (const void *)kern) == done.end()) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-            done.push_back((const void *)kern);
-        }
+    std::lock_guard<std::mutex> lock(mu);
+    if (std::find(done.begin(), done.end(), (const void *)kern) == done.end()) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        done.push_back((const void *)kern);
     }
+    return cudaSuccess;
+}
+template <class K, class... P>
+cudaError_t launch_staged_smem(K kern, size_t smem, int64_t work_ctas, int *grid_out, cudaStream_t s, P... args) {
+    cudaError_t e = opt_in_smem(kern, smem);
+    if (e != cudaSuccess) return e;
     const int g = resident_grid(kern, work_ctas, smem);
     if (grid_out) *grid_out = g;
     kern<<<g, kThreads, smem, s>>>(args...);
@@ -3042,6 +3133,93 @@ cudaError_t launch_resident(K kern, uint32_t grid, uint32_t *arrive, cudaStream_
 // Both orientations of one tensor from one read per pass (k_dual_staged).
 // The row-wise and column-wise partial maxima take the two halves of the
 // workspace's partial area.
+// Partial-maximum areas of the workspace: area 0 at kWsPartials, area 1 at
+// kWsStats (statistics partial sums live there only within a statistics
+// call).  Each holds the row-wise partials in its first half and the
+// column-wise ones in its second.
+float *partial_area(void *ws, int area) {
+    return reinterpret_cast<float *>(static_cast<char *>(ws) + (area ? kWsStats : kWsPartials));
+}
+static_assert(kWsStats + kMaxPartials * sizeof(float) <= kWorkspaceBytes, "area 1 fits the workspace");
+static_assert(kWsPartials + kMaxPartials * sizeof(float) <= kWsStats, "area 0 ends before area 1");
+
+// Both orientations' tensor-amax pass of a BF16 tensor on the tile route,
+// into `area`; points ar / ac at the partials.  The pass streams with little
+// arithmetic: 16-row x 1 KB chunks (contiguous kilobyte rows) read faster
+// than 128-byte tile rows, and the maxima do not depend on the traversal.
+cudaError_t dual_amax_pass(const QuantLaunch &qr, Args &ar, Args &ac, float *area, cudaStream_t s) {
+    constexpr uint32_t CW = kChunk / 32;
+    static_assert(CW == kMmaCW, "the tensor-core amax uses the same chunking");
+    const uint32_t ncc = (uint32_t)((ar.cols + CW - 1) / CW), nch = (uint32_t)(ar.rows / 16) * ncc;
+    ar.partials_out = area;
+    ac.partials_out = area + kMaxPartials / 2;
+    int g = 1;
+    cudaError_t e;
+    if (qr.rht) {
+        auto kern = k_amax_mma<true, true>;
+        if (resident_grid(kern, nch, kMmaSmem) > kMaxPartials / 2) return cudaErrorInvalidValue;
+        e = launch_staged_smem(kern, kMmaSmem, nch, &g, s, ar, ac, ncc, nch);
+    } else {
+        auto kern = k_dual_staged<__nv_bfloat16, 0, 0, false, true>;
+        if (resident_grid(kern, nch, ring_smem<true>()) > kMaxPartials / 2) return cudaErrorInvalidValue;
+        e = launch_staged<true>(kern, nch, &g, s, ar, ac, ncc, nch);
+    }
+    if (e != cudaSuccess) return e;
+    ar.partials = ar.partials_out;
+    ac.partials = ac.partials_out;
+    ar.n_partials = ac.n_partials = g;
+    return cudaSuccess;
+}
+
+// The quantization pass of the tile route (k_dual_tile).
+cudaError_t dual_tile_pass(const QuantLaunch &qr, const CUtensorMap &tm, uint32_t nct, uint32_t ntiles,
+                           const Args &ar, const Args &ac, cudaStream_t s) {
+    const int kgrid = qr.grid == kE2M1 ? kE2M1 : kE1M2;   // clamped E2M1 runs the uniform-grid kernels
+#define UFP4_T(GRID, ROUND, RHT)                                                                          \
+    if (kgrid == GRID && qr.round == ROUND && (qr.rht != 0) == RHT)                                       \
+        return launch_staged_smem(k_dual_tile<GRID, ROUND, RHT>, kTileSmem, ntiles, nullptr, s, tm, ar, ac, nct, \
+                                  ntiles);
+    UFP4_T(kE2M1, kRTNE, false) UFP4_T(kE2M1, kRTNE, true)
+    UFP4_T(kE2M1, kSR, false)   UFP4_T(kE2M1, kSR, true)
+    UFP4_T(kE1M2, kRTNE, false) UFP4_T(kE1M2, kRTNE, true)
+    UFP4_T(kE1M2, kSR, false)   UFP4_T(kE1M2, kSR, true)
+#undef UFP4_T
+    return cudaErrorInvalidValue;
+}
+
+// The quantization pass of the tile route with the transform-on amax pass
+// of the next tensor (br / bc, partials into area_b) in the same launch
+// (k_dual_tile_amax); next_tile: a zeroed counter in device memory.  One
+// amax CTA per SM; the grid is the resident one.
+cudaError_t dual_tile_amax_pass(const QuantLaunch &qr, const CUtensorMap &tm, uint32_t nct, uint32_t ntiles,
+                                const Args &ar, const Args &ac, Args &br, Args &bc, float *area_b,
+                                uint32_t *next_tile, cudaStream_t s) {
+    const uint32_t ncc = (uint32_t)((br.cols + kMmaCW - 1) / kMmaCW), nch = (uint32_t)(br.rows / 16) * ncc;
+    br.partials_out = area_b;
+    bc.partials_out = area_b + kMaxPartials / 2;
+    const uint32_t want = (uint32_t)std::max<int64_t>(1, std::min<int64_t>(num_sms(), nch));
+    const int kgrid = qr.grid == kE2M1 ? kE2M1 : kE1M2;
+#define UFP4_TA(GRID, ROUND, RHT)                                                                         \
+    if (kgrid == GRID && qr.round == ROUND && (qr.rht != 0) == RHT) {                                    \
+        auto kern = k_dual_tile_amax<GRID, ROUND, RHT>;                                                  \
+        cudaError_t e = opt_in_smem(kern, kTileAmaxSmem);                                                \
+        if (e != cudaSuccess) return e;                                                                  \
+        const int g = resident_grid(kern, (int64_t)ntiles + want, kTileAmaxSmem);                        \
+        const uint32_t namax = std::min<uint32_t>(want, (uint32_t)g);                                    \
+        kern<<<g, kThreads, kTileAmaxSmem, s>>>(tm, ar, ac, nct, ntiles, br, bc, ncc, nch, namax, next_tile); \
+        br.partials = br.partials_out;                                                                   \
+        bc.partials = bc.partials_out;                                                                   \
+        br.n_partials = bc.n_partials = (int)namax;                                                      \
+        return cudaGetLastError();                                                                       \
+    }
+    UFP4_TA(kE2M1, kRTNE, false) UFP4_TA(kE2M1, kRTNE, true)
+    UFP4_TA(kE2M1, kSR, false)   UFP4_TA(kE2M1, kSR, true)
+    UFP4_TA(kE1M2, kRTNE, false) UFP4_TA(kE1M2, kRTNE, true)
+    UFP4_TA(kE1M2, kSR, false)   UFP4_TA(kE1M2, kSR, true)
+#undef UFP4_TA
+    return cudaErrorInvalidValue;
+}
+
 template <class In>
 cudaError_t quantize_dual_typed(const QuantLaunch &qr, const QuantLaunch &qc, Args &ar, Args &ac, void *ws,
                                 cudaStream_t s) {
@@ -3080,42 +3258,10 @@ cudaError_t quantize_dual_typed(const QuantLaunch &qr, const QuantLaunch &qc, Ar
             }
         }
         if (!qr.amax_in || !qc.amax_in) {
-            // the amax pass streams with little arithmetic: 16-row x 1 KB
-            // chunks (contiguous kilobyte rows) read faster than 128-byte
-            // tile rows, and the maxima do not depend on the traversal
-            constexpr uint32_t CW = kChunk / 32;
-            const uint32_t ncc = (uint32_t)((ar.cols + CW - 1) / CW), nch = (uint32_t)(ar.rows / 16) * ncc;
-            ar.partials_out = reinterpret_cast<float *>(static_cast<char *>(ws) + kWsPartials);
-            ac.partials_out = ar.partials_out + kMaxPartials / 2;
-            int g = 1;
-            cudaError_t e;
-            if (qr.rht) {
-                // the tensor-core amax of both orientations (CW = kMmaCW: same chunking)
-                static_assert(CW == kMmaCW, "chunk widths");
-                auto kern = k_amax_mma<true, true>;
-                if (resident_grid(kern, nch, kMmaSmem) > kMaxPartials / 2) return cudaErrorInvalidValue;
-                e = launch_staged_smem(kern, kMmaSmem, nch, &g, s, ar, ac, ncc, nch);
-            } else {
-                auto kern = k_dual_staged<In, 0, 0, false, true>;
-                if (resident_grid(kern, nch, ring_smem<true>()) > kMaxPartials / 2) return cudaErrorInvalidValue;
-                e = launch_staged<true>(kern, nch, &g, s, ar, ac, ncc, nch);
-            }
+            cudaError_t e = dual_amax_pass(qr, ar, ac, partial_area(ws, 0), s);
             if (e != cudaSuccess) return e;
-            ar.partials = ar.partials_out;
-            ac.partials = ac.partials_out;
-            ar.n_partials = ac.n_partials = g;
         }
-        const int kgrid = qr.grid == kE2M1 ? kE2M1 : kE1M2;   // clamped E2M1 runs the uniform-grid kernels
-#define UFP4_T(GRID, ROUND, RHT)                                                                          \
-        if (kgrid == GRID && qr.round == ROUND && (qr.rht != 0) == RHT)                                   \
-            return launch_staged_smem(k_dual_tile<GRID, ROUND, RHT>, kTileSmem, ntiles, nullptr, s, tm, ar,       \
-                                      ac, nct, ntiles);
-        UFP4_T(kE2M1, kRTNE, false) UFP4_T(kE2M1, kRTNE, true)
-        UFP4_T(kE2M1, kSR, false)   UFP4_T(kE2M1, kSR, true)
-        UFP4_T(kE1M2, kRTNE, false) UFP4_T(kE1M2, kRTNE, true)
-        UFP4_T(kE1M2, kSR, false)   UFP4_T(kE1M2, kSR, true)
-#undef UFP4_T
-        return cudaErrorInvalidValue;
+        return dual_tile_pass(qr, tm, nct, ntiles, ar, ac, s);
     } else {
     constexpr uint32_t CW = kChunk / (16 * sizeof(In));
     const uint32_t ncc = (uint32_t)((ar.cols + CW - 1) / CW), nch = (uint32_t)(ar.rows / 16) * ncc;
@@ -3154,6 +3300,7 @@ Args make_args(const QuantLaunch &q, void *ws) {
     a.elem_base = q.elem_base;
     a.amax_in = q.amax_in;
     a.status = ws ? reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsStatus) : nullptr;
+    a.status_or = q.status_or;
     a.codes = q.codes; a.scales = q.scales; a.tensor_scale = q.tensor_scale;
     a.eplane = q.grid == kE1M2 ? q.eplane : nullptr;
     a.uqmax = q.grid == kE2M1C ? 2.0f : 3.5f;
@@ -3290,6 +3437,73 @@ cudaError_t launch_quantize_dual(const QuantLaunch &qr, const QuantLaunch &qc, v
     Args ar = make_args(qr, ws), ac = make_args(qc, ws);
     if (qr.dtype == 0) return quantize_dual_typed<__nv_bfloat16>(qr, qc, ar, ac, ws, s);
     return quantize_dual_typed<float>(qr, qc, ar, ac, ws, s);
+}
+
+// Which route launch_quantize_dual takes for a BF16 pair: the tile route
+// (an amax pass when a maximum is missing, then k_dual_tile) or another one
+// (the on-chip single pass, the staged FP32 kernels, two single passes).
+static bool dual_tile_route(const QuantLaunch &qr, const QuantLaunch &qc) {
+    const bool same = qr.grid == qc.grid && qr.round == qc.round && qr.rht == qc.rht &&
+                      (!qr.rht || qr.rht_seed == qc.rht_seed);
+    if (qr.dtype != 0 || !same || (qr.cols * 2) % 16 != 0 || qr.rows % 16 != 0) return false;
+    if (qr.amax_in || qc.amax_in) return true;
+    const int64_t nct = (qr.cols + kTileCols - 1) / kTileCols;
+    const int64_t ntiles = (qr.rows + kTileRows - 1) / kTileRows * nct;
+    const int64_t grid = std::min<int64_t>(num_sms(), ntiles);
+    return (ntiles + grid - 1) / grid > kResidentMax;   // else the on-chip single pass
+}
+
+cudaError_t launch_quantize_dual_batch(const QuantLaunch *qr, const QuantLaunch *qc, int n, void *ws,
+                                       cudaStream_t s) {
+    if (n < 0 || n > kMaxDualBatch) return cudaErrorInvalidValue;
+    // the status word and the tile counters start at zero; every pass then
+    // only raises the flag
+    cudaError_t e = cudaMemsetAsync(ws, 0, kWsPartials, s);
+    if (e != cudaSuccess) return e;
+    int area = 0;            // partial area of the tensor being quantized
+    bool have_amax = false;  // its amax pass ran inside the previous launch
+    Args pr{}, pc{};         // (then: its Args with the partials set)
+    for (int j = 0; j < n; ++j) {
+        QuantLaunch r = qr[j], c = qc[j];
+        r.status_or = c.status_or = 1;
+        if (!dual_tile_route(r, c)) {
+            e = launch_quantize_dual(r, c, ws, s);
+            if (e != cudaSuccess) return e;
+            continue;
+        }
+        Args ar = have_amax ? pr : make_args(r, ws), ac = have_amax ? pc : make_args(c, ws);
+        ac.status = nullptr;   // the row-wise prologue reports both
+        alignas(64) CUtensorMap tm;
+        if (!make_input_tile_map(&tm, ar.x, ar.rows, ar.cols, ar.ld, kTileCols, kTileRows))
+            return cudaErrorInvalidValue;
+        const uint32_t nct = (uint32_t)((ar.cols + kTileCols - 1) / kTileCols);
+        const uint32_t ntiles = (uint32_t)((ar.rows + kTileRows - 1) / kTileRows) * nct;
+        if (!have_amax && (!r.amax_in || !c.amax_in)) {
+            e = dual_amax_pass(r, ar, ac, partial_area(ws, area), s);
+            if (e != cudaSuccess) return e;
+        }
+        // the next tensor's amax pass (tensor cores, so the transform is on)
+        // joins this quantization pass
+        have_amax = false;
+        if (j + 1 < n) {
+            QuantLaunch r2 = qr[j + 1], c2 = qc[j + 1];
+            r2.status_or = c2.status_or = 1;
+            if (dual_tile_route(r2, c2) && r2.rht && (!r2.amax_in || !c2.amax_in)) {
+                pr = make_args(r2, ws);
+                pc = make_args(c2, ws);
+                uint32_t *next_tile = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsTileNext) + j;
+                e = dual_tile_amax_pass(r, tm, nct, ntiles, ar, ac, pr, pc, partial_area(ws, area ^ 1), next_tile,
+                                        s);
+                if (e != cudaSuccess) return e;
+                have_amax = true;
+                area ^= 1;
+                continue;
+            }
+        }
+        e = dual_tile_pass(r, tm, nct, ntiles, ar, ac, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_quantize_grouped(const QuantLaunch &q, const GroupQuant &gt, void *ws, cudaStream_t s) {
