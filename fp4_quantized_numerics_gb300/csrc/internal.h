@@ -10,14 +10,19 @@ namespace ufp4 {
 // Workspace layout (bytes from the start of the caller's scratch buffer).
 constexpr size_t kWsStatus = 0;            // uint32 status word
 constexpr size_t kWsArrive = 8;            // uint32 grid-barrier counter of the single-pass quantizer
-constexpr size_t kWsTileNext = 16;         // uint32 tile counters of a batched dual quantization, one per tensor
-constexpr int kMaxDualBatch = 32;
 constexpr size_t kWsPartials = 256;        // float partial maxima
-static_assert(kWsTileNext + kMaxDualBatch * sizeof(uint32_t) <= kWsPartials, "tile counters end before the partials");
 constexpr int kMaxPartials = 4096;
 constexpr size_t kWsStats = 32768;         // double partial sums, 8 per CTA
 constexpr int kMaxStatsCtas = 1024;
 constexpr size_t kWorkspaceBytes = kWsStats + size_t(kMaxStatsCtas) * 8 * sizeof(double);
+// A batched dual quantization (which takes no statistics) also uses the
+// statistics area: a second partial-maximum area at kWsStats and, after it,
+// one control block of kBatchCtlWords uint32 per tensor.
+constexpr int kMaxDualBatch = 32;
+constexpr size_t kWsBatchCtl = kWsStats + size_t(kMaxPartials) * sizeof(float);
+constexpr uint32_t kBatchCtlWords = 256;
+static_assert(kWsBatchCtl + size_t(kMaxDualBatch) * kBatchCtlWords * sizeof(uint32_t) <= kWorkspaceBytes,
+              "the control blocks fit the workspace");
 
 struct QuantLaunch {
     const void *x;

@@ -1397,19 +1397,49 @@ __device__ __forceinline__ void mma_bf16(const uint32_t (&a)[4], uint32_t b0, ui
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
-// The amax pass over chunks cta, cta + ncta, ... of x, staged in `dsm`
-// (kMmaSmem bytes); writes this CTA's partial maxima to partials_out[cta].
-template <bool ROW, bool COL>
-__device__ __forceinline__ void amax_mma_run(const Args &ar, const Args &ac, uint32_t ncc, uint32_t nchunks,
-                                             uint32_t cta, uint32_t ncta, uint8_t *dsm, float *s_red,
-                                             float *s_red2) {
+// Where the chunks of an amax loop come from: a fixed stride over the CTAs,
+// or one at a time from a counter in global memory that several CTAs share;
+// kNoChunk once exhausted (and from then on).  The shared source's claims
+// are made by thread 0 and published in `slot` (one word per ring stage).
+constexpr uint32_t kNoChunk = 0xFFFFFFFFu;
+struct StrideChunks {
+    static constexpr bool kShared = false;
+    uint32_t first, stride, n;
+    __device__ __forceinline__ uint32_t at(uint32_t jj, const volatile uint32_t *) const {
+        const uint64_t i = first + (uint64_t)jj * stride;
+        return i < n ? (uint32_t)i : kNoChunk;
+    }
+    __device__ __forceinline__ uint32_t claim() const { return kNoChunk; }
+};
+struct SharedChunks {
+    static constexpr bool kShared = true;
+    uint32_t *next, n;
+    __device__ __forceinline__ uint32_t at(uint32_t jj, const volatile uint32_t *slot) const {
+        return slot[jj % kMmaRing];
+    }
+    __device__ __forceinline__ uint32_t claim() const {
+        const uint32_t i = atomicAdd(next, 1u);
+        return i < n ? i : kNoChunk;
+    }
+};
+
+// The amax pass over the chunks of `src`, staged in `dsm` (kMmaSmem bytes);
+// folds this thread's maxima of |y| (unscaled) into mr (row-wise blocks)
+// and mc (column-wise blocks).
+template <bool ROW, bool COL, class Src>
+__device__ __forceinline__ void amax_mma_loop(const Args &ar, const Args &ac, uint32_t ncc, const Src &src,
+                                              uint8_t *dsm, float &mr, float &mc) {
     const Args &a = ROW ? ar : ac;   // the input as stored (both describe the same x)
     const uint32_t buf = ptx::smem_u32(dsm);
     const uint32_t bars = buf + kMmaRing * kMmaStage;
+    volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(dsm + kMmaRing * kMmaStage + 32);
     volatile int *abort = reinterpret_cast<volatile int *>(dsm + kMmaRing * kMmaStage + 60);
+    static_assert(kMmaRing * 8 <= 32 && 32 + kMmaRing * 4 <= 60, "barriers, slots and flag fit 64 bytes");
     if (threadIdx.x == 0) {
         for (int t = 0; t < kMmaRing; ++t) ptx::mbar_init(bars + 8u * t, 1);
         *abort = 0;
+        if (Src::kShared)
+            for (int t = 0; t < kMmaRing; ++t) slot[t] = src.claim();
         ptx::fence_mbar_init();
     }
     __syncthreads();
@@ -1419,17 +1449,17 @@ __device__ __forceinline__ void amax_mma_run(const Args &ar, const Args &ac, uin
     // each; thread 0 also posts the chunk's byte count (the barrier's phase
     // needs that single arrival, so copies may land before or after it).
     auto issue = [&](uint32_t jj) {
-        const uint32_t i = cta + jj * ncta;
-        if (i >= nchunks) return;
+        const uint32_t i = src.at(jj, slot);
+        if (i == kNoChunk) return;
         const uint32_t kb = i / ncc, cc = i - kb * ncc;
         const uint32_t c0 = cc * kMmaCW, r0 = kb * 16;
         const uint32_t ncols = min(kMmaCW, cols - c0), nrows = min(16u, rows - r0);
         const uint32_t bar = bars + 8u * (jj % kMmaRing);
         const uint32_t st = buf + (jj % kMmaRing) * kMmaStage;
         if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(bar, nrows * ncols * 2);
-        const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(a.x) + (int64_t)r0 * a.ld + c0;
+        const __nv_bfloat16 *src_x = static_cast<const __nv_bfloat16 *>(a.x) + (int64_t)r0 * a.ld + c0;
         for (uint32_t q = 2 * (threadIdx.x >> 5); q < min(nrows, 2 * (threadIdx.x >> 5) + 2); ++q)
-            ptx::bulk_load(st + q * kMmaPitch, src + (int64_t)q * a.ld, ncols * 2, bar);
+            ptx::bulk_load(st + q * kMmaPitch, src_x + (int64_t)q * a.ld, ncols * 2, bar);
         issued = jj + 1;
     };
     if ((threadIdx.x & 31) == 0)
@@ -1445,14 +1475,13 @@ __device__ __forceinline__ void amax_mma_run(const Args &ar, const Args &ac, uin
     const uint32_t bl0 = bv(n0, k0) | (bv(n0, k0 + 1) << 16), bl1 = bv(n0, k0 + 8) | (bv(n0, k0 + 9) << 16);
     const uint32_t bh0 = bv(n0 + 8, k0) | (bv(n0 + 8, k0 + 1) << 16);
     const uint32_t bh1 = bv(n0 + 8, k0 + 8) | (bv(n0 + 8, k0 + 9) << 16);
-    float mr = 0.0f, mc = 0.0f;
     // running max of |D| over the A rows that hold data (rows m = lane / 4 and lane / 4 + 8)
     auto acc = [&](float &m, const float (&d)[4], const float (&e)[4], bool lo_ok, bool hi_ok) {
         if (lo_ok) m = max_nan(max_nan(m, max_nan(fabsf(d[0]), fabsf(d[1]))), max_nan(fabsf(e[0]), fabsf(e[1])));
         if (hi_ok) m = max_nan(max_nan(m, max_nan(fabsf(d[2]), fabsf(d[3]))), max_nan(fabsf(e[2]), fabsf(e[3])));
     };
     auto process = [&](uint32_t jj) {
-        const uint32_t i = cta + jj * ncta;
+        const uint32_t i = src.at(jj, slot);
         const uint32_t kb = i / ncc, cc = i - kb * ncc;
         const uint32_t c0 = cc * kMmaCW, r0 = kb * 16;
         const uint32_t ncols = min(kMmaCW, cols - c0), nrows = min(16u, rows - r0);
@@ -1490,8 +1519,10 @@ __device__ __forceinline__ void amax_mma_run(const Args &ar, const Args &ac, uin
         }
     };
     bool ok = true;
-    while (j < nchunks && cta + j * ncta < nchunks) {
-        const uint32_t nj = (cta + (j + 1) * ncta < nchunks) ? 2u : 1u;
+    // (every thread reads the same chunk indices: computed, or published in
+    // `slot` before the barrier that precedes their use)
+    while (src.at(j, slot) != kNoChunk) {
+        const uint32_t nj = src.at(j + 1, slot) != kNoChunk ? 2u : 1u;
         bool mine = true;
         for (uint32_t t = 0; t < nj && mine; ++t)
             mine = ptx::mbar_wait_bounded(bars + 8u * ((j + t) % kMmaRing), ((j + t) / kMmaRing) & 1u, kRingWait);
@@ -1500,6 +1531,11 @@ __device__ __forceinline__ void amax_mma_run(const Args &ar, const Args &ac, uin
             for (uint32_t t = 0; t < nj; ++t) process(j + t);
         __syncthreads();
         if (*abort) { ok = false; break; }
+        if (Src::kShared) {
+            if (threadIdx.x == 0)
+                for (uint32_t t = 0; t < nj; ++t) slot[(j + t) % kMmaRing] = src.claim();
+            __syncthreads();
+        }
         if ((threadIdx.x & 31) == 0)
             for (uint32_t t = 0; t < nj; ++t) issue(j + t + kMmaRing);
         j += nj;
@@ -1511,17 +1547,22 @@ __device__ __forceinline__ void amax_mma_run(const Args &ar, const Args &ac, uin
             for (uint32_t h = j; h < issued; ++h)
                 if (!ptx::mbar_wait_bounded(bars + 8u * (h % kMmaRing), (h / kMmaRing) & 1u, kRingWait)) break;
     }
+}
+
+// The CTA's maxima (x 1/4: the transform's normalisation) as its partials.
+__device__ __forceinline__ void amax_partials_out(const Args &ar, const Args &ac, bool row, bool col, uint32_t cta,
+                                                  float mr, float mc, float *s_red, float *s_red2) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
         mr = max_nan(mr, __shfl_xor_sync(0xffffffffu, mr, o));
         mc = max_nan(mc, __shfl_xor_sync(0xffffffffu, mc, o));
     }
-    if (lane == 0) { s_red[warp] = mr; s_red2[warp] = mc; }
+    if ((threadIdx.x & 31) == 0) { s_red[threadIdx.x >> 5] = mr; s_red2[threadIdx.x >> 5] = mc; }
     __syncthreads();
     if (threadIdx.x == 0) {
         for (int w = 1; w < kThreads / 32; ++w) { mr = max_nan(mr, s_red[w]); mc = max_nan(mc, s_red2[w]); }
-        if (ROW) ar.partials_out[cta] = mr * 0.25f;
-        if (COL) ac.partials_out[cta] = mc * 0.25f;
+        if (row) ar.partials_out[cta] = mr * 0.25f;
+        if (col) ac.partials_out[cta] = mc * 0.25f;
     }
 }
 
@@ -1530,7 +1571,9 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_amax_mma(Args ar, 
                                                                       uint32_t nchunks) {
     extern __shared__ __align__(128) uint8_t dsm[];
     __shared__ float s_red[kThreads / 32], s_red2[kThreads / 32];
-    amax_mma_run<ROW, COL>(ar, ac, ncc, nchunks, blockIdx.x, gridDim.x, dsm, s_red, s_red2);
+    float mr = 0.0f, mc = 0.0f;
+    amax_mma_loop<ROW, COL>(ar, ac, ncc, StrideChunks{blockIdx.x, gridDim.x, nchunks}, dsm, mr, mc);
+    amax_partials_out(ar, ac, ROW, COL, blockIdx.x, mr, mc, s_red, s_red2);
 }
 
 // ================================================ dual orientation (X and X^T)
@@ -1930,30 +1973,60 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas)
     dual_padding(ar, ac, dual_geom(ar, ac));
 }
 
-// The quantization pass of one tensor (as k_dual_tile) with the tensor-amax
-// pass of the next one (as k_amax_mma<true, true>, both orientations of
-// x_next) in the same launch, so that the amax pass, which streams at HBM
-// speed with little arithmetic, runs beside a quantization pass that is
-// bound by instruction issue.  CTAs 0 .. namax-1 first take the amax chunks
-// (a fixed stride over namax CTAs; partial maxima in br / bc.partials_out
-// [0, namax)); then they, and from the start every other CTA, claim the
-// quantization tiles from the shared counter `next_tile` (zero before the
-// launch).  The amax ring and the tile ring share dynamic shared memory: the
-// amax run has consumed every copy it started when it returns.  Every
-// result equals that of the two separate launches.
+// Control block of one k_dual_tile_amax launch in device memory (zeroed
+// before the launch): the next quantization tile, the next amax chunk, and
+// per SM the number of the launch's CTAs that have started there.
+constexpr uint32_t kCtlTile = 0, kCtlChunk = 1, kCtlSm = 2, kCtlMaxSmid = kBatchCtlWords - kCtlSm;
+
+// The quantization pass of one tensor (k_dual_tile's work) and the
+// tensor-amax pass of the next one (k_amax_mma<true, true>'s work, both
+// orientations of x_next) in one launch, so that the amax pass, which
+// streams at HBM speed with little arithmetic, runs beside a quantization
+// pass that is bound by instruction issue.  The first CTA to start on each
+// SM begins with the amax chunks, every other CTA with the quantization
+// tiles; both kinds of work are claimed one unit at a time from counters in
+// `ctl`, and a CTA whose kind runs out takes what is left of the other, so
+// neither the CTAs' placement nor the two passes' relative speed leaves SMs
+// idle.  Every CTA writes its partial maxima of x_next to
+// br / bc.partials_out[blockIdx.x] (zero if it took no chunk).  The amax
+// ring and the tile ring share dynamic shared memory: each ring has
+// consumed every copy it started when its loop returns, and its barriers
+// are invalidated before the other ring reuses the bytes.  Every result
+// equals that of the two separate launches.
 template <int GRID, int ROUND, bool RHT>
 __global__ void __launch_bounds__(kThreads, kStagedMinCtas)
     k_dual_tile_amax(const __grid_constant__ CUtensorMap tmx, Args ar, Args ac, uint32_t nct, uint32_t ntiles,
-                     Args br, Args bc, uint32_t ncc, uint32_t nch, uint32_t namax, uint32_t *next_tile) {
+                     Args br, Args bc, uint32_t ncc, uint32_t nch, uint32_t *ctl) {
     extern __shared__ __align__(128) uint8_t dsm[];
     __shared__ float s_kr[256], s_kc[256];
     __shared__ float s_red[kThreads / 32], s_red2[kThreads / 32];
-    if (blockIdx.x < namax) {
-        amax_mma_run<true, true>(br, bc, ncc, nch, blockIdx.x, namax, dsm, s_red, s_red2);
-        ptx::fence_proxy_async();   // the amax stages' bytes are reused by the tile ring's copies
-        __syncthreads();
+    __shared__ uint32_t s_amax_first;
+    if (threadIdx.x == 0) {
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        s_amax_first = smid < kCtlMaxSmid && atomicAdd(ctl + kCtlSm + smid, 1u) == 0u;
     }
-    dual_tile_loop<GRID, ROUND, RHT>(&tmx, ar, ac, nct, SharedTiles{next_tile, ntiles}, dsm, s_kr, s_kc, s_red);
+    __syncthreads();
+    const bool amax_first = s_amax_first != 0;
+    const SharedChunks chunks{ctl + kCtlChunk, nch};
+    float mr = 0.0f, mc = 0.0f;
+    auto release = [&](uint32_t bars, int n) {   // a ring's barriers, before its bytes are reused
+        if (threadIdx.x == 0)
+            for (int t = 0; t < n; ++t) ptx::mbar_inval(bars + 8u * t);
+        ptx::fence_proxy_async();   // this CTA's generic accesses before the next ring's copies
+        __syncthreads();
+    };
+    if (amax_first) {
+        amax_mma_loop<true, true>(br, bc, ncc, chunks, dsm, mr, mc);
+        release(ptx::smem_u32(dsm) + kMmaRing * kMmaStage, kMmaRing);
+    }
+    dual_tile_loop<GRID, ROUND, RHT>(&tmx, ar, ac, nct, SharedTiles{ctl + kCtlTile, ntiles}, dsm, s_kr, s_kc,
+                                     s_red);
+    if (!amax_first) {
+        release(ptx::smem_u32(dsm) + ring_depth<false>() * kChunk, ring_depth<false>());
+        amax_mma_loop<true, true>(br, bc, ncc, chunks, dsm, mr, mc);
+    }
+    amax_partials_out(br, bc, true, true, blockIdx.x, mr, mc, s_red, s_red2);
     dual_padding(ar, ac, dual_geom(ar, ac));
 }
 constexpr uint32_t kTileAmaxSmem = kTileSmem > kMmaSmem ? kTileSmem : kMmaSmem;
@@ -3188,28 +3261,27 @@ cudaError_t dual_tile_pass(const QuantLaunch &qr, const CUtensorMap &tm, uint32_
 }
 
 // The quantization pass of the tile route with the transform-on amax pass
-// of the next tensor (br / bc, partials into area_b) in the same launch
-// (k_dual_tile_amax); next_tile: a zeroed counter in device memory.  One
-// amax CTA per SM; the grid is the resident one.
+// of the next tensor (br / bc, partials into area_b, one per CTA) in the
+// same launch (k_dual_tile_amax); ctl: its zeroed control block.  The grid
+// is the resident one.
 cudaError_t dual_tile_amax_pass(const QuantLaunch &qr, const CUtensorMap &tm, uint32_t nct, uint32_t ntiles,
-                                const Args &ar, const Args &ac, Args &br, Args &bc, float *area_b,
-                                uint32_t *next_tile, cudaStream_t s) {
+                                const Args &ar, const Args &ac, Args &br, Args &bc, float *area_b, uint32_t *ctl,
+                                cudaStream_t s) {
     const uint32_t ncc = (uint32_t)((br.cols + kMmaCW - 1) / kMmaCW), nch = (uint32_t)(br.rows / 16) * ncc;
     br.partials_out = area_b;
     bc.partials_out = area_b + kMaxPartials / 2;
-    const uint32_t want = (uint32_t)std::max<int64_t>(1, std::min<int64_t>(num_sms(), nch));
     const int kgrid = qr.grid == kE2M1 ? kE2M1 : kE1M2;
 #define UFP4_TA(GRID, ROUND, RHT)                                                                         \
     if (kgrid == GRID && qr.round == ROUND && (qr.rht != 0) == RHT) {                                    \
         auto kern = k_dual_tile_amax<GRID, ROUND, RHT>;                                                  \
         cudaError_t e = opt_in_smem(kern, kTileAmaxSmem);                                                \
         if (e != cudaSuccess) return e;                                                                  \
-        const int g = resident_grid(kern, (int64_t)ntiles + want, kTileAmaxSmem);                        \
-        const uint32_t namax = std::min<uint32_t>(want, (uint32_t)g);                                    \
-        kern<<<g, kThreads, kTileAmaxSmem, s>>>(tm, ar, ac, nct, ntiles, br, bc, ncc, nch, namax, next_tile); \
+        const int g = resident_grid(kern, (int64_t)ntiles + nch, kTileAmaxSmem);                         \
+        if (g > kMaxPartials / 2) return cudaErrorInvalidValue;                                          \
+        kern<<<g, kThreads, kTileAmaxSmem, s>>>(tm, ar, ac, nct, ntiles, br, bc, ncc, nch, ctl);         \
         br.partials = br.partials_out;                                                                   \
         bc.partials = bc.partials_out;                                                                   \
-        br.n_partials = bc.n_partials = (int)namax;                                                      \
+        br.n_partials = bc.n_partials = g;                                                               \
         return cudaGetLastError();                                                                       \
     }
     UFP4_TA(kE2M1, kRTNE, false) UFP4_TA(kE2M1, kRTNE, true)
@@ -3456,9 +3528,12 @@ static bool dual_tile_route(const QuantLaunch &qr, const QuantLaunch &qc) {
 cudaError_t launch_quantize_dual_batch(const QuantLaunch *qr, const QuantLaunch *qc, int n, void *ws,
                                        cudaStream_t s) {
     if (n < 0 || n > kMaxDualBatch) return cudaErrorInvalidValue;
-    // the status word and the tile counters start at zero; every pass then
-    // only raises the flag
-    cudaError_t e = cudaMemsetAsync(ws, 0, kWsPartials, s);
+    // the status word and the launches' control blocks start at zero; every
+    // pass then only raises the flag
+    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), s);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(static_cast<char *>(ws) + kWsBatchCtl, 0, kMaxDualBatch * kBatchCtlWords * sizeof(uint32_t),
+                        s);
     if (e != cudaSuccess) return e;
     int area = 0;            // partial area of the tensor being quantized
     bool have_amax = false;  // its amax pass ran inside the previous launch
@@ -3491,9 +3566,9 @@ cudaError_t launch_quantize_dual_batch(const QuantLaunch *qr, const QuantLaunch 
             if (dual_tile_route(r2, c2) && r2.rht && (!r2.amax_in || !c2.amax_in)) {
                 pr = make_args(r2, ws);
                 pc = make_args(c2, ws);
-                uint32_t *next_tile = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsTileNext) + j;
-                e = dual_tile_amax_pass(r, tm, nct, ntiles, ar, ac, pr, pc, partial_area(ws, area ^ 1), next_tile,
-                                        s);
+                uint32_t *ctl = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsBatchCtl) +
+                                (size_t)j * kBatchCtlWords;
+                e = dual_tile_amax_pass(r, tm, nct, ntiles, ar, ac, pr, pc, partial_area(ws, area ^ 1), ctl, s);
                 if (e != cudaSuccess) return e;
                 have_amax = true;
                 area ^= 1;

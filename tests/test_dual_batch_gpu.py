@@ -83,11 +83,12 @@ def test_training_step_operands(U):
 def test_chain_of_three_ragged(U, grid, rnd):
     """Three tile-route tensors, each needing its maxima: two folded amax
     passes (the partial areas alternate).  Ragged shapes: row counts off the
-    128-row tile, column counts off the 64-column tile and the 512-column
-    amax chunk; the quantized tensor's grid and rounding vary."""
-    a = _x(4, 3600, 4936)
-    b = _x(5, 4112, 4424, std=3.0)
-    c = _x(6, 2336, 7480)
+    128-row tile, column counts (multiples of 16, as row-wise blocks need)
+    off the 64-column tile and the 512-column amax chunk; the quantized
+    tensor's grid and rounding vary."""
+    a = _x(4, 3600, 4944)   # 29 x 78 = 2262 tiles
+    b = _x(5, 4112, 4432, std=3.0)   # 33 x 70 = 2310 tiles
+    c = _x(6, 2336, 7472)   # 19 x 117 = 2223 tiles
     kw = dict(grid=grid, rht=True, rht_seed=9)
     _check_batch(U, [dict(x=a, round=rnd, sr_seed=7, sr_counter_row=5, **kw), dict(x=b, round=rnd, sr_seed=8, **kw),
                      dict(x=c, **kw)])
@@ -109,6 +110,21 @@ def test_routes_that_do_not_fold(U):
             dict(x=d, grid=0, rht=True, rht_seed=3),                             # FP32: staged kernels
             dict(x=e, grid=0, rht=True, rht_seed=3, round=1, sr_seed=2)]         # after FP32: own amax pass
     _check_batch(U, jobs)
+
+
+def test_unbalanced_pairs(U):
+    """Folded pairs whose two kinds of work differ a lot in size, so that the
+    CTAs of one kind run out early and finish the other kind's work: a tiny
+    quantization (maxima given, so it takes the tile route) before a large
+    amax pass, and a large quantization before a tiny amax pass (a small
+    tensor with one maximum given takes the tile route too)."""
+    a = _x(18, 128, 256)
+    b = _x(19, 3584, 4928)
+    c = _x(20, 3584, 4928)
+    d = _x(21, 64, 128)
+    am = torch.tensor([40.0], device="cuda")
+    _check_batch(U, [dict(x=a, grid=1, rht=True, amax_row=am, amax_col=am), dict(x=b, grid=1, rht=True),
+                     dict(x=c, grid=0, rht=True, round=1, sr_seed=6), dict(x=d, grid=1, rht=True, amax_row=am)])
 
 
 def test_nonfinite_flag_covers_every_job(U):
