@@ -190,7 +190,7 @@ class Step:
     """Buffers and launches of one UFP4 training step (E1M2 + RHT on all
     GEMM operands, SR on dY), all through the libufp4 binding."""
 
-    def __init__(self, U, x, w, dy, grid, dual=True, policy="ufp4", batch=True):
+    def __init__(self, U, x, w, dy, grid, dual=True, policy="ufp4"):
         import torch
         self.U, self.torch = U, torch
         self.x, self.w, self.dy = x, w, dy
@@ -210,9 +210,6 @@ class Step:
         # two orientations then differ and are quantized one pass each
         self.policy = policy
         self.dual = dual and policy == "ufp4"
-        # one ufp4_quantize_dual_batch call (dY first: X's amax pass runs
-        # inside dY's quantization launch) instead of three dual calls
-        self.batch = batch and self.dual and grid != U.UFP4_MXFP4
         self.launches_per_step = self.count_launches(x.device) + 3
         self.q_elems = 2 * (x.numel() + w.numel() + dy.numel())
         self.flops_each = [2 * T * F * H, 2 * T * H * F, 2 * F * H * T]
@@ -225,8 +222,7 @@ class Step:
         import torch
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         n = 0
-        two_pass = []
-        for t in (self.dy, self.x, self.w):
+        for t in (self.x, self.w, self.dy):
             if self.grid == self.U.UFP4_MXFP4:   # no tensor amax: one pass per orientation
                 n += 2
                 continue
@@ -234,28 +230,13 @@ class Step:
             tiles = -(-rows // 128) * -(-cols // 64)
             if self.dual and t.dtype == torch.bfloat16 and -(-tiles // min(sms, tiles)) <= 14:
                 n += 1
-                two_pass.append(False)
             else:
                 n += 2 * (1 if self.dual else 2)
-                two_pass.append(True)
-        if self.batch:
-            # each two-pass tensor right after another one has its amax pass
-            # folded into that one's quantization launch
-            n -= sum(1 for a, b in zip(two_pass, two_pass[1:]) if a and b)
         return n
 
     def quantize_all(self):
         U, g = self.U, self.grid
         kw = dict(rht=True, rht_seed=2, ws=self.ws)
-        if self.batch:
-            U.ufp4_quantize_dual_batch(
-                [dict(x=self.dy, grid=g, rht=True, rht_seed=2, round=U.UFP4_SR, sr_seed=3,
-                      sr_counter_row=self.counter, sr_counter_col=self.counter, out_row=self.qdy_r,
-                      out_col=self.qdy_c),
-                 dict(x=self.x, grid=g, rht=True, rht_seed=2, out_row=self.qx_r, out_col=self.qx_c),
-                 dict(x=self.w, grid=g, rht=True, rht_seed=2, out_row=self.qw_r, out_col=self.qw_c)], ws=self.ws)
-            self.counter += 1
-            return
         if self.dual:
             # each operand in both orientations from one read per pass
             U.ufp4_quantize_dual(self.x, g, out_row=self.qx_r, out_col=self.qx_c, **kw)
@@ -320,7 +301,6 @@ def run_gpu(args):
     d = moe124b_inputs(dev, seed=rank)
     step = Step(U, d["x"], d["w"], d["dy"], U.UFP4_E1M2)
     n_launch = step.launches_per_step   # kernels per step (quantize phase + 3 GEMMs)
-    step_batch = step.batch
     flush = L2Flush(dev)
 
     for _ in range(args.warmup):
@@ -364,15 +344,6 @@ def run_gpu(args):
         e2e["value"] = ws_n * e2e["steps"] * q_bytes / e2e["value"] / 1e9
         del e2e["time_s"]
 
-    # the same quantize phase as three ufp4_quantize_dual calls (each
-    # tensor's amax pass and quantization pass back to back, 5 launches)
-    q_unbatched = None
-    if not args.quick and step.batch:
-        step.batch = False
-        qu_ms, _ = time_steps(step, min(args.steps, 30), flush)
-        step.batch = True
-        q_unbatched = sum(qu_ms) / len(qu_ms)
-
     extra = {}
     if not args.quick and rank == 0:
         extra["quantizer_x_65536x8192"] = quantizer_on_x(U, torch, dev, pk, flush, d["x"])
@@ -400,9 +371,7 @@ def run_gpu(args):
             "quantize": {"gbs": round(q_gbs, 1), "frac_hbm": round(q_gbs / ws_n / pk["hbm_gbs"], 4),
                          "ms_per_step": round(tq / args.steps, 4),
                          "elements_per_step": step_elems(WORKLOAD),
-                         "launches_per_step": n_launch - 3,
-                         "call": "ufp4_quantize_dual_batch (dY, X, W)" if step_batch else "ufp4_quantize_dual x 3",
-                         "ms_per_step_three_dual_calls": None if q_unbatched is None else round(q_unbatched, 4)},
+                         "launches_per_step": n_launch - 3},
             "gemm": {"tflops": round(gemm_tflops, 1), "ms_per_step": round(tg / args.steps, 4),
                      "ms_each": [round(v, 4) for v in gemm_each],
                      "frac_fp8_peak_sustained": round(per_gpu_tflops / fp8_sus, 4),

@@ -145,31 +145,6 @@ ufp4_status ufp4_quantize_dual(const void *x, int32_t dtype, int64_t rows, int64
     return from_cuda(launch_quantize_dual(qr, qc, workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-static_assert(UFP4_MAX_DUAL_BATCH == kMaxDualBatch, "batch limit of the header and the launcher");
-
-ufp4_status ufp4_quantize_dual_batch(const ufp4_dual_job *jobs, int32_t n, void *workspace,
-                                     size_t workspace_bytes, ufp4_stream_t stream) {
-    if (n < 0 || n > UFP4_MAX_DUAL_BATCH || (n > 0 && !jobs)) return UFP4_ERR_INVALID;
-    if (!valid_workspace(workspace, workspace_bytes)) return UFP4_ERR_INVALID;
-    std::vector<QuantLaunch> qr, qc;
-    for (int32_t j = 0; j < n; ++j) {
-        const ufp4_dual_job &d = jobs[j];
-        if (d.reserved != 0 || d.p_row.colwise != 0 || d.p_col.colwise != 1) return UFP4_ERR_INVALID;
-        if (d.p_row.grid == UFP4_MXFP4 || d.p_col.grid == UFP4_MXFP4) return UFP4_ERR_UNSUPPORTED;
-        QuantLaunch r, c;
-        ufp4_status st = check_quant_args(d.x, d.dtype, d.rows, d.cols, d.ld, &d.p_row, &d.out_row, &r);
-        if (st != UFP4_OK) return st;
-        st = check_quant_args(d.x, d.dtype, d.rows, d.cols, d.ld, &d.p_col, &d.out_col, &c);
-        if (st != UFP4_OK) return st;
-        if (d.rows == 0 || d.cols == 0) continue;
-        qr.push_back(r);
-        qc.push_back(c);
-    }
-    if (qr.empty()) return UFP4_OK;
-    return from_cuda(launch_quantize_dual_batch(qr.data(), qc.data(), (int)qr.size(), workspace,
-                                                reinterpret_cast<cudaStream_t>(stream)));
-}
-
 ufp4_status ufp4_check(const void *workspace, ufp4_stream_t stream) {
     if (workspace && !aligned(workspace, 16)) return UFP4_ERR_INVALID;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

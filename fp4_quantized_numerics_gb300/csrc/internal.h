@@ -15,14 +15,6 @@ constexpr int kMaxPartials = 4096;
 constexpr size_t kWsStats = 32768;         // double partial sums, 8 per CTA
 constexpr int kMaxStatsCtas = 1024;
 constexpr size_t kWorkspaceBytes = kWsStats + size_t(kMaxStatsCtas) * 8 * sizeof(double);
-// A batched dual quantization (which takes no statistics) also uses the
-// statistics area: a second partial-maximum area at kWsStats and, after it,
-// one control block of kBatchCtlWords uint32 per tensor.
-constexpr int kMaxDualBatch = 32;
-constexpr size_t kWsBatchCtl = kWsStats + size_t(kMaxPartials) * sizeof(float);
-constexpr uint32_t kBatchCtlWords = 256;
-static_assert(kWsBatchCtl + size_t(kMaxDualBatch) * kBatchCtlWords * sizeof(uint32_t) <= kWorkspaceBytes,
-              "the control blocks fit the workspace");
 
 struct QuantLaunch {
     const void *x;
@@ -37,7 +29,6 @@ struct QuantLaunch {
     float *tensor_scale;
     int64_t out_rows, k;       // result shape
     uint64_t elem_base;        // SR element offset (grouped segments)
-    int status_or = 0;         // 1: only raise the workspace's status flag, never clear it
 };
 
 int num_sms();
@@ -111,14 +102,6 @@ bool make_input_tile_map(void *tmap, const void *x, int64_t rows, int64_t cols, 
 // over x (falls back to two passes when the parameters or the layout do not
 // allow it).
 cudaError_t launch_quantize_dual(const QuantLaunch &qr, const QuantLaunch &qc, void *ws, cudaStream_t s);
-
-// Both orientations of n tensors, in order, each result equal to its own
-// launch_quantize_dual.  The workspace's status flag is cleared once and
-// raised by any tensor's non-finite maximum.  Where tensor j and tensor
-// j + 1 both take the tile route and j + 1 has the transform on and needs
-// its maxima, j + 1's amax pass runs inside j's quantization launch.
-cudaError_t launch_quantize_dual_batch(const QuantLaunch *qr, const QuantLaunch *qc, int n, void *ws,
-                                       cudaStream_t s);
 
 // Grouped quantization: x holds segments in row order; ws keeps one fp32
 // maximum per segment and the status word.

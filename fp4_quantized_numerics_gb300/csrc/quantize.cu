@@ -57,7 +57,6 @@ struct Args {
     float *partials_out;
     int n_partials;
     uint32_t *status;
-    uint32_t status_or;         // 1: the pass only raises the status flag (batched calls)
     uint8_t *codes, *scales;
     uint8_t *eplane;            // E1M2 correction plane beside the codes, or null
     float *tensor_scale;
@@ -170,7 +169,7 @@ __device__ __forceinline__ void tensor_scale_prologue(const Args &a, float qmax,
     if (fold) kfold *= 0.00390625f;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         if (a.tensor_scale) *a.tensor_scale = sd;
-        if (a.status && (!a.status_or || !isfinite(A_t))) *a.status = (isfinite(A_t) ? 0u : 1u);
+        if (a.status) *a.status = (isfinite(A_t) ? 0u : 1u);
     }
     for (int c = threadIdx.x; c < 256; c += blockDim.x) {
         const float d = e4m3_to_f32((uint32_t)c);
@@ -1397,49 +1396,18 @@ __device__ __forceinline__ void mma_bf16(const uint32_t (&a)[4], uint32_t b0, ui
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
-// Where the chunks of an amax loop come from: a fixed stride over the CTAs,
-// or one at a time from a counter in global memory that several CTAs share;
-// kNoChunk once exhausted (and from then on).  The shared source's claims
-// are made by thread 0 and published in `slot` (one word per ring stage).
-constexpr uint32_t kNoChunk = 0xFFFFFFFFu;
-struct StrideChunks {
-    static constexpr bool kShared = false;
-    uint32_t first, stride, n;
-    __device__ __forceinline__ uint32_t at(uint32_t jj, const volatile uint32_t *) const {
-        const uint64_t i = first + (uint64_t)jj * stride;
-        return i < n ? (uint32_t)i : kNoChunk;
-    }
-    __device__ __forceinline__ uint32_t claim() const { return kNoChunk; }
-};
-struct SharedChunks {
-    static constexpr bool kShared = true;
-    uint32_t *next, n;
-    __device__ __forceinline__ uint32_t at(uint32_t jj, const volatile uint32_t *slot) const {
-        return slot[jj % kMmaRing];
-    }
-    __device__ __forceinline__ uint32_t claim() const {
-        const uint32_t i = atomicAdd(next, 1u);
-        return i < n ? i : kNoChunk;
-    }
-};
-
-// The amax pass over the chunks of `src`, staged in `dsm` (kMmaSmem bytes);
-// folds this thread's maxima of |y| (unscaled) into mr (row-wise blocks)
-// and mc (column-wise blocks).
-template <bool ROW, bool COL, class Src>
-__device__ __forceinline__ void amax_mma_loop(const Args &ar, const Args &ac, uint32_t ncc, const Src &src,
-                                              uint8_t *dsm, float &mr, float &mc) {
+template <bool ROW, bool COL>
+__global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_amax_mma(Args ar, Args ac, uint32_t ncc,
+                                                                      uint32_t nchunks) {
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ float s_red[kThreads / 32], s_red2[kThreads / 32];
     const Args &a = ROW ? ar : ac;   // the input as stored (both describe the same x)
     const uint32_t buf = ptx::smem_u32(dsm);
     const uint32_t bars = buf + kMmaRing * kMmaStage;
-    volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(dsm + kMmaRing * kMmaStage + 32);
     volatile int *abort = reinterpret_cast<volatile int *>(dsm + kMmaRing * kMmaStage + 60);
-    static_assert(kMmaRing * 8 <= 32 && 32 + kMmaRing * 4 <= 60, "barriers, slots and flag fit 64 bytes");
     if (threadIdx.x == 0) {
         for (int t = 0; t < kMmaRing; ++t) ptx::mbar_init(bars + 8u * t, 1);
         *abort = 0;
-        if (Src::kShared)
-            for (int t = 0; t < kMmaRing; ++t) slot[t] = src.claim();
         ptx::fence_mbar_init();
     }
     __syncthreads();
@@ -1449,17 +1417,17 @@ __device__ __forceinline__ void amax_mma_loop(const Args &ar, const Args &ac, ui
     // each; thread 0 also posts the chunk's byte count (the barrier's phase
     // needs that single arrival, so copies may land before or after it).
     auto issue = [&](uint32_t jj) {
-        const uint32_t i = src.at(jj, slot);
-        if (i == kNoChunk) return;
+        const uint32_t i = blockIdx.x + jj * gridDim.x;
+        if (i >= nchunks) return;
         const uint32_t kb = i / ncc, cc = i - kb * ncc;
         const uint32_t c0 = cc * kMmaCW, r0 = kb * 16;
         const uint32_t ncols = min(kMmaCW, cols - c0), nrows = min(16u, rows - r0);
         const uint32_t bar = bars + 8u * (jj % kMmaRing);
         const uint32_t st = buf + (jj % kMmaRing) * kMmaStage;
         if (threadIdx.x == 0) ptx::mbar_arrive_expect_tx(bar, nrows * ncols * 2);
-        const __nv_bfloat16 *src_x = static_cast<const __nv_bfloat16 *>(a.x) + (int64_t)r0 * a.ld + c0;
+        const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(a.x) + (int64_t)r0 * a.ld + c0;
         for (uint32_t q = 2 * (threadIdx.x >> 5); q < min(nrows, 2 * (threadIdx.x >> 5) + 2); ++q)
-            ptx::bulk_load(st + q * kMmaPitch, src_x + (int64_t)q * a.ld, ncols * 2, bar);
+            ptx::bulk_load(st + q * kMmaPitch, src + (int64_t)q * a.ld, ncols * 2, bar);
         issued = jj + 1;
     };
     if ((threadIdx.x & 31) == 0)
@@ -1475,13 +1443,14 @@ __device__ __forceinline__ void amax_mma_loop(const Args &ar, const Args &ac, ui
     const uint32_t bl0 = bv(n0, k0) | (bv(n0, k0 + 1) << 16), bl1 = bv(n0, k0 + 8) | (bv(n0, k0 + 9) << 16);
     const uint32_t bh0 = bv(n0 + 8, k0) | (bv(n0 + 8, k0 + 1) << 16);
     const uint32_t bh1 = bv(n0 + 8, k0 + 8) | (bv(n0 + 8, k0 + 9) << 16);
+    float mr = 0.0f, mc = 0.0f;
     // running max of |D| over the A rows that hold data (rows m = lane / 4 and lane / 4 + 8)
     auto acc = [&](float &m, const float (&d)[4], const float (&e)[4], bool lo_ok, bool hi_ok) {
         if (lo_ok) m = max_nan(max_nan(m, max_nan(fabsf(d[0]), fabsf(d[1]))), max_nan(fabsf(e[0]), fabsf(e[1])));
         if (hi_ok) m = max_nan(max_nan(m, max_nan(fabsf(d[2]), fabsf(d[3]))), max_nan(fabsf(e[2]), fabsf(e[3])));
     };
     auto process = [&](uint32_t jj) {
-        const uint32_t i = src.at(jj, slot);
+        const uint32_t i = blockIdx.x + jj * gridDim.x;
         const uint32_t kb = i / ncc, cc = i - kb * ncc;
         const uint32_t c0 = cc * kMmaCW, r0 = kb * 16;
         const uint32_t ncols = min(kMmaCW, cols - c0), nrows = min(16u, rows - r0);
@@ -1519,10 +1488,8 @@ __device__ __forceinline__ void amax_mma_loop(const Args &ar, const Args &ac, ui
         }
     };
     bool ok = true;
-    // (every thread reads the same chunk indices: computed, or published in
-    // `slot` before the barrier that precedes their use)
-    while (src.at(j, slot) != kNoChunk) {
-        const uint32_t nj = src.at(j + 1, slot) != kNoChunk ? 2u : 1u;
+    while (j < nchunks && blockIdx.x + j * gridDim.x < nchunks) {
+        const uint32_t nj = (blockIdx.x + (j + 1) * gridDim.x < nchunks) ? 2u : 1u;
         bool mine = true;
         for (uint32_t t = 0; t < nj && mine; ++t)
             mine = ptx::mbar_wait_bounded(bars + 8u * ((j + t) % kMmaRing), ((j + t) / kMmaRing) & 1u, kRingWait);
@@ -1531,11 +1498,6 @@ __device__ __forceinline__ void amax_mma_loop(const Args &ar, const Args &ac, ui
             for (uint32_t t = 0; t < nj; ++t) process(j + t);
         __syncthreads();
         if (*abort) { ok = false; break; }
-        if (Src::kShared) {
-            if (threadIdx.x == 0)
-                for (uint32_t t = 0; t < nj; ++t) slot[(j + t) % kMmaRing] = src.claim();
-            __syncthreads();
-        }
         if ((threadIdx.x & 31) == 0)
             for (uint32_t t = 0; t < nj; ++t) issue(j + t + kMmaRing);
         j += nj;
@@ -1547,33 +1509,18 @@ __device__ __forceinline__ void amax_mma_loop(const Args &ar, const Args &ac, ui
             for (uint32_t h = j; h < issued; ++h)
                 if (!ptx::mbar_wait_bounded(bars + 8u * (h % kMmaRing), (h / kMmaRing) & 1u, kRingWait)) break;
     }
-}
-
-// The CTA's maxima (x 1/4: the transform's normalisation) as its partials.
-__device__ __forceinline__ void amax_partials_out(const Args &ar, const Args &ac, bool row, bool col, uint32_t cta,
-                                                  float mr, float mc, float *s_red, float *s_red2) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
         mr = max_nan(mr, __shfl_xor_sync(0xffffffffu, mr, o));
         mc = max_nan(mc, __shfl_xor_sync(0xffffffffu, mc, o));
     }
-    if ((threadIdx.x & 31) == 0) { s_red[threadIdx.x >> 5] = mr; s_red2[threadIdx.x >> 5] = mc; }
+    if (lane == 0) { s_red[warp] = mr; s_red2[warp] = mc; }
     __syncthreads();
     if (threadIdx.x == 0) {
         for (int w = 1; w < kThreads / 32; ++w) { mr = max_nan(mr, s_red[w]); mc = max_nan(mc, s_red2[w]); }
-        if (row) ar.partials_out[cta] = mr * 0.25f;
-        if (col) ac.partials_out[cta] = mc * 0.25f;
+        if (ROW) ar.partials_out[blockIdx.x] = mr * 0.25f;
+        if (COL) ac.partials_out[blockIdx.x] = mc * 0.25f;
     }
-}
-
-template <bool ROW, bool COL>
-__global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_amax_mma(Args ar, Args ac, uint32_t ncc,
-                                                                      uint32_t nchunks) {
-    extern __shared__ __align__(128) uint8_t dsm[];
-    __shared__ float s_red[kThreads / 32], s_red2[kThreads / 32];
-    float mr = 0.0f, mc = 0.0f;
-    amax_mma_loop<ROW, COL>(ar, ac, ncc, StrideChunks{blockIdx.x, gridDim.x, nchunks}, dsm, mr, mc);
-    amax_partials_out(ar, ac, ROW, COL, blockIdx.x, mr, mc, s_red, s_red2);
 }
 
 // ================================================ dual orientation (X and X^T)
@@ -1866,92 +1813,53 @@ __device__ __forceinline__ void dual_padding(const Args &ar, const Args &ac, con
     zero_pad_rows(ac);   // column-wise padding blocks come from zero-filled tile rows
 }
 
-// Where the tiles of a dual tile loop come from: a fixed stride (tiles
-// first, first + stride, ... below n), or one at a time from a counter in
-// global memory that several CTAs share (a CTA that joins late takes what is
-// left).  kNoTile once the tiles are exhausted; a claim never returns a tile
-// after returning kNoTile.
-constexpr uint32_t kNoTile = 0xFFFFFFFFu;
-struct StrideTiles {
-    uint32_t first, stride, n;
-    __device__ __forceinline__ uint32_t claim(uint32_t jj) const {
-        const uint64_t i = first + (uint64_t)jj * stride;
-        return i < n ? (uint32_t)i : kNoTile;
-    }
-};
-struct SharedTiles {
-    uint32_t *next, n;
-    __device__ __forceinline__ uint32_t claim(uint32_t) const {
-        const uint32_t i = atomicAdd(next, 1u);
-        return i < n ? i : kNoTile;
-    }
-};
-
-// The quantization loop of the dual tile kernels: tiles from `src` through
-// a 3-deep TMA ring in dsm (kTileSmem bytes).  Thread 0 claims each ring
-// slot's tile as it refills the slot and records it in the ring's control
-// area before arriving on the slot's barrier, so every thread reads the
-// same tile (or kNoTile, with no copy in flight) after its wait.  The
-// tensor scales and multiplier tables are computed by dual_tile_scales while
-// the first copies are in flight.
 template <int GRID, int ROUND, bool RHT>
-__device__ __forceinline__ void dual_tile_scales(const Args &ar, const Args &ac, float *s_kr, float *s_kc,
-                                                 float *s_red, float &Sr, float &Sc, bool &fr, bool &fc) {
-    const float qmax = GRID == kE2M1 ? 6.0f : ar.uqmax;
-    float amr = 0.0f, amc = 0.0f;
-    tensor_scale_prologue(ar, qmax, RHT ? 0.25f : 1.0f, s_kr, s_red, Sr, GRID == kE1M2 && ROUND == kRTNE, &fr, &amr);
-    tensor_scale_prologue(ac, qmax, RHT ? 0.25f : 1.0f, s_kc, s_red, Sc, GRID == kE1M2 && ROUND == kRTNE, &fc, &amc);
-    if (blockIdx.x == 0 && threadIdx.x == 0 && ar.status && !isfinite(amc)) *ar.status = 1u;
-}
-
-template <int GRID, int ROUND, bool RHT, class Src>
-__device__ __forceinline__ void dual_tile_loop(const CUtensorMap *tmx, const Args &ar, const Args &ac, uint32_t nct,
-                                               const Src &src, uint8_t *dsm, float *s_kr, float *s_kc,
-                                               float *s_red) {
+__global__ void __launch_bounds__(kThreads, kStagedMinCtas)
+    k_dual_tile(const __grid_constant__ CUtensorMap tmx, Args ar, Args ac, uint32_t nct, uint32_t ntiles) {
     constexpr int kRing = ring_depth<false>();
+    extern __shared__ __align__(128) uint8_t dsm[];
+    __shared__ float s_kr[256], s_kc[256];
+    __shared__ float s_red[kThreads / 32];
     const RingCtl ring = ring_init<kRing>(dsm);
-    volatile uint32_t *slot = reinterpret_cast<volatile uint32_t *>(dsm + kRing * kChunk + 32);
-    static_assert(kRing * 8 <= 32 && 32 + kRing * 4 <= 60, "slot tiles fit the ring's control area");
     uint8_t *stage_codes = dsm + kRing * kChunk + 64;            // [rb][cl] uint2
     uint8_t *stage_scales = stage_codes + 8 * kTileCols * 8;    // [rb][cl] byte
-    uint32_t issued = 0;
+    uint32_t issued = 0, j = 0;
     auto issue = [&](uint32_t jj) {
-        const uint32_t i = src.claim(jj);
-        const uint32_t bar = ring.bars + 8u * (jj % kRing);
-        slot[jj % kRing] = i;
-        if (i == kNoTile) {
-            ptx::mbar_arrive(bar);   // completes the phase: "no more tiles"
-            return;
-        }
+        const uint32_t i = blockIdx.x + jj * gridDim.x;
+        if (i >= ntiles) return;
         const uint32_t rt = i / nct, ct = i - rt * nct;
+        const uint32_t bar = ring.bars + 8u * (jj % kRing);
         ptx::mbar_arrive_expect_tx(bar, kTileBytes);   // out-of-range elements arrive as zeros
-        ptx::tma_load_2d(ring.buf + (jj % kRing) * kChunk, tmx, (int32_t)(ct * kTileCols),
+        ptx::tma_load_2d(ring.buf + (jj % kRing) * kChunk, &tmx, (int32_t)(ct * kTileCols),
                          (int32_t)(rt * kTileRows), bar);
         issued = jj + 1;
     };
     if (threadIdx.x == 0) {
-        ptx::prefetch_tmap(tmx);
+        ptx::prefetch_tmap(&tmx);
         for (uint32_t t = 0; t < kRing; ++t) issue(t);
     }
+    const float qmax = GRID == kE2M1 ? 6.0f : ar.uqmax;
     float Sr = 1.0f, Sc = 1.0f;
     bool fr = false, fc = false;
-    dual_tile_scales<GRID, ROUND, RHT>(ar, ac, s_kr, s_kc, s_red, Sr, Sc, fr, fc);
+    float amr = 0.0f, amc = 0.0f;
+    tensor_scale_prologue(ar, qmax, RHT ? 0.25f : 1.0f, s_kr, s_red, Sr, GRID == kE1M2 && ROUND == kRTNE, &fr, &amr);
+    tensor_scale_prologue(ac, qmax, RHT ? 0.25f : 1.0f, s_kc, s_red, Sc, GRID == kE1M2 && ROUND == kRTNE, &fc, &amc);
+    if (blockIdx.x == 0 && threadIdx.x == 0 && ar.status && !isfinite(amc)) *ar.status = 1u;
     const uint32_t smask = RHT ? rht_sign_mask(ar.rht_seed) : 0u;
     const Signs sgr = row_signs<__nv_bfloat16>(smask), sgc = col_signs<__nv_bfloat16>(smask);
+    const uint32_t nloc = ntiles > blockIdx.x ? (ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     const DualGeom g = dual_geom(ar, ac);
     bool ok = true;
-    uint32_t j = 0;
-    for (;; ++j) {
+    for (; j < nloc; ++j) {
         // each thread waits for the tile itself; no CTA barrier before the work
         const bool mine = ring_wait_own<kRing>(ring, j);
-        const uint32_t i = slot[j % kRing];
+        const uint32_t i = blockIdx.x + j * gridDim.x;
         const uint32_t rt = i / nct, ct = i - rt * nct;
-        if (mine && i != kNoTile)
+        if (mine)
             dual_tile_quant<GRID, ROUND, RHT, true>(ar, ac, g, ring.buf + (j % kRing) * kChunk, rt, ct, sgr, sgc, Sr,
                                                     Sc, s_kr, s_kc, fr, fc, stage_codes, stage_scales);
         __syncthreads();   // tile consumed; column-wise results staged
         if (*ring.abort) { ok = false; break; }
-        if (i == kNoTile) break;   // (no abort: every thread read the same slot)
         if (threadIdx.x == 0) issue(j + kRing);
         dual_tile_flush(ac, g, rt, ct, stage_codes, stage_scales);
         __syncthreads();   // staging buffers free for the next tile
@@ -1960,76 +1868,8 @@ __device__ __forceinline__ void dual_tile_loop(const CUtensorMap *tmx, const Arg
         if (threadIdx.x == 0) atomicOr(&g_quant_timeout, 1u);
         ring_drain<kRing>(ring, j, issued);
     }
+    dual_padding(ar, ac, g);
 }
-
-template <int GRID, int ROUND, bool RHT>
-__global__ void __launch_bounds__(kThreads, kStagedMinCtas)
-    k_dual_tile(const __grid_constant__ CUtensorMap tmx, Args ar, Args ac, uint32_t nct, uint32_t ntiles) {
-    extern __shared__ __align__(128) uint8_t dsm[];
-    __shared__ float s_kr[256], s_kc[256];
-    __shared__ float s_red[kThreads / 32];
-    dual_tile_loop<GRID, ROUND, RHT>(&tmx, ar, ac, nct, StrideTiles{blockIdx.x, gridDim.x, ntiles}, dsm, s_kr, s_kc,
-                                     s_red);
-    dual_padding(ar, ac, dual_geom(ar, ac));
-}
-
-// Control block of one k_dual_tile_amax launch in device memory (zeroed
-// before the launch): the next quantization tile, the next amax chunk, and
-// per SM the number of the launch's CTAs that have started there.
-constexpr uint32_t kCtlTile = 0, kCtlChunk = 1, kCtlSm = 2, kCtlMaxSmid = kBatchCtlWords - kCtlSm;
-
-// The quantization pass of one tensor (k_dual_tile's work) and the
-// tensor-amax pass of the next one (k_amax_mma<true, true>'s work, both
-// orientations of x_next) in one launch, so that the amax pass, which
-// streams at HBM speed with little arithmetic, runs beside a quantization
-// pass that is bound by instruction issue.  The first CTA to start on each
-// SM begins with the amax chunks, every other CTA with the quantization
-// tiles; both kinds of work are claimed one unit at a time from counters in
-// `ctl`, and a CTA whose kind runs out takes what is left of the other, so
-// neither the CTAs' placement nor the two passes' relative speed leaves SMs
-// idle.  Every CTA writes its partial maxima of x_next to
-// br / bc.partials_out[blockIdx.x] (zero if it took no chunk).  The amax
-// ring and the tile ring share dynamic shared memory: each ring has
-// consumed every copy it started when its loop returns, and its barriers
-// are invalidated before the other ring reuses the bytes.  Every result
-// equals that of the two separate launches.
-template <int GRID, int ROUND, bool RHT>
-__global__ void __launch_bounds__(kThreads, kStagedMinCtas)
-    k_dual_tile_amax(const __grid_constant__ CUtensorMap tmx, Args ar, Args ac, uint32_t nct, uint32_t ntiles,
-                     Args br, Args bc, uint32_t ncc, uint32_t nch, uint32_t *ctl) {
-    extern __shared__ __align__(128) uint8_t dsm[];
-    __shared__ float s_kr[256], s_kc[256];
-    __shared__ float s_red[kThreads / 32], s_red2[kThreads / 32];
-    __shared__ uint32_t s_amax_first;
-    if (threadIdx.x == 0) {
-        uint32_t smid;
-        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-        s_amax_first = smid < kCtlMaxSmid && atomicAdd(ctl + kCtlSm + smid, 1u) == 0u;
-    }
-    __syncthreads();
-    const bool amax_first = s_amax_first != 0;
-    const SharedChunks chunks{ctl + kCtlChunk, nch};
-    float mr = 0.0f, mc = 0.0f;
-    auto release = [&](uint32_t bars, int n) {   // a ring's barriers, before its bytes are reused
-        if (threadIdx.x == 0)
-            for (int t = 0; t < n; ++t) ptx::mbar_inval(bars + 8u * t);
-        ptx::fence_proxy_async();   // this CTA's generic accesses before the next ring's copies
-        __syncthreads();
-    };
-    if (amax_first) {
-        amax_mma_loop<true, true>(br, bc, ncc, chunks, dsm, mr, mc);
-        release(ptx::smem_u32(dsm) + kMmaRing * kMmaStage, kMmaRing);
-    }
-    dual_tile_loop<GRID, ROUND, RHT>(&tmx, ar, ac, nct, SharedTiles{ctl + kCtlTile, ntiles}, dsm, s_kr, s_kc,
-                                     s_red);
-    if (!amax_first) {
-        release(ptx::smem_u32(dsm) + ring_depth<false>() * kChunk, ring_depth<false>());
-        amax_mma_loop<true, true>(br, bc, ncc, chunks, dsm, mr, mc);
-    }
-    amax_partials_out(br, bc, true, true, blockIdx.x, mr, mc, s_red, s_red2);
-    dual_padding(ar, ac, dual_geom(ar, ac));
-}
-constexpr uint32_t kTileAmaxSmem = kTileSmem > kMmaSmem ? kTileSmem : kMmaSmem;
 
 // ======================================== on-chip single pass (dual, BF16)
 // For a tensor that fits in the GPU's shared memory (up to kResidentMax
@@ -3048,22 +2888,18 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t *codes, cons
 // ================================================================ dispatch
 // Launch of a staged kernel: opt in to the ring's dynamic shared memory once
 // per kernel, persistent grid of the CTAs that fit at once.
-template <class K>
-cudaError_t opt_in_smem(K kern, size_t smem) {
-    static std::mutex mu;
-    static std::vector<const void *> done;
-    std::lock_guard<std::mutex> lock(mu);
-    if (std::find(done.begin(), done.end(), (const void *)kern) == done.end()) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        done.push_back((const void *)kern);
-    }
-    return cudaSuccess;
-}
 template <class K, class... P>
 cudaError_t launch_staged_smem(K kern, size_t smem, int64_t work_ctas, int *grid_out, cudaStream_t s, P... args) {
-    cudaError_t e = opt_in_smem(kern, smem);
-    if (e != cudaSuccess) return e;
+    static std::mutex mu;
+    static std::vector<const void *> done;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (std::find(done.begin(), done.end(), (const void *)kern) == done.end()) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            done.push_back((const void *)kern);
+        }
+    }
     const int g = resident_grid(kern, work_ctas, smem);
     if (grid_out) *grid_out = g;
     kern<<<g, kThreads, smem, s>>>(args...);
@@ -3206,92 +3042,6 @@ cudaError_t launch_resident(K kern, uint32_t grid, uint32_t *arrive, cudaStream_
 // Both orientations of one tensor from one read per pass (k_dual_staged).
 // The row-wise and column-wise partial maxima take the two halves of the
 // workspace's partial area.
-// Partial-maximum areas of the workspace: area 0 at kWsPartials, area 1 at
-// kWsStats (statistics partial sums live there only within a statistics
-// call).  Each holds the row-wise partials in its first half and the
-// column-wise ones in its second.
-float *partial_area(void *ws, int area) {
-    return reinterpret_cast<float *>(static_cast<char *>(ws) + (area ? kWsStats : kWsPartials));
-}
-static_assert(kWsStats + kMaxPartials * sizeof(float) <= kWorkspaceBytes, "area 1 fits the workspace");
-static_assert(kWsPartials + kMaxPartials * sizeof(float) <= kWsStats, "area 0 ends before area 1");
-
-// Both orientations' tensor-amax pass of a BF16 tensor on the tile route,
-// into `area`; points ar / ac at the partials.  The pass streams with little
-// arithmetic: 16-row x 1 KB chunks (contiguous kilobyte rows) read faster
-// than 128-byte tile rows, and the maxima do not depend on the traversal.
-cudaError_t dual_amax_pass(const QuantLaunch &qr, Args &ar, Args &ac, float *area, cudaStream_t s) {
-    constexpr uint32_t CW = kChunk / 32;
-    static_assert(CW == kMmaCW, "the tensor-core amax uses the same chunking");
-    const uint32_t ncc = (uint32_t)((ar.cols + CW - 1) / CW), nch = (uint32_t)(ar.rows / 16) * ncc;
-    ar.partials_out = area;
-    ac.partials_out = area + kMaxPartials / 2;
-    int g = 1;
-    cudaError_t e;
-    if (qr.rht) {
-        auto kern = k_amax_mma<true, true>;
-        if (resident_grid(kern, nch, kMmaSmem) > kMaxPartials / 2) return cudaErrorInvalidValue;
-        e = launch_staged_smem(kern, kMmaSmem, nch, &g, s, ar, ac, ncc, nch);
-    } else {
-        auto kern = k_dual_staged<__nv_bfloat16, 0, 0, false, true>;
-        if (resident_grid(kern, nch, ring_smem<true>()) > kMaxPartials / 2) return cudaErrorInvalidValue;
-        e = launch_staged<true>(kern, nch, &g, s, ar, ac, ncc, nch);
-    }
-    if (e != cudaSuccess) return e;
-    ar.partials = ar.partials_out;
-    ac.partials = ac.partials_out;
-    ar.n_partials = ac.n_partials = g;
-    return cudaSuccess;
-}
-
-// The quantization pass of the tile route (k_dual_tile).
-cudaError_t dual_tile_pass(const QuantLaunch &qr, const CUtensorMap &tm, uint32_t nct, uint32_t ntiles,
-                           const Args &ar, const Args &ac, cudaStream_t s) {
-    const int kgrid = qr.grid == kE2M1 ? kE2M1 : kE1M2;   // clamped E2M1 runs the uniform-grid kernels
-#define UFP4_T(GRID, ROUND, RHT)                                                                          \
-    if (kgrid == GRID && qr.round == ROUND && (qr.rht != 0) == RHT)                                       \
-        return launch_staged_smem(k_dual_tile<GRID, ROUND, RHT>, kTileSmem, ntiles, nullptr, s, tm, ar, ac, nct, \
-                                  ntiles);
-    UFP4_T(kE2M1, kRTNE, false) UFP4_T(kE2M1, kRTNE, true)
-    UFP4_T(kE2M1, kSR, false)   UFP4_T(kE2M1, kSR, true)
-    UFP4_T(kE1M2, kRTNE, false) UFP4_T(kE1M2, kRTNE, true)
-    UFP4_T(kE1M2, kSR, false)   UFP4_T(kE1M2, kSR, true)
-#undef UFP4_T
-    return cudaErrorInvalidValue;
-}
-
-// The quantization pass of the tile route with the transform-on amax pass
-// of the next tensor (br / bc, partials into area_b, one per CTA) in the
-// same launch (k_dual_tile_amax); ctl: its zeroed control block.  The grid
-// is the resident one.
-cudaError_t dual_tile_amax_pass(const QuantLaunch &qr, const CUtensorMap &tm, uint32_t nct, uint32_t ntiles,
-                                const Args &ar, const Args &ac, Args &br, Args &bc, float *area_b, uint32_t *ctl,
-                                cudaStream_t s) {
-    const uint32_t ncc = (uint32_t)((br.cols + kMmaCW - 1) / kMmaCW), nch = (uint32_t)(br.rows / 16) * ncc;
-    br.partials_out = area_b;
-    bc.partials_out = area_b + kMaxPartials / 2;
-    const int kgrid = qr.grid == kE2M1 ? kE2M1 : kE1M2;
-#define UFP4_TA(GRID, ROUND, RHT)                                                                         \
-    if (kgrid == GRID && qr.round == ROUND && (qr.rht != 0) == RHT) {                                    \
-        auto kern = k_dual_tile_amax<GRID, ROUND, RHT>;                                                  \
-        cudaError_t e = opt_in_smem(kern, kTileAmaxSmem);                                                \
-        if (e != cudaSuccess) return e;                                                                  \
-        const int g = resident_grid(kern, (int64_t)ntiles + nch, kTileAmaxSmem);                         \
-        if (g > kMaxPartials / 2) return cudaErrorInvalidValue;                                          \
-        kern<<<g, kThreads, kTileAmaxSmem, s>>>(tm, ar, ac, nct, ntiles, br, bc, ncc, nch, ctl);         \
-        br.partials = br.partials_out;                                                                   \
-        bc.partials = bc.partials_out;                                                                   \
-        br.n_partials = bc.n_partials = g;                                                               \
-        return cudaGetLastError();                                                                       \
-    }
-    UFP4_TA(kE2M1, kRTNE, false) UFP4_TA(kE2M1, kRTNE, true)
-    UFP4_TA(kE2M1, kSR, false)   UFP4_TA(kE2M1, kSR, true)
-    UFP4_TA(kE1M2, kRTNE, false) UFP4_TA(kE1M2, kRTNE, true)
-    UFP4_TA(kE1M2, kSR, false)   UFP4_TA(kE1M2, kSR, true)
-#undef UFP4_TA
-    return cudaErrorInvalidValue;
-}
-
 template <class In>
 cudaError_t quantize_dual_typed(const QuantLaunch &qr, const QuantLaunch &qc, Args &ar, Args &ac, void *ws,
                                 cudaStream_t s) {
@@ -3330,10 +3080,42 @@ cudaError_t quantize_dual_typed(const QuantLaunch &qr, const QuantLaunch &qc, Ar
             }
         }
         if (!qr.amax_in || !qc.amax_in) {
-            cudaError_t e = dual_amax_pass(qr, ar, ac, partial_area(ws, 0), s);
+            // the amax pass streams with little arithmetic: 16-row x 1 KB
+            // chunks (contiguous kilobyte rows) read faster than 128-byte
+            // tile rows, and the maxima do not depend on the traversal
+            constexpr uint32_t CW = kChunk / 32;
+            const uint32_t ncc = (uint32_t)((ar.cols + CW - 1) / CW), nch = (uint32_t)(ar.rows / 16) * ncc;
+            ar.partials_out = reinterpret_cast<float *>(static_cast<char *>(ws) + kWsPartials);
+            ac.partials_out = ar.partials_out + kMaxPartials / 2;
+            int g = 1;
+            cudaError_t e;
+            if (qr.rht) {
+                // the tensor-core amax of both orientations (CW = kMmaCW: same chunking)
+                static_assert(CW == kMmaCW, "chunk widths");
+                auto kern = k_amax_mma<true, true>;
+                if (resident_grid(kern, nch, kMmaSmem) > kMaxPartials / 2) return cudaErrorInvalidValue;
+                e = launch_staged_smem(kern, kMmaSmem, nch, &g, s, ar, ac, ncc, nch);
+            } else {
+                auto kern = k_dual_staged<In, 0, 0, false, true>;
+                if (resident_grid(kern, nch, ring_smem<true>()) > kMaxPartials / 2) return cudaErrorInvalidValue;
+                e = launch_staged<true>(kern, nch, &g, s, ar, ac, ncc, nch);
+            }
             if (e != cudaSuccess) return e;
+            ar.partials = ar.partials_out;
+            ac.partials = ac.partials_out;
+            ar.n_partials = ac.n_partials = g;
         }
-        return dual_tile_pass(qr, tm, nct, ntiles, ar, ac, s);
+        const int kgrid = qr.grid == kE2M1 ? kE2M1 : kE1M2;   // clamped E2M1 runs the uniform-grid kernels
+#define UFP4_T(GRID, ROUND, RHT)                                                                          \
+        if (kgrid == GRID && qr.round == ROUND && (qr.rht != 0) == RHT)                                   \
+            return launch_staged_smem(k_dual_tile<GRID, ROUND, RHT>, kTileSmem, ntiles, nullptr, s, tm, ar,       \
+                                      ac, nct, ntiles);
+        UFP4_T(kE2M1, kRTNE, false) UFP4_T(kE2M1, kRTNE, true)
+        UFP4_T(kE2M1, kSR, false)   UFP4_T(kE2M1, kSR, true)
+        UFP4_T(kE1M2, kRTNE, false) UFP4_T(kE1M2, kRTNE, true)
+        UFP4_T(kE1M2, kSR, false)   UFP4_T(kE1M2, kSR, true)
+#undef UFP4_T
+        return cudaErrorInvalidValue;
     } else {
     constexpr uint32_t CW = kChunk / (16 * sizeof(In));
     const uint32_t ncc = (uint32_t)((ar.cols + CW - 1) / CW), nch = (uint32_t)(ar.rows / 16) * ncc;
@@ -3372,7 +3154,6 @@ Args make_args(const QuantLaunch &q, void *ws) {
     a.elem_base = q.elem_base;
     a.amax_in = q.amax_in;
     a.status = ws ? reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsStatus) : nullptr;
-    a.status_or = q.status_or;
     a.codes = q.codes; a.scales = q.scales; a.tensor_scale = q.tensor_scale;
     a.eplane = q.grid == kE1M2 ? q.eplane : nullptr;
     a.uqmax = q.grid == kE2M1C ? 2.0f : 3.5f;
@@ -3509,76 +3290,6 @@ cudaError_t launch_quantize_dual(const QuantLaunch &qr, const QuantLaunch &qc, v
     Args ar = make_args(qr, ws), ac = make_args(qc, ws);
     if (qr.dtype == 0) return quantize_dual_typed<__nv_bfloat16>(qr, qc, ar, ac, ws, s);
     return quantize_dual_typed<float>(qr, qc, ar, ac, ws, s);
-}
-
-// Which route launch_quantize_dual takes for a BF16 pair: the tile route
-// (an amax pass when a maximum is missing, then k_dual_tile) or another one
-// (the on-chip single pass, the staged FP32 kernels, two single passes).
-static bool dual_tile_route(const QuantLaunch &qr, const QuantLaunch &qc) {
-    const bool same = qr.grid == qc.grid && qr.round == qc.round && qr.rht == qc.rht &&
-                      (!qr.rht || qr.rht_seed == qc.rht_seed);
-    if (qr.dtype != 0 || !same || (qr.cols * 2) % 16 != 0 || qr.rows % 16 != 0) return false;
-    if (qr.amax_in || qc.amax_in) return true;
-    const int64_t nct = (qr.cols + kTileCols - 1) / kTileCols;
-    const int64_t ntiles = (qr.rows + kTileRows - 1) / kTileRows * nct;
-    const int64_t grid = std::min<int64_t>(num_sms(), ntiles);
-    return (ntiles + grid - 1) / grid > kResidentMax;   // else the on-chip single pass
-}
-
-cudaError_t launch_quantize_dual_batch(const QuantLaunch *qr, const QuantLaunch *qc, int n, void *ws,
-                                       cudaStream_t s) {
-    if (n < 0 || n > kMaxDualBatch) return cudaErrorInvalidValue;
-    // the status word and the launches' control blocks start at zero; every
-    // pass then only raises the flag
-    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), s);
-    if (e != cudaSuccess) return e;
-    e = cudaMemsetAsync(static_cast<char *>(ws) + kWsBatchCtl, 0, kMaxDualBatch * kBatchCtlWords * sizeof(uint32_t),
-                        s);
-    if (e != cudaSuccess) return e;
-    int area = 0;            // partial area of the tensor being quantized
-    bool have_amax = false;  // its amax pass ran inside the previous launch
-    Args pr{}, pc{};         // (then: its Args with the partials set)
-    for (int j = 0; j < n; ++j) {
-        QuantLaunch r = qr[j], c = qc[j];
-        r.status_or = c.status_or = 1;
-        if (!dual_tile_route(r, c)) {
-            e = launch_quantize_dual(r, c, ws, s);
-            if (e != cudaSuccess) return e;
-            continue;
-        }
-        Args ar = have_amax ? pr : make_args(r, ws), ac = have_amax ? pc : make_args(c, ws);
-        ac.status = nullptr;   // the row-wise prologue reports both
-        alignas(64) CUtensorMap tm;
-        if (!make_input_tile_map(&tm, ar.x, ar.rows, ar.cols, ar.ld, kTileCols, kTileRows))
-            return cudaErrorInvalidValue;
-        const uint32_t nct = (uint32_t)((ar.cols + kTileCols - 1) / kTileCols);
-        const uint32_t ntiles = (uint32_t)((ar.rows + kTileRows - 1) / kTileRows) * nct;
-        if (!have_amax && (!r.amax_in || !c.amax_in)) {
-            e = dual_amax_pass(r, ar, ac, partial_area(ws, area), s);
-            if (e != cudaSuccess) return e;
-        }
-        // the next tensor's amax pass (tensor cores, so the transform is on)
-        // joins this quantization pass
-        have_amax = false;
-        if (j + 1 < n) {
-            QuantLaunch r2 = qr[j + 1], c2 = qc[j + 1];
-            r2.status_or = c2.status_or = 1;
-            if (dual_tile_route(r2, c2) && r2.rht && (!r2.amax_in || !c2.amax_in)) {
-                pr = make_args(r2, ws);
-                pc = make_args(c2, ws);
-                uint32_t *ctl = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsBatchCtl) +
-                                (size_t)j * kBatchCtlWords;
-                e = dual_tile_amax_pass(r, tm, nct, ntiles, ar, ac, pr, pc, partial_area(ws, area ^ 1), ctl, s);
-                if (e != cudaSuccess) return e;
-                have_amax = true;
-                area ^= 1;
-                continue;
-            }
-        }
-        e = dual_tile_pass(r, tm, nct, ntiles, ar, ac, s);
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
 }
 
 cudaError_t launch_quantize_grouped(const QuantLaunch &q, const GroupQuant &gt, void *ws, cudaStream_t s) {

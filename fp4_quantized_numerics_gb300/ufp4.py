@@ -31,8 +31,7 @@ EXPORTED = ["ufp4_kpad", "ufp4_codes_bytes", "ufp4_scales_bytes", "ufp4_workspac
             "ufp4_quantize", "ufp4_check", "ufp4_dequantize", "ufp4_gemm", "ufp4_stats",
             "ufp4_status_string", "ufp4_quantize_noalloc", "ufp4_grouped_rows",
             "ufp4_grouped_kpad", "ufp4_quantize_grouped", "ufp4_gemm_grouped", "ufp4_quantize_dual",
-            "ufp4_gemm_amax", "ufp4_quantize_stats", "ufp4_quantize_grouped_dual",
-            "ufp4_quantize_dual_batch"]
+            "ufp4_gemm_amax", "ufp4_quantize_stats", "ufp4_quantize_grouped_dual"]
 
 
 class QParamsC(ctypes.Structure):
@@ -48,15 +47,6 @@ class QTensorC(ctypes.Structure):
                 ("tensor_scale", ctypes.c_void_p), ("rows", ctypes.c_int64),
                 ("k", ctypes.c_int64), ("grid", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("eplane", ctypes.c_void_p)]
-
-
-class DualJobC(ctypes.Structure):
-    _fields_ = [("x", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
-                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("ld", ctypes.c_int64),
-                ("p_row", QParamsC), ("p_col", QParamsC), ("out_row", QTensorC), ("out_col", QTensorC)]
-
-
-UFP4_MAX_DUAL_BATCH = 32
 
 
 class StatsC(ctypes.Structure):
@@ -103,8 +93,6 @@ def lib():
                                          ctypes.POINTER(QParamsC), ctypes.POINTER(QTensorC),
                                          ctypes.POINTER(QTensorC), vp, ctypes.c_size_t, vp]
         L.ufp4_quantize_dual.restype = ctypes.c_int
-        L.ufp4_quantize_dual_batch.argtypes = [ctypes.POINTER(DualJobC), ctypes.c_int32, vp, ctypes.c_size_t, vp]
-        L.ufp4_quantize_dual_batch.restype = ctypes.c_int
         L.ufp4_check.argtypes = [vp, vp]
         L.ufp4_check.restype = ctypes.c_int
         L.ufp4_dequantize.argtypes = [ctypes.POINTER(QTensorC), ctypes.c_int32, ctypes.c_uint64,
@@ -279,46 +267,6 @@ def ufp4_quantize_dual(x, grid, rht=False, rht_seed=0, round=UFP4_RTNE, sr_seed=
                                   ws.numel(), _stream(stream))
     _check(st, "ufp4_quantize_dual")
     return out_row, out_col
-
-
-def ufp4_quantize_dual_batch(jobs, ws=None, stream=None):
-    """Both orientations of several tensors in one call (ufp4_quantize_dual_batch).
-
-    jobs: sequence of dicts with the keyword arguments of ufp4_quantize_dual
-    (x and grid required; out_row / out_col optional).  Returns the list of
-    (out_row, out_col) pairs, each equal to its own ufp4_quantize_dual."""
-    arr = (DualJobC * max(len(jobs), 1))()
-    outs = []
-    dev = None
-    for i, job in enumerate(jobs):
-        job = dict(job)
-        x, grid = job.pop("x"), job.pop("grid")
-        _cuda(x, "x")
-        if x.dim() != 2 or x.stride(1) != 1:
-            raise ValueError("x must be 2-D with unit stride in its last dim")
-        rows, cols = x.shape
-        dev = x.device
-        out_row, out_col = job.pop("out_row", None), job.pop("out_col", None)
-        if out_row is None:
-            out_row = QTensor.empty(rows, cols, grid, x.device)
-        if out_col is None:
-            out_col = QTensor.empty(cols, rows, grid, x.device)
-        rht, rht_seed = job.pop("rht", False), job.pop("rht_seed", 0)
-        rnd, sr_seed = job.pop("round", UFP4_RTNE), job.pop("sr_seed", 0)
-        pr = qparams(grid, rht, rht_seed, rnd, sr_seed, job.pop("sr_counter_row", 0), False,
-                     job.pop("amax_row", None))
-        pc = qparams(grid, rht, rht_seed, rnd, sr_seed, job.pop("sr_counter_col", 0), True,
-                     job.pop("amax_col", None))
-        if job:
-            raise TypeError("unknown job keys: %s" % sorted(job))
-        arr[i] = DualJobC(x.data_ptr(), _dtype_code(x), 0, rows, cols, x.stride(0), pr, pc, out_row.c(),
-                          out_col.c())
-        outs.append((out_row, out_col))
-    if ws is None:
-        ws = workspace(dev)
-    st = lib().ufp4_quantize_dual_batch(arr, len(jobs), ws.data_ptr(), ws.numel(), _stream(stream))
-    _check(st, "ufp4_quantize_dual_batch")
-    return outs
 
 
 def ufp4_check(ws=None, stream=None):

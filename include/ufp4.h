@@ -235,46 +235,6 @@ UFP4_API ufp4_status ufp4_quantize_dual(const void *x, int32_t dtype, int64_t ro
                                         const ufp4_qtensor *out_row, const ufp4_qtensor *out_col,
                                         void *workspace, size_t workspace_bytes, ufp4_stream_t stream);
 
-/* One dual quantization request of ufp4_quantize_dual_batch: the arguments
- * of one ufp4_quantize_dual call (every field as there; out_row / out_col
- * name the caller's buffers).  `reserved` must be 0. */
-typedef struct ufp4_dual_job {
-    const void *x;
-    int32_t dtype;
-    int32_t reserved;
-    int64_t rows, cols, ld;
-    ufp4_qparams p_row, p_col;
-    ufp4_qtensor out_row, out_col;
-} ufp4_dual_job;
-
-#define UFP4_MAX_DUAL_BATCH 32
-
-/* The operand quantizations of a training step as one call: jobs[0..n-1],
- * each quantized in both orientations exactly as by its own
- * ufp4_quantize_dual (every code, scale, correction plane and tensor scale
- * bit for bit; the three training GEMMs consume every operand both ways,
- * [ZC] zhichai.net post, Key points "The fix -- UFP4").  What the call adds
- * is overlap between the tensors' passes: a tensor whose rows are 16-byte
- * multiples and too large for the on-chip single pass takes an amax pass
- * and a quantization pass; when jobs[j] and jobs[j+1] both take that route
- * and jobs[j+1] has the transform on and needs its maxima, jobs[j+1]'s amax
- * pass runs inside jobs[j]'s quantization launch -- the amax pass streams
- * at HBM speed while the quantization pass is bound by arithmetic, so
- * together they take less time than one after the other.  Put a tensor
- * with heavy arithmetic (stochastic rounding) right before the largest
- * tensor.  The order of the jobs changes no result.
- *   jobs      : host array of n (0 <= n <= UFP4_MAX_DUAL_BATCH) requests,
- *               each checked as ufp4_quantize_dual checks its arguments;
- *               zero-sized ones are skipped.  No job's output may overlap
- *               any job's input.
- *   workspace : required (workspace_bytes >= ufp4_workspace_bytes(), 16-byte
- *               aligned): the call clears its non-finite flag once, and the
- *               flag then reports any job's non-finite input (ufp4_check).
- * An invalid job returns UFP4_ERR_INVALID / UFP4_ERR_UNSUPPORTED before
- * anything is launched. */
-UFP4_API ufp4_status ufp4_quantize_dual_batch(const ufp4_dual_job *jobs, int32_t n, void *workspace,
-                                              size_t workspace_bytes, ufp4_stream_t stream);
-
 /* ufp4_quantize without a caller workspace, for callers that cannot
  * allocate device memory when they quantize (a frozen memory pool, a custom
  * allocator that owns all device memory, code that must not risk an

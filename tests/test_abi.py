@@ -263,57 +263,3 @@ def test_dual_and_grouped_reject_bad_arguments_on_host(L):
            ufp4.GemmGroupC(100, 64, 128, 0, 0, 0, 0, 0, 0, 0x4000, 32)]    # ldc < N
     for gg in bad:
         assert ggemm(a, b, [gg]) == INV, (gg.M, gg.K, gg.a_row, gg.a_k, gg.c, gg.ldc)
-
-
-def test_dual_batch_rejects_bad_arguments_on_host(L):
-    """ufp4_quantize_dual_batch checks every job as ufp4_quantize_dual does
-    and the batch itself (count, array, workspace) before any launch."""
-    from fp4_quantized_numerics_gb300 import ufp4
-    INV, UNS = ufp4.UFP4_ERR_INVALID, ufp4.UFP4_ERR_UNSUPPORTED
-    ws, x, wsb = 0x10000, 0x20000, L.ufp4_workspace_bytes()
-
-    def job(pr=None, pc=None, qr=None, qc=None, rows=64, cols=128, reserved=0):
-        return ufp4.DualJobC(x, 0, reserved, rows, cols, cols, pr or _q(), pc or _q(colwise=True),
-                             qr or _qt(rows, cols), qc or _qt(cols, rows))
-
-    def batch(jobs, n=None, w=ws, wb=wsb):
-        arr = (ufp4.DualJobC * max(len(jobs), 1))(*jobs)
-        return L.ufp4_quantize_dual_batch(arr if jobs or n else None, len(jobs) if n is None else n, w, wb, None)
-
-    good = job()
-    assert batch([good], n=-1) == INV                                     # negative count
-    assert batch([good] * 33) == INV                                      # beyond UFP4_MAX_DUAL_BATCH
-    assert L.ufp4_quantize_dual_batch(None, 1, ws, wsb, None) == INV     # no array
-    assert batch([good], w=0) == INV                                      # no workspace
-    assert batch([good], wb=wsb - 16) == INV                              # workspace too small
-    assert batch([good], w=ws + 8) == INV                                 # workspace alignment
-    assert batch([good, job(reserved=1)]) == INV                          # reserved field
-    assert batch([good, job(pr=_q(colwise=True))]) == INV                 # row params column-wise
-    assert batch([good, job(pc=_q())]) == INV                             # column params row-wise
-    assert batch([good, job(qc=_qt(64, 128))]) == INV                     # column result shape
-    assert batch([job(pr=_q(grid=3), pc=_q(grid=3, colwise=True), qr=_qt(64, 128, 3),
-                      qc=_qt(128, 64, 3))]) == UNS                        # MXFP4
-    assert batch([]) == ufp4.UFP4_OK                                      # nothing to do
-    assert batch([job(rows=0, qr=_qt(0, 128), qc=_qt(128, 0))]) == ufp4.UFP4_OK   # zero-sized only
-
-
-def test_dual_job_layout_matches_the_header(tmp_path):
-    """The binding's DualJobC has the C struct's size and field offsets (a C
-    program compiled against include/ufp4.h prints them)."""
-    import shutil
-    import subprocess
-    from fp4_quantized_numerics_gb300 import ufp4
-    cc = shutil.which("gcc") or shutil.which("cc")
-    if not cc:
-        pytest.skip("no C compiler")
-    fields = [f for f, _ in ufp4.DualJobC._fields_]
-    src = tmp_path / "layout.c"
-    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "ufp4.h"\nint main(void) {\n'
-                   '  printf("%zu\\n", sizeof(ufp4_dual_job));\n' +
-                   "".join('  printf("%%zu\\n", offsetof(ufp4_dual_job, %s));\n' % f for f in fields) +
-                   "  return 0;\n}\n")
-    exe = tmp_path / "layout"
-    subprocess.check_call([cc, "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
-    got = [int(v) for v in subprocess.check_output([str(exe)]).split()]
-    assert got[0] == ctypes.sizeof(ufp4.DualJobC)
-    assert got[1:] == [getattr(ufp4.DualJobC, f).offset for f in fields]
