@@ -51,8 +51,8 @@ def lib():
         L.ref_round_rtne.restype = ctypes.c_int
         L.ref_round_sr.argtypes = [ctypes.c_int, ctypes.c_float, ctypes.c_uint32]
         L.ref_round_sr.restype = ctypes.c_int
-        L.ref_sr_word.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64]
-        L.ref_sr_word.restype = ctypes.c_uint32
+        L.ref_sr_bits.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64]
+        L.ref_sr_bits.restype = ctypes.c_uint32
         vp = ctypes.c_void_p
         L.ref_quantize.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                    ctypes.c_int, ctypes.c_int, ctypes.c_uint64,
@@ -138,11 +138,13 @@ def round_rtne(grid, a):
 
 
 def round_sr(grid, a, r):
+    """SR of a >= 0 with the 16 random bits r (the low 16 bits are used)."""
     return lib().ref_round_sr(grid, float(a), int(r) & 0xFFFFFFFF)
 
 
-def sr_word(sr_seed, sr_counter, i):
-    return int(lib().ref_sr_word(sr_seed, sr_counter, i))
+def sr_bits(sr_seed, sr_counter, i):
+    """The 16 random bits of logical element i (see ref_sr_bits)."""
+    return int(lib().ref_sr_bits(sr_seed, sr_counter, i))
 
 
 # ------------------------------------------------------------------ tensors

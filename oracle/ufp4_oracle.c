@@ -192,8 +192,10 @@ int ref_round_rtne(int grid, float a)
 /* Stochastic rounding ([ZC] "The fix -- UFP4"; [HP] key contributions: SR on
  * dY only): with lo <= a < hi the neighbouring grid points, round up with
  * probability p = (a - lo)/(hi - lo).  READING: the Bernoulli draw compares
- * the top 24 bits of one Philox word, as u = (r >> 8) * 2^-24, against p;
- * both sides are exact in fp32, so the rounding is exactly unbiased. */
+ * a 16-bit uniform r (half of a Philox word, see ref_sr_bits) as
+ * u = r * 2^-16 against p, both exact in fp32: the round-up probability is p
+ * rounded up to a multiple of 2^-16, within 2^-16 of a grid step of the
+ * unbiased draw.  Only the low 16 bits of r are used. */
 int ref_round_sr(int grid, float a, uint32_t r)
 {
     const int top = ref_grid_levels(grid) - 1;
@@ -203,21 +205,23 @@ int ref_round_sr(int grid, float a, uint32_t r)
     const float lo = (float)ref_grid_value(grid, m);
     const float hi = (float)ref_grid_value(grid, m + 1);
     const float p = (a - lo) / (hi - lo);
-    const float u = (float)(r >> 8) * 0x1p-24f;
+    const float u = (float)(r & 0xFFFFu) * 0x1p-16f;
     return (u < p) ? m + 1 : m;
 }
 
-/* The Philox word that drives SR for logical element index i of the output
- * code buffer: key = sr_seed, counter = (i / 4, sr_counter), word i mod 4. */
-uint32_t ref_sr_word(uint64_t sr_seed, uint64_t sr_counter, uint64_t i)
+/* The 16 random bits that drive SR for logical element index i of the
+ * output code buffer: key = sr_seed, counter = (i / 8, sr_counter), and of
+ * the four words the call returns, word (i mod 8) / 2, its low half for
+ * even i and its high half for odd i. */
+uint32_t ref_sr_bits(uint64_t sr_seed, uint64_t sr_counter, uint64_t i)
 {
-    const uint64_t q = i >> 2;
+    const uint64_t q = i >> 3;
     const uint32_t ctr[4] = {(uint32_t)q, (uint32_t)(q >> 32),
                              (uint32_t)sr_counter, (uint32_t)(sr_counter >> 32)};
     const uint32_t key[2] = {(uint32_t)sr_seed, (uint32_t)(sr_seed >> 32)};
     uint32_t w[4];
     ref_philox4x32_10(ctr, key, w);
-    return w[i & 3];
+    return (w[(i >> 1) & 3] >> (16 * (unsigned)(i & 1))) & 0xFFFFu;
 }
 
 /* ------------------------------------------------------------------------
@@ -322,7 +326,7 @@ int ref_quantize_strided(const float *x, int64_t rows, int64_t k, int64_t ld,
                 int m;
                 if (round_mode == REF_SR) {
                     const uint64_t i = elem_base + (uint64_t)r * sr_row_stride + (uint64_t)(b * 16 + j);
-                    m = ref_round_sr(grid, a, ref_sr_word(sr_seed, sr_counter, i));
+                    m = ref_round_sr(grid, a, ref_sr_bits(sr_seed, sr_counter, i));
                 } else {
                     m = ref_round_rtne(grid, a);
                 }
@@ -519,7 +523,7 @@ int ref_quantize_mx(const float *x, int64_t rows, int64_t k, int64_t ld, int rht
                 int m;
                 if (round_mode == REF_SR) {
                     const uint64_t i = (uint64_t)r * (uint64_t)k + (uint64_t)(b * 32 + j);
-                    m = ref_round_sr(REF_E2M1, a, ref_sr_word(sr_seed, sr_counter, i));
+                    m = ref_round_sr(REF_E2M1, a, ref_sr_bits(sr_seed, sr_counter, i));
                 } else {
                     m = ref_round_rtne(REF_E2M1, a);
                 }

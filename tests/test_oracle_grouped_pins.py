@@ -51,7 +51,7 @@ def _brute_segment(oracle, M, grid, rnd, sr_seed, sr_counter, index_of):
                 q = F32(blk[j] * kk)
                 a = min(abs(float(q)), float(qmax))
                 if rnd == 1:
-                    m = oracle.round_sr(grid, a, oracle.sr_word(sr_seed, sr_counter, index_of(r, 16 * b + j)))
+                    m = oracle.round_sr(grid, a, oracle.sr_bits(sr_seed, sr_counter, index_of(r, 16 * b + j)))
                 else:
                     m = oracle.round_rtne(grid, a)
                 codes[r, 16 * b + j] = (8 if np.signbit(q) else 0) | m

@@ -37,14 +37,22 @@ def test_philox_known_answer_vectors(oracle):
         assert oracle.philox4x32_10(v[0:4], v[4:6]) == v[6:10]
 
 
-def test_sr_word_counter_layout(oracle):
-    # element i draws word i%4 of Philox(key=seed, ctr=(i//4, counter)).
+def test_sr_bits_counter_layout(oracle):
+    """Element i draws 16 bits: of Philox(key=seed, ctr=(i//8, counter)),
+    word (i%8)//2, low half for even i, high half for odd i.  Catches a wrong
+    counter split (i//4), word index or half order, and a dropped high word
+    of the 64-bit seed, counter or index."""
     seed, ctr = 0x0123456789ABCDEF, 0xFEDCBA9876543210
-    for i in [0, 1, 2, 3, 4, 7, 2**33 + 5]:
-        q = i >> 2
+    for i in [0, 1, 2, 3, 4, 5, 6, 7, 8, 15, 2**33 + 5, 2**35 + 14]:
+        q = i >> 3
         words = oracle.philox4x32_10([q & 0xFFFFFFFF, q >> 32, ctr & 0xFFFFFFFF, ctr >> 32],
                                      [seed & 0xFFFFFFFF, seed >> 32])
-        assert oracle.sr_word(seed, ctr, i) == words[i & 3]
+        want = (words[(i >> 1) & 3] >> (16 * (i & 1))) & 0xFFFF
+        assert oracle.sr_bits(seed, ctr, i) == want, i
+    # the eight elements of one counter use all 128 bits of the call, once
+    q = [oracle.sr_bits(seed, ctr, 8 + j) for j in range(8)]
+    words = oracle.philox4x32_10([1, 0, ctr & 0xFFFFFFFF, ctr >> 32], [seed & 0xFFFFFFFF, seed >> 32])
+    assert [q[2 * w] | (q[2 * w + 1] << 16) for w in range(4)] == words
 
 
 # ------------------------------------------------------------ Hadamard/RHT
@@ -281,10 +289,10 @@ def test_sr_is_unbiased_within_5_sigma(oracle, grid):
     g = np.random.default_rng(4)
     N = 4096
     for a in g.uniform(0, qmax, 24).astype(np.float32):
-        m0 = oracle.round_sr(grid, a, 0xFFFFFFFF)  # never rounds up: the floor
+        m0 = oracle.round_sr(grid, a, 0xFFFF)  # u = 1 - 2^-16: the floor unless p > u
         lo = oracle.grid_value(grid, m0)
         hi = oracle.grid_value(grid, min(m0 + 1, oracle.grid_levels(grid) - 1))
-        vals = [oracle.grid_value(grid, oracle.round_sr(grid, a, oracle.sr_word(3, 0, i)))
+        vals = [oracle.grid_value(grid, oracle.round_sr(grid, a, oracle.sr_bits(3, 0, i)))
                 for i in range(N)]
         p = (float(a) - lo) / (hi - lo) if hi > lo else 0.0
         sigma = (hi - lo) * math.sqrt(max(p * (1 - p), 1e-12) / N)
@@ -296,11 +304,16 @@ def test_sr_exact_points_and_edges(oracle):
     for grid in (0, 1, 2):
         for m in range(oracle.grid_levels(grid)):
             v = oracle.grid_value(grid, m)
-            for r in (0, 0x7FFFFFFF, 0xFFFFFFFF):
+            for r in (0, 0x7FFF, 0xFFFF):
                 assert oracle.round_sr(grid, v, r) == m
     # r = 0 gives u = 0 < p for any p > 0: always rounds up off-grid
     assert oracle.round_sr(1, 0.1, 0) == 1
-    assert oracle.round_sr(1, 0.1, 0xFFFFFFFF) == 0
+    assert oracle.round_sr(1, 0.1, 0xFFFF) == 0
+    # the draw's resolution: p = 0.2 exactly between the E1M2 points 0 and 0.5
+    # (a = 0.1) rounds up for r < ceil(0.2 * 2^16) = 13108, and only the low
+    # 16 bits of r count
+    assert oracle.round_sr(1, 0.1, 13107) == 1 and oracle.round_sr(1, 0.1, 13108) == 0
+    assert oracle.round_sr(1, 0.1, 0xABCD0000 | 13107) == 1
 
 
 # -------------------------------------------------- quantization end to end
