@@ -125,44 +125,44 @@ __device__ __forceinline__ uint32_t e1m2_rn(float q, float top = 7.0f) {
     return m | ((__float_as_uint(q) >> 28) & 8u);
 }
 
-// Stochastic rounding of q (in grid units) with 32 random bits r: floor to
-// the grid point below |q| (clamped to qmax), then up with probability
-// p = (a - lo) / (hi - lo) against u = (r >> 8) * 2^-24.  Returns the code.
+// Stochastic rounding of q (in grid units) with 16 random bits r (< 2^16):
+// floor to the grid point below |q| (clamped to qmax), then up with
+// probability p = (a - lo) / (hi - lo) against u = r * 2^-16.  Returns the code.
 template <int GRID>
 __device__ __forceinline__ uint32_t sr_code(float q, uint32_t r, uint32_t top = 7u) {
-    // The decision "up iff (r >> 8) 2^-24 < p", p the position of |q| between
-    // its grid neighbours, is taken in fixed point: with t = |q| scaled so
-    // that the neighbours are consecutive integers, T = ceil(t 2^24) holds
-    // the lower neighbour's index in its top bits and ceil(p 2^24) in its low
-    // 24 bits, and (r >> 8) < ceil(p 2^24) iff r < (T << 8) mod 2^32.  Exact:
-    // t 2^24 is an fp32 value below 2^27 and the conversion rounds up; one
-    // conversion per element instead of three.
+    // The decision "up iff r 2^-16 < p", p the position of |q| between its
+    // grid neighbours, is taken in fixed point: with t = |q| scaled so that
+    // the neighbours are consecutive integers, T = ceil(t 2^16) holds the
+    // lower neighbour's index in its top bits and ceil(p 2^16) in its low 16
+    // (a p above 1 - 2^-16 carries into the index: always up), and
+    // r < ceil(p 2^16) iff r < T mod 2^16.  Exact: t 2^16 is an fp32 value
+    // below 2^19 and the conversion rounds up; one conversion per element.
     const uint32_t sgn = (__float_as_uint(q) >> 28) & 8u;
     if (GRID == kE1M2) {
-        const float t = fminf(fabsf(q) * 33554432.0f, (float)(top << 24));   // 2|q| 2^24, at most top 2^24
+        const float t = fminf(fabsf(q) * 131072.0f, (float)(top << 16));   // 2|q| 2^16, at most top 2^16
         const uint32_t T = __float2uint_ru(t);
-        // the same decision as an addition: with P = T mod 2^24 and R = r >> 8,
-        // T + (2^24 - 1 - R) carries into bit 24 iff R < P (one three-input
-        // add; T < 2^27, so nothing overflows)
-        return sgn | ((T + 0xFFFFFFu - (r >> 8)) >> 24);
+        // the same decision as an addition: T + (2^16 - 1 - r) carries into
+        // bit 16 iff r < T mod 2^16 (T < 2^19, so nothing overflows)
+        return sgn | ((T + 0xFFFFu - r) >> 16);
     } else {
         const float a = fabsf(q);
         if (!(a < 6.0f)) return sgn | 7u;   // also NaN (non-finite input)
-        // neighbours 0.5 apart below 2, 1 apart below 4, 2 apart above
-        const float mul = a < 2.0f ? 33554432.0f : (a < 4.0f ? 16777216.0f : 8388608.0f);
+        // neighbours 0.5 apart below 2, 1 apart below 4, 2 apart above: ip
+        // counts the steps, and the lower neighbour's E2M1 index is ip,
+        // ip + 2, ip + 4
+        const float mul = a < 2.0f ? 131072.0f : (a < 4.0f ? 65536.0f : 32768.0f);
         const uint32_t T = __float2uint_ru(a * mul);
-        const uint32_t ip = T >> 24;
-        const uint32_t base = a < 2.0f ? ip : (a < 4.0f ? ip + 2u : 6u);   // E2M1 index of the lower neighbour
-        return sgn | (base + (r < (T << 8) ? 1u : 0u));
+        const uint32_t base = (T >> 16) + (a < 2.0f ? 0u : (a < 4.0f ? 2u : 4u));
+        return sgn | (base + (r < (T & 0xFFFFu) ? 1u : 0u));
     }
 }
 
-// sr_code<kE1M2> of q given as qs = q 2^25 (the caller's packed multiply;
+// sr_code<kE1M2> of q given as qs = q 2^17 (the caller's packed multiply;
 // exact: a power-of-two factor, and an overflow to inf clamps the same).
 __device__ __forceinline__ uint32_t sr_code_e1m2_scaled(float qs, uint32_t r, uint32_t top) {
     const uint32_t sgn = (__float_as_uint(qs) >> 28) & 8u;
-    const uint32_t T = __float2uint_ru(fminf(fabsf(qs), (float)(top << 24)));
-    return sgn | ((T + 0xFFFFFFu - (r >> 8)) >> 24);
+    const uint32_t T = __float2uint_ru(fminf(fabsf(qs), (float)(top << 16)));
+    return sgn | ((T + 0xFFFFu - r) >> 16);
 }
 
 // Grid value of a magnitude index.

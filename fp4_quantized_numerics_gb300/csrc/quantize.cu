@@ -261,28 +261,27 @@ __device__ __forceinline__ uint32_t codes8(const float q[8], const Args &a, uint
             for (int j = 0; j < 8; ++j) w |= e1m2_rn(q[j], (float)a.utop) << (4 * j);
         }
     } else {
+        // one Philox4x32-10 call per 8 codes: code j takes half (j % 2) of
+        // word j / 2 (i0 is a multiple of 8, so the call's counter is i0 / 8)
         const uint2 key = make_uint2((uint32_t)a.sr_seed, (uint32_t)(a.sr_seed >> 32));
-        const uint64_t c0 = i0 >> 2;
+        const uint64_t c = i0 >> 3;
+        const uint4 r = philox4x32_10(
+            make_uint4((uint32_t)c, (uint32_t)(c >> 32), (uint32_t)a.sr_counter, (uint32_t)(a.sr_counter >> 32)),
+            key);
+        const uint32_t rr[4] = {r.x, r.y, r.z, r.w};
         float qs[8];
         if (GRID == kE1M2) {
-            // the decision's 2^25 scaling, two values per packed multiply
-            const uint64_t S25 = pk2(33554432.0f, 33554432.0f);
+            // the decision's 2^17 scaling, two values per packed multiply
+            const uint64_t S17 = pk2(131072.0f, 131072.0f);
 #pragma unroll
-            for (int j = 0; j < 8; j += 2) upk2(mul2(pk2(q[j], q[j + 1]), S25), qs[j], qs[j + 1]);
+            for (int j = 0; j < 8; j += 2) upk2(mul2(pk2(q[j], q[j + 1]), S17), qs[j], qs[j + 1]);
         }
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            const uint64_t c = c0 + t;
-            const uint4 r = philox4x32_10(
-                make_uint4((uint32_t)c, (uint32_t)(c >> 32), (uint32_t)a.sr_counter,
-                           (uint32_t)(a.sr_counter >> 32)), key);
-            const uint32_t rr[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t code = GRID == kE1M2 ? sr_code_e1m2_scaled(qs[4 * t + j], rr[j], a.utop)
-                                                    : sr_code<GRID>(q[4 * t + j], rr[j], a.utop);
-                w |= code << (16 * t + 4 * j);
-            }
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t h = (j & 1) ? rr[j >> 1] >> 16 : rr[j >> 1] & 0xFFFFu;
+            const uint32_t code = GRID == kE1M2 ? sr_code_e1m2_scaled(qs[j], h, a.utop)
+                                                : sr_code<GRID>(q[j], h, a.utop);
+            w |= code << (4 * j);
         }
     }
     return w;

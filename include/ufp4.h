@@ -115,9 +115,10 @@ typedef enum { UFP4_BF16 = 0, UFP4_FP32 = 1 } ufp4_dtype;
  *                  of Philox4x32-10(key = rht_seed, counter = 0) is set.  Both
  *                  operands of a GEMM must use the same rht_seed.
  *   sr_seed, sr_counter : SR draws, for logical element i of the output
- *                  (i = row * k + col of the quantized orientation), word i%4
- *                  of Philox4x32-10(key = sr_seed, ctr = (i/4, sr_counter)),
- *                  and rounds up iff (word >> 8) * 2^-24 < p, p the position of
+ *                  (i = row * k + col of the quantized orientation), 16 bits:
+ *                  of Philox4x32-10(key = sr_seed, ctr = (i/8, sr_counter)),
+ *                  word (i%8)/2, its low half for even i and its high half for
+ *                  odd i; it rounds up iff bits * 2^-16 < p, p the position of
  *                  the value between its two neighbouring grid points.
  *   colwise      : 0 = 16-blocks run along the contiguous (last) dim and the
  *                  result is the quantization of X (rows x cols); 1 = blocks
