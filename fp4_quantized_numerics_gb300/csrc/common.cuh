@@ -103,6 +103,13 @@ __device__ __forceinline__ float max_nan(float a, float b) {
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
     return r;
 }
+// max_nan(a, max_nan(b, c)) in one instruction (the same value: NaN if any
+// input is NaN, else the exact maximum, in any order).
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 
 // ------------------------------------------------------------- grid codes
 // E2M1 round-to-nearest-even of a pair, satfinite; first argument goes to

@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(kThreads) k_amax_rowwise(Args a, FastDiv bdiv,
             float lo[8], hi[8];
             block_values<In, RHT>(cur.raw[t], sg, lo, hi);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) m = max_nan(m, max_nan(fabsf(lo[j]), fabsf(hi[j])));
+            for (int j = 0; j < 8; ++j) m = max3_nan(m, fabsf(lo[j]), fabsf(hi[j]));
         }
         cur = nxt;
     }
@@ -960,7 +960,7 @@ __global__ void __launch_bounds__(kThreads) k_amax_colwise(Args a, FastDiv cdiv,
         for (int i = 0; i < 16; ++i) {
             float c0, c1;
             upk2(P[i], c0, c1);
-            m = max_nan(m, max_nan(fabsf(c0), fabsf(c1)));
+            m = max3_nan(m, fabsf(c0), fabsf(c1));
         }
         cur = nxt;
     }
@@ -1204,7 +1204,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_row_staged(Args a,
                 for (int q = 0; q < 16; ++q) {
                     float u0, u1;
                     upk2(P[q], u0, u1);
-                    m = max_nan(m, max_nan(fabsf(u0), fabsf(u1)));
+                    m = max3_nan(m, fabsf(u0), fabsf(u1));
                 }
             }
         } else {
@@ -1221,7 +1221,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_row_staged(Args a,
                     float lo[8], hi[8];
                     block_values<In, RHT>(raw, sg, lo, hi);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) m = max_nan(m, max_nan(fabsf(lo[q]), fabsf(hi[q])));
+                    for (int q = 0; q < 8; ++q) m = max3_nan(m, fabsf(lo[q]), fabsf(hi[q]));
                 } else {
                     const uint32_t r = fdiv(gb, bdiv);
                     if (STATS)
@@ -1322,7 +1322,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_col_staged(Args a,
                 for (int q = 0; q < 16; ++q) {
                     float c0, c1;
                     upk2(P[q], c0, c1);
-                    m = max_nan(m, max_nan(fabsf(c0), fabsf(c1)));
+                    m = max3_nan(m, fabsf(c0), fabsf(c1));
                 }
             } else {
                 quant_unit_col<In, GRID, ROUND, RHT>(a, raw, kb, c, true, sg, S_enc, s_k, cstride, nkt, folded);
@@ -1445,8 +1445,8 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_amax_mma(Args ar, 
     float mr = 0.0f, mc = 0.0f;
     // running max of |D| over the A rows that hold data (rows m = lane / 4 and lane / 4 + 8)
     auto acc = [&](float &m, const float (&d)[4], const float (&e)[4], bool lo_ok, bool hi_ok) {
-        if (lo_ok) m = max_nan(max_nan(m, max_nan(fabsf(d[0]), fabsf(d[1]))), max_nan(fabsf(e[0]), fabsf(e[1])));
-        if (hi_ok) m = max_nan(max_nan(m, max_nan(fabsf(d[2]), fabsf(d[3]))), max_nan(fabsf(e[2]), fabsf(e[3])));
+        if (lo_ok) m = max3_nan(max3_nan(m, fabsf(d[0]), fabsf(d[1])), fabsf(e[0]), fabsf(e[1]));
+        if (hi_ok) m = max3_nan(max3_nan(m, fabsf(d[2]), fabsf(d[3])), fabsf(e[2]), fabsf(e[3]));
     };
     auto process = [&](uint32_t jj) {
         const uint32_t i = blockIdx.x + jj * gridDim.x;
@@ -1579,7 +1579,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_dual_staged(Args a
                 for (int q = 0; q < 16; ++q) {
                     float v0, v1;
                     upk2(P[q], v0, v1);
-                    mc = max_nan(mc, max_nan(fabsf(v0), fabsf(v1)));
+                    mc = max3_nan(mc, fabsf(v0), fabsf(v1));
                 }
             } else {
                 quant_unit_col<In, GRID, ROUND, RHT>(ac, raw, kb, c, true, sgc, Sc, s_kc, csc, nktc, fc);
@@ -1615,7 +1615,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_dual_staged(Args a
                     for (int q = 0; q < 16; ++q) {
                         float u0, u1;
                         upk2(P[q], u0, u1);
-                        mr = max_nan(mr, max_nan(fabsf(u0), fabsf(u1)));
+                        mr = max3_nan(mr, fabsf(u0), fabsf(u1));
                     }
                 } else {
                     const uint32_t b = cc * BPR + bc, r = kb * 16 + q0;
@@ -1632,7 +1632,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_dual_staged(Args a
                     float lo[8], hi[8];
                     block_values<In, RHT>(raw, sgr, lo, hi);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) mr = max_nan(mr, max_nan(fabsf(lo[q]), fabsf(hi[q])));
+                    for (int q = 0; q < 8; ++q) mr = max3_nan(mr, fabsf(lo[q]), fabsf(hi[q]));
                 } else {
                     quant_block_row<In, GRID, ROUND, RHT>(ar, raw, kb * 16 + q0, cc * BPR + bc, sgr, Sr, s_kr, csr,
                                                           nktr, fr);
@@ -1903,7 +1903,7 @@ __device__ __forceinline__ void tile_maxima(uint32_t st, uint32_t bl0, uint32_t 
         ra.load_shared(st + q * (kTileCols * 2) + bc * 32);
         rb.load_shared(st + (q + 64) * (kTileCols * 2) + bc * 32);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) mr = max_nan(mr, max_nan(fabsf(ra.get(e)), fabsf(rb.get(e))));
+        for (int e = 0; e < 16; ++e) mr = max3_nan(mr, fabsf(ra.get(e)), fabsf(rb.get(e)));
         mc = mr;
         return;
     }
@@ -1919,7 +1919,7 @@ __device__ __forceinline__ void tile_maxima(uint32_t st, uint32_t bl0, uint32_t 
             mma_bf16(af, bl0, bl1, d);
             mma_bf16(af, bh0, bh1, e);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) mr = max_nan(mr, max_nan(fabsf(d[k]), fabsf(e[k])));
+            for (int k = 0; k < 4; ++k) mr = max3_nan(mr, fabsf(d[k]), fabsf(e[k]));
         }
         // column-wise: A row m = column 16 sft + m, k = tile rows 16 band .. + 15
         {
@@ -1928,7 +1928,7 @@ __device__ __forceinline__ void tile_maxima(uint32_t st, uint32_t bl0, uint32_t 
             mma_bf16(af, bl0, bl1, d);
             mma_bf16(af, bh0, bh1, e);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) mc = max_nan(mc, max_nan(fabsf(d[k]), fabsf(e[k])));
+            for (int k = 0; k < 4; ++k) mc = max3_nan(mc, fabsf(d[k]), fabsf(e[k]));
         }
     }
 }
@@ -2106,7 +2106,7 @@ __global__ void __launch_bounds__(kThreads) k_amax_grouped(Args a, const __grid_
             float lo[8], hi[8];
             block_values<In, RHT>(raw, sg, lo, hi);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) m = max_nan(m, max_nan(fabsf(lo[j]), fabsf(hi[j])));
+            for (int j = 0; j < 8; ++j) m = max3_nan(m, fabsf(lo[j]), fabsf(hi[j]));
         } else {
             const int64_t seg_rows = sm.in_row[e + 1] - sm.in_row[e];
             const int64_t left = seg_rows - 16 * (int64_t)q;
@@ -2119,7 +2119,7 @@ __global__ void __launch_bounds__(kThreads) k_amax_grouped(Args a, const __grid_
             for (int i = 0; i < 16; ++i) {
                 float c0, c1;
                 upk2(P[i], c0, c1);
-                m = max_nan(m, max_nan(fabsf(c0), fabsf(c1)));
+                m = max3_nan(m, fabsf(c0), fabsf(c1));
             }
         }
     }
@@ -2274,7 +2274,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas)
                 float lo[8], hi[8];
                 block_values<In, RHT>(raw, sg, lo, hi);
 #pragma unroll
-                for (int t = 0; t < 8; ++t) m = max_nan(m, max_nan(fabsf(lo[t]), fabsf(hi[t])));
+                for (int t = 0; t < 8; ++t) m = max3_nan(m, fabsf(lo[t]), fabsf(hi[t]));
             } else {
                 e_cur = e;
                 const uint32_t orow = (uint32_t)(sm.out_off[e] + ((int64_t)r - sm.in_row[e]));
@@ -2439,7 +2439,7 @@ __device__ __forceinline__ void dual_tile_grouped(const Args &ar, const Args &ac
                 for (int i = 0; i < 16; ++i) {
                     float a, b;
                     upk2(P[i], a, b);
-                    mc = max_nan(mc, max_nan(fabsf(a), fabsf(b)));
+                    mc = max3_nan(mc, fabsf(a), fabsf(b));
                 }
             }
         } else {
@@ -2468,7 +2468,7 @@ __device__ __forceinline__ void dual_tile_grouped(const Args &ar, const Args &ac
                         float lo[8], hi[8];
                         block_values<__nv_bfloat16, RHT>(ra, sgr, lo, hi);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) mr = max_nan(mr, max_nan(fabsf(lo[j]), fabsf(hi[j])));
+                        for (int j = 0; j < 8; ++j) mr = max3_nan(mr, fabsf(lo[j]), fabsf(hi[j]));
                     }
                 } else {
                     // rows past the segment's end are the layout's zero padding rows
@@ -2731,7 +2731,7 @@ __device__ __forceinline__ void mx_store(const Args &a, float v[32], uint32_t r,
                                          uint32_t cstride, uint32_t nkt) {
     float amax = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) amax = max_nan(amax, fabsf(v[j]));
+    for (int j = 0; j < 32; j += 2) amax = max3_nan(amax, fabsf(v[j]), fabsf(v[j + 1]));
     if (!(amax <= kFltMax) && a.status) atomicOr(a.status, 1u);
     const uint32_t sb = mx_scale_byte(amax);
     const float f = __uint_as_float((254u - min(sb, 253u)) << 23);   // 2^-s, exact
