@@ -1705,6 +1705,11 @@ constexpr uint32_t kTileBytes = kTileRows * kTileCols * 2;   // BF16
 static_assert(kTileBytes == kChunk, "a tile fills one ring stage");
 constexpr uint32_t kColStageBytes = 8 * kTileCols * 8 + 8 * kTileCols;   // codes [8][64] x 8 B + scales [8][64]
 constexpr uint32_t kTileSmem = ring_smem<false>() + kColStageBytes;
+// k_dual_tile: a 2-deep tile ring and two staging buffers (tile j stages into
+// buffer j % 2), so one CTA barrier per tile orders both the ring slot's reuse
+// and the staging buffer's; 4 CTAs per SM fit (about 42 KB each).
+constexpr int kDualRing = 2;
+constexpr uint32_t kDualTileSmem = kDualRing * kChunk + 64 + 2 * kColStageBytes;
 
 // Geometry of the dual-orientation tile kernels, fixed per launch.
 struct DualGeom {
@@ -1815,13 +1820,13 @@ __device__ __forceinline__ void dual_padding(const Args &ar, const Args &ac, con
 template <int GRID, int ROUND, bool RHT>
 __global__ void __launch_bounds__(kThreads, kStagedMinCtas)
     k_dual_tile(const __grid_constant__ CUtensorMap tmx, Args ar, Args ac, uint32_t nct, uint32_t ntiles) {
-    constexpr int kRing = ring_depth<false>();
+    constexpr int kRing = kDualRing;
     extern __shared__ __align__(128) uint8_t dsm[];
     __shared__ float s_kr[256], s_kc[256];
     __shared__ float s_red[kThreads / 32];
     const RingCtl ring = ring_init<kRing>(dsm);
-    uint8_t *stage_codes = dsm + kRing * kChunk + 64;            // [rb][cl] uint2
-    uint8_t *stage_scales = stage_codes + 8 * kTileCols * 8;    // [rb][cl] byte
+    // staging buffer b: codes [rb][cl] uint2, then scales [rb][cl] byte
+    uint8_t *const stage0 = dsm + kRing * kChunk + 64;
     uint32_t issued = 0, j = 0;
     auto issue = [&](uint32_t jj) {
         const uint32_t i = blockIdx.x + jj * gridDim.x;
@@ -1854,14 +1859,17 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas)
         const bool mine = ring_wait_own<kRing>(ring, j);
         const uint32_t i = blockIdx.x + j * gridDim.x;
         const uint32_t rt = i / nct, ct = i - rt * nct;
+        uint8_t *const stage_codes = stage0 + (j & 1) * kColStageBytes;
+        uint8_t *const stage_scales = stage_codes + 8 * kTileCols * 8;
         if (mine)
             dual_tile_quant<GRID, ROUND, RHT, true>(ar, ac, g, ring.buf + (j % kRing) * kChunk, rt, ct, sgr, sgc, Sr,
                                                     Sc, s_kr, s_kc, fr, fc, stage_codes, stage_scales);
-        __syncthreads();   // tile consumed; column-wise results staged
+        // tile j consumed and its column-wise results staged; every thread has
+        // also finished flushing tile j - 1, whose buffer tile j + 1 reuses
+        __syncthreads();
         if (*ring.abort) { ok = false; break; }
         if (threadIdx.x == 0) issue(j + kRing);
         dual_tile_flush(ac, g, rt, ct, stage_codes, stage_scales);
-        __syncthreads();   // staging buffers free for the next tile
     }
     if (!ok) {
         if (threadIdx.x == 0) atomicOr(&g_quant_timeout, 1u);
@@ -3107,7 +3115,7 @@ cudaError_t quantize_dual_typed(const QuantLaunch &qr, const QuantLaunch &qc, Ar
         const int kgrid = qr.grid == kE2M1 ? kE2M1 : kE1M2;   // clamped E2M1 runs the uniform-grid kernels
 #define UFP4_T(GRID, ROUND, RHT)                                                                          \
         if (kgrid == GRID && qr.round == ROUND && (qr.rht != 0) == RHT)                                   \
-            return launch_staged_smem(k_dual_tile<GRID, ROUND, RHT>, kTileSmem, ntiles, nullptr, s, tm, ar,       \
+            return launch_staged_smem(k_dual_tile<GRID, ROUND, RHT>, kDualTileSmem, ntiles, nullptr, s, tm, ar,   \
                                       ac, nct, ntiles);
         UFP4_T(kE2M1, kRTNE, false) UFP4_T(kE2M1, kRTNE, true)
         UFP4_T(kE2M1, kSR, false)   UFP4_T(kE2M1, kSR, true)
