@@ -1705,11 +1705,13 @@ constexpr uint32_t kTileBytes = kTileRows * kTileCols * 2;   // BF16
 static_assert(kTileBytes == kChunk, "a tile fills one ring stage");
 constexpr uint32_t kColStageBytes = 8 * kTileCols * 8 + 8 * kTileCols;   // codes [8][64] x 8 B + scales [8][64]
 constexpr uint32_t kTileSmem = ring_smem<false>() + kColStageBytes;
-// k_dual_tile: a 2-deep tile ring and two staging buffers (tile j stages into
-// buffer j % 2), so one CTA barrier per tile orders both the ring slot's reuse
-// and the staging buffer's; 4 CTAs per SM fit (about 42 KB each).
+// k_dual_tile and k_dual_tile_grouped stage tile j's column-wise results in
+// buffer j % 2 of two, so one CTA barrier per tile orders both the ring
+// slot's reuse and the staging buffer's.  k_dual_tile's ring is 2 deep (4
+// CTAs per SM fit, about 42 KB each; a third stage measured no faster with
+// SR, whose registers allow 3 CTAs per SM); the grouped kernel keeps 3.
 constexpr int kDualRing = 2;
-constexpr uint32_t kDualTileSmem = kDualRing * kChunk + 64 + 2 * kColStageBytes;
+template <int KRING> constexpr uint32_t dual_smem() { return KRING * kChunk + 64 + 2 * kColStageBytes; }
 
 // Geometry of the dual-orientation tile kernels, fixed per launch.
 struct DualGeom {
@@ -2497,8 +2499,8 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas)
     extern __shared__ __align__(128) uint8_t dsm[];
     __shared__ float s_kr[256], s_kc[256];   // the current segment's per-code multipliers
     const RingCtl ring = ring_init<kRing>(dsm);
-    uint8_t *stage_codes = dsm + kRing * kChunk + 64;            // [rb][cl] uint2
-    uint8_t *stage_scales = stage_codes + 8 * kTileCols * 8;    // [rb][cl] byte
+    // staging buffer b: codes [rb][cl] uint2, then scales [rb][cl] byte
+    uint8_t *const stage0 = dsm + kRing * kChunk + 64;
     const uint32_t total = (uint32_t)gd.tiles[gd.n];
     const uint32_t per = (total + gridDim.x - 1) / gridDim.x;
     const uint32_t t0 = blockIdx.x * per;
@@ -2595,13 +2597,19 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas)
         const uint32_t kbl = (T + 63) / 64 * 4 - rt * 8;
         const uint32_t nkb = kbl < 8 ? kbl : 8u;
         const uint32_t kb0 = (uint32_t)(gd.koff[e] / 16) + rt * 8;
+        // (the tables are read only by the quantization, which every thread
+        // finished before the previous tile's barrier)
         if (!AMAX && e != e_cur) tables(e);   // uniform across the CTA
         e_cur = e;
+        uint8_t *const stage_codes = stage0 + (j & 1) * kColStageBytes;
+        uint8_t *const stage_scales = stage_codes + 8 * kTileCols * 8;
         if (mine)
             dual_tile_grouped<GRID, ROUND, RHT, AMAX>(ar, ac, g, ring.buf + (j % kRing) * kChunk, nvalid,
                                                       (uint32_t)gd.roff[e] + rt * kTileRows, kb0, nkb, ct, sgr, sgc,
                                                       Sr, Sc, s_kr, s_kc, fr, fc, stage_codes, stage_scales, mr, mc);
-        __syncthreads();   // tile consumed; column-wise results staged
+        // tile j consumed and its column-wise results staged; every thread has
+        // also finished flushing tile j - 1, whose buffer tile j + 1 reuses
+        __syncthreads();
         if (*ring.abort) { ok = false; break; }
         if (threadIdx.x == 0) issue(j + kRing);
         if (AMAX) {
@@ -2640,7 +2648,6 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas)
                     *reinterpret_cast<uint32_t *>(ac.scales + scale_offset32(c, kb0 + 4 * h, g.nktc)) = w;
                 }
             }
-            __syncthreads();   // staging buffers free for the next tile
         }
     }
     if (!ok) {
@@ -3115,8 +3122,8 @@ cudaError_t quantize_dual_typed(const QuantLaunch &qr, const QuantLaunch &qc, Ar
         const int kgrid = qr.grid == kE2M1 ? kE2M1 : kE1M2;   // clamped E2M1 runs the uniform-grid kernels
 #define UFP4_T(GRID, ROUND, RHT)                                                                          \
         if (kgrid == GRID && qr.round == ROUND && (qr.rht != 0) == RHT)                                   \
-            return launch_staged_smem(k_dual_tile<GRID, ROUND, RHT>, kDualTileSmem, ntiles, nullptr, s, tm, ar,   \
-                                      ac, nct, ntiles);
+            return launch_staged_smem(k_dual_tile<GRID, ROUND, RHT>, dual_smem<kDualRing>(), ntiles, nullptr, s,  \
+                                      tm, ar, ac, nct, ntiles);
         UFP4_T(kE2M1, kRTNE, false) UFP4_T(kE2M1, kRTNE, true)
         UFP4_T(kE2M1, kSR, false)   UFP4_T(kE2M1, kSR, true)
         UFP4_T(kE1M2, kRTNE, false) UFP4_T(kE1M2, kRTNE, true)
@@ -3181,16 +3188,17 @@ cudaError_t quantize_grouped_dual_bf16(const QuantLaunch &qr, const QuantLaunch 
     uint32_t *slots = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsPartials);
     cudaError_t e = cudaMemsetAsync(ws, 0, kWsPartials + 2 * (size_t)gd.n * sizeof(uint32_t), s);
     if (e != cudaSuccess || ntiles == 0) return e;
-    e = qr.rht ? launch_staged_smem(k_dual_tile_grouped<kE2M1, kRTNE, true, true>, kTileSmem, ntiles, nullptr, s,
-                                    tm, ar, ac, gd, nct, slots)
-               : launch_staged_smem(k_dual_tile_grouped<kE2M1, kRTNE, false, true>, kTileSmem, ntiles, nullptr, s,
-                                    tm, ar, ac, gd, nct, slots);
+    constexpr uint32_t smem = dual_smem<ring_depth<false>()>();
+    e = qr.rht ? launch_staged_smem(k_dual_tile_grouped<kE2M1, kRTNE, true, true>, smem, ntiles, nullptr, s, tm, ar,
+                                    ac, gd, nct, slots)
+               : launch_staged_smem(k_dual_tile_grouped<kE2M1, kRTNE, false, true>, smem, ntiles, nullptr, s, tm, ar,
+                                    ac, gd, nct, slots);
     if (e != cudaSuccess) return e;
     const int kgrid = qr.grid == kE2M1 ? kE2M1 : kE1M2;   // clamped E2M1 runs the uniform-grid kernels
 #define UFP4_GD(GRID, ROUND, RHT)                                                                             \
     if (kgrid == GRID && qr.round == ROUND && (qr.rht != 0) == RHT)                                          \
-        return launch_staged_smem(k_dual_tile_grouped<GRID, ROUND, RHT, false>, kTileSmem, ntiles, nullptr, s, tm, \
-                                  ar, ac, gd, nct, slots);
+        return launch_staged_smem(k_dual_tile_grouped<GRID, ROUND, RHT, false>, smem, ntiles, nullptr, s, tm, ar, ac,  \
+                                  gd, nct, slots);
     UFP4_GD(kE2M1, kRTNE, false) UFP4_GD(kE2M1, kRTNE, true)
     UFP4_GD(kE2M1, kSR, false)   UFP4_GD(kE2M1, kSR, true)
     UFP4_GD(kE1M2, kRTNE, false) UFP4_GD(kE1M2, kRTNE, true)
