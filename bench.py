@@ -637,7 +637,8 @@ def run_kernel(args):
     """One kernel of a step in isolation, for profiling: `steps` launches of
     the fwd_y GEMM (T x F x H), of the RHT quantization of X (T x H) in one
     orientation or both (quant_dual_*; the SR variant quantizes dY, T x F),
-    after `warmup` launches, the tensor amax given (quant_grouped_dual_e1m2:
+    after `warmup` launches, the tensor amax given (quant_resident_e1m2: W,
+    F x H, both ways with its maxima, the on-chip single pass; quant_grouped_dual_e1m2:
     the MoE-7.9B X both ways, its amax pass included).  --shape dense: T, H,
     F = 8192, 2048, 5632; moe124b: 65536, 8192, 2048.  Prints the mean event
     time."""
@@ -670,6 +671,15 @@ def run_kernel(args):
         fn = lambda: U.ufp4_gemm(a, b, out=c)
         work = 2.0 * T * F * H
         unit = "TFLOP/s"
+    elif kind == "quant_resident_e1m2":
+        # W (F x H) both ways with both tensor maxima computed: a tensor that
+        # fits on chip takes the single pass (one cooperative launch)
+        src = inputs.device_normal((F, H), 0.02, 22, dev)
+        qr = U.QTensor.empty(F, H, U.UFP4_E1M2, dev)
+        qc = U.QTensor.empty(H, F, U.UFP4_E1M2, dev)
+        fn = lambda: U.ufp4_quantize_dual(src, U.UFP4_E1M2, rht=True, out_row=qr, out_col=qc)
+        work = 2 * src.numel() * Q_BYTES_PER_ELEM
+        unit = "GB/s"
     elif kind.startswith("quant_dual") or kind == "amax_dual_e1m2":
         # both orientations from one read; SR variant on the dY shape; the
         # amax variant computes the tensor maxima (its amax pass is profiled)
@@ -1089,7 +1099,8 @@ def main():
     ap.add_argument("--kernel", default=None,
                     choices=["gemm_e2m1", "gemm_e1m2", "gemm_mxfp4", "quant_row_e1m2", "quant_col_e1m2", "quant_dual_e1m2",
                              "quant_dual_sr_e1m2", "amax_dual_e1m2",
-                             "quant_row_e2m1", "quant_col_e2m1", "quant_grouped_dual_e1m2", "all"],
+                             "quant_row_e2m1", "quant_col_e2m1", "quant_grouped_dual_e1m2", "quant_resident_e1m2",
+                             "all"],
                     help="time one kernel of the step in isolation (profiling); all: every public call once")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -1716,14 +1716,15 @@ struct DualGeom {
     uint32_t kvr, kbr, kbp;          // real row-wise blocks per row; real and padded column-wise blocks
     uint32_t cp, rb, q, bc;          // this thread's column pair / row block, and row / block column
 };
-__device__ __forceinline__ DualGeom dual_geom(const Args &ar, const Args &ac) {
+// tid: the thread's index within the 256 threads that share one tile's work
+__device__ __forceinline__ DualGeom dual_geom(const Args &ar, const Args &ac, uint32_t tid = threadIdx.x) {
     DualGeom g;
     g.csr = (uint32_t)(ar.kpad / 2); g.nktr = (uint32_t)ar.nkt;
     g.csc = (uint32_t)(ac.kpad / 2); g.nktc = (uint32_t)ac.nkt;
     g.cols = (uint32_t)ar.cols; g.rows = (uint32_t)ar.rows;
     g.kvr = g.cols / 16; g.kbr = g.rows / 16; g.kbp = (uint32_t)(ac.kpad / 16);
-    g.cp = threadIdx.x % 32; g.rb = threadIdx.x / 32;
-    g.q = threadIdx.x / 4; g.bc = threadIdx.x % 4;
+    g.cp = tid % 32; g.rb = tid / 32;
+    g.q = tid / 4; g.bc = tid % 4;
     return g;
 }
 
@@ -1732,13 +1733,14 @@ __device__ __forceinline__ DualGeom dual_geom(const Args &ar, const Args &ac) {
 // rows r0 + 16 rb .. + 15), staged in stage_codes / stage_scales when STAGE
 // (written out by dual_tile_flush), else stored directly.  Row-wise: rows
 // r0 + q and r0 + q + 64, block c0 / 16 + bc, stored directly.
-template <int GRID, int ROUND, bool RHT, bool STAGE>
+// PARTS: 1 the column-wise unit only, 2 the row-wise blocks only, 3 both.
+template <int GRID, int ROUND, bool RHT, bool STAGE, int PARTS = 3>
 __device__ __forceinline__ void dual_tile_quant(const Args &ar, const Args &ac, const DualGeom &g, uint32_t st,
                                                 uint32_t rt, uint32_t ct, const Signs &sgr, const Signs &sgc,
                                                 float Sr, float Sc, const float *s_kr, const float *s_kc, bool fr,
                                                 bool fc, uint8_t *stage_codes, uint8_t *stage_scales) {
     const uint32_t r0 = rt * kTileRows, c0 = ct * kTileCols;
-    {
+    if (PARTS & 1) {
         const uint32_t c = c0 + 2 * g.cp, kb = rt * 8 + g.rb;
         ColRaw<__nv_bfloat16> raw;
         raw.load_shared(st + 16 * g.rb * (kTileCols * 2) + g.cp * 4, kTileCols * 2);
@@ -1759,7 +1761,7 @@ __device__ __forceinline__ void dual_tile_quant(const Args &ar, const Args &ac, 
                                                             fc);
         }
     }
-    {
+    if (PARTS & 2) {
         const uint32_t r = r0 + g.q, b = ct * (kTileCols / 16) + g.bc;
         if (r < g.rows && b < g.kvr) {
             Raw<__nv_bfloat16> ra, rbw;
@@ -1896,26 +1898,30 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
 }
 
 // Maxima of |4 y| (or |x| without the transform) of one resident tile, row-wise
-// blocks into mr and column-wise blocks into mc.  Elements outside the tensor
-// arrive as zeros.
-template <bool RHT>
+// blocks into mr and column-wise blocks into mc, by the CTA's NT threads.
+// Elements outside the tensor arrive as zeros.
+template <bool RHT, int NT>
 __device__ __forceinline__ void tile_maxima(uint32_t st, uint32_t bl0, uint32_t bl1, uint32_t bh0, uint32_t bh1,
                                             float &mr, float &mc) {
+    static_assert(NT == 256 || NT == 512, "one or two row blocks per thread; 32 A groups over the warps");
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (!RHT) {
-        // the orientations share max |x|: the thread's two row-wise blocks
+        // the orientations share max |x|: the thread's row-wise blocks (rows
+        // q and q + 64 with 256 threads, row q with 512)
         const uint32_t q = threadIdx.x / 4, bc = threadIdx.x % 4;
-        Raw<__nv_bfloat16> ra, rb;
-        ra.load_shared(st + q * (kTileCols * 2) + bc * 32);
-        rb.load_shared(st + (q + 64) * (kTileCols * 2) + bc * 32);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) mr = max3_nan(mr, fabsf(ra.get(e)), fabsf(rb.get(e)));
+        for (uint32_t h = 0; h < 512 / NT; ++h) {
+            Raw<__nv_bfloat16> ra;
+            ra.load_shared(st + (q + 64 * h) * (kTileCols * 2) + bc * 32);
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) mr = max3_nan(mr, fabsf(ra.get(e)), fabsf(ra.get(e + 1)));
+        }
         mc = mr;
         return;
     }
 #pragma unroll
-    for (uint32_t u = 0; u < 4; ++u) {
-        const uint32_t G = warp + 8 * u, band = G / 4, sft = G % 4;
+    for (uint32_t u = 0; u < 32 / (NT / 32); ++u) {
+        const uint32_t G = warp + (NT / 32) * u, band = G / 4, sft = G % 4;
         float d[4], e[4];
         uint32_t af[4];
         // row-wise: A row m = tile row 16 band + m, block column (sft + m) % 4
@@ -1939,13 +1945,19 @@ __device__ __forceinline__ void tile_maxima(uint32_t st, uint32_t bl0, uint32_t 
     }
 }
 
+// The single pass runs 512 threads per CTA (one CTA per SM): the maxima
+// spread over 16 warps, and the quantization gives each tile's column-wise
+// units to threads 0-255 and its row-wise blocks to threads 256-511, both
+// stored directly, so the two halves need no barrier between them.
+constexpr int kResidentThreads = 512;
+
 template <int GRID, int ROUND, bool RHT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kResidentThreads, 1)
     k_dual_resident(const __grid_constant__ CUtensorMap tmx, Args ar, Args ac, uint32_t nct, uint32_t ntiles,
                     uint32_t *arrive) {
     extern __shared__ __align__(128) uint8_t dsm[];
     __shared__ float s_kr[256], s_kc[256];
-    __shared__ float s_red[kThreads / 32], s_red2[kThreads / 32];
+    __shared__ float s_red[kResidentThreads / 32], s_red2[kResidentThreads / 32];
     __shared__ int s_go;
     const uint32_t buf = ptx::smem_u32(dsm);
     const uint32_t bars = buf + kResidentMax * kTileBytes;
@@ -1985,7 +1997,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (uint32_t t = 0; t < nloc && ok; ++t) {
         ok = ptx::mbar_wait_bounded(bars + 8u * t, 0u, kRingWait);
-        if (ok) tile_maxima<RHT>(buf + t * kTileBytes, bl0, bl1, bh0, bh1, mr, mc);
+        if (ok) tile_maxima<RHT, kResidentThreads>(buf + t * kTileBytes, bl0, bl1, bh0, bh1, mr, mc);
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
@@ -1998,7 +2010,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // so that the others do not wait for it and see a non-finite amax), then
     // the grid barrier -- every CTA is resident (cooperative launch) -- bounded
     if (threadIdx.x == 0) {
-        for (int w = 1; w < kThreads / 32; ++w) { mr = max_nan(mr, s_red[w]); mc = max_nan(mc, s_red2[w]); }
+        for (int w = 1; w < kResidentThreads / 32; ++w) { mr = max_nan(mr, s_red[w]); mc = max_nan(mc, s_red2[w]); }
         ar.partials_out[blockIdx.x] = ok ? (RHT ? mr * 0.25f : mr) : __int_as_float(0x7FFFFFFF);
         ac.partials_out[blockIdx.x] = ok ? (RHT ? mc * 0.25f : mc) : __int_as_float(0x7FFFFFFF);
         __threadfence();
@@ -2034,12 +2046,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tensor_scale_prologue(ac, qmax, RHT ? 0.25f : 1.0f, s_kc, s_red, Sc, GRID == kE1M2 && ROUND == kRTNE, &fc, &amc);
     if (blockIdx.x == 0 && threadIdx.x == 0 && ar.status && !isfinite(amc)) *ar.status = 1u;
     const Signs sgr = row_signs<__nv_bfloat16>(smask), sgc = col_signs<__nv_bfloat16>(smask);
-    const DualGeom g = dual_geom(ar, ac);
+    const bool col_half = threadIdx.x < 256;
+    const DualGeom g = dual_geom(ar, ac, threadIdx.x & 255u);
     for (uint32_t t = 0; t < nloc; ++t) {
         uint32_t rt, ct;
         tile_of(t, rt, ct);
-        dual_tile_quant<GRID, ROUND, RHT, false>(ar, ac, g, buf + t * kTileBytes, rt, ct, sgr, sgc, Sr, Sc, s_kr,
-                                                 s_kc, fr, fc, nullptr, nullptr);
+        if (col_half)
+            dual_tile_quant<GRID, ROUND, RHT, false, 1>(ar, ac, g, buf + t * kTileBytes, rt, ct, sgr, sgc, Sr, Sc,
+                                                        s_kr, s_kc, fr, fc, nullptr, nullptr);
+        else
+            dual_tile_quant<GRID, ROUND, RHT, false, 2>(ar, ac, g, buf + t * kTileBytes, rt, ct, sgr, sgc, Sr, Sc,
+                                                        s_kr, s_kc, fr, fc, nullptr, nullptr);
     }
     dual_padding(ar, ac, g);
 }
@@ -3018,9 +3035,10 @@ cudaError_t quantize_typed(const QuantLaunch &q, Args &a, void *ws, cudaStream_t
     return cudaErrorInvalidValue;
 }
 
-// Cooperative launch of a single-pass kernel over `grid` CTAs of kThreads
-// with kResidentSmem bytes of shared memory, after zeroing its grid-barrier
-// counter.  cudaErrorNotSupported when the CTAs cannot all be resident.
+// Cooperative launch of a single-pass kernel over `grid` CTAs of
+// kResidentThreads with kResidentSmem bytes of shared memory, after zeroing
+// its grid-barrier counter.  cudaErrorNotSupported when the CTAs cannot all
+// be resident.
 template <class K, class... P>
 cudaError_t launch_resident(K kern, uint32_t grid, uint32_t *arrive, cudaStream_t s, P... args) {
     static std::mutex mu;
@@ -3034,13 +3052,13 @@ cudaError_t launch_resident(K kern, uint32_t grid, uint32_t *arrive, cudaStream_
         }
     }
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kResidentSmem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kResidentThreads, kResidentSmem) != cudaSuccess ||
         (int64_t)per_sm * num_sms() < (int64_t)grid)
         return cudaErrorNotSupported;
     cudaError_t e = cudaMemsetAsync(arrive, 0, sizeof(uint32_t), s);
     if (e != cudaSuccess) return e;
     void *argv[] = {static_cast<void *>(&args)...};
-    e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(grid), dim3(kThreads), argv,
+    e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(grid), dim3(kResidentThreads), argv,
                                     kResidentSmem, s);
     if (e == cudaErrorCooperativeLaunchTooLarge) {
         cudaGetLastError();   // not sticky: take the two-pass route
