@@ -1740,6 +1740,19 @@ __device__ __forceinline__ void dual_tile_quant(const Args &ar, const Args &ac, 
                                                 float Sr, float Sc, const float *s_kr, const float *s_kc, bool fr,
                                                 bool fc, uint8_t *stage_codes, uint8_t *stage_scales) {
     const uint32_t r0 = rt * kTileRows, c0 = ct * kTileCols;
+    if (PARTS & 2) {
+        const uint32_t r = r0 + g.q, b = ct * (kTileCols / 16) + g.bc;
+        if (r < g.rows && b < g.kvr) {
+            Raw<__nv_bfloat16> ra, rbw;
+            ra.load_shared(st + g.q * (kTileCols * 2) + g.bc * 32);
+            rbw.load_shared(st + (g.q + 64) * (kTileCols * 2) + g.bc * 32);
+            // one block at a time (measured faster than the packed pair, which
+            // holds twice the registers)
+            quant_block_row<__nv_bfloat16, GRID, ROUND, RHT>(ar, ra, r, b, sgr, Sr, s_kr, g.csr, g.nktr, fr);
+            if (r + 64 < g.rows)
+                quant_block_row<__nv_bfloat16, GRID, ROUND, RHT>(ar, rbw, r + 64, b, sgr, Sr, s_kr, g.csr, g.nktr, fr);
+        }
+    }
     if (PARTS & 1) {
         const uint32_t c = c0 + 2 * g.cp, kb = rt * 8 + g.rb;
         ColRaw<__nv_bfloat16> raw;
@@ -1759,19 +1772,6 @@ __device__ __forceinline__ void dual_tile_quant(const Args &ar, const Args &ac, 
             // padding blocks past the last row are written as zeros
             quant_unit_col<__nv_bfloat16, GRID, ROUND, RHT>(ac, raw, kb, c, kb < g.kbr, sgc, Sc, s_kc, g.csc, g.nktc,
                                                             fc);
-        }
-    }
-    if (PARTS & 2) {
-        const uint32_t r = r0 + g.q, b = ct * (kTileCols / 16) + g.bc;
-        if (r < g.rows && b < g.kvr) {
-            Raw<__nv_bfloat16> ra, rbw;
-            ra.load_shared(st + g.q * (kTileCols * 2) + g.bc * 32);
-            rbw.load_shared(st + (g.q + 64) * (kTileCols * 2) + g.bc * 32);
-            // one block at a time (measured faster than the packed pair, which
-            // holds twice the registers)
-            quant_block_row<__nv_bfloat16, GRID, ROUND, RHT>(ar, ra, r, b, sgr, Sr, s_kr, g.csr, g.nktr, fr);
-            if (r + 64 < g.rows)
-                quant_block_row<__nv_bfloat16, GRID, ROUND, RHT>(ar, rbw, r + 64, b, sgr, Sr, s_kr, g.csr, g.nktr, fr);
         }
     }
 }
