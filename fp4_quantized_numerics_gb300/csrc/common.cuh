@@ -57,6 +57,18 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
     return c;
 }
 
+// The same generator with its ten round keys given (rk[2r], rk[2r + 1] for
+// round r: the key after r increments), e.g. precomputed on the host.
+__device__ __forceinline__ uint4 philox4x32_10_keys(uint4 c, const uint32_t (&rk)[20]) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ rk[2 * r], lo1, hi0 ^ c.w ^ rk[2 * r + 1], lo0);
+    }
+    return c;
+}
+
 // RHT sign pattern d as a 16-bit mask (bit j set <=> d_j = -1): bits 0..15
 // of word 0 of Philox4x32-10(key = seed, counter = 0).
 __device__ __forceinline__ uint32_t rht_sign_mask(uint64_t seed) {

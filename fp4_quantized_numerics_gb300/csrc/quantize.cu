@@ -52,6 +52,10 @@ struct Args {
     int64_t out_rows, k, kpad;  // result: out_rows x k, padded to kpad
     int64_t nkt;                // kpad / 64
     uint64_t rht_seed, sr_seed, sr_counter, elem_base;
+    // Philox4x32-10 round keys of sr_seed (round r: srk[2r], srk[2r + 1]),
+    // set by set_sr_keys on the host, so that a round reads its key from the
+    // kernel's parameters instead of advancing it
+    uint32_t srk[20];
     const float *amax_in;
     const float *partials;
     float *partials_out;
@@ -263,11 +267,10 @@ __device__ __forceinline__ uint32_t codes8(const float q[8], const Args &a, uint
     } else {
         // one Philox4x32-10 call per 8 codes: code j takes half (j % 2) of
         // word j / 2 (i0 is a multiple of 8, so the call's counter is i0 / 8)
-        const uint2 key = make_uint2((uint32_t)a.sr_seed, (uint32_t)(a.sr_seed >> 32));
         const uint64_t c = i0 >> 3;
-        const uint4 r = philox4x32_10(
+        const uint4 r = philox4x32_10_keys(
             make_uint4((uint32_t)c, (uint32_t)(c >> 32), (uint32_t)a.sr_counter, (uint32_t)(a.sr_counter >> 32)),
-            key);
+            a.srk);
         const uint32_t rr[4] = {r.x, r.y, r.z, r.w};
         float qs[8];
         if (GRID == kE1M2) {
@@ -2331,12 +2334,25 @@ __global__ void __launch_bounds__(kThreads, kStagedMinCtas)
 template <bool AMAX, class K, class... P>
 cudaError_t launch_staged(K kern, int64_t work_ctas, int *grid_out, cudaStream_t s, P... args);
 
+// The round keys of Philox4x32-10 with key sr_seed (the key advances by the
+// Weyl constants 0x9E3779B9 / 0xBB67AE85 after each round).
+void set_sr_keys(Args &a) {
+    uint32_t k0 = (uint32_t)a.sr_seed, k1 = (uint32_t)(a.sr_seed >> 32);
+    for (int r = 0; r < 10; ++r) {
+        a.srk[2 * r] = k0;
+        a.srk[2 * r + 1] = k1;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+}
+
 Args grouped_args(const QuantLaunch &q, void *ws) {
     Args a{};
     a.x = q.x; a.ld = q.ld; a.cols = q.cols;
     a.out_rows = q.out_rows; a.k = q.k; a.kpad = kpad_of(q.k); a.nkt = a.kpad / 64;
     a.rows = q.colwise ? q.k : q.rows;   // column-wise: the SR row length is the whole k
     a.rht_seed = q.rht_seed; a.sr_seed = q.sr_seed; a.sr_counter = q.sr_counter; a.elem_base = 0;
+    set_sr_keys(a);
     a.status = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsStatus);
     a.codes = q.codes; a.scales = q.scales; a.tensor_scale = q.tensor_scale;
     a.eplane = q.grid == kE1M2 ? q.eplane : nullptr;
@@ -3179,6 +3195,7 @@ Args make_args(const QuantLaunch &q, void *ws) {
     a.rows = q.rows; a.cols = q.cols; a.ld = q.ld;
     a.out_rows = q.out_rows; a.k = q.k; a.kpad = kpad_of(q.k); a.nkt = a.kpad / 64;
     a.rht_seed = q.rht_seed; a.sr_seed = q.sr_seed; a.sr_counter = q.sr_counter;
+    set_sr_keys(a);
     a.elem_base = q.elem_base;
     a.amax_in = q.amax_in;
     a.status = ws ? reinterpret_cast<uint32_t *>(static_cast<char *>(ws) + kWsStatus) : nullptr;
