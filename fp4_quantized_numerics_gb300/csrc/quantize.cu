@@ -1703,7 +1703,6 @@ constexpr uint32_t kTileRows = 128, kTileCols = 64;
 constexpr uint32_t kTileBytes = kTileRows * kTileCols * 2;   // BF16
 static_assert(kTileBytes == kChunk, "a tile fills one ring stage");
 constexpr uint32_t kColStageBytes = 8 * kTileCols * 8 + 8 * kTileCols;   // codes [8][64] x 8 B + scales [8][64]
-constexpr uint32_t kTileSmem = ring_smem<false>() + kColStageBytes;
 // k_dual_tile and k_dual_tile_grouped stage tile j's column-wise results in
 // buffer j % 2 of two, so one CTA barrier per tile orders both the ring
 // slot's reuse and the staging buffer's.  k_dual_tile's ring is 2 deep (4
