@@ -371,6 +371,7 @@ def run_gpu(args):
             "quantize": {"gbs": round(q_gbs, 1), "frac_hbm": round(q_gbs / ws_n / pk["hbm_gbs"], 4),
                          "ms_per_step": round(tq / args.steps, 4),
                          "elements_per_step": step_elems(WORKLOAD),
+                         "elements_per_s": round(ws_n * step_elems(WORKLOAD) / (tq / args.steps * 1e-3)),
                          "launches_per_step": n_launch - 3},
             "gemm": {"tflops": round(gemm_tflops, 1), "ms_per_step": round(tg / args.steps, 4),
                      "ms_each": [round(v, 4) for v in gemm_each],
@@ -869,6 +870,7 @@ def all_workloads(U, torch, dev, pk, flush, with_oracle=True):
     q = U.QTensor.empty(256, 1024, U.UFP4_E1M2, dev)
     ms = _ev_time(lambda: U.ufp4_quantize(x, U.UFP4_E1M2, rht=True, rht_seed=2, out=q), flush)
     r["quantize_e1m2_rht_gbs"] = round(x.numel() * Q_BYTES_PER_ELEM / (ms * 1e-3) / 1e9, 2)
+    r["quantize_e1m2_rht_elems_per_s"] = round(x.numel() / (ms * 1e-3))
     r.update(_fracs(pk, q_gbs=r["quantize_e1m2_rht_gbs"]))
     for g, gn in ((0, "e2m1"), (1, "e1m2"), (2, "e2m1c"), (3, "mxfp4")):
         for rht in (False, True):
@@ -891,7 +893,7 @@ def all_workloads(U, torch, dev, pk, flush, with_oracle=True):
     d = inputs.outlier(0)
     x = torch.from_numpy(d["x"]).to(torch.bfloat16).to(dev)
     r = {"config": "BF16 4096 x 4096 N(0,1) + column offsets N(0,0.5), 4 columns x100", "numerics": {},
-         "quantize_gbs": {}}
+         "quantize_gbs": {}, "quantize_elems_per_s": {}}
     for g, gn in ((0, "e2m1"), (1, "e1m2"), (2, "e2m1c"), (3, "mxfp4")):
         bpe = MX_BYTES_PER_ELEM if g == U.UFP4_MXFP4 else Q_BYTES_PER_ELEM
         for rht in (False, True):
@@ -900,6 +902,7 @@ def all_workloads(U, torch, dev, pk, flush, with_oracle=True):
             qq = U.QTensor.empty(4096, 4096, g, dev, eplane=False)
             ms = _ev_time(lambda: U.ufp4_quantize(x, g, rht=rht, rht_seed=2, out=qq), flush)
             r["quantize_gbs"][key] = round(x.numel() * bpe / (ms * 1e-3) / 1e9, 1)
+            r["quantize_elems_per_s"][key] = round(x.numel() / (ms * 1e-3))
     r["quantize_frac_hbm"] = {k: round(v / pk["hbm_gbs"], 4) for k, v in r["quantize_gbs"].items()}
     n = r["numerics"]
     r["sqnr_ranking"] = {
@@ -924,7 +927,8 @@ def all_workloads(U, torch, dev, pk, flush, with_oracle=True):
         bpe = MX_BYTES_PER_ELEM if g == U.UFP4_MXFP4 else Q_BYTES_PER_ELEM
         qg = st.q_elems * bpe / (mq * 1e-3) / 1e9
         tf = sum(st.flops_each) / (mg * 1e-3) / 1e12
-        e = {"quantize_ms": round(mq, 4), "quantize_gbs": round(qg, 1), "gemm_ms": round(mg, 4),
+        e = {"quantize_ms": round(mq, 4), "quantize_gbs": round(qg, 1),
+             "quantize_elems_per_s": round(st.q_elems / (mq * 1e-3)), "gemm_ms": round(mg, 4),
              "gemm_tflops": round(tf, 1)}
         e.update(_fracs(pk, qg, tf, g, 3 * _gemm_bytes(T, F, H, mx=g == U.UFP4_MXFP4), sum(st.flops_each)))
         r[gn] = e
@@ -1002,7 +1006,8 @@ def all_workloads(U, torch, dev, pk, flush, with_oracle=True):
         flops = 3 * 2.0 * T * F * H
         qg = elems * Q_BYTES_PER_ELEM / (mq * 1e-3) / 1e9
         tf = flops / (mg * 1e-3) / 1e12
-        e = {"quantize_ms": round(mq, 4), "quantize_gbs": round(qg, 1), "gemm_ms": round(mg, 4),
+        e = {"quantize_ms": round(mq, 4), "quantize_gbs": round(qg, 1),
+             "quantize_elems_per_s": round(elems / (mq * 1e-3)), "gemm_ms": round(mg, 4),
              "gemm_tflops": round(tf, 1),
              "quantize_ms_six_single_orientation_calls": round(mq1, 4)}
         e.update(_fracs(pk, qg, tf, g, 3 * sum(_gemm_bytes(c, F, H) for c in counts), flops))
@@ -1025,7 +1030,8 @@ def all_workloads(U, torch, dev, pk, flush, with_oracle=True):
     mg = _ev_time(st.gemms, flush)
     qg = st.q_elems * Q_BYTES_PER_ELEM / (mq * 1e-3) / 1e9
     tf = sum(st.flops_each) / (mg * 1e-3) / 1e12
-    e = {"quantize_ms": round(mq, 4), "quantize_gbs": round(qg, 1), "gemm_ms": round(mg, 4),
+    e = {"quantize_ms": round(mq, 4), "quantize_gbs": round(qg, 1),
+         "quantize_elems_per_s": round(st.q_elems / (mq * 1e-3)), "gemm_ms": round(mg, 4),
          "gemm_tflops": round(tf, 1)}
     e.update(_fracs(pk, qg, tf, 0, 3 * _gemm_bytes(T, F, H), sum(st.flops_each)))
     out["moe124b_layer_e2m1"] = dict(config="the headline layer on the E2M1 grid (UFP4 recipe otherwise)", **e)
