@@ -636,7 +636,8 @@ def run_reference(args):
 
 def run_kernel(args):
     """One kernel of a step in isolation, for profiling: `steps` launches of
-    the fwd_y GEMM (T x F x H), of the RHT quantization of X (T x H) in one
+    the fwd_y GEMM (T x F x H; gemm_e1m2_dx / _dw: the bwd_dx and bwd_dw
+    products of the same layer), of the RHT quantization of X (T x H) in one
     orientation or both (quant_dual_*; the SR variant quantizes dY, T x F),
     after `warmup` launches, the tensor amax given (quant_resident_e1m2: W,
     F x H, both ways with its maxima, the on-chip single pass; quant_grouped_dual_e1m2:
@@ -666,9 +667,17 @@ def run_kernel(args):
     x = inputs.device_normal((T, H), 1.0, 21, dev)
     if kind.startswith("gemm"):
         grid = {"gemm_e2m1": U.UFP4_E2M1, "gemm_mxfp4": U.UFP4_MXFP4}.get(kind, U.UFP4_E1M2)
-        w = inputs.device_normal((F, H), 0.02, 22, dev)
-        a, b = U.ufp4_quantize(x, grid, rht=True), U.ufp4_quantize(w, grid, rht=True)
-        c = torch.empty(T, F, dtype=torch.float32, device=dev)
+        if kind == "gemm_e1m2_dx":     # dX = dY W: M = T, N = H, K = F
+            a_src = inputs.device_normal((T, F), 1e-3, 23, dev)
+            b_src = inputs.device_normal((H, F), 0.02, 22, dev)
+        elif kind == "gemm_e1m2_dw":   # dW = dY^T X: M = F, N = H, K = T
+            a_src = inputs.device_normal((F, T), 1e-3, 23, dev)
+            b_src = inputs.device_normal((H, T), 1.0, 21, dev)
+        else:                          # Y = X W^T: M = T, N = F, K = H
+            a_src, b_src = x, inputs.device_normal((F, H), 0.02, 22, dev)
+        a, b = U.ufp4_quantize(a_src, grid, rht=True), U.ufp4_quantize(b_src, grid, rht=True)
+        del a_src, b_src
+        c = torch.empty(a.rows, b.rows, dtype=torch.float32, device=dev)
         fn = lambda: U.ufp4_gemm(a, b, out=c)
         work = 2.0 * T * F * H
         unit = "TFLOP/s"
@@ -1103,7 +1112,8 @@ def main():
     ap.add_argument("--shape", default="dense", choices=["dense", "moe124b"],
                     help="layer shape of --kernel")
     ap.add_argument("--kernel", default=None,
-                    choices=["gemm_e2m1", "gemm_e1m2", "gemm_mxfp4", "quant_row_e1m2", "quant_col_e1m2", "quant_dual_e1m2",
+                    choices=["gemm_e2m1", "gemm_e1m2", "gemm_e1m2_dx", "gemm_e1m2_dw", "gemm_mxfp4",
+                             "quant_row_e1m2", "quant_col_e1m2", "quant_dual_e1m2",
                              "quant_dual_sr_e1m2", "amax_dual_e1m2",
                              "quant_row_e2m1", "quant_col_e2m1", "quant_grouped_dual_e1m2", "quant_resident_e1m2",
                              "all"],
