@@ -1099,7 +1099,7 @@ def all_workloads(U, torch, dev, pk, flush, with_oracle=True):
     return out
 
 
-def main():
+def build_parser():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
@@ -1118,6 +1118,11 @@ def main():
                              "quant_row_e2m1", "quant_col_e2m1", "quant_grouped_dual_e1m2", "quant_resident_e1m2",
                              "all"],
                     help="time one kernel of the step in isolation (profiling); all: every public call once")
+    return ap
+
+
+def main():
+    ap = build_parser()
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
