@@ -27,12 +27,10 @@
 // loaded planes) or warps 10-15 = expanders (E1M2 without planes).  The
 // accumulator (256 TMEM columns) is single-buffered: the epilogue pulls the
 // whole tile out (registers and shared staging) and hands the columns back
-// before it stores, so the stores overlap the next tile's MMAs (with short K
-// and a large C, one 2 KB store in flight per warp makes the stores the
-// longer of the two).  Block scales are staged in TMEM after the
-// accumulator, 12 columns per MMA K step.  Every wait is bounded: on timeout
-// the kernel raises g_ufp4_timeout, drains its own copies, frees TMEM and
-// returns.
+// before it stores, so the stores overlap the next tile's MMAs.  Block scales
+// are staged in TMEM after the accumulator, 12 columns per MMA K step.  Every
+// wait is bounded: on timeout the kernel raises g_ufp4_timeout, drains its
+// own copies, frees TMEM and returns.
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
